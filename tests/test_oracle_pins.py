@@ -1,0 +1,421 @@
+"""Pins of the float64 oracle to facts the pages and the mathematics fix.
+
+Each test checks the oracle against something other than itself: values the pages
+print for their seeded examples (tests/golden, each file names its page and section),
+brute force on tiny inputs, closed forms and invariants. The last group plants
+plausible mistakes in the oracle and checks that at least one pin catches each.
+"""
+import itertools
+import json
+import math
+import os
+
+import numpy as np
+import pytest
+import torch
+
+import moe_inputs as mi
+import oracle as O
+from oracle import moe_oracle as OM
+
+
+def _load(golden_dir, name):
+    with open(os.path.join(golden_dir, name)) as f:
+        return json.load(f)
+
+
+def _np(t):
+    return t.detach().cpu().double().numpy()
+
+
+def _tiny():
+    x, wg, w1, w3, w2 = mi.page_tiny_layer()
+    return _np(x), _np(wg), _np(torch.cat([w1, w3], 1)), _np(w2)
+
+
+# ----------------------------------------------------------------- page-printed values
+
+def check_tiny_loads(golden_dir):
+    g = _load(golden_dir, "tiny_layer.json")
+    x, wg, W13, W2 = _tiny()
+    ids, _ = O.route_softmax(O.router_logits(x, wg), 2)
+    return np.bincount(ids.ravel(), minlength=8).tolist() == g["tokens_per_expert"]
+
+
+def test_tiny_loads(golden_dir):
+    assert check_tiny_loads(golden_dir)
+
+
+def test_tiny_flops(golden_dir):
+    g = _load(golden_dir, "tiny_layer.json")
+    T, H, I, E, k = 64, 64, 96, 8, 2
+    flops = 2 * T * k * 3 * H * I
+    assert round(flops / 1e6, 1) == g["routed_mflop"]
+    assert round(flops * E / k / 1e6, 1) == g["dense_mflop"]
+    assert mi.TINY_F32.flops == flops
+
+
+def check_loop_vs_dense_tiny():
+    x, wg, W13, W2 = _tiny()
+    a, ids, w, _ = O.moe_forward(x, wg, W13, W2, 2)
+    b, *_ = O.moe_forward(x, wg, W13, W2, 2, dense=True)
+    return np.abs(a - b).max() <= 1e-12 * np.abs(a).max()
+
+
+def test_loop_vs_dense_tiny():
+    assert check_loop_vs_dense_tiny()
+
+
+def check_deepseek_toy(golden_dir):
+    g = _load(golden_dir, "deepseek_toy_router.json")
+    logits, bias = mi.page_deepseek_toy()
+    l, b = _np(logits), _np(bias)
+    ok = True
+    ids0, _ = O.route_sigmoid_grouped(l, 4, 4, 2, np.zeros(16), 2.5)
+    ids1, w1 = O.route_sigmoid_grouped(l, 4, 4, 2, b, 2.5)
+    ok &= ids0.tolist() == g["ids_no_bias"]
+    ok &= ids1.tolist() == g["ids_with_bias"]
+    ok &= [sorted(set(r)) for r in (ids1 // 4).tolist()] == g["groups_per_token"]
+    ok &= bool(np.all(np.abs(w1 - np.array(g["weights_right_3dp"])) <= 0.0005 + 1e-12))
+    ok &= bool(np.allclose(w1.sum(-1), 2.5, rtol=0, atol=1e-12))
+    # The page's "bug": weights taken from the biased scores on the same ids.
+    c = O.sigmoid(l) + b
+    wb = np.take_along_axis(c, ids1, -1)
+    wb = 2.5 * wb / wb.sum(-1, keepdims=True)
+    ok &= bool(np.all(np.abs(wb - np.array(g["weights_bug_3dp"])) <= 0.0005 + 1e-12))
+    ok &= round(float(np.abs(wb - w1).max()), 3) == g["max_weight_error_bug_3dp"]
+    return bool(ok)
+
+
+def test_deepseek_toy_router(golden_dir):
+    assert check_deepseek_toy(golden_dir)
+
+
+def check_align_example(golden_dir):
+    g = _load(golden_dir, "align_example.json")
+    ids = np.array(g["topk_ids"])
+    sid, eid, total, _ = O.moe_align(ids, g["block_m"], g["num_experts"])
+    return (ids.ravel().tolist() == g["flat"] and sid.tolist() == g["sorted_ids"]
+            and eid.tolist() == g["expert_ids"] and total == g["total"])
+
+
+def test_align_example(golden_dir):
+    assert check_align_example(golden_dir)
+
+
+def check_fused_cases(golden_dir):
+    g = _load(golden_dir, "fused_cases.json")
+    ok = True
+    for c in g["cases"]:
+        x, wg, w1, w3, w2 = mi.page_fused_case(c["T"], c["E"], c["bias"])
+        ids, _ = O.route_softmax(O.router_logits(_np(x), _np(wg)), c["k"])
+        _, _, total, counts = O.moe_align(ids, g["block_m"], c["E"])
+        ok &= counts.tolist() == c["loads"] and int(counts.sum()) == c["rows"]
+        ok &= total == c["padded"]
+    return bool(ok)
+
+
+def test_fused_case_loads_and_padding(golden_dir):
+    assert check_fused_cases(golden_dir)
+
+
+# ----------------------------------------------------------------- brute force
+
+def check_topk_brute(seed=0):
+    rng = np.random.default_rng(seed)
+    for _ in range(200):
+        n = int(rng.integers(1, 7))
+        k = int(rng.integers(1, n + 1))
+        keys = rng.integers(0, 4, size=n).astype(float)  # many exact ties
+        if O.topk_desc(keys[None], k)[0].tolist() != O.brute_topk(list(keys), k).tolist():
+            return False
+    return True
+
+
+def test_topk_brute_force_with_ties():
+    assert check_topk_brute()
+
+
+def check_align_brute(seed=0):
+    rng = np.random.default_rng(seed)
+    for T in range(1, 5):
+        for E in range(1, 6):
+            for k in range(1, min(3, E) + 1):
+                for B in range(1, 6):
+                    ids = np.stack([rng.permutation(E)[:k] for _ in range(T)])
+                    sid, eid, tot, _ = O.moe_align(ids, B, E)
+                    bs, be, bt = O.brute_align(ids, B, E)
+                    if not (tot == bt and sid.tolist() == bs.tolist() and eid.tolist() == be.tolist()):
+                        return False
+    return True
+
+
+def test_align_brute_force_small():
+    assert check_align_brute()
+
+
+def _ffn_scalar(xv, W1, W3, W2):
+    """SwiGLU expert by explicit scalar loops (the §1 formula, element by element)."""
+    I, H = W1.shape
+    outv = []
+    for jo in range(W2.shape[0]):
+        s = 0.0
+        for i in range(I):
+            g = sum(W1[i, h] * xv[h] for h in range(H))
+            u = sum(W3[i, h] * xv[h] for h in range(H))
+            s += W2[jo, i] * (g / (1.0 + math.exp(-g))) * u
+        outv.append(s)
+    return np.array(outv)
+
+
+def check_layer_brute(seed=0, mode=0):
+    """Tiny layer by brute force: scalar logits, k-subset enumeration, scalar experts."""
+    rng = np.random.default_rng(seed)
+    T, H, I, E, k = 4, 3, 2, 4, 2
+    x = rng.standard_normal((T, H))
+    Wg = rng.standard_normal((E, H))
+    W13 = rng.standard_normal((E, 2 * I, H))
+    W2 = rng.standard_normal((E, H, I))
+    bias = rng.standard_normal(E) * 0.1
+    scale = 1.7
+    if mode == 0:
+        out, ids, w, _ = O.moe_forward(x, Wg, W13, W2, k)
+    else:
+        out, ids, w, _ = O.moe_forward(x, Wg, W13, W2, k, mode=1, scale=scale, n_group=2,
+                                       topk_group=1, select_bias=bias)
+    for t in range(T):
+        lg = [sum(Wg[e, h] * x[t, h] for h in range(H)) for e in range(E)]
+        if mode == 0:
+            sel = O.brute_topk(lg, k)
+            ex = [math.exp(lg[e]) for e in sel]
+            wt = [v / sum(ex) for v in ex]
+        else:
+            s = [1 / (1 + math.exp(-v)) for v in lg]
+            c = [s[e] + bias[e] for e in range(E)]
+            gs = [sorted(c[2 * gi:2 * gi + 2], reverse=True) for gi in range(2)]
+            best_g = max(range(2), key=lambda gi: (gs[gi][0] + gs[gi][1], -gi))
+            elig = [c[e] if e // 2 == best_g else -math.inf for e in range(E)]
+            sel = O.brute_topk(elig, k)
+            wt = [scale * s[e] / sum(s[ee] for ee in sel) for e in sel]
+        ref = np.zeros(H)
+        for e, wv in zip(sel, wt):
+            ref += wv * _ffn_scalar(x[t], W13[e, :I], W13[e, I:], W2[e])
+        if ids[t].tolist() != list(sel) or np.abs(out[t] - ref).max() > 1e-12 * max(1.0, np.abs(ref).max()):
+            return False
+    return True
+
+
+@pytest.mark.parametrize("mode", [0, 1])
+def test_layer_brute_force(mode):
+    assert check_layer_brute(mode=mode)
+
+
+# ----------------------------------------------------------------- closed forms / invariants
+
+def _rand_layer(rng, T=9, H=8, I=6, E=4):
+    return (rng.standard_normal((T, H)), rng.standard_normal((E, H)),
+            rng.standard_normal((E, 2 * I, H)) / 3, rng.standard_normal((E, H, I)) / 3)
+
+
+def test_single_expert_is_dense_ffn():
+    rng = np.random.default_rng(1)
+    x, Wg, W13, W2 = _rand_layer(rng, E=1)
+    out, *_ = O.moe_forward(x, Wg, W13, W2, 1)
+    ref = np.stack([_ffn_scalar(x[t], W13[0, :6], W13[0, 6:], W2[0]) for t in range(x.shape[0])])
+    assert np.abs(out - ref).max() <= 1e-12 * np.abs(ref).max()
+
+
+@pytest.mark.parametrize("mode,scale", [(0, 1.0), (1, 2.5)])
+def test_identical_experts_give_scaled_ffn(mode, scale):
+    rng = np.random.default_rng(2)
+    x, Wg, W13, W2 = _rand_layer(rng, E=8)
+    W13[:] = W13[0]
+    W2[:] = W2[0]
+    out, *_ = O.moe_forward(x, Wg, W13, W2, 3, mode=mode, scale=scale,
+                            n_group=4 if mode else 1, topk_group=2 if mode else 1)
+    ref = np.stack([_ffn_scalar(x[t], W13[0, :6], W13[0, 6:], W2[0]) for t in range(x.shape[0])])
+    assert np.abs(out - scale * ref).max() <= 1e-12 * np.abs(ref).max()
+
+
+def test_k_equals_E_is_full_softmax_mixture():
+    rng = np.random.default_rng(3)
+    x, Wg, W13, W2 = _rand_layer(rng, E=5)
+    out, *_ = O.moe_forward(x, Wg, W13, W2, 5)
+    p = O.softmax(x @ Wg.T)
+    ref = sum(p[:, e:e + 1] * np.stack([_ffn_scalar(x[t], W13[e, :6], W13[e, 6:], W2[e])
+                                        for t in range(x.shape[0])]) for e in range(5))
+    assert np.abs(out - ref).max() <= 1e-12 * np.abs(ref).max()
+
+
+def test_linearity_in_W2_and_zero_input():
+    rng = np.random.default_rng(4)
+    x, Wg, W13, W2 = _rand_layer(rng)
+    a, *_ = O.moe_forward(x, Wg, W13, W2, 2)
+    b, *_ = O.moe_forward(x, Wg, W13, 3.0 * W2, 2)
+    assert np.abs(b - 3.0 * a).max() <= 1e-12 * np.abs(b).max()
+    z, *_ = O.moe_forward(np.zeros_like(x), Wg, W13, W2, 2)
+    assert np.all(z == 0)
+
+
+def test_softmax_topk_equals_topk_then_softmax():
+    rng = np.random.default_rng(5)
+    l = rng.standard_normal((50, 16)) * 3
+    i1, w1 = O.route_softmax(l, 4)
+    i2, w2 = O.route_topk_then_softmax(l, 4)
+    assert i1.tolist() == i2.tolist()
+    assert np.abs(w1 - w2).max() <= 1e-14
+
+
+def test_weights_sum_to_one_or_scale():
+    rng = np.random.default_rng(6)
+    l = rng.standard_normal((40, 32))
+    _, w = O.route_softmax(l, 8)
+    assert np.abs(w.sum(-1) - 1).max() <= 1e-12
+    _, w = O.route_sigmoid_grouped(l, 8, 8, 4, rng.standard_normal(32) * 0.05, 2.5)
+    assert np.abs(w.sum(-1) - 2.5).max() <= 1e-12
+    ids, _ = O.route_sigmoid_grouped(l, 8, 8, 4, None, 2.5)
+    assert all(len(set(r)) <= 4 for r in (ids // 4).tolist())   # at most topk_group groups
+
+
+def test_unnormalised_softmax_weights_are_full_probabilities():
+    rng = np.random.default_rng(7)
+    l = rng.standard_normal((10, 8))
+    ids, w = O.route_softmax(l, 2, renormalize=False)
+    p = np.exp(l) / np.exp(l).sum(-1, keepdims=True)
+    assert np.abs(w - np.take_along_axis(p, ids, -1)).max() <= 1e-15
+
+
+@pytest.mark.parametrize("B", [1, 4, 16, 128])
+def test_align_invariants(B):
+    ids = mi.random_topk_ids(300, 8, 64, seed=B, skew=1.0).numpy()
+    n = ids.size
+    L = O.max_padded_rows(300, 8, 64, B)
+    sid, eid, total, counts = O.moe_align(ids, B, 64, max_padded=L)
+    flat = ids.ravel()
+    assert counts.sum() == n and total % B == 0 and total <= L
+    real = sid[sid < n]
+    assert sorted(real.tolist()) == list(range(n))
+    assert (sid[:total] == n).sum() == total - n and np.all(sid[total:] == n)
+    assert np.all(np.diff(eid[:total // B]) >= 0) and np.all(eid[total // B:] == -1)
+    for tile in range(total // B):
+        rows = sid[tile * B:(tile + 1) * B]
+        rows = rows[rows < n]
+        assert len(rows) > 0 and np.all(flat[rows] == eid[tile])
+        assert np.all(np.diff(rows) > 0)  # stable: ascending flat row inside a run
+    assert set(eid[:total // B].tolist()) == set(np.nonzero(counts)[0].tolist())
+
+
+def test_margins_flag_near_ties():
+    l = np.array([[1.0, 1.0 + 5e-5, -2.0, 0.5]])
+    assert O.selection_margins(l, 1)[0] < 1e-4
+    assert O.selection_margins(l + np.array([[0, 1, 0, 0]]), 1)[0] > 1e-4
+
+
+# ----------------------------------------------------------------- planted mistakes
+
+def _all_pins(golden_dir):
+    return {
+        "tiny": check_tiny_loads(golden_dir),
+        "loop_dense": check_loop_vs_dense_tiny(),
+        "deepseek": check_deepseek_toy(golden_dir),
+        "align_example": check_align_example(golden_dir),
+        "fused_cases": check_fused_cases(golden_dir),
+        "topk_brute": check_topk_brute(),
+        "align_brute": check_align_brute(),
+        "brute0": check_layer_brute(mode=0),
+        "brute1": check_layer_brute(mode=1),
+    }
+
+
+def _mut_swap_gate_up(xrows, W13e, W2e):
+    I = W2e.shape[1]
+    h = O.f64(xrows) @ O.f64(W13e).T
+    return (OM.silu(h[:, I:]) * h[:, :I]) @ O.f64(W2e).T
+
+
+def _mut_no_renorm(logits, k, renormalize=True):
+    return _orig_route_softmax(logits, k, False)
+
+
+_orig_route_softmax = OM.route_softmax
+_orig_sigmoid = OM.sigmoid
+
+
+def _mut_topk_ascending(keys, k):
+    keys = O.f64(keys)
+    out = np.empty(keys.shape[:-1] + (k,), dtype=np.int64)
+    for row in np.ndindex(keys.shape[:-1]):
+        out[row] = np.argsort(keys[row], kind="stable")[:k]
+    return out
+
+
+def _mut_align_unstable(topk_ids, block_m, E, max_padded=None):
+    sid, eid, total, counts = _orig_align(topk_ids, block_m, E, max_padded)
+    n = np.asarray(topk_ids).size
+    pos = 0
+    for e in range(E):
+        p = (counts[e] + block_m - 1) // block_m * block_m
+        sid[pos:pos + counts[e]] = sid[pos:pos + counts[e]][::-1]
+        pos += p
+    return sid, eid, total, counts
+
+
+_orig_align = OM.moe_align
+
+
+def _mut_group_top1(logits, k, n_group, topk_group, select_bias=None, scale=1.0, renormalize=True):
+    l = O.f64(logits)
+    T, E = l.shape
+    s = OM.sigmoid(l)
+    c = s + (O.f64(select_bias)[None, :] if select_bias is not None else 0.0)
+    per = E // n_group
+    gscore = c.reshape(T, n_group, per).max(-1)
+    keep = OM.topk_desc(gscore, topk_group)
+    el = np.zeros((T, n_group), dtype=bool)
+    np.put_along_axis(el, keep, True, axis=-1)
+    ids = OM.topk_desc(np.where(np.repeat(el, per, 1), c, -np.inf), k)
+    w = np.take_along_axis(s, ids, -1)
+    return ids, scale * w / w.sum(-1, keepdims=True)
+
+
+def _mut_sigmoid_weights_biased(logits, k, n_group, topk_group, select_bias=None, scale=1.0,
+                                renormalize=True):
+    ids, _ = _orig_grouped(logits, k, n_group, topk_group, select_bias, scale, renormalize)
+    c = OM.sigmoid(O.f64(logits)) + (O.f64(select_bias) if select_bias is not None else 0.0)
+    w = np.take_along_axis(c, ids, -1)
+    return ids, scale * w / w.sum(-1, keepdims=True)
+
+
+_orig_grouped = OM.route_sigmoid_grouped
+
+
+def _mut_sentinel(topk_ids, block_m, E, max_padded=None):
+    sid, eid, total, counts = _orig_align(topk_ids, block_m, E, max_padded)
+    n = np.asarray(topk_ids).size
+    sid = np.where(sid == n, n - 1, sid)
+    return sid, eid, total, counts
+
+
+def _mut_loop_wrong_slot_weight(x, ids, w, W13, W2, tokens=None):
+    return _orig_loop(x, ids, w[:, ::-1], W13, W2, tokens)
+
+
+_orig_loop = OM.moe_loop
+
+
+@pytest.mark.parametrize("name,attr,mut", [
+    ("swap gate/up", "expert_ffn", _mut_swap_gate_up),
+    ("no renormalisation", "route_softmax", _mut_no_renorm),
+    ("ascending top-k", "topk_desc", _mut_topk_ascending),
+    ("unstable scatter", "moe_align", _mut_align_unstable),
+    ("group score top-1", "route_sigmoid_grouped", _mut_group_top1),
+    ("weights from biased scores", "route_sigmoid_grouped", _mut_sigmoid_weights_biased),
+    ("sentinel off by one", "moe_align", _mut_sentinel),
+    ("slot weights swapped", "moe_loop", _mut_loop_wrong_slot_weight),
+])
+def test_planted_mistake_is_caught(monkeypatch, golden_dir, name, attr, mut):
+    assert all(_all_pins(golden_dir).values())
+    monkeypatch.setattr(OM, attr, mut)
+    monkeypatch.setattr(O, attr, mut)
+    res = _all_pins(golden_dir)
+    assert not all(res.values()), f"planted mistake '{name}' passed every pin"
