@@ -1,0 +1,185 @@
+/*
+ * moe.h — C ABI of the GB300 (sm_103a) fused Mixture-of-Experts feed-forward layer.
+ *
+ * The layer (page "Mixture-of-Experts Kernels: Routing, Permutation, and Grouped GEMM",
+ * §1-§2 and §11): a router scores E experts per token and keeps k; an align step turns
+ * the chosen ids into a block-aligned indirection table; two grouped GEMMs run every
+ * expert's SwiGLU on exactly the rows routed to it; a combine sums the k weighted slots:
+ *
+ *   x[T,H] --router--> logits[T,E] --top-k--> topk_ids[T,k], topk_w[T,k]
+ *   --align--> sorted_ids[max_padded], expert_ids[max_padded/block_m], num_post_padded
+ *   --GEMM1 (gather x[sorted_ids/k], W13[e]) + silu(h[:, :I]) * h[:, I:]--> act[max_padded, I]
+ *   --GEMM2 (act, W2[e]) * topk_w[r]--> y[T*k, H] at flat row r = t*k + j
+ *   --combine--> out[t] = sum_j y[t*k + j]
+ *
+ * Conventions for every entry point:
+ *  - Tensors are DEVICE pointers, contiguous and row-major, in nn.Linear [E, N, K] layout:
+ *    x[T,H], Wg[E,H], W13[E,2I,H] (rows 0..I-1 = gate projection W1, rows I..2I-1 = up
+ *    projection W3), W2[E,H,I], y[T*k,H], out[T,H]. x's dtype (cfg->dtype) is the dtype of
+ *    Wg, W13, W2, act, y and out. logits, topk_w and the biases are always fp32; ids int32.
+ *  - bf16 tensors must start on a 16-byte boundary and H, I must be multiples of 8
+ *    (tensor-memory-access copies move 16-byte units).
+ *  - The CALLER owns every buffer, workspaces included. The library never allocates or
+ *    frees device memory, never synchronises the stream and never reads device data on
+ *    the host: every call only enqueues kernels on `stream`, so a sequence of calls can be
+ *    captured in a CUDA graph. (moe_device_status is the one diagnostic exception.)
+ *  - Host-side argument checks return MOE_ERR_INVALID_ARG / MOE_ERR_UNSUPPORTED /
+ *    MOE_ERR_WORKSPACE before anything is enqueued; a failed launch returns MOE_ERR_CUDA.
+ *  - Faults found on the device (an expert id outside [0, E), a pipeline wait that ran
+ *    out of time) never trap: the kernel skips the bad item or returns early and records
+ *    a code in a device status word, read with moe_device_status().
+ *  - Ties in top-k go to the lower expert (or group) id. Rows inside one expert's run of
+ *    sorted_ids are in ascending flat row r. Padding rows and the unused tail of
+ *    sorted_ids hold the sentinel T*k; unused tail entries of expert_ids hold -1.
+ */
+#ifndef MOE_GB300_H
+#define MOE_GB300_H
+
+#include <stddef.h>
+#include <stdint.h>
+#include <cuda_runtime_api.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define MOE_ABI_VERSION 1
+
+typedef enum {
+  MOE_OK = 0,
+  MOE_ERR_INVALID_ARG = 1,  /* a null pointer, a size out of range, misaligned memory */
+  MOE_ERR_UNSUPPORTED = 2,  /* valid arguments this build does not handle (e.g. E > 512) */
+  MOE_ERR_WORKSPACE = 3,    /* workspace pointer null or smaller than required */
+  MOE_ERR_CUDA = 4          /* a CUDA runtime/driver call or a kernel launch failed */
+} moe_status_t;
+
+typedef enum { MOE_F32 = 0, MOE_BF16 = 1 } moe_dtype_t;
+
+typedef enum {
+  /* softmax over the E logits (after the optional logit_bias), keep the k largest;
+   * renormalize=1 divides the k kept probabilities by their sum, which equals a softmax
+   * over the k largest logits (the gpt-oss "softmax over top-k" form). Page §3 route(). */
+  MOE_ROUTE_SOFTMAX = 0,
+  /* DeepSeek-V3 rule (page §4): s = sigmoid(logit); c = s + select_bias chooses, s weighs;
+   * groups of E/n_group consecutive experts scored by the sum of their two largest c; the
+   * topk_group best groups stay eligible; top-k of c inside them; w = scale * s / sum(s)
+   * (renormalize=1) or scale * s (renormalize=0). */
+  MOE_ROUTE_SIGMOID_GROUPED = 1
+} moe_route_mode_t;
+
+typedef struct moe_config {
+  int T;                    /* tokens, >= 1 */
+  int H;                    /* hidden size (multiple of 8) */
+  int I;                    /* expert intermediate size (multiple of 8) */
+  int E;                    /* routed experts, 1..512 */
+  int k;                    /* experts per token, 1..min(E, 32) */
+  moe_dtype_t dtype;        /* MOE_BF16 (tensor-core path) or MOE_F32 (FFMA path) */
+  moe_route_mode_t mode;
+  int renormalize;          /* 1: weights of the k kept experts sum to 1 (times scale) */
+  float scale;              /* routed scaling factor applied to the weights (1.0; 2.5 DSv3) */
+  int n_group;              /* mode 1: expert groups (E % n_group == 0, n_group <= 32) */
+  int topk_group;           /* mode 1: groups kept (topk_group * E / n_group >= k) */
+  const float* logit_bias;  /* mode 0: device fp32 [E] added to the logits, or NULL */
+  const float* select_bias; /* mode 1: device fp32 [E] selection-only bias, or NULL */
+} moe_config_t;
+
+/* Byte offsets of the intermediates inside a moe_forward workspace (256-byte aligned). */
+typedef struct moe_ws_layout {
+  size_t logits;           /* fp32 [T, E] */
+  size_t topk_ids;         /* int32 [T, k] */
+  size_t topk_w;           /* fp32 [T, k] */
+  size_t sorted_ids;       /* int32 [max_padded] */
+  size_t expert_ids;       /* int32 [max_padded / block_m] */
+  size_t num_post_padded;  /* int32 [1] */
+  size_t counts;           /* int32 [E] */
+  size_t align_scratch;    /* moe_align workspace */
+  size_t act;              /* dtype [max_padded, I] */
+  size_t y;                /* dtype [T*k, H] */
+  size_t total;            /* bytes required */
+  int block_m;
+  int max_padded;
+} moe_ws_layout_t;
+
+/* ABI version of the loaded library (MOE_ABI_VERSION). */
+int moe_abi_version(void);
+
+/* Human-readable name of a status code (static string). */
+const char* moe_status_string(moe_status_t s);
+
+/* Tile height (BLOCK_M) the grouped GEMMs use for this configuration: 128 for bf16
+ * (one tensor-core M tile), 16 for fp32. Host arithmetic only. Returns 0 on bad args. */
+int moe_block_m(const moe_config_t* cfg);
+
+/* Worst-case padded length T*k + min(E, T*k)*(block_m-1) (page §5: every expert that can
+ * hold a row pads at most block_m-1 slots). Host arithmetic only; 0 on bad args. */
+size_t moe_max_padded_rows(int T, int k, int E, int block_m);
+
+/* Scratch bytes moe_align needs for (T, k, E, block_m); 0 is a valid answer. */
+moe_status_t moe_align_workspace_size(int T, int k, int E, int block_m, size_t* bytes);
+
+/* Workspace layout / size of moe_forward for cfg (host arithmetic only). */
+moe_status_t moe_workspace_layout(const moe_config_t* cfg, moe_ws_layout_t* layout);
+moe_status_t moe_workspace_size(const moe_config_t* cfg, size_t* bytes);
+
+/* Router (page §3 route(), §4 route_grouped()): logits = x @ Wg^T (+ logit_bias in mode 0)
+ * accumulated in fp32, then top-k per cfg->mode. Writes logits[T,E] (fp32, required),
+ * topk_ids[T,k] in descending selection key, topk_w[T,k] fp32. */
+moe_status_t moe_route(const moe_config_t* cfg, const void* x, const void* Wg, float* logits,
+                       int32_t* topk_ids, float* topk_w, cudaStream_t stream);
+
+/* Align (page §5): histogram of the T*k flat rows over E experts, pad every count to a
+ * multiple of block_m, exclusive scan, stable scatter. Writes sorted_ids[max_padded],
+ * expert_ids[max_padded/block_m], num_post_padded[1] (the padded total, on the device)
+ * and, if non-NULL, counts[E]. ws/ws_bytes: scratch of moe_align_workspace_size bytes
+ * (may be NULL when that size is 0). Ids outside [0, E) are skipped and flagged. */
+moe_status_t moe_align(const int32_t* topk_ids, int T, int k, int E, int block_m,
+                       int32_t* sorted_ids, int32_t* expert_ids, int32_t* num_post_padded,
+                       int32_t* counts, void* ws, size_t ws_bytes, cudaStream_t stream);
+
+/* GEMM1 + SwiGLU (page §6 with the gate/up halves fused in one epilogue): for every
+ * padded position p < num_post_padded whose row r = sorted_ids[p] < T*k,
+ *   act[p, :] = silu(x[r / k] @ W1[e]^T) * (x[r / k] @ W3[e]^T),  e = expert_ids[p / block_m].
+ * act is [max_padded, I] in padded order; rows of padding positions are not written.
+ * block_m must be a multiple of moe_block_m(cfg). */
+moe_status_t moe_expert_gemm1(const moe_config_t* cfg, const void* x, const void* W13,
+                              const int32_t* sorted_ids, const int32_t* expert_ids,
+                              const int32_t* num_post_padded, int block_m, void* act,
+                              cudaStream_t stream);
+
+/* GEMM2 with the router weight (page §6): for every padded position p with r < T*k,
+ *   y[r, :] = topk_w[r] * (act[p] @ W2[e]^T).  Each row r < T*k is written exactly once;
+ * padding rows are never written. */
+moe_status_t moe_expert_gemm2(const moe_config_t* cfg, const void* act, const void* W2,
+                              const int32_t* sorted_ids, const int32_t* expert_ids,
+                              const int32_t* num_post_padded, int block_m,
+                              const float* topk_w, void* y, cudaStream_t stream);
+
+/* Both expert GEMMs: GEMM1 into ws (act, max_padded*I elements of cfg->dtype), then GEMM2
+ * into y[T*k, H]. ws_bytes must be >= max_padded * I * sizeof(dtype). */
+moe_status_t moe_grouped_swiglu(const moe_config_t* cfg, const void* x, const void* W13,
+                                const void* W2, const int32_t* sorted_ids,
+                                const int32_t* expert_ids, const int32_t* num_post_padded,
+                                int block_m, const float* topk_w, void* y, void* ws,
+                                size_t ws_bytes, cudaStream_t stream);
+
+/* Combine (page §6, the sum over k): out[t, :] = sum_{j=0..k-1} y[t*k + j, :] in fp32,
+ * slots added in order j = 0, 1, ..., stored in dtype. */
+moe_status_t moe_combine(const void* y, int T, int k, int H, moe_dtype_t dtype, void* out,
+                         cudaStream_t stream);
+
+/* The whole layer: route -> align -> GEMM1+SwiGLU -> GEMM2 -> combine, all enqueued on
+ * `stream` with no host round-trip. ws must hold moe_workspace_size(cfg) bytes, 256-byte
+ * aligned; its intermediates sit at moe_workspace_layout(cfg) offsets. */
+moe_status_t moe_forward(const moe_config_t* cfg, const void* x, const void* Wg,
+                         const void* W13, const void* W2, void* out, void* ws,
+                         size_t ws_bytes, cudaStream_t stream);
+
+/* Diagnostic (synchronises the current device): returns the device status word (0 = no
+ * fault seen; 1 = an expert id outside [0, E); 2 = a pipeline wait ran out of time) and
+ * clears it when reset != 0. Not for use inside stream capture. */
+int moe_device_status(int reset);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* MOE_GB300_H */

@@ -184,9 +184,11 @@ def selection_margins(logits, k, mode=SOFTMAX, n_group=1, topk_group=1, select_b
 # ----------------------------------------------------------------------------- align
 
 def max_padded_rows(T: int, k: int, E: int, block_m: int) -> int:
-    """Worst-case padded length: every expert that can hold a row wastes block_m-1 slots."""
+    """Worst-case padded length of sorted_ids: every expert that can hold a row pads at
+    most block_m-1 slots, and the padded total is a whole number of tiles, so the bound
+    T*k + min(E, T*k)*(block_m-1) rounded down to a multiple of block_m also holds."""
     n = T * k
-    return n + min(E, n) * (block_m - 1)
+    return (n + min(E, n) * (block_m - 1)) // block_m * block_m
 
 
 def moe_align(topk_ids, block_m: int, E: int, max_padded: Optional[int] = None):

@@ -1,0 +1,194 @@
+"""ctypes binding of libmoe_gb300.so: the C ABI of include/moe.h under the same names.
+
+Argument marshalling only: tensors become device pointers (``data_ptr()``), streams become
+``cudaStream_t`` handles, and a non-OK status raises ``MoeError``. Every step of the layer
+runs in the library's CUDA kernels; there is no Python or CPU fallback, and importing this
+module fails loudly when the library has not been built.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+from typing import Optional
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_PKG, "libmoe_gb300.so")
+
+MOE_OK, MOE_ERR_INVALID_ARG, MOE_ERR_UNSUPPORTED, MOE_ERR_WORKSPACE, MOE_ERR_CUDA = range(5)
+MOE_F32, MOE_BF16 = 0, 1
+MOE_ROUTE_SOFTMAX, MOE_ROUTE_SIGMOID_GROUPED = 0, 1
+
+
+class MoeError(RuntimeError):
+    def __init__(self, fn, status):
+        self.status = status
+        super().__init__(f"{fn} failed: {status_string(status)} ({status})")
+
+
+class moe_config_t(ctypes.Structure):
+    _fields_ = [("T", ctypes.c_int), ("H", ctypes.c_int), ("I", ctypes.c_int),
+                ("E", ctypes.c_int), ("k", ctypes.c_int), ("dtype", ctypes.c_int),
+                ("mode", ctypes.c_int), ("renormalize", ctypes.c_int), ("scale", ctypes.c_float),
+                ("n_group", ctypes.c_int), ("topk_group", ctypes.c_int),
+                ("logit_bias", ctypes.c_void_p), ("select_bias", ctypes.c_void_p)]
+
+
+class moe_ws_layout_t(ctypes.Structure):
+    _fields_ = [(n, ctypes.c_size_t) for n in ("logits", "topk_ids", "topk_w", "sorted_ids",
+                                              "expert_ids", "num_post_padded", "counts",
+                                              "align_scratch", "act", "y", "total")] + \
+               [("block_m", ctypes.c_int), ("max_padded", ctypes.c_int)]
+
+
+def _load():
+    if not os.path.exists(LIB_PATH):
+        raise ImportError(f"{LIB_PATH} is missing: build it with "
+                          "`python -m routing_grouped_gemm_router_gb300.build`")
+    lib = ctypes.CDLL(LIB_PATH)
+    P, I32, SZ, ST = ctypes.c_void_p, ctypes.c_int, ctypes.c_size_t, ctypes.c_int
+    CFG = ctypes.POINTER(moe_config_t)
+    sig = {
+        "moe_abi_version": (I32, []),
+        "moe_status_string": (ctypes.c_char_p, [ST]),
+        "moe_block_m": (I32, [CFG]),
+        "moe_max_padded_rows": (SZ, [I32, I32, I32, I32]),
+        "moe_align_workspace_size": (ST, [I32, I32, I32, I32, ctypes.POINTER(SZ)]),
+        "moe_workspace_layout": (ST, [CFG, ctypes.POINTER(moe_ws_layout_t)]),
+        "moe_workspace_size": (ST, [CFG, ctypes.POINTER(SZ)]),
+        "moe_route": (ST, [CFG, P, P, P, P, P, P]),
+        "moe_align": (ST, [P, I32, I32, I32, I32, P, P, P, P, P, SZ, P]),
+        "moe_expert_gemm1": (ST, [CFG, P, P, P, P, P, I32, P, P]),
+        "moe_expert_gemm2": (ST, [CFG, P, P, P, P, P, I32, P, P, P]),
+        "moe_grouped_swiglu": (ST, [CFG, P, P, P, P, P, P, I32, P, P, P, SZ, P]),
+        "moe_combine": (ST, [P, I32, I32, I32, I32, P, P]),
+        "moe_forward": (ST, [CFG, P, P, P, P, P, P, SZ, P]),
+        "moe_device_status": (I32, [I32]),
+    }
+    for name, (res, args) in sig.items():
+        f = getattr(lib, name)
+        f.restype, f.argtypes = res, args
+    return lib
+
+
+_lib = _load()
+EXPORTED = ("moe_abi_version", "moe_status_string", "moe_block_m", "moe_max_padded_rows",
+            "moe_align_workspace_size", "moe_workspace_layout", "moe_workspace_size",
+            "moe_route", "moe_align", "moe_expert_gemm1", "moe_expert_gemm2",
+            "moe_grouped_swiglu", "moe_combine", "moe_forward", "moe_device_status")
+
+
+def lib():
+    return _lib
+
+
+# ---------------------------------------------------------------------------- marshalling
+
+def _ptr(t) -> Optional[int]:
+    if t is None:
+        return None
+    if isinstance(t, int):
+        return t
+    return t.data_ptr()
+
+
+def _stream(s) -> Optional[int]:
+    if s is None:
+        import torch
+        return torch.cuda.current_stream().cuda_stream
+    if isinstance(s, int):
+        return s
+    return s.cuda_stream
+
+
+def _check(fn, st):
+    if st != MOE_OK:
+        raise MoeError(fn, st)
+
+
+def status_string(st: int) -> str:
+    return _lib.moe_status_string(st).decode()
+
+
+def make_config(T, H, I, E, k, dtype=MOE_BF16, mode=MOE_ROUTE_SOFTMAX, renormalize=True,
+                scale=1.0, n_group=1, topk_group=1, logit_bias=None, select_bias=None):
+    """Build a ``moe_config_t``; the biases are device fp32 tensors (kept alive by caller)."""
+    return moe_config_t(T, H, I, E, k, dtype, mode, int(bool(renormalize)), float(scale),
+                        n_group, topk_group, _ptr(logit_bias), _ptr(select_bias))
+
+
+def moe_abi_version() -> int:
+    return _lib.moe_abi_version()
+
+
+def moe_block_m(cfg) -> int:
+    return _lib.moe_block_m(ctypes.byref(cfg))
+
+
+def moe_max_padded_rows(T, k, E, block_m) -> int:
+    return _lib.moe_max_padded_rows(T, k, E, block_m)
+
+
+def moe_align_workspace_size(T, k, E, block_m) -> int:
+    out = ctypes.c_size_t(0)
+    _check("moe_align_workspace_size", _lib.moe_align_workspace_size(T, k, E, block_m, ctypes.byref(out)))
+    return out.value
+
+
+def moe_workspace_layout(cfg) -> moe_ws_layout_t:
+    out = moe_ws_layout_t()
+    _check("moe_workspace_layout", _lib.moe_workspace_layout(ctypes.byref(cfg), ctypes.byref(out)))
+    return out
+
+
+def moe_workspace_size(cfg) -> int:
+    out = ctypes.c_size_t(0)
+    _check("moe_workspace_size", _lib.moe_workspace_size(ctypes.byref(cfg), ctypes.byref(out)))
+    return out.value
+
+
+def moe_route(cfg, x, Wg, logits, topk_ids, topk_w, stream=None):
+    _check("moe_route", _lib.moe_route(ctypes.byref(cfg), _ptr(x), _ptr(Wg), _ptr(logits),
+                                       _ptr(topk_ids), _ptr(topk_w), _stream(stream)))
+
+
+def moe_align(topk_ids, T, k, E, block_m, sorted_ids, expert_ids, num_post_padded,
+              counts=None, ws=None, ws_bytes=0, stream=None):
+    _check("moe_align", _lib.moe_align(_ptr(topk_ids), T, k, E, block_m, _ptr(sorted_ids),
+                                       _ptr(expert_ids), _ptr(num_post_padded), _ptr(counts),
+                                       _ptr(ws), ws_bytes, _stream(stream)))
+
+
+def moe_expert_gemm1(cfg, x, W13, sorted_ids, expert_ids, num_post_padded, block_m, act,
+                     stream=None):
+    _check("moe_expert_gemm1", _lib.moe_expert_gemm1(
+        ctypes.byref(cfg), _ptr(x), _ptr(W13), _ptr(sorted_ids), _ptr(expert_ids),
+        _ptr(num_post_padded), block_m, _ptr(act), _stream(stream)))
+
+
+def moe_expert_gemm2(cfg, act, W2, sorted_ids, expert_ids, num_post_padded, block_m, topk_w, y,
+                     stream=None):
+    _check("moe_expert_gemm2", _lib.moe_expert_gemm2(
+        ctypes.byref(cfg), _ptr(act), _ptr(W2), _ptr(sorted_ids), _ptr(expert_ids),
+        _ptr(num_post_padded), block_m, _ptr(topk_w), _ptr(y), _stream(stream)))
+
+
+def moe_grouped_swiglu(cfg, x, W13, W2, sorted_ids, expert_ids, num_post_padded, block_m,
+                       topk_w, y, ws, ws_bytes, stream=None):
+    _check("moe_grouped_swiglu", _lib.moe_grouped_swiglu(
+        ctypes.byref(cfg), _ptr(x), _ptr(W13), _ptr(W2), _ptr(sorted_ids), _ptr(expert_ids),
+        _ptr(num_post_padded), block_m, _ptr(topk_w), _ptr(y), _ptr(ws), ws_bytes,
+        _stream(stream)))
+
+
+def moe_combine(y, T, k, H, dtype, out, stream=None):
+    _check("moe_combine", _lib.moe_combine(_ptr(y), T, k, H, dtype, _ptr(out), _stream(stream)))
+
+
+def moe_forward(cfg, x, Wg, W13, W2, out, ws, ws_bytes, stream=None):
+    _check("moe_forward", _lib.moe_forward(ctypes.byref(cfg), _ptr(x), _ptr(Wg), _ptr(W13),
+                                           _ptr(W2), _ptr(out), _ptr(ws), ws_bytes,
+                                           _stream(stream)))
+
+
+def moe_device_status(reset=True) -> int:
+    return _lib.moe_device_status(int(bool(reset)))

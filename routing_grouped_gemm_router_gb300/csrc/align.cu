@@ -1,0 +1,252 @@
+// align.cu — the block-aligned indirection table (sorted_ids / expert_ids / padded total).
+//
+// "Mixture-of-Experts Kernels: Routing, Permutation, and Grouped GEMM", §5: histogram of
+// the flat rows r = t*k + j over experts, round each count up to BLOCK_M, exclusive scan
+// for each expert's run start, scatter r to start[e] + rank. The rank is the number of
+// earlier rows (smaller r) routed to the same expert, so each run is in ascending r and
+// the table is deterministic. Nothing is sorted: the rank comes from a warp match
+// (__match_any_sync) inside a warp plus per-warp counts in shared memory across warps.
+//
+// Small problems (T*k <= kSmallRows) run all steps in one CTA. Larger ones split the rows
+// into chunks of kChunk: a per-chunk histogram kernel, a single-CTA scan kernel that turns
+// the chunk histograms into absolute write offsets, and a per-chunk scatter kernel.
+#include "common.cuh"
+
+namespace moe {
+
+constexpr int kAlignThreads = 1024;
+constexpr int kAlignWarps = kAlignThreads / 32;
+constexpr int kSmallRows = 4096;
+constexpr int kChunk = 1024;  // rows per CTA in the multi-CTA path (one round)
+
+__device__ int g_align_status;
+
+int align_status_read(int reset) {
+  int v = 0;
+  cudaMemcpyFromSymbol(&v, g_align_status, sizeof(int));
+  if (reset) {
+    int z = 0;
+    cudaMemcpyToSymbol(g_align_status, &z, sizeof(int));
+  }
+  return v;
+}
+
+size_t align_scratch_bytes(int T, int k, int E, int /*block_m*/) {
+  int64_t n = (int64_t)T * k;
+  if (n <= kSmallRows) return 0;
+  int64_t chunks = ceil_div64(n, kChunk);
+  return (size_t)(chunks * E) * sizeof(int32_t);
+}
+
+__device__ __forceinline__ int load_expert(const int32_t* ids, int r, int E) {
+  int e = ids[r];
+  if (e < 0 || e >= E) {
+    atomicExch(&g_align_status, kStatusBadExpert);
+    return -1;
+  }
+  return e;
+}
+
+// Block-wide exclusive scan over E <= kAlignThreads values (one per thread).
+__device__ int block_exclusive_scan(int v, int* warp_tot, int* total_out) {
+  const int lane = threadIdx.x % 32, warp = threadIdx.x / 32;
+  int inc = v;
+#pragma unroll
+  for (int off = 1; off < 32; off <<= 1) {
+    int o = __shfl_up_sync(0xffffffffu, inc, off);
+    if (lane >= off) inc += o;
+  }
+  if (lane == 31) warp_tot[warp] = inc;
+  __syncthreads();
+  if (warp == 0) {
+    int wv = lane < kAlignWarps ? warp_tot[lane] : 0;
+    int wi = wv;
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+      int o = __shfl_up_sync(0xffffffffu, wi, off);
+      if (lane >= off) wi += o;
+    }
+    if (lane < kAlignWarps) warp_tot[lane] = wi - wv;  // exclusive warp offsets
+    if (lane == 31) *total_out = wi;
+  }
+  __syncthreads();
+  return warp_tot[warp] + inc - v;
+}
+
+// Pads, scans and writes the per-expert metadata from cnt[E] (in shared memory).
+// Leaves start[e] in shared memory. Also writes expert_ids, the padding sentinels, the
+// sentinel tail of sorted_ids, num_post_padded and counts.
+__device__ void scan_and_fill(const int* cnt, int* start, int* warp_tot, int* total_sh, int n,
+                              int E, int B, int max_padded, int32_t* sorted_ids,
+                              int32_t* expert_ids, int32_t* npp, int32_t* counts) {
+  const int tid = threadIdx.x;
+  int c = tid < E ? cnt[tid] : 0;
+  int p = (c + B - 1) / B * B;
+  int st = block_exclusive_scan(p, warp_tot, total_sh);
+  if (tid < E) start[tid] = st;
+  __syncthreads();
+  const int total = *total_sh;
+  if (tid == 0) *npp = total;
+  if (counts && tid < E) counts[tid] = c;
+  // Sentinels: the padding slots of each run, then the tail [total, max_padded).
+  if (tid < E)
+    for (int q = st + c; q < st + p; ++q) sorted_ids[q] = n;
+  for (int q = total + tid; q < max_padded; q += blockDim.x) sorted_ids[q] = n;
+  // expert_ids: tile -> the expert whose run covers it (largest e with start[e] <= pos).
+  const int tiles = max_padded / B;
+  for (int tile = tid; tile < tiles; tile += blockDim.x) {
+    int pos = tile * B, e = -1;
+    if (pos < total) {
+      int lo = 0, hi = E - 1;
+      while (lo < hi) {
+        int mid = (lo + hi + 1) / 2;
+        if (start[mid] <= pos) lo = mid; else hi = mid - 1;
+      }
+      e = lo;
+    }
+    expert_ids[tile] = e;
+  }
+}
+
+// Stable scatter of rows [r0, r1) given each expert's next free slot run_base[e] (shared).
+// wcnt[kAlignWarps][E] (shared) must be zero on entry and is zero on exit.
+__device__ void stable_scatter(const int32_t* ids, int r0, int r1, int E, int* run_base,
+                               int* wcnt, int32_t* sorted_ids) {
+  const int lane = threadIdx.x % 32, warp = threadIdx.x / 32;
+  const unsigned lt_mask = (1u << lane) - 1u;
+  for (int base = r0; base < r1; base += blockDim.x) {
+    int r = base + threadIdx.x;
+    int e = r < r1 ? load_expert(ids, r, E) : -1;
+    unsigned peers = __match_any_sync(0xffffffffu, e);
+    int rank = __popc(peers & lt_mask);
+    if (e >= 0 && rank == 0) wcnt[warp * E + e] = __popc(peers);
+    __syncthreads();
+    if (e >= 0) {
+      int off = run_base[e] + rank;
+      for (int w = 0; w < warp; ++w) off += wcnt[w * E + e];
+      sorted_ids[off] = r;
+    }
+    __syncthreads();
+    for (int q = threadIdx.x; q < E; q += blockDim.x) {
+      int s = 0;
+      for (int w = 0; w < kAlignWarps; ++w) {
+        s += wcnt[w * E + q];
+        wcnt[w * E + q] = 0;
+      }
+      run_base[q] += s;
+    }
+    __syncthreads();
+  }
+}
+
+// ---- single CTA: histogram, scan, fill, scatter --------------------------------------
+__global__ void __launch_bounds__(kAlignThreads) align_small_kernel(
+    const int32_t* __restrict__ ids, int n, int E, int B, int max_padded,
+    int32_t* __restrict__ sorted_ids, int32_t* __restrict__ expert_ids, int32_t* npp,
+    int32_t* counts) {
+  extern __shared__ int sm[];
+  int* cnt = sm;                   // [E]
+  int* start = cnt + E;            // [E]
+  int* wcnt = start + E;           // [kAlignWarps * E]
+  int* warp_tot = wcnt + kAlignWarps * E;  // [32]
+  int* total_sh = warp_tot + 32;
+  for (int q = threadIdx.x; q < E * (2 + kAlignWarps); q += blockDim.x) sm[q] = 0;
+  __syncthreads();
+  for (int r = threadIdx.x; r < n; r += blockDim.x) {
+    int e = load_expert(ids, r, E);
+    if (e >= 0) atomicAdd(&cnt[e], 1);
+  }
+  __syncthreads();
+  scan_and_fill(cnt, start, warp_tot, total_sh, n, E, B, max_padded, sorted_ids, expert_ids,
+                npp, counts);
+  __syncthreads();
+  stable_scatter(ids, 0, n, E, start, wcnt, sorted_ids);
+}
+
+// ---- multi CTA: per-chunk histogram ---------------------------------------------------
+__global__ void __launch_bounds__(256) align_hist_kernel(const int32_t* __restrict__ ids,
+                                                         int n, int E,
+                                                         int32_t* __restrict__ chunk_cnt) {
+  extern __shared__ int hist[];
+  for (int q = threadIdx.x; q < E; q += blockDim.x) hist[q] = 0;
+  __syncthreads();
+  const int r0 = blockIdx.x * kChunk, r1 = min(n, r0 + kChunk);
+  for (int r = r0 + threadIdx.x; r < r1; r += blockDim.x) {
+    int e = load_expert(ids, r, E);
+    if (e >= 0) atomicAdd(&hist[e], 1);
+  }
+  __syncthreads();
+  for (int q = threadIdx.x; q < E; q += blockDim.x) chunk_cnt[(size_t)blockIdx.x * E + q] = hist[q];
+}
+
+// ---- multi CTA: totals, scan, fill, absolute chunk offsets ----------------------------
+__global__ void __launch_bounds__(kAlignThreads) align_scan_kernel(
+    int32_t* __restrict__ chunk_cnt, int chunks, int n, int E, int B, int max_padded,
+    int32_t* __restrict__ sorted_ids, int32_t* __restrict__ expert_ids, int32_t* npp,
+    int32_t* counts) {
+  extern __shared__ int sm[];
+  int* cnt = sm;
+  int* start = cnt + E;
+  int* warp_tot = start + E;
+  int* total_sh = warp_tot + 32;
+  // Per expert: running prefix over chunks (chunk-relative base) and the total count.
+  for (int e = threadIdx.x; e < E; e += blockDim.x) {
+    int run = 0;
+    for (int c = 0; c < chunks; ++c) {
+      int v = chunk_cnt[(size_t)c * E + e];
+      chunk_cnt[(size_t)c * E + e] = run;
+      run += v;
+    }
+    cnt[e] = run;
+  }
+  __syncthreads();
+  scan_and_fill(cnt, start, warp_tot, total_sh, n, E, B, max_padded, sorted_ids, expert_ids,
+                npp, counts);
+  __syncthreads();
+  for (int i = threadIdx.x; i < chunks * E; i += blockDim.x) chunk_cnt[i] += start[i % E];
+}
+
+// ---- multi CTA: stable scatter of one chunk --------------------------------------------
+__global__ void __launch_bounds__(kAlignThreads) align_scatter_kernel(
+    const int32_t* __restrict__ ids, const int32_t* __restrict__ chunk_base, int n, int E,
+    int32_t* __restrict__ sorted_ids) {
+  extern __shared__ int sm[];
+  int* run_base = sm;        // [E]
+  int* wcnt = run_base + E;  // [kAlignWarps * E]
+  for (int q = threadIdx.x; q < E; q += blockDim.x) run_base[q] = chunk_base[(size_t)blockIdx.x * E + q];
+  for (int q = threadIdx.x; q < kAlignWarps * E; q += blockDim.x) wcnt[q] = 0;
+  __syncthreads();
+  const int r0 = blockIdx.x * kChunk, r1 = min(n, r0 + kChunk);
+  stable_scatter(ids, r0, r1, E, run_base, wcnt, sorted_ids);
+}
+
+static bool set_smem(const void* fn, size_t bytes) {
+  if (bytes <= 48 * 1024) return true;
+  return cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bytes) ==
+         cudaSuccess;
+}
+
+moe_status_t launch_align(const int32_t* ids, int T, int k, int E, int B, int max_padded,
+                          int32_t* sorted_ids, int32_t* expert_ids, int32_t* npp,
+                          int32_t* counts, void* scratch, cudaStream_t s) {
+  const int n = T * k;
+  if (n <= kSmallRows) {
+    size_t smem = (size_t)(E * (2 + kAlignWarps) + 33) * sizeof(int);
+    if (!set_smem((const void*)align_small_kernel, smem)) return MOE_ERR_CUDA;
+    align_small_kernel<<<1, kAlignThreads, smem, s>>>(ids, n, E, B, max_padded, sorted_ids,
+                                                      expert_ids, npp, counts);
+    return last_launch_status();
+  }
+  const int chunks = ceil_div(n, kChunk);
+  int32_t* cc = (int32_t*)scratch;
+  align_hist_kernel<<<chunks, 256, E * sizeof(int), s>>>(ids, n, E, cc);
+  size_t smem_scan = (size_t)(2 * E + 33) * sizeof(int);
+  align_scan_kernel<<<1, kAlignThreads, smem_scan, s>>>(cc, chunks, n, E, B, max_padded,
+                                                        sorted_ids, expert_ids, npp, counts);
+  size_t smem_sc = (size_t)(E * (1 + kAlignWarps)) * sizeof(int);
+  if (!set_smem((const void*)align_scatter_kernel, smem_sc)) return MOE_ERR_CUDA;
+  align_scatter_kernel<<<chunks, kAlignThreads, smem_sc, s>>>(ids, cc, n, E, sorted_ids);
+  return last_launch_status();
+}
+
+}  // namespace moe

@@ -1,0 +1,258 @@
+// api.cu — the C ABI (include/moe.h): argument checks, workspace layout and the order in
+// which the kernels of the layer are enqueued. No entry point allocates, frees,
+// synchronises or reads device memory on the host (moe_device_status excepted).
+#include <mutex>
+
+#include "common.cuh"
+
+namespace moe {
+
+int num_sms() {
+  static int cache[64];
+  static std::once_flag once[64];
+  int dev = 0;
+  cudaGetDevice(&dev);
+  if (dev < 0 || dev >= 64) return 148;
+  std::call_once(once[dev], [dev] {
+    int v = 0;
+    cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, dev);
+    cache[dev] = v > 0 ? v : 148;
+  });
+  return cache[dev];
+}
+
+static bool aligned16(const void* p) { return ((uintptr_t)p & 15u) == 0; }
+
+static constexpr int kMaxE = 512;
+
+static moe_status_t check_cfg(const moe_config_t* c) {
+  if (!c) return MOE_ERR_INVALID_ARG;
+  if (c->T < 1 || c->H < 8 || c->I < 8 || c->E < 1 || c->k < 1 || c->k > c->E || c->k > 32)
+    return MOE_ERR_INVALID_ARG;
+  if (c->H % 8 || c->I % 8) return MOE_ERR_INVALID_ARG;
+  if (c->dtype != MOE_F32 && c->dtype != MOE_BF16) return MOE_ERR_INVALID_ARG;
+  if (c->mode != MOE_ROUTE_SOFTMAX && c->mode != MOE_ROUTE_SIGMOID_GROUPED)
+    return MOE_ERR_INVALID_ARG;
+  if (c->mode == MOE_ROUTE_SIGMOID_GROUPED) {
+    if (c->n_group < 1 || c->n_group > 32 || c->E % c->n_group) return MOE_ERR_INVALID_ARG;
+    if (c->topk_group < 1 || c->topk_group > c->n_group) return MOE_ERR_INVALID_ARG;
+    if ((int64_t)c->topk_group * (c->E / c->n_group) < c->k) return MOE_ERR_INVALID_ARG;
+  }
+  if (c->E > kMaxE) return MOE_ERR_UNSUPPORTED;
+  if ((int64_t)c->T * c->k > (int64_t)1 << 30) return MOE_ERR_UNSUPPORTED;
+  return MOE_OK;
+}
+
+static int block_m_for(moe_dtype_t d) { return d == MOE_BF16 ? 128 : 16; }
+
+static bool block_m_ok(const moe_config_t* c, int block_m) {
+  return block_m >= 1 && block_m % block_m_for(c->dtype) == 0 && block_m <= 4096;
+}
+
+}  // namespace moe
+
+using namespace moe;
+
+extern "C" {
+
+int moe_abi_version(void) { return MOE_ABI_VERSION; }
+
+const char* moe_status_string(moe_status_t s) {
+  switch (s) {
+    case MOE_OK: return "ok";
+    case MOE_ERR_INVALID_ARG: return "invalid argument";
+    case MOE_ERR_UNSUPPORTED: return "unsupported configuration";
+    case MOE_ERR_WORKSPACE: return "workspace missing or too small";
+    case MOE_ERR_CUDA: return "CUDA error";
+  }
+  return "unknown status";
+}
+
+int moe_block_m(const moe_config_t* cfg) {
+  if (check_cfg(cfg) != MOE_OK) return 0;
+  return block_m_for(cfg->dtype);
+}
+
+size_t moe_max_padded_rows(int T, int k, int E, int block_m) {
+  if (T < 1 || k < 1 || E < 1 || block_m < 1) return 0;
+  // total = sum_e ceil(n_e / B) * B <= T*k + min(E, T*k) * (B - 1), and total is a
+  // multiple of B, so it also fits the bound rounded down to whole tiles.
+  const int64_t n = (int64_t)T * k;
+  const int64_t bound = n + std::min<int64_t>(E, n) * (block_m - 1);
+  return (size_t)(bound / block_m * block_m);
+}
+
+moe_status_t moe_align_workspace_size(int T, int k, int E, int block_m, size_t* bytes) {
+  if (!bytes || T < 1 || k < 1 || k > E || E < 1 || block_m < 1) return MOE_ERR_INVALID_ARG;
+  if (E > kMaxE) return MOE_ERR_UNSUPPORTED;
+  *bytes = align_scratch_bytes(T, k, E, block_m);
+  return MOE_OK;
+}
+
+moe_status_t moe_workspace_layout(const moe_config_t* c, moe_ws_layout_t* L) {
+  moe_status_t st = check_cfg(c);
+  if (st != MOE_OK) return st;
+  if (!L) return MOE_ERR_INVALID_ARG;
+  const int B = block_m_for(c->dtype);
+  const size_t mp = moe_max_padded_rows(c->T, c->k, c->E, B);
+  const size_t es = dtype_size(c->dtype);
+  const size_t n = (size_t)c->T * c->k;
+  size_t off = 0;
+  auto take = [&](size_t bytes) {
+    size_t o = off;
+    off = align_up(off + bytes, 256);
+    return o;
+  };
+  L->logits = take((size_t)c->T * c->E * 4);
+  L->topk_ids = take(n * 4);
+  L->topk_w = take(n * 4);
+  L->sorted_ids = take(mp * 4);
+  L->expert_ids = take(mp / B * 4);
+  L->num_post_padded = take(4);
+  L->counts = take((size_t)c->E * 4);
+  L->align_scratch = take(align_scratch_bytes(c->T, c->k, c->E, B));
+  L->act = take(mp * c->I * es);
+  L->y = take(n * c->H * es);
+  L->total = off;
+  L->block_m = B;
+  L->max_padded = (int)mp;
+  return MOE_OK;
+}
+
+moe_status_t moe_workspace_size(const moe_config_t* c, size_t* bytes) {
+  moe_ws_layout_t L;
+  if (!bytes) return MOE_ERR_INVALID_ARG;
+  moe_status_t st = moe_workspace_layout(c, &L);
+  if (st == MOE_OK) *bytes = L.total;
+  return st;
+}
+
+moe_status_t moe_route(const moe_config_t* c, const void* x, const void* Wg, float* logits,
+                       int32_t* topk_ids, float* topk_w, cudaStream_t stream) {
+  moe_status_t st = check_cfg(c);
+  if (st != MOE_OK) return st;
+  if (!x || !Wg || !logits || !topk_ids || !topk_w) return MOE_ERR_INVALID_ARG;
+  if (c->dtype == MOE_BF16) {
+    if (!aligned16(x) || !aligned16(Wg)) return MOE_ERR_INVALID_ARG;
+    st = c->E <= 256 ? launch_router_tc(*c, x, Wg, logits, stream)
+                     : launch_router_simt(*c, x, Wg, logits, stream);
+  } else {
+    st = launch_router_simt(*c, x, Wg, logits, stream);
+  }
+  if (st != MOE_OK) return st;
+  return launch_topk(*c, logits, topk_ids, topk_w, stream);
+}
+
+moe_status_t moe_align(const int32_t* topk_ids, int T, int k, int E, int block_m,
+                       int32_t* sorted_ids, int32_t* expert_ids, int32_t* num_post_padded,
+                       int32_t* counts, void* ws, size_t ws_bytes, cudaStream_t stream) {
+  if (!topk_ids || !sorted_ids || !expert_ids || !num_post_padded) return MOE_ERR_INVALID_ARG;
+  if (T < 1 || k < 1 || E < 1 || k > E || block_m < 1 || block_m > 4096)
+    return MOE_ERR_INVALID_ARG;
+  if (E > kMaxE) return MOE_ERR_UNSUPPORTED;
+  if ((int64_t)T * k > (int64_t)1 << 30) return MOE_ERR_UNSUPPORTED;
+  const size_t need = align_scratch_bytes(T, k, E, block_m);
+  if (need && (!ws || ws_bytes < need)) return MOE_ERR_WORKSPACE;
+  const int mp = (int)moe_max_padded_rows(T, k, E, block_m);
+  return launch_align(topk_ids, T, k, E, block_m, mp, sorted_ids, expert_ids, num_post_padded,
+                      counts, ws, stream);
+}
+
+static moe_status_t check_gemm_args(const moe_config_t* c, int block_m) {
+  moe_status_t st = check_cfg(c);
+  if (st != MOE_OK) return st;
+  if (!block_m_ok(c, block_m)) return MOE_ERR_INVALID_ARG;
+  return MOE_OK;
+}
+
+moe_status_t moe_expert_gemm1(const moe_config_t* c, const void* x, const void* W13,
+                              const int32_t* sorted_ids, const int32_t* expert_ids,
+                              const int32_t* npp, int block_m, void* act, cudaStream_t stream) {
+  moe_status_t st = check_gemm_args(c, block_m);
+  if (st != MOE_OK) return st;
+  if (!x || !W13 || !sorted_ids || !expert_ids || !npp || !act) return MOE_ERR_INVALID_ARG;
+  const int mp = (int)moe_max_padded_rows(c->T, c->k, c->E, block_m);
+  if (c->dtype == MOE_BF16) {
+    if (!aligned16(x) || !aligned16(W13) || !aligned16(act) || !aligned16(sorted_ids))
+      return MOE_ERR_INVALID_ARG;
+    return launch_gemm1_tc(*c, x, W13, sorted_ids, expert_ids, npp, block_m, mp, act, stream);
+  }
+  return launch_gemm1_simt(*c, (const float*)x, (const float*)W13, sorted_ids, expert_ids, npp,
+                           block_m, mp, (float*)act, stream);
+}
+
+moe_status_t moe_expert_gemm2(const moe_config_t* c, const void* act, const void* W2,
+                              const int32_t* sorted_ids, const int32_t* expert_ids,
+                              const int32_t* npp, int block_m, const float* topk_w, void* y,
+                              cudaStream_t stream) {
+  moe_status_t st = check_gemm_args(c, block_m);
+  if (st != MOE_OK) return st;
+  if (!act || !W2 || !sorted_ids || !expert_ids || !npp || !topk_w || !y)
+    return MOE_ERR_INVALID_ARG;
+  const int mp = (int)moe_max_padded_rows(c->T, c->k, c->E, block_m);
+  if (c->dtype == MOE_BF16) {
+    if (!aligned16(act) || !aligned16(W2) || !aligned16(y)) return MOE_ERR_INVALID_ARG;
+    return launch_gemm2_tc(*c, act, W2, sorted_ids, expert_ids, npp, block_m, mp, topk_w, y,
+                           stream);
+  }
+  return launch_gemm2_simt(*c, (const float*)act, (const float*)W2, sorted_ids, expert_ids, npp,
+                           block_m, mp, topk_w, (float*)y, stream);
+}
+
+moe_status_t moe_grouped_swiglu(const moe_config_t* c, const void* x, const void* W13,
+                                const void* W2, const int32_t* sorted_ids,
+                                const int32_t* expert_ids, const int32_t* npp, int block_m,
+                                const float* topk_w, void* y, void* ws, size_t ws_bytes,
+                                cudaStream_t stream) {
+  moe_status_t st = check_gemm_args(c, block_m);
+  if (st != MOE_OK) return st;
+  const size_t mp = moe_max_padded_rows(c->T, c->k, c->E, block_m);
+  if (!ws || ws_bytes < mp * c->I * dtype_size(c->dtype)) return MOE_ERR_WORKSPACE;
+  st = moe_expert_gemm1(c, x, W13, sorted_ids, expert_ids, npp, block_m, ws, stream);
+  if (st != MOE_OK) return st;
+  return moe_expert_gemm2(c, ws, W2, sorted_ids, expert_ids, npp, block_m, topk_w, y, stream);
+}
+
+moe_status_t moe_combine(const void* y, int T, int k, int H, moe_dtype_t dtype, void* out,
+                         cudaStream_t stream) {
+  if (!y || !out || T < 1 || k < 1 || H < 8 || H % 8) return MOE_ERR_INVALID_ARG;
+  if (dtype != MOE_F32 && dtype != MOE_BF16) return MOE_ERR_INVALID_ARG;
+  if (!aligned16(y) || !aligned16(out)) return MOE_ERR_INVALID_ARG;
+  return launch_combine(y, T, k, H, dtype, out, stream);
+}
+
+moe_status_t moe_forward(const moe_config_t* c, const void* x, const void* Wg, const void* W13,
+                         const void* W2, void* out, void* ws, size_t ws_bytes,
+                         cudaStream_t stream) {
+  moe_ws_layout_t L;
+  moe_status_t st = moe_workspace_layout(c, &L);
+  if (st != MOE_OK) return st;
+  if (!x || !Wg || !W13 || !W2 || !out) return MOE_ERR_INVALID_ARG;
+  if (!ws || ws_bytes < L.total || ((uintptr_t)ws & 255u)) return MOE_ERR_WORKSPACE;
+  uint8_t* b = (uint8_t*)ws;
+  float* logits = (float*)(b + L.logits);
+  int32_t* ids = (int32_t*)(b + L.topk_ids);
+  float* w = (float*)(b + L.topk_w);
+  int32_t* sid = (int32_t*)(b + L.sorted_ids);
+  int32_t* eid = (int32_t*)(b + L.expert_ids);
+  int32_t* npp = (int32_t*)(b + L.num_post_padded);
+  int32_t* counts = (int32_t*)(b + L.counts);
+  if ((st = moe_route(c, x, Wg, logits, ids, w, stream)) != MOE_OK) return st;
+  if ((st = moe_align(ids, c->T, c->k, c->E, L.block_m, sid, eid, npp, counts,
+                      b + L.align_scratch, L.act - L.align_scratch, stream)) != MOE_OK)
+    return st;
+  if ((st = moe_expert_gemm1(c, x, W13, sid, eid, npp, L.block_m, b + L.act, stream)) != MOE_OK)
+    return st;
+  if ((st = moe_expert_gemm2(c, b + L.act, W2, sid, eid, npp, L.block_m, w, b + L.y, stream)) !=
+      MOE_OK)
+    return st;
+  return moe_combine(b + L.y, c->T, c->k, c->H, c->dtype, out, stream);
+}
+
+int moe_device_status(int reset) {
+  int a = align_status_read(reset);
+  int t = tc_status_read(reset);
+  return t ? t : a;
+}
+
+}  // extern "C"

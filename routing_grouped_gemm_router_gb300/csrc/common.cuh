@@ -1,0 +1,66 @@
+// common.cuh — shared host/device helpers of the MoE library (internal header).
+#pragma once
+
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include <algorithm>
+
+#include "../../include/moe.h"
+
+namespace moe {
+
+// Device status codes (moe_device_status).
+enum : int { kStatusOk = 0, kStatusBadExpert = 1, kStatusTimeout = 2 };
+
+__host__ __device__ inline int ceil_div(int a, int b) { return (a + b - 1) / b; }
+__host__ __device__ inline int64_t ceil_div64(int64_t a, int64_t b) { return (a + b - 1) / b; }
+
+inline size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
+
+// Number of SMs of the current device (cached per device).
+int num_sms();
+
+// Launch-error check shared by all entry points.
+inline moe_status_t last_launch_status() {
+  return cudaGetLastError() == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
+}
+
+inline size_t dtype_size(moe_dtype_t d) { return d == MOE_BF16 ? 2 : 4; }
+
+// ---------------------------------------------------------------- kernel entry wrappers
+// Implemented in the .cu files; all enqueue on `stream` and return MOE_OK/MOE_ERR_CUDA.
+
+moe_status_t launch_router_simt(const moe_config_t& c, const void* x, const void* Wg,
+                                float* logits, cudaStream_t s);
+moe_status_t launch_router_tc(const moe_config_t& c, const void* x, const void* Wg,
+                              float* logits, cudaStream_t s);
+moe_status_t launch_topk(const moe_config_t& c, const float* logits, int32_t* ids, float* w,
+                         cudaStream_t s);
+size_t align_scratch_bytes(int T, int k, int E, int block_m);
+moe_status_t launch_align(const int32_t* ids, int T, int k, int E, int block_m, int max_padded,
+                          int32_t* sorted_ids, int32_t* expert_ids, int32_t* npp,
+                          int32_t* counts, void* scratch, cudaStream_t s);
+moe_status_t launch_gemm1_simt(const moe_config_t& c, const float* x, const float* W13,
+                               const int32_t* sid, const int32_t* eid, const int32_t* npp,
+                               int block_m, int max_padded, float* act, cudaStream_t s);
+moe_status_t launch_gemm2_simt(const moe_config_t& c, const float* act, const float* W2,
+                               const int32_t* sid, const int32_t* eid, const int32_t* npp,
+                               int block_m, int max_padded, const float* topk_w, float* y,
+                               cudaStream_t s);
+moe_status_t launch_gemm1_tc(const moe_config_t& c, const void* x, const void* W13,
+                             const int32_t* sid, const int32_t* eid, const int32_t* npp,
+                             int block_m, int max_padded, void* act, cudaStream_t s);
+moe_status_t launch_gemm2_tc(const moe_config_t& c, const void* act, const void* W2,
+                             const int32_t* sid, const int32_t* eid, const int32_t* npp,
+                             int block_m, int max_padded, const float* topk_w, void* y,
+                             cudaStream_t s);
+moe_status_t launch_combine(const void* y, int T, int k, int H, moe_dtype_t dt, void* out,
+                            cudaStream_t s);
+
+int align_status_read(int reset);
+int tc_status_read(int reset);
+
+}  // namespace moe

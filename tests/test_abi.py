@@ -1,0 +1,110 @@
+"""The C-ABI library loads, exports every declared entry point, and its host-side logic
+(argument checks, sizes, workspace layout) behaves, all without a GPU."""
+import ctypes
+import os
+import re
+
+import pytest
+
+import oracle as O
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def L():
+    from routing_grouped_gemm_router_gb300 import build
+    build.build()
+    from routing_grouped_gemm_router_gb300 import _lib
+    return _lib
+
+
+def _declared():
+    names = []
+    for h in os.listdir(os.path.join(ROOT, "include")):
+        if h.endswith(".h"):
+            src = open(os.path.join(ROOT, "include", h)).read()
+            src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+            names += re.findall(r"\b(moe_\w+)\s*\(", src)
+    return sorted(set(names))
+
+
+def test_library_exports_every_declared_symbol(L):
+    decl = _declared()
+    assert "moe_forward" in decl and "moe_align" in decl and "moe_route" in decl
+    cdll = ctypes.CDLL(L.LIB_PATH)
+    missing = [n for n in decl if not hasattr(cdll, n)]
+    assert not missing, f"declared but not exported: {missing}"
+    assert set(decl) <= set(L.EXPORTED) | set(decl)
+    assert L.moe_abi_version() == 1
+
+
+def test_status_strings(L):
+    for s in range(5):
+        assert L.status_string(s)
+
+
+@pytest.mark.parametrize("T,k,E,B", [(64, 2, 8, 16), (1, 4, 128, 128), (4096, 8, 256, 128),
+                                     (3, 3, 5, 4), (37, 1, 8, 16)])
+def test_max_padded_matches_oracle(L, T, k, E, B):
+    assert L.moe_max_padded_rows(T, k, E, B) == O.max_padded_rows(T, k, E, B)
+
+
+def test_block_m_and_workspace(L):
+    cfg = L.make_config(4096, 4096, 14336, 8, 2, L.MOE_BF16)
+    assert L.moe_block_m(cfg) == 128
+    lay = L.moe_workspace_layout(cfg)
+    assert lay.block_m == 128 and lay.max_padded == O.max_padded_rows(4096, 2, 8, 128)
+    offs = [lay.logits, lay.topk_ids, lay.topk_w, lay.sorted_ids, lay.expert_ids,
+            lay.num_post_padded, lay.counts, lay.align_scratch, lay.act, lay.y]
+    assert all(o % 256 == 0 for o in offs) and offs == sorted(offs)
+    assert lay.total >= lay.y + 4096 * 2 * 4096 * 2
+    assert L.moe_workspace_size(cfg) == lay.total
+    cfg32 = L.make_config(64, 64, 96, 8, 2, L.MOE_F32)
+    assert L.moe_block_m(cfg32) == 16
+
+
+@pytest.mark.parametrize("kw", [dict(T=0), dict(k=9), dict(H=12), dict(I=100), dict(E=0)])
+def test_invalid_configs_rejected(L, kw):
+    a = dict(T=4, H=64, I=96, E=8, k=2)
+    a.update(kw)
+    cfg = L.make_config(a["T"], a["H"], a["I"], a["E"], a["k"], L.MOE_F32)
+    with pytest.raises(L.MoeError) as ei:
+        L.moe_workspace_size(cfg)
+    assert ei.value.status == L.MOE_ERR_INVALID_ARG
+
+
+def test_grouped_router_config_checks(L):
+    bad_group = L.make_config(4, 64, 96, 10, 2, L.MOE_BF16, L.MOE_ROUTE_SIGMOID_GROUPED,
+                              n_group=4, topk_group=2)
+    with pytest.raises(L.MoeError):
+        L.moe_workspace_size(bad_group)
+    too_few = L.make_config(4, 64, 96, 16, 8, L.MOE_BF16, L.MOE_ROUTE_SIGMOID_GROUPED,
+                            n_group=8, topk_group=2)   # 2 groups x 2 experts < k = 8
+    with pytest.raises(L.MoeError):
+        L.moe_workspace_size(too_few)
+    too_many_e = L.make_config(4, 64, 96, 1024, 2, L.MOE_BF16)
+    with pytest.raises(L.MoeError) as ei:
+        L.moe_workspace_size(too_many_e)
+    assert ei.value.status == L.MOE_ERR_UNSUPPORTED
+
+
+def test_null_pointers_rejected_before_any_launch(L):
+    cfg = L.make_config(4, 64, 96, 8, 2, L.MOE_F32)
+    with pytest.raises(L.MoeError) as ei:
+        L.moe_route(cfg, 0, 0, 0, 0, 0, stream=0)
+    assert ei.value.status == L.MOE_ERR_INVALID_ARG
+    with pytest.raises(L.MoeError) as ei:
+        L.moe_forward(cfg, 16, 16, 16, 16, 16, 0, 0, stream=0)
+    assert ei.value.status == L.MOE_ERR_WORKSPACE
+    with pytest.raises(L.MoeError) as ei:
+        L.moe_align(0, 4, 2, 8, 16, 0, 0, 0, stream=0)
+    assert ei.value.status == L.MOE_ERR_INVALID_ARG
+
+
+def test_align_workspace_sizes(L):
+    assert L.moe_align_workspace_size(64, 2, 8, 16) == 0           # one-CTA path
+    assert L.moe_align_workspace_size(8192, 8, 128, 128) >= 64 * 128 * 4
+    with pytest.raises(L.MoeError) as ei:
+        L.moe_align(16, 8192, 8, 128, 128, 16, 16, 16, ws=None, ws_bytes=0, stream=0)
+    assert ei.value.status == L.MOE_ERR_WORKSPACE

@@ -1,0 +1,77 @@
+"""Parity at the full workload sizes, in the launch configuration the benchmark times.
+
+Each layer is drawn on the GPU (seeded), routed, aligned and run through moe_forward.
+Routing and the indirection table are checked bit-exactly for every token; the layer
+output is checked on a sample of tokens (tokens of the hottest and of the least-loaded
+non-empty expert among them), each recomputed by the float64 oracle.
+"""
+import numpy as np
+import pytest
+import torch
+
+import moe_inputs as mi
+import oracle as O
+from _helpers import (LazyExperts, assert_close, enforce_margins, oracle_logits,
+                      oracle_route_from_logits, sample_tokens, to_np)
+
+pytestmark = [pytest.mark.gpu, pytest.mark.slow]
+DEV = "cuda"
+
+
+@pytest.fixture(scope="module")
+def L():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    from routing_grouped_gemm_router_gb300 import build
+    build.build()
+    from routing_grouped_gemm_router_gb300 import _lib
+    _lib.moe_device_status(True)
+    yield _lib
+    torch.cuda.synchronize()
+    assert _lib.moe_device_status(True) == 0
+
+
+CASES = [(mi.MIXTRAL, 48), (mi.QWEN3, 48), (mi.DSV3, 16)] + \
+        [(mi.GPTOSS.with_T(T), T) for T in mi.GPTOSS_T]
+
+
+@pytest.mark.parametrize("wl,n_sample", CASES, ids=[c[0].name for c in CASES])
+def test_full_size_parity(L, wl, n_sample):
+    from routing_grouped_gemm_router_gb300.layer import MoELayer
+    inp = mi.make_layer(wl, DEV)
+    redraws = enforce_margins(inp)
+    layer = MoELayer(inp.Wg, inp.W13, inp.W2, wl.k, wl.mode, wl.renormalize, wl.scale,
+                     wl.n_group, wl.topk_group, inp.logit_bias, inp.select_bias)
+    out = layer(inp.x)
+    torch.cuda.synchronize()
+    mids = layer.intermediates(wl.T)
+
+    # routing: all tokens, both readings
+    sb = to_np(inp.select_bias) if inp.select_bias is not None else None
+    g_logits = to_np(mids["logits"])
+    l_in = g_logits + (to_np(inp.logit_bias)[None] if inp.logit_bias is not None else 0)
+    g_ids = to_np(mids["topk_ids"])
+    ids_i, w_i = oracle_route_from_logits(l_in, wl, sb)
+    assert np.array_equal(g_ids, ids_i)
+    assert np.abs(to_np(mids["topk_w"]) - w_i).max() <= 2e-5 * max(1.0, np.abs(w_i).max())
+    l_ref = oracle_logits(inp)
+    ids_o, w_o = oracle_route_from_logits(l_ref, wl, sb)
+    assert np.array_equal(g_ids, ids_o), f"routing differs ({redraws} margin redraws)"
+
+    # align: bit-exact
+    B, mp = mids["block_m"], mids["max_padded"]
+    sid, eid, total, counts = O.moe_align(ids_o, B, wl.E, max_padded=mp)
+    assert int(mids["num_post_padded"].item()) == total
+    assert np.array_equal(to_np(mids["counts"]), counts)
+    assert np.array_equal(to_np(mids["sorted_ids"]), sid)
+    assert np.array_equal(to_np(mids["expert_ids"]), eid)
+    if wl.name.startswith("qwen3"):
+        assert (counts == 0).any(), "the skewed workload should leave some experts empty"
+
+    # output: sampled tokens against the float64 oracle
+    toks = sample_tokens(ids_o, n_sample, seed=wl.seed)
+    ref = O.moe_loop(to_np(inp.x[torch.as_tensor(toks, device=DEV)]),
+                     ids_o[toks], w_o[toks], LazyExperts(inp.W13), LazyExperts(inp.W2))
+    got = to_np(out[torch.as_tensor(toks, device=DEV)])
+    assert_close(got, ref, wl.dtype)
+    assert torch.isfinite(out.float()).all()

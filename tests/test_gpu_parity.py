@@ -1,0 +1,423 @@
+"""Parity of the CUDA path (through the C ABI) with the float64 oracle.
+
+Integer work (ids, counts, sorted_ids, expert_ids, padded total) must be bit-exact;
+floating point within the tolerances of tests/_helpers.py. Routing decisions are compared
+both ways: the oracle's top-k fed with the GPU's fp32 logits, and the oracle's own float64
+routing on inputs whose selection margins exceed 1e-4.
+"""
+import zlib
+
+import numpy as np
+import pytest
+import torch
+
+import moe_inputs as mi
+import oracle as O
+from _helpers import (TOPK_W_RTOL, assert_close, enforce_margins, oracle_logits,
+                      oracle_route_from_logits, to_np, weights_for_oracle)
+
+pytestmark = pytest.mark.gpu
+
+DEV = "cuda"
+
+
+@pytest.fixture(scope="module")
+def L():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    from routing_grouped_gemm_router_gb300 import build
+    build.build()
+    from routing_grouped_gemm_router_gb300 import _lib
+    _lib.moe_device_status(True)
+    yield _lib
+    torch.cuda.synchronize()
+    assert _lib.moe_device_status(True) == 0, "a kernel recorded a device fault"
+
+
+def _layer(L, inp):
+    from routing_grouped_gemm_router_gb300.layer import MoELayer
+    wl = inp.wl
+    return MoELayer(inp.Wg, inp.W13, inp.W2, wl.k, wl.mode, wl.renormalize, wl.scale,
+                    wl.n_group, wl.topk_group, inp.logit_bias, inp.select_bias)
+
+
+def _to_dev(inp):
+    f = lambda t: None if t is None else t.to(DEV).contiguous()  # noqa: E731
+    return mi.LayerInputs(inp.wl, f(inp.x), f(inp.Wg), f(inp.W13), f(inp.W2), f(inp.logit_bias),
+                          f(inp.select_bias))
+
+
+def _check_routing_and_align(inp, mids):
+    """ids/weights/align of one forward against the oracle. Returns the oracle's (ids, w)."""
+    wl = inp.wl
+    sb = to_np(inp.select_bias) if inp.select_bias is not None else None
+    g_logits = to_np(mids["logits"])
+    g_ids = to_np(mids["topk_ids"])
+    g_w = to_np(mids["topk_w"])
+    # (i) the oracle's top-k on the GPU's logits (+ the mode-0 offset the kernel adds)
+    l_in = g_logits + (to_np(inp.logit_bias)[None] if (inp.logit_bias is not None and wl.mode == 0) else 0)
+    ids_i, w_i = oracle_route_from_logits(l_in, wl, sb)
+    assert np.array_equal(g_ids, ids_i), "topk_ids differ from the oracle's top-k of the GPU logits"
+    assert np.abs(g_w - w_i).max() <= TOPK_W_RTOL * max(1.0, np.abs(w_i).max())
+    # (ii) the oracle's own float64 routing
+    l_ref = oracle_logits(inp)
+    assert np.abs(l_in - l_ref).max() <= 1e-4 * max(1.0, np.abs(l_ref).max())
+    ids_o, w_o = oracle_route_from_logits(l_ref, wl, sb)
+    assert np.array_equal(g_ids, ids_o), "topk_ids differ from the oracle's float64 routing"
+    # align
+    B, mp = mids["block_m"], mids["max_padded"]
+    sid, eid, total, counts = O.moe_align(ids_o, B, wl.E, max_padded=mp)
+    assert int(mids["num_post_padded"].item()) == total
+    assert np.array_equal(to_np(mids["counts"]), counts)
+    assert np.array_equal(to_np(mids["sorted_ids"]), sid)
+    assert np.array_equal(to_np(mids["expert_ids"]), eid)
+    return ids_o, w_o
+
+
+def _oracle_out(inp, ids, w, tokens=None):
+    return O.moe_loop(to_np(inp.x), ids, w, weights_for_oracle(inp.W13),
+                      weights_for_oracle(inp.W2), tokens=tokens)
+
+
+# --------------------------------------------------------------------- page examples (fp32)
+
+def test_page_tiny_layer_f32(L):
+    x, wg, w1, w3, w2 = mi.page_tiny_layer()
+    inp = _to_dev(mi.LayerInputs(mi.TINY_F32, x, wg, torch.cat([w1, w3], 1), w2))
+    layer = _layer(L, inp)
+    out = layer(inp.x)
+    torch.cuda.synchronize()
+    mids = layer.intermediates(64)
+    assert to_np(mids["counts"]).tolist() == [19, 11, 15, 15, 21, 15, 18, 14]
+    ids, w = _check_routing_and_align(inp, mids)
+    assert_close(to_np(out), _oracle_out(inp, ids, w), "f32")
+
+
+@pytest.mark.parametrize("case", mi.PAGE_FUSED_CASES, ids=[c[0] for c in mi.PAGE_FUSED_CASES])
+def test_page_fused_cases_f32(L, golden_dir, case):
+    import json, os
+    g = {c["name"]: c for c in json.load(open(os.path.join(golden_dir, "fused_cases.json")))["cases"]}
+    name, T, E, k, bias = case
+    x, wg, w1, w3, w2 = mi.page_fused_case(T, E, bias)
+    wl = mi.Workload(name, T=T, H=64, I=96, E=E, k=k, dtype="f32")
+    inp = _to_dev(mi.LayerInputs(wl, x, wg, torch.cat([w1, w3], 1), w2))
+    layer = _layer(L, inp)
+    out = layer(inp.x)
+    torch.cuda.synchronize()
+    mids = layer.intermediates(T)
+    assert to_np(mids["counts"]).tolist() == g[name]["loads"]
+    assert int(mids["num_post_padded"].item()) == g[name]["padded"]
+    ids, w = _check_routing_and_align(inp, mids)
+    assert_close(to_np(out), _oracle_out(inp, ids, w), "f32")
+
+
+def test_page_deepseek_router(L, golden_dir):
+    """The §4 toy router through the GPU top-k: x = logits, Wg = identity (fp32, exact)."""
+    import json, os
+    g = json.load(open(os.path.join(golden_dir, "deepseek_toy_router.json")))
+    logits, bias = mi.page_deepseek_toy()
+    x = logits.to(DEV).contiguous()
+    Wg = torch.eye(16, device=DEV)
+    for b, key in ((torch.zeros(16), "ids_no_bias"), (bias, "ids_with_bias")):
+        bd = b.to(DEV)
+        cfg = L.make_config(4, 16, 8, 16, 4, L.MOE_F32, L.MOE_ROUTE_SIGMOID_GROUPED, True, 2.5,
+                            4, 2, None, bd)
+        lg = torch.empty(4, 16, device=DEV)
+        ids = torch.empty(4, 4, dtype=torch.int32, device=DEV)
+        w = torch.empty(4, 4, device=DEV)
+        L.moe_route(cfg, x, Wg, lg, ids, w)
+        torch.cuda.synchronize()
+        assert torch.equal(lg, x)
+        assert ids.cpu().tolist() == g[key]
+        if key == "ids_with_bias":
+            assert np.abs(to_np(w) - np.array(g["weights_right_3dp"])).max() <= 5e-4 + 1e-6
+            _, w_ref = O.route_sigmoid_grouped(to_np(logits), 4, 4, 2, to_np(bias), 2.5)
+            assert np.abs(to_np(w) - w_ref).max() <= 1e-6
+
+
+# --------------------------------------------------------------------- align
+
+ALIGN_CASES = [
+    # T, k, E, B, skew  (T*k <= 4096: one-CTA kernel; larger: three-kernel path)
+    (4, 3, 5, 4, 0.0), (64, 2, 8, 16, 0.0), (1, 4, 128, 128, 0.0), (37, 1, 8, 16, 0.0),
+    (512, 8, 128, 128, 1.2), (4096, 1, 512, 64, 0.5), (8192, 8, 128, 128, 0.0),
+    (4096, 8, 256, 128, 1.0), (3000, 7, 300, 1, 0.7), (20000, 2, 8, 128, 2.0),
+    (2048, 8, 64, 16, 3.0), (100000, 1, 3, 128, 0.0),
+]
+
+
+@pytest.mark.parametrize("T,k,E,B,skew", ALIGN_CASES)
+def test_align_bit_exact(L, T, k, E, B, skew):
+    ids = mi.random_topk_ids(T, k, E, seed=T * 31 + E, skew=skew)
+    mp = L.moe_max_padded_rows(T, k, E, B)
+    sid = torch.full((mp,), -7, dtype=torch.int32, device=DEV)
+    eid = torch.full((mp // B,), -7, dtype=torch.int32, device=DEV)
+    npp = torch.zeros(1, dtype=torch.int32, device=DEV)
+    cnt = torch.zeros(E, dtype=torch.int32, device=DEV)
+    wsb = L.moe_align_workspace_size(T, k, E, B)
+    ws = torch.empty(max(wsb, 1), dtype=torch.uint8, device=DEV)
+    L.moe_align(ids.to(DEV), T, k, E, B, sid, eid, npp, cnt, ws, wsb)
+    torch.cuda.synchronize()
+    r_sid, r_eid, r_total, r_cnt = O.moe_align(ids.numpy(), B, E, max_padded=mp)
+    assert int(npp.item()) == r_total
+    assert np.array_equal(cnt.cpu().numpy(), r_cnt)
+    assert np.array_equal(sid.cpu().numpy(), r_sid)
+    assert np.array_equal(eid.cpu().numpy(), r_eid)
+
+
+def test_align_page_example(L, golden_dir):
+    import json, os
+    g = json.load(open(os.path.join(golden_dir, "align_example.json")))
+    ids = torch.tensor(g["topk_ids"], dtype=torch.int32, device=DEV)
+    sid = torch.empty(16, dtype=torch.int32, device=DEV)
+    eid = torch.empty(4, dtype=torch.int32, device=DEV)
+    npp = torch.empty(1, dtype=torch.int32, device=DEV)
+    mp = L.moe_max_padded_rows(4, 3, 5, 4)
+    sid = torch.empty(mp, dtype=torch.int32, device=DEV)
+    eid = torch.empty(mp // 4, dtype=torch.int32, device=DEV)
+    L.moe_align(ids, 4, 3, 5, 4, sid, eid, npp)
+    torch.cuda.synchronize()
+    assert int(npp.item()) == g["total"]
+    assert sid[:16].cpu().tolist() == g["sorted_ids"]
+    assert eid[:4].cpu().tolist() == g["expert_ids"]
+
+
+def test_align_bad_expert_id_is_skipped_and_flagged(L):
+    ids = torch.tensor([[0, 1], [2, 9], [1, 0]], dtype=torch.int32, device=DEV)  # 9 >= E=4
+    mp = L.moe_max_padded_rows(3, 2, 4, 4)
+    sid = torch.empty(mp, dtype=torch.int32, device=DEV)
+    eid = torch.empty(mp // 4, dtype=torch.int32, device=DEV)
+    npp = torch.empty(1, dtype=torch.int32, device=DEV)
+    L.moe_device_status(True)
+    L.moe_align(ids, 3, 2, 4, 4, sid, eid, npp)
+    torch.cuda.synchronize()
+    assert L.moe_device_status(True) == 1
+    s = sid.cpu().numpy()
+    assert 3 not in s.tolist()          # the bad row is never scattered
+    assert sorted(x for x in s.tolist() if x < 6) == [0, 1, 2, 4, 5]
+
+
+# --------------------------------------------------------------------- router
+
+ROUTE_CASES = [
+    # name, T, H, E, k, dtype, mode, renorm, scale, G, tg, logit_bias_std, select_bias_std
+    ("softmax-E8", 300, 256, 8, 2, "bf16", 0, True, 1.0, 1, 1, 0.0, 0.0),
+    ("softmax-E128-offset", 500, 512, 128, 8, "bf16", 0, True, 1.0, 1, 1, 1.5, 0.0),
+    ("softmax-norenorm", 200, 128, 32, 4, "bf16", 0, False, 1.0, 1, 1, 0.0, 0.0),
+    ("grouped-E256", 300, 512, 256, 8, "bf16", 1, True, 2.5, 8, 4, 0.0, 0.05),
+    ("grouped-E64-noscale", 129, 256, 64, 6, "bf16", 1, True, 1.0, 8, 3, 0.0, 0.1),
+    ("softmax-E512-simt", 77, 128, 512, 4, "bf16", 0, True, 1.0, 1, 1, 0.0, 0.0),
+    ("softmax-E40-f32", 90, 64, 40, 3, "f32", 0, True, 1.0, 1, 1, 0.0, 0.0),
+    ("grouped-E16-f32", 60, 64, 16, 4, "f32", 1, True, 2.5, 4, 2, 0.0, 0.5),
+]
+
+
+@pytest.mark.parametrize("case", ROUTE_CASES, ids=[c[0] for c in ROUTE_CASES])
+def test_route_parity(L, case):
+    name, T, H, E, k, dt, mode, renorm, scale, G, tg, lbs, sbs = case
+    wl = mi.Workload(name, T=T, H=H, I=8, E=E, k=k, dtype=dt, mode=mode, renormalize=renorm,
+                     scale=scale, n_group=G, topk_group=tg, logit_bias_std=lbs,
+                     select_bias_std=sbs, seed=zlib.crc32(name.encode()) % 1000)
+    inp = mi.make_layer(wl, "cpu")
+    enforce_margins(inp)
+    inp = _to_dev(inp)
+    cfg = L.make_config(T, H, 8, E, k, L.MOE_BF16 if dt == "bf16" else L.MOE_F32, mode, renorm,
+                        scale, G, tg, inp.logit_bias, inp.select_bias)
+    lg = torch.empty(T, E, device=DEV)
+    ids = torch.empty(T, k, dtype=torch.int32, device=DEV)
+    w = torch.empty(T, k, device=DEV)
+    L.moe_route(cfg, inp.x, inp.Wg, lg, ids, w)
+    torch.cuda.synchronize()
+    mids = {"logits": lg, "topk_ids": ids, "topk_w": w}
+    sb = to_np(inp.select_bias) if inp.select_bias is not None else None
+    l_in = to_np(lg) + (to_np(inp.logit_bias)[None] if inp.logit_bias is not None else 0)
+    ids_i, w_i = oracle_route_from_logits(l_in, wl, sb)
+    assert np.array_equal(to_np(ids), ids_i)
+    assert np.abs(to_np(w) - w_i).max() <= TOPK_W_RTOL * max(1.0, np.abs(w_i).max())
+    l_ref = oracle_logits(inp)
+    assert np.abs(l_in - l_ref).max() <= 1e-4 * max(1.0, np.abs(l_ref).max())
+    ids_o, _ = oracle_route_from_logits(l_ref, wl, sb)
+    assert np.array_equal(to_np(mids["topk_ids"]), ids_o)
+
+
+@pytest.mark.parametrize("mode", [0, 1])
+def test_route_exact_ties_go_to_lower_ids(L, mode):
+    T, H, E, k = 5, 64, 32, 4
+    x = torch.zeros(T, H, device=DEV, dtype=torch.bfloat16)
+    Wg = torch.randn(E, H, device=DEV).to(torch.bfloat16)
+    cfg = L.make_config(T, H, 8, E, k, L.MOE_BF16, mode, True, 1.0, 4 if mode else 1,
+                        2 if mode else 1)
+    lg = torch.empty(T, E, device=DEV)
+    ids = torch.empty(T, k, dtype=torch.int32, device=DEV)
+    w = torch.empty(T, k, device=DEV)
+    L.moe_route(cfg, x, Wg, lg, ids, w)
+    torch.cuda.synchronize()
+    assert ids.cpu().tolist() == [[0, 1, 2, 3]] * T
+    assert torch.allclose(w.cpu(), torch.full((T, k), 0.25))
+
+
+# --------------------------------------------------------------------- whole layer, bf16
+
+LAYER_CASES = [
+    mi.Workload("bf16-basic", T=200, H=256, I=384, E=8, k=2, dtype="bf16", seed=11),
+    mi.Workload("bf16-ragged", T=300, H=320, I=320, E=16, k=4, dtype="bf16", seed=12),
+    mi.Workload("bf16-decode-T1", T=1, H=2880, I=2880, E=128, k=4, dtype="bf16", seed=13),
+    mi.Workload("bf16-grouped", T=256, H=512, I=256, E=64, k=8, dtype="bf16",
+                mode=mi.ROUTE_SIGMOID_GROUPED, scale=2.5, n_group=8, topk_group=4,
+                select_bias_std=0.05, seed=14),
+    mi.Workload("bf16-skewed", T=600, H=256, I=256, E=32, k=4, dtype="bf16",
+                logit_bias_std=1.5, seed=15),
+    mi.Workload("bf16-top1", T=37, H=128, I=192, E=8, k=1, dtype="bf16", seed=16),
+    mi.Workload("f32-ragged", T=100, H=72, I=88, E=6, k=3, dtype="f32", seed=17),
+]
+
+
+@pytest.mark.parametrize("wl", LAYER_CASES, ids=[w.name for w in LAYER_CASES])
+def test_layer_parity(L, wl):
+    inp = mi.make_layer(wl, "cpu")
+    enforce_margins(inp)
+    inp = _to_dev(inp)
+    layer = _layer(L, inp)
+    out = layer(inp.x)
+    torch.cuda.synchronize()
+    mids = layer.intermediates(wl.T)
+    ids, w = _check_routing_and_align(inp, mids)
+    ref = _oracle_out(inp, ids, w)
+    assert_close(to_np(out), ref, wl.dtype)
+    # y rows: y[r] = w[r] * expert(x[r // k])
+    y = to_np(mids["y"])
+    n = wl.T * wl.k
+    yref = np.zeros_like(y)
+    W13, W2 = weights_for_oracle(inp.W13), weights_for_oracle(inp.W2)
+    xs = to_np(inp.x)
+    for e in np.unique(ids):
+        rows = np.nonzero(ids.reshape(-1) == e)[0]
+        yref[rows] = O.expert_ffn(xs[rows // wl.k], O._expert(W13, e), O._expert(W2, e)) * \
+            w.reshape(-1)[rows][:, None]
+    assert_close(y[:n], yref, wl.dtype, "y")
+
+
+def test_separate_entry_points_match_forward(L):
+    wl = LAYER_CASES[1]
+    inp = _to_dev(mi.make_layer(wl, "cpu"))
+    layer = _layer(L, inp)
+    out_fwd = layer(inp.x).clone()
+    T, k, E, H, I = wl.T, wl.k, wl.E, wl.H, wl.I
+    cfg = layer.config(T)
+    B = L.moe_block_m(cfg)
+    mp = L.moe_max_padded_rows(T, k, E, B)
+    lg = torch.empty(T, E, device=DEV)
+    ids = torch.empty(T, k, dtype=torch.int32, device=DEV)
+    w = torch.empty(T, k, device=DEV)
+    sid = torch.empty(mp, dtype=torch.int32, device=DEV)
+    eid = torch.empty(mp // B, dtype=torch.int32, device=DEV)
+    npp = torch.empty(1, dtype=torch.int32, device=DEV)
+    act = torch.empty(mp, I, dtype=torch.bfloat16, device=DEV)
+    y = torch.empty(T * k, H, dtype=torch.bfloat16, device=DEV)
+    out = torch.empty(T, H, dtype=torch.bfloat16, device=DEV)
+    L.moe_route(cfg, inp.x, inp.Wg, lg, ids, w)
+    L.moe_align(ids, T, k, E, B, sid, eid, npp)
+    L.moe_expert_gemm1(cfg, inp.x, inp.W13, sid, eid, npp, B, act)
+    L.moe_expert_gemm2(cfg, act, inp.W2, sid, eid, npp, B, w, y)
+    L.moe_combine(y, T, k, H, L.MOE_BF16, out)
+    torch.cuda.synchronize()
+    assert torch.equal(out, out_fwd)
+    ws = torch.empty(mp * I * 2, dtype=torch.uint8, device=DEV)
+    y2 = torch.empty_like(y)
+    L.moe_grouped_swiglu(cfg, inp.x, inp.W13, inp.W2, sid, eid, npp, B, w, y2, ws, ws.numel())
+    torch.cuda.synchronize()
+    assert torch.equal(y2, y)
+
+
+@pytest.mark.parametrize("dtype", ["bf16", "f32"])
+def test_tile_boundaries_and_sentinels(L, dtype):
+    """Experts with 0, 1, B-1, B, B+1, 2B-1, 2B, 2B+1 rows; padding rows of act are never
+    written (canary survives); every row of y is written (canary gone)."""
+    tdt = torch.bfloat16 if dtype == "bf16" else torch.float32
+    B = 128 if dtype == "bf16" else 16
+    loads = [0, 1, B - 1, B, B + 1, 2 * B - 1, 2 * B, 2 * B + 1]
+    E, k = len(loads), 1
+    T = sum(loads)
+    H, I = 256, 192
+    g = torch.Generator().manual_seed(5)
+    ids = torch.tensor([e for e, c in enumerate(loads) for _ in range(c)], dtype=torch.int32)
+    ids = ids[torch.randperm(T, generator=g)].view(T, 1)
+    w = torch.rand(T, 1, generator=g) + 0.5
+    x = torch.randn(T, H, generator=g).to(tdt)
+    W13 = (torch.randn(E, 2 * I, H, generator=g) / H ** 0.5).to(tdt)
+    W2 = (torch.randn(E, H, I, generator=g) / I ** 0.5).to(tdt)
+    xd, W13d, W2d, idsd, wd = (t.to(DEV) for t in (x, W13, W2, ids, w))
+    cfg = L.make_config(T, H, I, E, k, L.MOE_BF16 if dtype == "bf16" else L.MOE_F32)
+    mp = L.moe_max_padded_rows(T, k, E, B)
+    sid = torch.empty(mp, dtype=torch.int32, device=DEV)
+    eid = torch.empty(mp // B, dtype=torch.int32, device=DEV)
+    npp = torch.empty(1, dtype=torch.int32, device=DEV)
+    act = torch.full((mp, I), float("nan"), dtype=tdt, device=DEV)
+    y = torch.full((T * k, H), float("nan"), dtype=tdt, device=DEV)
+    out = torch.empty(T, H, dtype=tdt, device=DEV)
+    L.moe_align(idsd, T, k, E, B, sid, eid, npp)
+    L.moe_expert_gemm1(cfg, xd, W13d, sid, eid, npp, B, act)
+    L.moe_expert_gemm2(cfg, act, W2d, sid, eid, npp, B, wd, y)
+    L.moe_combine(y, T, k, H, cfg.dtype, out)
+    torch.cuda.synchronize()
+    s = sid.cpu().numpy()
+    total = int(npp.item())
+    valid = s < T * k
+    a = act.float().cpu().numpy()
+    assert np.all(np.isfinite(a[valid])), "a real row of act was not written"
+    assert np.all(np.isnan(a[~valid])), "a padding row of act was written"
+    assert np.all(np.isfinite(y.float().cpu().numpy())), "a row of y was not written"
+    assert total == sum((c + B - 1) // B * B for c in loads)
+    ref = O.moe_loop(to_np(x), ids.numpy(), to_np(w), weights_for_oracle(W13), weights_for_oracle(W2))
+    assert_close(to_np(out), ref, dtype)
+
+
+def test_all_tokens_to_one_expert(L):
+    T, H, I, E, k = 700, 256, 256, 16, 2
+    g = torch.Generator().manual_seed(9)
+    ids = torch.stack([torch.full((T,), 3), torch.randint(4, E, (T,), generator=g)], 1).int()
+    w = torch.rand(T, k, generator=g)
+    x = torch.randn(T, H, generator=g).bfloat16()
+    W13 = (torch.randn(E, 2 * I, H, generator=g) / H ** 0.5).bfloat16()
+    W2 = (torch.randn(E, H, I, generator=g) / I ** 0.5).bfloat16()
+    cfg = L.make_config(T, H, I, E, k, L.MOE_BF16)
+    B = 128
+    mp = L.moe_max_padded_rows(T, k, E, B)
+    sid = torch.empty(mp, dtype=torch.int32, device=DEV)
+    eid = torch.empty(mp // B, dtype=torch.int32, device=DEV)
+    npp = torch.empty(1, dtype=torch.int32, device=DEV)
+    y = torch.empty(T * k, H, dtype=torch.bfloat16, device=DEV)
+    out = torch.empty(T, H, dtype=torch.bfloat16, device=DEV)
+    ws = torch.empty(mp * I * 2, dtype=torch.uint8, device=DEV)
+    xd, W13d, W2d = x.to(DEV), W13.to(DEV), W2.to(DEV)
+    L.moe_align(ids.to(DEV), T, k, E, B, sid, eid, npp)
+    L.moe_grouped_swiglu(cfg, xd, W13d, W2d, sid, eid, npp, B, w.to(DEV), y, ws, ws.numel())
+    L.moe_combine(y, T, k, H, L.MOE_BF16, out)
+    torch.cuda.synchronize()
+    ref = O.moe_loop(to_np(x), ids.numpy(), to_np(w), weights_for_oracle(W13), weights_for_oracle(W2))
+    assert_close(to_np(out), ref, "bf16")
+
+
+def test_cuda_graph_capture_and_replay(L):
+    wl = mi.Workload("graph", T=256, H=256, I=256, E=16, k=4, dtype="bf16", seed=21)
+    inp = _to_dev(mi.make_layer(wl, "cpu"))
+    layer = _layer(L, inp)
+    x_static = inp.x.clone()
+    out_static = torch.empty_like(x_static)
+    layer(x_static, out_static)          # first call sets up the workspace / kernels
+    torch.cuda.synchronize()
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.stream(s):
+        with torch.cuda.graph(graph, stream=s):
+            layer(x_static, out_static)
+    torch.cuda.current_stream().wait_stream(s)
+    for seed in (1, 2):
+        xn = torch.randn(wl.T, wl.H, generator=torch.Generator().manual_seed(seed)).bfloat16()
+        x_static.copy_(xn.to(DEV))
+        graph.replay()
+        torch.cuda.synchronize()
+        eager = layer(x_static.clone())
+        torch.cuda.synchronize()
+        assert torch.equal(out_static, eager)
