@@ -1,0 +1,400 @@
+"""Benchmark of the fused MoE layer (one step = route -> align -> GEMM1+SwiGLU -> GEMM2 ->
+combine over one batch of T tokens).
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl ours|reference]
+
+Prints ONE JSON line. ``value`` is the layer's useful throughput, 6*T*k*H*I FLOPs per step
+(padding and router excluded) over the device-timed step, summed over ranks; ``e2e`` is the
+same metric through the public API (MoELayer -> moe_forward) with the tokens copied in from
+pinned host memory and the output read back inside the timed region. Under torchrun each
+rank runs its own replica of the layer on its own tokens (weak scaling, no data-path
+collective); the timing takes the max over ranks.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import re
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import moe_inputs as mi  # noqa: E402
+
+METRIC = "MoE layer TFLOPS (6*T*k*H*I/s) & % BF16 peak; decode weight GB/s vs HBM"
+DEFAULT_WORKLOAD = "mixtral-prefill"
+
+
+def parse():
+    p = argparse.ArgumentParser()
+    p.add_argument("--gpus", type=int, default=1)
+    p.add_argument("--steps", type=int, default=100)
+    p.add_argument("--warmup", type=int, default=10)
+    p.add_argument("--workload", default=DEFAULT_WORKLOAD,
+                   help="mixtral-prefill | qwen3-skewed | deepseek-v3 | gpt-oss-decode@T=<n>")
+    p.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    p.add_argument("--no-cpu-baseline", action="store_true")
+    p.add_argument("--cpu-sample-tokens", type=int, default=0)
+    return p.parse_args()
+
+
+def workload(name: str) -> mi.Workload:
+    if name.startswith("gpt-oss-decode@T="):
+        return mi.GPTOSS.with_T(int(name.split("=")[1]))
+    return mi.WORKLOADS[name]
+
+
+def is_decode(wl):
+    return wl.name.startswith("gpt-oss-decode")
+
+
+def peaks():
+    """(HBM GB/s, bf16 burst TF/s, bf16 sustained TF/s, source)."""
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            d = json.load(f)
+        return d["hbm_gbs"], d["bf16_tflops"], d["bf16_tflops_sustained"], "measured"
+    except Exception:
+        return 6800.0, 1900.0, 1700.0, "fallback"
+
+
+def profile_traffic(kernel: str, wl_name: str, src_path: str):
+    """DRAM bytes per launch recorded in a committed ncu summary, if the kernel source it
+    was taken on is unchanged (the summary stores the source's sha256); else None."""
+    path = os.path.join(ROOT, "profiles", f"{kernel}_{wl_name.split('@')[0]}.md")
+    if not os.path.exists(path):
+        return None
+    txt = open(path).read()
+    m = re.search(r"traffic_bytes_per_launch:\s*([0-9.eE+]+)", txt)
+    h = re.search(r"source_sha256:\s*([0-9a-f]{64})", txt)
+    if not m or not h:
+        return None
+    cur = hashlib.sha256(open(src_path, "rb").read()).hexdigest()
+    return float(m.group(1)) if cur == h.group(1) else None
+
+
+class ClockSampler:
+    """nvidia-smi sampled every 100 ms while the timed region runs."""
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index):
+        self.index = index
+        self.p = None
+
+    def start(self):
+        try:
+            self.p = subprocess.Popen(["nvidia-smi", f"--id={self.index}", f"--query-gpu={self.Q}",
+                                       "--format=csv,noheader,nounits", "-lms", "100"],
+                                      stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except Exception:
+            self.p = None
+
+    def stop(self):
+        if self.p is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.p.terminate()
+        out, _ = self.p.communicate(timeout=10)
+        sm, mx, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in out.strip().splitlines():
+            f = [x.strip() for x in line.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                mx = float(f[2])
+            except ValueError:
+                continue
+            for n, v in zip(names, f[5:9]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": mx,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+def dist_setup(n_gpus):
+    import torch
+    if n_gpus > 1 or int(os.environ.get("WORLD_SIZE", "1")) > 1:
+        import torch.distributed as dist
+        local = int(os.environ.get("LOCAL_RANK", "0"))
+        if torch.cuda.is_available():
+            torch.cuda.set_device(local)
+        dist.init_process_group("nccl" if torch.cuda.is_available() else "gloo")
+        return dist, dist.get_rank(), dist.get_world_size(), local
+    return None, 0, 1, 0
+
+
+def max_over_ranks(dist, v: float, device) -> float:
+    if dist is None:
+        return v
+    import torch
+    t = torch.tensor([v], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+# ------------------------------------------------------------------------------ CPU oracle
+
+def time_oracle(wl, x, Wg, W13, W2, lb, sb, n_tokens):
+    """The float64 oracle (route + per-expert loop), as it stands, on the first ``n_tokens``
+    tokens of the same layer. Returns (seconds, tokens, threads)."""
+    import numpy as np
+    import oracle as O
+    xs = x[:n_tokens]
+    t0 = time.perf_counter()
+    logits = O.router_logits(xs, Wg, lb if wl.mode == 0 else None)
+    ids, w = O.route(logits, wl.k, wl.mode, wl.renormalize, wl.scale, wl.n_group,
+                     wl.topk_group, sb)
+    out = O.moe_loop(xs, ids, w, W13, W2)
+    dt = time.perf_counter() - t0
+    assert np.isfinite(out).all()
+    threads = len(os.sched_getaffinity(0)) if hasattr(os, "sched_getaffinity") else os.cpu_count()
+    return dt, xs.shape[0], threads
+
+
+def host_copies(inp):
+    """Host copies for the oracle: fp64 tokens/router, raw bf16 bits of the expert weights."""
+    import numpy as np
+    import torch
+
+    def bits(t):
+        if t.dtype != torch.bfloat16:
+            return t.detach().double().cpu().numpy()
+        return t.detach().cpu().contiguous().view(torch.int16).numpy().view(np.uint16)
+
+    def f64(t):
+        return t.detach().float().cpu().double().numpy()
+    lb = f64(inp.logit_bias) if inp.logit_bias is not None else None
+    sb = f64(inp.select_bias) if inp.select_bias is not None else None
+    return f64(inp.x), f64(inp.Wg), bits(inp.W13), bits(inp.W2), lb, sb
+
+
+def default_sample(wl):
+    """Tokens per oracle pass: about 10-20 s on a 16-core host (the per-expert bf16 -> fp64
+    weight conversion dominates)."""
+    return {"mixtral-prefill": 256, "qwen3-skewed": 96,
+            "deepseek-v3": 24}.get(wl.name.split("@")[0], wl.T)
+
+
+# ------------------------------------------------------------------------------ arms
+
+def run_reference(args, wl):
+    """Reference arm: the float64 CPU oracle on the host cores, rank 0 only."""
+    import torch
+    dist, rank, world, local = dist_setup(args.gpus)
+    if rank != 0:
+        if dist is not None:
+            dist.destroy_process_group()
+        return
+    dev = "cuda" if torch.cuda.is_available() else "cpu"
+    inp = mi.make_layer(wl, dev, seed=wl.seed)
+    x, Wg, W13, W2, lb, sb = host_copies(inp)
+    del inp
+    n = args.cpu_sample_tokens or default_sample(wl)
+    for _ in range(max(0, args.warmup)):
+        time_oracle(wl, x, Wg, W13, W2, lb, sb, min(n, 2))
+    secs, threads = 0.0, 1
+    for _ in range(args.steps):
+        dt, n, threads = time_oracle(wl, x, Wg, W13, W2, lb, sb, n)
+        secs += dt
+    flops = 6 * n * wl.k * wl.H * wl.I
+    val = flops * args.steps / secs / 1e12
+    line = {"metric": METRIC, "value": val, "unit": "TFLOPS", "n_gpus": args.gpus,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": secs / args.steps * 1e3,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic", "impl": "reference",
+            "config": {"workload": wl.name, "T": wl.T, "H": wl.H, "I": wl.I, "E": wl.E, "k": wl.k},
+            "cpu_baseline": {"value": val, "unit": "TFLOPS", "cores": threads, "kind": "oracle",
+                             "sample": f"first {n} of {wl.T} tokens per step, float64 oracle "
+                                       "(router + per-expert loop)"},
+            "e2e": {"value": val, "unit": "TFLOPS", "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+    if dist is not None:
+        dist.destroy_process_group()
+
+
+def run_ours(args, wl):
+    import torch
+    dist, rank, world, local = dist_setup(args.gpus)
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    from routing_grouped_gemm_router_gb300 import _lib as L  # fails loudly if not built
+    from routing_grouped_gemm_router_gb300.layer import MoELayer
+
+    inp = mi.make_layer(wl, dev, seed=wl.seed + 1000 * rank)
+    layer = MoELayer(inp.Wg, inp.W13, inp.W2, wl.k, wl.mode, wl.renormalize, wl.scale,
+                     wl.n_group, wl.topk_group, inp.logit_bias, inp.select_bias)
+    T, k, E, H, I = wl.T, wl.k, wl.E, wl.H, wl.I
+    cfg = layer.config(T)
+    ws, lay = layer.workspace(T)
+    B = lay.block_m
+    base = ws.data_ptr()
+    p = {n: base + getattr(lay, n) for n in ("logits", "topk_ids", "topk_w", "sorted_ids",
+                                               "expert_ids", "num_post_padded", "counts",
+                                               "align_scratch", "act", "y")}
+    ws_align = lay.act - lay.align_scratch
+    out = torch.empty(T, H, dtype=inp.x.dtype, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    sh = stream.cuda_stream
+
+    def step(ev=None):
+        # The same kernels moe_forward enqueues, called stage by stage so that CUDA events
+        # between them give each stage's device time.
+        if ev is not None:
+            ev[0].record(stream)
+        L.moe_route(cfg, inp.x, inp.Wg, p["logits"], p["topk_ids"], p["topk_w"], sh)
+        if ev is not None:
+            ev[1].record(stream)
+        L.moe_align(p["topk_ids"], T, k, E, B, p["sorted_ids"], p["expert_ids"],
+                    p["num_post_padded"], p["counts"], p["align_scratch"], ws_align, sh)
+        if ev is not None:
+            ev[2].record(stream)
+        L.moe_expert_gemm1(cfg, inp.x, inp.W13, p["sorted_ids"], p["expert_ids"],
+                           p["num_post_padded"], B, p["act"], sh)
+        if ev is not None:
+            ev[3].record(stream)
+        L.moe_expert_gemm2(cfg, p["act"], inp.W2, p["sorted_ids"], p["expert_ids"],
+                           p["num_post_padded"], B, p["topk_w"], p["y"], sh)
+        if ev is not None:
+            ev[4].record(stream)
+        L.moe_combine(p["y"], T, k, H, cfg.dtype, out, sh)
+        if ev is not None:
+            ev[5].record(stream)
+
+    # router GEMM + top-k, align (one kernel up to 4096 rows, else three), GEMM1, GEMM2, combine
+    launches_per_step = 2 + (1 if T * k <= 4096 else 3) + 2 + 1
+
+    for _ in range(max(3, args.warmup)):
+        step()
+    torch.cuda.synchronize()
+    npp = int(ws[lay.num_post_padded:lay.num_post_padded + 4].view(torch.int32).item())
+    counts = ws[lay.counts:lay.counts + 4 * E].view(torch.int32).cpu()
+    active = int((counts > 0).sum())
+
+    # ---- device-timed steps (inputs resident in HBM; expert weights larger than L2)
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(6)] for _ in range(args.steps)]
+    sampler = ClockSampler(local)
+    sampler.start()
+    time.sleep(0.3)
+    if dist is not None:
+        dist.barrier()
+    torch.cuda.synchronize()
+    t_start = torch.cuda.Event(enable_timing=True)
+    t_end = torch.cuda.Event(enable_timing=True)
+    t_start.record(stream)
+    for i in range(args.steps):
+        step(evs[i])
+    t_end.record(stream)
+    torch.cuda.synchronize()
+    if dist is not None:
+        dist.barrier()
+    clocks = sampler.stop()
+    ms = max_over_ranks(dist, t_start.elapsed_time(t_end) / args.steps, dev)
+    stage = {n: statistics.mean(e[i].elapsed_time(e[i + 1]) for e in evs)
+             for i, n in enumerate(("route", "align", "gemm1", "gemm2", "combine"))}
+
+    # ---- end to end through the public API: H2D of x, moe_forward, D2H of out
+    x_host = inp.x.cpu().pin_memory()
+    out_host = torch.empty(T, H, dtype=inp.x.dtype).pin_memory()
+    x_dev = torch.empty_like(inp.x)
+    for _ in range(3):
+        x_dev.copy_(x_host, non_blocking=True)
+        layer(x_dev, out)
+        out_host.copy_(out, non_blocking=True)
+    torch.cuda.synchronize()
+    if dist is not None:
+        dist.barrier()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(args.steps):
+        x_dev.copy_(x_host, non_blocking=True)
+        layer(x_dev, out)
+        out_host.copy_(out, non_blocking=True)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = max_over_ranks(dist, e0.elapsed_time(e1) / args.steps, dev)
+    bytes_io = T * H * inp.x.element_size()
+
+    flops = wl.flops
+    value = flops * world / (ms * 1e-3) / 1e12
+    e2e_val = flops * world / (e2e_ms * 1e-3) / 1e12
+    hbm, bf16_burst, bf16_sus, peak_src = peaks()
+    src = os.path.join(ROOT, "routing_grouped_gemm_router_gb300", "csrc", "gemm_tc.cu")
+    if is_decode(wl):
+        # decode is HBM-bound: GEMM1 streams the gate/up weights of every active expert
+        w_bytes = active * 2 * H * I * 2
+        roof = {"bound": "hbm", "achieved": w_bytes / (stage["gemm1"] * 1e-3) / 1e9,
+                "peak": hbm, "unit": "GB/s", "kernel": "gemm1 (gate/up grouped GEMM)",
+                "algorithmic_bytes_per_launch": w_bytes,
+                "peak_kind": f"{peak_src} HBM copy bandwidth"}
+    else:
+        g1_flops = 4 * T * k * H * I
+        roof = {"bound": "tensor", "achieved": g1_flops / (stage["gemm1"] * 1e-3) / 1e12,
+                "peak": bf16_sus, "unit": "TFLOP/s",
+                "kernel": "gemm1 (gate/up grouped GEMM + SwiGLU)",
+                "algorithmic_flops_per_launch": g1_flops,
+                "peak_kind": f"{peak_src} bf16 sustained (kernel timed inside a long step loop)"}
+    roof["frac"] = roof["achieved"] / roof["peak"]
+    roof["traffic"] = profile_traffic("gemm1", wl.name, src)
+
+    line = {"metric": METRIC, "value": value, "unit": "TFLOPS", "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+            "dtype": "bf16" if wl.dtype == "bf16" else "f32",
+            "data": "synthetic (seeded N(0,1) tokens, N(0,1/fan_in) weights, random init)",
+            "config": {"workload": wl.name, "T": T, "H": H, "I": I, "E": E, "k": k,
+                       "mode": "sigmoid-grouped" if wl.mode else "softmax",
+                       "global_batch": T * world, "parallelism": f"replicas x{world}",
+                       "l2": "inputs larger than L2 (expert weights "
+                             f"{E * 3 * H * I * inp.x.element_size() / 1e9:.2f} GB)",
+                       "block_m": B, "num_post_padded": npp, "active_experts": active},
+            "stages_ms": {n: round(v, 5) for n, v in stage.items()},
+            "roofline": roof,
+            "e2e": {"value": e2e_val, "unit": "TFLOPS", "h2d_bytes_per_step": bytes_io,
+                    "d2h_bytes_per_step": bytes_io, "ms_per_step": e2e_ms},
+            "gpu_launches": launches_per_step * args.steps,
+            "clocks": clocks}
+    if is_decode(wl):
+        line["weight_gbs"] = active * 3 * H * I * 2 / (ms * 1e-3) / 1e9
+        line["weight_gbs_frac_of_hbm"] = line["weight_gbs"] / hbm
+    else:
+        line["frac_of_bf16_peak"] = value / bf16_sus
+
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        del layer
+        x, Wg, W13, W2, lb, sb = host_copies(inp)
+        n = args.cpu_sample_tokens or default_sample(wl)
+        dt, n, threads = time_oracle(wl, x, Wg, W13, W2, lb, sb, n)
+        line["cpu_baseline"] = {"value": 6 * n * k * H * I / dt / 1e12, "unit": "TFLOPS",
+                                "cores": threads, "kind": "oracle",
+                                "sample": f"first {n} of {T} tokens, one pass of the float64 "
+                                          f"oracle (router + per-expert loop), {dt:.1f} s"}
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if dist is not None:
+        dist.barrier()
+        dist.destroy_process_group()
+
+
+def main():
+    args = parse()
+    wl = workload(args.workload)
+    if args.impl == "reference":
+        run_reference(args, wl)
+    else:
+        run_ours(args, wl)
+
+
+if __name__ == "__main__":
+    main()

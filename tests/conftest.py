@@ -16,3 +16,9 @@ def pytest_configure(config):
 @pytest.fixture(scope="session")
 def golden_dir():
     return os.path.join(os.path.dirname(os.path.abspath(__file__)), "golden")
+
+
+def build_library():
+    """Compile libmoe_gb300.so if needed (build script loaded by path, see __graft_entry__)."""
+    import __graft_entry__
+    __graft_entry__.build()

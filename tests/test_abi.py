@@ -13,8 +13,8 @@ ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
 
 @pytest.fixture(scope="module")
 def L():
-    from routing_grouped_gemm_router_gb300 import build
-    build.build()
+    from conftest import build_library
+    build_library()
     from routing_grouped_gemm_router_gb300 import _lib
     return _lib
 

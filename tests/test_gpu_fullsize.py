@@ -22,8 +22,8 @@ DEV = "cuda"
 def L():
     if not torch.cuda.is_available():
         pytest.skip("no CUDA device")
-    from routing_grouped_gemm_router_gb300 import build
-    build.build()
+    from conftest import build_library
+    build_library()
     from routing_grouped_gemm_router_gb300 import _lib
     _lib.moe_device_status(True)
     yield _lib
