@@ -179,10 +179,9 @@ def host_copies(inp):
 
 
 def default_sample(wl):
-    """Tokens per oracle pass: about 10-20 s on a 16-core host (the per-expert bf16 -> fp64
-    weight conversion dominates)."""
-    return {"mixtral-prefill": 256, "qwen3-skewed": 96,
-            "deepseek-v3": 24}.get(wl.name.split("@")[0], wl.T)
+    """Tokens per oracle pass: about 10-20 s of float64 work on a 16-core host."""
+    return {"mixtral-prefill": 1536, "qwen3-skewed": 768,
+            "deepseek-v3": 256}.get(wl.name.split("@")[0], wl.T)
 
 
 # ------------------------------------------------------------------------------ arms

@@ -13,6 +13,7 @@ import torch
 
 import moe_inputs as mi
 import oracle as O
+from oracle import moe_oracle as OM
 from _helpers import (TOPK_W_RTOL, assert_close, enforce_margins, oracle_logits,
                       oracle_route_from_logits, to_np, weights_for_oracle)
 
@@ -292,7 +293,7 @@ def test_layer_parity(L, wl):
     xs = to_np(inp.x)
     for e in np.unique(ids):
         rows = np.nonzero(ids.reshape(-1) == e)[0]
-        yref[rows] = O.expert_ffn(xs[rows // wl.k], O._expert(W13, e), O._expert(W2, e)) * \
+        yref[rows] = O.expert_ffn(xs[rows // wl.k], OM._expert(W13, e), OM._expert(W2, e)) * \
             w.reshape(-1)[rows][:, None]
     assert_close(y[:n], yref, wl.dtype, "y")
 
