@@ -136,6 +136,21 @@ moe_status_t moe_align(const int32_t* topk_ids, int T, int k, int E, int block_m
                        int32_t* sorted_ids, int32_t* expert_ids, int32_t* num_post_padded,
                        int32_t* counts, void* ws, size_t ws_bytes, cudaStream_t stream);
 
+/* moe_align without a workspace argument. The pages have no counterpart: this exists for
+ * callers that cannot give the library any device memory besides their inputs and outputs
+ * (an application or server whose device memory is owned by its own pool, or a path where
+ * cudaMalloc, which can synchronise the device, is not acceptable). Same arguments, results
+ * and checks as moe_align, but the per-chunk histograms live in a fixed 256 KiB array inside
+ * the library (held by every GPU that loads it until the process exits), so it never
+ * allocates. Limit: ceil(T*k / 1024) * E <= 65536 (e.g. T*k <= 524288 at E = 128); larger
+ * problems return MOE_ERR_UNSUPPORTED without launching anything. The first call on a device
+ * looks up the array's device address (make it before any stream capture). All calls on a
+ * device share the array and it keeps the last call's contents (nothing in it needs to start
+ * at zero: every call overwrites the part it reads); calls that overlap on the GPU race. */
+moe_status_t moe_align_noalloc(const int32_t* topk_ids, int T, int k, int E, int block_m,
+                               int32_t* sorted_ids, int32_t* expert_ids,
+                               int32_t* num_post_padded, int32_t* counts, cudaStream_t stream);
+
 /* GEMM1 + SwiGLU (page §6 with the gate/up halves fused in one epilogue): for every
  * padded position p < num_post_padded whose row r = sorted_ids[p] < T*k,
  *   act[p, :] = silu(x[r / k] @ W1[e]^T) * (x[r / k] @ W3[e]^T),  e = expert_ids[p / block_m].

@@ -57,6 +57,7 @@ def _load():
         "moe_workspace_size": (ST, [CFG, ctypes.POINTER(SZ)]),
         "moe_route": (ST, [CFG, P, P, P, P, P, P]),
         "moe_align": (ST, [P, I32, I32, I32, I32, P, P, P, P, P, SZ, P]),
+        "moe_align_noalloc": (ST, [P, I32, I32, I32, I32, P, P, P, P, P]),
         "moe_expert_gemm1": (ST, [CFG, P, P, P, P, P, I32, P, P]),
         "moe_expert_gemm2": (ST, [CFG, P, P, P, P, P, I32, P, P, P]),
         "moe_grouped_swiglu": (ST, [CFG, P, P, P, P, P, P, I32, P, P, P, SZ, P]),
@@ -73,7 +74,7 @@ def _load():
 _lib = _load()
 EXPORTED = ("moe_abi_version", "moe_status_string", "moe_block_m", "moe_max_padded_rows",
             "moe_align_workspace_size", "moe_workspace_layout", "moe_workspace_size",
-            "moe_route", "moe_align", "moe_expert_gemm1", "moe_expert_gemm2",
+            "moe_route", "moe_align", "moe_align_noalloc", "moe_expert_gemm1", "moe_expert_gemm2",
             "moe_grouped_swiglu", "moe_combine", "moe_forward", "moe_device_status")
 
 
@@ -156,6 +157,14 @@ def moe_align(topk_ids, T, k, E, block_m, sorted_ids, expert_ids, num_post_padde
     _check("moe_align", _lib.moe_align(_ptr(topk_ids), T, k, E, block_m, _ptr(sorted_ids),
                                        _ptr(expert_ids), _ptr(num_post_padded), _ptr(counts),
                                        _ptr(ws), ws_bytes, _stream(stream)))
+
+
+def moe_align_noalloc(topk_ids, T, k, E, block_m, sorted_ids, expert_ids, num_post_padded,
+                      counts=None, stream=None):
+    """moe_align for callers that cannot provide scratch memory (see include/moe.h)."""
+    _check("moe_align_noalloc", _lib.moe_align_noalloc(
+        _ptr(topk_ids), T, k, E, block_m, _ptr(sorted_ids), _ptr(expert_ids),
+        _ptr(num_post_padded), _ptr(counts), _stream(stream)))
 
 
 def moe_expert_gemm1(cfg, x, W13, sorted_ids, expert_ids, num_post_padded, block_m, act,

@@ -10,6 +10,8 @@
 // Small problems (T*k <= kSmallRows) run all steps in one CTA. Larger ones split the rows
 // into chunks of kChunk: a per-chunk histogram kernel, a single-CTA scan kernel that turns
 // the chunk histograms into absolute write offsets, and a per-chunk scatter kernel.
+#include <mutex>
+
 #include "common.cuh"
 
 namespace moe {
@@ -219,6 +221,64 @@ __global__ void __launch_bounds__(kAlignThreads) align_scatter_kernel(
   const int r0 = blockIdx.x * kChunk, r1 = min(n, r0 + kChunk);
   stable_scatter(ids, r0, r1, E, run_base, wcnt, sorted_ids);
 }
+
+// ---- variant without caller-provided scratch ------------------------------------------
+// Some callers cannot hand this library any device memory beyond their own inputs and
+// outputs: code running inside a host application or inference server whose device memory
+// is wholly owned by someone else's pool, or latency-critical paths where cudaMalloc (which
+// may synchronise the device) is not allowed. For them the per-chunk histograms live in a
+// fixed array of this file, which every GPU that loads the library keeps until exit.
+constexpr int kNoAllocScratchInts = 1 << 16;  // 256 KiB per GPU: chunks * E <= 65536
+static __device__ __align__(256) int32_t g_align_noalloc_scratch[kNoAllocScratchInts];
+
+// Device address of the array for the current device, looked up once per device with that
+// device current (in host code the array's name is not a device address).
+static int32_t* noalloc_scratch(moe_status_t* st) {
+  static std::mutex mu;
+  static int32_t* ptr[64] = {};
+  int dev = -1;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) {
+    *st = MOE_ERR_CUDA;
+    return nullptr;
+  }
+  std::lock_guard<std::mutex> lock(mu);
+  if (!ptr[dev]) {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_align_noalloc_scratch) != cudaSuccess || !p) {
+      cudaGetLastError();
+      *st = MOE_ERR_CUDA;
+      return nullptr;
+    }
+    ptr[dev] = (int32_t*)p;
+  }
+  return ptr[dev];
+}
+
+}  // namespace moe
+
+extern "C" moe_status_t moe_align_noalloc(const int32_t* topk_ids, int T, int k, int E,
+                                          int block_m, int32_t* sorted_ids,
+                                          int32_t* expert_ids, int32_t* num_post_padded,
+                                          int32_t* counts, cudaStream_t stream) {
+  using namespace moe;
+  if (!topk_ids || !sorted_ids || !expert_ids || !num_post_padded) return MOE_ERR_INVALID_ARG;
+  if (T < 1 || k < 1 || E < 1 || k > E || block_m < 1 || block_m > 4096)
+    return MOE_ERR_INVALID_ARG;
+  if (E > 512 || (int64_t)T * k > (int64_t)1 << 30) return MOE_ERR_UNSUPPORTED;
+  // Histograms beyond the fixed array: refuse rather than write past it.
+  if (align_scratch_bytes(T, k, E, block_m) > sizeof(int32_t) * (size_t)kNoAllocScratchInts)
+    return MOE_ERR_UNSUPPORTED;
+  moe_status_t st = MOE_OK;
+  int32_t* scratch = noalloc_scratch(&st);
+  if (!scratch) return st;
+  const int64_t n = (int64_t)T * k;
+  const int64_t bound = n + std::min<int64_t>(E, n) * (block_m - 1);
+  const int mp = (int)(bound / block_m * block_m);
+  return launch_align(topk_ids, T, k, E, block_m, mp, sorted_ids, expert_ids, num_post_padded,
+                      counts, scratch, stream);
+}
+
+namespace moe {
 
 static bool set_smem(const void* fn, size_t bytes) {
   if (bytes <= 48 * 1024) return true;
