@@ -42,6 +42,8 @@ def parse():
     p.add_argument("--impl", default="ours", choices=["ours", "reference"])
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--cpu-sample-tokens", type=int, default=0)
+    p.add_argument("--tokens", type=int, default=0,
+                   help="override T of the workload (smaller cases for profiling)")
     return p.parse_args()
 
 
@@ -389,6 +391,8 @@ def run_ours(args, wl):
 def main():
     args = parse()
     wl = workload(args.workload)
+    if args.tokens:
+        wl = wl.with_T(args.tokens)
     if args.impl == "reference":
         run_reference(args, wl)
     else:
