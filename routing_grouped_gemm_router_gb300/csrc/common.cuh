@@ -8,7 +8,7 @@
 
 #include <algorithm>
 
-#include "../../include/moe.h"
+#include "moe.h"
 
 namespace moe {
 

@@ -7,17 +7,22 @@
 // GEMM", §6, and the "fused-moe-kernel" skill card, Grouped GEMM Structure):
 //   * every 128-row M tile belongs to ONE expert, expert_ids[p / block_m];
 //   * tiles at or past num_post_padded (read on the device) are never started;
-//   * GEMM1 gathers the token rows x[sorted_ids[p] / k] with TMA gather4 (4 rows per copy)
-//     and computes gate and up as the two halves of one N=256 MMA, so the epilogue applies
+//   * GEMM1 gathers the token rows x[sorted_ids[p] / k] itself (no permuted copy of x) and
+//     computes gate and up as the two halves of one N=256 MMA, so the epilogue applies
 //     silu(gate) * up (§6 fused into the GEMM1 epilogue, as the page's exercise suggests);
 //   * GEMM2 reads act in padded order with plain 2-D TMA, multiplies by topk_w[r] and
 //     scatters each row to y[r], r = sorted_ids[p]; padding rows are never stored.
 //
 // Design (GB300-first, not the page's Triton kernel): one persistent CTA per SM walks a
 // static tile sequence (rasterised GROUP_M m-tiles per weight panel, the skill card's L2
-// grouping) with three warp roles: warp 0 issues TMA copies into a ring of STAGES shared-
-// memory stages, warp 1 (one lane) issues tcgen05.mma into one of two TMEM accumulators,
-// warps 2-5 drain the other accumulator (epilogue) while the next tile accumulates.
+// grouping) with three warp roles: producer warps fill a ring of STAGES shared-memory
+// stages, one MMA warp (one lane) issues tcgen05.mma into one of two TMEM accumulators, and
+// four epilogue warps drain the other accumulator while the next tile accumulates.
+// Producers: GEMM2 and the router use one warp issuing 2-D/3-D TMA tiles. GEMM1 uses four
+// warps that gather A with 16-byte cp.async (each warp instruction moves four whole 128-byte
+// token rows, written straight into the swizzled layout the MMA reads) while thread 0 moves
+// the weight panels by TMA. (A TMA gather4 producer moves only four rows per instruction;
+// on GB300 it capped GEMM1 near 470 TFLOP/s, against ~1300 TFLOP/s with contiguous tiles.)
 // Every mbarrier wait is bounded: on time-out the kernel records kStatusTimeout, stops
 // issuing work, lets copies in flight land and frees its TMEM before returning.
 #include <cudaTypedefs.h>
@@ -32,7 +37,6 @@ namespace tc {
 constexpr int BM = 128;          // MMA M (TMEM lanes)
 constexpr int BK = 64;           // 64 bf16 = 128 bytes = one swizzle row
 constexpr int UMMA_K = 16;       // K of one kind::f16 MMA
-constexpr int kThreads = 192;    // warp 0 TMA, warp 1 MMA, warps 2..5 epilogue
 constexpr int kGroupM = 8;       // m-tiles that share one weight panel in the raster
 constexpr uint64_t kTimeoutNs = 2000000000ull;  // 2 s per wait
 
@@ -108,14 +112,23 @@ __device__ __forceinline__ void tma_3d(void* dst, const CUtensorMap* tm, uint64_
       "l"((uint64_t)tm), "r"(c0), "r"(c1), "r"(c2), "r"(su32(bar))
       : "memory");
 }
-// Four rows r0..r3, columns [col, col + box width) of a 2-D map whose box is one row high.
-__device__ __forceinline__ void tma_gather4(void* dst, const CUtensorMap* tm, uint64_t* bar,
-                                            int col, int r0, int r1, int r2, int r3) {
-  asm volatile(
-      "cp.async.bulk.tensor.2d.shared::cluster.global.tile::gather4.mbarrier::complete_tx::bytes"
-      " [%0], [%1, {%2, %3, %4, %5, %6}], [%7];" ::"r"(su32(dst)),
-      "l"((uint64_t)tm), "r"(col), "r"(r0), "r"(r1), "r"(r2), "r"(r3), "r"(su32(bar))
-      : "memory");
+// 16-byte global -> shared copy that bypasses L1; src_bytes = 0 fills the 16 bytes with zeros.
+__device__ __forceinline__ void cp_async16(uint32_t dst, const void* src, uint32_t src_bytes) {
+  asm volatile("cp.async.cg.shared.global.L2::128B [%0], [%1], 16, %2;" ::"r"(dst), "l"(src),
+               "r"(src_bytes)
+               : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() {
+  asm volatile("cp.async.commit_group;" ::: "memory");
+}
+template <int N>
+__device__ __forceinline__ void cp_async_wait() {
+  asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
+}
+// Orders this thread's generic-proxy shared-memory writes before later async-proxy reads
+// (the tensor core reads its operands through the async proxy).
+__device__ __forceinline__ void fence_proxy_async_smem() {
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }
 __device__ __forceinline__ void prefetch_tmap(const CUtensorMap* tm) {
   asm volatile("prefetch.tensormap [%0];" ::"l"((uint64_t)tm) : "memory");
@@ -211,6 +224,16 @@ struct Params {
   const float* topk_w;
   void* out;
   int64_t ld_out;  // elements per output row
+  const void* x;   // GEMM1: token rows [T, K] bf16, gathered with cp.async
+};
+
+// Warp roles: producers, then one MMA warp, then four epilogue warps.
+template <int MODE>
+struct Roles {
+  static constexpr int kProdWarps = MODE == kGemm1 ? 4 : 1;
+  static constexpr int kMmaWarp = kProdWarps;
+  static constexpr int kThreads = (kProdWarps + 5) * 32;
+  static constexpr int kFullArrivals = MODE == kGemm1 ? 2 : 1;  // GEMM1: TMA + copies done
 };
 
 template <int MODE>
@@ -243,7 +266,7 @@ __device__ __forceinline__ void tile_of(int w, int num_m, int n_tiles, int& m, i
 
 // --------------------------------------------------------------------- the kernel
 template <int MODE, int BN, int STAGES>
-__global__ void __launch_bounds__(kThreads, 1)
+__global__ void __launch_bounds__(Roles<MODE>::kThreads, 1)
     gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                    const __grid_constant__ CUtensorMap tmB2, const Params P) {
   constexpr int A_BYTES = BM * 128;
@@ -264,11 +287,13 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint32_t* tmem_slot = (uint32_t*)(drain + 1);
   volatile int* abort_flag = (volatile int*)(tmem_slot + 1);
 
+  constexpr int kProdWarps = Roles<MODE>::kProdWarps;
+  constexpr int kMmaWarp = Roles<MODE>::kMmaWarp;
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < STAGES; ++s) {
-      mbar_init(&full[s], 1);
+      mbar_init(&full[s], Roles<MODE>::kFullArrivals);
       mbar_init(&empty[s], 1);
     }
     for (int b = 0; b < 2; ++b) {
@@ -278,11 +303,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_init(drain, 1);
     *abort_flag = 0;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
-    prefetch_tmap(&tmA);
+    if (MODE != kGemm1) prefetch_tmap(&tmA);
     prefetch_tmap(&tmB);
     if (MODE == kGemm1) prefetch_tmap(&tmB2);
   }
-  if (warp == 1) {
+  if (warp == kMmaWarp) {
     tmem_alloc(tmem_slot, TMEM_COLS);
     tmem_relinquish();
     tc_fence_before();
@@ -295,7 +320,66 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int total = num_m * P.n_tiles;
   const int num_kb = (P.K + BK - 1) / BK;
 
-  if (warp == 0) {
+  if (MODE == kGemm1 && warp < kProdWarps) {
+    // ------------------------------------------------------------ GEMM1 producers
+    // Producer warp `slot` owns ring slot `slot` and fills every STAGES-th k-block of this
+    // CTA's tile sequence: lane 0 issues the weight TMA (expect_tx arrival), then each lane
+    // copies 16-byte chunk lane%8 of tile rows 4*i + lane/8 (i = 0..31), so every warp
+    // instruction moves four whole 128-byte token rows; the warp waits for its own copies,
+    // fences the async proxy, and lane 0 adds the second arrival of the full barrier.
+    // With one warp per slot, STAGES stages load concurrently and independently.
+    static_assert(MODE != kGemm1 || STAGES == kProdWarps, "one producer warp per ring slot");
+    const int slot = warp;
+    const int sub = lane & 7, rsub = lane >> 3;
+    const char* xb = (const char*)P.x;
+    const uint32_t a = su32(sA + slot * A_BYTES);
+    uint8_t* b = sB + slot * B_BYTES;
+    int g = 0;  // k-blocks of this CTA's tile sequence before the current tile
+    bool ok = true;
+    for (int w = blockIdx.x; w < total && ok; w += gridDim.x) {
+      int m, n;
+      tile_of(w, num_m, P.n_tiles, m, n);
+      const int e = P.eid[(m * BM) / P.block_m];
+      if (e < 0) continue;
+      const int kb0 = ((slot - g) % STAGES + STAGES) % STAGES;
+      if (kb0 < num_kb) {
+        int tok[32];
+#pragma unroll
+        for (int i = 0; i < 32; ++i) {
+          const int r = P.sid[m * BM + 4 * i + rsub];
+          tok[i] = r < P.n_rows ? r / P.k : 0;
+        }
+        for (int kb = kb0; kb < num_kb; kb += STAGES) {
+          const uint32_t use = (uint32_t)((g + kb) / STAGES);
+          int okw = 1;
+          if (lane == 0) okw = wait_bounded(&empty[slot], (use & 1u) ^ 1u, abort_flag);
+          okw = __shfl_sync(0xffffffffu, okw, 0);
+          if (!okw) { ok = false; break; }
+          if (lane == 0) {
+            mbar_expect_tx(&full[slot], B_BYTES);
+            tma_3d(b, &tmB, &full[slot], kb * BK, n * 128, e);
+            tma_3d(b + 128 * 128, &tmB2, &full[slot], kb * BK, n * 128, e);
+          }
+          const int col = kb * BK + sub * 8;
+          const uint32_t nbytes = col < P.K ? 16u : 0u;
+          const int64_t coff = (int64_t)(col < P.K ? col : 0) * 2;
+#pragma unroll
+          for (int i = 0; i < 32; ++i) {
+            const int row = 4 * i + rsub;
+            cp_async16(a + row * 128 + ((sub ^ (row & 7)) << 4),
+                       xb + (int64_t)tok[i] * P.K * 2 + coff, nbytes);
+          }
+          cp_async_commit();
+          cp_async_wait<0>();
+          fence_proxy_async_smem();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&full[slot]);
+        }
+      }
+      g += num_kb;
+    }
+    cp_async_wait<0>();
+  } else if (MODE != kGemm1 && warp == 0) {
     // ------------------------------------------------------------ TMA producer
     int stage = 0;
     uint32_t phase = 0;
@@ -304,45 +388,27 @@ __global__ void __launch_bounds__(kThreads, 1)
       tile_of(w, num_m, P.n_tiles, m, n);
       const int e = MODE == kRouter ? 0 : P.eid[(m * BM) / P.block_m];
       if (e < 0) continue;
-      int t0 = 0, t1 = 0, t2 = 0, t3 = 0;
-      if (MODE == kGemm1) {
-        const int4 r4 = *reinterpret_cast<const int4*>(P.sid + m * BM + lane * 4);
-        t0 = r4.x < P.n_rows ? r4.x / P.k : 0;
-        t1 = r4.y < P.n_rows ? r4.y / P.k : 0;
-        t2 = r4.z < P.n_rows ? r4.z / P.k : 0;
-        t3 = r4.w < P.n_rows ? r4.w / P.k : 0;
-      }
       for (int kb = 0; kb < num_kb; ++kb) {
         int ok = 1;
         if (lane == 0) ok = wait_bounded(&empty[stage], phase ^ 1u, abort_flag);
         ok = __shfl_sync(0xffffffffu, ok, 0);
         if (!ok) goto producer_done;
-        if (lane == 0) mbar_expect_tx(&full[stage], A_BYTES + B_BYTES);
-        __syncwarp();
-        uint8_t* a = sA + stage * A_BYTES;
-        uint8_t* b = sB + stage * B_BYTES;
-        if (MODE == kGemm1) {
-          tma_gather4(a + lane * 512, &tmA, &full[stage], kb * BK, t0, t1, t2, t3);
-          if (lane == 0) {
-            tma_3d(b, &tmB, &full[stage], kb * BK, n * 128, e);
-            tma_3d(b + 128 * 128, &tmB2, &full[stage], kb * BK, n * 128, e);
-          }
-        } else if (MODE == kGemm2) {
-          if (lane == 0) {
-            tma_2d(a, &tmA, &full[stage], kb * BK, m * BM);
+        if (lane == 0) {
+          uint8_t* a = sA + stage * A_BYTES;
+          uint8_t* b = sB + stage * B_BYTES;
+          mbar_expect_tx(&full[stage], A_BYTES + B_BYTES);
+          tma_2d(a, &tmA, &full[stage], kb * BK, m * BM);
+          if (MODE == kGemm2)
             tma_3d(b, &tmB, &full[stage], kb * BK, n * BN, e);
-          }
-        } else {
-          if (lane == 0) {
-            tma_2d(a, &tmA, &full[stage], kb * BK, m * BM);
+          else
             tma_2d(b, &tmB, &full[stage], kb * BK, 0);
-          }
         }
+        __syncwarp();
         if (++stage == STAGES) { stage = 0; phase ^= 1u; }
       }
     }
   producer_done:;
-  } else if (warp == 1) {
+  } else if (warp == kMmaWarp) {
     // ------------------------------------------------------------ MMA issuer (one lane)
     if (lane == 0) {
       int stage = 0;
@@ -383,8 +449,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
     }
     __syncwarp();
-  } else {
-    // ------------------------------------------------------------ epilogue (warps 2..5)
+  } else if (warp > kMmaWarp) {
+    // ------------------------------------------------------------ epilogue (4 warps)
     const int q = warp & 3;  // TMEM lane quarter this warp may access
     const int row = q * 32 + lane;
     int acc = 0;
@@ -488,7 +554,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     while (gtimer() - t0 < 200000ull) {
     }
   }
-  if (warp == 1) {
+  if (warp == kMmaWarp) {
     tc_fence_after();
     tmem_dealloc(tmem_base, TMEM_COLS);
   }
@@ -550,7 +616,7 @@ static moe_status_t launch(const CUtensorMap& a, const CUtensorMap& b, const CUt
   }
   int grid = std::min(num_sms(), max_tiles);
   if (grid < 1) return MOE_OK;
-  kern<<<grid, kThreads, smem, s>>>(a, b, b2, P);
+  kern<<<grid, Roles<MODE>::kThreads, smem, s>>>(a, b, b2, P);
   return last_launch_status();
 }
 
@@ -570,13 +636,8 @@ moe_status_t launch_gemm1_tc(const moe_config_t& c, const void* x, const void* W
                              const int32_t* sid, const int32_t* eid, const int32_t* npp,
                              int block_m, int max_padded, void* act, cudaStream_t s) {
   using namespace tc;
-  CUtensorMap mA, mG, mU;
-  const uint64_t H = c.H, I = c.I, E = c.E, T = c.T;
-  {
-    uint64_t d[2] = {H, T}, st[1] = {H};
-    uint32_t box[2] = {BK, 1};
-    if (!make_map(&mA, x, 2, d, st, box, false)) return MOE_ERR_CUDA;
-  }
+  CUtensorMap mG, mU;
+  const uint64_t H = c.H, I = c.I, E = c.E;
   {
     uint64_t d[3] = {H, I, E}, st[2] = {H, 2 * I * H};
     uint32_t box[3] = {BK, 128, 1};
@@ -597,8 +658,9 @@ moe_status_t launch_gemm1_tc(const moe_config_t& c, const void* x, const void* W
   P.npp = npp;
   P.out = act;
   P.ld_out = c.I;
+  P.x = x;
   const int max_tiles = (max_padded / BM) * P.n_tiles;
-  return launch<kGemm1, Cfg<kGemm1>::BN, Cfg<kGemm1>::STAGES>(mA, mG, mU, P, max_tiles, s);
+  return launch<kGemm1, Cfg<kGemm1>::BN, Cfg<kGemm1>::STAGES>(mG, mG, mU, P, max_tiles, s);
 }
 
 moe_status_t launch_gemm2_tc(const moe_config_t& c, const void* act, const void* W2,
