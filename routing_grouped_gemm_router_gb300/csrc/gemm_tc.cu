@@ -14,8 +14,8 @@
 //     scatters each row to y[r], r = sorted_ids[p]; padding rows are never stored.
 //
 // Design (GB300-first, not the page's Triton kernel): one persistent CTA per SM walks a
-// static tile sequence (rasterised GROUP_M m-tiles per weight panel, the skill card's L2
-// grouping) with three warp roles: producer warps fill a ring of STAGES shared-memory
+// static tile sequence (expert-major: every m-tile of an expert per weight panel, the skill
+// card's L2 grouping taken to expert granularity) with three warp roles: producer warps fill a ring of STAGES shared-memory
 // stages, one MMA warp (one lane) issues tcgen05.mma into one of two TMEM accumulators, and
 // four epilogue warps drain the other accumulator while the next tile accumulates.
 // Producers: GEMM2 and the router use one warp issuing 2-D/3-D TMA tiles. GEMM1 uses four
@@ -254,6 +254,41 @@ __host__ __device__ constexpr size_t smem_bytes_for(int bn, int stages) {
   return 1024 + (size_t)stages * (BM * 128 + (size_t)bn * 128) + 256;
 }
 
+// Expert-major raster for the grouped GEMMs: work item w visits, expert by expert, each
+// weight panel n with ALL of that expert's m-tiles back to back, so the CTAs running at the
+// same time share a few weight panels (one HBM read each) and the expert's token rows stay
+// in L2 across its panels. w / n_tiles always lands inside the owning expert's run of
+// m-tiles, so its expert id is expert_ids[w / n_tiles]; the run [lo, hi) is found by binary
+// search (each expert's tiles are contiguous). Returns the expert (-1: skip the tile).
+__device__ __forceinline__ int expert_tile_of(int w, int num_m, int n_tiles, const int32_t* eid,
+                                              int block_m, int& m, int& n) {
+  const int v = w / n_tiles;
+  const int e = eid[(v * BM) / block_m];
+  if (e < 0) {
+    m = v;
+    n = w - v * n_tiles;
+    return e;
+  }
+  int lo = 0, hi = v;  // first tile of the run: smallest t <= v with eid == e
+  while (lo < hi) {
+    const int mid = (lo + hi) >> 1;
+    if (eid[(mid * BM) / block_m] == e) hi = mid; else lo = mid + 1;
+  }
+  const int first = lo;
+  lo = v + 1;
+  hi = num_m;  // one past the last tile of the run
+  while (lo < hi) {
+    const int mid = (lo + hi) >> 1;
+    if (eid[(mid * BM) / block_m] == e) lo = mid + 1; else hi = mid;
+  }
+  const int mt = lo - first;
+  const int local = w - first * n_tiles;
+  m = first + local % mt;
+  n = local / mt;
+  return e;
+}
+
+// Router raster: GROUP_M m-tiles per panel (only one panel, n_tiles = 1, in practice).
 __device__ __forceinline__ void tile_of(int w, int num_m, int n_tiles, int& m, int& n) {
   const int per_group = kGroupM * n_tiles;
   const int g = w / per_group;
@@ -338,8 +373,7 @@ __global__ void __launch_bounds__(Roles<MODE>::kThreads, 1)
     bool ok = true;
     for (int w = blockIdx.x; w < total && ok; w += gridDim.x) {
       int m, n;
-      tile_of(w, num_m, P.n_tiles, m, n);
-      const int e = P.eid[(m * BM) / P.block_m];
+      const int e = expert_tile_of(w, num_m, P.n_tiles, P.eid, P.block_m, m, n);
       if (e < 0) continue;
       const int kb0 = ((slot - g) % STAGES + STAGES) % STAGES;
       if (kb0 < num_kb) {
@@ -384,9 +418,9 @@ __global__ void __launch_bounds__(Roles<MODE>::kThreads, 1)
     int stage = 0;
     uint32_t phase = 0;
     for (int w = blockIdx.x; w < total; w += gridDim.x) {
-      int m, n;
-      tile_of(w, num_m, P.n_tiles, m, n);
-      const int e = MODE == kRouter ? 0 : P.eid[(m * BM) / P.block_m];
+      int m, n, e = 0;
+      if (MODE == kRouter) tile_of(w, num_m, P.n_tiles, m, n);
+      else e = expert_tile_of(w, num_m, P.n_tiles, P.eid, P.block_m, m, n);
       if (e < 0) continue;
       for (int kb = 0; kb < num_kb; ++kb) {
         int ok = 1;
@@ -417,9 +451,9 @@ __global__ void __launch_bounds__(Roles<MODE>::kThreads, 1)
       uint32_t acc_phase = 0;
       bool ok = true, issued = false;
       for (int w = blockIdx.x; w < total && ok; w += gridDim.x) {
-        int m, n;
-        tile_of(w, num_m, P.n_tiles, m, n);
-        const int e = MODE == kRouter ? 0 : P.eid[(m * BM) / P.block_m];
+        int m, n, e = 0;
+        if (MODE == kRouter) tile_of(w, num_m, P.n_tiles, m, n);
+        else e = expert_tile_of(w, num_m, P.n_tiles, P.eid, P.block_m, m, n);
         if (e < 0) continue;
         if (!wait_bounded(&tempty[acc], acc_phase ^ 1u, abort_flag)) { ok = false; break; }
         tc_fence_after();
@@ -456,9 +490,9 @@ __global__ void __launch_bounds__(Roles<MODE>::kThreads, 1)
     int acc = 0;
     uint32_t acc_phase = 0;
     for (int w = blockIdx.x; w < total; w += gridDim.x) {
-      int m, n;
-      tile_of(w, num_m, P.n_tiles, m, n);
-      const int e = MODE == kRouter ? 0 : P.eid[(m * BM) / P.block_m];
+      int m, n, e = 0;
+      if (MODE == kRouter) tile_of(w, num_m, P.n_tiles, m, n);
+      else e = expert_tile_of(w, num_m, P.n_tiles, P.eid, P.block_m, m, n);
       if (e < 0) continue;
       int ok = 1;
       if (lane == 0) ok = wait_bounded(&tfull[acc], acc_phase, abort_flag);
