@@ -24,6 +24,7 @@ int num_sms() {
 static bool aligned16(const void* p) { return ((uintptr_t)p & 15u) == 0; }
 
 static constexpr int kMaxE = 512;
+static constexpr int kFewTokens = 128;  // router on CUDA cores up to this many tokens
 
 static moe_status_t check_cfg(const moe_config_t* c) {
   if (!c) return MOE_ERR_INVALID_ARG;
@@ -132,13 +133,15 @@ moe_status_t moe_route(const moe_config_t* c, const void* x, const void* Wg, flo
   moe_status_t st = check_cfg(c);
   if (st != MOE_OK) return st;
   if (!x || !Wg || !logits || !topk_ids || !topk_w) return MOE_ERR_INVALID_ARG;
-  if (c->dtype == MOE_BF16) {
-    if (!aligned16(x) || !aligned16(Wg)) return MOE_ERR_INVALID_ARG;
-    st = c->E <= 256 ? launch_router_tc(*c, x, Wg, logits, stream)
-                     : launch_router_simt(*c, x, Wg, logits, stream);
-  } else {
+  // Few tokens (decode): spread the router rows over many SMs on CUDA cores. Otherwise
+  // bf16 runs on the tensor cores (E <= 256 fits one MMA N), fp32 on FFMA tiles.
+  if (c->dtype == MOE_BF16 && (!aligned16(x) || !aligned16(Wg))) return MOE_ERR_INVALID_ARG;
+  if (c->T <= kFewTokens && aligned16(x) && aligned16(Wg))
+    st = launch_router_few_tokens(*c, x, Wg, logits, stream);
+  else if (c->dtype == MOE_BF16 && c->E <= 256)
+    st = launch_router_tc(*c, x, Wg, logits, stream);
+  else
     st = launch_router_simt(*c, x, Wg, logits, stream);
-  }
   if (st != MOE_OK) return st;
   return launch_topk(*c, logits, topk_ids, topk_w, stream);
 }

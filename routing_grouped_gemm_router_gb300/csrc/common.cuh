@@ -35,6 +35,8 @@ inline size_t dtype_size(moe_dtype_t d) { return d == MOE_BF16 ? 2 : 4; }
 
 moe_status_t launch_router_simt(const moe_config_t& c, const void* x, const void* Wg,
                                 float* logits, cudaStream_t s);
+moe_status_t launch_router_few_tokens(const moe_config_t& c, const void* x, const void* Wg,
+                                      float* logits, cudaStream_t s);
 moe_status_t launch_router_tc(const moe_config_t& c, const void* x, const void* Wg,
                               float* logits, cudaStream_t s);
 moe_status_t launch_topk(const moe_config_t& c, const float* logits, int32_t* ids, float* w,

@@ -18,10 +18,10 @@
 // card's L2 grouping taken to expert granularity) with three warp roles: producer warps fill a ring of STAGES shared-memory
 // stages, one MMA warp (one lane) issues tcgen05.mma into one of two TMEM accumulators, and
 // four epilogue warps drain the other accumulator while the next tile accumulates.
-// Producers: GEMM2 and the router use one warp issuing 2-D/3-D TMA tiles. GEMM1 uses four
-// warps that gather A with 16-byte cp.async (each warp instruction moves four whole 128-byte
-// token rows, written straight into the swizzled layout the MMA reads) while thread 0 moves
-// the weight panels by TMA. (A TMA gather4 producer moves only four rows per instruction;
+// Producers: GEMM2 and the router use one warp issuing 2-D/3-D TMA tiles. GEMM1 uses eight
+// warps (two per ring slot) that gather A with 16-byte cp.async (each warp instruction moves
+// four whole 128-byte token rows, written straight into the swizzled layout the MMA reads)
+// while one lane per slot moves the weight panels by TMA. (A TMA gather4 producer moves only four rows per instruction;
 // on GB300 it capped GEMM1 near 470 TFLOP/s, against ~1300 TFLOP/s with contiguous tiles.)
 // Every mbarrier wait is bounded: on time-out the kernel records kStatusTimeout, stops
 // issuing work, lets copies in flight land and frees its TMEM before returning.
@@ -230,10 +230,11 @@ struct Params {
 // Warp roles: producers, then one MMA warp, then four epilogue warps.
 template <int MODE>
 struct Roles {
-  static constexpr int kProdWarps = MODE == kGemm1 ? 4 : 1;
+  static constexpr int kProdWarps = MODE == kGemm1 ? 8 : 1;   // GEMM1: two per ring slot
   static constexpr int kMmaWarp = kProdWarps;
   static constexpr int kThreads = (kProdWarps + 5) * 32;
-  static constexpr int kFullArrivals = MODE == kGemm1 ? 2 : 1;  // GEMM1: TMA + copies done
+  // GEMM1: the weight TMA's expect_tx arrival plus one arrival per producer warp of the slot
+  static constexpr int kFullArrivals = MODE == kGemm1 ? 3 : 1;
 };
 
 template <int MODE>
@@ -357,14 +358,16 @@ __global__ void __launch_bounds__(Roles<MODE>::kThreads, 1)
 
   if (MODE == kGemm1 && warp < kProdWarps) {
     // ------------------------------------------------------------ GEMM1 producers
-    // Producer warp `slot` owns ring slot `slot` and fills every STAGES-th k-block of this
-    // CTA's tile sequence: lane 0 issues the weight TMA (expect_tx arrival), then each lane
-    // copies 16-byte chunk lane%8 of tile rows 4*i + lane/8 (i = 0..31), so every warp
-    // instruction moves four whole 128-byte token rows; the warp waits for its own copies,
-    // fences the async proxy, and lane 0 adds the second arrival of the full barrier.
-    // With one warp per slot, STAGES stages load concurrently and independently.
-    static_assert(MODE != kGemm1 || STAGES == kProdWarps, "one producer warp per ring slot");
-    const int slot = warp;
+    // Producer warps 2s and 2s+1 own ring slot s and fill every STAGES-th k-block of this
+    // CTA's tile sequence. Warp 2s's lane 0 issues the weight TMA (expect_tx arrival). Each
+    // warp copies 64 of the tile's 128 token rows: lane l moves 16-byte chunk l%8 of rows
+    // base + 4*i + l/8 (i = 0..15), so every warp instruction moves four whole 128-byte
+    // rows. Padding rows (sentinel ids) are zero-filled without reading memory. The warp
+    // waits for its own copies, fences the async proxy, and lane 0 arrives. Each slot's
+    // stage loads independently of the others, so STAGES stages are in flight.
+    static_assert(MODE != kGemm1 || kProdWarps == 2 * STAGES, "two producer warps per slot");
+    const int slot = warp >> 1;
+    const int rbase = (warp & 1) * 64;
     const int sub = lane & 7, rsub = lane >> 3;
     const char* xb = (const char*)P.x;
     const uint32_t a = su32(sA + slot * A_BYTES);
@@ -377,11 +380,11 @@ __global__ void __launch_bounds__(Roles<MODE>::kThreads, 1)
       if (e < 0) continue;
       const int kb0 = ((slot - g) % STAGES + STAGES) % STAGES;
       if (kb0 < num_kb) {
-        int tok[32];
+        int tok[16];
 #pragma unroll
-        for (int i = 0; i < 32; ++i) {
-          const int r = P.sid[m * BM + 4 * i + rsub];
-          tok[i] = r < P.n_rows ? r / P.k : 0;
+        for (int i = 0; i < 16; ++i) {
+          const int r = P.sid[m * BM + rbase + 4 * i + rsub];
+          tok[i] = r < P.n_rows ? r / P.k : -1;
         }
         for (int kb = kb0; kb < num_kb; kb += STAGES) {
           const uint32_t use = (uint32_t)((g + kb) / STAGES);
@@ -389,19 +392,21 @@ __global__ void __launch_bounds__(Roles<MODE>::kThreads, 1)
           if (lane == 0) okw = wait_bounded(&empty[slot], (use & 1u) ^ 1u, abort_flag);
           okw = __shfl_sync(0xffffffffu, okw, 0);
           if (!okw) { ok = false; break; }
-          if (lane == 0) {
+          if (lane == 0 && rbase == 0) {
             mbar_expect_tx(&full[slot], B_BYTES);
             tma_3d(b, &tmB, &full[slot], kb * BK, n * 128, e);
             tma_3d(b + 128 * 128, &tmB2, &full[slot], kb * BK, n * 128, e);
           }
           const int col = kb * BK + sub * 8;
-          const uint32_t nbytes = col < P.K ? 16u : 0u;
-          const int64_t coff = (int64_t)(col < P.K ? col : 0) * 2;
+          const bool col_ok = col < P.K;
+          const int64_t coff = (int64_t)(col_ok ? col : 0) * 2;
 #pragma unroll
-          for (int i = 0; i < 32; ++i) {
-            const int row = 4 * i + rsub;
+          for (int i = 0; i < 16; ++i) {
+            const int row = rbase + 4 * i + rsub;
+            const bool live = col_ok && tok[i] >= 0;
             cp_async16(a + row * 128 + ((sub ^ (row & 7)) << 4),
-                       xb + (int64_t)tok[i] * P.K * 2 + coff, nbytes);
+                       xb + (int64_t)(tok[i] >= 0 ? tok[i] : 0) * P.K * 2 + coff,
+                       live ? 16u : 0u);
           }
           cp_async_commit();
           cp_async_wait<0>();

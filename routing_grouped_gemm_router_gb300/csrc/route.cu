@@ -64,6 +64,95 @@ __global__ void __launch_bounds__(256) router_simt_kernel(const T* __restrict__ 
   }
 }
 
+// ------------------------------------------------------------------------------------
+// Router GEMM for few tokens (decode): a warp owns one expert and a block of TB tokens,
+// streams that expert's router row in 16-byte pieces and keeps one fp32 sum per token; lane
+// partial sums are reduced with shuffles. E/8 x ceil(T/TB) CTAs of 8 warps spread the
+// router matrix over many SMs instead of one tensor-core tile.
+// ------------------------------------------------------------------------------------
+template <typename T>
+__device__ __forceinline__ void load8(const T* p, float (&v)[8]);
+template <>
+__device__ __forceinline__ void load8<__nv_bfloat16>(const __nv_bfloat16* p, float (&v)[8]) {
+  const uint4 q = *reinterpret_cast<const uint4*>(p);
+  const __nv_bfloat162* h = reinterpret_cast<const __nv_bfloat162*>(&q);
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    float2 f = __bfloat1622float2(h[i]);
+    v[2 * i] = f.x;
+    v[2 * i + 1] = f.y;
+  }
+}
+template <>
+__device__ __forceinline__ void load8<float>(const float* p, float (&v)[8]) {
+  const float4 a = *reinterpret_cast<const float4*>(p);
+  const float4 b = *reinterpret_cast<const float4*>(p + 4);
+  v[0] = a.x; v[1] = a.y; v[2] = a.z; v[3] = a.w; v[4] = b.x; v[5] = b.y; v[6] = b.z; v[7] = b.w;
+}
+
+template <typename T, int TB>
+__global__ void __launch_bounds__(256) router_few_tokens_kernel(const T* __restrict__ x,
+                                                                const T* __restrict__ Wg,
+                                                                float* __restrict__ logits,
+                                                                int Tn, int H, int E) {
+  const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+  const int e = blockIdx.x * 8 + warp;
+  const int t0 = blockIdx.y * TB;
+  if (e >= E) return;
+  // Token rows past the end are clamped to the last row (loaded, never stored), so every
+  // load below is unconditional and the loads of a group can all be in flight together.
+  const T* xr[TB];
+#pragma unroll
+  for (int t = 0; t < TB; ++t) xr[t] = x + (size_t)min(t0 + t, Tn - 1) * H;
+  float acc[TB];
+#pragma unroll
+  for (int t = 0; t < TB; ++t) acc[t] = 0.f;
+  const T* w = Wg + (size_t)e * H;
+#pragma unroll 2
+  for (int h = lane * 8; h < H; h += 256) {
+    float wv[8];
+    load8(w + h, wv);
+#pragma unroll
+    for (int tg = 0; tg < TB; tg += 8) {
+      constexpr int G = TB < 8 ? TB : 8;
+      float xv[G][8];
+#pragma unroll
+      for (int j = 0; j < G; ++j) load8(xr[tg + j] + h, xv[j]);
+#pragma unroll
+      for (int j = 0; j < G; ++j)
+#pragma unroll
+        for (int q = 0; q < 8; ++q) acc[tg + j] = fmaf(xv[j][q], wv[q], acc[tg + j]);
+    }
+  }
+#pragma unroll
+  for (int t = 0; t < TB; ++t) {
+    float v = acc[t];
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) v += __shfl_xor_sync(0xffffffffu, v, off);
+    if (lane == (t & 31) && t0 + t < Tn) logits[(size_t)(t0 + t) * E + e] = v;
+  }
+}
+
+template <int TB>
+static void launch_few(const moe_config_t& c, const void* x, const void* Wg, float* logits,
+                       cudaStream_t s) {
+  dim3 grid(ceil_div(c.E, 8), ceil_div(c.T, TB));
+  if (c.dtype == MOE_F32)
+    router_few_tokens_kernel<float, TB><<<grid, 256, 0, s>>>((const float*)x, (const float*)Wg,
+                                                             logits, c.T, c.H, c.E);
+  else
+    router_few_tokens_kernel<__nv_bfloat16, TB><<<grid, 256, 0, s>>>(
+        (const __nv_bfloat16*)x, (const __nv_bfloat16*)Wg, logits, c.T, c.H, c.E);
+}
+
+moe_status_t launch_router_few_tokens(const moe_config_t& c, const void* x, const void* Wg,
+                                      float* logits, cudaStream_t s) {
+  if (c.T <= 1) launch_few<1>(c, x, Wg, logits, s);
+  else if (c.T <= 8) launch_few<8>(c, x, Wg, logits, s);
+  else launch_few<16>(c, x, Wg, logits, s);
+  return last_launch_status();
+}
+
 moe_status_t launch_router_simt(const moe_config_t& c, const void* x, const void* Wg,
                                 float* logits, cudaStream_t s) {
   dim3 grid(ceil_div(c.T, 64), ceil_div(c.E, 64));

@@ -209,6 +209,9 @@ ROUTE_CASES = [
     ("grouped-E64-noscale", 129, 256, 64, 6, "bf16", 1, True, 1.0, 8, 3, 0.0, 0.1),
     ("softmax-E512-simt", 77, 128, 512, 4, "bf16", 0, True, 1.0, 1, 1, 0.0, 0.0),
     ("softmax-E40-f32", 90, 64, 40, 3, "f32", 0, True, 1.0, 1, 1, 0.0, 0.0),
+    ("softmax-E300-tiles", 200, 128, 300, 4, "bf16", 0, True, 1.0, 1, 1, 0.0, 0.0),
+    ("softmax-f32-tiles", 300, 64, 40, 3, "f32", 0, True, 1.0, 1, 1, 0.0, 0.0),
+    ("grouped-decode-T3", 3, 256, 256, 8, "bf16", 1, True, 2.5, 8, 4, 0.0, 0.05),
     ("grouped-E16-f32", 60, 64, 16, 4, "f32", 1, True, 2.5, 4, 2, 0.0, 0.5),
 ]
 
