@@ -190,7 +190,8 @@ moe_status_t moe_forward(const moe_config_t* cfg, const void* x, const void* Wg,
                          size_t ws_bytes, cudaStream_t stream);
 
 /* Diagnostic (synchronises the current device): returns the device status word (0 = no
- * fault seen; 1 = an expert id outside [0, E); 2 = a pipeline wait ran out of time) and
+ * fault seen; 1 = an expert id outside [0, E); 2 = a pipeline wait ran out of time; 3 = the
+ * two CTAs of a tensor-core pair were given different tensor-memory columns) and
  * clears it when reset != 0. Not for use inside stream capture. */
 int moe_device_status(int reset);
 

@@ -253,9 +253,10 @@ moe_status_t moe_forward(const moe_config_t* c, const void* x, const void* Wg, c
 }
 
 int moe_device_status(int reset) {
-  int a = align_status_read(reset);
-  int t = tc_status_read(reset);
-  return t ? t : a;
+  const int a = align_status_read(reset);
+  const int r = router_status_read(reset);
+  const int g = grouped_status_read(reset);
+  return g ? g : (r ? r : a);
 }
 
 }  // extern "C"

@@ -13,7 +13,7 @@
 namespace moe {
 
 // Device status codes (moe_device_status).
-enum : int { kStatusOk = 0, kStatusBadExpert = 1, kStatusTimeout = 2 };
+enum : int { kStatusOk = 0, kStatusBadExpert = 1, kStatusTimeout = 2, kStatusPairTmem = 3 };
 
 __host__ __device__ inline int ceil_div(int a, int b) { return (a + b - 1) / b; }
 __host__ __device__ inline int64_t ceil_div64(int64_t a, int64_t b) { return (a + b - 1) / b; }
@@ -63,6 +63,7 @@ moe_status_t launch_combine(const void* y, int T, int k, int H, moe_dtype_t dt, 
                             cudaStream_t s);
 
 int align_status_read(int reset);
-int tc_status_read(int reset);
+int router_status_read(int reset);
+int grouped_status_read(int reset);
 
 }  // namespace moe
