@@ -242,8 +242,9 @@ def run_ours(args, wl):
     base = ws.data_ptr()
     p = {n: base + getattr(lay, n) for n in ("logits", "topk_ids", "topk_w", "sorted_ids",
                                                "expert_ids", "num_post_padded", "counts",
-                                               "align_scratch", "act", "y")}
+                                               "align_scratch", "act", "xs", "y")}
     ws_align = lay.act - lay.align_scratch
+    ws_xs = lay.y - lay.xs
     out = torch.empty(T, H, dtype=inp.x.dtype, device=dev)
     stream = torch.cuda.current_stream(dev)
     sh = stream.cuda_stream
@@ -261,7 +262,7 @@ def run_ours(args, wl):
         if ev is not None:
             ev[2].record(stream)
         L.moe_expert_gemm1(cfg, inp.x, inp.W13, p["sorted_ids"], p["expert_ids"],
-                           p["num_post_padded"], B, p["act"], sh)
+                           p["num_post_padded"], B, p["act"], p["xs"], ws_xs, sh)
         if ev is not None:
             ev[3].record(stream)
         L.moe_expert_gemm2(cfg, p["act"], inp.W2, p["sorted_ids"], p["expert_ids"],
@@ -272,8 +273,9 @@ def run_ours(args, wl):
         if ev is not None:
             ev[5].record(stream)
 
-    # router GEMM + top-k, align (one kernel up to 4096 rows, else three), GEMM1, GEMM2, combine
-    launches_per_step = 2 + (1 if T * k <= 4096 else 3) + 2 + 1
+    # router GEMM + top-k, align (one kernel up to 4096 rows, else three), row gather + GEMM1
+    # (bf16), GEMM2, combine
+    launches_per_step = 2 + (1 if T * k <= 4096 else 3) + (2 if wl.dtype == "bf16" else 1) + 1 + 1
 
     for _ in range(max(3, args.warmup)):
         step()

@@ -94,6 +94,7 @@ typedef struct moe_ws_layout {
   size_t counts;           /* int32 [E] */
   size_t align_scratch;    /* moe_align workspace */
   size_t act;              /* dtype [max_padded, I] */
+  size_t xs;               /* bf16 [max_padded, H]: routed token rows in padded order */
   size_t y;                /* dtype [T*k, H] */
   size_t total;            /* bytes required */
   int block_m;
@@ -155,11 +156,15 @@ moe_status_t moe_align_noalloc(const int32_t* topk_ids, int T, int k, int E, int
  * padded position p < num_post_padded whose row r = sorted_ids[p] < T*k,
  *   act[p, :] = silu(x[r / k] @ W1[e]^T) * (x[r / k] @ W3[e]^T),  e = expert_ids[p / block_m].
  * act is [max_padded, I] in padded order; rows of padding positions are not written.
- * block_m must be a multiple of moe_block_m(cfg). */
+ * block_m must be a multiple of moe_block_m(cfg). bf16: the routed token rows are first
+ * gathered into padded order in ws (moe_expert_gemm1_workspace_size bytes, 256-byte
+ * aligned), then multiplied on the tensor cores; fp32 gathers inside the GEMM (ws unused). */
+moe_status_t moe_expert_gemm1_workspace_size(const moe_config_t* cfg, int block_m,
+                                             size_t* bytes);
 moe_status_t moe_expert_gemm1(const moe_config_t* cfg, const void* x, const void* W13,
                               const int32_t* sorted_ids, const int32_t* expert_ids,
                               const int32_t* num_post_padded, int block_m, void* act,
-                              cudaStream_t stream);
+                              void* ws, size_t ws_bytes, cudaStream_t stream);
 
 /* GEMM2 with the router weight (page §6): for every padded position p with r < T*k,
  *   y[r, :] = topk_w[r] * (act[p] @ W2[e]^T).  Each row r < T*k is written exactly once;
@@ -169,8 +174,10 @@ moe_status_t moe_expert_gemm2(const moe_config_t* cfg, const void* act, const vo
                               const int32_t* num_post_padded, int block_m,
                               const float* topk_w, void* y, cudaStream_t stream);
 
-/* Both expert GEMMs: GEMM1 into ws (act, max_padded*I elements of cfg->dtype), then GEMM2
- * into y[T*k, H]. ws_bytes must be >= max_padded * I * sizeof(dtype). */
+/* Both expert GEMMs: GEMM1 into ws (act, then GEMM1's scratch), then GEMM2 into y[T*k, H].
+ * ws: moe_grouped_swiglu_workspace_size bytes, 256-byte aligned. */
+moe_status_t moe_grouped_swiglu_workspace_size(const moe_config_t* cfg, int block_m,
+                                               size_t* bytes);
 moe_status_t moe_grouped_swiglu(const moe_config_t* cfg, const void* x, const void* W13,
                                 const void* W2, const int32_t* sorted_ids,
                                 const int32_t* expert_ids, const int32_t* num_post_padded,

@@ -36,7 +36,7 @@ class moe_config_t(ctypes.Structure):
 class moe_ws_layout_t(ctypes.Structure):
     _fields_ = [(n, ctypes.c_size_t) for n in ("logits", "topk_ids", "topk_w", "sorted_ids",
                                               "expert_ids", "num_post_padded", "counts",
-                                              "align_scratch", "act", "y", "total")] + \
+                                              "align_scratch", "act", "xs", "y", "total")] + \
                [("block_m", ctypes.c_int), ("max_padded", ctypes.c_int)]
 
 
@@ -58,7 +58,9 @@ def _load():
         "moe_route": (ST, [CFG, P, P, P, P, P, P]),
         "moe_align": (ST, [P, I32, I32, I32, I32, P, P, P, P, P, SZ, P]),
         "moe_align_noalloc": (ST, [P, I32, I32, I32, I32, P, P, P, P, P]),
-        "moe_expert_gemm1": (ST, [CFG, P, P, P, P, P, I32, P, P]),
+        "moe_expert_gemm1_workspace_size": (ST, [CFG, I32, ctypes.POINTER(SZ)]),
+        "moe_expert_gemm1": (ST, [CFG, P, P, P, P, P, I32, P, P, SZ, P]),
+        "moe_grouped_swiglu_workspace_size": (ST, [CFG, I32, ctypes.POINTER(SZ)]),
         "moe_expert_gemm2": (ST, [CFG, P, P, P, P, P, I32, P, P, P]),
         "moe_grouped_swiglu": (ST, [CFG, P, P, P, P, P, P, I32, P, P, P, SZ, P]),
         "moe_combine": (ST, [P, I32, I32, I32, I32, P, P]),
@@ -74,7 +76,8 @@ def _load():
 _lib = _load()
 EXPORTED = ("moe_abi_version", "moe_status_string", "moe_block_m", "moe_max_padded_rows",
             "moe_align_workspace_size", "moe_workspace_layout", "moe_workspace_size",
-            "moe_route", "moe_align", "moe_align_noalloc", "moe_expert_gemm1", "moe_expert_gemm2",
+            "moe_route", "moe_align", "moe_align_noalloc", "moe_expert_gemm1_workspace_size",
+            "moe_expert_gemm1", "moe_grouped_swiglu_workspace_size", "moe_expert_gemm2",
             "moe_grouped_swiglu", "moe_combine", "moe_forward", "moe_device_status")
 
 
@@ -167,11 +170,25 @@ def moe_align_noalloc(topk_ids, T, k, E, block_m, sorted_ids, expert_ids, num_po
         _ptr(num_post_padded), _ptr(counts), _stream(stream)))
 
 
+def moe_expert_gemm1_workspace_size(cfg, block_m) -> int:
+    out = ctypes.c_size_t(0)
+    _check("moe_expert_gemm1_workspace_size",
+           _lib.moe_expert_gemm1_workspace_size(ctypes.byref(cfg), block_m, ctypes.byref(out)))
+    return out.value
+
+
+def moe_grouped_swiglu_workspace_size(cfg, block_m) -> int:
+    out = ctypes.c_size_t(0)
+    _check("moe_grouped_swiglu_workspace_size",
+           _lib.moe_grouped_swiglu_workspace_size(ctypes.byref(cfg), block_m, ctypes.byref(out)))
+    return out.value
+
+
 def moe_expert_gemm1(cfg, x, W13, sorted_ids, expert_ids, num_post_padded, block_m, act,
-                     stream=None):
+                     ws=None, ws_bytes=0, stream=None):
     _check("moe_expert_gemm1", _lib.moe_expert_gemm1(
         ctypes.byref(cfg), _ptr(x), _ptr(W13), _ptr(sorted_ids), _ptr(expert_ids),
-        _ptr(num_post_padded), block_m, _ptr(act), _stream(stream)))
+        _ptr(num_post_padded), block_m, _ptr(act), _ptr(ws), ws_bytes, _stream(stream)))
 
 
 def moe_expert_gemm2(cfg, act, W2, sorted_ids, expert_ids, num_post_padded, block_m, topk_w, y,

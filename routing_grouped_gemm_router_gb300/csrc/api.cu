@@ -50,6 +50,12 @@ static bool block_m_ok(const moe_config_t* c, int block_m) {
   return block_m >= 1 && block_m % block_m_for(c->dtype) == 0 && block_m <= 4096;
 }
 
+// Bytes of GEMM1's scratch: the routed token rows in padded order (bf16 path only).
+static size_t gemm1_scratch_bytes(const moe_config_t* c, int block_m) {
+  if (c->dtype != MOE_BF16) return 0;
+  return align_up(moe_max_padded_rows(c->T, c->k, c->E, block_m) * (size_t)c->H * 2, 256);
+}
+
 }  // namespace moe
 
 using namespace moe;
@@ -113,6 +119,7 @@ moe_status_t moe_workspace_layout(const moe_config_t* c, moe_ws_layout_t* L) {
   L->counts = take((size_t)c->E * 4);
   L->align_scratch = take(align_scratch_bytes(c->T, c->k, c->E, B));
   L->act = take(mp * c->I * es);
+  L->xs = take(gemm1_scratch_bytes(c, B));
   L->y = take(n * c->H * es);
   L->total = off;
   L->block_m = B;
@@ -168,17 +175,29 @@ static moe_status_t check_gemm_args(const moe_config_t* c, int block_m) {
   return MOE_OK;
 }
 
+moe_status_t moe_expert_gemm1_workspace_size(const moe_config_t* c, int block_m, size_t* bytes) {
+  moe_status_t st = check_gemm_args(c, block_m);
+  if (st != MOE_OK) return st;
+  if (!bytes) return MOE_ERR_INVALID_ARG;
+  *bytes = gemm1_scratch_bytes(c, block_m);
+  return MOE_OK;
+}
+
 moe_status_t moe_expert_gemm1(const moe_config_t* c, const void* x, const void* W13,
                               const int32_t* sorted_ids, const int32_t* expert_ids,
-                              const int32_t* npp, int block_m, void* act, cudaStream_t stream) {
+                              const int32_t* npp, int block_m, void* act, void* ws,
+                              size_t ws_bytes, cudaStream_t stream) {
   moe_status_t st = check_gemm_args(c, block_m);
   if (st != MOE_OK) return st;
   if (!x || !W13 || !sorted_ids || !expert_ids || !npp || !act) return MOE_ERR_INVALID_ARG;
   const int mp = (int)moe_max_padded_rows(c->T, c->k, c->E, block_m);
   if (c->dtype == MOE_BF16) {
-    if (!aligned16(x) || !aligned16(W13) || !aligned16(act) || !aligned16(sorted_ids))
-      return MOE_ERR_INVALID_ARG;
-    return launch_gemm1_tc(*c, x, W13, sorted_ids, expert_ids, npp, block_m, mp, act, stream);
+    if (!aligned16(x) || !aligned16(W13) || !aligned16(act)) return MOE_ERR_INVALID_ARG;
+    const size_t need = gemm1_scratch_bytes(c, block_m);
+    if (!ws || ws_bytes < need || ((uintptr_t)ws & 255u)) return MOE_ERR_WORKSPACE;
+    st = launch_gather_rows(x, sorted_ids, npp, c->T * c->k, c->k, c->H * 2, ws, stream);
+    if (st != MOE_OK) return st;
+    return launch_gemm1_tc(*c, ws, W13, sorted_ids, expert_ids, npp, block_m, mp, act, stream);
   }
   return launch_gemm1_simt(*c, (const float*)x, (const float*)W13, sorted_ids, expert_ids, npp,
                            block_m, mp, (float*)act, stream);
@@ -202,18 +221,32 @@ moe_status_t moe_expert_gemm2(const moe_config_t* c, const void* act, const void
                            block_m, mp, topk_w, (float*)y, stream);
 }
 
+moe_status_t moe_grouped_swiglu_workspace_size(const moe_config_t* c, int block_m,
+                                               size_t* bytes) {
+  moe_status_t st = check_gemm_args(c, block_m);
+  if (st != MOE_OK) return st;
+  if (!bytes) return MOE_ERR_INVALID_ARG;
+  const size_t mp = moe_max_padded_rows(c->T, c->k, c->E, block_m);
+  *bytes = align_up(mp * c->I * dtype_size(c->dtype), 256) + gemm1_scratch_bytes(c, block_m);
+  return MOE_OK;
+}
+
 moe_status_t moe_grouped_swiglu(const moe_config_t* c, const void* x, const void* W13,
                                 const void* W2, const int32_t* sorted_ids,
                                 const int32_t* expert_ids, const int32_t* npp, int block_m,
                                 const float* topk_w, void* y, void* ws, size_t ws_bytes,
                                 cudaStream_t stream) {
-  moe_status_t st = check_gemm_args(c, block_m);
+  size_t need = 0;
+  moe_status_t st = moe_grouped_swiglu_workspace_size(c, block_m, &need);
   if (st != MOE_OK) return st;
+  if (!ws || ws_bytes < need || ((uintptr_t)ws & 255u)) return MOE_ERR_WORKSPACE;
   const size_t mp = moe_max_padded_rows(c->T, c->k, c->E, block_m);
-  if (!ws || ws_bytes < mp * c->I * dtype_size(c->dtype)) return MOE_ERR_WORKSPACE;
-  st = moe_expert_gemm1(c, x, W13, sorted_ids, expert_ids, npp, block_m, ws, stream);
+  const size_t act_bytes = align_up(mp * c->I * dtype_size(c->dtype), 256);
+  uint8_t* act = (uint8_t*)ws;
+  st = moe_expert_gemm1(c, x, W13, sorted_ids, expert_ids, npp, block_m, act, act + act_bytes,
+                        ws_bytes - act_bytes, stream);
   if (st != MOE_OK) return st;
-  return moe_expert_gemm2(c, ws, W2, sorted_ids, expert_ids, npp, block_m, topk_w, y, stream);
+  return moe_expert_gemm2(c, act, W2, sorted_ids, expert_ids, npp, block_m, topk_w, y, stream);
 }
 
 moe_status_t moe_combine(const void* y, int T, int k, int H, moe_dtype_t dtype, void* out,
@@ -244,7 +277,8 @@ moe_status_t moe_forward(const moe_config_t* c, const void* x, const void* Wg, c
   if ((st = moe_align(ids, c->T, c->k, c->E, L.block_m, sid, eid, npp, counts,
                       b + L.align_scratch, L.act - L.align_scratch, stream)) != MOE_OK)
     return st;
-  if ((st = moe_expert_gemm1(c, x, W13, sid, eid, npp, L.block_m, b + L.act, stream)) != MOE_OK)
+  if ((st = moe_expert_gemm1(c, x, W13, sid, eid, npp, L.block_m, b + L.act, b + L.xs,
+                             L.y - L.xs, stream)) != MOE_OK)
     return st;
   if ((st = moe_expert_gemm2(c, b + L.act, W2, sid, eid, npp, L.block_m, w, b + L.y, stream)) !=
       MOE_OK)

@@ -52,13 +52,15 @@ moe_status_t launch_gemm2_simt(const moe_config_t& c, const float* act, const fl
                                const int32_t* sid, const int32_t* eid, const int32_t* npp,
                                int block_m, int max_padded, const float* topk_w, float* y,
                                cudaStream_t s);
-moe_status_t launch_gemm1_tc(const moe_config_t& c, const void* x, const void* W13,
+moe_status_t launch_gemm1_tc(const moe_config_t& c, const void* xs, const void* W13,
                              const int32_t* sid, const int32_t* eid, const int32_t* npp,
                              int block_m, int max_padded, void* act, cudaStream_t s);
 moe_status_t launch_gemm2_tc(const moe_config_t& c, const void* act, const void* W2,
                              const int32_t* sid, const int32_t* eid, const int32_t* npp,
                              int block_m, int max_padded, const float* topk_w, void* y,
                              cudaStream_t s);
+moe_status_t launch_gather_rows(const void* x, const int32_t* sid, const int32_t* npp,
+                                int n_rows, int k, int row_bytes, void* xs, cudaStream_t s);
 moe_status_t launch_combine(const void* y, int T, int k, int H, moe_dtype_t dt, void* out,
                             cudaStream_t s);
 

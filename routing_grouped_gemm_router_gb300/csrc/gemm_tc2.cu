@@ -4,28 +4,32 @@
 // GEMM", §6, and the "fused-moe-kernel" skill card, Grouped GEMM Structure):
 //   * every 128-row m-tile belongs to ONE expert, expert_ids[p / block_m];
 //   * tiles at or past num_post_padded (read on the device) are never started;
-//   * GEMM1 gathers the token rows x[sorted_ids[p] / k] itself (no permuted copy of x) and
-//     computes gate and up as the two halves of one N=256 MMA, so the epilogue applies
-//     silu(gate) * up (§6 fused into the GEMM1 epilogue, as the page's exercise suggests);
+//   * GEMM1 multiplies the token rows x[sorted_ids[p] / k], gathered into padded order by a
+//     bandwidth-bound pass just before (gather.cu), and computes gate and up as the two
+//     halves of one N=256 MMA, so the epilogue applies silu(gate) * up (§6 fused into the
+//     GEMM1 epilogue, as the page's exercise suggests);
 //   * GEMM2 reads act in padded order, multiplies by topk_w[r] and scatters each row to
 //     y[r], r = sorted_ids[p]; padding rows are never stored.
 //
-// Design. A cluster of two CTAs on two SMs runs M=256 MMAs: each CTA holds 128 token rows of
-// A, half of the weight panel (B) and its own 128 rows of the fp32 accumulator in TMEM. The
+// Design. A cluster of two CTAs on two SMs runs M=256 MMAs: each CTA holds 128 rows of A,
+// half of the weight panel (B) and its own 128 rows of the fp32 accumulator in TMEM. The
 // weight panel per SM is therefore half of a one-CTA tile's, which halves the shared-memory
 // traffic per MMA and leaves room for 6 pipeline stages. The two m-tiles of a pair come from
 // the SAME expert: an expert with an odd number of m-tiles ends with a pair whose second
-// half is masked (its rows are zero-filled or ignored and never stored).
+// half is masked (its rows are loaded but never stored).
 //
-// Warp roles in each CTA: producers fill a 6-slot ring of 32 KB stages (GEMM1: one warp
-// per slot gathers token rows with 16-byte cp.async straight into the 128-byte-swizzled
-// layout, and one lane per slot loads the CTA's half of the gate/up panel by TMA; GEMM2: one
-// warp issues 2-D/3-D TMA tiles). Both CTAs' TMA copies complete on the LEADER's stage
-// barrier (the pair form of the copy), whose expect_tx counts the bytes of both; GEMM1's
-// gather warps arrive on it too (the peer's remotely). The leader's MMA warp (one lane)
-// issues the pair's MMAs and commits with a multicast to both CTAs (stage free /
-// accumulator ready); four epilogue warps per CTA drain their TMEM rows (double-buffered
-// accumulators, 2 x 256 columns) and release the accumulator on the leader's barrier.
+// Warp roles in each CTA: one producer warp issues the TMA copies of A and of the CTA's half
+// of B into a 6-slot ring of 32 KB stages; both CTAs' copies complete on the LEADER's stage
+// barrier (pair form of the copy), whose expect_tx counts the bytes of both. The leader's MMA
+// warp (one lane) issues the pair's MMAs and commits with a multicast to both CTAs (stage
+// free / accumulator ready); four epilogue warps per CTA drain their TMEM rows
+// (double-buffered accumulators, 2 x 256 columns) and release the accumulator on the
+// leader's barrier.
+//
+// An earlier version gathered A inside this kernel (TMA gather4, then cp.async producer
+// warps); on GB300 the gather kept the MMA pipe half idle, while the separate gather pass
+// costs one extra write and read of the routed rows (about 2.5 % of the Mixtral-shaped
+// layer's bytes).
 //
 // Work order: expert by expert, each weight panel with all of that expert's m-tile pairs
 // back to back (the skill card's L2 grouping at expert granularity), so the pairs running at
@@ -63,22 +67,18 @@ struct Params {
   const float* topk_w;
   void* out;
   int64_t ld_out;
-  const void* x;  // GEMM1 token rows [T, K]
 };
 
 template <int MODE>
 struct Roles {
-  static constexpr int kWps = MODE == kGemm1 ? 2 : 0;  // gather warps per ring slot
-  static constexpr int kProdWarps = MODE == kGemm1 ? kStages * kWps : 1;
-  static constexpr int kMmaWarp = kProdWarps;
-  static constexpr int kEpiWarp0 = kProdWarps + 1;
-  static constexpr int kThreads = (kProdWarps + 5) * 32;
-  // The leader's full barrier of a stage completes on: the leader's expect_tx arrival (for
-  // the TMA bytes of BOTH CTAs, whose copies all complete on this barrier) plus, in GEMM1,
-  // one arrival per gather warp of each CTA (the peer's arrive remotely).
-  static constexpr int kFullArrivals = 1 + 2 * kWps;
-  static constexpr uint32_t kPairTmaBytes =
-      MODE == kGemm1 ? 2u * B_BYTES : 2u * (A_BYTES + B_BYTES);
+  static constexpr int kProdWarps = 1;
+  static constexpr int kMmaWarp = 1;
+  static constexpr int kEpiWarp0 = 2;
+  static constexpr int kThreads = 6 * 32;
+  // The leader's full barrier of a stage completes on the leader's expect_tx arrival, which
+  // counts the TMA bytes of BOTH CTAs: their copies all complete on this one barrier.
+  static constexpr int kFullArrivals = 1;
+  static constexpr uint32_t kPairTmaBytes = 2u * (A_BYTES + B_BYTES);
 };
 
 struct Layout {
@@ -168,7 +168,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Roles<MODE>::kThread
     mbar_init(drain, 1);
     *abort_flag = 0;
     mbar_init_fence();
-    if (MODE == kGemm2) prefetch_tmap(&tmA);
+    prefetch_tmap(&tmA);
     prefetch_tmap(&tmB0);
     if (MODE == kGemm1) prefetch_tmap(&tmB1);
   }
@@ -252,74 +252,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Roles<MODE>::kThread
   const int pair = blockIdx.x >> 1, num_pairs = gridDim.x >> 1;
   const int num_kb = (P.K + BK - 1) / BK;
 
-  if (MODE == kGemm1 && warp < R::kProdWarps) {
-    // ------------------------------------------------------------ GEMM1 gather producers
-    // Warps kWps*s .. kWps*s+kWps-1 own ring slot s and fill every kStages-th k-block of the
-    // pair's work sequence. Each warp copies 128/kWps of the CTA's 128 token rows: lane l
-    // moves 16-byte chunk l%8 of rows base + 4*i + l/8, so every warp instruction moves four
-    // whole 128-byte rows; padding rows and a masked half are zero-filled without a memory
-    // read.
-    // The warp waits for its own copies, fences the async proxy, and lane 0 arrives.
-    constexpr int kWps = R::kWps > 0 ? R::kWps : 1;
-    constexpr int NR = 32 / kWps;  // 4-row groups per warp
-    const int slot = warp / kWps;
-    const int rbase = (warp % kWps) * (BM / kWps);
-    const int sub = lane & 7, rsub = lane >> 3;
-    const char* xb = (const char*)P.x;
-    const uint32_t a = su32(sA + slot * A_BYTES);
-    uint8_t* b = sB + slot * B_BYTES;
-    const CUtensorMap* tmW = rank ? &tmB1 : &tmB0;  // leader: gate rows, peer: up rows
-    const uint32_t full_leader = cluster_addr(&full[slot], 0);
-    int g = 0;
-    bool ok = true;
-    for (int w = pair; w < total && ok; w += num_pairs) {
-      int m0, n, e;
-      bool live1;
-      item_of(w, P.n_tiles, tb, m0, n, e, live1);
-      const bool live = leader || live1;
-      const int kb0 = ((slot - g) % kStages + kStages) % kStages;
-      if (kb0 < num_kb) {
-        int tok[NR];
-#pragma unroll
-        for (int i = 0; i < NR; ++i) {
-          const int r = live ? P.sid[(m0 + (int)rank) * BM + rbase + 4 * i + rsub] : P.n_rows;
-          tok[i] = r < P.n_rows ? r / P.k : -1;
-        }
-        for (int kb = kb0; kb < num_kb; kb += kStages) {
-          const uint32_t use = (uint32_t)((g + kb) / kStages);
-          int okw = 1;
-          if (lane == 0) okw = wait_bounded(&empty[slot], (use & 1u) ^ 1u, abort_flag, status);
-          okw = __shfl_sync(0xffffffffu, okw, 0);
-          if (!okw) { ok = false; break; }
-          if (lane == 0 && rbase == 0) {
-            if (leader) mbar_expect_tx(&full[slot], R::kPairTmaBytes);
-            tma_3d_pair(b, tmW, full_leader, kb * BK, n * 128, e);
-          }
-          const int col = kb * BK + sub * 8;
-          const bool col_ok = col < P.K;
-          const int64_t coff = (int64_t)(col_ok ? col : 0) * 2;
-#pragma unroll
-          for (int i = 0; i < NR; ++i) {
-            const int row = rbase + 4 * i + rsub;
-            cp_async16(a + row * 128 + ((sub ^ (row & 7)) << 4),
-                       xb + (int64_t)(tok[i] >= 0 ? tok[i] : 0) * P.K * 2 + coff,
-                       (col_ok && tok[i] >= 0) ? 16u : 0u);
-          }
-          cp_async_commit();
-          cp_async_wait<0>();
-          fence_proxy_async_smem();
-          __syncwarp();
-          if (lane == 0) {
-            if (leader) mbar_arrive(&full[slot]);
-            else mbar_arrive_cta(&full[slot], 0);
-          }
-        }
-      }
-      g += num_kb;
-    }
-    cp_async_wait<0>();
-  } else if (MODE == kGemm2 && warp == 0) {
-    // ------------------------------------------------------------ GEMM2 TMA producer
+  if (warp == 0) {
+    // ------------------------------------------------------------ TMA producer
     if (lane == 0) {
       int g = 0;
       for (int w = pair; w < total; w += num_pairs) {
@@ -336,7 +270,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Roles<MODE>::kThread
           const uint32_t fl = cluster_addr(&full[s], 0);
           if (leader) mbar_expect_tx(&full[s], R::kPairTmaBytes);
           tma_2d_pair(sA + s * A_BYTES, &tmA, fl, kb * BK, (m0 + (int)rank) * BM);
-          tma_3d_pair(sB + s * B_BYTES, &tmB0, fl, kb * BK, n * 256 + (int)rank * 128, e);
+          if (MODE == kGemm1)  // leader: gate rows of panel n, peer: up rows
+            tma_3d_pair(sB + s * B_BYTES, rank ? &tmB1 : &tmB0, fl, kb * BK, n * 128, e);
+          else                 // leader: rows n*256 .. +127 of W2[e], peer: the next 128
+            tma_3d_pair(sB + s * B_BYTES, &tmB0, fl, kb * BK, n * 256 + (int)rank * 128, e);
         }
         if (!ok) break;
       }
@@ -527,13 +464,18 @@ int grouped_status_read(int reset) {
   return v;
 }
 
-moe_status_t launch_gemm1_tc(const moe_config_t& c, const void* x, const void* W13,
+moe_status_t launch_gemm1_tc(const moe_config_t& c, const void* xs, const void* W13,
                              const int32_t* sid, const int32_t* eid, const int32_t* npp,
                              int block_m, int max_padded, void* act, cudaStream_t s) {
   using namespace tc2;
   if (max_padded / BM > kMaxTiles) return MOE_ERR_UNSUPPORTED;
-  CUtensorMap mG, mU;
+  CUtensorMap mA, mG, mU;
   const uint64_t H = c.H, I = c.I, E = c.E;
+  {
+    uint64_t d[2] = {H, (uint64_t)max_padded}, st[1] = {H};
+    uint32_t box[2] = {BK, BM};
+    if (!make_map(&mA, xs, 2, d, st, box, false)) return MOE_ERR_CUDA;
+  }
   {
     uint64_t d[3] = {H, I, E}, st[2] = {H, 2 * I * H};
     uint32_t box[3] = {BK, 128, 1};
@@ -553,8 +495,7 @@ moe_status_t launch_gemm1_tc(const moe_config_t& c, const void* x, const void* W
   P.npp = npp;
   P.out = act;
   P.ld_out = c.I;
-  P.x = x;
-  return launch<kGemm1>(mG, mG, mU, P, max_items_for(max_padded, P.n_rows, c.E, P.n_tiles), s);
+  return launch<kGemm1>(mA, mG, mU, P, max_items_for(max_padded, P.n_rows, c.E, P.n_tiles), s);
 }
 
 moe_status_t launch_gemm2_tc(const moe_config_t& c, const void* act, const void* W2,

@@ -321,12 +321,15 @@ def test_separate_entry_points_match_forward(L):
     out = torch.empty(T, H, dtype=torch.bfloat16, device=DEV)
     L.moe_route(cfg, inp.x, inp.Wg, lg, ids, w)
     L.moe_align(ids, T, k, E, B, sid, eid, npp)
-    L.moe_expert_gemm1(cfg, inp.x, inp.W13, sid, eid, npp, B, act)
+    g1b = L.moe_expert_gemm1_workspace_size(cfg, B)
+    g1ws = torch.empty(max(g1b, 1), dtype=torch.uint8, device=DEV)
+    L.moe_expert_gemm1(cfg, inp.x, inp.W13, sid, eid, npp, B, act, g1ws, g1b)
     L.moe_expert_gemm2(cfg, act, inp.W2, sid, eid, npp, B, w, y)
     L.moe_combine(y, T, k, H, L.MOE_BF16, out)
     torch.cuda.synchronize()
     assert torch.equal(out, out_fwd)
-    ws = torch.empty(mp * I * 2, dtype=torch.uint8, device=DEV)
+    wsb = L.moe_grouped_swiglu_workspace_size(cfg, B)
+    ws = torch.empty(wsb, dtype=torch.uint8, device=DEV)
     y2 = torch.empty_like(y)
     L.moe_grouped_swiglu(cfg, inp.x, inp.W13, inp.W2, sid, eid, npp, B, w, y2, ws, ws.numel())
     torch.cuda.synchronize()
@@ -360,7 +363,9 @@ def test_tile_boundaries_and_sentinels(L, dtype):
     y = torch.full((T * k, H), float("nan"), dtype=tdt, device=DEV)
     out = torch.empty(T, H, dtype=tdt, device=DEV)
     L.moe_align(idsd, T, k, E, B, sid, eid, npp)
-    L.moe_expert_gemm1(cfg, xd, W13d, sid, eid, npp, B, act)
+    g1b = L.moe_expert_gemm1_workspace_size(cfg, B)
+    g1ws = torch.empty(max(g1b, 1), dtype=torch.uint8, device=DEV)
+    L.moe_expert_gemm1(cfg, xd, W13d, sid, eid, npp, B, act, g1ws, g1b)
     L.moe_expert_gemm2(cfg, act, W2d, sid, eid, npp, B, wd, y)
     L.moe_combine(y, T, k, H, cfg.dtype, out)
     torch.cuda.synchronize()
@@ -392,7 +397,7 @@ def test_all_tokens_to_one_expert(L):
     npp = torch.empty(1, dtype=torch.int32, device=DEV)
     y = torch.empty(T * k, H, dtype=torch.bfloat16, device=DEV)
     out = torch.empty(T, H, dtype=torch.bfloat16, device=DEV)
-    ws = torch.empty(mp * I * 2, dtype=torch.uint8, device=DEV)
+    ws = torch.empty(L.moe_grouped_swiglu_workspace_size(cfg, B), dtype=torch.uint8, device=DEV)
     xd, W13d, W2d = x.to(DEV), W13.to(DEV), W2.to(DEV)
     L.moe_align(ids.to(DEV), T, k, E, B, sid, eid, npp)
     L.moe_grouped_swiglu(cfg, xd, W13d, W2d, sid, eid, npp, B, w.to(DEV), y, ws, ws.numel())
