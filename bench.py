@@ -248,6 +248,7 @@ def run_ours(args, wl):
     out = torch.empty(T, H, dtype=inp.x.dtype, device=dev)
     stream = torch.cuda.current_stream(dev)
     sh = stream.cuda_stream
+    gathered = wl.dtype == "bf16"  # bf16 GEMM1 = row gather + tensor-core GEMM, timed apart
 
     def step(ev=None):
         # The same kernels moe_forward enqueues, called stage by stage so that CUDA events
@@ -261,17 +262,27 @@ def run_ours(args, wl):
                     p["num_post_padded"], p["counts"], p["align_scratch"], ws_align, sh)
         if ev is not None:
             ev[2].record(stream)
-        L.moe_expert_gemm1(cfg, inp.x, inp.W13, p["sorted_ids"], p["expert_ids"],
-                           p["num_post_padded"], B, p["act"], p["xs"], ws_xs, sh)
+        if gathered:
+            L.moe_gather_rows(inp.x, p["sorted_ids"], p["num_post_padded"], T, k, H, cfg.dtype,
+                              p["xs"], sh)
+            if ev is not None:
+                ev[3].record(stream)
+            L.moe_expert_gemm1_gathered(cfg, p["xs"], inp.W13, p["sorted_ids"], p["expert_ids"],
+                                        p["num_post_padded"], B, p["act"], sh)
+        else:
+            if ev is not None:
+                ev[3].record(stream)
+            L.moe_expert_gemm1(cfg, inp.x, inp.W13, p["sorted_ids"], p["expert_ids"],
+                               p["num_post_padded"], B, p["act"], p["xs"], ws_xs, sh)
         if ev is not None:
-            ev[3].record(stream)
+            ev[4].record(stream)
         L.moe_expert_gemm2(cfg, p["act"], inp.W2, p["sorted_ids"], p["expert_ids"],
                            p["num_post_padded"], B, p["topk_w"], p["y"], sh)
         if ev is not None:
-            ev[4].record(stream)
+            ev[5].record(stream)
         L.moe_combine(p["y"], T, k, H, cfg.dtype, out, sh)
         if ev is not None:
-            ev[5].record(stream)
+            ev[6].record(stream)
 
     # router GEMM + top-k, align (one kernel up to 4096 rows, else three), row gather + GEMM1
     # (bf16), GEMM2, combine
@@ -285,7 +296,7 @@ def run_ours(args, wl):
     active = int((counts > 0).sum())
 
     # ---- device-timed steps (inputs resident in HBM; expert weights larger than L2)
-    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(6)] for _ in range(args.steps)]
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(7)] for _ in range(args.steps)]
     sampler = ClockSampler(local)
     sampler.start()
     time.sleep(0.3)
@@ -304,7 +315,7 @@ def run_ours(args, wl):
     clocks = sampler.stop()
     ms = max_over_ranks(dist, t_start.elapsed_time(t_end) / args.steps, dev)
     stage = {n: statistics.mean(e[i].elapsed_time(e[i + 1]) for e in evs)
-             for i, n in enumerate(("route", "align", "gemm1", "gemm2", "combine"))}
+             for i, n in enumerate(("route", "align", "gather", "gemm1", "gemm2", "combine"))}
 
     # ---- end to end through the public API: H2D of x, moe_forward, D2H of out
     x_host = inp.x.cpu().pin_memory()
@@ -333,7 +344,7 @@ def run_ours(args, wl):
     value = flops * world / (ms * 1e-3) / 1e12
     e2e_val = flops * world / (e2e_ms * 1e-3) / 1e12
     hbm, bf16_burst, bf16_sus, peak_src = peaks()
-    src = os.path.join(ROOT, "routing_grouped_gemm_router_gb300", "csrc", "gemm_tc.cu")
+    src = os.path.join(ROOT, "routing_grouped_gemm_router_gb300", "csrc", "gemm_tc2.cu")
     if is_decode(wl):
         # decode is HBM-bound: GEMM1 streams the gate/up weights of every active expert
         w_bytes = active * 2 * H * I * 2

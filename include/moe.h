@@ -166,6 +166,21 @@ moe_status_t moe_expert_gemm1(const moe_config_t* cfg, const void* x, const void
                               const int32_t* num_post_padded, int block_m, void* act,
                               void* ws, size_t ws_bytes, cudaStream_t stream);
 
+/* The two halves of the bf16 moe_expert_gemm1, for callers that keep the routed rows:
+ * moe_gather_rows writes xs[p, :] = x[sorted_ids[p] / k, :] for every p < num_post_padded
+ * with sorted_ids[p] < T*k (padding rows untouched; xs is [max_padded, H] of dtype, 16-byte
+ * aligned); moe_expert_gemm1_gathered runs GEMM1 + SwiGLU on those rows (bf16 only, else
+ * MOE_ERR_UNSUPPORTED). Page §2 lists both feeds, a permuted copy and an in-GEMM gather;
+ * this pair is the permuted-copy feed with the permutation taken from sorted_ids. */
+moe_status_t moe_gather_rows(const void* x, const int32_t* sorted_ids,
+                             const int32_t* num_post_padded, int T, int k, int H,
+                             moe_dtype_t dtype, void* xs, cudaStream_t stream);
+moe_status_t moe_expert_gemm1_gathered(const moe_config_t* cfg, const void* xs,
+                                       const void* W13, const int32_t* sorted_ids,
+                                       const int32_t* expert_ids,
+                                       const int32_t* num_post_padded, int block_m, void* act,
+                                       cudaStream_t stream);
+
 /* GEMM2 with the router weight (page §6): for every padded position p with r < T*k,
  *   y[r, :] = topk_w[r] * (act[p] @ W2[e]^T).  Each row r < T*k is written exactly once;
  * padding rows are never written. */

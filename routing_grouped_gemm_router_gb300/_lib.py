@@ -60,6 +60,8 @@ def _load():
         "moe_align_noalloc": (ST, [P, I32, I32, I32, I32, P, P, P, P, P]),
         "moe_expert_gemm1_workspace_size": (ST, [CFG, I32, ctypes.POINTER(SZ)]),
         "moe_expert_gemm1": (ST, [CFG, P, P, P, P, P, I32, P, P, SZ, P]),
+        "moe_gather_rows": (ST, [P, P, P, I32, I32, I32, I32, P, P]),
+        "moe_expert_gemm1_gathered": (ST, [CFG, P, P, P, P, P, I32, P, P]),
         "moe_grouped_swiglu_workspace_size": (ST, [CFG, I32, ctypes.POINTER(SZ)]),
         "moe_expert_gemm2": (ST, [CFG, P, P, P, P, P, I32, P, P, P]),
         "moe_grouped_swiglu": (ST, [CFG, P, P, P, P, P, P, I32, P, P, P, SZ, P]),
@@ -77,7 +79,8 @@ _lib = _load()
 EXPORTED = ("moe_abi_version", "moe_status_string", "moe_block_m", "moe_max_padded_rows",
             "moe_align_workspace_size", "moe_workspace_layout", "moe_workspace_size",
             "moe_route", "moe_align", "moe_align_noalloc", "moe_expert_gemm1_workspace_size",
-            "moe_expert_gemm1", "moe_grouped_swiglu_workspace_size", "moe_expert_gemm2",
+            "moe_expert_gemm1", "moe_gather_rows", "moe_expert_gemm1_gathered",
+            "moe_grouped_swiglu_workspace_size", "moe_expert_gemm2",
             "moe_grouped_swiglu", "moe_combine", "moe_forward", "moe_device_status")
 
 
@@ -189,6 +192,19 @@ def moe_expert_gemm1(cfg, x, W13, sorted_ids, expert_ids, num_post_padded, block
     _check("moe_expert_gemm1", _lib.moe_expert_gemm1(
         ctypes.byref(cfg), _ptr(x), _ptr(W13), _ptr(sorted_ids), _ptr(expert_ids),
         _ptr(num_post_padded), block_m, _ptr(act), _ptr(ws), ws_bytes, _stream(stream)))
+
+
+def moe_gather_rows(x, sorted_ids, num_post_padded, T, k, H, dtype, xs, stream=None):
+    _check("moe_gather_rows", _lib.moe_gather_rows(
+        _ptr(x), _ptr(sorted_ids), _ptr(num_post_padded), T, k, H, dtype, _ptr(xs),
+        _stream(stream)))
+
+
+def moe_expert_gemm1_gathered(cfg, xs, W13, sorted_ids, expert_ids, num_post_padded, block_m,
+                              act, stream=None):
+    _check("moe_expert_gemm1_gathered", _lib.moe_expert_gemm1_gathered(
+        ctypes.byref(cfg), _ptr(xs), _ptr(W13), _ptr(sorted_ids), _ptr(expert_ids),
+        _ptr(num_post_padded), block_m, _ptr(act), _stream(stream)))
 
 
 def moe_expert_gemm2(cfg, act, W2, sorted_ids, expert_ids, num_post_padded, block_m, topk_w, y,

@@ -183,6 +183,30 @@ moe_status_t moe_expert_gemm1_workspace_size(const moe_config_t* c, int block_m,
   return MOE_OK;
 }
 
+moe_status_t moe_gather_rows(const void* x, const int32_t* sorted_ids,
+                             const int32_t* num_post_padded, int T, int k, int H,
+                             moe_dtype_t dtype, void* xs, cudaStream_t stream) {
+  if (!x || !sorted_ids || !num_post_padded || !xs || T < 1 || k < 1 || H < 8 || H % 8)
+    return MOE_ERR_INVALID_ARG;
+  if (dtype != MOE_F32 && dtype != MOE_BF16) return MOE_ERR_INVALID_ARG;
+  if (!aligned16(x) || !aligned16(xs)) return MOE_ERR_INVALID_ARG;
+  return launch_gather_rows(x, sorted_ids, num_post_padded, T * k, k,
+                            H * (int)dtype_size(dtype), xs, stream);
+}
+
+moe_status_t moe_expert_gemm1_gathered(const moe_config_t* c, const void* xs, const void* W13,
+                                       const int32_t* sorted_ids, const int32_t* expert_ids,
+                                       const int32_t* npp, int block_m, void* act,
+                                       cudaStream_t stream) {
+  moe_status_t st = check_gemm_args(c, block_m);
+  if (st != MOE_OK) return st;
+  if (c->dtype != MOE_BF16) return MOE_ERR_UNSUPPORTED;
+  if (!xs || !W13 || !sorted_ids || !expert_ids || !npp || !act) return MOE_ERR_INVALID_ARG;
+  if (!aligned16(xs) || !aligned16(W13) || !aligned16(act)) return MOE_ERR_INVALID_ARG;
+  const int mp = (int)moe_max_padded_rows(c->T, c->k, c->E, block_m);
+  return launch_gemm1_tc(*c, xs, W13, sorted_ids, expert_ids, npp, block_m, mp, act, stream);
+}
+
 moe_status_t moe_expert_gemm1(const moe_config_t* c, const void* x, const void* W13,
                               const int32_t* sorted_ids, const int32_t* expert_ids,
                               const int32_t* npp, int block_m, void* act, void* ws,
@@ -192,12 +216,12 @@ moe_status_t moe_expert_gemm1(const moe_config_t* c, const void* x, const void* 
   if (!x || !W13 || !sorted_ids || !expert_ids || !npp || !act) return MOE_ERR_INVALID_ARG;
   const int mp = (int)moe_max_padded_rows(c->T, c->k, c->E, block_m);
   if (c->dtype == MOE_BF16) {
-    if (!aligned16(x) || !aligned16(W13) || !aligned16(act)) return MOE_ERR_INVALID_ARG;
     const size_t need = gemm1_scratch_bytes(c, block_m);
     if (!ws || ws_bytes < need || ((uintptr_t)ws & 255u)) return MOE_ERR_WORKSPACE;
-    st = launch_gather_rows(x, sorted_ids, npp, c->T * c->k, c->k, c->H * 2, ws, stream);
+    st = moe_gather_rows(x, sorted_ids, npp, c->T, c->k, c->H, c->dtype, ws, stream);
     if (st != MOE_OK) return st;
-    return launch_gemm1_tc(*c, ws, W13, sorted_ids, expert_ids, npp, block_m, mp, act, stream);
+    return moe_expert_gemm1_gathered(c, ws, W13, sorted_ids, expert_ids, npp, block_m, act,
+                                     stream);
   }
   return launch_gemm1_simt(*c, (const float*)x, (const float*)W13, sorted_ids, expert_ids, npp,
                            block_m, mp, (float*)act, stream);

@@ -328,6 +328,15 @@ def test_separate_entry_points_match_forward(L):
     L.moe_combine(y, T, k, H, L.MOE_BF16, out)
     torch.cuda.synchronize()
     assert torch.equal(out, out_fwd)
+    # the bf16 GEMM1 split in its two public halves gives the same act
+    xs = torch.empty(mp, H, dtype=torch.bfloat16, device=DEV)
+    act2 = torch.empty_like(act)
+    L.moe_gather_rows(inp.x, sid, npp, T, k, H, L.MOE_BF16, xs)
+    L.moe_expert_gemm1_gathered(cfg, xs, inp.W13, sid, eid, npp, B, act2)
+    torch.cuda.synchronize()
+    real = (sid < T * k).nonzero().flatten()
+    assert torch.equal(act2[real], act[real])
+    assert torch.equal(xs[real], inp.x[(sid[real] // k).long()])
     wsb = L.moe_grouped_swiglu_workspace_size(cfg, B)
     ws = torch.empty(wsb, dtype=torch.uint8, device=DEV)
     y2 = torch.empty_like(y)
