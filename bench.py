@@ -42,6 +42,8 @@ def parse():
     p.add_argument("--impl", default="ours", choices=["ours", "reference"])
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--cpu-sample-tokens", type=int, default=0)
+    p.add_argument("--no-graph", action="store_true",
+                   help="time eager launches instead of CUDA-graph replays of the step")
     p.add_argument("--tokens", type=int, default=0,
                    help="override T of the workload (smaller cases for profiling)")
     return p.parse_args()
@@ -250,7 +252,7 @@ def run_ours(args, wl):
     sh = stream.cuda_stream
     gathered = wl.dtype == "bf16"  # bf16 GEMM1 = row gather + tensor-core GEMM, timed apart
 
-    def step(ev=None):
+    def step(ev=None, sh=sh):
         # The same kernels moe_forward enqueues, called stage by stage so that CUDA events
         # between them give each stage's device time.
         if ev is not None:
@@ -295,8 +297,21 @@ def run_ours(args, wl):
     counts = ws[lay.counts:lay.counts + 4 * E].view(torch.int32).cpu()
     active = int((counts > 0).sum())
 
+    # ---- the step captured once in a CUDA graph (no host work or launch gaps in the timing)
+    graph = None
+    if not args.no_graph:
+        cap = torch.cuda.Stream(dev)
+        cap.wait_stream(stream)
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.stream(cap):
+            with torch.cuda.graph(graph, stream=cap):
+                step(sh=cap.cuda_stream)
+        stream.wait_stream(cap)
+        for _ in range(3):
+            graph.replay()
+        torch.cuda.synchronize()
+
     # ---- device-timed steps (inputs resident in HBM; expert weights larger than L2)
-    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(7)] for _ in range(args.steps)]
     sampler = ClockSampler(local)
     sampler.start()
     time.sleep(0.3)
@@ -307,13 +322,21 @@ def run_ours(args, wl):
     t_end = torch.cuda.Event(enable_timing=True)
     t_start.record(stream)
     for i in range(args.steps):
-        step(evs[i])
+        if graph is not None:
+            graph.replay()
+        else:
+            step()
     t_end.record(stream)
     torch.cuda.synchronize()
     if dist is not None:
         dist.barrier()
-    clocks = sampler.stop()
     ms = max_over_ranks(dist, t_start.elapsed_time(t_end) / args.steps, dev)
+    # per-stage device times: the same steps launched eagerly with CUDA events between stages
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(7)] for _ in range(args.steps)]
+    for i in range(args.steps):
+        step(evs[i])
+    torch.cuda.synchronize()
+    clocks = sampler.stop()
     stage = {n: statistics.mean(e[i].elapsed_time(e[i + 1]) for e in evs)
              for i, n in enumerate(("route", "align", "gather", "gemm1", "gemm2", "combine"))}
 
@@ -364,6 +387,7 @@ def run_ours(args, wl):
 
     line = {"metric": METRIC, "value": value, "unit": "TFLOPS", "n_gpus": world,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
+            "timing": "CUDA-graph replays of the step" if graph is not None else "eager launches",
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
             "dtype": "bf16" if wl.dtype == "bf16" else "f32",
             "data": "synthetic (seeded N(0,1) tokens, N(0,1/fan_in) weights, random init)",

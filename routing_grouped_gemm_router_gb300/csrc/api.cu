@@ -140,8 +140,8 @@ moe_status_t moe_route(const moe_config_t* c, const void* x, const void* Wg, flo
   moe_status_t st = check_cfg(c);
   if (st != MOE_OK) return st;
   if (!x || !Wg || !logits || !topk_ids || !topk_w) return MOE_ERR_INVALID_ARG;
-  // Few tokens (decode): spread the router rows over many SMs on CUDA cores. Otherwise
-  // bf16 runs on the tensor cores (E <= 256 fits one MMA N), fp32 on FFMA tiles.
+  // Few tokens (decode): CUDA cores, router rows spread over many SMs. Otherwise bf16 runs
+  // on the tensor cores (E <= 256 fits one MMA N), fp32 on FFMA tiles.
   if (c->dtype == MOE_BF16 && (!aligned16(x) || !aligned16(Wg))) return MOE_ERR_INVALID_ARG;
   if (c->T <= kFewTokens && aligned16(x) && aligned16(Wg))
     st = launch_router_few_tokens(*c, x, Wg, logits, stream);

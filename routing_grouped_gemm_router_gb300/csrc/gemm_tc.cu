@@ -1,7 +1,8 @@
 // gemm_tc.cu — the router GEMM on the tensor cores: logits[T, E] = x[T, H] . Wg[E, H]^T,
 // bf16 inputs, fp32 accumulation in TMEM ("Mixture-of-Experts Kernels: Routing,
 // Permutation, and Grouped GEMM", §3: logits = x @ w_gate.T, the scores every router starts
-// from). E <= 256 fits one MMA N, so a 128-token tile is one tcgen05.mma accumulator.
+// from). E <= 256 fits one MMA N; with few 128-token tiles, E is split into BN-wide tiles so
+// every SM gets one.
 //
 // One persistent CTA per SM (up to ceil(T/128) CTAs) with three warp roles: warp 0 issues
 // TMA copies of x and Wg k-blocks into a 4-stage shared-memory ring, warp 1 (one lane)
@@ -23,7 +24,7 @@ constexpr int kStages = 4;
 
 struct RouterParams {
   int T, E, H;
-  int m_tiles;
+  int m_tiles, n_tiles;  // 128-token tiles x BN-expert tiles
   float* logits;
 };
 
@@ -87,7 +88,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     // ------------------------------------------------------------ TMA producer
     int stage = 0;
     uint32_t phase = 0;
-    for (int m = blockIdx.x; m < P.m_tiles; m += gridDim.x) {
+    for (int w = blockIdx.x; w < P.m_tiles * P.n_tiles; w += gridDim.x) {
+      const int m = w / P.n_tiles, n = w - m * P.n_tiles;
       for (int kb = 0; kb < num_kb; ++kb) {
         int ok = 1;
         if (lane == 0) ok = wait_bounded(&empty[stage], phase ^ 1u, abort_flag, status);
@@ -96,7 +98,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (lane == 0) {
           mbar_expect_tx(&full[stage], A_BYTES + B_BYTES);
           tma_2d(sA + stage * A_BYTES, &tmX, &full[stage], kb * BK, m * BM);
-          tma_2d(sB + stage * B_BYTES, &tmW, &full[stage], kb * BK, 0);
+          tma_2d(sB + stage * B_BYTES, &tmW, &full[stage], kb * BK, n * BN);
         }
         __syncwarp();
         if (++stage == kStages) { stage = 0; phase ^= 1u; }
@@ -109,7 +111,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       int stage = 0, acc = 0;
       uint32_t phase = 0, acc_phase = 0;
       bool ok = true, issued = false;
-      for (int m = blockIdx.x; m < P.m_tiles && ok; m += gridDim.x) {
+      for (int w = blockIdx.x; w < P.m_tiles * P.n_tiles && ok; w += gridDim.x) {
         if (!wait_bounded(&tempty[acc], acc_phase ^ 1u, abort_flag, status)) break;
         tc_fence_after();
         const uint32_t d = tmem_base + (uint32_t)(acc * BN);
@@ -142,7 +144,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int q = warp & 3;  // TMEM lane quarter this warp may access
     int acc = 0;
     uint32_t acc_phase = 0;
-    for (int m = blockIdx.x; m < P.m_tiles; m += gridDim.x) {
+    for (int w = blockIdx.x; w < P.m_tiles * P.n_tiles; w += gridDim.x) {
+      const int m = w / P.n_tiles, n = w - m * P.n_tiles;
       int ok = 1;
       if (lane == 0) ok = wait_bounded(&tfull[acc], acc_phase, abort_flag, status);
       ok = __shfl_sync(0xffffffffu, ok, 0);
@@ -150,7 +153,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       tc_fence_after();
       const uint32_t tbase = tmem_base + (uint32_t)(acc * BN) + ((uint32_t)(q * 32) << 16);
       const int t = m * BM + q * 32 + lane;
-      float* dst = P.logits + (int64_t)t * P.E;
+      float* dst = P.logits + (int64_t)t * P.E + n * BN;
+      const int ncols = P.E - n * BN;
 #pragma unroll 1
       for (int c = 0; c < BN / 32; ++c) {
         uint32_t v32[32];
@@ -159,7 +163,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (t < P.T) {
 #pragma unroll
           for (int j = 0; j < 32; ++j)
-            if (c * 32 + j < P.E) dst[c * 32 + j] = __uint_as_float(v32[j]);
+            if (c * 32 + j < ncols) dst[c * 32 + j] = __uint_as_float(v32[j]);
         }
       }
       tc_fence_before();
@@ -196,7 +200,7 @@ static moe_status_t launch_router(const CUtensorMap& mx, const CUtensorMap& mw,
       return MOE_ERR_CUDA;
     configured_dev = dev;
   }
-  const int grid = std::min(num_sms(), P.m_tiles);
+  const int grid = std::min(num_sms(), P.m_tiles * P.n_tiles);
   kern<<<grid, kThreads, smem, s>>>(mx, mw, P);
   return last_launch_status();
 }
@@ -216,7 +220,12 @@ int router_status_read(int reset) {
 moe_status_t launch_router_tc(const moe_config_t& c, const void* x, const void* Wg,
                               float* logits, cudaStream_t s) {
   using namespace tc;
-  const int bn = (c.E + 31) / 32 * 32;
+  // Expert tile BN (multiple of 32, <= 256): the smallest split of E that still gives every
+  // SM a tile, when there are few 128-token tiles.
+  const int m_tiles = ceil_div(c.T, BM);
+  int bn = (c.E + 31) / 32 * 32;
+  while (bn > 32 && m_tiles * ceil_div(c.E, bn) < num_sms()) bn = (bn / 2 + 31) / 32 * 32;
+  if (bn > 256) return MOE_ERR_UNSUPPORTED;
   CUtensorMap mx, mw;
   const uint64_t H = c.H, E = c.E, T = c.T;
   {
@@ -229,7 +238,7 @@ moe_status_t launch_router_tc(const moe_config_t& c, const void* x, const void* 
     uint32_t box[2] = {BK, (uint32_t)bn};
     if (!make_map(&mw, Wg, 2, d, st, box, true)) return MOE_ERR_CUDA;
   }
-  RouterParams P{c.T, c.E, c.H, ceil_div(c.T, BM), logits};
+  RouterParams P{c.T, c.E, c.H, m_tiles, ceil_div(c.E, bn), logits};
   switch (bn) {
     case 32: return launch_router<32>(mx, mw, P, s);
     case 64: return launch_router<64>(mx, mw, P, s);
