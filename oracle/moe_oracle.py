@@ -247,13 +247,26 @@ def _expert(W, e):
     return bf16_bits_to_f64(a) if a.dtype == np.uint16 else f64(a)
 
 
-def moe_loop(x, ids, w, W13, W2, tokens=None) -> np.ndarray:
+def apply_expert_map(expert_ids, expert_map):
+    """[P2 §10, "Try this": expert parallelism] relabel each tile of the align table with the
+    local weight slot of its expert, or -1 when the expert is not on this device (its tiles
+    are skipped)."""
+    eid = np.asarray(expert_ids, dtype=np.int64).copy()
+    m = np.asarray(expert_map, dtype=np.int64)
+    valid = eid >= 0
+    eid[valid] = m[eid[valid]]
+    return eid
+
+
+def moe_loop(x, ids, w, W13, W2, tokens=None, expert_map=None) -> np.ndarray:
     """Version A [P2 §3 moe_loop]: for each expert, gather the (token, slot) pairs routed
     to it in ascending flat row, run the expert once on those token rows, and add the
     weighted outputs back at their tokens. Experts with no rows are skipped.
 
     ``tokens`` restricts the computation to a subset of tokens (rows of the result
     follow that subset's order); the result for a token depends only on that token.
+    ``expert_map`` (expert parallelism): expert e uses weight slot expert_map[e], and an
+    expert mapped to -1 lives on another device and contributes nothing here.
     """
     x = f64(x)
     ids = np.asarray(ids, dtype=np.int64)
@@ -264,12 +277,15 @@ def moe_loop(x, ids, w, W13, W2, tokens=None) -> np.ndarray:
     sub_ids, sub_w = ids[tokens], w[tokens]
     H = x.shape[1]
     out = np.zeros((tokens.size, H))
-    E = W13.shape[0]
+    E = int(max(W13.shape[0], sub_ids.max() + 1 if sub_ids.size else 0))
     for e in range(E):
         t_local, slot = np.nonzero(sub_ids == e)
         if t_local.size == 0:
             continue
-        ye = expert_ffn(x[tokens[t_local]], _expert(W13, e), _expert(W2, e))
+        we = e if expert_map is None else int(expert_map[e])
+        if we < 0:
+            continue
+        ye = expert_ffn(x[tokens[t_local]], _expert(W13, we), _expert(W2, we))
         np.add.at(out, t_local, ye * sub_w[t_local, slot][:, None])
     return out
 

@@ -311,6 +311,44 @@ def test_margins_flag_near_ties():
     assert O.selection_margins(l + np.array([[0, 1, 0, 0]]), 1)[0] > 1e-4
 
 
+# ----------------------------------------------------------------- expert parallelism
+
+def test_expert_map_remote_equals_zeroed_down_projection():
+    """A remote expert (map -1) contributes nothing: the same as zeroing its W2."""
+    rng = np.random.default_rng(8)
+    x, Wg, W13, W2 = _rand_layer(rng, E=6)
+    out, ids, w, _ = O.moe_forward(x, Wg, W13, W2, 3)
+    emap = np.array([0, -1, 2, -1, 4, 5])
+    got = O.moe_loop(x, ids, w, W13, W2, expert_map=emap)
+    W2z = W2.copy()
+    W2z[[1, 3]] = 0.0
+    ref = O.moe_loop(x, ids, w, W13, W2z)
+    assert np.abs(got - ref).max() <= 1e-12 * np.abs(ref).max()
+    assert np.abs(got - out).max() > 1e-3  # the remote experts did matter
+
+
+def test_expert_map_permuted_slots_are_invariant():
+    """Storing the local experts in other weight slots, with the map pointing at them,
+    gives the identical layer output."""
+    rng = np.random.default_rng(9)
+    x, Wg, W13, W2 = _rand_layer(rng, E=5)
+    out, ids, w, _ = O.moe_forward(x, Wg, W13, W2, 2)
+    perm = np.array([3, 0, 4, 1, 2])  # expert e lives in slot perm[e]
+    W13p, W2p = np.empty_like(W13), np.empty_like(W2)
+    W13p[perm], W2p[perm] = W13, W2
+    got = O.moe_loop(x, ids, w, W13p, W2p, expert_map=perm)
+    assert np.array_equal(got, out)
+
+
+def test_apply_expert_map_on_align_table():
+    ids = mi.random_topk_ids(40, 3, 7, seed=4).numpy()
+    sid, eid, total, _ = O.moe_align(ids, 4, 7, max_padded=O.max_padded_rows(40, 3, 7, 4))
+    emap = np.array([-1, 6, 5, -1, 3, 2, 1])
+    mapped = O.apply_expert_map(eid, emap)
+    for t, e in enumerate(eid):
+        assert mapped[t] == (-1 if e < 0 else emap[e])
+
+
 # ----------------------------------------------------------------- planted mistakes
 
 def _all_pins(golden_dir):
