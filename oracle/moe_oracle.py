@@ -307,11 +307,26 @@ def moe_dense(x, ids, w, W13, W2) -> np.ndarray:
     return out
 
 
+def add_shared_experts(ids, w, E, n_shared):
+    """[P2 §1 model table: DeepSeek-V3 and Kimi K2 have 256 / 384 routed experts "+1
+    shared"] a shared expert runs on every token with weight 1, outside the router: append
+    slots k..k+n_shared-1 holding experts E..E+n_shared-1 (their weights follow the routed
+    experts' in W13/W2)."""
+    T = ids.shape[0]
+    sid = np.broadcast_to(np.arange(E, E + n_shared), (T, n_shared))
+    return (np.concatenate([ids, sid], axis=1),
+            np.concatenate([w, np.ones((T, n_shared))], axis=1))
+
+
 def moe_forward(x, Wg, W13, W2, k, mode=SOFTMAX, renormalize=True, scale=1.0,
-                n_group=1, topk_group=1, logit_bias=None, select_bias=None, dense=False):
-    """Route then run version A (or B). Returns (out, ids, w, logits)."""
+                n_group=1, topk_group=1, logit_bias=None, select_bias=None, dense=False,
+                n_shared=0):
+    """Route then run version A (or B). Returns (out, ids, w, logits); with shared experts,
+    ids/w include their slots."""
     logits = router_logits(x, Wg, logit_bias if mode == SOFTMAX else None)
     ids, w = route(logits, k, mode, renormalize, scale, n_group, topk_group, select_bias)
+    if n_shared:
+        ids, w = add_shared_experts(ids, w, Wg.shape[0], n_shared)
     out = (moe_dense if dense else moe_loop)(x, ids, w, W13, W2)
     return out, ids, w, logits
 

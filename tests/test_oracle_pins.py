@@ -349,6 +349,24 @@ def test_apply_expert_map_on_align_table():
         assert mapped[t] == (-1 if e < 0 else emap[e])
 
 
+# ----------------------------------------------------------------- shared expert
+
+def test_shared_expert_adds_a_dense_ffn():
+    """Routed layer plus one shared expert = routed layer + the dense SwiGLU FFN of the
+    shared weights on every token (scalar loops), whatever the routed scale."""
+    rng = np.random.default_rng(10)
+    x, Wg, W13, W2 = _rand_layer(rng, E=5)
+    W13s = np.concatenate([W13, rng.standard_normal((1,) + W13.shape[1:]) / 3])
+    W2s = np.concatenate([W2, rng.standard_normal((1,) + W2.shape[1:]) / 3])
+    routed, *_ = O.moe_forward(x, Wg, W13, W2, 2, scale=1.7)
+    both, ids, w, _ = O.moe_forward(x, Wg, W13s, W2s, 2, scale=1.7, n_shared=1)
+    dense = np.stack([_ffn_scalar(x[t], W13s[5, :6], W13s[5, 6:], W2s[5]) for t in range(x.shape[0])])
+    assert np.abs(both - (routed + dense)).max() <= 1e-12 * np.abs(both).max()
+    assert ids.shape[1] == 3 and np.all(ids[:, 2] == 5) and np.all(w[:, 2] == 1.0)
+    b2, *_ = O.moe_forward(x, Wg, W13s, W2s, 2, scale=1.7, n_shared=1, dense=True)
+    assert np.abs(b2 - both).max() <= 1e-12 * np.abs(both).max()
+
+
 # ----------------------------------------------------------------- planted mistakes
 
 def _all_pins(golden_dir):
