@@ -44,6 +44,11 @@ def parse():
     p.add_argument("--cpu-sample-tokens", type=int, default=0)
     p.add_argument("--no-graph", action="store_true",
                    help="time eager launches instead of CUDA-graph replays of the step")
+    p.add_argument("--shared", type=int, default=0,
+                   help="shared experts (weight 1 on every token) added to the routed ones")
+    p.add_argument("--ep-half", action="store_true",
+                   help="expert parallelism: odd experts on another device (expert_map -1); "
+                        "the metric counts the rows of local experts only")
     p.add_argument("--tokens", type=int, default=0,
                    help="override T of the workload (smaller cases for profiling)")
     return p.parse_args()
@@ -235,9 +240,22 @@ def run_ours(args, wl):
     from routing_grouped_gemm_router_gb300.layer import MoELayer
 
     inp = mi.make_layer(wl, dev, seed=wl.seed + 1000 * rank)
+    if args.shared:  # shared experts' weights follow the routed experts'
+        g = torch.Generator(device=dev)
+        g.manual_seed(wl.seed + 77)
+        inp.W13 = torch.cat([inp.W13, (torch.randn(args.shared, 2 * wl.I, wl.H, generator=g,
+                                                   device=dev) / wl.H ** 0.5).to(inp.W13.dtype)])
+        inp.W2 = torch.cat([inp.W2, (torch.randn(args.shared, wl.H, wl.I, generator=g,
+                                                 device=dev) / wl.I ** 0.5).to(inp.W2.dtype)])
+    emap = None
+    if args.ep_half:
+        emap = torch.tensor([e if e % 2 == 0 else -1 for e in range(wl.E + args.shared)],
+                            dtype=torch.int32, device=dev)
     layer = MoELayer(inp.Wg, inp.W13, inp.W2, wl.k, wl.mode, wl.renormalize, wl.scale,
-                     wl.n_group, wl.topk_group, inp.logit_bias, inp.select_bias)
-    T, k, E, H, I = wl.T, wl.k, wl.E, wl.H, wl.I
+                     wl.n_group, wl.topk_group, inp.logit_bias, inp.select_bias, emap,
+                     n_shared=args.shared)
+    # the align step, the grouped GEMMs and the combine see shared experts as ordinary ones
+    T, k, E, H, I = wl.T, wl.k + args.shared, wl.E + args.shared, wl.H, wl.I
     cfg = layer.config(T)
     ws, lay = layer.workspace(T)
     B = lay.block_m
@@ -262,6 +280,8 @@ def run_ours(args, wl):
             ev[1].record(stream)
         L.moe_align(p["topk_ids"], T, k, E, B, p["sorted_ids"], p["expert_ids"],
                     p["num_post_padded"], p["counts"], p["align_scratch"], ws_align, sh)
+        if emap is not None:
+            L.moe_apply_expert_map(p["expert_ids"], lay.max_padded // B, emap, E, sh)
         if ev is not None:
             ev[2].record(stream)
         if gathered:
@@ -282,20 +302,26 @@ def run_ours(args, wl):
                            p["num_post_padded"], B, p["topk_w"], p["y"], sh)
         if ev is not None:
             ev[5].record(stream)
-        L.moe_combine(p["y"], T, k, H, cfg.dtype, out, sh)
+        if emap is not None:
+            L.moe_combine_local(p["y"], p["topk_ids"], emap, T, k, H, cfg.dtype, out, sh)
+        else:
+            L.moe_combine(p["y"], T, k, H, cfg.dtype, out, sh)
         if ev is not None:
             ev[6].record(stream)
 
     # router GEMM + top-k, align (one kernel up to 4096 rows, else three), row gather + GEMM1
     # (bf16), GEMM2, combine
-    launches_per_step = 2 + (1 if T * k <= 4096 else 3) + (2 if wl.dtype == "bf16" else 1) + 1 + 1
+    launches_per_step = 2 + (1 if T * k <= 4096 else 3) + (2 if wl.dtype == "bf16" else 1) + 1 + 1 + (1 if emap is not None else 0)
 
     for _ in range(max(3, args.warmup)):
         step()
     torch.cuda.synchronize()
     npp = int(ws[lay.num_post_padded:lay.num_post_padded + 4].view(torch.int32).item())
     counts = ws[lay.counts:lay.counts + 4 * E].view(torch.int32).cpu()
+    if emap is not None:  # only the local experts' rows and weights are this device's work
+        counts = counts * (emap.cpu() >= 0)
     active = int((counts > 0).sum())
+    local_rows = int(counts.sum())
 
     # ---- the step captured once in a CUDA graph (no host work or launch gaps in the timing)
     graph = None
@@ -363,7 +389,7 @@ def run_ours(args, wl):
     e2e_ms = max_over_ranks(dist, e0.elapsed_time(e1) / args.steps, dev)
     bytes_io = T * H * inp.x.element_size()
 
-    flops = wl.flops
+    flops = 6 * local_rows * H * I  # useful rows (all T*k rows unless experts are remote)
     value = flops * world / (ms * 1e-3) / 1e12
     e2e_val = flops * world / (e2e_ms * 1e-3) / 1e12
     hbm, bf16_burst, bf16_sus, peak_src = peaks()
@@ -376,7 +402,7 @@ def run_ours(args, wl):
                 "algorithmic_bytes_per_launch": w_bytes,
                 "peak_kind": f"{peak_src} HBM copy bandwidth"}
     else:
-        g1_flops = 4 * T * k * H * I
+        g1_flops = 4 * local_rows * H * I
         roof = {"bound": "tensor", "achieved": g1_flops / (stage["gemm1"] * 1e-3) / 1e12,
                 "peak": bf16_sus, "unit": "TFLOP/s",
                 "kernel": "gemm1 (gate/up grouped GEMM + SwiGLU)",
@@ -391,7 +417,9 @@ def run_ours(args, wl):
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
             "dtype": "bf16" if wl.dtype == "bf16" else "f32",
             "data": "synthetic (seeded N(0,1) tokens, N(0,1/fan_in) weights, random init)",
-            "config": {"workload": wl.name, "T": T, "H": H, "I": I, "E": E, "k": k,
+            "config": {"workload": wl.name + ("+ep-half" if emap is not None else "")
+                       + (f"+shared{args.shared}" if args.shared else ""),
+                       "T": T, "H": H, "I": I, "E": wl.E, "k": wl.k, "n_shared": args.shared,
                        "mode": "sigmoid-grouped" if wl.mode else "softmax",
                        "global_batch": T * world, "parallelism": f"replicas x{world}",
                        "l2": "inputs larger than L2 (expert weights "

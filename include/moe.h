@@ -43,7 +43,7 @@
 extern "C" {
 #endif
 
-#define MOE_ABI_VERSION 1
+#define MOE_ABI_VERSION 2
 
 typedef enum {
   MOE_OK = 0,
@@ -81,6 +81,17 @@ typedef struct moe_config {
   int topk_group;           /* mode 1: groups kept (topk_group * E / n_group >= k) */
   const float* logit_bias;  /* mode 0: device fp32 [E] added to the logits, or NULL */
   const float* select_bias; /* mode 1: device fp32 [E] selection-only bias, or NULL */
+  /* Expert parallelism (page §10, "Try this"): device int32 [E] or NULL. Expert e's weights
+   * sit in slot expert_map[e] of W13/W2 (0 <= slot < E); -1 marks an expert held by another
+   * device: its tiles are skipped and its slots add nothing to out. Routing stays global. */
+  const int32_t* expert_map;
+  /* Shared experts (page §1: DeepSeek-V3 / Kimi K2 "+1 shared"): n_shared >= 0 SwiGLU experts
+   * applied to every token with weight 1, outside the router and its scale. Their weights
+   * follow the routed experts: W13/W2 hold E + n_shared experts. The router writes them as
+   * slots k..k+n_shared-1 of every token (ids E..E+n_shared-1); align, the grouped GEMMs and
+   * the combine then see k + n_shared slots and E + n_shared experts (expert_map, if given,
+   * has E + n_shared entries). */
+  int n_shared;
 } moe_config_t;
 
 /* Byte offsets of the intermediates inside a moe_forward workspace (256-byte aligned). */
@@ -124,7 +135,8 @@ moe_status_t moe_workspace_size(const moe_config_t* cfg, size_t* bytes);
 
 /* Router (page §3 route(), §4 route_grouped()): logits = x @ Wg^T (+ logit_bias in mode 0)
  * accumulated in fp32, then top-k per cfg->mode. Writes logits[T,E] (fp32, required),
- * topk_ids[T,k] in descending selection key, topk_w[T,k] fp32. */
+ * topk_ids[T,k+n_shared] (routed slots in descending selection key, then the shared
+ * experts E..E+n_shared-1) and topk_w[T,k+n_shared] fp32 (shared slots: 1). */
 moe_status_t moe_route(const moe_config_t* cfg, const void* x, const void* Wg, float* logits,
                        int32_t* topk_ids, float* topk_w, cudaStream_t stream);
 
@@ -151,6 +163,12 @@ moe_status_t moe_align(const int32_t* topk_ids, int T, int k, int E, int block_m
 moe_status_t moe_align_noalloc(const int32_t* topk_ids, int T, int k, int E, int block_m,
                                int32_t* sorted_ids, int32_t* expert_ids,
                                int32_t* num_post_padded, int32_t* counts, cudaStream_t stream);
+
+/* Expert parallelism, applied to an align table: every tile label e >= 0 of
+ * expert_ids[0..num_tiles) becomes expert_map[e] (-1: not on this device, skipped by the
+ * GEMMs). Map entries outside [-1, E) become -1 and set device status 1. */
+moe_status_t moe_apply_expert_map(int32_t* expert_ids, int num_tiles, const int32_t* expert_map,
+                                  int E, cudaStream_t stream);
 
 /* GEMM1 + SwiGLU (page §6 with the gate/up halves fused in one epilogue): for every
  * padded position p < num_post_padded whose row r = sorted_ids[p] < T*k,
@@ -204,8 +222,15 @@ moe_status_t moe_grouped_swiglu(const moe_config_t* cfg, const void* x, const vo
 moe_status_t moe_combine(const void* y, int T, int k, int H, moe_dtype_t dtype, void* out,
                          cudaStream_t stream);
 
-/* The whole layer: route -> align -> GEMM1+SwiGLU -> GEMM2 -> combine, all enqueued on
- * `stream` with no host round-trip. ws must hold moe_workspace_size(cfg) bytes, 256-byte
+/* Combine with expert parallelism: as moe_combine, but slot j of token t is skipped when
+ * expert_map[topk_ids[t, j]] < 0 (its expert is on another device and its y row is not
+ * written here). topk_ids [T, k] int32, expert_map [E] int32, both on the device. */
+moe_status_t moe_combine_local(const void* y, const int32_t* topk_ids, const int32_t* expert_map,
+                               int T, int k, int H, moe_dtype_t dtype, void* out,
+                               cudaStream_t stream);
+
+/* The whole layer: route -> align (-> expert map) -> GEMM1+SwiGLU -> GEMM2 -> combine, all
+ * enqueued on `stream` with no host round-trip. ws must hold moe_workspace_size(cfg) bytes, 256-byte
  * aligned; its intermediates sit at moe_workspace_layout(cfg) offsets. */
 moe_status_t moe_forward(const moe_config_t* cfg, const void* x, const void* Wg,
                          const void* W13, const void* W2, void* out, void* ws,

@@ -30,7 +30,8 @@ class moe_config_t(ctypes.Structure):
                 ("E", ctypes.c_int), ("k", ctypes.c_int), ("dtype", ctypes.c_int),
                 ("mode", ctypes.c_int), ("renormalize", ctypes.c_int), ("scale", ctypes.c_float),
                 ("n_group", ctypes.c_int), ("topk_group", ctypes.c_int),
-                ("logit_bias", ctypes.c_void_p), ("select_bias", ctypes.c_void_p)]
+                ("logit_bias", ctypes.c_void_p), ("select_bias", ctypes.c_void_p),
+                ("expert_map", ctypes.c_void_p), ("n_shared", ctypes.c_int)]
 
 
 class moe_ws_layout_t(ctypes.Structure):
@@ -66,6 +67,8 @@ def _load():
         "moe_expert_gemm2": (ST, [CFG, P, P, P, P, P, I32, P, P, P]),
         "moe_grouped_swiglu": (ST, [CFG, P, P, P, P, P, P, I32, P, P, P, SZ, P]),
         "moe_combine": (ST, [P, I32, I32, I32, I32, P, P]),
+        "moe_apply_expert_map": (ST, [P, I32, P, I32, P]),
+        "moe_combine_local": (ST, [P, P, P, I32, I32, I32, I32, P, P]),
         "moe_forward": (ST, [CFG, P, P, P, P, P, P, SZ, P]),
         "moe_device_status": (I32, [I32]),
     }
@@ -81,7 +84,8 @@ EXPORTED = ("moe_abi_version", "moe_status_string", "moe_block_m", "moe_max_padd
             "moe_route", "moe_align", "moe_align_noalloc", "moe_expert_gemm1_workspace_size",
             "moe_expert_gemm1", "moe_gather_rows", "moe_expert_gemm1_gathered",
             "moe_grouped_swiglu_workspace_size", "moe_expert_gemm2",
-            "moe_grouped_swiglu", "moe_combine", "moe_forward", "moe_device_status")
+            "moe_grouped_swiglu", "moe_combine", "moe_apply_expert_map", "moe_combine_local",
+            "moe_forward", "moe_device_status")
 
 
 def lib():
@@ -117,10 +121,13 @@ def status_string(st: int) -> str:
 
 
 def make_config(T, H, I, E, k, dtype=MOE_BF16, mode=MOE_ROUTE_SOFTMAX, renormalize=True,
-                scale=1.0, n_group=1, topk_group=1, logit_bias=None, select_bias=None):
-    """Build a ``moe_config_t``; the biases are device fp32 tensors (kept alive by caller)."""
+                scale=1.0, n_group=1, topk_group=1, logit_bias=None, select_bias=None,
+                expert_map=None, n_shared=0):
+    """Build a ``moe_config_t``; biases (fp32) and expert_map (int32) are device tensors
+    the caller keeps alive."""
     return moe_config_t(T, H, I, E, k, dtype, mode, int(bool(renormalize)), float(scale),
-                        n_group, topk_group, _ptr(logit_bias), _ptr(select_bias))
+                        n_group, topk_group, _ptr(logit_bias), _ptr(select_bias),
+                        _ptr(expert_map), int(n_shared))
 
 
 def moe_abi_version() -> int:
@@ -224,6 +231,16 @@ def moe_grouped_swiglu(cfg, x, W13, W2, sorted_ids, expert_ids, num_post_padded,
 
 def moe_combine(y, T, k, H, dtype, out, stream=None):
     _check("moe_combine", _lib.moe_combine(_ptr(y), T, k, H, dtype, _ptr(out), _stream(stream)))
+
+
+def moe_apply_expert_map(expert_ids, num_tiles, expert_map, E, stream=None):
+    _check("moe_apply_expert_map", _lib.moe_apply_expert_map(
+        _ptr(expert_ids), num_tiles, _ptr(expert_map), E, _stream(stream)))
+
+
+def moe_combine_local(y, topk_ids, expert_map, T, k, H, dtype, out, stream=None):
+    _check("moe_combine_local", _lib.moe_combine_local(
+        _ptr(y), _ptr(topk_ids), _ptr(expert_map), T, k, H, dtype, _ptr(out), _stream(stream)))
 
 
 def moe_forward(cfg, x, Wg, W13, W2, out, ws, ws_bytes, stream=None):

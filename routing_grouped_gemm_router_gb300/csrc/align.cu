@@ -280,6 +280,30 @@ extern "C" moe_status_t moe_align_noalloc(const int32_t* topk_ids, int T, int k,
 
 namespace moe {
 
+// ---- expert parallelism: relabel tiles with local weight slots ------------------------
+__global__ void __launch_bounds__(256) apply_expert_map_kernel(int32_t* __restrict__ eid,
+                                                               int tiles,
+                                                               const int32_t* __restrict__ map,
+                                                               int E) {
+  for (int t = blockIdx.x * blockDim.x + threadIdx.x; t < tiles; t += gridDim.x * blockDim.x) {
+    const int e = eid[t];
+    if (e < 0) continue;
+    int slot = e < E ? map[e] : -1;
+    if (slot < -1 || slot >= E) {
+      atomicExch(&g_align_status, kStatusBadExpert);
+      slot = -1;
+    }
+    eid[t] = slot;
+  }
+}
+
+moe_status_t launch_apply_expert_map(int32_t* eid, int tiles, const int32_t* map, int E,
+                                     cudaStream_t s) {
+  const int blocks = std::max(1, std::min(ceil_div(tiles, 256), 64));
+  apply_expert_map_kernel<<<blocks, 256, 0, s>>>(eid, tiles, map, E);
+  return last_launch_status();
+}
+
 static bool set_smem(const void* fn, size_t bytes) {
   if (bytes <= 48 * 1024) return true;
   return cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bytes) ==

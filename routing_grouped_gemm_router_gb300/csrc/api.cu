@@ -39,9 +39,20 @@ static moe_status_t check_cfg(const moe_config_t* c) {
     if (c->topk_group < 1 || c->topk_group > c->n_group) return MOE_ERR_INVALID_ARG;
     if ((int64_t)c->topk_group * (c->E / c->n_group) < c->k) return MOE_ERR_INVALID_ARG;
   }
-  if (c->E > kMaxE) return MOE_ERR_UNSUPPORTED;
-  if ((int64_t)c->T * c->k > (int64_t)1 << 30) return MOE_ERR_UNSUPPORTED;
+  if (c->n_shared < 0 || c->n_shared > 8 || c->k + c->n_shared > 32) return MOE_ERR_INVALID_ARG;
+  if (c->E + c->n_shared > kMaxE) return MOE_ERR_UNSUPPORTED;
+  if ((int64_t)c->T * (c->k + c->n_shared) > (int64_t)1 << 30) return MOE_ERR_UNSUPPORTED;
   return MOE_OK;
+}
+
+// The configuration the align step, the grouped GEMMs and the combine see: shared experts
+// are ordinary experts E..E+n_shared-1 present in slots k..k+n_shared-1 of every token.
+static moe_config_t effective(const moe_config_t* c) {
+  moe_config_t e = *c;
+  e.k = c->k + c->n_shared;
+  e.E = c->E + c->n_shared;
+  e.n_shared = 0;
+  return e;
 }
 
 static int block_m_for(moe_dtype_t d) { return d == MOE_BF16 ? 128 : 16; }
@@ -96,10 +107,12 @@ moe_status_t moe_align_workspace_size(int T, int k, int E, int block_m, size_t* 
   return MOE_OK;
 }
 
-moe_status_t moe_workspace_layout(const moe_config_t* c, moe_ws_layout_t* L) {
-  moe_status_t st = check_cfg(c);
+moe_status_t moe_workspace_layout(const moe_config_t* cfg, moe_ws_layout_t* L) {
+  moe_status_t st = check_cfg(cfg);
   if (st != MOE_OK) return st;
   if (!L) return MOE_ERR_INVALID_ARG;
+  const moe_config_t eff = effective(cfg);
+  const moe_config_t* c = &eff;
   const int B = block_m_for(c->dtype);
   const size_t mp = moe_max_padded_rows(c->T, c->k, c->E, B);
   const size_t es = dtype_size(c->dtype);
@@ -110,7 +123,7 @@ moe_status_t moe_workspace_layout(const moe_config_t* c, moe_ws_layout_t* L) {
     off = align_up(off + bytes, 256);
     return o;
   };
-  L->logits = take((size_t)c->T * c->E * 4);
+  L->logits = take((size_t)c->T * cfg->E * 4);
   L->topk_ids = take(n * 4);
   L->topk_w = take(n * 4);
   L->sorted_ids = take(mp * 4);
@@ -175,8 +188,11 @@ static moe_status_t check_gemm_args(const moe_config_t* c, int block_m) {
   return MOE_OK;
 }
 
-moe_status_t moe_expert_gemm1_workspace_size(const moe_config_t* c, int block_m, size_t* bytes) {
-  moe_status_t st = check_gemm_args(c, block_m);
+moe_status_t moe_expert_gemm1_workspace_size(const moe_config_t* cfg, int block_m,
+                                             size_t* bytes) {
+  moe_status_t st = check_gemm_args(cfg, block_m);
+  const moe_config_t eff = effective(cfg);
+  const moe_config_t* c = &eff;
   if (st != MOE_OK) return st;
   if (!bytes) return MOE_ERR_INVALID_ARG;
   *bytes = gemm1_scratch_bytes(c, block_m);
@@ -194,11 +210,13 @@ moe_status_t moe_gather_rows(const void* x, const int32_t* sorted_ids,
                             H * (int)dtype_size(dtype), xs, stream);
 }
 
-moe_status_t moe_expert_gemm1_gathered(const moe_config_t* c, const void* xs, const void* W13,
-                                       const int32_t* sorted_ids, const int32_t* expert_ids,
-                                       const int32_t* npp, int block_m, void* act,
-                                       cudaStream_t stream) {
-  moe_status_t st = check_gemm_args(c, block_m);
+moe_status_t moe_expert_gemm1_gathered(const moe_config_t* cfg, const void* xs,
+                                       const void* W13, const int32_t* sorted_ids,
+                                       const int32_t* expert_ids, const int32_t* npp,
+                                       int block_m, void* act, cudaStream_t stream) {
+  moe_status_t st = check_gemm_args(cfg, block_m);
+  const moe_config_t eff = effective(cfg);
+  const moe_config_t* c = &eff;
   if (st != MOE_OK) return st;
   if (c->dtype != MOE_BF16) return MOE_ERR_UNSUPPORTED;
   if (!xs || !W13 || !sorted_ids || !expert_ids || !npp || !act) return MOE_ERR_INVALID_ARG;
@@ -207,11 +225,13 @@ moe_status_t moe_expert_gemm1_gathered(const moe_config_t* c, const void* xs, co
   return launch_gemm1_tc(*c, xs, W13, sorted_ids, expert_ids, npp, block_m, mp, act, stream);
 }
 
-moe_status_t moe_expert_gemm1(const moe_config_t* c, const void* x, const void* W13,
+moe_status_t moe_expert_gemm1(const moe_config_t* cfg, const void* x, const void* W13,
                               const int32_t* sorted_ids, const int32_t* expert_ids,
                               const int32_t* npp, int block_m, void* act, void* ws,
                               size_t ws_bytes, cudaStream_t stream) {
-  moe_status_t st = check_gemm_args(c, block_m);
+  moe_status_t st = check_gemm_args(cfg, block_m);
+  const moe_config_t eff = effective(cfg);
+  const moe_config_t* c = &eff;
   if (st != MOE_OK) return st;
   if (!x || !W13 || !sorted_ids || !expert_ids || !npp || !act) return MOE_ERR_INVALID_ARG;
   const int mp = (int)moe_max_padded_rows(c->T, c->k, c->E, block_m);
@@ -220,18 +240,20 @@ moe_status_t moe_expert_gemm1(const moe_config_t* c, const void* x, const void* 
     if (!ws || ws_bytes < need || ((uintptr_t)ws & 255u)) return MOE_ERR_WORKSPACE;
     st = moe_gather_rows(x, sorted_ids, npp, c->T, c->k, c->H, c->dtype, ws, stream);
     if (st != MOE_OK) return st;
-    return moe_expert_gemm1_gathered(c, ws, W13, sorted_ids, expert_ids, npp, block_m, act,
+    return moe_expert_gemm1_gathered(cfg, ws, W13, sorted_ids, expert_ids, npp, block_m, act,
                                      stream);
   }
   return launch_gemm1_simt(*c, (const float*)x, (const float*)W13, sorted_ids, expert_ids, npp,
                            block_m, mp, (float*)act, stream);
 }
 
-moe_status_t moe_expert_gemm2(const moe_config_t* c, const void* act, const void* W2,
+moe_status_t moe_expert_gemm2(const moe_config_t* cfg, const void* act, const void* W2,
                               const int32_t* sorted_ids, const int32_t* expert_ids,
                               const int32_t* npp, int block_m, const float* topk_w, void* y,
                               cudaStream_t stream) {
-  moe_status_t st = check_gemm_args(c, block_m);
+  moe_status_t st = check_gemm_args(cfg, block_m);
+  const moe_config_t eff = effective(cfg);
+  const moe_config_t* c = &eff;
   if (st != MOE_OK) return st;
   if (!act || !W2 || !sorted_ids || !expert_ids || !npp || !topk_w || !y)
     return MOE_ERR_INVALID_ARG;
@@ -245,9 +267,11 @@ moe_status_t moe_expert_gemm2(const moe_config_t* c, const void* act, const void
                            block_m, mp, topk_w, (float*)y, stream);
 }
 
-moe_status_t moe_grouped_swiglu_workspace_size(const moe_config_t* c, int block_m,
+moe_status_t moe_grouped_swiglu_workspace_size(const moe_config_t* cfg, int block_m,
                                                size_t* bytes) {
-  moe_status_t st = check_gemm_args(c, block_m);
+  moe_status_t st = check_gemm_args(cfg, block_m);
+  const moe_config_t eff = effective(cfg);
+  const moe_config_t* c = &eff;
   if (st != MOE_OK) return st;
   if (!bytes) return MOE_ERR_INVALID_ARG;
   const size_t mp = moe_max_padded_rows(c->T, c->k, c->E, block_m);
@@ -264,8 +288,9 @@ moe_status_t moe_grouped_swiglu(const moe_config_t* c, const void* x, const void
   moe_status_t st = moe_grouped_swiglu_workspace_size(c, block_m, &need);
   if (st != MOE_OK) return st;
   if (!ws || ws_bytes < need || ((uintptr_t)ws & 255u)) return MOE_ERR_WORKSPACE;
-  const size_t mp = moe_max_padded_rows(c->T, c->k, c->E, block_m);
-  const size_t act_bytes = align_up(mp * c->I * dtype_size(c->dtype), 256);
+  const moe_config_t eff = effective(c);
+  const size_t mp = moe_max_padded_rows(eff.T, eff.k, eff.E, block_m);
+  const size_t act_bytes = align_up(mp * eff.I * dtype_size(eff.dtype), 256);
   uint8_t* act = (uint8_t*)ws;
   st = moe_expert_gemm1(c, x, W13, sorted_ids, expert_ids, npp, block_m, act, act + act_bytes,
                         ws_bytes - act_bytes, stream);
@@ -279,6 +304,23 @@ moe_status_t moe_combine(const void* y, int T, int k, int H, moe_dtype_t dtype, 
   if (dtype != MOE_F32 && dtype != MOE_BF16) return MOE_ERR_INVALID_ARG;
   if (!aligned16(y) || !aligned16(out)) return MOE_ERR_INVALID_ARG;
   return launch_combine(y, T, k, H, dtype, out, stream);
+}
+
+moe_status_t moe_apply_expert_map(int32_t* expert_ids, int num_tiles, const int32_t* expert_map,
+                                  int E, cudaStream_t stream) {
+  if (!expert_ids || !expert_map || num_tiles < 0 || E < 1) return MOE_ERR_INVALID_ARG;
+  if (num_tiles == 0) return MOE_OK;
+  return launch_apply_expert_map(expert_ids, num_tiles, expert_map, E, stream);
+}
+
+moe_status_t moe_combine_local(const void* y, const int32_t* topk_ids, const int32_t* expert_map,
+                               int T, int k, int H, moe_dtype_t dtype, void* out,
+                               cudaStream_t stream) {
+  if (!y || !topk_ids || !expert_map || !out || T < 1 || k < 1 || H < 8 || H % 8)
+    return MOE_ERR_INVALID_ARG;
+  if (dtype != MOE_F32 && dtype != MOE_BF16) return MOE_ERR_INVALID_ARG;
+  if (!aligned16(y) || !aligned16(out)) return MOE_ERR_INVALID_ARG;
+  return launch_combine_local(y, topk_ids, expert_map, T, k, H, dtype, out, stream);
 }
 
 moe_status_t moe_forward(const moe_config_t* c, const void* x, const void* Wg, const void* W13,
@@ -298,8 +340,13 @@ moe_status_t moe_forward(const moe_config_t* c, const void* x, const void* Wg, c
   int32_t* npp = (int32_t*)(b + L.num_post_padded);
   int32_t* counts = (int32_t*)(b + L.counts);
   if ((st = moe_route(c, x, Wg, logits, ids, w, stream)) != MOE_OK) return st;
-  if ((st = moe_align(ids, c->T, c->k, c->E, L.block_m, sid, eid, npp, counts,
+  const moe_config_t e = effective(c);  // shared experts as ordinary slots / experts
+  if ((st = moe_align(ids, e.T, e.k, e.E, L.block_m, sid, eid, npp, counts,
                       b + L.align_scratch, L.act - L.align_scratch, stream)) != MOE_OK)
+    return st;
+  if (c->expert_map &&
+      (st = moe_apply_expert_map(eid, L.max_padded / L.block_m, c->expert_map, e.E, stream)) !=
+          MOE_OK)
     return st;
   if ((st = moe_expert_gemm1(c, x, W13, sid, eid, npp, L.block_m, b + L.act, b + L.xs,
                              L.y - L.xs, stream)) != MOE_OK)
@@ -307,7 +354,9 @@ moe_status_t moe_forward(const moe_config_t* c, const void* x, const void* Wg, c
   if ((st = moe_expert_gemm2(c, b + L.act, W2, sid, eid, npp, L.block_m, w, b + L.y, stream)) !=
       MOE_OK)
     return st;
-  return moe_combine(b + L.y, c->T, c->k, c->H, c->dtype, out, stream);
+  if (c->expert_map)
+    return moe_combine_local(b + L.y, ids, c->expert_map, e.T, e.k, e.H, e.dtype, out, stream);
+  return moe_combine(b + L.y, e.T, e.k, e.H, e.dtype, out, stream);
 }
 
 int moe_device_status(int reset) {

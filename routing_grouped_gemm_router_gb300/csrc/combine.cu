@@ -53,6 +53,59 @@ __global__ void __launch_bounds__(256) combine_f32_kernel(const float4* __restri
   }
 }
 
+// Expert parallelism: slots whose expert is on another device (map < 0) are skipped.
+template <bool BF16>
+__global__ void __launch_bounds__(256) combine_local_kernel(const void* __restrict__ y,
+                                                            const int32_t* __restrict__ ids,
+                                                            const int32_t* __restrict__ map,
+                                                            void* __restrict__ out, int T,
+                                                            int k, int vec_per_row) {
+  const int64_t total = (int64_t)T * vec_per_row;
+  for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < total;
+       i += (int64_t)gridDim.x * blockDim.x) {
+    const int64_t t = i / vec_per_row, v = i % vec_per_row;
+    float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+    for (int j = 0; j < k; ++j) {
+      if (map[ids[t * k + j]] < 0) continue;
+      if (BF16) {
+        const uint4 q = __ldcs((const uint4*)y + (t * k + j) * vec_per_row + v);
+        const __nv_bfloat162* h = reinterpret_cast<const __nv_bfloat162*>(&q);
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+          float2 f = __bfloat1622float2(h[c]);
+          acc[2 * c] += f.x;
+          acc[2 * c + 1] += f.y;
+        }
+      } else {
+        const float4 q = __ldcs((const float4*)y + (t * k + j) * vec_per_row + v);
+        acc[0] += q.x; acc[1] += q.y; acc[2] += q.z; acc[3] += q.w;
+      }
+    }
+    if (BF16) {
+      uint4 o;
+      __nv_bfloat162* oh = reinterpret_cast<__nv_bfloat162*>(&o);
+#pragma unroll
+      for (int c = 0; c < 4; ++c) oh[c] = __floats2bfloat162_rn(acc[2 * c], acc[2 * c + 1]);
+      ((uint4*)out)[i] = o;
+    } else {
+      ((float4*)out)[i] = make_float4(acc[0], acc[1], acc[2], acc[3]);
+    }
+  }
+}
+
+moe_status_t launch_combine_local(const void* y, const int32_t* ids, const int32_t* map, int T,
+                                  int k, int H, moe_dtype_t dt, void* out, cudaStream_t s) {
+  const int vec = dt == MOE_BF16 ? H / 8 : H / 4;
+  const int64_t total = (int64_t)T * vec;
+  int blocks = (int)std::min<int64_t>(ceil_div64(total, 256), (int64_t)num_sms() * 8);
+  if (blocks < 1) blocks = 1;
+  if (dt == MOE_BF16)
+    combine_local_kernel<true><<<blocks, 256, 0, s>>>(y, ids, map, out, T, k, vec);
+  else
+    combine_local_kernel<false><<<blocks, 256, 0, s>>>(y, ids, map, out, T, k, vec);
+  return last_launch_status();
+}
+
 moe_status_t launch_combine(const void* y, int T, int k, int H, moe_dtype_t dt, void* out,
                             cudaStream_t s) {
   const int vec = dt == MOE_BF16 ? H / 8 : H / 4;

@@ -201,7 +201,8 @@ constexpr int kMaxPerLane = 16;  // E <= 512
 __global__ void __launch_bounds__(kTopkWarps * 32) topk_kernel(
     const float* __restrict__ logits, int Tn, int E, int k, int mode, int renorm, float scale,
     int n_group, int topk_group, const float* __restrict__ logit_bias,
-    const float* __restrict__ select_bias, int32_t* __restrict__ ids, float* __restrict__ w) {
+    const float* __restrict__ select_bias, int n_shared, int32_t* __restrict__ ids,
+    float* __restrict__ w) {
   __shared__ float skey[kTopkWarps][512];
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
   const int t = blockIdx.x * kTopkWarps + warp;
@@ -308,9 +309,13 @@ __global__ void __launch_bounds__(kTopkWarps * 32) topk_kernel(
     float sv = lane < k ? my_sel_val : 0.f;
     wj = renorm ? sv / warp_sum(sv) : sv;
   }
+  const int kk = k + n_shared;  // row stride: routed slots, then the shared experts
   if (lane < k) {
-    ids[(size_t)t * k + lane] = my_sel_id;
-    w[(size_t)t * k + lane] = scale * wj;
+    ids[(size_t)t * kk + lane] = my_sel_id;
+    w[(size_t)t * kk + lane] = scale * wj;
+  } else if (lane < kk) {
+    ids[(size_t)t * kk + lane] = E + (lane - k);
+    w[(size_t)t * kk + lane] = 1.f;
   }
 }
 
@@ -319,7 +324,7 @@ moe_status_t launch_topk(const moe_config_t& c, const float* logits, int32_t* id
   int grid = ceil_div(c.T, kTopkWarps);
   topk_kernel<<<grid, kTopkWarps * 32, 0, s>>>(logits, c.T, c.E, c.k, (int)c.mode,
                                               c.renormalize, c.scale, c.n_group, c.topk_group,
-                                              c.logit_bias, c.select_bias, ids, w);
+                                              c.logit_bias, c.select_bias, c.n_shared, ids, w);
   return last_launch_status();
 }
 

@@ -22,9 +22,12 @@ class MoELayer:
 
     def __init__(self, Wg, W13, W2, k, mode=L.MOE_ROUTE_SOFTMAX, renormalize=True, scale=1.0,
                  n_group=1, topk_group=1, logit_bias: Optional[torch.Tensor] = None,
-                 select_bias: Optional[torch.Tensor] = None):
+                 select_bias: Optional[torch.Tensor] = None,
+                 expert_map: Optional[torch.Tensor] = None, n_shared: int = 0):
+        """W13/W2 hold E routed experts followed by n_shared shared experts."""
         self.Wg, self.W13, self.W2 = Wg, W13, W2
         self.E, self.H = Wg.shape
+        self.n_shared = n_shared
         self.I = W2.shape[2]
         self.k = k
         self.dtype = {torch.bfloat16: L.MOE_BF16, torch.float32: L.MOE_F32}[Wg.dtype]
@@ -32,13 +35,16 @@ class MoELayer:
         self.n_group, self.topk_group = n_group, topk_group
         self.logit_bias = logit_bias.float().contiguous() if logit_bias is not None else None
         self.select_bias = select_bias.float().contiguous() if select_bias is not None else None
+        self.expert_map = (expert_map.to(torch.int32).contiguous()
+                           if expert_map is not None else None)
         self._ws = None
         self._ws_T = None
 
     def config(self, T):
         return L.make_config(T, self.H, self.I, self.E, self.k, self.dtype, self.mode,
                              self.renormalize, self.scale, self.n_group, self.topk_group,
-                             self.logit_bias, self.select_bias)
+                             self.logit_bias, self.select_bias, self.expert_map,
+                             self.n_shared)
 
     def workspace(self, T):
         if self._ws_T != T:
@@ -61,7 +67,8 @@ class MoELayer:
     # Views of the intermediates the last forward left in the workspace (tests, debugging).
     def intermediates(self, T):
         ws, lay = self.workspace(T)
-        n = T * self.k
+        kk = self.k + self.n_shared
+        n = T * kk
         dt = self.Wg.dtype
 
         def view(off, count, dtype):
@@ -70,12 +77,12 @@ class MoELayer:
 
         return {
             "logits": view(lay.logits, T * self.E, torch.float32).view(T, self.E),
-            "topk_ids": view(lay.topk_ids, n, torch.int32).view(T, self.k),
-            "topk_w": view(lay.topk_w, n, torch.float32).view(T, self.k),
+            "topk_ids": view(lay.topk_ids, n, torch.int32).view(T, kk),
+            "topk_w": view(lay.topk_w, n, torch.float32).view(T, kk),
             "sorted_ids": view(lay.sorted_ids, lay.max_padded, torch.int32),
             "expert_ids": view(lay.expert_ids, lay.max_padded // lay.block_m, torch.int32),
             "num_post_padded": view(lay.num_post_padded, 1, torch.int32),
-            "counts": view(lay.counts, self.E, torch.int32),
+            "counts": view(lay.counts, self.E + self.n_shared, torch.int32),
             "y": view(lay.y, n * self.H, dt).view(n, self.H),
             "block_m": lay.block_m,
             "max_padded": lay.max_padded,

@@ -439,3 +439,73 @@ def test_cuda_graph_capture_and_replay(L):
         eager = layer(x_static.clone())
         torch.cuda.synchronize()
         assert torch.equal(out_static, eager)
+
+
+# --------------------------------------------------------------------- expert parallelism
+
+@pytest.mark.parametrize("dtype,variant", [("bf16", "half"), ("bf16", "perm"), ("f32", "half")])
+def test_expert_map(L, dtype, variant):
+    """Odd experts held elsewhere (map -1), or local experts stored in permuted weight slots:
+    the layer equals the oracle with the same expert_map; tiles carry the mapped labels."""
+    H, I = (256, 256) if dtype == "bf16" else (64, 96)
+    wl = mi.Workload("ep", T=300, H=H, I=I, E=16, k=4, dtype=dtype, seed=31)
+    inp = mi.make_layer(wl, "cpu")
+    enforce_margins(inp)
+    E = wl.E
+    if variant == "half":
+        emap = torch.tensor([e if e % 2 == 0 else -1 for e in range(E)], dtype=torch.int32)
+        W13, W2 = inp.W13, inp.W2
+    else:
+        emap = torch.tensor([(5 * e + 3) % E for e in range(E)], dtype=torch.int32)
+        W13, W2 = torch.empty_like(inp.W13), torch.empty_like(inp.W2)
+        W13[emap.long()], W2[emap.long()] = inp.W13, inp.W2
+    dev = _to_dev(mi.LayerInputs(wl, inp.x, inp.Wg, W13, W2))
+    from routing_grouped_gemm_router_gb300.layer import MoELayer
+    layer = MoELayer(dev.Wg, dev.W13, dev.W2, wl.k, expert_map=emap.to(DEV))
+    out = layer(dev.x)
+    torch.cuda.synchronize()
+    mids = layer.intermediates(wl.T)
+    ids, w = O.route_softmax(oracle_logits(inp), wl.k)
+    assert np.array_equal(to_np(mids["topk_ids"]), ids)
+    B, mp = mids["block_m"], mids["max_padded"]
+    _, eid, _, _ = O.moe_align(ids, B, E, max_padded=mp)
+    assert np.array_equal(to_np(mids["expert_ids"]), O.apply_expert_map(eid, emap.numpy()))
+    ref = O.moe_loop(to_np(inp.x), ids, w, weights_for_oracle(W13), weights_for_oracle(W2),
+                     expert_map=emap.numpy())
+    assert_close(to_np(out), ref, dtype)
+    if variant == "perm":  # same layer as without expert parallelism
+        plain = O.moe_loop(to_np(inp.x), ids, w, weights_for_oracle(inp.W13),
+                           weights_for_oracle(inp.W2))
+        assert_close(to_np(out), plain, dtype)
+
+
+# --------------------------------------------------------------------- shared experts
+
+@pytest.mark.parametrize("dtype", ["bf16", "f32"])
+def test_shared_expert(L, dtype):
+    """DeepSeek-style layer with one shared expert (weight 1 on every token), grouped
+    sigmoid routing with scale 2.5: equals the oracle with the shared slot appended."""
+    H, I = (256, 256) if dtype == "bf16" else (64, 96)
+    wl = mi.Workload("shared", T=200, H=H, I=I, E=16, k=4, dtype=dtype,
+                     mode=mi.ROUTE_SIGMOID_GROUPED, scale=2.5, n_group=4, topk_group=2,
+                     select_bias_std=0.05, seed=41)
+    inp = mi.make_layer(wl, "cpu")
+    enforce_margins(inp)
+    g = torch.Generator().manual_seed(42)
+    tdt = inp.W13.dtype
+    W13 = torch.cat([inp.W13, (torch.randn(1, 2 * I, H, generator=g) / H ** 0.5).to(tdt)])
+    W2 = torch.cat([inp.W2, (torch.randn(1, H, I, generator=g) / I ** 0.5).to(tdt)])
+    dev = _to_dev(mi.LayerInputs(wl, inp.x, inp.Wg, W13, W2, None, inp.select_bias))
+    from routing_grouped_gemm_router_gb300.layer import MoELayer
+    layer = MoELayer(dev.Wg, dev.W13, dev.W2, wl.k, wl.mode, True, wl.scale, wl.n_group,
+                     wl.topk_group, None, dev.select_bias, n_shared=1)
+    out = layer(dev.x)
+    torch.cuda.synchronize()
+    mids = layer.intermediates(wl.T)
+    ids, w = O.route_sigmoid_grouped(oracle_logits(inp), wl.k, wl.n_group, wl.topk_group,
+                                     to_np(inp.select_bias), wl.scale)
+    ids, w = O.add_shared_experts(ids, w, wl.E, 1)
+    assert np.array_equal(to_np(mids["topk_ids"]), ids)
+    assert np.all(to_np(mids["topk_w"])[:, -1] == 1.0)
+    ref = O.moe_loop(to_np(inp.x), ids, w, weights_for_oracle(W13), weights_for_oracle(W2))
+    assert_close(to_np(out), ref, dtype)
