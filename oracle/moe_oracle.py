@@ -290,6 +290,45 @@ def moe_loop(x, ids, w, W13, W2, tokens=None, expert_map=None) -> np.ndarray:
     return out
 
 
+def masked_forward(x_masked, counts, W13, W2, row_w=None) -> np.ndarray:
+    """[P2 §9, DeepGEMM's "masked" layout; §7 fixed-capacity layouts for CUDA-graph decode]
+    tokens already bucketed per expert: x_masked[E, C, H] with counts[e] valid rows in
+    expert e's bucket. y[e, i] = row_w[e, i] * expert_e(x[e, i]) for i < counts[e]; rows past
+    the count are not computed (returned as NaN here, "not written")."""
+    x = f64(x_masked)
+    E, C, H = x.shape
+    y = np.full((E, C, H), np.nan)
+    for e in range(E):
+        n = int(counts[e])
+        if n == 0:
+            continue
+        ye = expert_ffn(x[e, :n], _expert(W13, e), _expert(W2, e))
+        wv = np.ones(n) if row_w is None else f64(row_w)[e, :n]
+        y[e, :n] = ye * wv[:, None]
+    return y
+
+
+def dispatch_masked(x, ids, w, E, capacity):
+    """Bucket the routed (token, slot) rows by expert, in ascending flat row, into a
+    fixed-capacity layout (the expert-parallel dispatch a masked layout stands for).
+    Returns x_masked[E, C, H], row_w[E, C], counts[E] and the (t, j) of every bucket row."""
+    x = f64(x)
+    T, k = ids.shape
+    xm = np.zeros((E, capacity, x.shape[1]))
+    wm = np.zeros((E, capacity))
+    counts = np.zeros(E, dtype=np.int64)
+    where = np.full((E, capacity, 2), -1, dtype=np.int64)
+    for r in range(T * k):
+        t, j = divmod(r, k)
+        e = int(ids[t, j])
+        i = counts[e]
+        if i >= capacity:
+            raise ValueError("capacity exceeded")
+        xm[e, i], wm[e, i], where[e, i] = x[t], w[t, j], (t, j)
+        counts[e] += 1
+    return xm, wm, counts, where
+
+
 def moe_dense(x, ids, w, W13, W2) -> np.ndarray:
     """Version B [P2 §3 moe_dense]: run EVERY expert on EVERY token, then combine with a
     [T, E] gate matrix holding the k routed weights per token (zeros elsewhere).

@@ -367,6 +367,24 @@ def test_shared_expert_adds_a_dense_ffn():
     assert np.abs(b2 - both).max() <= 1e-12 * np.abs(both).max()
 
 
+# ----------------------------------------------------------------- masked layout
+
+def test_masked_layout_recombines_to_the_routed_layer():
+    """Dispatching the routed rows into fixed-capacity expert buckets, running the masked
+    forward and summing each token's buckets back gives the per-expert loop's output."""
+    rng = np.random.default_rng(11)
+    x, Wg, W13, W2 = _rand_layer(rng, T=12, E=4)
+    out, ids, w, _ = O.moe_forward(x, Wg, W13, W2, 2)
+    xm, wm, counts, where = O.dispatch_masked(x, ids, w, 4, capacity=16)
+    ym = O.masked_forward(xm, counts, W13, W2, wm)
+    back = np.zeros_like(out)
+    for e in range(4):
+        for i in range(counts[e]):
+            back[where[e, i, 0]] += ym[e, i]
+    assert np.abs(back - out).max() <= 1e-12 * np.abs(out).max()
+    assert counts.sum() == 24 and np.isnan(ym[0, counts[0]:]).all()
+
+
 # ----------------------------------------------------------------- planted mistakes
 
 def _all_pins(golden_dir):
