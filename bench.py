@@ -46,6 +46,9 @@ def parse():
                    help="time eager launches instead of CUDA-graph replays of the step")
     p.add_argument("--shared", type=int, default=0,
                    help="shared experts (weight 1 on every token) added to the routed ones")
+    p.add_argument("--masked", action="store_true",
+                   help="fixed-capacity expert layout (tokens already bucketed per expert, no "
+                        "router/align): moe_masked_forward on the workload's shape")
     p.add_argument("--ep-half", action="store_true",
                    help="expert parallelism: odd experts on another device (expert_map -1); "
                         "the metric counts the rows of local experts only")
@@ -453,6 +456,68 @@ def run_ours(args, wl):
         dist.destroy_process_group()
 
 
+def run_masked(args, wl):
+    """moe_masked_forward on buckets filled by a seeded uniform top-k draw of T tokens."""
+    import torch
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    from routing_grouped_gemm_router_gb300 import _lib as L
+    g = torch.Generator(device=dev)
+    g.manual_seed(wl.seed)
+    T, k, E, H, I = wl.T, wl.k, wl.E, wl.H, wl.I
+    ids = torch.rand(T, E, generator=g, device=dev).topk(k, dim=1).indices
+    counts = torch.bincount(ids.flatten(), minlength=E).to(torch.int32)
+    B = 128
+    cap = max(B, (int(counts.max()) + B - 1) // B * B)
+    inp = mi.make_layer(wl, dev, seed=wl.seed)
+    xm = torch.randn(E, cap, H, generator=g, device=dev).to(torch.bfloat16)
+    rw = torch.rand(E, cap, generator=g, device=dev)
+    y = torch.empty(E, cap, H, dtype=torch.bfloat16, device=dev)
+    cfg = L.make_config(1, H, I, E, 1, L.MOE_BF16)
+    wsb = L.moe_masked_workspace_size(cfg, cap)
+    ws = torch.empty(wsb, dtype=torch.uint8, device=dev)
+
+    def step(sh=None):
+        L.moe_masked_forward(cfg, xm, counts, cap, rw, inp.W13, inp.W2, y, ws, wsb, sh)
+
+    for _ in range(max(3, args.warmup)):
+        step()
+    cap_s = torch.cuda.Stream(dev)
+    cap_s.wait_stream(torch.cuda.current_stream(dev))
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.stream(cap_s):
+        with torch.cuda.graph(graph, stream=cap_s):
+            step(cap_s.cuda_stream)
+    torch.cuda.current_stream(dev).wait_stream(cap_s)
+    for _ in range(3):
+        graph.replay()
+    torch.cuda.synchronize()
+    sampler = ClockSampler(0)
+    sampler.start()
+    time.sleep(0.3)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for _ in range(args.steps):
+        graph.replay()
+    e1.record()
+    torch.cuda.synchronize()
+    clocks = sampler.stop()
+    ms = e0.elapsed_time(e1) / args.steps
+    rows = int(counts.sum())
+    active = int((counts > 0).sum())
+    hbm, _, _, _ = peaks()
+    gbs = active * 3 * H * I * 2 / (ms * 1e-3) / 1e9
+    line = {"metric": METRIC, "value": 6 * rows * H * I / (ms * 1e-3) / 1e12, "unit": "TFLOPS",
+            "n_gpus": 1, "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
+            "timing": "CUDA-graph replays of moe_masked_forward",
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+            "data": "synthetic (uniform top-k draw bucketed per expert)",
+            "config": {"workload": wl.name + "+masked", "T": T, "H": H, "I": I, "E": E, "k": k,
+                       "capacity": cap, "rows": rows, "active_experts": active},
+            "weight_gbs": gbs, "weight_gbs_frac_of_hbm": gbs / hbm, "clocks": clocks}
+    print(json.dumps(line), flush=True)
+
+
 def main():
     args = parse()
     wl = workload(args.workload)
@@ -460,6 +525,8 @@ def main():
         wl = wl.with_T(args.tokens)
     if args.impl == "reference":
         run_reference(args, wl)
+    elif args.masked:
+        run_masked(args, wl)
     else:
         run_ours(args, wl)
 

@@ -229,6 +229,25 @@ moe_status_t moe_combine_local(const void* y, const int32_t* topk_ids, const int
                                int T, int k, int H, moe_dtype_t dtype, void* out,
                                cudaStream_t stream);
 
+/* Fixed-capacity ("masked") expert layout for decode without an align step (page §7:
+ * "fixed-capacity masked layouts that keep shapes static for CUDA Graphs"; §9: DeepGEMM's
+ * masked layout, a capacity per expert plus a valid-row count). Tokens arrive bucketed:
+ * x_masked[E, C, H] (cfg->dtype) with counts[e] valid rows (device int32 [E], 0..C) in
+ * expert e's bucket; for i < counts[e]:
+ *   y_masked[e, i, :] = row_w[e, i] * W2[e] (silu(W1[e] x) * (W3[e] x)),   x = x_masked[e, i]
+ * (row_w: device fp32 [E, C], or NULL for weight 1). Rows past a count are never written.
+ * C must be a multiple of moe_block_m(cfg); cfg->T, k and the router fields are ignored.
+ * moe_masked_table builds the equivalent sorted_ids / expert_ids / num_post_padded (the
+ * identity on valid rows, tiles past a count labelled -1) for callers of the GEMM entries. */
+moe_status_t moe_masked_table(const int32_t* counts, int E, int capacity, int block_m,
+                              int32_t* sorted_ids, int32_t* expert_ids,
+                              int32_t* num_post_padded, cudaStream_t stream);
+moe_status_t moe_masked_workspace_size(const moe_config_t* cfg, int capacity, size_t* bytes);
+moe_status_t moe_masked_forward(const moe_config_t* cfg, const void* x_masked,
+                                const int32_t* counts, int capacity, const float* row_w,
+                                const void* W13, const void* W2, void* y_masked, void* ws,
+                                size_t ws_bytes, cudaStream_t stream);
+
 /* The whole layer: route -> align (-> expert map) -> GEMM1+SwiGLU -> GEMM2 -> combine, all
  * enqueued on `stream` with no host round-trip. ws must hold moe_workspace_size(cfg) bytes, 256-byte
  * aligned; its intermediates sit at moe_workspace_layout(cfg) offsets. */

@@ -7,7 +7,8 @@ the C ABI) plus ``layer.MoELayer``, which owns the workspace and calls ``moe_for
 from ._lib import (EXPORTED, MOE_BF16, MOE_F32, MOE_ROUTE_SIGMOID_GROUPED,  # noqa: F401
                    MOE_ROUTE_SOFTMAX, MoeError, make_config, moe_abi_version, moe_align,
                    moe_align_workspace_size, moe_apply_expert_map, moe_block_m, moe_combine,
-                   moe_combine_local, moe_config_t,
+                   moe_combine_local, moe_config_t, moe_masked_forward, moe_masked_table,
+                   moe_masked_workspace_size,
                    moe_device_status, moe_expert_gemm1, moe_expert_gemm1_workspace_size,
                    moe_expert_gemm1_gathered, moe_gather_rows,
                    moe_expert_gemm2, moe_forward, moe_grouped_swiglu,

@@ -68,6 +68,9 @@ def _load():
         "moe_grouped_swiglu": (ST, [CFG, P, P, P, P, P, P, I32, P, P, P, SZ, P]),
         "moe_combine": (ST, [P, I32, I32, I32, I32, P, P]),
         "moe_apply_expert_map": (ST, [P, I32, P, I32, P]),
+        "moe_masked_table": (ST, [P, I32, I32, I32, P, P, P, P]),
+        "moe_masked_workspace_size": (ST, [CFG, I32, ctypes.POINTER(SZ)]),
+        "moe_masked_forward": (ST, [CFG, P, P, I32, P, P, P, P, P, SZ, P]),
         "moe_combine_local": (ST, [P, P, P, I32, I32, I32, I32, P, P]),
         "moe_forward": (ST, [CFG, P, P, P, P, P, P, SZ, P]),
         "moe_device_status": (I32, [I32]),
@@ -85,6 +88,7 @@ EXPORTED = ("moe_abi_version", "moe_status_string", "moe_block_m", "moe_max_padd
             "moe_expert_gemm1", "moe_gather_rows", "moe_expert_gemm1_gathered",
             "moe_grouped_swiglu_workspace_size", "moe_expert_gemm2",
             "moe_grouped_swiglu", "moe_combine", "moe_apply_expert_map", "moe_combine_local",
+            "moe_masked_table", "moe_masked_workspace_size", "moe_masked_forward",
             "moe_forward", "moe_device_status")
 
 
@@ -241,6 +245,27 @@ def moe_apply_expert_map(expert_ids, num_tiles, expert_map, E, stream=None):
 def moe_combine_local(y, topk_ids, expert_map, T, k, H, dtype, out, stream=None):
     _check("moe_combine_local", _lib.moe_combine_local(
         _ptr(y), _ptr(topk_ids), _ptr(expert_map), T, k, H, dtype, _ptr(out), _stream(stream)))
+
+
+def moe_masked_table(counts, E, capacity, block_m, sorted_ids, expert_ids, num_post_padded,
+                     stream=None):
+    _check("moe_masked_table", _lib.moe_masked_table(
+        _ptr(counts), E, capacity, block_m, _ptr(sorted_ids), _ptr(expert_ids),
+        _ptr(num_post_padded), _stream(stream)))
+
+
+def moe_masked_workspace_size(cfg, capacity) -> int:
+    out = ctypes.c_size_t(0)
+    _check("moe_masked_workspace_size",
+           _lib.moe_masked_workspace_size(ctypes.byref(cfg), capacity, ctypes.byref(out)))
+    return out.value
+
+
+def moe_masked_forward(cfg, x_masked, counts, capacity, row_w, W13, W2, y_masked, ws, ws_bytes,
+                       stream=None):
+    _check("moe_masked_forward", _lib.moe_masked_forward(
+        ctypes.byref(cfg), _ptr(x_masked), _ptr(counts), capacity, _ptr(row_w), _ptr(W13),
+        _ptr(W2), _ptr(y_masked), _ptr(ws), ws_bytes, _stream(stream)))
 
 
 def moe_forward(cfg, x, Wg, W13, W2, out, ws, ws_bytes, stream=None):

@@ -304,6 +304,37 @@ moe_status_t launch_apply_expert_map(int32_t* eid, int tiles, const int32_t* map
   return last_launch_status();
 }
 
+// ---- fixed-capacity (masked) layout: the table is the identity on valid rows ----------
+// Position p = e*C + i holds row p itself when i < counts[e], else the sentinel E*C; a tile
+// is labelled e when its first row is valid, else -1 (skipped). Optionally fills ones[].
+__global__ void __launch_bounds__(256) masked_table_kernel(const int32_t* __restrict__ counts,
+                                                           int E, int C, int B,
+                                                           int32_t* __restrict__ sid,
+                                                           int32_t* __restrict__ eid,
+                                                           int32_t* __restrict__ npp,
+                                                           float* __restrict__ ones) {
+  const int n = E * C;
+  for (int p = blockIdx.x * blockDim.x + threadIdx.x; p < n; p += gridDim.x * blockDim.x) {
+    const int e = p / C, i = p - e * C;
+    int c = counts[e];
+    if (c < 0 || c > C) {
+      atomicExch(&g_align_status, kStatusBadExpert);
+      c = c < 0 ? 0 : C;
+    }
+    sid[p] = i < c ? p : n;
+    if (ones) ones[p] = 1.f;
+    if (i % B == 0) eid[p / B] = i < c ? e : -1;
+  }
+  if (blockIdx.x == 0 && threadIdx.x == 0) *npp = n;
+}
+
+moe_status_t launch_masked_table(const int32_t* counts, int E, int C, int B, int32_t* sid,
+                                 int32_t* eid, int32_t* npp, float* ones, cudaStream_t s) {
+  const int blocks = std::max(1, std::min(ceil_div(E * C, 256), num_sms() * 4));
+  masked_table_kernel<<<blocks, 256, 0, s>>>(counts, E, C, B, sid, eid, npp, ones);
+  return last_launch_status();
+}
+
 static bool set_smem(const void* fn, size_t bytes) {
   if (bytes <= 48 * 1024) return true;
   return cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bytes) ==

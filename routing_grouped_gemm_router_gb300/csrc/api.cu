@@ -323,6 +323,94 @@ moe_status_t moe_combine_local(const void* y, const int32_t* topk_ids, const int
   return launch_combine_local(y, topk_ids, expert_map, T, k, H, dtype, out, stream);
 }
 
+// ---- fixed-capacity (masked) layout ---------------------------------------------------
+// The masked layout is the grouped GEMMs' padded order with the identity as the table: an
+// internal configuration with T = E*C rows, one slot each.
+static moe_status_t masked_cfg(const moe_config_t* cfg, int capacity, moe_config_t* m) {
+  if (!cfg) return MOE_ERR_INVALID_ARG;
+  moe_config_t c = *cfg;
+  c.T = 1;
+  c.k = 1;
+  c.mode = MOE_ROUTE_SOFTMAX;
+  c.n_group = c.topk_group = 1;
+  c.n_shared = 0;
+  c.expert_map = nullptr;
+  moe_status_t st = check_cfg(&c);
+  if (st != MOE_OK) return st;
+  const int B = block_m_for(c.dtype);
+  if (capacity < B || capacity % B || (int64_t)capacity * c.E > (int64_t)1 << 29)
+    return MOE_ERR_INVALID_ARG;
+  c.T = capacity * c.E;
+  *m = c;
+  return MOE_OK;
+}
+
+moe_status_t moe_masked_table(const int32_t* counts, int E, int capacity, int block_m,
+                              int32_t* sorted_ids, int32_t* expert_ids,
+                              int32_t* num_post_padded, cudaStream_t stream) {
+  if (!counts || !sorted_ids || !expert_ids || !num_post_padded || E < 1 || block_m < 1 ||
+      capacity < block_m || capacity % block_m)
+    return MOE_ERR_INVALID_ARG;
+  return launch_masked_table(counts, E, capacity, block_m, sorted_ids, expert_ids,
+                             num_post_padded, nullptr, stream);
+}
+
+moe_status_t moe_masked_workspace_size(const moe_config_t* cfg, int capacity, size_t* bytes) {
+  moe_config_t m;
+  moe_status_t st = masked_cfg(cfg, capacity, &m);
+  if (st != MOE_OK) return st;
+  if (!bytes) return MOE_ERR_INVALID_ARG;
+  const size_t n = (size_t)m.T, B = block_m_for(m.dtype);
+  *bytes = align_up(n * 4, 256) + align_up(n / B * 4, 256) + 256 + align_up(n * 4, 256) +
+           align_up(n * m.I * dtype_size(m.dtype), 256);
+  return MOE_OK;
+}
+
+moe_status_t moe_masked_forward(const moe_config_t* cfg, const void* x_masked,
+                                const int32_t* counts, int capacity, const float* row_w,
+                                const void* W13, const void* W2, void* y_masked, void* ws,
+                                size_t ws_bytes, cudaStream_t stream) {
+  moe_config_t m;
+  moe_status_t st = masked_cfg(cfg, capacity, &m);
+  if (st != MOE_OK) return st;
+  if (!x_masked || !counts || !W13 || !W2 || !y_masked) return MOE_ERR_INVALID_ARG;
+  size_t need = 0;
+  moe_masked_workspace_size(cfg, capacity, &need);
+  if (!ws || ws_bytes < need || ((uintptr_t)ws & 255u)) return MOE_ERR_WORKSPACE;
+  const size_t n = (size_t)m.T;
+  const int B = block_m_for(m.dtype);
+  uint8_t* b = (uint8_t*)ws;
+  int32_t* sid = (int32_t*)b;
+  b += align_up(n * 4, 256);
+  int32_t* eid = (int32_t*)b;
+  b += align_up(n / B * 4, 256);
+  int32_t* npp = (int32_t*)b;
+  b += 256;
+  float* ones = (float*)b;
+  b += align_up(n * 4, 256);
+  void* act = b;
+  st = launch_masked_table(counts, m.E, capacity, B, sid, eid, npp, row_w ? nullptr : ones,
+                           stream);
+  if (st != MOE_OK) return st;
+  // The masked rows are already in padded order: GEMM1 reads them directly (bf16) or gathers
+  // them with one slot per row (fp32). The row extent handed to the kernels is E*C, the size
+  // of the caller's buffers, so tile rows past it read as zeros.
+  const int rows = (int)n;
+  const float* w = row_w ? row_w : ones;
+  if (m.dtype == MOE_BF16) {
+    if (!aligned16(x_masked) || !aligned16(W13) || !aligned16(W2) || !aligned16(y_masked))
+      return MOE_ERR_INVALID_ARG;
+    st = launch_gemm1_tc(m, x_masked, W13, sid, eid, npp, B, rows, act, stream);
+    if (st != MOE_OK) return st;
+    return launch_gemm2_tc(m, act, W2, sid, eid, npp, B, rows, w, y_masked, stream);
+  }
+  st = launch_gemm1_simt(m, (const float*)x_masked, (const float*)W13, sid, eid, npp, B, rows,
+                         (float*)act, stream);
+  if (st != MOE_OK) return st;
+  return launch_gemm2_simt(m, (const float*)act, (const float*)W2, sid, eid, npp, B, rows, w,
+                           (float*)y_masked, stream);
+}
+
 moe_status_t moe_forward(const moe_config_t* c, const void* x, const void* Wg, const void* W13,
                          const void* W2, void* out, void* ws, size_t ws_bytes,
                          cudaStream_t stream) {

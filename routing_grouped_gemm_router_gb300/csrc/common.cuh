@@ -61,6 +61,8 @@ moe_status_t launch_gemm2_tc(const moe_config_t& c, const void* act, const void*
                              cudaStream_t s);
 moe_status_t launch_gather_rows(const void* x, const int32_t* sid, const int32_t* npp,
                                 int n_rows, int k, int row_bytes, void* xs, cudaStream_t s);
+moe_status_t launch_masked_table(const int32_t* counts, int E, int C, int B, int32_t* sid,
+                                 int32_t* eid, int32_t* npp, float* ones, cudaStream_t s);
 moe_status_t launch_apply_expert_map(int32_t* eid, int tiles, const int32_t* map, int E,
                                      cudaStream_t s);
 moe_status_t launch_combine_local(const void* y, const int32_t* ids, const int32_t* map, int T,

@@ -509,3 +509,50 @@ def test_shared_expert(L, dtype):
     assert np.all(to_np(mids["topk_w"])[:, -1] == 1.0)
     ref = O.moe_loop(to_np(inp.x), ids, w, weights_for_oracle(W13), weights_for_oracle(W2))
     assert_close(to_np(out), ref, dtype)
+
+
+# --------------------------------------------------------------------- fixed-capacity layout
+
+@pytest.mark.parametrize("dtype,with_w", [("bf16", True), ("bf16", False), ("f32", True)])
+def test_masked_layout(L, dtype, with_w):
+    """Tokens bucketed per expert with a fixed capacity: valid rows equal the oracle's
+    masked forward; rows past each count are never written (canary survives)."""
+    H, I = (256, 384) if dtype == "bf16" else (64, 96)
+    B = 128 if dtype == "bf16" else 16
+    wl = mi.Workload("masked", T=150, H=H, I=I, E=8, k=2, dtype=dtype, seed=51)
+    inp = mi.make_layer(wl, "cpu")
+    ids, w = O.route_softmax(oracle_logits(inp), wl.k)
+    cap = -(-int(np.bincount(ids.ravel(), minlength=wl.E).max()) // B) * B + B
+    xm, wm, counts, _ = O.dispatch_masked(to_np(inp.x), ids, w, wl.E, cap)
+    tdt = inp.x.dtype
+    xm_d = torch.tensor(xm, dtype=tdt, device=DEV)
+    wm_d = torch.tensor(wm, dtype=torch.float32, device=DEV) if with_w else None
+    cnt_d = torch.tensor(counts, dtype=torch.int32, device=DEV)
+    y = torch.full((wl.E, cap, H), float("nan"), dtype=tdt, device=DEV)
+    cfg = L.make_config(1, H, I, wl.E, 1, L.MOE_BF16 if dtype == "bf16" else L.MOE_F32)
+    wsb = L.moe_masked_workspace_size(cfg, cap)
+    ws = torch.empty(wsb, dtype=torch.uint8, device=DEV)
+    W13, W2 = inp.W13.to(DEV), inp.W2.to(DEV)
+    for rep in range(2):
+        L.moe_masked_forward(cfg, xm_d, cnt_d, cap, wm_d, W13, W2, y, ws, wsb)
+    torch.cuda.synchronize()
+    ref = O.masked_forward(to_np(xm_d), counts, weights_for_oracle(inp.W13),
+                           weights_for_oracle(inp.W2), wm if with_w else None)
+    got = to_np(y)
+    valid = ~np.isnan(ref[:, :, 0])
+    assert np.array_equal(valid, np.arange(cap)[None, :] < counts[:, None])
+    assert np.all(np.isnan(got[~valid])), "a row past an expert's count was written"
+    assert_close(got[valid], ref[valid], dtype)
+    # the table alone: identity on valid rows, tiles past a count labelled -1
+    n = wl.E * cap
+    sid = torch.empty(n, dtype=torch.int32, device=DEV)
+    eid = torch.empty(n // B, dtype=torch.int32, device=DEV)
+    npp = torch.empty(1, dtype=torch.int32, device=DEV)
+    L.moe_masked_table(cnt_d, wl.E, cap, B, sid, eid, npp)
+    torch.cuda.synchronize()
+    p = np.arange(n)
+    exp_sid = np.where((p % cap) < counts[p // cap], p, n)
+    t = np.arange(n // B)
+    exp_eid = np.where(((t * B) % cap) < counts[(t * B) // cap], (t * B) // cap, -1)
+    assert np.array_equal(sid.cpu().numpy(), exp_sid) and int(npp.item()) == n
+    assert np.array_equal(eid.cpu().numpy(), exp_eid)
