@@ -49,6 +49,34 @@ def f64(a) -> np.ndarray:
     return np.asarray(a, dtype=np.float64)
 
 
+def e4m3_to_f64(codes: np.ndarray) -> np.ndarray:
+    """Decode FP8 E4M3 (OCP "FN" variant) bytes from the format's definition: 1 sign bit,
+    4 exponent bits (bias 7), 3 mantissa bits; exponent 0 is subnormal (m/8 * 2^-6); the
+    all-ones code S.1111.111 is NaN (no infinities), so the largest finite value is 448."""
+    c = np.asarray(codes, dtype=np.uint8).astype(np.int64)
+    sign = np.where(c & 0x80, -1.0, 1.0)
+    e = (c >> 3) & 0xF
+    m = c & 0x7
+    val = np.where(e == 0, m / 8.0 * 2.0 ** -6, (1.0 + m / 8.0) * 2.0 ** (e - 7))
+    val = np.where((e == 0xF) & (m == 0x7), np.nan, val)
+    return sign * val
+
+
+def dequant_blockwise(codes: np.ndarray, scales: np.ndarray, block: int = 128) -> np.ndarray:
+    """FP8 expert weights with their scales ([P2] §8: one byte per weight; §9: the FP8 weight
+    variants of the fused kernel; §10: FP8 scale handling checked against a wide reference):
+    w[..., n, c] = e4m3(codes[..., n, c]) * scales[..., n // block, c // block].
+    Reading: the pages name FP8 scales but not their granularity; one scale per
+    block x block tile of each expert matrix (block = 128) is the plainest form that
+    covers per-expert scales (one tile) as a special case."""
+    v = e4m3_to_f64(codes)
+    sc = f64(scales)
+    n, k = v.shape[-2], v.shape[-1]
+    rows = np.arange(n) // block
+    cols = np.arange(k) // block
+    return v * sc[..., rows[:, None], cols[None, :]]
+
+
 # ----------------------------------------------------------------------------- top-k
 
 def topk_desc(keys: np.ndarray, k: int) -> np.ndarray:

@@ -385,6 +385,32 @@ def test_masked_layout_recombines_to_the_routed_layer():
     assert counts.sum() == 24 and np.isnan(ym[0, counts[0]:]).all()
 
 
+# ----------------------------------------------------------------- FP8 weights
+
+def test_e4m3_decoder_known_codes():
+    """Values fixed by the E4M3 definition: 1.0 = 0.0111.000, 448 = 0.1111.110 (largest),
+    smallest subnormal 2^-9 = 0.0000.001, smallest normal 2^-6, -2 = 1.1000.000, NaN = x.1111.111."""
+    vals = O.e4m3_to_f64(np.array([0x38, 0x7E, 0x01, 0x08, 0xC0, 0x00, 0x80, 0x3C]))
+    assert vals.tolist() == [1.0, 448.0, 2.0 ** -9, 2.0 ** -6, -2.0, 0.0, -0.0, 1.5]
+    assert np.isnan(O.e4m3_to_f64(np.array([0x7F, 0xFF]))).all()
+
+
+def test_e4m3_decoder_matches_torch_on_all_codes():
+    codes = np.arange(256, dtype=np.uint8)
+    ref = torch.from_numpy(codes).view(torch.float8_e4m3fn).float().double().numpy()
+    got = O.e4m3_to_f64(codes)
+    both_nan = np.isnan(ref) & np.isnan(got)
+    assert np.array_equal(got[~both_nan], ref[~both_nan]) and np.isnan(got).sum() == 2
+
+
+def test_dequant_blockwise_uses_the_right_block():
+    codes = np.full((1, 200, 300), 0x38, dtype=np.uint8)   # all ones
+    scales = np.arange(1 * 2 * 3, dtype=np.float64).reshape(1, 2, 3) + 1.0
+    w = O.dequant_blockwise(codes, scales)
+    assert w[0, 0, 0] == 1 and w[0, 127, 127] == 1 and w[0, 128, 0] == 4
+    assert w[0, 0, 128] == 2 and w[0, 199, 299] == 6 and w[0, 130, 260] == 6
+
+
 # ----------------------------------------------------------------- planted mistakes
 
 def _all_pins(golden_dir):
