@@ -77,6 +77,16 @@ def dequant_blockwise(codes: np.ndarray, scales: np.ndarray, block: int = 128) -
     return v * sc[..., rows[:, None], cols[None, :]]
 
 
+def dequant_w13(codes13: np.ndarray, scales13: np.ndarray, block: int = 128) -> np.ndarray:
+    """FP8 W13[E, 2I, H]: the gate rows 0..I-1 and the up rows I..2I-1 are two matrices,
+    each with its own block grid (scales13[E, 2, ceil(I/block), ceil(H/block)]), as when
+    gate and up projections are quantised separately and then stacked."""
+    I = codes13.shape[-2] // 2
+    gate = dequant_blockwise(codes13[..., :I, :], scales13[:, 0], block)
+    up = dequant_blockwise(codes13[..., I:, :], scales13[:, 1], block)
+    return np.concatenate([gate, up], axis=-2)
+
+
 # ----------------------------------------------------------------------------- top-k
 
 def topk_desc(keys: np.ndarray, k: int) -> np.ndarray:

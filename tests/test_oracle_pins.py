@@ -411,6 +411,20 @@ def test_dequant_blockwise_uses_the_right_block():
     assert w[0, 0, 128] == 2 and w[0, 199, 299] == 6 and w[0, 130, 260] == 6
 
 
+def test_dequant_w13_gate_and_up_have_their_own_grids():
+    I, H = 200, 130
+    codes = np.full((2, 2 * I, H), 0x38, dtype=np.uint8)          # all ones
+    sc = np.zeros((2, 2, 2, 2))
+    sc[:, 0] = [[1.0, 2.0], [3.0, 4.0]]
+    sc[:, 1] = [[10.0, 20.0], [30.0, 40.0]]
+    w = O.dequant_w13(codes, sc)
+    assert w.shape == (2, 2 * I, H)
+    assert w[1, 0, 0] == 1 and w[1, 127, 129] == 2 and w[1, 128, 0] == 3 and w[1, I - 1, 128] == 4
+    # the first up row starts the up grid (a single stacked grid would give block 1 here)
+    assert w[1, I, 0] == 10 and w[1, I + 127, 128] == 20 and w[1, I + 128, 0] == 30
+    assert w[0, 2 * I - 1, H - 1] == 40
+
+
 # ----------------------------------------------------------------- planted mistakes
 
 def _all_pins(golden_dir):
