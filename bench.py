@@ -52,6 +52,9 @@ def parse():
     p.add_argument("--ep-half", action="store_true",
                    help="expert parallelism: odd experts on another device (expert_map -1); "
                         "the metric counts the rows of local experts only")
+    p.add_argument("--fp8", action="store_true",
+                   help="FP8 E4M3 expert weights with 128x128 block scales (the seeded bf16 "
+                        "weights quantised); tokens, router and GEMM arithmetic stay bf16")
     p.add_argument("--tokens", type=int, default=0,
                    help="override T of the workload (smaller cases for profiling)")
     return p.parse_args()
@@ -250,13 +253,19 @@ def run_ours(args, wl):
                                                    device=dev) / wl.H ** 0.5).to(inp.W13.dtype)])
         inp.W2 = torch.cat([inp.W2, (torch.randn(args.shared, wl.H, wl.I, generator=g,
                                                  device=dev) / wl.I ** 0.5).to(inp.W2.dtype)])
+    sc13 = sc2 = None
+    if args.fp8:  # codes + block scales replace the bf16 expert weights
+        inp.W13, sc13 = mi.quantize_fp8_w13(inp.W13)
+        inp.W2, sc2 = mi.quantize_fp8_blocks(inp.W2)
+        torch.cuda.empty_cache()
     emap = None
     if args.ep_half:
         emap = torch.tensor([e if e % 2 == 0 else -1 for e in range(wl.E + args.shared)],
                             dtype=torch.int32, device=dev)
     layer = MoELayer(inp.Wg, inp.W13, inp.W2, wl.k, wl.mode, wl.renormalize, wl.scale,
                      wl.n_group, wl.topk_group, inp.logit_bias, inp.select_bias, emap,
-                     n_shared=args.shared)
+                     n_shared=args.shared, w13_scale=sc13, w2_scale=sc2)
+    wbytes = 1 if args.fp8 else inp.x.element_size()  # bytes per expert weight
     # the align step, the grouped GEMMs and the combine see shared experts as ordinary ones
     T, k, E, H, I = wl.T, wl.k + args.shared, wl.E + args.shared, wl.H, wl.I
     cfg = layer.config(T)
@@ -399,7 +408,7 @@ def run_ours(args, wl):
     src = os.path.join(ROOT, "routing_grouped_gemm_router_gb300", "csrc", "gemm_tc2.cu")
     if is_decode(wl):
         # decode is HBM-bound: GEMM1 streams the gate/up weights of every active expert
-        w_bytes = active * 2 * H * I * 2
+        w_bytes = active * 2 * H * I * wbytes
         roof = {"bound": "hbm", "achieved": w_bytes / (stage["gemm1"] * 1e-3) / 1e9,
                 "peak": hbm, "unit": "GB/s", "kernel": "gemm1 (gate/up grouped GEMM)",
                 "algorithmic_bytes_per_launch": w_bytes,
@@ -412,7 +421,7 @@ def run_ours(args, wl):
                 "algorithmic_flops_per_launch": g1_flops,
                 "peak_kind": f"{peak_src} bf16 sustained (kernel timed inside a long step loop)"}
     roof["frac"] = roof["achieved"] / roof["peak"]
-    roof["traffic"] = profile_traffic("gemm1", wl.name, src)
+    roof["traffic"] = profile_traffic("gemm1" + ("_fp8" if args.fp8 else ""), wl.name, src)
 
     line = {"metric": METRIC, "value": value, "unit": "TFLOPS", "n_gpus": world,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
@@ -421,12 +430,15 @@ def run_ours(args, wl):
             "dtype": "bf16" if wl.dtype == "bf16" else "f32",
             "data": "synthetic (seeded N(0,1) tokens, N(0,1/fan_in) weights, random init)",
             "config": {"workload": wl.name + ("+ep-half" if emap is not None else "")
-                       + (f"+shared{args.shared}" if args.shared else ""),
+                       + (f"+shared{args.shared}" if args.shared else "")
+                       + ("+fp8" if args.fp8 else ""),
+                       "expert_weights": "fp8-e4m3, fp32 scale per 128x128 block" if args.fp8
+                       else ("bf16" if wl.dtype == "bf16" else "f32"),
                        "T": T, "H": H, "I": I, "E": wl.E, "k": wl.k, "n_shared": args.shared,
                        "mode": "sigmoid-grouped" if wl.mode else "softmax",
                        "global_batch": T * world, "parallelism": f"replicas x{world}",
                        "l2": "inputs larger than L2 (expert weights "
-                             f"{E * 3 * H * I * inp.x.element_size() / 1e9:.2f} GB)",
+                             f"{E * 3 * H * I * wbytes / 1e9:.2f} GB)",
                        "block_m": B, "num_post_padded": npp, "active_experts": active},
             "stages_ms": {n: round(v, 5) for n, v in stage.items()},
             "roofline": roof,
@@ -435,12 +447,12 @@ def run_ours(args, wl):
             "gpu_launches": launches_per_step * args.steps,
             "clocks": clocks}
     if is_decode(wl):
-        line["weight_gbs"] = active * 3 * H * I * 2 / (ms * 1e-3) / 1e9
+        line["weight_gbs"] = active * 3 * H * I * wbytes / (ms * 1e-3) / 1e9
         line["weight_gbs_frac_of_hbm"] = line["weight_gbs"] / hbm
     else:
         line["frac_of_bf16_peak"] = value / bf16_sus
 
-    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+    if rank == 0 and world == 1 and not args.no_cpu_baseline and not args.fp8:
         del layer
         x, Wg, W13, W2, lb, sb = host_copies(inp)
         n = args.cpu_sample_tokens or default_sample(wl)

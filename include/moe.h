@@ -16,7 +16,8 @@
  *  - Tensors are DEVICE pointers, contiguous and row-major, in nn.Linear [E, N, K] layout:
  *    x[T,H], Wg[E,H], W13[E,2I,H] (rows 0..I-1 = gate projection W1, rows I..2I-1 = up
  *    projection W3), W2[E,H,I], y[T*k,H], out[T,H]. x's dtype (cfg->dtype) is the dtype of
- *    Wg, W13, W2, act, y and out. logits, topk_w and the biases are always fp32; ids int32.
+ *    Wg, act, y and out, and of W13 and W2 unless cfg->weight_format selects FP8 weights.
+ *    logits, topk_w, the biases and the weight scales are always fp32; ids int32.
  *  - bf16 tensors must start on a 16-byte boundary and H, I must be multiples of 8
  *    (tensor-memory-access copies move 16-byte units).
  *  - The CALLER owns every buffer, workspaces included. The library never allocates or
@@ -43,7 +44,7 @@
 extern "C" {
 #endif
 
-#define MOE_ABI_VERSION 2
+#define MOE_ABI_VERSION 3
 
 typedef enum {
   MOE_OK = 0,
@@ -66,6 +67,21 @@ typedef enum {
    * (renormalize=1) or scale * s (renormalize=0). */
   MOE_ROUTE_SIGMOID_GROUPED = 1
 } moe_route_mode_t;
+
+/* Storage of the expert weights W13 and W2 (page §8: an FP8 expert holds one byte per
+ * weight; §9: the FP8 weight variants of the fused kernel; §10: FP8 scale handling).
+ * The router weight Wg always has cfg->dtype. */
+typedef enum {
+  MOE_WEIGHTS_NATIVE = 0, /* W13, W2 in cfg->dtype */
+  /* W13, W2 hold FP8 E4M3 (OCP "FN": bias 7, max 448, no infinities) bytes, same shapes;
+   * the weight used is code * scale of the code's 128 x 128 block (fp32 scales):
+   *   W13: w13_scale[E', 2, ceil(I/128), ceil(H/128)] - grid 0 covers the gate rows
+   *        0..I-1, grid 1 the up rows I..2I-1 (row blocks start at row 0 and row I);
+   *   W2 : w2_scale[E', ceil(H/128), ceil(I/128)].
+   * E' = E + n_shared. Needs dtype MOE_BF16 and H, I multiples of 16. The tensor cores
+   * see bf16(code * scale): exact when the scale is a power of two. */
+  MOE_WEIGHTS_FP8_E4M3_B128 = 1
+} moe_weight_format_t;
 
 typedef struct moe_config {
   int T;                    /* tokens, >= 1 */
@@ -92,6 +108,9 @@ typedef struct moe_config {
    * the combine then see k + n_shared slots and E + n_shared experts (expert_map, if given,
    * has E + n_shared entries). */
   int n_shared;
+  moe_weight_format_t weight_format; /* MOE_WEIGHTS_NATIVE (0) unless FP8 weights */
+  const float* w13_scale;            /* device fp32 block scales of W13 (FP8 only) */
+  const float* w2_scale;             /* device fp32 block scales of W2 (FP8 only) */
 } moe_config_t;
 
 /* Byte offsets of the intermediates inside a moe_forward workspace (256-byte aligned). */

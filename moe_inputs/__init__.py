@@ -131,6 +131,36 @@ def make_layer(wl: Workload, device="cpu", seed: Optional[int] = None) -> LayerI
     return LayerInputs(wl, x, Wg, W13, W2, lb, sb)
 
 
+def quantize_fp8_blocks(W: torch.Tensor, block: int = 128):
+    """FP8 E4M3 codes (uint8) and fp32 scales of W[E, N, K], one scale per block x block
+    tile: the smallest power of two with amax / scale <= 448 (the E4M3 maximum), so that
+    code * scale reproduces W to E4M3 precision. Input preparation only: the layer takes the
+    codes and scales as they are, and so does the oracle."""
+    E, N, K = W.shape
+    RB, KB = -(-N // block), -(-K // block)
+    codes = torch.empty((E, N, K), dtype=torch.uint8, device=W.device)
+    scales = torch.empty((E, RB, KB), dtype=torch.float32, device=W.device)
+    for e in range(E):
+        w = torch.zeros(RB * block, KB * block, dtype=torch.float32, device=W.device)
+        w[:N, :K] = W[e].float()
+        amax = w.view(RB, block, KB, block).abs().amax(dim=(1, 3)) / 448.0
+        m, ex = torch.frexp(amax.clamp_min(2.0 ** -100))   # amax = m * 2^ex, m in [0.5, 1)
+        sc = torch.ldexp(torch.ones_like(m), ex - (m == 0.5).to(ex.dtype))
+        q = w / sc.repeat_interleave(block, 0).repeat_interleave(block, 1)
+        codes[e] = q[:N, :K].to(torch.float8_e4m3fn).view(torch.uint8)
+        scales[e] = sc
+    return codes, scales
+
+
+def quantize_fp8_w13(W13: torch.Tensor, block: int = 128):
+    """Codes of W13[E, 2I, H] and scales[E, 2, ceil(I/block), ceil(H/block)]: the gate rows
+    and the up rows are quantised as two separate matrices."""
+    I = W13.shape[1] // 2
+    cg, sg = quantize_fp8_blocks(W13[:, :I], block)
+    cu, su = quantize_fp8_blocks(W13[:, I:], block)
+    return torch.cat([cg, cu], 1), torch.stack([sg, su], 1)
+
+
 def redraw_rows(x: torch.Tensor, rows, seed: int, attempt: int) -> None:
     """Replace token rows ``rows`` of ``x`` in place by fresh N(0,1) draws.
 

@@ -17,6 +17,7 @@ LIB_PATH = os.path.join(_PKG, "libmoe_gb300.so")
 MOE_OK, MOE_ERR_INVALID_ARG, MOE_ERR_UNSUPPORTED, MOE_ERR_WORKSPACE, MOE_ERR_CUDA = range(5)
 MOE_F32, MOE_BF16 = 0, 1
 MOE_ROUTE_SOFTMAX, MOE_ROUTE_SIGMOID_GROUPED = 0, 1
+MOE_WEIGHTS_NATIVE, MOE_WEIGHTS_FP8_E4M3_B128 = 0, 1
 
 
 class MoeError(RuntimeError):
@@ -31,7 +32,9 @@ class moe_config_t(ctypes.Structure):
                 ("mode", ctypes.c_int), ("renormalize", ctypes.c_int), ("scale", ctypes.c_float),
                 ("n_group", ctypes.c_int), ("topk_group", ctypes.c_int),
                 ("logit_bias", ctypes.c_void_p), ("select_bias", ctypes.c_void_p),
-                ("expert_map", ctypes.c_void_p), ("n_shared", ctypes.c_int)]
+                ("expert_map", ctypes.c_void_p), ("n_shared", ctypes.c_int),
+                ("weight_format", ctypes.c_int), ("w13_scale", ctypes.c_void_p),
+                ("w2_scale", ctypes.c_void_p)]
 
 
 class moe_ws_layout_t(ctypes.Structure):
@@ -126,12 +129,16 @@ def status_string(st: int) -> str:
 
 def make_config(T, H, I, E, k, dtype=MOE_BF16, mode=MOE_ROUTE_SOFTMAX, renormalize=True,
                 scale=1.0, n_group=1, topk_group=1, logit_bias=None, select_bias=None,
-                expert_map=None, n_shared=0):
-    """Build a ``moe_config_t``; biases (fp32) and expert_map (int32) are device tensors
-    the caller keeps alive."""
+                expert_map=None, n_shared=0, w13_scale=None, w2_scale=None):
+    """Build a ``moe_config_t``; biases (fp32), expert_map (int32) and the FP8 block scales
+    (fp32) are device tensors the caller keeps alive. Passing both scales selects FP8
+    E4M3 expert weights (W13/W2 then hold the codes as uint8 / float8_e4m3fn)."""
+    fp8 = w13_scale is not None or w2_scale is not None
     return moe_config_t(T, H, I, E, k, dtype, mode, int(bool(renormalize)), float(scale),
                         n_group, topk_group, _ptr(logit_bias), _ptr(select_bias),
-                        _ptr(expert_map), int(n_shared))
+                        _ptr(expert_map), int(n_shared),
+                        MOE_WEIGHTS_FP8_E4M3_B128 if fp8 else MOE_WEIGHTS_NATIVE,
+                        _ptr(w13_scale), _ptr(w2_scale))
 
 
 def moe_abi_version() -> int:

@@ -40,6 +40,16 @@ static moe_status_t check_cfg(const moe_config_t* c) {
     if ((int64_t)c->topk_group * (c->E / c->n_group) < c->k) return MOE_ERR_INVALID_ARG;
   }
   if (c->n_shared < 0 || c->n_shared > 8 || c->k + c->n_shared > 32) return MOE_ERR_INVALID_ARG;
+  if (c->weight_format != MOE_WEIGHTS_NATIVE && c->weight_format != MOE_WEIGHTS_FP8_E4M3_B128)
+    return MOE_ERR_INVALID_ARG;
+  if (c->weight_format == MOE_WEIGHTS_FP8_E4M3_B128) {
+    // FP8 codes feed the bf16 tensor-core path; byte rows must be 16-byte multiples.
+    if (c->dtype != MOE_BF16) return MOE_ERR_UNSUPPORTED;
+    if (c->H % 16 || c->I % 16) return MOE_ERR_INVALID_ARG;
+    if (!c->w13_scale || !c->w2_scale || ((uintptr_t)c->w13_scale & 3u) ||
+        ((uintptr_t)c->w2_scale & 3u))
+      return MOE_ERR_INVALID_ARG;
+  }
   if (c->E + c->n_shared > kMaxE) return MOE_ERR_UNSUPPORTED;
   if ((int64_t)c->T * (c->k + c->n_shared) > (int64_t)1 << 30) return MOE_ERR_UNSUPPORTED;
   return MOE_OK;

@@ -46,13 +46,13 @@ using namespace ptx;
 __device__ int g_grouped_status;
 
 enum Mode { kGemm1 = 0, kGemm2 = 1 };
-constexpr int kStages = 6;
 constexpr int kMaxTiles = 4096;  // 128-row m-tiles per launch (max_padded <= 524288)
 constexpr int kMaxRuns = 1024;   // run boundaries in the m-tile sequence (<= 2E)
 constexpr int kAccs = 2;                 // 256-column accumulators in TMEM
 constexpr int kTmemCols = 256 * kAccs;
 constexpr int A_BYTES = BM * 128;
 constexpr int B_BYTES = 128 * 128;  // this CTA's half of an N=256 weight panel
+constexpr int RAW_BYTES = 128 * BK;  // the same half panel as FP8 codes (no swizzle)
 
 struct Params {
   int n_rows;     // valid flat rows T*k; sorted_ids >= n_rows are padding
@@ -67,25 +67,45 @@ struct Params {
   const float* topk_w;
   void* out;
   int64_t ld_out;
+  // FP8 weights: fp32 scale of each 128 x 128 block, [slots][grids][row blocks][k blocks]
+  // (GEMM1: grid 0 = gate rows, grid 1 = up rows; GEMM2: one grid).
+  const float* scale;
+  int sc_rb, sc_kb;  // row blocks and k blocks of one grid
+  int n_slots;       // expert slots the weights hold
 };
 
-template <int MODE>
+// FP8 weights add kCvtGroups groups of kCvtWarps converter warps (6..) and a ring of raw
+// FP8 tiles; the shared memory they take costs two pipeline stages. Group i owns the ring
+// slots s with s % kCvtGroups == i (the slot count is a multiple of the group count), so
+// every raw-tile barrier is waited on by one group, phase after phase: a parity wait must
+// never start while the phase before the awaited one is still open, or it would pass at
+// once. Each group then has several stage-times for a stage, and each converter warp
+// arrives once on the leader's stage barrier (from the peer a cluster-scope release).
+template <bool FP8>
 struct Roles {
   static constexpr int kProdWarps = 1;
   static constexpr int kMmaWarp = 1;
   static constexpr int kEpiWarp0 = 2;
-  static constexpr int kThreads = 6 * 32;
+  static constexpr int kCvtWarp0 = 6;
+  static constexpr int kCvtGroups = 2;
+  static constexpr int kCvtWarps = 4;  // warps per group; each converts 128 / kCvtWarps rows
+  static constexpr int kThreads = (FP8 ? 6 + kCvtWarps * kCvtGroups : 6) * 32;
   // The leader's full barrier of a stage completes on the leader's expect_tx arrival, which
-  // counts the TMA bytes of BOTH CTAs: their copies all complete on this one barrier.
-  static constexpr int kFullArrivals = 1;
-  static constexpr uint32_t kPairTmaBytes = 2u * (A_BYTES + B_BYTES);
+  // counts the TMA bytes of BOTH CTAs: their copies all complete on this one barrier. With
+  // FP8 weights the B halves are written by the converter warps of both CTAs instead: the
+  // four converter warps of each CTA arrive once.
+  static constexpr int kFullArrivals = FP8 ? 1 + 2 * kCvtWarps : 1;
+  static constexpr uint32_t kPairTmaBytes = FP8 ? 2u * A_BYTES : 2u * (A_BYTES + B_BYTES);
 };
 
+template <bool FP8>
 struct Layout {
+  static constexpr int kStages = FP8 ? 4 : 6;
   static constexpr size_t a = 0;
   static constexpr size_t b = a + (size_t)kStages * A_BYTES;
-  static constexpr size_t bars = b + (size_t)kStages * B_BYTES;
-  static constexpr size_t n_bars = 2 * kStages + 5;
+  static constexpr size_t raw = b + (size_t)kStages * B_BYTES;
+  static constexpr size_t bars = raw + (FP8 ? (size_t)kStages * RAW_BYTES : 0);
+  static constexpr size_t n_bars = 3 * kStages + 5;  // full, empty, raw full; tfull, tempty, drain
   static constexpr size_t misc = bars + n_bars * 8;  // tmem slot, abort flag, run count
   static constexpr size_t bnd = misc + 16;
   static constexpr size_t run_first = bnd + kMaxRuns * 4;
@@ -96,7 +116,10 @@ struct Layout {
   static constexpr size_t end = flags + kMaxTiles;
   static constexpr size_t bytes = 1024 + end;  // + alignment slack
 };
-static_assert(Layout::bytes <= 232448, "shared memory");
+static_assert(Layout<false>::bytes <= 232448, "shared memory");
+static_assert(Layout<true>::bytes <= 232448, "shared memory");
+static_assert(Layout<true>::kStages % Roles<true>::kCvtGroups == 0,
+              "each converter group must own whole ring slots");
 
 struct Table {
   const int* run_first;
@@ -123,33 +146,60 @@ __device__ __forceinline__ void item_of(int w, int n_tiles, const Table& tb, int
   e = tb.run_e[lo];
 }
 
-template <int MODE>
-__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Roles<MODE>::kThreads, 1)
+// E4M3 -> bf16 with integer operations only. An E4M3 byte s.eeee.mmm moved into the bf16
+// bit pattern s.0000eeee.mmm0000 is, read as bf16, the code's value times 2^-120, for
+// subnormal codes too (E4M3 exponent 0 lands in the bf16 subnormal range with the same
+// mantissa). The bf16 subnormals take part in the bf16 multiply below without flushing.
+// (The NaN code 0x7F is not propagated; weights hold finite codes.)
+__device__ __forceinline__ void e4m3x4_to_bf16x4_lowexp(uint32_t x, uint32_t& p01, uint32_t& p23) {
+  const uint32_t a = __byte_perm(x, 0u, 0x1404u);  // [b1 0 b0 0]
+  const uint32_t b = __byte_perm(x, 0u, 0x3424u);  // [b3 0 b2 0]
+  p01 = (a & 0x80008000u) | ((a & 0x7F007F00u) >> 4);
+  p23 = (b & 0x80008000u) | ((b & 0x7F007F00u) >> 4);
+}
+__device__ __forceinline__ uint32_t bf16x2_mul(uint32_t a, uint32_t b) {
+  uint32_t d;
+  asm("mul.rn.bf16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+  return d;
+}
+// General scale: exact fp32 products, one rounding to bf16.
+__device__ __forceinline__ uint32_t bf16x2_lowexp_scale_f32(uint32_t p, float sc) {
+  const float lo = __uint_as_float(p << 16) * 0x1p120f;
+  const float hi = __uint_as_float(p & 0xFFFF0000u) * 0x1p120f;
+  return pack_bf16(lo * sc, hi * sc);
+}
+
+template <int MODE, bool FP8>
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Roles<FP8>::kThreads, 1)
     grouped_pair_kernel(const __grid_constant__ CUtensorMap tmA,
                         const __grid_constant__ CUtensorMap tmB0,
                         const __grid_constant__ CUtensorMap tmB1, const Params P) {
-  using R = Roles<MODE>;
+  using R = Roles<FP8>;
+  using L = Layout<FP8>;
+  constexpr int kStages = L::kStages;
   constexpr uint32_t IDESC = idesc_bf16(256, 256);
 
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = (uint8_t*)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
-  uint8_t* sA = smem + Layout::a;
-  uint8_t* sB = smem + Layout::b;
-  uint64_t* bars = (uint64_t*)(smem + Layout::bars);
+  uint8_t* sA = smem + L::a;
+  uint8_t* sB = smem + L::b;
+  uint8_t* sRaw = smem + L::raw;
+  uint64_t* bars = (uint64_t*)(smem + L::bars);
   uint64_t* full = bars;
   uint64_t* empty = bars + kStages;
-  uint64_t* tfull = bars + 2 * kStages;
+  uint64_t* rawfull = bars + 2 * kStages;
+  uint64_t* tfull = bars + 3 * kStages;
   uint64_t* tempty = tfull + 2;
   uint64_t* drain = tempty + 2;
-  uint32_t* tmem_slot = (uint32_t*)(smem + Layout::misc);
-  volatile int* abort_flag = (volatile int*)(smem + Layout::misc + 4);
-  int* nruns_sh = (int*)(smem + Layout::misc + 8);
-  int* bnd = (int*)(smem + Layout::bnd);
-  int* run_first = (int*)(smem + Layout::run_first);
-  int* run_len = (int*)(smem + Layout::run_len);
-  int* run_e = (int*)(smem + Layout::run_e);
-  int* run_pref = (int*)(smem + Layout::run_pref);
-  uint8_t* flags = smem + Layout::flags;
+  uint32_t* tmem_slot = (uint32_t*)(smem + L::misc);
+  volatile int* abort_flag = (volatile int*)(smem + L::misc + 4);
+  int* nruns_sh = (int*)(smem + L::misc + 8);
+  int* bnd = (int*)(smem + L::bnd);
+  int* run_first = (int*)(smem + L::run_first);
+  int* run_len = (int*)(smem + L::run_len);
+  int* run_e = (int*)(smem + L::run_e);
+  int* run_pref = (int*)(smem + L::run_pref);
+  uint8_t* flags = smem + L::flags;
   int* status = &g_grouped_status;
 
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
@@ -160,6 +210,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Roles<MODE>::kThread
     for (int s = 0; s < kStages; ++s) {
       mbar_init(&full[s], R::kFullArrivals);  // only the leader's are used
       mbar_init(&empty[s], 1);
+      mbar_init(&rawfull[s], 1);              // FP8: this CTA's raw weight tile landed
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(&tfull[b], 1);
@@ -270,10 +321,16 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Roles<MODE>::kThread
           const uint32_t fl = cluster_addr(&full[s], 0);
           if (leader) mbar_expect_tx(&full[s], R::kPairTmaBytes);
           tma_2d_pair(sA + s * A_BYTES, &tmA, fl, kb * BK, (m0 + (int)rank) * BM);
-          if (MODE == kGemm1)  // leader: gate rows of panel n, peer: up rows
-            tma_3d_pair(sB + s * B_BYTES, rank ? &tmB1 : &tmB0, fl, kb * BK, n * 128, e);
-          else                 // leader: rows n*256 .. +127 of W2[e], peer: the next 128
-            tma_3d_pair(sB + s * B_BYTES, &tmB0, fl, kb * BK, n * 256 + (int)rank * 128, e);
+          // leader: gate rows of panel n (GEMM1) / rows n*256 .. +127 of W2[e] (GEMM2);
+          // peer: the up rows / the next 128 rows
+          const CUtensorMap* tb_map = (MODE == kGemm1 && rank) ? &tmB1 : &tmB0;
+          const int brow = MODE == kGemm1 ? n * 128 : n * 256 + (int)rank * 128;
+          if (FP8) {  // raw codes to this CTA's ring; the converter warps write sB
+            mbar_expect_tx(&rawfull[s], RAW_BYTES);
+            tma_3d(sRaw + s * RAW_BYTES, tb_map, &rawfull[s], kb * BK, brow, e);
+          } else {
+            tma_3d_pair(sB + s * B_BYTES, tb_map, fl, kb * BK, brow, e);
+          }
         }
         if (!ok) break;
       }
@@ -316,7 +373,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Roles<MODE>::kThread
       }
     }
     __syncwarp();
-  } else if (warp >= R::kEpiWarp0) {
+  } else if (warp >= R::kEpiWarp0 && warp < R::kEpiWarp0 + 4) {
     // ------------------------------------------------------------ epilogue (4 warps)
     const int q = warp & 3;  // TMEM lane quarter this warp may access
     const int row = q * 32 + lane;
@@ -398,6 +455,74 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Roles<MODE>::kThread
       }
       if (++acc == kAccs) { acc = 0; acc_phase ^= 1u; }
     }
+  } else if (FP8 && warp >= R::kCvtWarp0) {
+    // ------------------------------------------------------------ FP8 converters (4 warps)
+    // Warp cw turns rows cw*32 .. cw*32+31 of this CTA's raw 128 x 64 code tile into the
+    // 128-byte-swizzled bf16 K-major layout the MMA descriptor expects (16-byte chunk c of
+    // row r at r*128 + ((c ^ (r & 7)) << 4)), scaled by the tile's block scale; then makes
+    // the writes visible to the tensor cores and arrives on the leader's stage barrier.
+    const int cw = (warp - R::kCvtWarp0) % R::kCvtWarps;
+    const int grp = (warp - R::kCvtWarp0) / R::kCvtWarps;
+    const int grid = MODE == kGemm1 ? (int)rank : 0;
+    int g = 0;
+    for (int w = pair; w < total; w += num_pairs) {
+      int m0, n, e;
+      bool live1;
+      item_of(w, P.n_tiles, tb, m0, n, e, live1);
+      const int rb = MODE == kGemm1 ? n : 2 * n + (int)rank;
+      const bool sc_ok = e >= 0 && e < P.n_slots && rb < P.sc_rb;
+      const float* srow =
+          P.scale + (((int64_t)e * (MODE == kGemm1 ? 2 : 1) + grid) * P.sc_rb + rb) * P.sc_kb;
+      bool ok = true;
+      for (int kb = 0; kb < num_kb; ++kb, ++g) {
+        if ((g % kStages) % R::kCvtGroups != grp) continue;  // the group's own slots
+        const int s = g % kStages;
+        const float sc = sc_ok ? __ldg(srow + (kb >> 1)) : 0.f;  // in flight during the wait
+        int okw = 1;
+        if (lane == 0) okw = wait_bounded(&rawfull[s], (uint32_t)(g / kStages) & 1u, abort_flag, status);
+        okw = __shfl_sync(0xffffffffu, okw, 0);
+        if (!okw) {
+          ok = false;
+          break;
+        }
+        // A power-of-two scale below 2^8 (or 0) times 2^120 is an exact bf16: one packed
+        // bf16 multiply per two weights, exact. Any other scale: fp32 products.
+        const float scb = sc * 0x1p120f;
+        const bool fast = (__float_as_uint(sc) & 0x807FFFFFu) == 0 && sc < 0x1p8f;
+        const uint32_t sc2 = (__float_as_uint(scb) >> 16) * 0x10001u;
+        const uint8_t* src = sRaw + s * RAW_BYTES;
+        uint8_t* dst = sB + s * B_BYTES;
+#pragma unroll
+        for (int j = 0; j < 16 / R::kCvtWarps; ++j) {
+          // 16-code unit u: row u/4, codes (u%4)*16 .. +15; 512 units per stage
+          const int u = cw * (512 / R::kCvtWarps) + j * 32 + lane;
+          const int r = u >> 2, h = u & 3;
+          const uint4 q = *reinterpret_cast<const uint4*>(src + u * 16);
+          uint32_t v[8];
+          e4m3x4_to_bf16x4_lowexp(q.x, v[0], v[1]);
+          e4m3x4_to_bf16x4_lowexp(q.y, v[2], v[3]);
+          e4m3x4_to_bf16x4_lowexp(q.z, v[4], v[5]);
+          e4m3x4_to_bf16x4_lowexp(q.w, v[6], v[7]);
+          if (fast) {
+#pragma unroll
+            for (int i = 0; i < 8; ++i) v[i] = bf16x2_mul(v[i], sc2);
+          } else {
+#pragma unroll
+            for (int i = 0; i < 8; ++i) v[i] = bf16x2_lowexp_scale_f32(v[i], sc);
+          }
+          uint8_t* drow = dst + r * 128;
+          *reinterpret_cast<uint4*>(drow + (((2 * h) ^ (r & 7)) << 4)) = make_uint4(v[0], v[1], v[2], v[3]);
+          *reinterpret_cast<uint4*>(drow + (((2 * h + 1) ^ (r & 7)) << 4)) = make_uint4(v[4], v[5], v[6], v[7]);
+        }
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) {
+          if (leader) mbar_arrive(&full[s]);
+          else mbar_arrive_cta(&full[s], 0);
+        }
+      }
+      if (!ok) break;
+    }
   }
 
   __syncthreads();
@@ -413,11 +538,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Roles<MODE>::kThread
   }
 }
 
-template <int MODE>
+template <int MODE, bool FP8>
 static moe_status_t launch(const CUtensorMap& a, const CUtensorMap& b0, const CUtensorMap& b1,
                            const Params& P, int max_items, cudaStream_t s) {
-  auto kern = grouped_pair_kernel<MODE>;
-  constexpr size_t smem = Layout::bytes;
+  auto kern = grouped_pair_kernel<MODE, FP8>;
+  constexpr size_t smem = Layout<FP8>::bytes;
   // Persistent grid: as many CTA pairs as can be resident at once (SMs that cannot be
   // paired inside a GPC stay idle rather than forming a second wave).
   static thread_local int configured_dev = -1, resident_pairs = 0;
@@ -429,7 +554,7 @@ static moe_status_t launch(const CUtensorMap& a, const CUtensorMap& b0, const CU
       return MOE_ERR_CUDA;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(2 * (num_sms() / 2));
-    cfg.blockDim = dim3(Roles<MODE>::kThreads);
+    cfg.blockDim = dim3(Roles<FP8>::kThreads);
     cfg.dynamicSmemBytes = smem;
     int clusters = 0;
     if (cudaOccupancyMaxActiveClusters(&clusters, (void*)kern, &cfg) != cudaSuccess ||
@@ -442,7 +567,7 @@ static moe_status_t launch(const CUtensorMap& a, const CUtensorMap& b0, const CU
   }
   const int pairs = std::min(resident_pairs, max_items);
   if (pairs < 1) return MOE_OK;
-  kern<<<2 * pairs, Roles<MODE>::kThreads, smem, s>>>(a, b0, b1, P);
+  kern<<<2 * pairs, Roles<FP8>::kThreads, smem, s>>>(a, b0, b1, P);
   return last_launch_status();
 }
 
@@ -469,6 +594,7 @@ moe_status_t launch_gemm1_tc(const moe_config_t& c, const void* xs, const void* 
                              int block_m, int max_padded, void* act, cudaStream_t s) {
   using namespace tc2;
   if (max_padded / BM > kMaxTiles) return MOE_ERR_UNSUPPORTED;
+  const bool fp8 = c.weight_format == MOE_WEIGHTS_FP8_E4M3_B128;
   CUtensorMap mA, mG, mU;
   const uint64_t H = c.H, I = c.I, E = c.E;
   {
@@ -479,9 +605,9 @@ moe_status_t launch_gemm1_tc(const moe_config_t& c, const void* xs, const void* 
   {
     uint64_t d[3] = {H, I, E}, st[2] = {H, 2 * I * H};
     uint32_t box[3] = {BK, 128, 1};
-    if (!make_map(&mG, W13, 3, d, st, box, true)) return MOE_ERR_CUDA;
-    const __nv_bfloat16* up = (const __nv_bfloat16*)W13 + I * H;
-    if (!make_map(&mU, up, 3, d, st, box, true)) return MOE_ERR_CUDA;
+    const uint8_t* up = (const uint8_t*)W13 + I * H * (fp8 ? 1 : 2);
+    if (!make_map(&mG, W13, 3, d, st, box, true, fp8)) return MOE_ERR_CUDA;
+    if (!make_map(&mU, up, 3, d, st, box, true, fp8)) return MOE_ERR_CUDA;
   }
   Params P{};
   P.n_rows = c.T * c.k;
@@ -495,7 +621,13 @@ moe_status_t launch_gemm1_tc(const moe_config_t& c, const void* xs, const void* 
   P.npp = npp;
   P.out = act;
   P.ld_out = c.I;
-  return launch<kGemm1>(mA, mG, mU, P, max_items_for(max_padded, P.n_rows, c.E, P.n_tiles), s);
+  P.scale = c.w13_scale;
+  P.sc_rb = ceil_div(c.I, 128);
+  P.sc_kb = ceil_div(c.H, 128);
+  P.n_slots = c.E;
+  const int items = max_items_for(max_padded, P.n_rows, c.E, P.n_tiles);
+  return fp8 ? launch<kGemm1, true>(mA, mG, mU, P, items, s)
+             : launch<kGemm1, false>(mA, mG, mU, P, items, s);
 }
 
 moe_status_t launch_gemm2_tc(const moe_config_t& c, const void* act, const void* W2,
@@ -504,6 +636,7 @@ moe_status_t launch_gemm2_tc(const moe_config_t& c, const void* act, const void*
                              cudaStream_t s) {
   using namespace tc2;
   if (max_padded / BM > kMaxTiles) return MOE_ERR_UNSUPPORTED;
+  const bool fp8 = c.weight_format == MOE_WEIGHTS_FP8_E4M3_B128;
   CUtensorMap mA, mB;
   const uint64_t H = c.H, I = c.I, E = c.E;
   {
@@ -514,7 +647,7 @@ moe_status_t launch_gemm2_tc(const moe_config_t& c, const void* act, const void*
   {
     uint64_t d[3] = {I, H, E}, st[2] = {I, H * I};
     uint32_t box[3] = {BK, 128, 1};
-    if (!make_map(&mB, W2, 3, d, st, box, true)) return MOE_ERR_CUDA;
+    if (!make_map(&mB, W2, 3, d, st, box, true, fp8)) return MOE_ERR_CUDA;
   }
   Params P{};
   P.n_rows = c.T * c.k;
@@ -529,7 +662,13 @@ moe_status_t launch_gemm2_tc(const moe_config_t& c, const void* act, const void*
   P.topk_w = topk_w;
   P.out = y;
   P.ld_out = c.H;
-  return launch<kGemm2>(mA, mB, mB, P, max_items_for(max_padded, P.n_rows, c.E, P.n_tiles), s);
+  P.scale = c.w2_scale;
+  P.sc_rb = ceil_div(c.H, 128);
+  P.sc_kb = ceil_div(c.I, 128);
+  P.n_slots = c.E;
+  const int items = max_items_for(max_padded, P.n_rows, c.E, P.n_tiles);
+  return fp8 ? launch<kGemm2, true>(mA, mB, mB, P, items, s)
+             : launch<kGemm2, false>(mA, mB, mB, P, items, s);
 }
 
 }  // namespace moe

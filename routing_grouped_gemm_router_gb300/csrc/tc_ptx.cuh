@@ -291,9 +291,11 @@ inline PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
   return fn;
 }
 
-// bf16 tensor map with 128-byte swizzle; dims/strides in elements (dim 0 innermost).
+// bf16 tensor map with 128-byte swizzle, or (fp8) a byte map without swizzle whose rows of
+// BK codes land densely; dims/strides in elements (dim 0 innermost).
 inline bool make_map(CUtensorMap* m, const void* base, int rank, const uint64_t* dims,
-                     const uint64_t* strides_elems, const uint32_t* box, bool weights) {
+                     const uint64_t* strides_elems, const uint32_t* box, bool weights,
+                     bool fp8 = false) {
   auto fn = encode_fn();
   if (!fn) return false;
   cuuint64_t gdim[3], gstr[2];
@@ -302,9 +304,10 @@ inline bool make_map(CUtensorMap* m, const void* base, int rank, const uint64_t*
     gdim[i] = dims[i];
     bdim[i] = box[i];
   }
-  for (int i = 0; i + 1 < rank; ++i) gstr[i] = strides_elems[i] * 2;
-  CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, rank, const_cast<void*>(base), gdim, gstr,
-                  bdim, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+  for (int i = 0; i + 1 < rank; ++i) gstr[i] = strides_elems[i] * (fp8 ? 1 : 2);
+  CUresult r = fn(m, fp8 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, rank,
+                  const_cast<void*>(base), gdim, gstr, bdim, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                  fp8 ? CU_TENSOR_MAP_SWIZZLE_NONE : CU_TENSOR_MAP_SWIZZLE_128B,
                   weights ? CU_TENSOR_MAP_L2_PROMOTION_L2_256B : CU_TENSOR_MAP_L2_PROMOTION_L2_128B,
                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS;

@@ -18,13 +18,23 @@ class MoELayer:
     x[T,H], Wg[E,H], W13[E,2I,H] (gate rows 0..I-1, up rows I..2I-1), W2[E,H,I] in one
     dtype (bf16 or fp32), all on one CUDA device. ``forward`` enqueues the whole layer on
     the current stream without a host round-trip.
+
+    FP8 expert weights: W13/W2 hold E4M3 codes (torch.float8_e4m3fn or uint8) and
+    w13_scale[E', 2, ceil(I/128), ceil(H/128)], w2_scale[E', ceil(H/128), ceil(I/128)] the
+    fp32 scale of each 128 x 128 block (E' = E + n_shared); x and Wg stay bf16.
     """
 
     def __init__(self, Wg, W13, W2, k, mode=L.MOE_ROUTE_SOFTMAX, renormalize=True, scale=1.0,
                  n_group=1, topk_group=1, logit_bias: Optional[torch.Tensor] = None,
                  select_bias: Optional[torch.Tensor] = None,
-                 expert_map: Optional[torch.Tensor] = None, n_shared: int = 0):
+                 expert_map: Optional[torch.Tensor] = None, n_shared: int = 0,
+                 w13_scale: Optional[torch.Tensor] = None,
+                 w2_scale: Optional[torch.Tensor] = None):
         """W13/W2 hold E routed experts followed by n_shared shared experts."""
+        if (w13_scale is None) != (w2_scale is None):
+            raise ValueError("FP8 weights need both w13_scale and w2_scale")
+        self.w13_scale = w13_scale.float().contiguous() if w13_scale is not None else None
+        self.w2_scale = w2_scale.float().contiguous() if w2_scale is not None else None
         self.Wg, self.W13, self.W2 = Wg, W13, W2
         self.E, self.H = Wg.shape
         self.n_shared = n_shared
@@ -44,7 +54,7 @@ class MoELayer:
         return L.make_config(T, self.H, self.I, self.E, self.k, self.dtype, self.mode,
                              self.renormalize, self.scale, self.n_group, self.topk_group,
                              self.logit_bias, self.select_bias, self.expert_map,
-                             self.n_shared)
+                             self.n_shared, self.w13_scale, self.w2_scale)
 
     def workspace(self, T):
         if self._ws_T != T:

@@ -90,6 +90,20 @@ class LazyExperts:
         return weights_for_oracle(self.W[int(e)])
 
 
+class LazyFp8Experts:
+    """FP8 expert weights (codes + block scales) left on the device; ``[e]`` dequantises one
+    expert on the host with the oracle (code * scale of its 128 x 128 block)."""
+
+    def __init__(self, codes: torch.Tensor, scales: torch.Tensor, w13: bool):
+        self.codes, self.scales, self.w13 = codes, scales, w13
+        self.shape = tuple(codes.shape)
+
+    def __getitem__(self, e):
+        c = self.codes[int(e)].cpu().numpy()[None]
+        s = self.scales[int(e)].double().cpu().numpy()[None]
+        return (O.dequant_w13(c, s) if self.w13 else O.dequant_blockwise(c, s))[0]
+
+
 def sample_tokens(ids: np.ndarray, n: int, seed: int = 0) -> np.ndarray:
     """n token indices: tokens routed to the hottest expert and to the least-loaded
     non-empty expert, then uniform picks."""

@@ -36,7 +36,7 @@ def test_library_exports_every_declared_symbol(L):
     missing = [n for n in decl if not hasattr(cdll, n)]
     assert not missing, f"declared but not exported: {missing}"
     assert set(decl) <= set(L.EXPORTED) | set(decl)
-    assert L.moe_abi_version() == 2
+    assert L.moe_abi_version() == 3
 
 
 def test_status_strings(L):
@@ -108,3 +108,23 @@ def test_align_workspace_sizes(L):
     with pytest.raises(L.MoeError) as ei:
         L.moe_align(16, 8192, 8, 128, 128, 16, 16, 16, ws=None, ws_bytes=0, stream=0)
     assert ei.value.status == L.MOE_ERR_WORKSPACE
+
+
+def test_fp8_weight_config_checks(L):
+    ok = L.make_config(4, 64, 96, 8, 2, L.MOE_BF16, w13_scale=256, w2_scale=512)
+    assert ok.weight_format == L.MOE_WEIGHTS_FP8_E4M3_B128
+    assert L.moe_workspace_size(ok) > 0
+    cases = [(L.make_config(4, 64, 96, 8, 2, L.MOE_F32, w13_scale=256, w2_scale=512),
+              L.MOE_ERR_UNSUPPORTED),                                   # fp32 activations
+             (L.make_config(4, 72, 96, 8, 2, L.MOE_BF16, w13_scale=256, w2_scale=512),
+              L.MOE_ERR_INVALID_ARG),                                   # H % 16
+             (L.make_config(4, 64, 104, 8, 2, L.MOE_BF16, w13_scale=256, w2_scale=512),
+              L.MOE_ERR_INVALID_ARG),                                   # I % 16
+             (L.make_config(4, 64, 96, 8, 2, L.MOE_BF16, w13_scale=256),
+              L.MOE_ERR_INVALID_ARG),                                   # a scale missing
+             (L.make_config(4, 64, 96, 8, 2, L.MOE_BF16, w13_scale=258, w2_scale=512),
+              L.MOE_ERR_INVALID_ARG)]                                   # misaligned scale
+    for cfg, want in cases:
+        with pytest.raises(L.MoeError) as ei:
+            L.moe_workspace_size(cfg)
+        assert ei.value.status == want

@@ -11,7 +11,7 @@ import torch
 
 import moe_inputs as mi
 import oracle as O
-from _helpers import (LazyExperts, assert_close, enforce_margins, oracle_logits,
+from _helpers import (LazyExperts, LazyFp8Experts, assert_close, enforce_margins, oracle_logits,
                       oracle_route_from_logits, sample_tokens, to_np)
 
 pytestmark = [pytest.mark.gpu, pytest.mark.slow]
@@ -72,6 +72,37 @@ def test_full_size_parity(L, wl, n_sample):
     toks = sample_tokens(ids_o, n_sample, seed=wl.seed)
     ref = O.moe_loop(to_np(inp.x[torch.as_tensor(toks, device=DEV)]),
                      ids_o[toks], w_o[toks], LazyExperts(inp.W13), LazyExperts(inp.W2))
+    got = to_np(out[torch.as_tensor(toks, device=DEV)])
+    assert_close(got, ref, wl.dtype)
+    assert torch.isfinite(out.float()).all()
+
+
+FP8_CASES = [(mi.DSV3, 16), (mi.GPTOSS.with_T(1), 1), (mi.GPTOSS.with_T(128), 32)]
+
+
+@pytest.mark.parametrize("wl,n_sample", FP8_CASES, ids=[c[0].name + "-fp8" for c in FP8_CASES])
+def test_full_size_fp8_parity(L, wl, n_sample):
+    """Full-size layers with FP8 E4M3 expert weights (128 x 128 block scales, drawn by
+    quantising the seeded bf16 weights): routing bit-exact, sampled tokens against the
+    oracle on the dequantised weights."""
+    from routing_grouped_gemm_router_gb300.layer import MoELayer
+    inp = mi.make_layer(wl, DEV)
+    enforce_margins(inp)
+    c13, s13 = mi.quantize_fp8_w13(inp.W13)
+    c2, s2 = mi.quantize_fp8_blocks(inp.W2)
+    inp.W13 = inp.W2 = None
+    torch.cuda.empty_cache()
+    layer = MoELayer(inp.Wg, c13, c2, wl.k, wl.mode, wl.renormalize, wl.scale, wl.n_group,
+                     wl.topk_group, inp.logit_bias, inp.select_bias, w13_scale=s13, w2_scale=s2)
+    out = layer(inp.x)
+    torch.cuda.synchronize()
+    mids = layer.intermediates(wl.T)
+    sb = to_np(inp.select_bias) if inp.select_bias is not None else None
+    ids_o, w_o = oracle_route_from_logits(oracle_logits(inp), wl, sb)
+    assert np.array_equal(to_np(mids["topk_ids"]), ids_o)
+    toks = sample_tokens(ids_o, n_sample, seed=wl.seed)
+    ref = O.moe_loop(to_np(inp.x[torch.as_tensor(toks, device=DEV)]), ids_o[toks], w_o[toks],
+                     LazyFp8Experts(c13, s13, True), LazyFp8Experts(c2, s2, False))
     got = to_np(out[torch.as_tensor(toks, device=DEV)])
     assert_close(got, ref, wl.dtype)
     assert torch.isfinite(out.float()).all()

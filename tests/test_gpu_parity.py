@@ -345,10 +345,13 @@ def test_separate_entry_points_match_forward(L):
     assert torch.equal(y2, y)
 
 
-@pytest.mark.parametrize("dtype", ["bf16", "f32"])
+@pytest.mark.parametrize("dtype", ["bf16", "f32", "fp8"])
 def test_tile_boundaries_and_sentinels(L, dtype):
     """Experts with 0, 1, B-1, B, B+1, 2B-1, 2B, 2B+1 rows; padding rows of act are never
-    written (canary survives); every row of y is written (canary gone)."""
+    written (canary survives); every row of y is written (canary gone). "fp8": bf16
+    activations with FP8 E4M3 expert weights."""
+    fp8 = dtype == "fp8"
+    dtype = "bf16" if fp8 else dtype
     tdt = torch.bfloat16 if dtype == "bf16" else torch.float32
     B = 128 if dtype == "bf16" else 16
     loads = [0, 1, B - 1, B, B + 1, 2 * B - 1, 2 * B, 2 * B + 1]
@@ -362,8 +365,12 @@ def test_tile_boundaries_and_sentinels(L, dtype):
     x = torch.randn(T, H, generator=g).to(tdt)
     W13 = (torch.randn(E, 2 * I, H, generator=g) / H ** 0.5).to(tdt)
     W2 = (torch.randn(E, H, I, generator=g) / I ** 0.5).to(tdt)
+    sc = {}
+    if fp8:
+        (W13, s13), (W2, s2) = mi.quantize_fp8_w13(W13), mi.quantize_fp8_blocks(W2)
+        sc = dict(w13_scale=s13.to(DEV), w2_scale=s2.to(DEV))
     xd, W13d, W2d, idsd, wd = (t.to(DEV) for t in (x, W13, W2, ids, w))
-    cfg = L.make_config(T, H, I, E, k, L.MOE_BF16 if dtype == "bf16" else L.MOE_F32)
+    cfg = L.make_config(T, H, I, E, k, L.MOE_BF16 if dtype == "bf16" else L.MOE_F32, **sc)
     mp = L.moe_max_padded_rows(T, k, E, B)
     sid = torch.empty(mp, dtype=torch.int32, device=DEV)
     eid = torch.empty(mp // B, dtype=torch.int32, device=DEV)
@@ -386,7 +393,12 @@ def test_tile_boundaries_and_sentinels(L, dtype):
     assert np.all(np.isnan(a[~valid])), "a padding row of act was written"
     assert np.all(np.isfinite(y.float().cpu().numpy())), "a row of y was not written"
     assert total == sum((c + B - 1) // B * B for c in loads)
-    ref = O.moe_loop(to_np(x), ids.numpy(), to_np(w), weights_for_oracle(W13), weights_for_oracle(W2))
+    if fp8:
+        w13o = O.dequant_w13(W13.numpy(), s13.double().numpy())
+        w2o = O.dequant_blockwise(W2.numpy(), s2.double().numpy())
+    else:
+        w13o, w2o = weights_for_oracle(W13), weights_for_oracle(W2)
+    ref = O.moe_loop(to_np(x), ids.numpy(), to_np(w), w13o, w2o)
     assert_close(to_np(out), ref, dtype)
 
 
@@ -556,3 +568,97 @@ def test_masked_layout(L, dtype, with_w):
     exp_eid = np.where(((t * B) % cap) < counts[(t * B) // cap], (t * B) // cap, -1)
     assert np.array_equal(sid.cpu().numpy(), exp_sid) and int(npp.item()) == n
     assert np.array_equal(eid.cpu().numpy(), exp_eid)
+
+
+# --------------------------------------------------------------------- FP8 expert weights
+
+FP8_CASES = [
+    # ragged: H = 2.5 scale blocks, I = 2 panels + 16 rows, GEMM2 K = 4.25 k-blocks
+    (mi.Workload("fp8-ragged", T=300, H=320, I=272, E=8, k=2, dtype="bf16", seed=61), 0, False),
+    # grouped sigmoid router, scale 2.5, one shared expert
+    (mi.Workload("fp8-grouped-shared", T=256, H=512, I=384, E=32, k=8, dtype="bf16",
+                 mode=mi.ROUTE_SIGMOID_GROUPED, scale=2.5, n_group=8, topk_group=4,
+                 select_bias_std=0.05, seed=62), 1, False),
+    # scales that are not powers of two: the kernel rounds code * scale to bf16 once
+    (mi.Workload("fp8-any-scale", T=200, H=256, I=256, E=16, k=4, dtype="bf16", seed=63), 0, True),
+    # decode: one token
+    (mi.Workload("fp8-decode", T=1, H=512, I=512, E=64, k=4, dtype="bf16", seed=64), 0, False),
+]
+
+
+def _fp8_weights(inp, n_shared, any_scale, seed):
+    g = torch.Generator().manual_seed(seed)
+    H, I = inp.wl.H, inp.wl.I
+    W13, W2 = inp.W13, inp.W2
+    if n_shared:
+        W13 = torch.cat([W13, (torch.randn(n_shared, 2 * I, H, generator=g) / H ** 0.5).bfloat16()])
+        W2 = torch.cat([W2, (torch.randn(n_shared, H, I, generator=g) / I ** 0.5).bfloat16()])
+    (c13, s13), (c2, s2) = mi.quantize_fp8_w13(W13), mi.quantize_fp8_blocks(W2)
+    if any_scale:
+        s13 = s13 * (1.0 + torch.rand(s13.shape, generator=g))
+        s2 = s2 * (1.0 + torch.rand(s2.shape, generator=g))
+    return c13, s13, c2, s2
+
+
+@pytest.mark.parametrize("wl,n_shared,any_scale", FP8_CASES, ids=[c[0].name for c in FP8_CASES])
+def test_fp8_layer_parity(L, wl, n_shared, any_scale):
+    """moe_forward with FP8 E4M3 expert weights and 128 x 128 block scales equals the
+    float64 oracle run on the dequantised weights (code * scale)."""
+    from routing_grouped_gemm_router_gb300.layer import MoELayer
+    inp = mi.make_layer(wl, "cpu")
+    enforce_margins(inp)
+    c13, s13, c2, s2 = _fp8_weights(inp, n_shared, any_scale, wl.seed)
+    d = lambda t: None if t is None else t.to(DEV).contiguous()  # noqa: E731
+    layer = MoELayer(d(inp.Wg), d(c13), d(c2), wl.k, wl.mode, wl.renormalize, wl.scale,
+                     wl.n_group, wl.topk_group, d(inp.logit_bias), d(inp.select_bias),
+                     n_shared=n_shared, w13_scale=d(s13), w2_scale=d(s2))
+    out = layer(d(inp.x))
+    torch.cuda.synchronize()
+    mids = layer.intermediates(wl.T)
+    sb = to_np(inp.select_bias) if inp.select_bias is not None else None
+    ids, w = oracle_route_from_logits(oracle_logits(inp), wl, sb)
+    if n_shared:
+        ids, w = O.add_shared_experts(ids, w, wl.E, n_shared)
+    assert np.array_equal(to_np(mids["topk_ids"]), ids)
+    w13o = O.dequant_w13(c13.numpy(), s13.double().numpy())
+    w2o = O.dequant_blockwise(c2.numpy(), s2.double().numpy())
+    ref = O.moe_loop(to_np(inp.x), ids, w, w13o, w2o)
+    assert_close(to_np(out), ref, "bf16")
+    if not any_scale:
+        # power-of-two scales: the dequantised weights are exact in bf16, so the result is
+        # the bf16 layer's on those weights, bit for bit
+        layer_bf = MoELayer(d(inp.Wg), d(torch.tensor(w13o).bfloat16()),
+                            d(torch.tensor(w2o).bfloat16()), wl.k, wl.mode, wl.renormalize,
+                            wl.scale, wl.n_group, wl.topk_group, d(inp.logit_bias),
+                            d(inp.select_bias), n_shared=n_shared)
+        out_bf = layer_bf(d(inp.x))
+        torch.cuda.synchronize()
+        assert torch.equal(out_bf, out)
+
+
+def test_fp8_masked_layout(L):
+    """The fixed-capacity layout with FP8 weights: valid rows equal the oracle's masked
+    forward on the dequantised weights; rows past each count are never written."""
+    H, I, E, B = 256, 384, 8, 128
+    wl = mi.Workload("fp8-masked", T=150, H=H, I=I, E=E, k=2, dtype="bf16", seed=65)
+    inp = mi.make_layer(wl, "cpu")
+    ids, w = O.route_softmax(oracle_logits(inp), wl.k)
+    cap = -(-int(np.bincount(ids.ravel(), minlength=E).max()) // B) * B + B
+    xm, wm, counts, _ = O.dispatch_masked(to_np(inp.x), ids, w, E, cap)
+    c13, s13, c2, s2 = _fp8_weights(inp, 0, False, 65)
+    s13d, s2d = s13.to(DEV), s2.to(DEV)   # the config points at these: keep them alive
+    cfg = L.make_config(1, H, I, E, 1, L.MOE_BF16, w13_scale=s13d, w2_scale=s2d)
+    xm_d = torch.tensor(xm, dtype=torch.bfloat16, device=DEV)
+    y = torch.full((E, cap, H), float("nan"), dtype=torch.bfloat16, device=DEV)
+    wsb = L.moe_masked_workspace_size(cfg, cap)
+    ws = torch.empty(wsb, dtype=torch.uint8, device=DEV)
+    L.moe_masked_forward(cfg, xm_d, torch.tensor(counts, dtype=torch.int32, device=DEV), cap,
+                         torch.tensor(wm, dtype=torch.float32, device=DEV), c13.to(DEV),
+                         c2.to(DEV), y, ws, wsb)
+    torch.cuda.synchronize()
+    ref = O.masked_forward(to_np(xm_d), counts, O.dequant_w13(c13.numpy(), s13.double().numpy()),
+                           O.dequant_blockwise(c2.numpy(), s2.double().numpy()), wm)
+    got = to_np(y)
+    valid = ~np.isnan(ref[:, :, 0])
+    assert np.all(np.isnan(got[~valid])), "a row past an expert's count was written"
+    assert_close(got[valid], ref[valid], "bf16")
