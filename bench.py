@@ -193,6 +193,13 @@ def host_copies(inp):
     return f64(inp.x), f64(inp.Wg), bits(inp.W13), bits(inp.W2), lb, sb
 
 
+def split_ws_bytes(L, cfg, B, gemm):
+    """Split-K scratch a grouped GEMM of this configuration uses (0: no split)."""
+    if gemm == 1:
+        return L.moe_expert_gemm1_gathered_workspace_size(cfg, B) if cfg.dtype == L.MOE_BF16 else 0
+    return L.moe_expert_gemm2_workspace_size(cfg, B)
+
+
 def default_sample(wl):
     """Tokens per oracle pass: about 10-20 s of float64 work on a 16-core host."""
     return {"mixtral-prefill": 1536, "qwen3-skewed": 768,
@@ -274,7 +281,8 @@ def run_ours(args, wl):
     base = ws.data_ptr()
     p = {n: base + getattr(lay, n) for n in ("logits", "topk_ids", "topk_w", "sorted_ids",
                                                "expert_ids", "num_post_padded", "counts",
-                                               "align_scratch", "act", "xs", "y")}
+                                               "align_scratch", "act", "xs", "y", "splitk")}
+    ws_split = lay.total - lay.splitk
     ws_align = lay.act - lay.align_scratch
     ws_xs = lay.y - lay.xs
     out = torch.empty(T, H, dtype=inp.x.dtype, device=dev)
@@ -302,7 +310,8 @@ def run_ours(args, wl):
             if ev is not None:
                 ev[3].record(stream)
             L.moe_expert_gemm1_gathered(cfg, p["xs"], inp.W13, p["sorted_ids"], p["expert_ids"],
-                                        p["num_post_padded"], B, p["act"], sh)
+                                        p["num_post_padded"], B, p["act"], p["splitk"],
+                                        ws_split, sh)
         else:
             if ev is not None:
                 ev[3].record(stream)
@@ -311,7 +320,8 @@ def run_ours(args, wl):
         if ev is not None:
             ev[4].record(stream)
         L.moe_expert_gemm2(cfg, p["act"], inp.W2, p["sorted_ids"], p["expert_ids"],
-                           p["num_post_padded"], B, p["topk_w"], p["y"], sh)
+                           p["num_post_padded"], B, p["topk_w"], p["y"], p["splitk"], ws_split,
+                           sh)
         if ev is not None:
             ev[5].record(stream)
         if emap is not None:
@@ -324,6 +334,8 @@ def run_ours(args, wl):
     # router GEMM + top-k, align (one kernel up to 4096 rows, else three), row gather + GEMM1
     # (bf16), GEMM2, combine
     launches_per_step = 2 + (1 if T * k <= 4096 else 3) + (2 if wl.dtype == "bf16" else 1) + 1 + 1 + (1 if emap is not None else 0)
+    # split-K GEMMs (few work items) each add one counter-zeroing kernel
+    launches_per_step += sum(1 for g in (1, 2) if split_ws_bytes(L, cfg, B, g) > 0)
 
     for _ in range(max(3, args.warmup)):
         step()

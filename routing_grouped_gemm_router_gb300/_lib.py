@@ -40,7 +40,8 @@ class moe_config_t(ctypes.Structure):
 class moe_ws_layout_t(ctypes.Structure):
     _fields_ = [(n, ctypes.c_size_t) for n in ("logits", "topk_ids", "topk_w", "sorted_ids",
                                               "expert_ids", "num_post_padded", "counts",
-                                              "align_scratch", "act", "xs", "y", "total")] + \
+                                              "align_scratch", "act", "xs", "y", "splitk",
+                                              "total")] + \
                [("block_m", ctypes.c_int), ("max_padded", ctypes.c_int)]
 
 
@@ -65,9 +66,11 @@ def _load():
         "moe_expert_gemm1_workspace_size": (ST, [CFG, I32, ctypes.POINTER(SZ)]),
         "moe_expert_gemm1": (ST, [CFG, P, P, P, P, P, I32, P, P, SZ, P]),
         "moe_gather_rows": (ST, [P, P, P, I32, I32, I32, I32, P, P]),
-        "moe_expert_gemm1_gathered": (ST, [CFG, P, P, P, P, P, I32, P, P]),
+        "moe_expert_gemm1_gathered_workspace_size": (ST, [CFG, I32, ctypes.POINTER(SZ)]),
+        "moe_expert_gemm1_gathered": (ST, [CFG, P, P, P, P, P, I32, P, P, SZ, P]),
+        "moe_expert_gemm2_workspace_size": (ST, [CFG, I32, ctypes.POINTER(SZ)]),
         "moe_grouped_swiglu_workspace_size": (ST, [CFG, I32, ctypes.POINTER(SZ)]),
-        "moe_expert_gemm2": (ST, [CFG, P, P, P, P, P, I32, P, P, P]),
+        "moe_expert_gemm2": (ST, [CFG, P, P, P, P, P, I32, P, P, P, SZ, P]),
         "moe_grouped_swiglu": (ST, [CFG, P, P, P, P, P, P, I32, P, P, P, SZ, P]),
         "moe_combine": (ST, [P, I32, I32, I32, I32, P, P]),
         "moe_apply_expert_map": (ST, [P, I32, P, I32, P]),
@@ -88,8 +91,9 @@ _lib = _load()
 EXPORTED = ("moe_abi_version", "moe_status_string", "moe_block_m", "moe_max_padded_rows",
             "moe_align_workspace_size", "moe_workspace_layout", "moe_workspace_size",
             "moe_route", "moe_align", "moe_align_noalloc", "moe_expert_gemm1_workspace_size",
-            "moe_expert_gemm1", "moe_gather_rows", "moe_expert_gemm1_gathered",
-            "moe_grouped_swiglu_workspace_size", "moe_expert_gemm2",
+            "moe_expert_gemm1", "moe_gather_rows", "moe_expert_gemm1_gathered_workspace_size",
+            "moe_expert_gemm1_gathered", "moe_grouped_swiglu_workspace_size",
+            "moe_expert_gemm2_workspace_size", "moe_expert_gemm2",
             "moe_grouped_swiglu", "moe_combine", "moe_apply_expert_map", "moe_combine_local",
             "moe_masked_table", "moe_masked_workspace_size", "moe_masked_forward",
             "moe_forward", "moe_device_status")
@@ -198,6 +202,21 @@ def moe_expert_gemm1_workspace_size(cfg, block_m) -> int:
     return out.value
 
 
+def moe_expert_gemm1_gathered_workspace_size(cfg, block_m) -> int:
+    out = ctypes.c_size_t(0)
+    _check("moe_expert_gemm1_gathered_workspace_size",
+           _lib.moe_expert_gemm1_gathered_workspace_size(ctypes.byref(cfg), block_m,
+                                                         ctypes.byref(out)))
+    return out.value
+
+
+def moe_expert_gemm2_workspace_size(cfg, block_m) -> int:
+    out = ctypes.c_size_t(0)
+    _check("moe_expert_gemm2_workspace_size",
+           _lib.moe_expert_gemm2_workspace_size(ctypes.byref(cfg), block_m, ctypes.byref(out)))
+    return out.value
+
+
 def moe_grouped_swiglu_workspace_size(cfg, block_m) -> int:
     out = ctypes.c_size_t(0)
     _check("moe_grouped_swiglu_workspace_size",
@@ -219,17 +238,18 @@ def moe_gather_rows(x, sorted_ids, num_post_padded, T, k, H, dtype, xs, stream=N
 
 
 def moe_expert_gemm1_gathered(cfg, xs, W13, sorted_ids, expert_ids, num_post_padded, block_m,
-                              act, stream=None):
+                              act, ws=None, ws_bytes=0, stream=None):
     _check("moe_expert_gemm1_gathered", _lib.moe_expert_gemm1_gathered(
         ctypes.byref(cfg), _ptr(xs), _ptr(W13), _ptr(sorted_ids), _ptr(expert_ids),
-        _ptr(num_post_padded), block_m, _ptr(act), _stream(stream)))
+        _ptr(num_post_padded), block_m, _ptr(act), _ptr(ws), ws_bytes, _stream(stream)))
 
 
 def moe_expert_gemm2(cfg, act, W2, sorted_ids, expert_ids, num_post_padded, block_m, topk_w, y,
-                     stream=None):
+                     ws=None, ws_bytes=0, stream=None):
     _check("moe_expert_gemm2", _lib.moe_expert_gemm2(
         ctypes.byref(cfg), _ptr(act), _ptr(W2), _ptr(sorted_ids), _ptr(expert_ids),
-        _ptr(num_post_padded), block_m, _ptr(topk_w), _ptr(y), _stream(stream)))
+        _ptr(num_post_padded), block_m, _ptr(topk_w), _ptr(y), _ptr(ws), ws_bytes,
+        _stream(stream)))
 
 
 def moe_grouped_swiglu(cfg, x, W13, W2, sorted_ids, expert_ids, num_post_padded, block_m,

@@ -146,6 +146,8 @@ __global__ void __launch_bounds__(kAlignThreads) align_small_kernel(
     const int32_t* __restrict__ ids, int n, int E, int B, int max_padded,
     int32_t* __restrict__ sorted_ids, int32_t* __restrict__ expert_ids, int32_t* npp,
     int32_t* counts) {
+  pdl_wait();
+  pdl_trigger();
   extern __shared__ int sm[];
   int* cnt = sm;                   // [E]
   int* start = cnt + E;            // [E]
@@ -169,6 +171,8 @@ __global__ void __launch_bounds__(kAlignThreads) align_small_kernel(
 __global__ void __launch_bounds__(256) align_hist_kernel(const int32_t* __restrict__ ids,
                                                          int n, int E,
                                                          int32_t* __restrict__ chunk_cnt) {
+  pdl_wait();
+  pdl_trigger();
   extern __shared__ int hist[];
   for (int q = threadIdx.x; q < E; q += blockDim.x) hist[q] = 0;
   __syncthreads();
@@ -186,6 +190,8 @@ __global__ void __launch_bounds__(kAlignThreads) align_scan_kernel(
     int32_t* __restrict__ chunk_cnt, int chunks, int n, int E, int B, int max_padded,
     int32_t* __restrict__ sorted_ids, int32_t* __restrict__ expert_ids, int32_t* npp,
     int32_t* counts) {
+  pdl_wait();
+  pdl_trigger();
   extern __shared__ int sm[];
   int* cnt = sm;
   int* start = cnt + E;
@@ -212,6 +218,8 @@ __global__ void __launch_bounds__(kAlignThreads) align_scan_kernel(
 __global__ void __launch_bounds__(kAlignThreads) align_scatter_kernel(
     const int32_t* __restrict__ ids, const int32_t* __restrict__ chunk_base, int n, int E,
     int32_t* __restrict__ sorted_ids) {
+  pdl_wait();
+  pdl_trigger();
   extern __shared__ int sm[];
   int* run_base = sm;        // [E]
   int* wcnt = run_base + E;  // [kAlignWarps * E]
@@ -285,6 +293,8 @@ __global__ void __launch_bounds__(256) apply_expert_map_kernel(int32_t* __restri
                                                                int tiles,
                                                                const int32_t* __restrict__ map,
                                                                int E) {
+  pdl_wait();
+  pdl_trigger();
   for (int t = blockIdx.x * blockDim.x + threadIdx.x; t < tiles; t += gridDim.x * blockDim.x) {
     const int e = eid[t];
     if (e < 0) continue;
@@ -300,8 +310,7 @@ __global__ void __launch_bounds__(256) apply_expert_map_kernel(int32_t* __restri
 moe_status_t launch_apply_expert_map(int32_t* eid, int tiles, const int32_t* map, int E,
                                      cudaStream_t s) {
   const int blocks = std::max(1, std::min(ceil_div(tiles, 256), 64));
-  apply_expert_map_kernel<<<blocks, 256, 0, s>>>(eid, tiles, map, E);
-  return last_launch_status();
+  return launch_k(apply_expert_map_kernel, dim3(blocks), dim3(256), 0, s, eid, tiles, map, E);
 }
 
 // ---- fixed-capacity (masked) layout: the table is the identity on valid rows ----------
@@ -313,6 +322,8 @@ __global__ void __launch_bounds__(256) masked_table_kernel(const int32_t* __rest
                                                            int32_t* __restrict__ eid,
                                                            int32_t* __restrict__ npp,
                                                            float* __restrict__ ones) {
+  pdl_wait();
+  pdl_trigger();
   const int n = E * C;
   for (int p = blockIdx.x * blockDim.x + threadIdx.x; p < n; p += gridDim.x * blockDim.x) {
     const int e = p / C, i = p - e * C;
@@ -331,8 +342,8 @@ __global__ void __launch_bounds__(256) masked_table_kernel(const int32_t* __rest
 moe_status_t launch_masked_table(const int32_t* counts, int E, int C, int B, int32_t* sid,
                                  int32_t* eid, int32_t* npp, float* ones, cudaStream_t s) {
   const int blocks = std::max(1, std::min(ceil_div(E * C, 256), num_sms() * 4));
-  masked_table_kernel<<<blocks, 256, 0, s>>>(counts, E, C, B, sid, eid, npp, ones);
-  return last_launch_status();
+  return launch_k(masked_table_kernel, dim3(blocks), dim3(256), 0, s, counts, E, C, B, sid, eid,
+                  npp, ones);
 }
 
 static bool set_smem(const void* fn, size_t bytes) {
@@ -348,20 +359,22 @@ moe_status_t launch_align(const int32_t* ids, int T, int k, int E, int B, int ma
   if (n <= kSmallRows) {
     size_t smem = (size_t)(E * (2 + kAlignWarps) + 33) * sizeof(int);
     if (!set_smem((const void*)align_small_kernel, smem)) return MOE_ERR_CUDA;
-    align_small_kernel<<<1, kAlignThreads, smem, s>>>(ids, n, E, B, max_padded, sorted_ids,
-                                                      expert_ids, npp, counts);
-    return last_launch_status();
+    return launch_k(align_small_kernel, dim3(1), dim3(kAlignThreads), smem, s, ids, n, E, B,
+                    max_padded, sorted_ids, expert_ids, npp, counts);
   }
   const int chunks = ceil_div(n, kChunk);
   int32_t* cc = (int32_t*)scratch;
-  align_hist_kernel<<<chunks, 256, E * sizeof(int), s>>>(ids, n, E, cc);
+  if (launch_k(align_hist_kernel, dim3(chunks), dim3(256), E * sizeof(int), s, ids, n, E, cc) !=
+      MOE_OK)
+    return MOE_ERR_CUDA;
   size_t smem_scan = (size_t)(2 * E + 33) * sizeof(int);
-  align_scan_kernel<<<1, kAlignThreads, smem_scan, s>>>(cc, chunks, n, E, B, max_padded,
-                                                        sorted_ids, expert_ids, npp, counts);
+  if (launch_k(align_scan_kernel, dim3(1), dim3(kAlignThreads), smem_scan, s, cc, chunks, n, E, B,
+               max_padded, sorted_ids, expert_ids, npp, counts) != MOE_OK)
+    return MOE_ERR_CUDA;
   size_t smem_sc = (size_t)(E * (1 + kAlignWarps)) * sizeof(int);
   if (!set_smem((const void*)align_scatter_kernel, smem_sc)) return MOE_ERR_CUDA;
-  align_scatter_kernel<<<chunks, kAlignThreads, smem_sc, s>>>(ids, cc, n, E, sorted_ids);
-  return last_launch_status();
+  return launch_k(align_scatter_kernel, dim3(chunks), dim3(kAlignThreads), smem_sc, s, ids, cc, n,
+                  E, sorted_ids);
 }
 
 }  // namespace moe

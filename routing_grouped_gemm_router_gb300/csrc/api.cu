@@ -71,10 +71,19 @@ static bool block_m_ok(const moe_config_t* c, int block_m) {
   return block_m >= 1 && block_m % block_m_for(c->dtype) == 0 && block_m <= 4096;
 }
 
-// Bytes of GEMM1's scratch: the routed token rows in padded order (bf16 path only).
-static size_t gemm1_scratch_bytes(const moe_config_t* c, int block_m) {
+// Bytes of the gathered routed rows in padded order (bf16 path only).
+static size_t gather_bytes(const moe_config_t* c, int block_m) {
   if (c->dtype != MOE_BF16) return 0;
   return align_up(moe_max_padded_rows(c->T, c->k, c->E, block_m) * (size_t)c->H * 2, 256);
+}
+// Split-K scratch of grouped GEMM 1 or 2 (bf16 tensor-core path only).
+static size_t split_bytes(int gemm, const moe_config_t* c, int block_m) {
+  if (c->dtype != MOE_BF16) return 0;
+  return gemm_split_bytes(gemm, *c, (int)moe_max_padded_rows(c->T, c->k, c->E, block_m));
+}
+// Bytes of GEMM1's scratch: the gathered rows, then GEMM1's split-K scratch.
+static size_t gemm1_scratch_bytes(const moe_config_t* c, int block_m) {
+  return gather_bytes(c, block_m) + split_bytes(1, c, block_m);
 }
 
 }  // namespace moe
@@ -142,8 +151,9 @@ moe_status_t moe_workspace_layout(const moe_config_t* cfg, moe_ws_layout_t* L) {
   L->counts = take((size_t)c->E * 4);
   L->align_scratch = take(align_scratch_bytes(c->T, c->k, c->E, B));
   L->act = take(mp * c->I * es);
-  L->xs = take(gemm1_scratch_bytes(c, B));
+  L->xs = take(gather_bytes(c, B));
   L->y = take(n * c->H * es);
+  L->splitk = take(std::max(split_bytes(1, c, B), split_bytes(2, c, B)));
   L->total = off;
   L->block_m = B;
   L->max_padded = (int)mp;
@@ -220,10 +230,21 @@ moe_status_t moe_gather_rows(const void* x, const int32_t* sorted_ids,
                             H * (int)dtype_size(dtype), xs, stream);
 }
 
+moe_status_t moe_expert_gemm1_gathered_workspace_size(const moe_config_t* cfg, int block_m,
+                                                      size_t* bytes) {
+  moe_status_t st = check_gemm_args(cfg, block_m);
+  if (st != MOE_OK) return st;
+  if (!bytes) return MOE_ERR_INVALID_ARG;
+  const moe_config_t eff = effective(cfg);
+  *bytes = split_bytes(1, &eff, block_m);
+  return MOE_OK;
+}
+
 moe_status_t moe_expert_gemm1_gathered(const moe_config_t* cfg, const void* xs,
                                        const void* W13, const int32_t* sorted_ids,
                                        const int32_t* expert_ids, const int32_t* npp,
-                                       int block_m, void* act, cudaStream_t stream) {
+                                       int block_m, void* act, void* ws, size_t ws_bytes,
+                                       cudaStream_t stream) {
   moe_status_t st = check_gemm_args(cfg, block_m);
   const moe_config_t eff = effective(cfg);
   const moe_config_t* c = &eff;
@@ -231,8 +252,11 @@ moe_status_t moe_expert_gemm1_gathered(const moe_config_t* cfg, const void* xs,
   if (c->dtype != MOE_BF16) return MOE_ERR_UNSUPPORTED;
   if (!xs || !W13 || !sorted_ids || !expert_ids || !npp || !act) return MOE_ERR_INVALID_ARG;
   if (!aligned16(xs) || !aligned16(W13) || !aligned16(act)) return MOE_ERR_INVALID_ARG;
+  const size_t need = split_bytes(1, c, block_m);
+  if (need && (!ws || ws_bytes < need || ((uintptr_t)ws & 255u))) return MOE_ERR_WORKSPACE;
   const int mp = (int)moe_max_padded_rows(c->T, c->k, c->E, block_m);
-  return launch_gemm1_tc(*c, xs, W13, sorted_ids, expert_ids, npp, block_m, mp, act, stream);
+  return launch_gemm1_tc(*c, xs, W13, sorted_ids, expert_ids, npp, block_m, mp, act, ws,
+                         ws_bytes, stream);
 }
 
 moe_status_t moe_expert_gemm1(const moe_config_t* cfg, const void* x, const void* W13,
@@ -250,17 +274,28 @@ moe_status_t moe_expert_gemm1(const moe_config_t* cfg, const void* x, const void
     if (!ws || ws_bytes < need || ((uintptr_t)ws & 255u)) return MOE_ERR_WORKSPACE;
     st = moe_gather_rows(x, sorted_ids, npp, c->T, c->k, c->H, c->dtype, ws, stream);
     if (st != MOE_OK) return st;
+    const size_t gb = gather_bytes(c, block_m);
     return moe_expert_gemm1_gathered(cfg, ws, W13, sorted_ids, expert_ids, npp, block_m, act,
-                                     stream);
+                                     (uint8_t*)ws + gb, ws_bytes - gb, stream);
   }
   return launch_gemm1_simt(*c, (const float*)x, (const float*)W13, sorted_ids, expert_ids, npp,
                            block_m, mp, (float*)act, stream);
 }
 
+moe_status_t moe_expert_gemm2_workspace_size(const moe_config_t* cfg, int block_m,
+                                             size_t* bytes) {
+  moe_status_t st = check_gemm_args(cfg, block_m);
+  if (st != MOE_OK) return st;
+  if (!bytes) return MOE_ERR_INVALID_ARG;
+  const moe_config_t eff = effective(cfg);
+  *bytes = split_bytes(2, &eff, block_m);
+  return MOE_OK;
+}
+
 moe_status_t moe_expert_gemm2(const moe_config_t* cfg, const void* act, const void* W2,
                               const int32_t* sorted_ids, const int32_t* expert_ids,
                               const int32_t* npp, int block_m, const float* topk_w, void* y,
-                              cudaStream_t stream) {
+                              void* ws, size_t ws_bytes, cudaStream_t stream) {
   moe_status_t st = check_gemm_args(cfg, block_m);
   const moe_config_t eff = effective(cfg);
   const moe_config_t* c = &eff;
@@ -270,8 +305,10 @@ moe_status_t moe_expert_gemm2(const moe_config_t* cfg, const void* act, const vo
   const int mp = (int)moe_max_padded_rows(c->T, c->k, c->E, block_m);
   if (c->dtype == MOE_BF16) {
     if (!aligned16(act) || !aligned16(W2) || !aligned16(y)) return MOE_ERR_INVALID_ARG;
+    const size_t need = split_bytes(2, c, block_m);
+    if (need && (!ws || ws_bytes < need || ((uintptr_t)ws & 255u))) return MOE_ERR_WORKSPACE;
     return launch_gemm2_tc(*c, act, W2, sorted_ids, expert_ids, npp, block_m, mp, topk_w, y,
-                           stream);
+                           ws, ws_bytes, stream);
   }
   return launch_gemm2_simt(*c, (const float*)act, (const float*)W2, sorted_ids, expert_ids, npp,
                            block_m, mp, topk_w, (float*)y, stream);
@@ -285,7 +322,8 @@ moe_status_t moe_grouped_swiglu_workspace_size(const moe_config_t* cfg, int bloc
   if (st != MOE_OK) return st;
   if (!bytes) return MOE_ERR_INVALID_ARG;
   const size_t mp = moe_max_padded_rows(c->T, c->k, c->E, block_m);
-  *bytes = align_up(mp * c->I * dtype_size(c->dtype), 256) + gemm1_scratch_bytes(c, block_m);
+  *bytes = align_up(mp * c->I * dtype_size(c->dtype), 256) +
+           std::max(gemm1_scratch_bytes(c, block_m), split_bytes(2, c, block_m));
   return MOE_OK;
 }
 
@@ -305,7 +343,8 @@ moe_status_t moe_grouped_swiglu(const moe_config_t* c, const void* x, const void
   st = moe_expert_gemm1(c, x, W13, sorted_ids, expert_ids, npp, block_m, act, act + act_bytes,
                         ws_bytes - act_bytes, stream);
   if (st != MOE_OK) return st;
-  return moe_expert_gemm2(c, act, W2, sorted_ids, expert_ids, npp, block_m, topk_w, y, stream);
+  return moe_expert_gemm2(c, act, W2, sorted_ids, expert_ids, npp, block_m, topk_w, y,
+                          act + act_bytes, ws_bytes - act_bytes, stream);
 }
 
 moe_status_t moe_combine(const void* y, int T, int k, int H, moe_dtype_t dtype, void* out,
@@ -372,7 +411,8 @@ moe_status_t moe_masked_workspace_size(const moe_config_t* cfg, int capacity, si
   if (!bytes) return MOE_ERR_INVALID_ARG;
   const size_t n = (size_t)m.T, B = block_m_for(m.dtype);
   *bytes = align_up(n * 4, 256) + align_up(n / B * 4, 256) + 256 + align_up(n * 4, 256) +
-           align_up(n * m.I * dtype_size(m.dtype), 256);
+           align_up(n * m.I * dtype_size(m.dtype), 256) +
+           std::max(split_bytes(1, &m, (int)B), split_bytes(2, &m, (int)B));
   return MOE_OK;
 }
 
@@ -399,6 +439,9 @@ moe_status_t moe_masked_forward(const moe_config_t* cfg, const void* x_masked,
   float* ones = (float*)b;
   b += align_up(n * 4, 256);
   void* act = b;
+  b += align_up(n * m.I * dtype_size(m.dtype), 256);
+  void* split_ws = b;  // split-K scratch, shared by the two GEMMs (they run one after another)
+  const size_t split_ws_bytes = std::max(split_bytes(1, &m, B), split_bytes(2, &m, B));
   st = launch_masked_table(counts, m.E, capacity, B, sid, eid, npp, row_w ? nullptr : ones,
                            stream);
   if (st != MOE_OK) return st;
@@ -410,9 +453,11 @@ moe_status_t moe_masked_forward(const moe_config_t* cfg, const void* x_masked,
   if (m.dtype == MOE_BF16) {
     if (!aligned16(x_masked) || !aligned16(W13) || !aligned16(W2) || !aligned16(y_masked))
       return MOE_ERR_INVALID_ARG;
-    st = launch_gemm1_tc(m, x_masked, W13, sid, eid, npp, B, rows, act, stream);
+    st = launch_gemm1_tc(m, x_masked, W13, sid, eid, npp, B, rows, act, split_ws,
+                         split_ws_bytes, stream);
     if (st != MOE_OK) return st;
-    return launch_gemm2_tc(m, act, W2, sid, eid, npp, B, rows, w, y_masked, stream);
+    return launch_gemm2_tc(m, act, W2, sid, eid, npp, B, rows, w, y_masked, split_ws,
+                           split_ws_bytes, stream);
   }
   st = launch_gemm1_simt(m, (const float*)x_masked, (const float*)W13, sid, eid, npp, B, rows,
                          (float*)act, stream);
@@ -446,11 +491,18 @@ moe_status_t moe_forward(const moe_config_t* c, const void* x, const void* Wg, c
       (st = moe_apply_expert_map(eid, L.max_padded / L.block_m, c->expert_map, e.E, stream)) !=
           MOE_OK)
     return st;
-  if ((st = moe_expert_gemm1(c, x, W13, sid, eid, npp, L.block_m, b + L.act, b + L.xs,
-                             L.y - L.xs, stream)) != MOE_OK)
+  if (e.dtype == MOE_BF16) {  // gather pass, then the tensor-core GEMM1 (split-K scratch)
+    if ((st = moe_gather_rows(x, sid, npp, e.T, e.k, e.H, e.dtype, b + L.xs, stream)) != MOE_OK)
+      return st;
+    if ((st = moe_expert_gemm1_gathered(c, b + L.xs, W13, sid, eid, npp, L.block_m, b + L.act,
+                                        b + L.splitk, L.total - L.splitk, stream)) != MOE_OK)
+      return st;
+  } else if ((st = moe_expert_gemm1(c, x, W13, sid, eid, npp, L.block_m, b + L.act, nullptr, 0,
+                                    stream)) != MOE_OK) {
     return st;
-  if ((st = moe_expert_gemm2(c, b + L.act, W2, sid, eid, npp, L.block_m, w, b + L.y, stream)) !=
-      MOE_OK)
+  }
+  if ((st = moe_expert_gemm2(c, b + L.act, W2, sid, eid, npp, L.block_m, w, b + L.y,
+                             b + L.splitk, L.total - L.splitk, stream)) != MOE_OK)
     return st;
   if (c->expert_map)
     return moe_combine_local(b + L.y, ids, c->expert_map, e.T, e.k, e.H, e.dtype, out, stream);

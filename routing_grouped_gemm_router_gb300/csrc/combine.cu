@@ -12,6 +12,8 @@ namespace moe {
 __global__ void __launch_bounds__(256) combine_bf16_kernel(const uint4* __restrict__ y,
                                                            uint4* __restrict__ out, int T,
                                                            int k, int vec_per_row) {
+  pdl_wait();
+  pdl_trigger();
   const int64_t total = (int64_t)T * vec_per_row;
   for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < total;
        i += (int64_t)gridDim.x * blockDim.x) {
@@ -39,6 +41,8 @@ __global__ void __launch_bounds__(256) combine_bf16_kernel(const uint4* __restri
 __global__ void __launch_bounds__(256) combine_f32_kernel(const float4* __restrict__ y,
                                                           float4* __restrict__ out, int T,
                                                           int k, int vec_per_row) {
+  pdl_wait();
+  pdl_trigger();
   const int64_t total = (int64_t)T * vec_per_row;
   for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < total;
        i += (int64_t)gridDim.x * blockDim.x) {
@@ -60,6 +64,8 @@ __global__ void __launch_bounds__(256) combine_local_kernel(const void* __restri
                                                             const int32_t* __restrict__ map,
                                                             void* __restrict__ out, int T,
                                                             int k, int vec_per_row) {
+  pdl_wait();
+  pdl_trigger();
   const int64_t total = (int64_t)T * vec_per_row;
   for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < total;
        i += (int64_t)gridDim.x * blockDim.x) {
@@ -100,10 +106,10 @@ moe_status_t launch_combine_local(const void* y, const int32_t* ids, const int32
   int blocks = (int)std::min<int64_t>(ceil_div64(total, 256), (int64_t)num_sms() * 8);
   if (blocks < 1) blocks = 1;
   if (dt == MOE_BF16)
-    combine_local_kernel<true><<<blocks, 256, 0, s>>>(y, ids, map, out, T, k, vec);
-  else
-    combine_local_kernel<false><<<blocks, 256, 0, s>>>(y, ids, map, out, T, k, vec);
-  return last_launch_status();
+    return launch_k(combine_local_kernel<true>, dim3(blocks), dim3(256), 0, s, y, ids, map, out, T,
+                    k, vec);
+  return launch_k(combine_local_kernel<false>, dim3(blocks), dim3(256), 0, s, y, ids, map, out, T, k,
+                  vec);
 }
 
 moe_status_t launch_combine(const void* y, int T, int k, int H, moe_dtype_t dt, void* out,
@@ -113,10 +119,10 @@ moe_status_t launch_combine(const void* y, int T, int k, int H, moe_dtype_t dt, 
   int blocks = (int)std::min<int64_t>(ceil_div64(total, 256), (int64_t)num_sms() * 8);
   if (blocks < 1) blocks = 1;
   if (dt == MOE_BF16)
-    combine_bf16_kernel<<<blocks, 256, 0, s>>>((const uint4*)y, (uint4*)out, T, k, vec);
-  else
-    combine_f32_kernel<<<blocks, 256, 0, s>>>((const float4*)y, (float4*)out, T, k, vec);
-  return last_launch_status();
+    return launch_k(combine_bf16_kernel, dim3(blocks), dim3(256), 0, s, (const uint4*)y,
+                    (uint4*)out, T, k, vec);
+  return launch_k(combine_f32_kernel, dim3(blocks), dim3(256), 0, s, (const float4*)y,
+                  (float4*)out, T, k, vec);
 }
 
 }  // namespace moe

@@ -7,6 +7,7 @@
 #include <stdint.h>
 
 #include <algorithm>
+#include <utility>
 
 #include "moe.h"
 
@@ -30,6 +31,34 @@ inline moe_status_t last_launch_status() {
 
 inline size_t dtype_size(moe_dtype_t d) { return d == MOE_BF16 ? 2 : 4; }
 
+// ---------------------------------------------------------------- programmatic dependent launch
+// Every kernel of the library is launched with programmatic stream serialisation and starts
+// with pdl_wait() (before any global-memory access, before any early return): its launch and
+// prologue overlap the previous kernel's tail, while its memory operations still begin only
+// after the previous grid has completed and its writes are visible. pdl_trigger() lets the
+// next kernel launch as soon as every CTA of this grid has started.
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_trigger() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
+template <typename... KArgs, typename... Args>
+inline moe_status_t launch_k(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                             cudaStream_t s, Args&&... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kern, std::forward<Args>(args)...) == cudaSuccess ? MOE_OK
+                                                                                    : MOE_ERR_CUDA;
+}
+
 // ---------------------------------------------------------------- kernel entry wrappers
 // Implemented in the .cu files; all enqueue on `stream` and return MOE_OK/MOE_ERR_CUDA.
 
@@ -52,13 +81,16 @@ moe_status_t launch_gemm2_simt(const moe_config_t& c, const float* act, const fl
                                const int32_t* sid, const int32_t* eid, const int32_t* npp,
                                int block_m, int max_padded, const float* topk_w, float* y,
                                cudaStream_t s);
+// Split-K scratch (fp32 partials + tile counters) of grouped GEMM 1 or 2; 0 = no split.
+size_t gemm_split_bytes(int gemm, const moe_config_t& c, int max_padded);
 moe_status_t launch_gemm1_tc(const moe_config_t& c, const void* xs, const void* W13,
                              const int32_t* sid, const int32_t* eid, const int32_t* npp,
-                             int block_m, int max_padded, void* act, cudaStream_t s);
+                             int block_m, int max_padded, void* act, void* ws, size_t ws_bytes,
+                             cudaStream_t s);
 moe_status_t launch_gemm2_tc(const moe_config_t& c, const void* act, const void* W2,
                              const int32_t* sid, const int32_t* eid, const int32_t* npp,
                              int block_m, int max_padded, const float* topk_w, void* y,
-                             cudaStream_t s);
+                             void* ws, size_t ws_bytes, cudaStream_t s);
 moe_status_t launch_gather_rows(const void* x, const int32_t* sid, const int32_t* npp,
                                 int n_rows, int k, int row_bytes, void* xs, cudaStream_t s);
 moe_status_t launch_masked_table(const int32_t* counts, int E, int C, int B, int32_t* sid,

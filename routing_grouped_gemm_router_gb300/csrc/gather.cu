@@ -16,6 +16,8 @@ __global__ void __launch_bounds__(256) gather_rows_kernel(const uint4* __restric
                                                           const int32_t* __restrict__ npp,
                                                           int n_rows, int k, int vec,
                                                           uint4* __restrict__ xs) {
+  pdl_wait();
+  pdl_trigger();
   const int lane = threadIdx.x & 31;
   const int warps = gridDim.x * (blockDim.x >> 5);
   const int total = *npp;
@@ -39,9 +41,8 @@ __global__ void __launch_bounds__(256) gather_rows_kernel(const uint4* __restric
 moe_status_t launch_gather_rows(const void* x, const int32_t* sid, const int32_t* npp,
                                 int n_rows, int k, int row_bytes, void* xs, cudaStream_t s) {
   const int blocks = num_sms() * 4;
-  gather_rows_kernel<<<blocks, 256, 0, s>>>((const uint4*)x, sid, npp, n_rows, k, row_bytes / 16,
-                                            (uint4*)xs);
-  return last_launch_status();
+  return launch_k(gather_rows_kernel, dim3(blocks), dim3(256), 0, s, (const uint4*)x, sid, npp,
+                  n_rows, k, row_bytes / 16, (uint4*)xs);
 }
 
 }  // namespace moe

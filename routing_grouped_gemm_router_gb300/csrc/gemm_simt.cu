@@ -17,6 +17,8 @@ __global__ void __launch_bounds__(256) gemm1_simt_kernel(
     const float* __restrict__ x, const float* __restrict__ W13, const int32_t* __restrict__ sid,
     const int32_t* __restrict__ eid, const int32_t* __restrict__ npp, int block_m, int n_rows,
     int k, int H, int I, float* __restrict__ act) {
+  pdl_wait();
+  pdl_trigger();
   __shared__ float As[kSimtBK][kSimtBM];
   __shared__ float Bg[kSimtBK][kSimtBN + 1];
   __shared__ float Bu[kSimtBK][kSimtBN + 1];
@@ -74,6 +76,8 @@ __global__ void __launch_bounds__(256) gemm2_simt_kernel(
     const float* __restrict__ act, const float* __restrict__ W2, const int32_t* __restrict__ sid,
     const int32_t* __restrict__ eid, const int32_t* __restrict__ npp, int block_m, int n_rows,
     int H, int I, const float* __restrict__ topk_w, float* __restrict__ y) {
+  pdl_wait();
+  pdl_trigger();
   __shared__ float As[kSimtBK][kSimtBM];
   __shared__ float Bs[kSimtBK][kSimtBN + 1];
   const int p0 = blockIdx.x * kSimtBM;
@@ -117,9 +121,8 @@ moe_status_t launch_gemm1_simt(const moe_config_t& c, const float* x, const floa
                                const int32_t* sid, const int32_t* eid, const int32_t* npp,
                                int block_m, int max_padded, float* act, cudaStream_t s) {
   dim3 grid(max_padded / kSimtBM, ceil_div(c.I, kSimtBN));
-  gemm1_simt_kernel<<<grid, 256, 0, s>>>(x, W13, sid, eid, npp, block_m, c.T * c.k, c.k, c.H,
-                                         c.I, act);
-  return last_launch_status();
+  return launch_k(gemm1_simt_kernel, grid, dim3(256), 0, s, x, W13, sid, eid, npp, block_m,
+                  c.T * c.k, c.k, c.H, c.I, act);
 }
 
 moe_status_t launch_gemm2_simt(const moe_config_t& c, const float* act, const float* W2,
@@ -127,9 +130,8 @@ moe_status_t launch_gemm2_simt(const moe_config_t& c, const float* act, const fl
                                int block_m, int max_padded, const float* topk_w, float* y,
                                cudaStream_t s) {
   dim3 grid(max_padded / kSimtBM, ceil_div(c.H, kSimtBN));
-  gemm2_simt_kernel<<<grid, 256, 0, s>>>(act, W2, sid, eid, npp, block_m, c.T * c.k, c.H, c.I,
-                                         topk_w, y);
-  return last_launch_status();
+  return launch_k(gemm2_simt_kernel, grid, dim3(256), 0, s, act, W2, sid, eid, npp, block_m,
+                  c.T * c.k, c.H, c.I, topk_w, y);
 }
 
 }  // namespace moe

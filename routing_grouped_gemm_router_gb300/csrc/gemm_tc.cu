@@ -58,6 +58,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   volatile int* abort_flag = (volatile int*)(tmem_slot + 1);
   int* status = &g_router_status;
 
+  pdl_trigger();
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
   if (threadIdx.x == 0) {
     for (int s = 0; s < kStages; ++s) {
@@ -83,6 +84,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
   const int num_kb = (P.H + BK - 1) / BK;
+  pdl_wait();  // x, Wg and logits are touched only past this point
 
   if (warp == 0) {
     // ------------------------------------------------------------ TMA producer
@@ -201,8 +203,7 @@ static moe_status_t launch_router(const CUtensorMap& mx, const CUtensorMap& mw,
     configured_dev = dev;
   }
   const int grid = std::min(num_sms(), P.m_tiles * P.n_tiles);
-  kern<<<grid, kThreads, smem, s>>>(mx, mw, P);
-  return last_launch_status();
+  return launch_k(kern, dim3(grid), dim3(kThreads), smem, s, mx, mw, P);
 }
 
 }  // namespace tc

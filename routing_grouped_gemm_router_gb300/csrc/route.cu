@@ -25,6 +25,8 @@ __global__ void __launch_bounds__(256) router_simt_kernel(const T* __restrict__ 
                                                           const T* __restrict__ Wg,
                                                           float* __restrict__ logits, int Tn,
                                                           int H, int E) {
+  pdl_wait();
+  pdl_trigger();
   __shared__ float xs[32][64 + 1];
   __shared__ float ws[32][64 + 1];
   const int t0 = blockIdx.x * 64, e0 = blockIdx.y * 64;
@@ -95,6 +97,8 @@ __global__ void __launch_bounds__(256) router_few_tokens_kernel(const T* __restr
                                                                 const T* __restrict__ Wg,
                                                                 float* __restrict__ logits,
                                                                 int Tn, int H, int E) {
+  pdl_wait();
+  pdl_trigger();
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
   const int e = blockIdx.x * 8 + warp;
   const int t0 = blockIdx.y * TB;
@@ -134,35 +138,31 @@ __global__ void __launch_bounds__(256) router_few_tokens_kernel(const T* __restr
 }
 
 template <int TB>
-static void launch_few(const moe_config_t& c, const void* x, const void* Wg, float* logits,
-                       cudaStream_t s) {
+static moe_status_t launch_few(const moe_config_t& c, const void* x, const void* Wg,
+                               float* logits, cudaStream_t s) {
   dim3 grid(ceil_div(c.E, 8), ceil_div(c.T, TB));
   if (c.dtype == MOE_F32)
-    router_few_tokens_kernel<float, TB><<<grid, 256, 0, s>>>((const float*)x, (const float*)Wg,
-                                                             logits, c.T, c.H, c.E);
-  else
-    router_few_tokens_kernel<__nv_bfloat16, TB><<<grid, 256, 0, s>>>(
-        (const __nv_bfloat16*)x, (const __nv_bfloat16*)Wg, logits, c.T, c.H, c.E);
+    return launch_k(router_few_tokens_kernel<float, TB>, grid, dim3(256), 0, s, (const float*)x,
+                    (const float*)Wg, logits, c.T, c.H, c.E);
+  return launch_k(router_few_tokens_kernel<__nv_bfloat16, TB>, grid, dim3(256), 0, s,
+                  (const __nv_bfloat16*)x, (const __nv_bfloat16*)Wg, logits, c.T, c.H, c.E);
 }
 
 moe_status_t launch_router_few_tokens(const moe_config_t& c, const void* x, const void* Wg,
                                       float* logits, cudaStream_t s) {
-  if (c.T <= 1) launch_few<1>(c, x, Wg, logits, s);
-  else if (c.T <= 8) launch_few<8>(c, x, Wg, logits, s);
-  else launch_few<16>(c, x, Wg, logits, s);
-  return last_launch_status();
+  if (c.T <= 1) return launch_few<1>(c, x, Wg, logits, s);
+  if (c.T <= 8) return launch_few<8>(c, x, Wg, logits, s);
+  return launch_few<16>(c, x, Wg, logits, s);
 }
 
 moe_status_t launch_router_simt(const moe_config_t& c, const void* x, const void* Wg,
                                 float* logits, cudaStream_t s) {
   dim3 grid(ceil_div(c.T, 64), ceil_div(c.E, 64));
   if (c.dtype == MOE_F32)
-    router_simt_kernel<float><<<grid, 256, 0, s>>>((const float*)x, (const float*)Wg, logits,
-                                                   c.T, c.H, c.E);
-  else
-    router_simt_kernel<__nv_bfloat16><<<grid, 256, 0, s>>>(
-        (const __nv_bfloat16*)x, (const __nv_bfloat16*)Wg, logits, c.T, c.H, c.E);
-  return last_launch_status();
+    return launch_k(router_simt_kernel<float>, grid, dim3(256), 0, s, (const float*)x,
+                    (const float*)Wg, logits, c.T, c.H, c.E);
+  return launch_k(router_simt_kernel<__nv_bfloat16>, grid, dim3(256), 0, s, (const __nv_bfloat16*)x,
+                  (const __nv_bfloat16*)Wg, logits, c.T, c.H, c.E);
 }
 
 // ------------------------------------------------------------------------------------
@@ -203,6 +203,8 @@ __global__ void __launch_bounds__(kTopkWarps * 32) topk_kernel(
     int n_group, int topk_group, const float* __restrict__ logit_bias,
     const float* __restrict__ select_bias, int n_shared, int32_t* __restrict__ ids,
     float* __restrict__ w) {
+  pdl_wait();
+  pdl_trigger();
   __shared__ float skey[kTopkWarps][512];
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
   const int t = blockIdx.x * kTopkWarps + warp;
@@ -322,10 +324,9 @@ __global__ void __launch_bounds__(kTopkWarps * 32) topk_kernel(
 moe_status_t launch_topk(const moe_config_t& c, const float* logits, int32_t* ids, float* w,
                          cudaStream_t s) {
   int grid = ceil_div(c.T, kTopkWarps);
-  topk_kernel<<<grid, kTopkWarps * 32, 0, s>>>(logits, c.T, c.E, c.k, (int)c.mode,
-                                              c.renormalize, c.scale, c.n_group, c.topk_group,
-                                              c.logit_bias, c.select_bias, c.n_shared, ids, w);
-  return last_launch_status();
+  return launch_k(topk_kernel, dim3(grid), dim3(kTopkWarps * 32), 0, s, logits, c.T, c.E, c.k,
+                  (int)c.mode, c.renormalize, c.scale, c.n_group, c.topk_group, c.logit_bias,
+                  c.select_bias, c.n_shared, ids, w);
 }
 
 }  // namespace moe

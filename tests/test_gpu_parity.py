@@ -272,6 +272,8 @@ LAYER_CASES = [
     mi.Workload("bf16-skewed", T=600, H=256, I=256, E=32, k=4, dtype="bf16",
                 logit_bias_std=1.5, seed=15),
     mi.Workload("bf16-top1", T=37, H=128, I=192, E=8, k=1, dtype="bf16", seed=16),
+    # decode with split-K over ragged k-block ranges (GEMM1 5 k-blocks, GEMM2 7 in 4 splits)
+    mi.Workload("bf16-decode-splitk", T=2, H=320, I=448, E=16, k=4, dtype="bf16", seed=18),
     mi.Workload("f32-ragged", T=100, H=72, I=88, E=6, k=3, dtype="f32", seed=17),
 ]
 
@@ -324,7 +326,9 @@ def test_separate_entry_points_match_forward(L):
     g1b = L.moe_expert_gemm1_workspace_size(cfg, B)
     g1ws = torch.empty(max(g1b, 1), dtype=torch.uint8, device=DEV)
     L.moe_expert_gemm1(cfg, inp.x, inp.W13, sid, eid, npp, B, act, g1ws, g1b)
-    L.moe_expert_gemm2(cfg, act, inp.W2, sid, eid, npp, B, w, y)
+    g2b = L.moe_expert_gemm2_workspace_size(cfg, B)
+    g2ws = torch.empty(max(g2b, 1), dtype=torch.uint8, device=DEV)
+    L.moe_expert_gemm2(cfg, act, inp.W2, sid, eid, npp, B, w, y, g2ws, g2b)
     L.moe_combine(y, T, k, H, L.MOE_BF16, out)
     torch.cuda.synchronize()
     assert torch.equal(out, out_fwd)
@@ -332,7 +336,9 @@ def test_separate_entry_points_match_forward(L):
     xs = torch.empty(mp, H, dtype=torch.bfloat16, device=DEV)
     act2 = torch.empty_like(act)
     L.moe_gather_rows(inp.x, sid, npp, T, k, H, L.MOE_BF16, xs)
-    L.moe_expert_gemm1_gathered(cfg, xs, inp.W13, sid, eid, npp, B, act2)
+    gb = L.moe_expert_gemm1_gathered_workspace_size(cfg, B)
+    gws = torch.empty(max(gb, 1), dtype=torch.uint8, device=DEV)
+    L.moe_expert_gemm1_gathered(cfg, xs, inp.W13, sid, eid, npp, B, act2, gws, gb)
     torch.cuda.synchronize()
     real = (sid < T * k).nonzero().flatten()
     assert torch.equal(act2[real], act[real])
@@ -382,7 +388,9 @@ def test_tile_boundaries_and_sentinels(L, dtype):
     g1b = L.moe_expert_gemm1_workspace_size(cfg, B)
     g1ws = torch.empty(max(g1b, 1), dtype=torch.uint8, device=DEV)
     L.moe_expert_gemm1(cfg, xd, W13d, sid, eid, npp, B, act, g1ws, g1b)
-    L.moe_expert_gemm2(cfg, act, W2d, sid, eid, npp, B, wd, y)
+    g2b = L.moe_expert_gemm2_workspace_size(cfg, B)
+    g2ws = torch.empty(max(g2b, 1), dtype=torch.uint8, device=DEV)
+    L.moe_expert_gemm2(cfg, act, W2d, sid, eid, npp, B, wd, y, g2ws, g2b)
     L.moe_combine(y, T, k, H, cfg.dtype, out)
     torch.cuda.synchronize()
     s = sid.cpu().numpy()
