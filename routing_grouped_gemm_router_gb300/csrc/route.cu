@@ -4,7 +4,7 @@
 // GEMM": §3 route() (softmax over E, top-k, renormalise) and §4 route_grouped() (sigmoid
 // scores, selection-only bias, groups scored by the sum of their two best biased scores,
 // top-k inside the kept groups, weights from the unbiased scores, renormalise, scale).
-#include "common.cuh"
+#include "route_dev.cuh"
 
 namespace moe {
 
@@ -72,26 +72,6 @@ __global__ void __launch_bounds__(256) router_simt_kernel(const T* __restrict__ 
 // partial sums are reduced with shuffles. E/8 x ceil(T/TB) CTAs of 8 warps spread the
 // router matrix over many SMs instead of one tensor-core tile.
 // ------------------------------------------------------------------------------------
-template <typename T>
-__device__ __forceinline__ void load8(const T* p, float (&v)[8]);
-template <>
-__device__ __forceinline__ void load8<__nv_bfloat16>(const __nv_bfloat16* p, float (&v)[8]) {
-  const uint4 q = *reinterpret_cast<const uint4*>(p);
-  const __nv_bfloat162* h = reinterpret_cast<const __nv_bfloat162*>(&q);
-#pragma unroll
-  for (int i = 0; i < 4; ++i) {
-    float2 f = __bfloat1622float2(h[i]);
-    v[2 * i] = f.x;
-    v[2 * i + 1] = f.y;
-  }
-}
-template <>
-__device__ __forceinline__ void load8<float>(const float* p, float (&v)[8]) {
-  const float4 a = *reinterpret_cast<const float4*>(p);
-  const float4 b = *reinterpret_cast<const float4*>(p + 4);
-  v[0] = a.x; v[1] = a.y; v[2] = a.z; v[3] = a.w; v[4] = b.x; v[5] = b.y; v[6] = b.z; v[7] = b.w;
-}
-
 template <typename T, int TB>
 __global__ void __launch_bounds__(256) router_few_tokens_kernel(const T* __restrict__ x,
                                                                 const T* __restrict__ Wg,
@@ -99,42 +79,11 @@ __global__ void __launch_bounds__(256) router_few_tokens_kernel(const T* __restr
                                                                 int Tn, int H, int E) {
   pdl_wait();
   pdl_trigger();
-  const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+  const int warp = threadIdx.x / 32;
   const int e = blockIdx.x * 8 + warp;
   const int t0 = blockIdx.y * TB;
   if (e >= E) return;
-  // Token rows past the end are clamped to the last row (loaded, never stored), so every
-  // load below is unconditional and the loads of a group can all be in flight together.
-  const T* xr[TB];
-#pragma unroll
-  for (int t = 0; t < TB; ++t) xr[t] = x + (size_t)min(t0 + t, Tn - 1) * H;
-  float acc[TB];
-#pragma unroll
-  for (int t = 0; t < TB; ++t) acc[t] = 0.f;
-  const T* w = Wg + (size_t)e * H;
-#pragma unroll 2
-  for (int h = lane * 8; h < H; h += 256) {
-    float wv[8];
-    load8(w + h, wv);
-#pragma unroll
-    for (int tg = 0; tg < TB; tg += 8) {
-      constexpr int G = TB < 8 ? TB : 8;
-      float xv[G][8];
-#pragma unroll
-      for (int j = 0; j < G; ++j) load8(xr[tg + j] + h, xv[j]);
-#pragma unroll
-      for (int j = 0; j < G; ++j)
-#pragma unroll
-        for (int q = 0; q < 8; ++q) acc[tg + j] = fmaf(xv[j][q], wv[q], acc[tg + j]);
-    }
-  }
-#pragma unroll
-  for (int t = 0; t < TB; ++t) {
-    float v = acc[t];
-#pragma unroll
-    for (int off = 16; off > 0; off >>= 1) v += __shfl_xor_sync(0xffffffffu, v, off);
-    if (lane == (t & 31) && t0 + t < Tn) logits[(size_t)(t0 + t) * E + e] = v;
-  }
+  router_warp_logits<T, TB>(x, Wg, logits, t0, Tn, H, E, e);
 }
 
 template <int TB>
@@ -170,34 +119,6 @@ moe_status_t launch_router_simt(const moe_config_t& c, const void* x, const void
 // warp-wide argmax (larger key wins, equal keys go to the lower id) over the experts not
 // taken yet, so slot j holds the j-th largest key.
 // ------------------------------------------------------------------------------------
-struct KeyId {
-  float v;
-  int e;
-};
-
-__device__ __forceinline__ bool better(float v, int e, float v2, int e2) {
-  return v > v2 || (v == v2 && e < e2);
-}
-
-__device__ __forceinline__ KeyId warp_argmax(float v, int e) {
-#pragma unroll
-  for (int off = 16; off > 0; off >>= 1) {
-    float v2 = __shfl_xor_sync(0xffffffffu, v, off);
-    int e2 = __shfl_xor_sync(0xffffffffu, e, off);
-    if (better(v2, e2, v, e)) { v = v2; e = e2; }
-  }
-  return {v, e};
-}
-
-__device__ __forceinline__ float warp_sum(float v) {
-#pragma unroll
-  for (int off = 16; off > 0; off >>= 1) v += __shfl_xor_sync(0xffffffffu, v, off);
-  return v;
-}
-
-constexpr int kTopkWarps = 8;
-constexpr int kMaxPerLane = 16;  // E <= 512
-
 __global__ void __launch_bounds__(kTopkWarps * 32) topk_kernel(
     const float* __restrict__ logits, int Tn, int E, int k, int mode, int renorm, float scale,
     int n_group, int topk_group, const float* __restrict__ logit_bias,
@@ -206,119 +127,11 @@ __global__ void __launch_bounds__(kTopkWarps * 32) topk_kernel(
   pdl_wait();
   pdl_trigger();
   __shared__ float skey[kTopkWarps][512];
-  const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+  const int warp = threadIdx.x / 32;
   const int t = blockIdx.x * kTopkWarps + warp;
   if (t >= Tn) return;
-  const float* lrow = logits + (size_t)t * E;
-  const float NEG = -INFINITY;
-
-  float key[kMaxPerLane], val[kMaxPerLane];
-#pragma unroll
-  for (int i = 0; i < kMaxPerLane; ++i) {
-    int e = lane + 32 * i;
-    key[i] = NEG;
-    val[i] = 0.f;
-    if (e < E) {
-      float l = lrow[e];
-      if (mode == MOE_ROUTE_SOFTMAX) {
-        if (logit_bias) l += logit_bias[e];
-        key[i] = l;
-        val[i] = l;
-      } else {
-        float sg = 1.f / (1.f + expf(-l));
-        val[i] = sg;
-        key[i] = select_bias ? sg + select_bias[e] : sg;
-      }
-    }
-  }
-
-  if (mode == MOE_ROUTE_SIGMOID_GROUPED && n_group > 1) {
-    // Group score = sum of the two largest biased keys of E/n_group consecutive experts.
-#pragma unroll
-    for (int i = 0; i < kMaxPerLane; ++i) {
-      int e = lane + 32 * i;
-      if (e < E) skey[warp][e] = key[i];
-    }
-    __syncwarp();
-    const int per = E / n_group;
-    float gscore = NEG;
-    if (lane < n_group) {
-      float b1 = NEG, b2 = NEG;
-      for (int q = 0; q < per; ++q) {
-        float v = skey[warp][lane * per + q];
-        if (v > b1) { b2 = b1; b1 = v; } else if (v > b2) { b2 = v; }
-      }
-      gscore = per >= 2 ? b1 + b2 : b1;
-    }
-    uint32_t kept = 0;
-    for (int g = 0; g < topk_group; ++g) {
-      KeyId best = warp_argmax(lane < n_group ? gscore : NEG, lane < n_group ? lane : 1 << 30);
-      kept |= 1u << best.e;
-      if (lane == best.e) gscore = NEG;
-    }
-#pragma unroll
-    for (int i = 0; i < kMaxPerLane; ++i) {
-      int e = lane + 32 * i;
-      if (e < E && !((kept >> (e / per)) & 1u)) key[i] = NEG;
-    }
-  }
-
-  // k rounds of warp argmax. Taken entries drop to a key below every real one.
-  float my_sel_val = 0.f;   // lane j keeps the value of slot j
-  int my_sel_id = 0;
-  bool taken[kMaxPerLane];
-#pragma unroll
-  for (int i = 0; i < kMaxPerLane; ++i) taken[i] = false;
-  for (int j = 0; j < k; ++j) {
-    float bv = NEG;
-    int be = 1 << 30;
-#pragma unroll
-    for (int i = 0; i < kMaxPerLane; ++i) {
-      int e = lane + 32 * i;
-      if (e < E && !taken[i] && (be == (1 << 30) || better(key[i], e, bv, be))) {
-        bv = key[i];
-        be = e;
-      }
-    }
-    KeyId best = warp_argmax(bv, be);
-    float sel_val = 0.f;
-    if ((best.e & 31) == lane) {
-      int i = best.e >> 5;
-#pragma unroll
-      for (int q = 0; q < kMaxPerLane; ++q)
-        if (q == i) { taken[q] = true; sel_val = val[q]; }
-    }
-    sel_val = __shfl_sync(0xffffffffu, sel_val, best.e & 31);
-    if (lane == j) { my_sel_val = sel_val; my_sel_id = best.e; }
-  }
-
-  float wj;
-  if (mode == MOE_ROUTE_SOFTMAX) {
-    float top = __shfl_sync(0xffffffffu, my_sel_val, 0);  // slot 0 holds the largest logit
-    if (renorm) {
-      float ex = lane < k ? expf(my_sel_val - top) : 0.f;
-      wj = ex / warp_sum(ex);
-    } else {
-      float part = 0.f;
-#pragma unroll
-      for (int i = 0; i < kMaxPerLane; ++i) {
-        int e = lane + 32 * i;
-        if (e < E) part += expf(val[i] - top);
-      }
-      wj = expf(my_sel_val - top) / warp_sum(part);
-    }
-  } else {
-    float sv = lane < k ? my_sel_val : 0.f;
-    wj = renorm ? sv / warp_sum(sv) : sv;
-  }
-  const int kk = k + n_shared;  // row stride: routed slots, then the shared experts
-  if (lane < k) {
-    ids[(size_t)t * kk + lane] = my_sel_id;
-    w[(size_t)t * kk + lane] = scale * wj;
-  } else if (lane < kk) {
-    ids[(size_t)t * kk + lane] = E + (lane - k);
-    w[(size_t)t * kk + lane] = 1.f;
-  }
+  topk_token(logits, t, E, k, mode, renorm, scale, n_group, topk_group, logit_bias, select_bias,
+             n_shared, ids, w, skey[warp]);
 }
 
 moe_status_t launch_topk(const moe_config_t& c, const float* logits, int32_t* ids, float* w,
