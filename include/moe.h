@@ -290,6 +290,13 @@ moe_status_t moe_forward(const moe_config_t* cfg, const void* x, const void* Wg,
                          const void* W13, const void* W2, void* out, void* ws,
                          size_t ws_bytes, cudaStream_t stream);
 
+/* Diagnostic self-test of the failure path: enqueues one CTA whose pipeline waits nothing
+ * will satisfy (it also holds tensor memory). After the 2 s pipeline-wait limit the waits
+ * give up, the CTA frees its tensor memory and returns, and the device status word reads 2
+ * (a pipeline wait ran out of time): a stalled pipeline ends with a status, not a hang, and
+ * the context stays usable. Takes about 2 s of device time. */
+moe_status_t moe_selftest_wait_timeout(cudaStream_t stream);
+
 /* Diagnostic (synchronises the current device): returns the device status word (0 = no
  * fault seen; 1 = an expert id outside [0, E); 2 = a pipeline wait ran out of time; 3 = the
  * two CTAs of a tensor-core pair were given different tensor-memory columns) and

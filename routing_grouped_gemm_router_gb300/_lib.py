@@ -80,6 +80,7 @@ def _load():
         "moe_combine_local": (ST, [P, P, P, I32, I32, I32, I32, P, P]),
         "moe_forward": (ST, [CFG, P, P, P, P, P, P, SZ, P]),
         "moe_device_status": (I32, [I32]),
+        "moe_selftest_wait_timeout": (ST, [P]),
     }
     for name, (res, args) in sig.items():
         f = getattr(lib, name)
@@ -96,7 +97,7 @@ EXPORTED = ("moe_abi_version", "moe_status_string", "moe_block_m", "moe_max_padd
             "moe_expert_gemm2_workspace_size", "moe_expert_gemm2",
             "moe_grouped_swiglu", "moe_combine", "moe_apply_expert_map", "moe_combine_local",
             "moe_masked_table", "moe_masked_workspace_size", "moe_masked_forward",
-            "moe_forward", "moe_device_status")
+            "moe_forward", "moe_device_status", "moe_selftest_wait_timeout")
 
 
 def lib():
@@ -143,6 +144,12 @@ def make_config(T, H, I, E, k, dtype=MOE_BF16, mode=MOE_ROUTE_SOFTMAX, renormali
                         _ptr(expert_map), int(n_shared),
                         MOE_WEIGHTS_FP8_E4M3_B128 if fp8 else MOE_WEIGHTS_NATIVE,
                         _ptr(w13_scale), _ptr(w2_scale))
+
+
+def moe_selftest_wait_timeout(stream=None):
+    """Diagnostic: a CTA whose pipeline waits time out (see include/moe.h); afterwards
+    moe_device_status() reads 2."""
+    _check("moe_selftest_wait_timeout", _lib.moe_selftest_wait_timeout(_stream(stream)))
 
 
 def moe_abi_version() -> int:

@@ -509,6 +509,10 @@ moe_status_t moe_forward(const moe_config_t* c, const void* x, const void* Wg, c
   return moe_combine(b + L.y, e.T, e.k, e.H, e.dtype, out, stream);
 }
 
+moe_status_t moe_selftest_wait_timeout(cudaStream_t stream) {
+  return launch_selftest_wait(stream);
+}
+
 int moe_device_status(int reset) {
   const int a = align_status_read(reset);
   const int r = router_status_read(reset);

@@ -102,6 +102,8 @@ moe_status_t launch_combine_local(const void* y, const int32_t* ids, const int32
 moe_status_t launch_combine(const void* y, int T, int k, int H, moe_dtype_t dt, void* out,
                             cudaStream_t s);
 
+moe_status_t launch_selftest_wait(cudaStream_t s);
+
 int align_status_read(int reset);
 int router_status_read(int reset);
 int grouped_status_read(int reset);

@@ -773,7 +773,45 @@ static moe_status_t setup_split(const SplitPlan& sp, void* ws, size_t ws_bytes, 
                   P.cnt, n);
 }
 
+// Failure-path self-test: one CTA allocates tensor memory, then two warps wait, through the
+// same bounded wait as the GEMM pipelines, on mbarriers that nothing ever arrives on. The
+// first wait gives up after the pipeline time limit, raises the CTA's abort flag and records
+// kStatusTimeout; the second sees the flag and gives up too; the CTA frees its tensor
+// memory and returns.
+__global__ void __launch_bounds__(64, 1) selftest_wait_kernel() {
+  pdl_wait();
+  pdl_trigger();
+  __shared__ uint64_t bars[2];
+  __shared__ uint32_t tmem_slot;
+  __shared__ int abort_sh;
+  volatile int* abort_flag = &abort_sh;
+  const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+  if (threadIdx.x == 0) {
+    mbar_init(&bars[0], 1);
+    mbar_init(&bars[1], 1);
+    *abort_flag = 0;
+    mbar_init_fence();
+  }
+  if (warp == 1) {
+    tmem_alloc<1>(&tmem_slot, 32);
+    tmem_relinquish<1>();
+    tc_fence_before();
+  }
+  __syncthreads();
+  tc_fence_after();
+  if (lane == 0) wait_bounded(&bars[warp], 0, abort_flag, &g_grouped_status);
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc<1>(tmem_slot, 32);
+  }
+}
+
 }  // namespace tc2
+
+moe_status_t launch_selftest_wait(cudaStream_t s) {
+  return launch_k(tc2::selftest_wait_kernel, dim3(1), dim3(64), 0, s);
+}
 
 int grouped_status_read(int reset) {
   int v = 0;

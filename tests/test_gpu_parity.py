@@ -410,6 +410,28 @@ def test_tile_boundaries_and_sentinels(L, dtype):
     assert_close(to_np(out), ref, dtype)
 
 
+def test_stalled_pipeline_times_out_with_a_status(L):
+    """A pipeline wait that nothing satisfies gives up after its limit (about 2 s): the kernel
+    returns, the status word reads 2, and the context still runs a layer correctly."""
+    import time
+    L.moe_device_status(True)
+    t0 = time.time()
+    L.moe_selftest_wait_timeout()
+    torch.cuda.synchronize()
+    dt = time.time() - t0
+    assert L.moe_device_status(True) == 2
+    assert 1.5 < dt < 30
+    wl = mi.Workload("after-timeout", T=64, H=128, I=128, E=8, k=2, dtype="bf16", seed=71)
+    inp = mi.make_layer(wl, "cpu")
+    enforce_margins(inp)
+    inp = _to_dev(inp)
+    out = _layer(L, inp)(inp.x)
+    torch.cuda.synchronize()
+    ids, w = oracle_route_from_logits(oracle_logits(inp), wl)
+    assert_close(to_np(out), _oracle_out(inp, ids, w), "bf16")
+    assert L.moe_device_status(True) == 0
+
+
 def test_all_tokens_to_one_expert(L):
     T, H, I, E, k = 700, 256, 256, 16, 2
     g = torch.Generator().manual_seed(9)
