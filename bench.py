@@ -269,9 +269,17 @@ def run_ours(args, wl):
     if args.ep_half:
         emap = torch.tensor([e if e % 2 == 0 else -1 for e in range(wl.E + args.shared)],
                             dtype=torch.int32, device=dev)
-    layer = MoELayer(inp.Wg, inp.W13, inp.W2, wl.k, wl.mode, wl.renormalize, wl.scale,
-                     wl.n_group, wl.topk_group, inp.logit_bias, inp.select_bias, emap,
-                     n_shared=args.shared, w13_scale=sc13, w2_scale=sc2)
+    # Decode streams only the active experts' weights (gpt-oss T=1: 0.2 GB, not much more
+    # than the 126 MB L2): successive steps rotate over three copies of the expert weights so
+    # that each step reads them from HBM, not from L2 left warm by the step before.
+    n_copies = 3 if is_decode(wl) else 1
+    W13s = [inp.W13] + [inp.W13.clone() for _ in range(n_copies - 1)]
+    W2s = [inp.W2] + [inp.W2.clone() for _ in range(n_copies - 1)]
+    layers = [MoELayer(inp.Wg, W13s[c], W2s[c], wl.k, wl.mode, wl.renormalize, wl.scale,
+                       wl.n_group, wl.topk_group, inp.logit_bias, inp.select_bias, emap,
+                       n_shared=args.shared, w13_scale=sc13, w2_scale=sc2)
+              for c in range(n_copies)]
+    layer = layers[0]
     wbytes = 1 if args.fp8 else inp.x.element_size()  # bytes per expert weight
     # the align step, the grouped GEMMs and the combine see shared experts as ordinary ones
     T, k, E, H, I = wl.T, wl.k + args.shared, wl.E + args.shared, wl.H, wl.I
@@ -290,7 +298,7 @@ def run_ours(args, wl):
     sh = stream.cuda_stream
     gathered = wl.dtype == "bf16"  # bf16 GEMM1 = row gather + tensor-core GEMM, timed apart
 
-    def step(ev=None, sh=sh):
+    def step(ev=None, sh=sh, c=0):
         # The same kernels moe_forward enqueues, called stage by stage so that CUDA events
         # between them give each stage's device time.
         if ev is not None:
@@ -309,17 +317,17 @@ def run_ours(args, wl):
                               p["xs"], sh)
             if ev is not None:
                 ev[3].record(stream)
-            L.moe_expert_gemm1_gathered(cfg, p["xs"], inp.W13, p["sorted_ids"], p["expert_ids"],
+            L.moe_expert_gemm1_gathered(cfg, p["xs"], W13s[c], p["sorted_ids"], p["expert_ids"],
                                         p["num_post_padded"], B, p["act"], p["splitk"],
                                         ws_split, sh)
         else:
             if ev is not None:
                 ev[3].record(stream)
-            L.moe_expert_gemm1(cfg, inp.x, inp.W13, p["sorted_ids"], p["expert_ids"],
+            L.moe_expert_gemm1(cfg, inp.x, W13s[c], p["sorted_ids"], p["expert_ids"],
                                p["num_post_padded"], B, p["act"], p["xs"], ws_xs, sh)
         if ev is not None:
             ev[4].record(stream)
-        L.moe_expert_gemm2(cfg, p["act"], inp.W2, p["sorted_ids"], p["expert_ids"],
+        L.moe_expert_gemm2(cfg, p["act"], W2s[c], p["sorted_ids"], p["expert_ids"],
                            p["num_post_padded"], B, p["topk_w"], p["y"], p["splitk"], ws_split,
                            sh)
         if ev is not None:
@@ -333,9 +341,9 @@ def run_ours(args, wl):
 
     # router GEMM + top-k, align (one kernel up to 4096 rows, else three), row gather + GEMM1
     # (bf16), GEMM2, combine
-    def forward(sh=sh):
+    def forward(sh=sh, c=0):
         # the timed step: the public entry point, moe_forward, with the workspace above
-        L.moe_forward(cfg, inp.x, inp.Wg, inp.W13, inp.W2, out, ws, lay.total, sh)
+        L.moe_forward(cfg, inp.x, inp.Wg, W13s[c], W2s[c], out, ws, lay.total, sh)
 
     # kernels moe_forward enqueues: router GEMM + top-k, align (one kernel up to 4096 rows,
     # else three), expert map, row gather (bf16), GEMM1, GEMM2 (each + a counter-zeroing
@@ -356,18 +364,22 @@ def run_ours(args, wl):
     local_rows = int(counts.sum())
 
     # ---- the step captured once in a CUDA graph (no host work or launch gaps in the timing)
-    graph = None
+    graphs = []
     if not args.no_graph:
-        cap = torch.cuda.Stream(dev)
-        cap.wait_stream(stream)
-        graph = torch.cuda.CUDAGraph()
-        with torch.cuda.stream(cap):
-            with torch.cuda.graph(graph, stream=cap):
-                forward(sh=cap.cuda_stream)
-        stream.wait_stream(cap)
+        for c in range(n_copies):
+            cap = torch.cuda.Stream(dev)
+            cap.wait_stream(stream)
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.stream(cap):
+                with torch.cuda.graph(g, stream=cap):
+                    forward(sh=cap.cuda_stream, c=c)
+            stream.wait_stream(cap)
+            graphs.append(g)
         for _ in range(3):
-            graph.replay()
+            for g in graphs:
+                g.replay()
         torch.cuda.synchronize()
+    graph = graphs[0] if graphs else None
 
     # ---- device-timed steps (inputs resident in HBM; expert weights larger than L2)
     sampler = ClockSampler(local)
@@ -381,9 +393,9 @@ def run_ours(args, wl):
     t_start.record(stream)
     for i in range(args.steps):
         if graph is not None:
-            graph.replay()
+            graphs[i % n_copies].replay()
         else:
-            forward()
+            forward(c=i % n_copies)
     t_end.record(stream)
     torch.cuda.synchronize()
     if dist is not None:
@@ -392,7 +404,7 @@ def run_ours(args, wl):
     # per-stage device times: the same steps launched eagerly with CUDA events between stages
     evs = [[torch.cuda.Event(enable_timing=True) for _ in range(7)] for _ in range(args.steps)]
     for i in range(args.steps):
-        step(evs[i])
+        step(evs[i], c=i % n_copies)
     torch.cuda.synchronize()
     clocks = sampler.stop()
     stage = {n: statistics.mean(e[i].elapsed_time(e[i + 1]) for e in evs)
@@ -402,9 +414,9 @@ def run_ours(args, wl):
     x_host = inp.x.cpu().pin_memory()
     out_host = torch.empty(T, H, dtype=inp.x.dtype).pin_memory()
     x_dev = torch.empty_like(inp.x)
-    for _ in range(3):
+    for i in range(3):
         x_dev.copy_(x_host, non_blocking=True)
-        layer(x_dev, out)
+        layers[i % n_copies](x_dev, out)
         out_host.copy_(out, non_blocking=True)
     torch.cuda.synchronize()
     if dist is not None:
@@ -412,9 +424,9 @@ def run_ours(args, wl):
     e0 = torch.cuda.Event(enable_timing=True)
     e1 = torch.cuda.Event(enable_timing=True)
     e0.record(stream)
-    for _ in range(args.steps):
+    for i in range(args.steps):
         x_dev.copy_(x_host, non_blocking=True)
-        layer(x_dev, out)
+        layers[i % n_copies](x_dev, out)
         out_host.copy_(out, non_blocking=True)
     e1.record(stream)
     torch.cuda.synchronize()
@@ -426,8 +438,13 @@ def run_ours(args, wl):
     e2e_val = flops * world / (e2e_ms * 1e-3) / 1e12
     hbm, bf16_burst, bf16_sus, peak_src = peaks()
     src = os.path.join(ROOT, "routing_grouped_gemm_router_gb300", "csrc", "gemm_tc2.cu")
-    if is_decode(wl):
-        # decode is HBM-bound: GEMM1 streams the gate/up weights of every active expert
+    # The bound follows the layer's intensity, useful FLOPs per byte of active expert weights
+    # (T*k/A for bf16), against the ridge of the measured peaks: decode and the
+    # DeepSeek-V3-shaped layer (128 FLOP/B) stream weights; Mixtral and Qwen3 are compute.
+    intensity = flops / max(1, active * 3 * H * I * wbytes)
+    hbm_bound = is_decode(wl) or intensity < bf16_sus * 1e12 / (hbm * 1e9)
+    if hbm_bound:
+        # GEMM1 streams the gate/up weights of every active expert
         w_bytes = active * 2 * H * I * wbytes
         roof = {"bound": "hbm", "achieved": w_bytes / (stage["gemm1"] * 1e-3) / 1e9,
                 "peak": hbm, "unit": "GB/s", "kernel": "gemm1 (gate/up grouped GEMM)",
@@ -458,8 +475,11 @@ def run_ours(args, wl):
                        "T": T, "H": H, "I": I, "E": wl.E, "k": wl.k, "n_shared": args.shared,
                        "mode": "sigmoid-grouped" if wl.mode else "softmax",
                        "global_batch": T * world, "parallelism": f"replicas x{world}",
-                       "l2": "inputs larger than L2 (expert weights "
-                             f"{E * 3 * H * I * wbytes / 1e9:.2f} GB)",
+                       "l2": (f"{n_copies} copies of the expert weights rotated between "
+                              f"steps ({active * 3 * H * I * wbytes / 1e6:.0f} MB of active "
+                              "weights per step; L2 126 MB)") if n_copies > 1 else
+                             ("inputs larger than L2 (expert weights "
+                              f"{E * 3 * H * I * wbytes / 1e9:.2f} GB)"),
                        "block_m": B, "num_post_padded": npp, "active_experts": active},
             "stages_ms": {n: round(v, 5) for n, v in stage.items()},
             "roofline": roof,
@@ -467,14 +487,15 @@ def run_ours(args, wl):
                     "d2h_bytes_per_step": bytes_io, "ms_per_step": e2e_ms},
             "gpu_launches": launches_per_step * args.steps,
             "clocks": clocks}
-    if is_decode(wl):
+    line["intensity_flop_per_weight_byte"] = intensity
+    if hbm_bound:
         line["weight_gbs"] = active * 3 * H * I * wbytes / (ms * 1e-3) / 1e9
         line["weight_gbs_frac_of_hbm"] = line["weight_gbs"] / hbm
-    else:
+    if not is_decode(wl):
         line["frac_of_bf16_peak"] = value / bf16_sus
 
     if rank == 0 and world == 1 and not args.no_cpu_baseline and not args.fp8:
-        del layer
+        del layer, layers, W13s, W2s
         x, Wg, W13, W2, lb, sb = host_copies(inp)
         n = args.cpu_sample_tokens or default_sample(wl)
         dt, n, threads = time_oracle(wl, x, Wg, W13, W2, lb, sb, n)
@@ -510,28 +531,36 @@ def run_masked(args, wl):
     wsb = L.moe_masked_workspace_size(cfg, cap)
     ws = torch.empty(wsb, dtype=torch.uint8, device=dev)
 
-    def step(sh=None):
-        L.moe_masked_forward(cfg, xm, counts, cap, rw, inp.W13, inp.W2, y, ws, wsb, sh)
+    # three copies of the expert weights rotated between steps (each step reads from HBM)
+    W13s = [inp.W13, inp.W13.clone(), inp.W13.clone()]
+    W2s = [inp.W2, inp.W2.clone(), inp.W2.clone()]
 
-    for _ in range(max(3, args.warmup)):
-        step()
-    cap_s = torch.cuda.Stream(dev)
-    cap_s.wait_stream(torch.cuda.current_stream(dev))
-    graph = torch.cuda.CUDAGraph()
-    with torch.cuda.stream(cap_s):
-        with torch.cuda.graph(graph, stream=cap_s):
-            step(cap_s.cuda_stream)
-    torch.cuda.current_stream(dev).wait_stream(cap_s)
+    def step(sh=None, c=0):
+        L.moe_masked_forward(cfg, xm, counts, cap, rw, W13s[c], W2s[c], y, ws, wsb, sh)
+
+    for i in range(max(3, args.warmup)):
+        step(c=i % 3)
+    graphs = []
+    for c in range(3):
+        cap_s = torch.cuda.Stream(dev)
+        cap_s.wait_stream(torch.cuda.current_stream(dev))
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.stream(cap_s):
+            with torch.cuda.graph(g, stream=cap_s):
+                step(cap_s.cuda_stream, c)
+        torch.cuda.current_stream(dev).wait_stream(cap_s)
+        graphs.append(g)
     for _ in range(3):
-        graph.replay()
+        for g in graphs:
+            g.replay()
     torch.cuda.synchronize()
     sampler = ClockSampler(0)
     sampler.start()
     time.sleep(0.3)
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     e0.record()
-    for _ in range(args.steps):
-        graph.replay()
+    for i in range(args.steps):
+        graphs[i % 3].replay()
     e1.record()
     torch.cuda.synchronize()
     clocks = sampler.stop()
@@ -546,7 +575,8 @@ def run_masked(args, wl):
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
             "data": "synthetic (uniform top-k draw bucketed per expert)",
             "config": {"workload": wl.name + "+masked", "T": T, "H": H, "I": I, "E": E, "k": k,
-                       "capacity": cap, "rows": rows, "active_experts": active},
+                       "capacity": cap, "rows": rows, "active_experts": active,
+                       "l2": "3 copies of the expert weights rotated between steps"},
             "weight_gbs": gbs, "weight_gbs_frac_of_hbm": gbs / hbm, "clocks": clocks}
     print(json.dumps(line), flush=True)
 
