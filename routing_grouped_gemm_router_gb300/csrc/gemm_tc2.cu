@@ -332,7 +332,26 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Roles<FP8>::kThreads
     tc_fence_before();
   }
 
+  // Everything up to griddepcontrol.wait touches shared and tensor memory only, so it
+  // overlaps the previous kernel's tail.
+  cluster_sync();  // barriers of both CTAs initialised, TMEM allocated in both
+  tc_fence_after();
+  const uint32_t tmem_base = *tmem_slot;
+  bool pair_tmem_mismatch = false;
+  if (threadIdx.x == 0) {
+    // Both CTAs of the pair must see the same TMEM columns: the leader's MMAs write the
+    // peer's rows at the leader's address. A mismatch stops the kernel with a status code.
+    uint32_t peer_slot, other;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(peer_slot) : "r"(su32(tmem_slot)), "r"(rank ^ 1u));
+    asm volatile("ld.shared::cluster.u32 %0, [%1];" : "=r"(other) : "r"(peer_slot) : "memory");
+    if (other != tmem_base) {
+      *abort_flag = 1;
+      pair_tmem_mismatch = true;
+    }
+  }
+
   pdl_wait();  // global memory is touched only past this point
+  if (pair_tmem_mismatch) atomicExch(status, kStatusPairTmem);
   // ---- run table: expert runs of the m-tile sequence, pairs per run, prefix of pairs
   const int num_m = min((*P.npp) / BM, kMaxTiles);
   for (int t = threadIdx.x; t < num_m; t += blockDim.x) {
@@ -384,21 +403,6 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Roles<FP8>::kThreads
     if (lane == 0) {
       run_pref[nr] = pairs;
       *nruns_sh = nr;
-    }
-  }
-  __syncthreads();
-  cluster_sync();  // barriers of both CTAs initialised, TMEM allocated in both
-  tc_fence_after();
-  const uint32_t tmem_base = *tmem_slot;
-  if (threadIdx.x == 0) {
-    // Both CTAs of the pair must see the same TMEM columns: the leader's MMAs write the
-    // peer's rows at the leader's address. A mismatch stops the kernel with a status code.
-    uint32_t peer_slot, other;
-    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(peer_slot) : "r"(su32(tmem_slot)), "r"(rank ^ 1u));
-    asm volatile("ld.shared::cluster.u32 %0, [%1];" : "=r"(other) : "r"(peer_slot) : "memory");
-    if (other != tmem_base) {
-      *abort_flag = 1;
-      atomicExch(status, kStatusPairTmem);
     }
   }
   __syncthreads();
