@@ -49,7 +49,7 @@ extern "C" {
 typedef enum {
   MOE_OK = 0,
   MOE_ERR_INVALID_ARG = 1,  /* a null pointer, a size out of range, misaligned memory */
-  MOE_ERR_UNSUPPORTED = 2,  /* valid arguments this build does not handle (e.g. E > 512) */
+  MOE_ERR_UNSUPPORTED = 2,  /* valid arguments the library does not handle (e.g. E > 512) */
   MOE_ERR_WORKSPACE = 3,    /* workspace pointer null or smaller than required */
   MOE_ERR_CUDA = 4          /* a CUDA runtime/driver call or a kernel launch failed */
 } moe_status_t;
