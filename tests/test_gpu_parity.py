@@ -485,10 +485,14 @@ def test_cuda_graph_capture_and_replay(L):
 
 # --------------------------------------------------------------------- expert parallelism
 
-@pytest.mark.parametrize("dtype,variant", [("bf16", "half"), ("bf16", "perm"), ("f32", "half")])
+@pytest.mark.parametrize("dtype,variant", [("bf16", "half"), ("bf16", "perm"), ("f32", "half"),
+                                           ("fp8", "perm")])
 def test_expert_map(L, dtype, variant):
     """Odd experts held elsewhere (map -1), or local experts stored in permuted weight slots:
-    the layer equals the oracle with the same expert_map; tiles carry the mapped labels."""
+    the layer equals the oracle with the same expert_map; tiles carry the mapped labels.
+    "fp8": the permuted slots hold FP8 codes whose block scales are permuted with them."""
+    fp8 = dtype == "fp8"
+    dtype = "bf16" if fp8 else dtype
     H, I = (256, 256) if dtype == "bf16" else (64, 96)
     wl = mi.Workload("ep", T=300, H=H, I=I, E=16, k=4, dtype=dtype, seed=31)
     inp = mi.make_layer(wl, "cpu")
@@ -501,9 +505,13 @@ def test_expert_map(L, dtype, variant):
         emap = torch.tensor([(5 * e + 3) % E for e in range(E)], dtype=torch.int32)
         W13, W2 = torch.empty_like(inp.W13), torch.empty_like(inp.W2)
         W13[emap.long()], W2[emap.long()] = inp.W13, inp.W2
+    sc = {}
+    if fp8:  # quantise the stored (slot-ordered) weights; the oracle takes their exact values
+        (W13, s13), (W2, s2) = mi.quantize_fp8_w13(W13), mi.quantize_fp8_blocks(W2)
+        sc = dict(w13_scale=s13.to(DEV), w2_scale=s2.to(DEV))
     dev = _to_dev(mi.LayerInputs(wl, inp.x, inp.Wg, W13, W2))
     from routing_grouped_gemm_router_gb300.layer import MoELayer
-    layer = MoELayer(dev.Wg, dev.W13, dev.W2, wl.k, expert_map=emap.to(DEV))
+    layer = MoELayer(dev.Wg, dev.W13, dev.W2, wl.k, expert_map=emap.to(DEV), **sc)
     out = layer(dev.x)
     torch.cuda.synchronize()
     mids = layer.intermediates(wl.T)
@@ -512,10 +520,14 @@ def test_expert_map(L, dtype, variant):
     B, mp = mids["block_m"], mids["max_padded"]
     _, eid, _, _ = O.moe_align(ids, B, E, max_padded=mp)
     assert np.array_equal(to_np(mids["expert_ids"]), O.apply_expert_map(eid, emap.numpy()))
-    ref = O.moe_loop(to_np(inp.x), ids, w, weights_for_oracle(W13), weights_for_oracle(W2),
-                     expert_map=emap.numpy())
+    if fp8:
+        W13o = O.dequant_w13(W13.numpy(), s13.double().numpy())
+        W2o = O.dequant_blockwise(W2.numpy(), s2.double().numpy())
+    else:
+        W13o, W2o = weights_for_oracle(W13), weights_for_oracle(W2)
+    ref = O.moe_loop(to_np(inp.x), ids, w, W13o, W2o, expert_map=emap.numpy())
     assert_close(to_np(out), ref, dtype)
-    if variant == "perm":  # same layer as without expert parallelism
+    if variant == "perm" and not fp8:  # same layer as without expert parallelism
         plain = O.moe_loop(to_np(inp.x), ids, w, weights_for_oracle(inp.W13),
                            weights_for_oracle(inp.W2))
         assert_close(to_np(out), plain, dtype)
