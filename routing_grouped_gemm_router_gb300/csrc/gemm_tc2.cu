@@ -34,8 +34,14 @@
 // Work order: expert by expert, each weight panel with all of that expert's m-tile pairs
 // back to back (the skill card's L2 grouping at expert granularity), so the pairs running at
 // the same time share a few panels. Each CTA builds the (expert run -> pair) table in shared
-// memory from expert_ids at start-up. Every mbarrier wait is bounded (time-out: status
-// kStatusTimeout, abort, copies in flight drained, TMEM freed).
+// memory from expert_ids at start-up, after the programmatic-launch dependency wait; barrier
+// set-up, TMEM allocation and the pair check come before it and overlap the previous
+// kernel. Every mbarrier wait is bounded (time-out: status kStatusTimeout, abort, copies in
+// flight drained, TMEM freed).
+//
+// Variants of the same kernel: split-K for decode-sized problems (items split along K, fp32
+// partial sums, the last split of a tile finishes it), and FP8 E4M3 weights with 128 x 128
+// block scales, turned into the bf16 operand by converter warps (see Roles below).
 #include "tc_ptx.cuh"
 
 namespace moe {
