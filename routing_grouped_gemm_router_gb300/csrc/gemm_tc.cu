@@ -221,11 +221,16 @@ int router_status_read(int reset) {
 moe_status_t launch_router_tc(const moe_config_t& c, const void* x, const void* Wg,
                               float* logits, cudaStream_t s) {
   using namespace tc;
-  // Expert tile BN (multiple of 32, <= 256): the smallest split of E that still gives every
-  // SM a tile, when there are few 128-token tiles.
+  // Expert tile BN (multiple of 32, <= 256): split E into narrower tiles while all tiles
+  // still run in one wave. A tile's time is set by its K loop, not by BN, so a second wave
+  // of narrower tiles costs a whole tile time more.
   const int m_tiles = ceil_div(c.T, BM);
   int bn = (c.E + 31) / 32 * 32;
-  while (bn > 32 && m_tiles * ceil_div(c.E, bn) < num_sms()) bn = (bn / 2 + 31) / 32 * 32;
+  while (bn > 32) {
+    const int half = (bn / 2 + 31) / 32 * 32;
+    if (m_tiles * ceil_div(c.E, half) > num_sms()) break;
+    bn = half;
+  }
   if (bn > 256) return MOE_ERR_UNSUPPORTED;
   CUtensorMap mx, mw;
   const uint64_t H = c.H, E = c.E, T = c.T;
