@@ -427,8 +427,21 @@ def test_dequant_w13_gate_and_up_have_their_own_grids():
 
 # ----------------------------------------------------------------- planted mistakes
 
+def check_fp8():
+    """The FP8 pins as one check (a planted mistake may also make them raise)."""
+    try:
+        test_e4m3_decoder_known_codes()
+        test_e4m3_decoder_matches_torch_on_all_codes()
+        test_dequant_blockwise_uses_the_right_block()
+        test_dequant_w13_gate_and_up_have_their_own_grids()
+        return True
+    except (AssertionError, IndexError, ValueError):
+        return False
+
+
 def _all_pins(golden_dir):
     return {
+        "fp8": check_fp8(),
         "tiny": check_tiny_loads(golden_dir),
         "loop_dense": check_loop_vs_dense_tiny(),
         "deepseek": check_deepseek_toy(golden_dir),
@@ -517,6 +530,28 @@ def _mut_loop_wrong_slot_weight(x, ids, w, W13, W2, tokens=None):
 _orig_loop = OM.moe_loop
 
 
+def _mut_e4m3_bias8(codes):
+    c = np.asarray(codes, dtype=np.uint8).astype(np.int64)
+    sign = np.where(c & 0x80, -1.0, 1.0)
+    e, m = (c >> 3) & 0xF, c & 0x7
+    val = np.where(e == 0, m / 8.0 * 2.0 ** -7, (1.0 + m / 8.0) * 2.0 ** (e - 8))
+    return sign * np.where((e == 0xF) & (m == 0x7), np.nan, val)
+
+
+def _mut_scale_grid_transposed(codes, scales, block=128):
+    v = OM.e4m3_to_f64(codes)
+    sc = O.f64(scales)
+    n, k = v.shape[-2], v.shape[-1]
+    rows = np.arange(n) // block
+    cols = np.arange(k) // block
+    return v * sc[..., cols[None, :] % sc.shape[-2], rows[:, None] % sc.shape[-1]]
+
+
+def _mut_w13_one_stacked_grid(codes13, scales13, block=128):
+    E, G, RB, KB = scales13.shape
+    return OM.dequant_blockwise(codes13, np.asarray(scales13).reshape(E, G * RB, KB), block)
+
+
 @pytest.mark.parametrize("name,attr,mut", [
     ("swap gate/up", "expert_ffn", _mut_swap_gate_up),
     ("no renormalisation", "route_softmax", _mut_no_renorm),
@@ -526,6 +561,9 @@ _orig_loop = OM.moe_loop
     ("weights from biased scores", "route_sigmoid_grouped", _mut_sigmoid_weights_biased),
     ("sentinel off by one", "moe_align", _mut_sentinel),
     ("slot weights swapped", "moe_loop", _mut_loop_wrong_slot_weight),
+    ("E4M3 exponent bias 8", "e4m3_to_f64", _mut_e4m3_bias8),
+    ("block scales indexed transposed", "dequant_blockwise", _mut_scale_grid_transposed),
+    ("gate and up on one stacked scale grid", "dequant_w13", _mut_w13_one_stacked_grid),
 ])
 def test_planted_mistake_is_caught(monkeypatch, golden_dir, name, attr, mut):
     assert all(_all_pins(golden_dir).values())
