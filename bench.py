@@ -57,6 +57,8 @@ def parse():
                         "weights quantised); tokens, router and GEMM arithmetic stay bf16")
     p.add_argument("--tokens", type=int, default=0,
                    help="override T of the workload (smaller cases for profiling)")
+    p.add_argument("--experts", type=int, default=0,
+                   help="override E of the workload (smaller cases for profiling)")
     return p.parse_args()
 
 
@@ -80,19 +82,31 @@ def peaks():
         return 6800.0, 1900.0, 1700.0, "fallback"
 
 
-def profile_traffic(kernel: str, wl_name: str, src_path: str):
+def profile_traffic(kernel: str, wl_name: str, active: int, src_path: str):
     """DRAM bytes per launch recorded in a committed ncu summary, if the kernel source it
-    was taken on is unchanged (the summary stores the source's sha256); else None."""
-    path = os.path.join(ROOT, "profiles", f"{kernel}_{wl_name.split('@')[0]}.md")
+    was taken on is unchanged (the summary stores the source's sha256); else None.
+
+    A summary holds either a per-launch figure of its own workload, or a figure per active
+    expert taken on a smaller expert count of the same launch shape (the same rows per
+    expert, the same split), scaled here by the launch's active experts; the workloads it
+    stands for are listed on its traffic_workloads line (names without the @E= suffix)."""
+    base = wl_name.split("@")[0]
+    path = os.path.join(ROOT, "profiles", f"{kernel}_{base}.md")
     if not os.path.exists(path):
         return None
     txt = open(path).read()
-    m = re.search(r"traffic_bytes_per_launch:\s*([0-9.eE+]+)", txt)
     h = re.search(r"source_sha256:\s*([0-9a-f]{64})", txt)
-    if not m or not h:
+    if not h or hashlib.sha256(open(src_path, "rb").read()).hexdigest() != h.group(1):
         return None
-    cur = hashlib.sha256(open(src_path, "rb").read()).hexdigest()
-    return float(m.group(1)) if cur == h.group(1) else None
+    m = re.search(r"traffic_bytes_per_launch:\s*([0-9.eE+]+)", txt)
+    if m:
+        return float(m.group(1)) if wl_name == base else None
+    m = re.search(r"traffic_bytes_per_active_expert:\s*([0-9.eE+]+)", txt)
+    w = re.search(r"traffic_workloads:(.*)", txt)
+    name = re.sub(r"@E=\d+", "", wl_name)
+    if m and w and name in w.group(1).split():
+        return float(m.group(1)) * active
+    return None
 
 
 class ClockSampler:
@@ -458,7 +472,8 @@ def run_ours(args, wl):
                 "algorithmic_flops_per_launch": g1_flops,
                 "peak_kind": f"{peak_src} bf16 sustained (kernel timed inside a long step loop)"}
     roof["frac"] = roof["achieved"] / roof["peak"]
-    roof["traffic"] = profile_traffic("gemm1" + ("_fp8" if args.fp8 else ""), wl.name, src)
+    roof["traffic"] = profile_traffic("gemm1" + ("_fp8" if args.fp8 else ""), wl.name,
+                                      active, src)
 
     line = {"metric": METRIC, "value": value, "unit": "TFLOPS", "n_gpus": world,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
@@ -586,6 +601,9 @@ def main():
     wl = workload(args.workload)
     if args.tokens:
         wl = wl.with_T(args.tokens)
+    if args.experts:
+        import dataclasses
+        wl = dataclasses.replace(wl, E=args.experts, name=f"{wl.name}@E={args.experts}")
     if args.impl == "reference":
         run_reference(args, wl)
     elif args.masked:
