@@ -310,7 +310,10 @@ def run_ours(args, wl):
     out = torch.empty(T, H, dtype=inp.x.dtype, device=dev)
     stream = torch.cuda.current_stream(dev)
     sh = stream.cuda_stream
-    gathered = wl.dtype == "bf16"  # bf16 GEMM1 = row gather + tensor-core GEMM, timed apart
+    # bf16 GEMM1 = row gather + tensor-core GEMM, timed apart; small batches (decode up to
+    # 8 tokens) run the CUDA-core grouped GEMMs, which read the token rows in place
+    small = L.moe_small_batch(cfg)
+    gathered = wl.dtype == "bf16" and not small
 
     def step(ev=None, sh=sh, c=0):
         # The same kernels moe_forward enqueues, called stage by stage so that CUDA events
@@ -360,11 +363,11 @@ def run_ours(args, wl):
         L.moe_forward(cfg, inp.x, inp.Wg, W13s[c], W2s[c], out, ws, lay.total, sh)
 
     # kernels moe_forward enqueues: router GEMM + top-k, align (one kernel up to 4096 rows,
-    # else three), expert map, row gather (bf16), GEMM1, GEMM2 (each + a counter-zeroing
-    # kernel when split along K) and the combine
+    # else three), expert map, row gather (bf16 tensor-core path), GEMM1, GEMM2 (each + a
+    # counter-zeroing kernel when split along K) and the combine
     launches_per_step = 2 + (1 if T * k <= 4096 else 3) + (1 if emap is not None else 0) + \
-        (1 if wl.dtype == "bf16" else 0) + 3 + \
-        sum(1 for g in (1, 2) if split_ws_bytes(L, cfg, B, g) > 0)
+        (1 if gathered else 0) + 3 + \
+        (0 if small else sum(1 for g in (1, 2) if split_ws_bytes(L, cfg, B, g) > 0))
 
     for _ in range(max(3, args.warmup)):
         step()
@@ -451,7 +454,6 @@ def run_ours(args, wl):
     value = flops * world / (ms * 1e-3) / 1e12
     e2e_val = flops * world / (e2e_ms * 1e-3) / 1e12
     hbm, bf16_burst, bf16_sus, peak_src = peaks()
-    src = os.path.join(ROOT, "routing_grouped_gemm_router_gb300", "csrc", "gemm_tc2.cu")
     # The bound follows the layer's intensity, useful FLOPs per byte of active expert weights
     # (T*k/A for bf16), against the ridge of the measured peaks: decode and the
     # DeepSeek-V3-shaped layer (128 FLOP/B) stream weights; Mixtral and Qwen3 are compute.
@@ -461,7 +463,9 @@ def run_ours(args, wl):
         # GEMM1 streams the gate/up weights of every active expert
         w_bytes = active * 2 * H * I * wbytes
         roof = {"bound": "hbm", "achieved": w_bytes / (stage["gemm1"] * 1e-3) / 1e9,
-                "peak": hbm, "unit": "GB/s", "kernel": "gemm1 (gate/up grouped GEMM)",
+                "peak": hbm, "unit": "GB/s",
+                "kernel": "gemm1 (gate/up grouped GEMV, small batch)" if small else
+                          "gemm1 (gate/up grouped GEMM)",
                 "algorithmic_bytes_per_launch": w_bytes,
                 "peak_kind": f"{peak_src} HBM copy bandwidth"}
     else:
@@ -472,8 +476,10 @@ def run_ours(args, wl):
                 "algorithmic_flops_per_launch": g1_flops,
                 "peak_kind": f"{peak_src} bf16 sustained (kernel timed inside a long step loop)"}
     roof["frac"] = roof["achieved"] / roof["peak"]
-    roof["traffic"] = profile_traffic("gemm1" + ("_fp8" if args.fp8 else ""), wl.name,
-                                      active, src)
+    kern = "gemv1" if small else "gemm1"
+    src = os.path.join(ROOT, "routing_grouped_gemm_router_gb300", "csrc",
+                       "gemv.cu" if small else "gemm_tc2.cu")
+    roof["traffic"] = profile_traffic(kern + ("_fp8" if args.fp8 else ""), wl.name, active, src)
 
     line = {"metric": METRIC, "value": value, "unit": "TFLOPS", "n_gpus": world,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,

@@ -44,7 +44,7 @@
 extern "C" {
 #endif
 
-#define MOE_ABI_VERSION 4
+#define MOE_ABI_VERSION 5
 
 typedef enum {
   MOE_OK = 0,
@@ -142,6 +142,11 @@ const char* moe_status_string(moe_status_t s);
  * (one tensor-core M tile), 16 for fp32. Host arithmetic only. Returns 0 on bad args. */
 int moe_block_m(const moe_config_t* cfg);
 
+/* 1 when the grouped GEMMs of this configuration run as the small-batch kernels (bf16
+ * layers of at most 2 tokens, or at most 32 with FP8 expert weights; see
+ * moe_expert_gemm1), 0 otherwise or on bad args. Host arithmetic only. */
+int moe_small_batch(const moe_config_t* cfg);
+
 /* Worst-case padded length T*k + min(E, T*k)*(block_m-1) (page §5: every expert that can
  * hold a row pads at most block_m-1 slots). Host arithmetic only; 0 on bad args. */
 size_t moe_max_padded_rows(int T, int k, int E, int block_m);
@@ -202,7 +207,15 @@ moe_status_t moe_apply_expert_map(int32_t* expert_ids, int num_tiles, const int3
  * work items cannot fill the GPU twice over (decode), each item is split along K; the
  * splits write fp32 partial sums to the GEMM's workspace and the last split of a tile adds
  * them in split order and applies the epilogue (deterministic). The workspace sizes below
- * include that scratch; it depends only on cfg and block_m. */
+ * include that scratch; it depends only on cfg and block_m.
+ *
+ * Small batches (moe_small_batch(cfg) = 1: bf16 layers of at most 2 tokens, 32 with FP8
+ * weights): a tile then holds a few
+ * real rows, and both grouped GEMMs run on CUDA cores as one pass over the active experts'
+ * weights, fp32 products of the same operands summed in another order than the tensor-core
+ * kernels' (the results agree to within rounding, not bit for bit). FP8 weights: each
+ * 16-code partial sum is scaled by its block scale. No workspace is touched and the bf16
+ * moe_expert_gemm1 reads the token rows in place (no gather). */
 moe_status_t moe_expert_gemm1_workspace_size(const moe_config_t* cfg, int block_m,
                                              size_t* bytes);
 moe_status_t moe_expert_gemm1(const moe_config_t* cfg, const void* x, const void* W13,

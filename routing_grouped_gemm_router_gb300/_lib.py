@@ -56,6 +56,7 @@ def _load():
         "moe_abi_version": (I32, []),
         "moe_status_string": (ctypes.c_char_p, [ST]),
         "moe_block_m": (I32, [CFG]),
+        "moe_small_batch": (I32, [CFG]),
         "moe_max_padded_rows": (SZ, [I32, I32, I32, I32]),
         "moe_align_workspace_size": (ST, [I32, I32, I32, I32, ctypes.POINTER(SZ)]),
         "moe_workspace_layout": (ST, [CFG, ctypes.POINTER(moe_ws_layout_t)]),
@@ -89,7 +90,8 @@ def _load():
 
 
 _lib = _load()
-EXPORTED = ("moe_abi_version", "moe_status_string", "moe_block_m", "moe_max_padded_rows",
+EXPORTED = ("moe_abi_version", "moe_status_string", "moe_block_m", "moe_small_batch",
+            "moe_max_padded_rows",
             "moe_align_workspace_size", "moe_workspace_layout", "moe_workspace_size",
             "moe_route", "moe_align", "moe_align_noalloc", "moe_expert_gemm1_workspace_size",
             "moe_expert_gemm1", "moe_gather_rows", "moe_expert_gemm1_gathered_workspace_size",
@@ -158,6 +160,11 @@ def moe_abi_version() -> int:
 
 def moe_block_m(cfg) -> int:
     return _lib.moe_block_m(ctypes.byref(cfg))
+
+
+def moe_small_batch(cfg) -> bool:
+    """Whether the grouped GEMMs of cfg run as the small-batch (decode) kernels."""
+    return bool(_lib.moe_small_batch(ctypes.byref(cfg)))
 
 
 def moe_max_padded_rows(T, k, E, block_m) -> int:

@@ -110,6 +110,13 @@ int moe_block_m(const moe_config_t* cfg) {
   return block_m_for(cfg->dtype);
 }
 
+int moe_small_batch(const moe_config_t* cfg) {
+  if (check_cfg(cfg) != MOE_OK) return 0;
+  const moe_config_t e = effective(cfg);
+  const int B = block_m_for(e.dtype);
+  return gemv_applies(e, (int)moe_max_padded_rows(e.T, e.k, e.E, B)) ? 1 : 0;
+}
+
 size_t moe_max_padded_rows(int T, int k, int E, int block_m) {
   if (T < 1 || k < 1 || E < 1 || block_m < 1) return 0;
   // total = sum_e ceil(n_e / B) * B <= T*k + min(E, T*k) * (B - 1), and total is a
@@ -255,6 +262,8 @@ moe_status_t moe_expert_gemm1_gathered(const moe_config_t* cfg, const void* xs,
   const size_t need = split_bytes(1, c, block_m);
   if (need && (!ws || ws_bytes < need || ((uintptr_t)ws & 255u))) return MOE_ERR_WORKSPACE;
   const int mp = (int)moe_max_padded_rows(c->T, c->k, c->E, block_m);
+  if (gemv_applies(*c, mp))
+    return launch_gemv1(*c, xs, true, W13, sorted_ids, expert_ids, npp, block_m, act, stream);
   return launch_gemm1_tc(*c, xs, W13, sorted_ids, expert_ids, npp, block_m, mp, act, ws,
                          ws_bytes, stream);
 }
@@ -270,6 +279,10 @@ moe_status_t moe_expert_gemm1(const moe_config_t* cfg, const void* x, const void
   if (!x || !W13 || !sorted_ids || !expert_ids || !npp || !act) return MOE_ERR_INVALID_ARG;
   const int mp = (int)moe_max_padded_rows(c->T, c->k, c->E, block_m);
   if (c->dtype == MOE_BF16) {
+    if (gemv_applies(*c, mp)) {  // small batch: the token rows are read in place
+      if (!aligned16(x) || !aligned16(W13) || !aligned16(act)) return MOE_ERR_INVALID_ARG;
+      return launch_gemv1(*c, x, false, W13, sorted_ids, expert_ids, npp, block_m, act, stream);
+    }
     const size_t need = gemm1_scratch_bytes(c, block_m);
     if (!ws || ws_bytes < need || ((uintptr_t)ws & 255u)) return MOE_ERR_WORKSPACE;
     st = moe_gather_rows(x, sorted_ids, npp, c->T, c->k, c->H, c->dtype, ws, stream);
@@ -307,6 +320,8 @@ moe_status_t moe_expert_gemm2(const moe_config_t* cfg, const void* act, const vo
     if (!aligned16(act) || !aligned16(W2) || !aligned16(y)) return MOE_ERR_INVALID_ARG;
     const size_t need = split_bytes(2, c, block_m);
     if (need && (!ws || ws_bytes < need || ((uintptr_t)ws & 255u))) return MOE_ERR_WORKSPACE;
+    if (gemv_applies(*c, mp))
+      return launch_gemv2(*c, act, W2, sorted_ids, expert_ids, npp, block_m, topk_w, y, stream);
     return launch_gemm2_tc(*c, act, W2, sorted_ids, expert_ids, npp, block_m, mp, topk_w, y,
                            ws, ws_bytes, stream);
   }
@@ -491,7 +506,13 @@ moe_status_t moe_forward(const moe_config_t* c, const void* x, const void* Wg, c
       (st = moe_apply_expert_map(eid, L.max_padded / L.block_m, c->expert_map, e.E, stream)) !=
           MOE_OK)
     return st;
-  if (e.dtype == MOE_BF16) {  // gather pass, then the tensor-core GEMM1 (split-K scratch)
+  if (e.dtype == MOE_BF16 && gemv_applies(e, (int)L.max_padded)) {
+    // a small batch: GEMM1 reads the token rows in place, no gather pass
+    if (!aligned16(x) || !aligned16(W13) || !aligned16(W2)) return MOE_ERR_INVALID_ARG;
+    if ((st = launch_gemv1(e, x, false, W13, sid, eid, npp, L.block_m, b + L.act, stream)) !=
+        MOE_OK)
+      return st;
+  } else if (e.dtype == MOE_BF16) {  // gather pass, then the tensor-core GEMM1 (split-K scratch)
     if ((st = moe_gather_rows(x, sid, npp, e.T, e.k, e.H, e.dtype, b + L.xs, stream)) != MOE_OK)
       return st;
     if ((st = moe_expert_gemm1_gathered(c, b + L.xs, W13, sid, eid, npp, L.block_m, b + L.act,

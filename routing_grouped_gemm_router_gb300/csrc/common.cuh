@@ -91,6 +91,16 @@ moe_status_t launch_gemm2_tc(const moe_config_t& c, const void* act, const void*
                              const int32_t* sid, const int32_t* eid, const int32_t* npp,
                              int block_m, int max_padded, const float* topk_w, void* y,
                              void* ws, size_t ws_bytes, cudaStream_t s);
+// Grouped GEMMs of small bf16 batches on CUDA cores (gemv.cu): whether they apply to a
+// layer, and the two GEMMs with the tensor-core kernels' inputs and outputs (GEMM1 reads
+// the routed rows gathered in padded order, or the token rows through sorted_ids).
+bool gemv_applies(const moe_config_t& c, int max_padded);
+moe_status_t launch_gemv1(const moe_config_t& c, const void* a, bool gathered, const void* W13,
+                          const int32_t* sid, const int32_t* eid, const int32_t* npp,
+                          int block_m, void* act, cudaStream_t s);
+moe_status_t launch_gemv2(const moe_config_t& c, const void* act, const void* W2,
+                          const int32_t* sid, const int32_t* eid, const int32_t* npp,
+                          int block_m, const float* topk_w, void* y, cudaStream_t s);
 moe_status_t launch_gather_rows(const void* x, const int32_t* sid, const int32_t* npp,
                                 int n_rows, int k, int row_bytes, void* xs, cudaStream_t s);
 moe_status_t launch_masked_table(const int32_t* counts, int E, int C, int B, int32_t* sid,

@@ -272,8 +272,13 @@ LAYER_CASES = [
     mi.Workload("bf16-skewed", T=600, H=256, I=256, E=32, k=4, dtype="bf16",
                 logit_bias_std=1.5, seed=15),
     mi.Workload("bf16-top1", T=37, H=128, I=192, E=8, k=1, dtype="bf16", seed=16),
-    # decode with split-K over ragged k-block ranges (GEMM1 5 k-blocks, GEMM2 7 in 4 splits)
-    mi.Workload("bf16-decode-splitk", T=2, H=320, I=448, E=16, k=4, dtype="bf16", seed=18),
+    # decode above the small-batch limit: tensor cores with split-K over ragged k-block
+    # ranges (GEMM1 5 k-blocks in 2 splits, GEMM2 7 in 4)
+    mi.Workload("bf16-decode-splitk", T=9, H=320, I=448, E=8, k=4, dtype="bf16", seed=18),
+    # small batches (CUDA-core grouped GEMMs): passes of two rows, the second case with K and
+    # N off the 256-element step
+    mi.Workload("bf16-decode-T2", T=2, H=2880, I=2880, E=32, k=4, dtype="bf16", seed=19),
+    mi.Workload("bf16-decode-T2-ragged", T=2, H=1000, I=776, E=4, k=2, dtype="bf16", seed=20),
     mi.Workload("f32-ragged", T=100, H=72, I=88, E=6, k=3, dtype="f32", seed=17),
 ]
 
@@ -303,13 +308,18 @@ def test_layer_parity(L, wl):
     assert_close(y[:n], yref, wl.dtype, "y")
 
 
-def test_separate_entry_points_match_forward(L):
-    wl = LAYER_CASES[1]
+ENTRY_CASES = [LAYER_CASES[1],
+               mi.Workload("bf16-small-entry", T=2, H=320, I=448, E=8, k=2, dtype="bf16", seed=22)]
+
+
+@pytest.mark.parametrize("wl", ENTRY_CASES, ids=[w.name for w in ENTRY_CASES])
+def test_separate_entry_points_match_forward(L, wl):
     inp = _to_dev(mi.make_layer(wl, "cpu"))
     layer = _layer(L, inp)
     out_fwd = layer(inp.x).clone()
     T, k, E, H, I = wl.T, wl.k, wl.E, wl.H, wl.I
     cfg = layer.config(T)
+    assert L.moe_small_batch(cfg) == (T <= 2)
     B = L.moe_block_m(cfg)
     mp = L.moe_max_padded_rows(T, k, E, B)
     lg = torch.empty(T, E, device=DEV)
@@ -351,16 +361,23 @@ def test_separate_entry_points_match_forward(L):
     assert torch.equal(y2, y)
 
 
-@pytest.mark.parametrize("dtype", ["bf16", "f32", "fp8"])
+@pytest.mark.parametrize("dtype", ["bf16", "f32", "fp8", "bf16-small", "fp8-small"])
 def test_tile_boundaries_and_sentinels(L, dtype):
     """Experts with 0, 1, B-1, B, B+1, 2B-1, 2B, 2B+1 rows; padding rows of act are never
     written (canary survives); every row of y is written (canary gone). "fp8": bf16
-    activations with FP8 E4M3 expert weights."""
+    activations with FP8 E4M3 expert weights. "-small": a few rows, which the small-batch
+    kernels take (bf16: experts with 0 and 2 rows; FP8: 0, 1, 2 and 5, the last in two
+    passes)."""
+    small = dtype.endswith("-small")
+    dtype = dtype.replace("-small", "")
     fp8 = dtype == "fp8"
     dtype = "bf16" if fp8 else dtype
     tdt = torch.bfloat16 if dtype == "bf16" else torch.float32
     B = 128 if dtype == "bf16" else 16
-    loads = [0, 1, B - 1, B, B + 1, 2 * B - 1, 2 * B, 2 * B + 1]
+    if small:
+        loads = [0, 1, 2, 5] if fp8 else [0, 2]
+    else:
+        loads = [0, 1, B - 1, B, B + 1, 2 * B - 1, 2 * B, 2 * B + 1]
     E, k = len(loads), 1
     T = sum(loads)
     H, I = 256, 192
@@ -377,6 +394,7 @@ def test_tile_boundaries_and_sentinels(L, dtype):
         sc = dict(w13_scale=s13.to(DEV), w2_scale=s2.to(DEV))
     xd, W13d, W2d, idsd, wd = (t.to(DEV) for t in (x, W13, W2, ids, w))
     cfg = L.make_config(T, H, I, E, k, L.MOE_BF16 if dtype == "bf16" else L.MOE_F32, **sc)
+    assert L.moe_small_batch(cfg) == small
     mp = L.moe_max_padded_rows(T, k, E, B)
     sid = torch.empty(mp, dtype=torch.int32, device=DEV)
     eid = torch.empty(mp // B, dtype=torch.int32, device=DEV)
@@ -408,6 +426,50 @@ def test_tile_boundaries_and_sentinels(L, dtype):
         w13o, w2o = weights_for_oracle(W13), weights_for_oracle(W2)
     ref = O.moe_loop(to_np(x), ids.numpy(), to_np(w), w13o, w2o)
     assert_close(to_np(out), ref, dtype)
+
+
+@pytest.mark.parametrize("fp8", [False, True], ids=["bf16", "fp8"])
+def test_small_batch_repeated_expert(L, fp8):
+    """One token that lists an expert twice (valid input for the align and grouped GEMM entry
+    points): that expert's tile holds more real rows than there are tokens, so the
+    small-batch kernels (one row a pass at T = 1) stream its weights in two passes; y and the
+    combined output equal the oracle's."""
+    T, k, E, H, I = 1, 3, 4, 320, 448
+    g = torch.Generator().manual_seed(23)
+    ids = torch.tensor([[2, 2, 0]], dtype=torch.int32)
+    w = torch.rand(T, k, generator=g) + 0.5
+    x = torch.randn(T, H, generator=g).bfloat16()
+    W13 = (torch.randn(E, 2 * I, H, generator=g) / H ** 0.5).bfloat16()
+    W2 = (torch.randn(E, H, I, generator=g) / I ** 0.5).bfloat16()
+    sc = {}
+    if fp8:
+        (W13, s13), (W2, s2) = mi.quantize_fp8_w13(W13), mi.quantize_fp8_blocks(W2)
+        sc = dict(w13_scale=s13.to(DEV), w2_scale=s2.to(DEV))
+        w13o = O.dequant_w13(W13.numpy(), s13.double().numpy())
+        w2o = O.dequant_blockwise(W2.numpy(), s2.double().numpy())
+    else:
+        w13o, w2o = weights_for_oracle(W13), weights_for_oracle(W2)
+    cfg = L.make_config(T, H, I, E, k, L.MOE_BF16, **sc)
+    assert L.moe_small_batch(cfg)
+    B = 128
+    mp = L.moe_max_padded_rows(T, k, E, B)
+    sid = torch.empty(mp, dtype=torch.int32, device=DEV)
+    eid = torch.empty(mp // B, dtype=torch.int32, device=DEV)
+    npp = torch.empty(1, dtype=torch.int32, device=DEV)
+    y = torch.full((T * k, H), float("nan"), dtype=torch.bfloat16, device=DEV)
+    out = torch.empty(T, H, dtype=torch.bfloat16, device=DEV)
+    ws = torch.empty(L.moe_grouped_swiglu_workspace_size(cfg, B), dtype=torch.uint8, device=DEV)
+    L.moe_align(ids.to(DEV), T, k, E, B, sid, eid, npp)
+    L.moe_grouped_swiglu(cfg, x.to(DEV), W13.to(DEV), W2.to(DEV), sid, eid, npp, B, w.to(DEV), y,
+                         ws, ws.numel())
+    L.moe_combine(y, T, k, H, L.MOE_BF16, out)
+    torch.cuda.synchronize()
+    xs = to_np(x)
+    yref = np.stack([O.expert_ffn(xs, OM._expert(w13o, e), OM._expert(w2o, e))[0] * w[0, j].item()
+                     for j, e in enumerate(ids[0].tolist())])
+    assert_close(to_np(y), yref, "bf16", "y")
+    ref = O.moe_loop(xs, ids.numpy(), to_np(w), w13o, w2o)
+    assert_close(to_np(out), ref, "bf16")
 
 
 def test_stalled_pipeline_times_out_with_a_status(L):
@@ -485,16 +547,17 @@ def test_cuda_graph_capture_and_replay(L):
 
 # --------------------------------------------------------------------- expert parallelism
 
-@pytest.mark.parametrize("dtype,variant", [("bf16", "half"), ("bf16", "perm"), ("f32", "half"),
-                                           ("fp8", "perm")])
-def test_expert_map(L, dtype, variant):
+@pytest.mark.parametrize("dtype,variant,T", [("bf16", "half", 300), ("bf16", "perm", 300),
+                                             ("f32", "half", 300), ("fp8", "perm", 300),
+                                             ("bf16", "half", 2), ("fp8", "perm", 6)])
+def test_expert_map(L, dtype, variant, T):
     """Odd experts held elsewhere (map -1), or local experts stored in permuted weight slots:
     the layer equals the oracle with the same expert_map; tiles carry the mapped labels.
     "fp8": the permuted slots hold FP8 codes whose block scales are permuted with them."""
     fp8 = dtype == "fp8"
     dtype = "bf16" if fp8 else dtype
     H, I = (256, 256) if dtype == "bf16" else (64, 96)
-    wl = mi.Workload("ep", T=300, H=H, I=I, E=16, k=4, dtype=dtype, seed=31)
+    wl = mi.Workload("ep", T=T, H=H, I=I, E=16, k=4, dtype=dtype, seed=31)
     inp = mi.make_layer(wl, "cpu")
     enforce_margins(inp)
     E = wl.E
@@ -535,12 +598,12 @@ def test_expert_map(L, dtype, variant):
 
 # --------------------------------------------------------------------- shared experts
 
-@pytest.mark.parametrize("dtype", ["bf16", "f32"])
-def test_shared_expert(L, dtype):
+@pytest.mark.parametrize("dtype,T", [("bf16", 200), ("f32", 200), ("bf16", 2)])
+def test_shared_expert(L, dtype, T):
     """DeepSeek-style layer with one shared expert (weight 1 on every token), grouped
     sigmoid routing with scale 2.5: equals the oracle with the shared slot appended."""
     H, I = (256, 256) if dtype == "bf16" else (64, 96)
-    wl = mi.Workload("shared", T=200, H=H, I=I, E=16, k=4, dtype=dtype,
+    wl = mi.Workload("shared", T=T, H=H, I=I, E=16, k=4, dtype=dtype,
                      mode=mi.ROUTE_SIGMOID_GROUPED, scale=2.5, n_group=4, topk_group=2,
                      select_bias_std=0.05, seed=41)
     inp = mi.make_layer(wl, "cpu")
@@ -623,8 +686,13 @@ FP8_CASES = [
                  select_bias_std=0.05, seed=62), 1, False),
     # scales that are not powers of two: the kernel rounds code * scale to bf16 once
     (mi.Workload("fp8-any-scale", T=200, H=256, I=256, E=16, k=4, dtype="bf16", seed=63), 0, True),
-    # decode: one token
+    # decode (small-batch kernels): one token; six tokens on four experts (rows of an expert
+    # in two passes) with K off the 512-code step and any scales; three tokens + a shared one
     (mi.Workload("fp8-decode", T=1, H=512, I=512, E=64, k=4, dtype="bf16", seed=64), 0, False),
+    (mi.Workload("fp8-decode-ragged", T=6, H=1040, I=784, E=4, k=2, dtype="bf16", seed=66), 0,
+     True),
+    (mi.Workload("fp8-decode-shared", T=3, H=2880, I=1024, E=16, k=4, dtype="bf16", seed=67), 1,
+     False),
 ]
 
 
@@ -668,14 +736,19 @@ def test_fp8_layer_parity(L, wl, n_shared, any_scale):
     assert_close(to_np(out), ref, "bf16")
     if not any_scale:
         # power-of-two scales: the dequantised weights are exact in bf16, so the result is
-        # the bf16 layer's on those weights, bit for bit
+        # the bf16 layer's on those weights: bit for bit on the tensor cores (codes scaled
+        # before the products); the small-batch kernels scale 16-code partial sums instead,
+        # which agrees to within rounding
         layer_bf = MoELayer(d(inp.Wg), d(torch.tensor(w13o).bfloat16()),
                             d(torch.tensor(w2o).bfloat16()), wl.k, wl.mode, wl.renormalize,
                             wl.scale, wl.n_group, wl.topk_group, d(inp.logit_bias),
                             d(inp.select_bias), n_shared=n_shared)
         out_bf = layer_bf(d(inp.x))
         torch.cuda.synchronize()
-        assert torch.equal(out_bf, out)
+        if L.moe_small_batch(layer.config(wl.T)):
+            assert_close(to_np(out), to_np(out_bf).astype(np.float64), "bf16")
+        else:
+            assert torch.equal(out_bf, out)
 
 
 def test_fp8_masked_layout(L):
