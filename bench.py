@@ -363,9 +363,11 @@ def run_ours(args, wl):
         L.moe_forward(cfg, inp.x, inp.Wg, W13s[c], W2s[c], out, ws, lay.total, sh)
 
     # kernels moe_forward enqueues: router GEMM + top-k, align (one kernel up to 4096 rows,
-    # else three), expert map, row gather (bf16 tensor-core path), GEMM1, GEMM2 (each + a
-    # counter-zeroing kernel when split along K) and the combine
-    launches_per_step = 2 + (1 if T * k <= 4096 else 3) + (1 if emap is not None else 0) + \
+    # else three; up to 8 tokens top-k and align are one kernel), expert map, row gather
+    # (bf16 tensor-core path), GEMM1, GEMM2 (each + a counter-zeroing kernel when split
+    # along K) and the combine
+    routing_launches = 2 if (T <= 8 and T * k <= 4096) else 2 + (1 if T * k <= 4096 else 3)
+    launches_per_step = routing_launches + (1 if emap is not None else 0) + \
         (1 if gathered else 0) + 3 + \
         (0 if small else sum(1 for g in (1, 2) if split_ws_bytes(L, cfg, B, g) > 0))
 

@@ -9,10 +9,12 @@
 //
 // Small problems (T*k <= kSmallRows) run all steps in one CTA. Larger ones split the rows
 // into chunks of kChunk: a per-chunk histogram kernel, a single-CTA scan kernel that turns
-// the chunk histograms into absolute write offsets, and a per-chunk scatter kernel.
+// the chunk histograms into absolute write offsets, and a per-chunk scatter kernel. Inside
+// the layer, a batch of at most kTopkWarps tokens also takes its top-k in that one CTA
+// (topk_align_small_kernel): the routing tail of a decode step is then a single launch.
 #include <mutex>
 
-#include "common.cuh"
+#include "route_dev.cuh"
 
 namespace moe {
 
@@ -142,13 +144,11 @@ __device__ void stable_scatter(const int32_t* ids, int r0, int r1, int E, int* r
 }
 
 // ---- single CTA: histogram, scan, fill, scatter --------------------------------------
-__global__ void __launch_bounds__(kAlignThreads) align_small_kernel(
-    const int32_t* __restrict__ ids, int n, int E, int B, int max_padded,
-    int32_t* __restrict__ sorted_ids, int32_t* __restrict__ expert_ids, int32_t* npp,
-    int32_t* counts) {
-  pdl_wait();
-  pdl_trigger();
-  extern __shared__ int sm[];
+__device__ __forceinline__ void align_small_body(const int32_t* __restrict__ ids, int n, int E,
+                                                 int B, int max_padded,
+                                                 int32_t* __restrict__ sorted_ids,
+                                                 int32_t* __restrict__ expert_ids, int32_t* npp,
+                                                 int32_t* counts, int* sm) {
   int* cnt = sm;                   // [E]
   int* start = cnt + E;            // [E]
   int* wcnt = start + E;           // [kAlignWarps * E]
@@ -165,6 +165,47 @@ __global__ void __launch_bounds__(kAlignThreads) align_small_kernel(
                 npp, counts);
   __syncthreads();
   stable_scatter(ids, 0, n, E, start, wcnt, sorted_ids);
+}
+
+__global__ void __launch_bounds__(kAlignThreads) align_small_kernel(
+    const int32_t* __restrict__ ids, int n, int E, int B, int max_padded,
+    int32_t* __restrict__ sorted_ids, int32_t* __restrict__ expert_ids, int32_t* npp,
+    int32_t* counts) {
+  pdl_wait();
+  pdl_trigger();
+  extern __shared__ int sm[];
+  align_small_body(ids, n, E, B, max_padded, sorted_ids, expert_ids, npp, counts, sm);
+}
+
+// ---- single CTA: top-k of at most kTopkWarps tokens, then the table ---------------------
+// Warp t routes token t with the same top-k as the separate top-k kernel (writing its ids
+// and weights), the CTA synchronises (its global writes are then visible to all of its
+// threads) and builds the table from those ids. Router experts: c.E; table experts and
+// slots: the effective E_eff, kk (shared experts included).
+struct TopkArgs {
+  const float* logits;
+  int Tn, E, k, mode, renorm;
+  float scale;
+  int n_group, topk_group;
+  const float* logit_bias;
+  const float* select_bias;
+  int n_shared;
+};
+
+__global__ void __launch_bounds__(kAlignThreads) topk_align_small_kernel(
+    const TopkArgs a, int32_t* __restrict__ ids, float* __restrict__ w, int n, int E_eff, int B,
+    int max_padded, int32_t* __restrict__ sorted_ids, int32_t* __restrict__ expert_ids,
+    int32_t* npp, int32_t* counts) {
+  pdl_wait();
+  pdl_trigger();
+  extern __shared__ int sm[];
+  const int warp = threadIdx.x / 32;
+  if (warp < a.Tn)
+    topk_token(a.logits, warp, a.E, a.k, a.mode, a.renorm, a.scale, a.n_group, a.topk_group,
+               a.logit_bias, a.select_bias, a.n_shared, ids, w,
+               reinterpret_cast<float*>(sm) + warp * 512);
+  __syncthreads();
+  align_small_body(ids, n, E_eff, B, max_padded, sorted_ids, expert_ids, npp, counts, sm);
 }
 
 // ---- multi CTA: per-chunk histogram ---------------------------------------------------
@@ -375,6 +416,26 @@ moe_status_t launch_align(const int32_t* ids, int T, int k, int E, int B, int ma
   if (!set_smem((const void*)align_scatter_kernel, smem_sc)) return MOE_ERR_CUDA;
   return launch_k(align_scatter_kernel, dim3(chunks), dim3(kAlignThreads), smem_sc, s, ids, cc, n,
                   E, sorted_ids);
+}
+
+bool topk_align_fits(const moe_config_t& c) {
+  const int64_t kk = c.k + c.n_shared;
+  return c.T <= kTopkWarps && c.T * kk <= kSmallRows;
+}
+
+moe_status_t launch_topk_align_small(const moe_config_t& c, const float* logits, int32_t* ids,
+                                     float* w, int B, int max_padded, int32_t* sorted_ids,
+                                     int32_t* expert_ids, int32_t* npp, int32_t* counts,
+                                     cudaStream_t s) {
+  if (!topk_align_fits(c)) return MOE_ERR_UNSUPPORTED;
+  const int kk = c.k + c.n_shared, E_eff = c.E + c.n_shared;
+  const size_t smem = std::max((size_t)(E_eff * (2 + kAlignWarps) + 33) * sizeof(int),
+                               (size_t)kTopkWarps * 512 * sizeof(float));
+  if (!set_smem((const void*)topk_align_small_kernel, smem)) return MOE_ERR_CUDA;
+  const TopkArgs a{logits, c.T, c.E, c.k, (int)c.mode, c.renormalize, c.scale, c.n_group,
+                   c.topk_group, c.logit_bias, c.select_bias, c.n_shared};
+  return launch_k(topk_align_small_kernel, dim3(1), dim3(kAlignThreads), smem, s, a, ids, w,
+                  c.T * kk, E_eff, B, max_padded, sorted_ids, expert_ids, npp, counts);
 }
 
 }  // namespace moe

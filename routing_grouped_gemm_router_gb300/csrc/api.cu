@@ -175,21 +175,24 @@ moe_status_t moe_workspace_size(const moe_config_t* c, size_t* bytes) {
   return st;
 }
 
+// The router GEMM of moe_route (logits only). Few tokens (decode): CUDA cores, router rows
+// spread over many SMs. Otherwise bf16 runs on the tensor cores (E <= 256 fits one MMA N),
+// fp32 on FFMA tiles.
+static moe_status_t router_logits(const moe_config_t* c, const void* x, const void* Wg,
+                                  float* logits, cudaStream_t stream) {
+  if (c->dtype == MOE_BF16 && (!aligned16(x) || !aligned16(Wg))) return MOE_ERR_INVALID_ARG;
+  if (c->T <= kFewTokens && aligned16(x) && aligned16(Wg))
+    return launch_router_few_tokens(*c, x, Wg, logits, stream);
+  if (c->dtype == MOE_BF16 && c->E <= 256) return launch_router_tc(*c, x, Wg, logits, stream);
+  return launch_router_simt(*c, x, Wg, logits, stream);
+}
+
 moe_status_t moe_route(const moe_config_t* c, const void* x, const void* Wg, float* logits,
                        int32_t* topk_ids, float* topk_w, cudaStream_t stream) {
   moe_status_t st = check_cfg(c);
   if (st != MOE_OK) return st;
   if (!x || !Wg || !logits || !topk_ids || !topk_w) return MOE_ERR_INVALID_ARG;
-  // Few tokens (decode): CUDA cores, router rows spread over many SMs. Otherwise bf16 runs
-  // on the tensor cores (E <= 256 fits one MMA N), fp32 on FFMA tiles.
-  if (c->dtype == MOE_BF16 && (!aligned16(x) || !aligned16(Wg))) return MOE_ERR_INVALID_ARG;
-  if (c->T <= kFewTokens && aligned16(x) && aligned16(Wg))
-    st = launch_router_few_tokens(*c, x, Wg, logits, stream);
-  else if (c->dtype == MOE_BF16 && c->E <= 256)
-    st = launch_router_tc(*c, x, Wg, logits, stream);
-  else
-    st = launch_router_simt(*c, x, Wg, logits, stream);
-  if (st != MOE_OK) return st;
+  if ((st = router_logits(c, x, Wg, logits, stream)) != MOE_OK) return st;
   return launch_topk(*c, logits, topk_ids, topk_w, stream);
 }
 
@@ -497,11 +500,20 @@ moe_status_t moe_forward(const moe_config_t* c, const void* x, const void* Wg, c
   int32_t* eid = (int32_t*)(b + L.expert_ids);
   int32_t* npp = (int32_t*)(b + L.num_post_padded);
   int32_t* counts = (int32_t*)(b + L.counts);
-  if ((st = moe_route(c, x, Wg, logits, ids, w, stream)) != MOE_OK) return st;
   const moe_config_t e = effective(c);  // shared experts as ordinary slots / experts
-  if ((st = moe_align(ids, e.T, e.k, e.E, L.block_m, sid, eid, npp, counts,
-                      b + L.align_scratch, L.act - L.align_scratch, stream)) != MOE_OK)
-    return st;
+  if (topk_align_fits(*c)) {
+    // decode-sized batch: router GEMM, then top-k and the align table in one CTA (the same
+    // device code as moe_route's top-k and moe_align's one-CTA table)
+    if ((st = router_logits(c, x, Wg, logits, stream)) != MOE_OK) return st;
+    if ((st = launch_topk_align_small(*c, logits, ids, w, L.block_m, L.max_padded, sid, eid,
+                                      npp, counts, stream)) != MOE_OK)
+      return st;
+  } else {
+    if ((st = moe_route(c, x, Wg, logits, ids, w, stream)) != MOE_OK) return st;
+    if ((st = moe_align(ids, e.T, e.k, e.E, L.block_m, sid, eid, npp, counts,
+                        b + L.align_scratch, L.act - L.align_scratch, stream)) != MOE_OK)
+      return st;
+  }
   if (c->expert_map &&
       (st = moe_apply_expert_map(eid, L.max_padded / L.block_m, c->expert_map, e.E, stream)) !=
           MOE_OK)

@@ -74,6 +74,13 @@ size_t align_scratch_bytes(int T, int k, int E, int block_m);
 moe_status_t launch_align(const int32_t* ids, int T, int k, int E, int block_m, int max_padded,
                           int32_t* sorted_ids, int32_t* expert_ids, int32_t* npp,
                           int32_t* counts, void* scratch, cudaStream_t s);
+// Top-k of a batch of at most 8 tokens and its align table in one single-CTA launch (the
+// routing tail of moe_forward for decode); topk_align_fits says whether cfg qualifies.
+bool topk_align_fits(const moe_config_t& c);
+moe_status_t launch_topk_align_small(const moe_config_t& c, const float* logits, int32_t* ids,
+                                     float* w, int B, int max_padded, int32_t* sorted_ids,
+                                     int32_t* expert_ids, int32_t* npp, int32_t* counts,
+                                     cudaStream_t s);
 moe_status_t launch_gemm1_simt(const moe_config_t& c, const float* x, const float* W13,
                                const int32_t* sid, const int32_t* eid, const int32_t* npp,
                                int block_m, int max_padded, float* act, cudaStream_t s);

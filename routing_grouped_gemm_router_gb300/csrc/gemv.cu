@@ -12,7 +12,7 @@
 // tensor-core kernels pay for 128-row tiles that such a stream does not need. Here one warp
 // owns two weight rows of one expert at a time (an item; GEMM1: the gate and up rows of
 // output column n; GEMM2: the rows of columns n and n+1): the 32 lanes stream them in
-// 16-byte pieces (512 contiguous bytes of a row per step, four or eight steps in flight) and
+// 16-byte pieces (512 contiguous bytes of a row per step, four to eight steps in flight) and
 // multiply every piece against the tile's real rows in fp32 registers (one, two or four rows
 // a pass, from the batch size); the lane sums meet in a shuffle reduction. The activations
 // (a few rows, read by every warp of the tile) come through L1; the weights bypass it. Each
@@ -203,10 +203,17 @@ __device__ __forceinline__ void item_pass(const Params& P, const uint8_t* w0, co
 
 // MODE 0: GEMM1 (item = output column n of act: gate row n, up row N + n).
 // MODE 1: GEMM2 (item = output columns n, n + 1 of y: W2 rows n, n + 1).
-// RMAX: real rows a pass takes (a tile holds at most T of them); one pass shape per kernel
-// keeps each within the 128 registers of two CTAs an SM.
+// RMAX: real rows a pass takes (a tile holds at most T of them); one pass shape per kernel.
+// Pieces in flight per row and CTAs per SM, measured at one and two tokens on GB300: bf16
+// passes of 1-2 rows run 3 CTAs an SM (80 registers; 6 or 4 pieces in flight), 5-6 % faster
+// than 2 CTAs with 8 pieces; FP8 codes (half the bytes a piece) keep 2 CTAs and 8 pieces.
 template <int MODE, bool FP8, int RMAX>
-__global__ void __launch_bounds__(kThreads, 2) gemv_kernel(const Params P) {
+constexpr int kMinCtas = (!FP8 && RMAX <= 2) ? 3 : 2;
+template <int MODE, bool FP8, int RMAX>
+constexpr int kPieces = RMAX == 1 ? (FP8 ? 8 : 6) : 4;
+
+template <int MODE, bool FP8, int RMAX>
+__global__ void __launch_bounds__(kThreads, (kMinCtas<MODE, FP8, RMAX>)) gemv_kernel(const Params P) {
   pdl_wait();
   pdl_trigger();
   __shared__ int2 rows_sh[kWarps][kTile];
@@ -251,7 +258,7 @@ __global__ void __launch_bounds__(kThreads, 2) gemv_kernel(const Params P) {
     }
     for (int rc = 0; rc < nvalid; rc += RMAX) {
       const int rv = min(RMAX, nvalid - rc);
-      item_pass<MODE, FP8, RMAX, RMAX == 1 ? 8 : 4>(P, w0, w1, s0, s1, rl + rc, rv, n);
+      item_pass<MODE, FP8, RMAX, kPieces<MODE, FP8, RMAX>>(P, w0, w1, s0, s1, rl + rc, rv, n);
     }
   }
 }

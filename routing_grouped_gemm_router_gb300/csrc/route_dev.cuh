@@ -1,6 +1,6 @@
-// route_dev.cuh — device building blocks of the router shared by the router kernels and the
-// fused small-batch front kernel (internal header). The arithmetic lives only here, so the
-// fused and the separate paths produce identical logits, ids and weights.
+// route_dev.cuh — device building blocks of the router shared by the router kernels, the
+// top-k kernel and the small-batch top-k + align kernel (internal header). The arithmetic
+// lives only here, so the combined and the separate paths produce identical ids and weights.
 #pragma once
 
 #include "common.cuh"
@@ -44,20 +44,49 @@ __device__ __forceinline__ void router_warp_logits(const T* __restrict__ x,
 #pragma unroll
   for (int t = 0; t < TB; ++t) acc[t] = 0.f;
   const T* w = Wg + (size_t)e * H;
+  if constexpr (TB == 1 && sizeof(T) == 2) {
+    // one bf16 token: eight 16-byte pieces of the router row (and of x) in flight a lane, all
+    // loaded before any is used, so a 2880-wide row takes two round trips
+    constexpr int kPieces = 8;
+    for (int h0 = lane * 8; h0 < H; h0 += 256 * kPieces) {
+      uint4 wq[kPieces], xq[kPieces];
+#pragma unroll
+      for (int j = 0; j < kPieces; ++j) {
+        const int h = h0 + j * 256;
+        if (h < H) {
+          wq[j] = *reinterpret_cast<const uint4*>(w + h);
+          xq[j] = *reinterpret_cast<const uint4*>(xr[0] + h);
+        }
+      }
+#pragma unroll
+      for (int j = 0; j < kPieces; ++j) {
+        if (h0 + j * 256 >= H) break;
+        const __nv_bfloat162* wp = reinterpret_cast<const __nv_bfloat162*>(&wq[j]);
+        const __nv_bfloat162* xp = reinterpret_cast<const __nv_bfloat162*>(&xq[j]);
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          const float2 wf = __bfloat1622float2(wp[i]), xf = __bfloat1622float2(xp[i]);
+          acc[0] = fmaf(xf.x, wf.x, acc[0]);
+          acc[0] = fmaf(xf.y, wf.y, acc[0]);
+        }
+      }
+    }
+  } else {
 #pragma unroll 2
-  for (int h = lane * 8; h < H; h += 256) {
-    float wv[8];
-    load8(w + h, wv);
+    for (int h = lane * 8; h < H; h += 256) {
+      float wv[8];
+      load8(w + h, wv);
 #pragma unroll
-    for (int tg = 0; tg < TB; tg += 8) {
-      constexpr int G = TB < 8 ? TB : 8;
-      float xv[G][8];
+      for (int tg = 0; tg < TB; tg += 8) {
+        constexpr int G = TB < 8 ? TB : 8;
+        float xv[G][8];
 #pragma unroll
-      for (int j = 0; j < G; ++j) load8(xr[tg + j] + h, xv[j]);
+        for (int j = 0; j < G; ++j) load8(xr[tg + j] + h, xv[j]);
 #pragma unroll
-      for (int j = 0; j < G; ++j)
+        for (int j = 0; j < G; ++j)
 #pragma unroll
-        for (int q = 0; q < 8; ++q) acc[tg + j] = fmaf(xv[j][q], wv[q], acc[tg + j]);
+          for (int q = 0; q < 8; ++q) acc[tg + j] = fmaf(xv[j][q], wv[q], acc[tg + j]);
+      }
     }
   }
 #pragma unroll
@@ -102,8 +131,7 @@ constexpr int kMaxPerLane = 16;  // E <= 512
 // slot j holds the j-th largest key; then the weights of the mode (softmax over E or over
 // the k kept logits; sigmoid scores renormalised and scaled), written to row t of ids / w,
 // after which the shared experts' slots follow. skey_w: this warp's 512 floats of shared memory (used
-// by the group scores of mode 1). Logits are read from L2 (ld.global.cg): in the fused
-// front kernel they were written by other CTAs of the cluster.
+// by the group scores of mode 1). Logits are read from L2 (ld.global.cg).
 __device__ __forceinline__ void topk_token(const float* __restrict__ logits, int t, int E, int k,
                                            int mode, int renorm, float scale, int n_group,
                                            int topk_group, const float* __restrict__ logit_bias,
