@@ -192,6 +192,7 @@ struct TopkArgs {
   int n_shared;
 };
 
+template <int MPL>
 __global__ void __launch_bounds__(kAlignThreads) topk_align_small_kernel(
     const TopkArgs a, int32_t* __restrict__ ids, float* __restrict__ w, int n, int E_eff, int B,
     int max_padded, int32_t* __restrict__ sorted_ids, int32_t* __restrict__ expert_ids,
@@ -201,7 +202,7 @@ __global__ void __launch_bounds__(kAlignThreads) topk_align_small_kernel(
   extern __shared__ int sm[];
   const int warp = threadIdx.x / 32;
   if (warp < a.Tn)
-    topk_token(a.logits, warp, a.E, a.k, a.mode, a.renorm, a.scale, a.n_group, a.topk_group,
+    topk_token<MPL>(a.logits, warp, a.E, a.k, a.mode, a.renorm, a.scale, a.n_group, a.topk_group,
                a.logit_bias, a.select_bias, a.n_shared, ids, w,
                reinterpret_cast<float*>(sm) + warp * 512);
   __syncthreads();
@@ -431,11 +432,18 @@ moe_status_t launch_topk_align_small(const moe_config_t& c, const float* logits,
   const int kk = c.k + c.n_shared, E_eff = c.E + c.n_shared;
   const size_t smem = std::max((size_t)(E_eff * (2 + kAlignWarps) + 33) * sizeof(int),
                                (size_t)kTopkWarps * 512 * sizeof(float));
-  if (!set_smem((const void*)topk_align_small_kernel, smem)) return MOE_ERR_CUDA;
   const TopkArgs a{logits, c.T, c.E, c.k, (int)c.mode, c.renormalize, c.scale, c.n_group,
                    c.topk_group, c.logit_bias, c.select_bias, c.n_shared};
-  return launch_k(topk_align_small_kernel, dim3(1), dim3(kAlignThreads), smem, s, a, ids, w,
-                  c.T * kk, E_eff, B, max_padded, sorted_ids, expert_ids, npp, counts);
+  auto run = [&](auto kern) {
+    if (!set_smem((const void*)kern, smem)) return MOE_ERR_CUDA;
+    return launch_k(kern, dim3(1), dim3(kAlignThreads), smem, s, a, ids, w, c.T * kk, E_eff, B,
+                    max_padded, sorted_ids, expert_ids, npp, counts);
+  };
+  switch (topk_per_lane(c.E)) {
+    case 4: return run(topk_align_small_kernel<4>);
+    case 8: return run(topk_align_small_kernel<8>);
+    default: return run(topk_align_small_kernel<kMaxPerLane>);
+  }
 }
 
 }  // namespace moe

@@ -119,6 +119,7 @@ moe_status_t launch_router_simt(const moe_config_t& c, const void* x, const void
 // warp-wide argmax (larger key wins, equal keys go to the lower id) over the experts not
 // taken yet, so slot j holds the j-th largest key.
 // ------------------------------------------------------------------------------------
+template <int MPL>
 __global__ void __launch_bounds__(kTopkWarps * 32) topk_kernel(
     const float* __restrict__ logits, int Tn, int E, int k, int mode, int renorm, float scale,
     int n_group, int topk_group, const float* __restrict__ logit_bias,
@@ -130,16 +131,26 @@ __global__ void __launch_bounds__(kTopkWarps * 32) topk_kernel(
   const int warp = threadIdx.x / 32;
   const int t = blockIdx.x * kTopkWarps + warp;
   if (t >= Tn) return;
-  topk_token(logits, t, E, k, mode, renorm, scale, n_group, topk_group, logit_bias, select_bias,
+  topk_token<MPL>(logits, t, E, k, mode, renorm, scale, n_group, topk_group, logit_bias, select_bias,
              n_shared, ids, w, skey[warp]);
+}
+
+template <int MPL>
+static moe_status_t launch_topk_mpl(const moe_config_t& c, const float* logits, int32_t* ids,
+                                    float* w, cudaStream_t s) {
+  int grid = ceil_div(c.T, kTopkWarps);
+  return launch_k(topk_kernel<MPL>, dim3(grid), dim3(kTopkWarps * 32), 0, s, logits, c.T, c.E,
+                  c.k, (int)c.mode, c.renormalize, c.scale, c.n_group, c.topk_group,
+                  c.logit_bias, c.select_bias, c.n_shared, ids, w);
 }
 
 moe_status_t launch_topk(const moe_config_t& c, const float* logits, int32_t* ids, float* w,
                          cudaStream_t s) {
-  int grid = ceil_div(c.T, kTopkWarps);
-  return launch_k(topk_kernel, dim3(grid), dim3(kTopkWarps * 32), 0, s, logits, c.T, c.E, c.k,
-                  (int)c.mode, c.renormalize, c.scale, c.n_group, c.topk_group, c.logit_bias,
-                  c.select_bias, c.n_shared, ids, w);
+  switch (topk_per_lane(c.E)) {
+    case 4: return launch_topk_mpl<4>(c, logits, ids, w, s);
+    case 8: return launch_topk_mpl<8>(c, logits, ids, w, s);
+    default: return launch_topk_mpl<kMaxPerLane>(c, logits, ids, w, s);
+  }
 }
 
 }  // namespace moe

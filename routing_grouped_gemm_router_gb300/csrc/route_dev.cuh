@@ -126,12 +126,17 @@ __device__ __forceinline__ float warp_sum(float v) {
 constexpr int kTopkWarps = 8;
 constexpr int kMaxPerLane = 16;  // E <= 512
 
-// Top-k of one token, one warp (lane l holds experts l + 32*i): k rounds of a warp-wide
+// Experts a lane holds for E router experts (4, 8 or 16): top-k loops run over that many.
+inline int topk_per_lane(int E) { return E <= 128 ? 4 : (E <= 256 ? 8 : kMaxPerLane); }
+
+// Top-k of one token, one warp (lane l holds experts l + 32*i, i < MPL, 32*MPL >= E): k
+// rounds of a warp-wide
 // argmax (larger key wins, equal keys go to the lower id) over the experts not taken yet, so
 // slot j holds the j-th largest key; then the weights of the mode (softmax over E or over
 // the k kept logits; sigmoid scores renormalised and scaled), written to row t of ids / w,
 // after which the shared experts' slots follow. skey_w: this warp's 512 floats of shared memory (used
 // by the group scores of mode 1). Logits are read from L2 (ld.global.cg).
+template <int MPL>
 __device__ __forceinline__ void topk_token(const float* __restrict__ logits, int t, int E, int k,
                                            int mode, int renorm, float scale, int n_group,
                                            int topk_group, const float* __restrict__ logit_bias,
@@ -142,9 +147,9 @@ __device__ __forceinline__ void topk_token(const float* __restrict__ logits, int
   const float* lrow = logits + (size_t)t * E;
   const float NEG = -INFINITY;
 
-  float key[kMaxPerLane], val[kMaxPerLane];
+  float key[MPL], val[MPL];
 #pragma unroll
-  for (int i = 0; i < kMaxPerLane; ++i) {
+  for (int i = 0; i < MPL; ++i) {
     int e = lane + 32 * i;
     key[i] = NEG;
     val[i] = 0.f;
@@ -165,7 +170,7 @@ __device__ __forceinline__ void topk_token(const float* __restrict__ logits, int
   if (mode == MOE_ROUTE_SIGMOID_GROUPED && n_group > 1) {
     // Group score = sum of the two largest biased keys of E/n_group consecutive experts.
 #pragma unroll
-    for (int i = 0; i < kMaxPerLane; ++i) {
+    for (int i = 0; i < MPL; ++i) {
       int e = lane + 32 * i;
       if (e < E) skey_w[e] = key[i];
     }
@@ -187,7 +192,7 @@ __device__ __forceinline__ void topk_token(const float* __restrict__ logits, int
       if (lane == best.e) gscore = NEG;
     }
 #pragma unroll
-    for (int i = 0; i < kMaxPerLane; ++i) {
+    for (int i = 0; i < MPL; ++i) {
       int e = lane + 32 * i;
       if (e < E && !((kept >> (e / per)) & 1u)) key[i] = NEG;
     }
@@ -196,14 +201,14 @@ __device__ __forceinline__ void topk_token(const float* __restrict__ logits, int
   // k rounds of warp argmax. Taken entries drop to a key below every real one.
   float my_sel_val = 0.f;   // lane j keeps the value of slot j
   int my_sel_id = 0;
-  bool taken[kMaxPerLane];
+  bool taken[MPL];
 #pragma unroll
-  for (int i = 0; i < kMaxPerLane; ++i) taken[i] = false;
+  for (int i = 0; i < MPL; ++i) taken[i] = false;
   for (int j = 0; j < k; ++j) {
     float bv = NEG;
     int be = 1 << 30;
 #pragma unroll
-    for (int i = 0; i < kMaxPerLane; ++i) {
+    for (int i = 0; i < MPL; ++i) {
       int e = lane + 32 * i;
       if (e < E && !taken[i] && (be == (1 << 30) || better(key[i], e, bv, be))) {
         bv = key[i];
@@ -215,7 +220,7 @@ __device__ __forceinline__ void topk_token(const float* __restrict__ logits, int
     if ((best.e & 31) == lane) {
       int i = best.e >> 5;
 #pragma unroll
-      for (int q = 0; q < kMaxPerLane; ++q)
+      for (int q = 0; q < MPL; ++q)
         if (q == i) { taken[q] = true; sel_val = val[q]; }
     }
     sel_val = __shfl_sync(0xffffffffu, sel_val, best.e & 31);
@@ -231,7 +236,7 @@ __device__ __forceinline__ void topk_token(const float* __restrict__ logits, int
     } else {
       float part = 0.f;
 #pragma unroll
-      for (int i = 0; i < kMaxPerLane; ++i) {
+      for (int i = 0; i < MPL; ++i) {
         int e = lane + 32 * i;
         if (e < E) part += expf(val[i] - top);
       }
