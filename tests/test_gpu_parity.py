@@ -279,6 +279,12 @@ LAYER_CASES = [
     # N off the 256-element step
     mi.Workload("bf16-decode-T2", T=2, H=2880, I=2880, E=32, k=4, dtype="bf16", seed=19),
     mi.Workload("bf16-decode-T2-ragged", T=2, H=1000, I=776, E=4, k=2, dtype="bf16", seed=20),
+    # decode batches route through the one-CTA top-k + align kernel at every expert count:
+    # 8 experts a lane (grouped sigmoid, E = 256) and 16 (E = 300)
+    mi.Workload("bf16-decode-grouped-E256", T=3, H=256, I=256, E=256, k=8, dtype="bf16",
+                mode=mi.ROUTE_SIGMOID_GROUPED, scale=2.5, n_group=8, topk_group=4,
+                select_bias_std=0.05, seed=24),
+    mi.Workload("bf16-decode-E300", T=2, H=128, I=128, E=300, k=4, dtype="bf16", seed=25),
     mi.Workload("f32-ragged", T=100, H=72, I=88, E=6, k=3, dtype="f32", seed=17),
 ]
 
