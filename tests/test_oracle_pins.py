@@ -311,6 +311,28 @@ def test_margins_flag_near_ties():
     assert O.selection_margins(l + np.array([[0, 1, 0, 0]]), 1)[0] > 1e-4
 
 
+def _grouped_margin_case(shift):
+    """Mode 1 by hand: logits 0 give s = 0.5 exactly, so the selection bias fixes every
+    biased score c. Four groups of two experts; group scores (sum of the two c) are 2.0,
+    1.5, 1.5 - 5e-5 - shift, 0.5; two groups are kept, so the gap between the second and
+    the third group score is 5e-5 + shift. The eligible experts' top three keys (1.2, 0.9,
+    0.8) are far apart, so that group gap alone decides the margin."""
+    c = np.array([1.2, 0.8, 0.9, 0.6, 0.8, 0.69995 - shift, 0.3, 0.2])
+    return np.zeros((1, 8)), c - 0.5
+
+
+def check_grouped_margins():
+    l, b = _grouped_margin_case(0.0)
+    near = O.selection_margins(l, 2, 1, n_group=4, topk_group=2, select_bias=b)[0]
+    l, b = _grouped_margin_case(1e-3)
+    far = O.selection_margins(l, 2, 1, n_group=4, topk_group=2, select_bias=b)[0]
+    return bool(abs(near - 5e-5) < 1e-12 and abs(far - (5e-5 + 1e-3)) < 1e-12)
+
+
+def test_margins_flag_near_tie_between_kept_and_dropped_group():
+    assert check_grouped_margins()
+
+
 # ----------------------------------------------------------------- expert parallelism
 
 def test_expert_map_remote_equals_zeroed_down_projection():
@@ -340,13 +362,17 @@ def test_expert_map_permuted_slots_are_invariant():
     assert np.array_equal(got, out)
 
 
+def check_apply_expert_map():
+    """A table labelled by hand: tiles of experts 0, 0, 1, 3, 2 and two unused tail tiles
+    (-1). Expert 0 sits in slot 2, expert 1 on another device, 2 in slot 0, 3 in slot 1, so
+    the relabelled table is written out below; the tail stays -1 (it is not expert -1)."""
+    eid = np.array([0, 0, 1, 3, 2, -1, -1])
+    emap = np.array([2, -1, 0, 1])
+    return O.apply_expert_map(eid, emap).tolist() == [2, 2, -1, 1, 0, -1, -1]
+
+
 def test_apply_expert_map_on_align_table():
-    ids = mi.random_topk_ids(40, 3, 7, seed=4).numpy()
-    sid, eid, total, _ = O.moe_align(ids, 4, 7, max_padded=O.max_padded_rows(40, 3, 7, 4))
-    emap = np.array([-1, 6, 5, -1, 3, 2, 1])
-    mapped = O.apply_expert_map(eid, emap)
-    for t, e in enumerate(eid):
-        assert mapped[t] == (-1 if e < 0 else emap[e])
+    assert check_apply_expert_map()
 
 
 # ----------------------------------------------------------------- shared expert
@@ -403,6 +429,24 @@ def test_e4m3_decoder_matches_torch_on_all_codes():
     assert np.array_equal(got[~both_nan], ref[~both_nan]) and np.isnan(got).sum() == 2
 
 
+def check_bf16_widening():
+    """Every one of the 65 536 bf16 codes widens to the value torch's bf16 -> fp32
+    conversion gives (NaN codes to NaN), plus a few codes fixed by the format: 0x3F80 = 1,
+    0xC000 = -2, 0x0001 = 2^-133 (smallest subnormal), 0x7F7F = largest finite."""
+    codes = np.arange(1 << 16, dtype=np.uint16)
+    ref = torch.from_numpy(codes.view(np.int16)).view(torch.bfloat16).float().double().numpy()
+    with np.errstate(invalid="ignore"):  # signalling-NaN codes
+        got = O.bf16_bits_to_f64(codes)
+    nan = np.isnan(ref)
+    known = O.bf16_bits_to_f64(np.array([0x3F80, 0xC000, 0x0001, 0x7F7F], dtype=np.uint16))
+    return bool(np.array_equal(np.isnan(got), nan) and np.array_equal(got[~nan], ref[~nan])
+                and known.tolist() == [1.0, -2.0, 2.0 ** -133, (2 - 2 ** -7) * 2.0 ** 127])
+
+
+def test_bf16_widening_matches_torch_on_all_codes():
+    assert check_bf16_widening()
+
+
 def test_dequant_blockwise_uses_the_right_block():
     codes = np.full((1, 200, 300), 0x38, dtype=np.uint8)   # all ones
     scales = np.arange(1 * 2 * 3, dtype=np.float64).reshape(1, 2, 3) + 1.0
@@ -442,6 +486,9 @@ def check_fp8():
 def _all_pins(golden_dir):
     return {
         "fp8": check_fp8(),
+        "bf16": check_bf16_widening(),
+        "grouped_margins": check_grouped_margins(),
+        "expert_map": check_apply_expert_map(),
         "tiny": check_tiny_loads(golden_dir),
         "loop_dense": check_loop_vs_dense_tiny(),
         "deepseek": check_deepseek_toy(golden_dir),
@@ -552,6 +599,30 @@ def _mut_w13_one_stacked_grid(codes13, scales13, block=128):
     return OM.dequant_blockwise(codes13, np.asarray(scales13).reshape(E, G * RB, KB), block)
 
 
+def _mut_bf16_shift15(bits):
+    u32 = bits.astype(np.uint16).astype(np.uint32) << np.uint32(15)
+    with np.errstate(invalid="ignore"):
+        return u32.view(np.float32).astype(np.float64)
+
+
+def _mut_margins_group_gap_off_by_one(logits, k, mode=0, n_group=1, topk_group=1,
+                                      select_bias=None):
+    """Group gap taken one place too late (between the next two dropped groups)."""
+    if mode == 0:
+        return _orig_margins(logits, k, mode, n_group, topk_group, select_bias)
+    return _orig_margins(logits, k, mode, n_group, min(topk_group + 1, n_group - 1),
+                         select_bias)
+
+
+_orig_margins = OM.selection_margins
+
+
+def _mut_map_tail_too(expert_ids, expert_map):
+    """The map also applied to the unused tail (-1 read as the map's last entry)."""
+    eid = np.asarray(expert_ids, dtype=np.int64)
+    return np.asarray(expert_map, dtype=np.int64)[eid]
+
+
 @pytest.mark.parametrize("name,attr,mut", [
     ("swap gate/up", "expert_ffn", _mut_swap_gate_up),
     ("no renormalisation", "route_softmax", _mut_no_renorm),
@@ -564,6 +635,9 @@ def _mut_w13_one_stacked_grid(codes13, scales13, block=128):
     ("E4M3 exponent bias 8", "e4m3_to_f64", _mut_e4m3_bias8),
     ("block scales indexed transposed", "dequant_blockwise", _mut_scale_grid_transposed),
     ("gate and up on one stacked scale grid", "dequant_w13", _mut_w13_one_stacked_grid),
+    ("bf16 widened with a shift of 15", "bf16_bits_to_f64", _mut_bf16_shift15),
+    ("group-score gap one place late", "selection_margins", _mut_margins_group_gap_off_by_one),
+    ("expert map applied to the unused tail", "apply_expert_map", _mut_map_tail_too),
 ])
 def test_planted_mistake_is_caught(monkeypatch, golden_dir, name, attr, mut):
     assert all(_all_pins(golden_dir).values())
