@@ -350,7 +350,7 @@ def run_ours(args, wl):
         if ev is not None:
             ev[5].record(stream)
         if emap is not None:
-            L.moe_combine_local(p["y"], p["topk_ids"], emap, T, k, H, cfg.dtype, out, sh)
+            L.moe_combine_local(p["y"], p["topk_ids"], emap, E, T, k, H, cfg.dtype, out, sh)
         else:
             L.moe_combine(p["y"], T, k, H, cfg.dtype, out, sh)
         if ev is not None:

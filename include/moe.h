@@ -44,7 +44,7 @@
 extern "C" {
 #endif
 
-#define MOE_ABI_VERSION 5
+#define MOE_ABI_VERSION 6
 
 typedef enum {
   MOE_OK = 0,
@@ -182,7 +182,10 @@ moe_status_t moe_align(const int32_t* topk_ids, int T, int k, int E, int block_m
  * the library (held by every GPU that loads it until the process exits), so it never
  * allocates. Limit: ceil(T*k / 1024) * E <= 65536 (e.g. T*k <= 524288 at E = 128); larger
  * problems return MOE_ERR_UNSUPPORTED without launching anything. The first call on a device
- * looks up the array's device address (make it before any stream capture). All calls on a
+ * looks up the array's device address (make it before any stream capture) and keeps it for
+ * the life of the process: after cudaDeviceReset, or any teardown of the device's primary
+ * context, the library's module reloads and that address is stale, so this entry point must
+ * not be called on that device again in the same process. All calls on a
  * device share the array and it keeps the last call's contents (nothing in it needs to start
  * at zero: every call overwrites the part it reads); calls that overlap on the GPU race. */
 moe_status_t moe_align_noalloc(const int32_t* topk_ids, int T, int k, int E, int block_m,
@@ -272,9 +275,11 @@ moe_status_t moe_combine(const void* y, int T, int k, int H, moe_dtype_t dtype, 
 
 /* Combine with expert parallelism: as moe_combine, but slot j of token t is skipped when
  * expert_map[topk_ids[t, j]] < 0 (its expert is on another device and its y row is not
- * written here). topk_ids [T, k] int32, expert_map [E] int32, both on the device. */
+ * written here). topk_ids [T, k] int32, expert_map [E] int32, both on the device. A slot
+ * whose id lies outside [0, E) is skipped too (its y row was never written: the align step
+ * drops such ids) and sets device status 1. */
 moe_status_t moe_combine_local(const void* y, const int32_t* topk_ids, const int32_t* expert_map,
-                               int T, int k, int H, moe_dtype_t dtype, void* out,
+                               int E, int T, int k, int H, moe_dtype_t dtype, void* out,
                                cudaStream_t stream);
 
 /* Fixed-capacity ("masked") expert layout for decode without an align step (page §7:
@@ -311,7 +316,7 @@ moe_status_t moe_forward(const moe_config_t* cfg, const void* x, const void* Wg,
 moe_status_t moe_selftest_wait_timeout(cudaStream_t stream);
 
 /* Diagnostic (synchronises the current device): returns the device status word (0 = no
- * fault seen; 1 = an expert id outside [0, E); 2 = a pipeline wait ran out of time; 3 = the
+ * fault seen; 1 = an expert id outside [0, E); 2 = a wait ran out of time; 3 = the
  * two CTAs of a tensor-core pair were given different tensor-memory columns) and
  * clears it when reset != 0. Not for use inside stream capture. */
 int moe_device_status(int reset);

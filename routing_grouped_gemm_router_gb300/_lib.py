@@ -78,7 +78,7 @@ def _load():
         "moe_masked_table": (ST, [P, I32, I32, I32, P, P, P, P]),
         "moe_masked_workspace_size": (ST, [CFG, I32, ctypes.POINTER(SZ)]),
         "moe_masked_forward": (ST, [CFG, P, P, I32, P, P, P, P, P, SZ, P]),
-        "moe_combine_local": (ST, [P, P, P, I32, I32, I32, I32, P, P]),
+        "moe_combine_local": (ST, [P, P, P, I32, I32, I32, I32, I32, P, P]),
         "moe_forward": (ST, [CFG, P, P, P, P, P, P, SZ, P]),
         "moe_device_status": (I32, [I32]),
         "moe_selftest_wait_timeout": (ST, [P]),
@@ -283,9 +283,10 @@ def moe_apply_expert_map(expert_ids, num_tiles, expert_map, E, stream=None):
         _ptr(expert_ids), num_tiles, _ptr(expert_map), E, _stream(stream)))
 
 
-def moe_combine_local(y, topk_ids, expert_map, T, k, H, dtype, out, stream=None):
+def moe_combine_local(y, topk_ids, expert_map, E, T, k, H, dtype, out, stream=None):
     _check("moe_combine_local", _lib.moe_combine_local(
-        _ptr(y), _ptr(topk_ids), _ptr(expert_map), T, k, H, dtype, _ptr(out), _stream(stream)))
+        _ptr(y), _ptr(topk_ids), _ptr(expert_map), E, T, k, H, dtype, _ptr(out),
+        _stream(stream)))
 
 
 def moe_masked_table(counts, E, capacity, block_m, sorted_ids, expert_ids, num_post_padded,

@@ -311,19 +311,15 @@ extern "C" moe_status_t moe_align_noalloc(const int32_t* topk_ids, int T, int k,
                                           int32_t* expert_ids, int32_t* num_post_padded,
                                           int32_t* counts, cudaStream_t stream) {
   using namespace moe;
-  if (!topk_ids || !sorted_ids || !expert_ids || !num_post_padded) return MOE_ERR_INVALID_ARG;
-  if (T < 1 || k < 1 || E < 1 || k > E || block_m < 1 || block_m > 4096)
-    return MOE_ERR_INVALID_ARG;
-  if (E > 512 || (int64_t)T * k > (int64_t)1 << 30) return MOE_ERR_UNSUPPORTED;
+  int mp = 0;
+  moe_status_t st = align_check_args(topk_ids, T, k, E, block_m, sorted_ids, expert_ids,
+                                     num_post_padded, &mp);
+  if (st != MOE_OK) return st;
   // Histograms beyond the fixed array: refuse rather than write past it.
   if (align_scratch_bytes(T, k, E, block_m) > sizeof(int32_t) * (size_t)kNoAllocScratchInts)
     return MOE_ERR_UNSUPPORTED;
-  moe_status_t st = MOE_OK;
   int32_t* scratch = noalloc_scratch(&st);
   if (!scratch) return st;
-  const int64_t n = (int64_t)T * k;
-  const int64_t bound = n + std::min<int64_t>(E, n) * (block_m - 1);
-  const int mp = (int)(bound / block_m * block_m);
   return launch_align(topk_ids, T, k, E, block_m, mp, sorted_ids, expert_ids, num_post_padded,
                       counts, scratch, stream);
 }

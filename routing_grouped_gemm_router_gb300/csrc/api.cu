@@ -86,6 +86,20 @@ static size_t gemm1_scratch_bytes(const moe_config_t* c, int block_m) {
   return gather_bytes(c, block_m) + split_bytes(1, c, block_m);
 }
 
+// Argument checks of the align entry points (moe_align, moe_align_noalloc) and the padded
+// table length they write.
+moe_status_t align_check_args(const int32_t* topk_ids, int T, int k, int E, int block_m,
+                              const int32_t* sorted_ids, const int32_t* expert_ids,
+                              const int32_t* num_post_padded, int* max_padded) {
+  if (!topk_ids || !sorted_ids || !expert_ids || !num_post_padded) return MOE_ERR_INVALID_ARG;
+  if (T < 1 || k < 1 || E < 1 || k > E || block_m < 1 || block_m > 4096)
+    return MOE_ERR_INVALID_ARG;
+  if (E > kMaxE) return MOE_ERR_UNSUPPORTED;
+  if ((int64_t)T * k > (int64_t)1 << 30) return MOE_ERR_UNSUPPORTED;
+  *max_padded = (int)moe_max_padded_rows(T, k, E, block_m);
+  return MOE_OK;
+}
+
 }  // namespace moe
 
 using namespace moe;
@@ -199,14 +213,12 @@ moe_status_t moe_route(const moe_config_t* c, const void* x, const void* Wg, flo
 moe_status_t moe_align(const int32_t* topk_ids, int T, int k, int E, int block_m,
                        int32_t* sorted_ids, int32_t* expert_ids, int32_t* num_post_padded,
                        int32_t* counts, void* ws, size_t ws_bytes, cudaStream_t stream) {
-  if (!topk_ids || !sorted_ids || !expert_ids || !num_post_padded) return MOE_ERR_INVALID_ARG;
-  if (T < 1 || k < 1 || E < 1 || k > E || block_m < 1 || block_m > 4096)
-    return MOE_ERR_INVALID_ARG;
-  if (E > kMaxE) return MOE_ERR_UNSUPPORTED;
-  if ((int64_t)T * k > (int64_t)1 << 30) return MOE_ERR_UNSUPPORTED;
+  int mp = 0;
+  const moe_status_t st = align_check_args(topk_ids, T, k, E, block_m, sorted_ids, expert_ids,
+                                           num_post_padded, &mp);
+  if (st != MOE_OK) return st;
   const size_t need = align_scratch_bytes(T, k, E, block_m);
   if (need && (!ws || ws_bytes < need)) return MOE_ERR_WORKSPACE;
-  const int mp = (int)moe_max_padded_rows(T, k, E, block_m);
   return launch_align(topk_ids, T, k, E, block_m, mp, sorted_ids, expert_ids, num_post_padded,
                       counts, ws, stream);
 }
@@ -381,13 +393,13 @@ moe_status_t moe_apply_expert_map(int32_t* expert_ids, int num_tiles, const int3
 }
 
 moe_status_t moe_combine_local(const void* y, const int32_t* topk_ids, const int32_t* expert_map,
-                               int T, int k, int H, moe_dtype_t dtype, void* out,
+                               int E, int T, int k, int H, moe_dtype_t dtype, void* out,
                                cudaStream_t stream) {
-  if (!y || !topk_ids || !expert_map || !out || T < 1 || k < 1 || H < 8 || H % 8)
+  if (!y || !topk_ids || !expert_map || !out || E < 1 || T < 1 || k < 1 || H < 8 || H % 8)
     return MOE_ERR_INVALID_ARG;
   if (dtype != MOE_F32 && dtype != MOE_BF16) return MOE_ERR_INVALID_ARG;
   if (!aligned16(y) || !aligned16(out)) return MOE_ERR_INVALID_ARG;
-  return launch_combine_local(y, topk_ids, expert_map, T, k, H, dtype, out, stream);
+  return launch_combine_local(y, topk_ids, expert_map, E, T, k, H, dtype, out, stream);
 }
 
 // ---- fixed-capacity (masked) layout ---------------------------------------------------
@@ -538,7 +550,8 @@ moe_status_t moe_forward(const moe_config_t* c, const void* x, const void* Wg, c
                              b + L.splitk, L.total - L.splitk, stream)) != MOE_OK)
     return st;
   if (c->expert_map)
-    return moe_combine_local(b + L.y, ids, c->expert_map, e.T, e.k, e.H, e.dtype, out, stream);
+    return moe_combine_local(b + L.y, ids, c->expert_map, e.E, e.T, e.k, e.H, e.dtype, out,
+                             stream);
   return moe_combine(b + L.y, e.T, e.k, e.H, e.dtype, out, stream);
 }
 
@@ -550,7 +563,8 @@ int moe_device_status(int reset) {
   const int a = align_status_read(reset);
   const int r = router_status_read(reset);
   const int g = grouped_status_read(reset);
-  return g ? g : (r ? r : a);
+  const int c = combine_status_read(reset);
+  return g ? g : (r ? r : (a ? a : c));
 }
 
 }  // extern "C"

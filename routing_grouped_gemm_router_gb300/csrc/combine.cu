@@ -9,6 +9,18 @@
 
 namespace moe {
 
+__device__ int g_combine_status;
+
+int combine_status_read(int reset) {
+  int v = 0;
+  cudaMemcpyFromSymbol(&v, g_combine_status, sizeof(int));
+  if (reset) {
+    int z = 0;
+    cudaMemcpyToSymbol(g_combine_status, &z, sizeof(int));
+  }
+  return v;
+}
+
 __global__ void __launch_bounds__(256) combine_bf16_kernel(const uint4* __restrict__ y,
                                                            uint4* __restrict__ out, int T,
                                                            int k, int vec_per_row) {
@@ -57,12 +69,13 @@ __global__ void __launch_bounds__(256) combine_f32_kernel(const float4* __restri
   }
 }
 
-// Expert parallelism: slots whose expert is on another device (map < 0) are skipped.
+// Expert parallelism: slots whose expert is on another device (map < 0) are skipped, and so
+// are slots with an id outside [0, E) (never aligned, so never computed; status 1).
 template <bool BF16>
 __global__ void __launch_bounds__(256) combine_local_kernel(const void* __restrict__ y,
                                                             const int32_t* __restrict__ ids,
                                                             const int32_t* __restrict__ map,
-                                                            void* __restrict__ out, int T,
+                                                            void* __restrict__ out, int E, int T,
                                                             int k, int vec_per_row) {
   pdl_wait();
   pdl_trigger();
@@ -72,7 +85,12 @@ __global__ void __launch_bounds__(256) combine_local_kernel(const void* __restri
     const int64_t t = i / vec_per_row, v = i % vec_per_row;
     float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
     for (int j = 0; j < k; ++j) {
-      if (map[ids[t * k + j]] < 0) continue;
+      const int e = ids[t * k + j];
+      if (e < 0 || e >= E) {
+        if (v == 0) atomicExch(&g_combine_status, kStatusBadExpert);
+        continue;
+      }
+      if (map[e] < 0) continue;
       if (BF16) {
         const uint4 q = __ldcs((const uint4*)y + (t * k + j) * vec_per_row + v);
         const __nv_bfloat162* h = reinterpret_cast<const __nv_bfloat162*>(&q);
@@ -99,17 +117,17 @@ __global__ void __launch_bounds__(256) combine_local_kernel(const void* __restri
   }
 }
 
-moe_status_t launch_combine_local(const void* y, const int32_t* ids, const int32_t* map, int T,
-                                  int k, int H, moe_dtype_t dt, void* out, cudaStream_t s) {
+moe_status_t launch_combine_local(const void* y, const int32_t* ids, const int32_t* map, int E,
+                                  int T, int k, int H, moe_dtype_t dt, void* out, cudaStream_t s) {
   const int vec = dt == MOE_BF16 ? H / 8 : H / 4;
   const int64_t total = (int64_t)T * vec;
   int blocks = (int)std::min<int64_t>(ceil_div64(total, 256), (int64_t)num_sms() * 8);
   if (blocks < 1) blocks = 1;
   if (dt == MOE_BF16)
-    return launch_k(combine_local_kernel<true>, dim3(blocks), dim3(256), 0, s, y, ids, map, out, T,
-                    k, vec);
-  return launch_k(combine_local_kernel<false>, dim3(blocks), dim3(256), 0, s, y, ids, map, out, T, k,
-                  vec);
+    return launch_k(combine_local_kernel<true>, dim3(blocks), dim3(256), 0, s, y, ids, map, out, E,
+                    T, k, vec);
+  return launch_k(combine_local_kernel<false>, dim3(blocks), dim3(256), 0, s, y, ids, map, out, E,
+                  T, k, vec);
 }
 
 moe_status_t launch_combine(const void* y, int T, int k, int H, moe_dtype_t dt, void* out,

@@ -71,6 +71,10 @@ moe_status_t launch_router_tc(const moe_config_t& c, const void* x, const void* 
 moe_status_t launch_topk(const moe_config_t& c, const float* logits, int32_t* ids, float* w,
                          cudaStream_t s);
 size_t align_scratch_bytes(int T, int k, int E, int block_m);
+// Argument checks shared by the align entry points; sets the padded table length.
+moe_status_t align_check_args(const int32_t* topk_ids, int T, int k, int E, int block_m,
+                              const int32_t* sorted_ids, const int32_t* expert_ids,
+                              const int32_t* num_post_padded, int* max_padded);
 moe_status_t launch_align(const int32_t* ids, int T, int k, int E, int block_m, int max_padded,
                           int32_t* sorted_ids, int32_t* expert_ids, int32_t* npp,
                           int32_t* counts, void* scratch, cudaStream_t s);
@@ -114,8 +118,8 @@ moe_status_t launch_masked_table(const int32_t* counts, int E, int C, int B, int
                                  int32_t* eid, int32_t* npp, float* ones, cudaStream_t s);
 moe_status_t launch_apply_expert_map(int32_t* eid, int tiles, const int32_t* map, int E,
                                      cudaStream_t s);
-moe_status_t launch_combine_local(const void* y, const int32_t* ids, const int32_t* map, int T,
-                                  int k, int H, moe_dtype_t dt, void* out, cudaStream_t s);
+moe_status_t launch_combine_local(const void* y, const int32_t* ids, const int32_t* map, int E,
+                                  int T, int k, int H, moe_dtype_t dt, void* out, cudaStream_t s);
 moe_status_t launch_combine(const void* y, int T, int k, int H, moe_dtype_t dt, void* out,
                             cudaStream_t s);
 
@@ -124,5 +128,6 @@ moe_status_t launch_selftest_wait(cudaStream_t s);
 int align_status_read(int reset);
 int router_status_read(int reset);
 int grouped_status_read(int reset);
+int combine_status_read(int reset);
 
 }  // namespace moe

@@ -602,6 +602,23 @@ def test_expert_map(L, dtype, variant, T):
         assert_close(to_np(out), plain, dtype)
 
 
+def test_combine_local_skips_and_flags_bad_expert_id(L):
+    """A slot whose id lies outside [0, E) is left out of the sum (its y row was never
+    computed) and sets device status 1; remote slots (map -1) are left out silently."""
+    T, k, E, H = 3, 2, 4, 16
+    ids = torch.tensor([[0, 1], [2, 9], [3, -1]], dtype=torch.int32, device=DEV)
+    emap = torch.tensor([0, -1, 2, 3], dtype=torch.int32, device=DEV)
+    y = (torch.arange(T * k * H, dtype=torch.float32, device=DEV).view(T * k, H) + 1.0)
+    out = torch.full((T, H), -7.0, dtype=torch.float32, device=DEV)
+    L.moe_device_status(True)
+    L.moe_combine_local(y, ids, emap, E, T, k, H, L.MOE_F32, out)
+    torch.cuda.synchronize()
+    assert L.moe_device_status(True) == 1
+    yc = y.cpu()
+    ref = torch.stack([yc[0], yc[2], yc[4]])  # slots (0,1), (1,1), (2,1) dropped
+    assert torch.equal(out.cpu(), ref)
+
+
 # --------------------------------------------------------------------- shared experts
 
 @pytest.mark.parametrize("dtype,T", [("bf16", 200), ("f32", 200), ("bf16", 2)])

@@ -67,9 +67,25 @@ def test_noalloc_matches_workspace_align_on_consecutive_calls(L):
         assert sorted(s[s < n].tolist()) == list(range(n))
 
 
+def test_noalloc_at_exactly_its_limit(L):
+    """The largest accepted problem fills the fixed array to the last int: 524288 rows are
+    512 chunks of 1024, times 128 experts = 65536 histogram entries."""
+    T, k, E, B = 65536, 8, 128, 128
+    assert L.moe_align_workspace_size(T, k, E, B) == 4 * 65536
+    ids = mi.random_topk_ids(T, k, E, seed=5, skew=0.5).to(DEV)
+    for _ in range(2):
+        ref = _with_workspace(L, ids, T, k, E, B)
+        got = _without_workspace(L, ids, T, k, E, B)
+        torch.cuda.synchronize()
+        for a, b in zip(got, ref):
+            assert torch.equal(a, b)
+    assert L.moe_device_status(True) == 0
+
+
 def test_noalloc_rejects_problems_beyond_its_fixed_scratch(L):
-    T, k, E, B = 1 << 17, 8, 128, 128          # 1024 chunks x 128 experts > 65536 ints
-    with pytest.raises(L.MoeError) as ei:
-        L.moe_align_noalloc(16, T, k, E, B, 16, 16, 16)
-    assert ei.value.status == L.MOE_ERR_UNSUPPORTED
+    # one chunk more than the array holds: 524296 rows are 513 chunks x 128 > 65536 ints
+    for T, k, E, B in [(65537, 8, 128, 128), (1 << 17, 8, 128, 128)]:
+        with pytest.raises(L.MoeError) as ei:
+            L.moe_align_noalloc(16, T, k, E, B, 16, 16, 16)
+        assert ei.value.status == L.MOE_ERR_UNSUPPORTED
     assert L.moe_device_status(True) == 0
