@@ -32,7 +32,7 @@ METRIC = "MoE layer TFLOPS (6*T*k*H*I/s) & % BF16 peak; decode weight GB/s vs HB
 DEFAULT_WORKLOAD = "mixtral-prefill"
 
 
-def parse():
+def parse(argv=None):
     p = argparse.ArgumentParser()
     p.add_argument("--gpus", type=int, default=1)
     p.add_argument("--steps", type=int, default=100)
@@ -59,7 +59,11 @@ def parse():
                    help="override T of the workload (smaller cases for profiling)")
     p.add_argument("--experts", type=int, default=0,
                    help="override E of the workload (smaller cases for profiling)")
-    return p.parse_args()
+    p.add_argument("--no-sweep", action="store_true",
+                   help="only the headline workload (the default run also measures the other "
+                        "prefill shapes, the decode sweep and FP8 decode)")
+    p.add_argument("--sweep-steps", type=int, default=10)
+    return p.parse_args(argv)
 
 
 def workload(name: str) -> mi.Workload:
@@ -220,6 +224,99 @@ def default_sample(wl):
             "deepseek-v3": 256}.get(wl.name.split("@")[0], wl.T)
 
 
+# ------------------------------------------------------------------------------ ranks
+
+class RankCtx:
+    """This process's place in the job: one replica of the layer per rank (no data-path
+    collective); the process group only serves the barriers around timed regions and the
+    max-over-ranks of the timings."""
+
+    def __init__(self, dist, rank, world, local):
+        self.dist, self.rank, self.world, self.local = dist, rank, world, local
+
+    def barrier(self):
+        if self.dist is not None:
+            self.dist.barrier()
+
+    def max(self, v, device="cpu"):
+        return max_over_ranks(self.dist, v, device)
+
+    def finish(self):
+        if self.dist is not None:
+            self.dist.barrier()
+            self.dist.destroy_process_group()
+
+
+class CudaTimer:
+    """Device time between two CUDA events recorded on the launching stream."""
+
+    def __init__(self, stream):
+        import torch
+        self.stream = stream
+        self.e0 = torch.cuda.Event(enable_timing=True)
+        self.e1 = torch.cuda.Event(enable_timing=True)
+
+    def start(self):
+        self.e0.record(self.stream)
+
+    def stop(self):
+        self.e1.record(self.stream)
+
+    def ms(self):
+        return self.e0.elapsed_time(self.e1)
+
+
+class WallTimer:
+    """Host wall time (the CPU-only plumbing tests)."""
+
+    def start(self):
+        self.t0 = time.perf_counter()
+
+    def stop(self):
+        self.t1 = time.perf_counter()
+
+    def ms(self):
+        return (self.t1 - self.t0) * 1e3
+
+
+def timed(ctx, steps, run, sync, timer, device="cpu"):
+    """Time `steps` calls of run(i): barrier and sync before, timer around the loop, sync and
+    barrier after; returns ms per step, the maximum over ranks."""
+    ctx.barrier()
+    sync()
+    timer.start()
+    for i in range(steps):
+        run(i)
+    timer.stop()
+    sync()
+    ctx.barrier()
+    return ctx.max(timer.ms() / steps, device)
+
+
+def workload_label(wl, shared=0, fp8=False, ep_half=False):
+    return (wl.name + ("+ep-half" if ep_half else "") + (f"+shared{shared}" if shared else "")
+            + ("+fp8" if fp8 else ""))
+
+
+def static_config(wl, world, shared=0, fp8=False, ep_half=False):
+    """The `config` of a bench line: the workload and how it is laid out and timed. Both arms
+    print exactly this (nothing measured goes in here)."""
+    wbytes = 1 if fp8 else (2 if wl.dtype == "bf16" else 4)
+    E = wl.E + shared
+    if is_decode(wl):
+        l2 = ("3 copies of the expert weights rotated between steps, so each step streams its "
+              "active experts from HBM (L2 126 MB)")
+    else:
+        l2 = f"inputs larger than L2 (expert weights {E * 3 * wl.H * wl.I * wbytes / 1e9:.2f} GB)"
+    return {"workload": workload_label(wl, shared, fp8, ep_half),
+            "expert_weights": "fp8-e4m3, fp32 scale per 128x128 block" if fp8 else
+                              ("bf16" if wl.dtype == "bf16" else "f32"),
+            "T": wl.T, "H": wl.H, "I": wl.I, "E": wl.E, "k": wl.k, "n_shared": shared,
+            "mode": "sigmoid-grouped" if wl.mode else "softmax",
+            "global_batch": wl.T * world, "parallelism": f"replicas x{world}", "l2": l2,
+            "block_m": 128 if wl.dtype == "bf16" else 16}
+
+
 # ------------------------------------------------------------------------------ arms
 
 def run_reference(args, wl):
@@ -247,7 +344,7 @@ def run_reference(args, wl):
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": secs / args.steps * 1e3,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
             "data": "synthetic", "impl": "reference",
-            "config": {"workload": wl.name, "T": wl.T, "H": wl.H, "I": wl.I, "E": wl.E, "k": wl.k},
+            "config": static_config(wl, args.gpus),
             "cpu_baseline": {"value": val, "unit": "TFLOPS", "cores": threads, "kind": "oracle",
                              "sample": f"first {n} of {wl.T} tokens per step, float64 oracle "
                                        "(router + per-expert loop)"},
@@ -258,30 +355,34 @@ def run_reference(args, wl):
         dist.destroy_process_group()
 
 
-def run_ours(args, wl):
+def measure_layer(args, wl, ctx, seed, steps, warmup, shared=0, fp8=False, ep_half=False,
+                  e2e=True, cpu_baseline=False):
+    """One layer configuration on this rank's GPU: CUDA-graph replays of moe_forward (the
+    device-timed steps), the same stages launched eagerly with events between them, and
+    (e2e) the public API with host copies of the tokens and the output. Times are maxima
+    over ranks. Returns a dict of raw measurements (summarize() turns it into line fields)."""
     import torch
-    dist, rank, world, local = dist_setup(args.gpus)
-    dev = torch.device("cuda", local)
+    dev = torch.device("cuda", ctx.local)
     torch.cuda.set_device(dev)
     from routing_grouped_gemm_router_gb300 import _lib as L  # fails loudly if not built
     from routing_grouped_gemm_router_gb300.layer import MoELayer
 
-    inp = mi.make_layer(wl, dev, seed=wl.seed + 1000 * rank)
-    if args.shared:  # shared experts' weights follow the routed experts'
+    inp = mi.make_layer(wl, dev, seed=seed)
+    if shared:  # shared experts' weights follow the routed experts'
         g = torch.Generator(device=dev)
         g.manual_seed(wl.seed + 77)
-        inp.W13 = torch.cat([inp.W13, (torch.randn(args.shared, 2 * wl.I, wl.H, generator=g,
+        inp.W13 = torch.cat([inp.W13, (torch.randn(shared, 2 * wl.I, wl.H, generator=g,
                                                    device=dev) / wl.H ** 0.5).to(inp.W13.dtype)])
-        inp.W2 = torch.cat([inp.W2, (torch.randn(args.shared, wl.H, wl.I, generator=g,
+        inp.W2 = torch.cat([inp.W2, (torch.randn(shared, wl.H, wl.I, generator=g,
                                                  device=dev) / wl.I ** 0.5).to(inp.W2.dtype)])
     sc13 = sc2 = None
-    if args.fp8:  # codes + block scales replace the bf16 expert weights
+    if fp8:  # codes + block scales replace the bf16 expert weights
         inp.W13, sc13 = mi.quantize_fp8_w13(inp.W13)
         inp.W2, sc2 = mi.quantize_fp8_blocks(inp.W2)
         torch.cuda.empty_cache()
     emap = None
-    if args.ep_half:
-        emap = torch.tensor([e if e % 2 == 0 else -1 for e in range(wl.E + args.shared)],
+    if ep_half:
+        emap = torch.tensor([e if e % 2 == 0 else -1 for e in range(wl.E + shared)],
                             dtype=torch.int32, device=dev)
     # Decode streams only the active experts' weights (gpt-oss T=1: 0.2 GB, not much more
     # than the 126 MB L2): successive steps rotate over three copies of the expert weights so
@@ -291,12 +392,12 @@ def run_ours(args, wl):
     W2s = [inp.W2] + [inp.W2.clone() for _ in range(n_copies - 1)]
     layers = [MoELayer(inp.Wg, W13s[c], W2s[c], wl.k, wl.mode, wl.renormalize, wl.scale,
                        wl.n_group, wl.topk_group, inp.logit_bias, inp.select_bias, emap,
-                       n_shared=args.shared, w13_scale=sc13, w2_scale=sc2)
+                       n_shared=shared, w13_scale=sc13, w2_scale=sc2)
               for c in range(n_copies)]
     layer = layers[0]
-    wbytes = 1 if args.fp8 else inp.x.element_size()  # bytes per expert weight
+    wbytes = 1 if fp8 else inp.x.element_size()  # bytes per expert weight
     # the align step, the grouped GEMMs and the combine see shared experts as ordinary ones
-    T, k, E, H, I = wl.T, wl.k + args.shared, wl.E + args.shared, wl.H, wl.I
+    T, k, E, H, I = wl.T, wl.k + shared, wl.E + shared, wl.H, wl.I
     cfg = layer.config(T)
     ws, lay = layer.workspace(T)
     B = lay.block_m
@@ -356,8 +457,6 @@ def run_ours(args, wl):
         if ev is not None:
             ev[6].record(stream)
 
-    # router GEMM + top-k, align (one kernel up to 4096 rows, else three), row gather + GEMM1
-    # (bf16), GEMM2, combine
     def forward(sh=sh, c=0):
         # the timed step: the public entry point, moe_forward, with the workspace above
         L.moe_forward(cfg, inp.x, inp.Wg, W13s[c], W2s[c], out, ws, lay.total, sh)
@@ -371,7 +470,7 @@ def run_ours(args, wl):
         (1 if gathered else 0) + 3 + \
         (0 if small else sum(1 for g in (1, 2) if split_ws_bytes(L, cfg, B, g) > 0))
 
-    for _ in range(max(3, args.warmup)):
+    for _ in range(max(3, warmup)):
         step()
         forward()
     torch.cuda.synchronize()
@@ -398,139 +497,182 @@ def run_ours(args, wl):
             for g in graphs:
                 g.replay()
         torch.cuda.synchronize()
-    graph = graphs[0] if graphs else None
 
-    # ---- device-timed steps (inputs resident in HBM; expert weights larger than L2)
-    sampler = ClockSampler(local)
-    sampler.start()
-    time.sleep(0.3)
-    if dist is not None:
-        dist.barrier()
-    torch.cuda.synchronize()
-    t_start = torch.cuda.Event(enable_timing=True)
-    t_end = torch.cuda.Event(enable_timing=True)
-    t_start.record(stream)
-    for i in range(args.steps):
-        if graph is not None:
+    def run_step(i):
+        if graphs:
             graphs[i % n_copies].replay()
         else:
             forward(c=i % n_copies)
-    t_end.record(stream)
-    torch.cuda.synchronize()
-    if dist is not None:
-        dist.barrier()
-    ms = max_over_ranks(dist, t_start.elapsed_time(t_end) / args.steps, dev)
+
+    # ---- device-timed steps (inputs resident in HBM; expert weights larger than L2)
+    sampler = ClockSampler(ctx.local)
+    sampler.start()
+    time.sleep(0.3)
+    ms = timed(ctx, steps, run_step, torch.cuda.synchronize, CudaTimer(stream), dev)
     # per-stage device times: the same steps launched eagerly with CUDA events between stages
-    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(7)] for _ in range(args.steps)]
-    for i in range(args.steps):
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(7)] for _ in range(steps)]
+    for i in range(steps):
         step(evs[i], c=i % n_copies)
     torch.cuda.synchronize()
     clocks = sampler.stop()
     stage = {n: statistics.mean(e[i].elapsed_time(e[i + 1]) for e in evs)
              for i, n in enumerate(("route", "align", "gather", "gemm1", "gemm2", "combine"))}
+    res = {"ms": ms, "stage": stage, "clocks": clocks, "npp": npp, "active": active,
+           "local_rows": local_rows, "small": bool(small), "n_copies": n_copies,
+           "wbytes": wbytes, "launches_per_step": launches_per_step, "graph": bool(graphs),
+           "T": T, "k": k, "E": E, "H": H, "I": I, "block_m": B}
+    del graphs
 
     # ---- end to end through the public API: H2D of x, moe_forward, D2H of out
-    x_host = inp.x.cpu().pin_memory()
-    out_host = torch.empty(T, H, dtype=inp.x.dtype).pin_memory()
-    x_dev = torch.empty_like(inp.x)
-    for i in range(3):
-        x_dev.copy_(x_host, non_blocking=True)
-        layers[i % n_copies](x_dev, out)
-        out_host.copy_(out, non_blocking=True)
-    torch.cuda.synchronize()
-    if dist is not None:
-        dist.barrier()
-    e0 = torch.cuda.Event(enable_timing=True)
-    e1 = torch.cuda.Event(enable_timing=True)
-    e0.record(stream)
-    for i in range(args.steps):
-        x_dev.copy_(x_host, non_blocking=True)
-        layers[i % n_copies](x_dev, out)
-        out_host.copy_(out, non_blocking=True)
-    e1.record(stream)
-    torch.cuda.synchronize()
-    e2e_ms = max_over_ranks(dist, e0.elapsed_time(e1) / args.steps, dev)
-    bytes_io = T * H * inp.x.element_size()
+    if e2e:
+        x_host = inp.x.cpu().pin_memory()
+        out_host = torch.empty(T, H, dtype=inp.x.dtype).pin_memory()
+        x_dev = torch.empty_like(inp.x)
 
-    flops = 6 * local_rows * H * I  # useful rows (all T*k rows unless experts are remote)
-    value = flops * world / (ms * 1e-3) / 1e12
-    e2e_val = flops * world / (e2e_ms * 1e-3) / 1e12
-    hbm, bf16_burst, bf16_sus, peak_src = peaks()
-    # The bound follows the layer's intensity, useful FLOPs per byte of active expert weights
-    # (T*k/A for bf16), against the ridge of the measured peaks: decode and the
-    # DeepSeek-V3-shaped layer (128 FLOP/B) stream weights; Mixtral and Qwen3 are compute.
-    intensity = flops / max(1, active * 3 * H * I * wbytes)
-    hbm_bound = is_decode(wl) or intensity < bf16_sus * 1e12 / (hbm * 1e9)
-    if hbm_bound:
-        # GEMM1 streams the gate/up weights of every active expert
-        w_bytes = active * 2 * H * I * wbytes
-        roof = {"bound": "hbm", "achieved": w_bytes / (stage["gemm1"] * 1e-3) / 1e9,
-                "peak": hbm, "unit": "GB/s",
-                "kernel": "gemm1 (gate/up grouped GEMV, small batch)" if small else
-                          "gemm1 (gate/up grouped GEMM)",
-                "algorithmic_bytes_per_launch": w_bytes,
-                "peak_kind": f"{peak_src} HBM copy bandwidth"}
-    else:
-        g1_flops = 4 * local_rows * H * I
-        roof = {"bound": "tensor", "achieved": g1_flops / (stage["gemm1"] * 1e-3) / 1e12,
-                "peak": bf16_sus, "unit": "TFLOP/s",
-                "kernel": "gemm1 (gate/up grouped GEMM + SwiGLU)",
-                "algorithmic_flops_per_launch": g1_flops,
-                "peak_kind": f"{peak_src} bf16 sustained (kernel timed inside a long step loop)"}
-    roof["frac"] = roof["achieved"] / roof["peak"]
-    kern = "gemv1" if small else "gemm1"
-    src = os.path.join(ROOT, "routing_grouped_gemm_router_gb300", "csrc",
-                       "gemv.cu" if small else "gemm_tc2.cu")
-    roof["traffic"] = profile_traffic(kern + ("_fp8" if args.fp8 else ""), wl.name, active, src)
+        def e2e_step(i):
+            x_dev.copy_(x_host, non_blocking=True)
+            layers[i % n_copies](x_dev, out)
+            out_host.copy_(out, non_blocking=True)
 
-    line = {"metric": METRIC, "value": value, "unit": "TFLOPS", "n_gpus": world,
-            "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
-            "timing": ("CUDA-graph replays of moe_forward" if graph is not None else
-                       "eager moe_forward calls") + "; stages_ms: the separate entry points, eager",
-            "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
-            "dtype": "bf16" if wl.dtype == "bf16" else "f32",
-            "data": "synthetic (seeded N(0,1) tokens, N(0,1/fan_in) weights, random init)",
-            "config": {"workload": wl.name + ("+ep-half" if emap is not None else "")
-                       + (f"+shared{args.shared}" if args.shared else "")
-                       + ("+fp8" if args.fp8 else ""),
-                       "expert_weights": "fp8-e4m3, fp32 scale per 128x128 block" if args.fp8
-                       else ("bf16" if wl.dtype == "bf16" else "f32"),
-                       "T": T, "H": H, "I": I, "E": wl.E, "k": wl.k, "n_shared": args.shared,
-                       "mode": "sigmoid-grouped" if wl.mode else "softmax",
-                       "global_batch": T * world, "parallelism": f"replicas x{world}",
-                       "l2": (f"{n_copies} copies of the expert weights rotated between "
-                              f"steps ({active * 3 * H * I * wbytes / 1e6:.0f} MB of active "
-                              "weights per step; L2 126 MB)") if n_copies > 1 else
-                             ("inputs larger than L2 (expert weights "
-                              f"{E * 3 * H * I * wbytes / 1e9:.2f} GB)"),
-                       "block_m": B, "num_post_padded": npp, "active_experts": active},
-            "stages_ms": {n: round(v, 5) for n, v in stage.items()},
-            "roofline": roof,
-            "e2e": {"value": e2e_val, "unit": "TFLOPS", "h2d_bytes_per_step": bytes_io,
-                    "d2h_bytes_per_step": bytes_io, "ms_per_step": e2e_ms},
-            "gpu_launches": launches_per_step * args.steps,
-            "clocks": clocks}
-    line["intensity_flop_per_weight_byte"] = intensity
-    if hbm_bound:
-        line["weight_gbs"] = active * 3 * H * I * wbytes / (ms * 1e-3) / 1e9
-        line["weight_gbs_frac_of_hbm"] = line["weight_gbs"] / hbm
-    if not is_decode(wl):
-        line["frac_of_bf16_peak"] = value / bf16_sus
+        for i in range(3):
+            e2e_step(i)
+        torch.cuda.synchronize()
+        res["e2e_ms"] = timed(ctx, steps, e2e_step, torch.cuda.synchronize, CudaTimer(stream),
+                              dev)
+        res["io_bytes"] = T * H * inp.x.element_size()
 
-    if rank == 0 and world == 1 and not args.no_cpu_baseline and not args.fp8:
+    if cpu_baseline:
         del layer, layers, W13s, W2s
         x, Wg, W13, W2, lb, sb = host_copies(inp)
         n = args.cpu_sample_tokens or default_sample(wl)
         dt, n, threads = time_oracle(wl, x, Wg, W13, W2, lb, sb, n)
-        line["cpu_baseline"] = {"value": 6 * n * k * H * I / dt / 1e12, "unit": "TFLOPS",
-                                "cores": threads, "kind": "oracle",
-                                "sample": f"first {n} of {T} tokens, one pass of the float64 "
-                                          f"oracle (router + per-expert loop), {dt:.1f} s"}
+        res["cpu_baseline"] = {"value": 6 * n * k * H * I / dt / 1e12, "unit": "TFLOPS",
+                               "cores": threads, "kind": "oracle",
+                               "sample": f"first {n} of {T} tokens, one pass of the float64 "
+                                         f"oracle (router + per-expert loop), {dt:.1f} s"}
+    return res
+
+
+def summarize(wl, m, world, fp8=False):
+    """Line fields of one measured configuration: the metric (useful TFLOPS, summed over
+    ranks), active-expert weight GB/s for weight-bound layers, and the roofline of GEMM1,
+    the dominant kernel, against the measured peaks."""
+    H, I = m["H"], m["I"]
+    flops = 6 * m["local_rows"] * H * I  # useful rows (all T*k rows unless experts are remote)
+    value = flops * world / (m["ms"] * 1e-3) / 1e12
+    hbm, bf16_burst, bf16_sus, peak_src = peaks()
+    wbytes, active = m["wbytes"], m["active"]
+    # The bound follows the layer's intensity, useful FLOPs per byte of active expert weights
+    # (T*k/A for bf16), against the ridge of the measured peaks: decode and the
+    # DeepSeek-V3-shaped layer (128 FLOP/B) stream weights; Mixtral and Qwen3 are compute.
+    intensity = flops / max(1, active * 3 * H * I * wbytes)
+    hbm_bound = is_decode(wl) or intensity < bf16_burst * 1e12 / (hbm * 1e9)
+    g1_ms = m["stage"]["gemm1"]
+    # GEMM1 is timed alone (eager, CUDA events around it), tens of milliseconds of work at a
+    # time: the burst peaks are its denominators.
+    if hbm_bound:
+        w_bytes = active * 2 * H * I * wbytes   # gate/up weights of every active expert
+        roof = {"bound": "hbm", "achieved": w_bytes / (g1_ms * 1e-3) / 1e9, "peak": hbm,
+                "unit": "GB/s",
+                "kernel": "gemm1 (gate/up grouped GEMV, small batch)" if m["small"] else
+                          "gemm1 (gate/up grouped GEMM)",
+                "algorithmic_bytes_per_launch": w_bytes,
+                "peak_kind": f"{peak_src} HBM copy bandwidth"}
+    else:
+        g1_flops = 4 * m["local_rows"] * H * I
+        roof = {"bound": "tensor", "achieved": g1_flops / (g1_ms * 1e-3) / 1e12,
+                "peak": bf16_burst, "unit": "TFLOP/s",
+                "kernel": "gemm1 (gate/up grouped GEMM + SwiGLU)",
+                "algorithmic_flops_per_launch": g1_flops,
+                "peak_kind": f"{peak_src} bf16 burst (GEMM1 timed alone, CUDA events)"}
+    roof["frac"] = roof["achieved"] / roof["peak"]
+    kern = "gemv1" if m["small"] else "gemm1"
+    src = os.path.join(ROOT, "routing_grouped_gemm_router_gb300", "csrc",
+                       "gemv.cu" if m["small"] else "gemm_tc2.cu")
+    roof["traffic"] = profile_traffic(kern + ("_fp8" if fp8 else ""), wl.name, active, src)
+    f = {"value": value, "ms_per_step": m["ms"], "roofline": roof,
+         "intensity_flop_per_weight_byte": intensity,
+         "routing": {"num_post_padded": m["npp"], "active_experts": active,
+                     "rows": m["local_rows"]}}
+    if hbm_bound:
+        f["weight_gbs"] = active * 3 * H * I * wbytes * world / (m["ms"] * 1e-3) / 1e9
+        f["weight_gbs_frac_of_hbm"] = f["weight_gbs"] / (hbm * world)
+    if not is_decode(wl):
+        f["frac_of_bf16_peak"] = value / (bf16_burst * world)
+        f["frac_of_bf16_peak_kind"] = "layer TFLOPS / measured bf16 burst (CUDA-graph replays)"
+    return f
+
+
+# The rest of the metric, measured in the default run next to the headline (one GPU): the
+# other prefill shapes, the decode sweep and FP8 expert weights at decode.
+SWEEP = [("qwen3-skewed", False), ("deepseek-v3", False),
+         ("gpt-oss-decode@T=1", False), ("gpt-oss-decode@T=8", False),
+         ("gpt-oss-decode@T=32", False), ("gpt-oss-decode@T=128", False),
+         ("gpt-oss-decode@T=1", True), ("gpt-oss-decode@T=128", True)]
+
+
+def run_sweep(args, ctx):
+    import torch
+    out = []
+    for name, fp8 in SWEEP:
+        wl = workload(name)
+        m = measure_layer(args, wl, ctx, seed=wl.seed, steps=args.sweep_steps,
+                          warmup=3, fp8=fp8, e2e=False)
+        f = summarize(wl, m, 1, fp8)
+        r = f["roofline"]
+        entry = {"workload": workload_label(wl, fp8=fp8), "ms": round(m["ms"], 5),
+                 "tflops": round(f["value"], 2), "steps": args.sweep_steps,
+                 "gemm1_roofline": {k: (round(v, 4) if isinstance(v, float) else v)
+                                    for k, v in r.items()},
+                 "stages_ms": {n: round(v, 5) for n, v in m["stage"].items()},
+                 "routing": f["routing"], "clocks": m["clocks"]}
+        for key in ("weight_gbs", "weight_gbs_frac_of_hbm", "frac_of_bf16_peak"):
+            if key in f:
+                entry[key] = round(f[key], 4)
+        out.append(entry)
+        del m
+        torch.cuda.empty_cache()
+    return out
+
+
+def run_ours(args, wl, measure=None):
+    """The repo arm: each rank measures its own replica (seed offset by rank) and rank 0
+    prints one line whose value sums the ranks' useful FLOPs over the slowest rank's time."""
+    dist, rank, world, local = dist_setup(args.gpus)
+    ctx = RankCtx(dist, rank, world, local)
+    measure = measure or measure_layer
+    headline = rank == 0 and world == 1 and not args.no_cpu_baseline and not args.fp8
+    m = measure(args, wl, ctx, seed=wl.seed + 1000 * rank, steps=args.steps,
+                warmup=args.warmup, shared=args.shared, fp8=args.fp8, ep_half=args.ep_half,
+                e2e=True, cpu_baseline=headline)
+    f = summarize(wl, m, world, args.fp8)
+    line = {"metric": METRIC, "value": f["value"], "unit": "TFLOPS", "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": m["ms"],
+            "timing": ("CUDA-graph replays of moe_forward" if m["graph"] else
+                       "eager moe_forward calls") + "; stages_ms: the separate entry points, eager",
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+            "dtype": "bf16" if wl.dtype == "bf16" else "f32",
+            "data": "synthetic (seeded N(0,1) tokens, N(0,1/fan_in) weights, random init)",
+            "config": static_config(wl, world, args.shared, args.fp8, args.ep_half),
+            "stages_ms": {n: round(v, 5) for n, v in m["stage"].items()},
+            "roofline": f["roofline"],
+            "e2e": {"value": f["value"] * m["ms"] / m["e2e_ms"], "unit": "TFLOPS",
+                    "h2d_bytes_per_step": m["io_bytes"], "d2h_bytes_per_step": m["io_bytes"],
+                    "ms_per_step": m["e2e_ms"]},
+            "gpu_launches": m["launches_per_step"] * args.steps,
+            "clocks": m["clocks"]}
+    for key in ("intensity_flop_per_weight_byte", "routing", "weight_gbs",
+                "weight_gbs_frac_of_hbm", "frac_of_bf16_peak", "frac_of_bf16_peak_kind"):
+        if key in f:
+            line[key] = f[key]
+    if "cpu_baseline" in m:
+        line["cpu_baseline"] = m["cpu_baseline"]
+    if world == 1 and not args.no_sweep and args.workload == DEFAULT_WORKLOAD and \
+            not (args.tokens or args.experts or args.fp8 or args.shared or args.ep_half):
+        line["sweep"] = run_sweep(args, ctx)
     if rank == 0:
         print(json.dumps(line), flush=True)
-    if dist is not None:
-        dist.barrier()
-        dist.destroy_process_group()
+    ctx.finish()
 
 
 def run_masked(args, wl):

@@ -90,6 +90,19 @@ class LazyExperts:
         return weights_for_oracle(self.W[int(e)])
 
 
+class LazyExpertsF64:
+    """As LazyExperts, but each expert is widened to float64 on the device (exact for bf16
+    and fp32) before it is copied: for the tests that walk every expert of a multi-GB layer
+    several times, where widening on the host would dominate."""
+
+    def __init__(self, W: torch.Tensor):
+        self.W = W
+        self.shape = tuple(W.shape)
+
+    def __getitem__(self, e):
+        return self.W[int(e)].double().cpu().numpy()
+
+
 class LazyFp8Experts:
     """FP8 expert weights (codes + block scales) left on the device; ``[e]`` dequantises one
     expert on the host with the oracle (code * scale of its 128 x 128 block)."""

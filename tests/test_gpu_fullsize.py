@@ -11,7 +11,7 @@ import torch
 
 import moe_inputs as mi
 import oracle as O
-from _helpers import (LazyExperts, LazyFp8Experts, assert_close, enforce_margins, oracle_logits,
+from _helpers import (LazyExperts, LazyExpertsF64, LazyFp8Experts, assert_close, enforce_margins, oracle_logits,
                       oracle_route_from_logits, sample_tokens, to_np)
 
 pytestmark = [pytest.mark.gpu, pytest.mark.slow]
@@ -106,3 +106,35 @@ def test_full_size_fp8_parity(L, wl, n_sample):
     got = to_np(out[torch.as_tensor(toks, device=DEV)])
     assert_close(got, ref, wl.dtype)
     assert torch.isfinite(out.float()).all()
+
+
+B_CASES = [mi.MIXTRAL, mi.QWEN3, mi.DSV3, mi.GPTOSS.with_T(128)]
+
+
+@pytest.mark.parametrize("wl", B_CASES, ids=[w.name for w in B_CASES])
+def test_version_b_agrees_with_version_a_at_full_size(L, wl):
+    """The oracle's two independent forms ("Mixture-of-Experts Kernels: Routing,
+    Permutation, and Grouped GEMM", §3: a per-expert loop and a dense run-every-expert
+    version that must agree) on a fixed 64-token subset of the full-size layer, tokens of
+    the hottest and of the least-loaded non-empty expert among them, with the layer's
+    bf16 weights widened exactly: A and B agree to 1e-12 relative (in float64 they differ
+    only in the order of the sum over experts). The layer's own output on those tokens is
+    then checked against B within the bf16 tolerance."""
+    from routing_grouped_gemm_router_gb300.layer import MoELayer
+    inp = mi.make_layer(wl, DEV)
+    enforce_margins(inp)
+    sb = to_np(inp.select_bias) if inp.select_bias is not None else None
+    ids, w = oracle_route_from_logits(oracle_logits(inp), wl, sb)
+    toks = sample_tokens(ids, 64, seed=wl.seed + 1)
+    assert toks.size == 64
+    xs = to_np(inp.x[torch.as_tensor(toks, device=DEV)])
+    W13, W2 = LazyExpertsF64(inp.W13), LazyExpertsF64(inp.W2)
+    a = O.moe_loop(xs, ids[toks], w[toks], W13, W2)
+    b = O.moe_dense(xs, ids[toks], w[toks], W13, W2)
+    assert np.abs(a - b).max() <= 1e-12 * np.abs(a).max()
+    layer = MoELayer(inp.Wg, inp.W13, inp.W2, wl.k, wl.mode, wl.renormalize, wl.scale,
+                     wl.n_group, wl.topk_group, inp.logit_bias, inp.select_bias)
+    out = layer(inp.x)
+    torch.cuda.synchronize()
+    assert np.array_equal(to_np(layer.intermediates(wl.T)["topk_ids"]), ids)
+    assert_close(to_np(out[torch.as_tensor(toks, device=DEV)]), b, wl.dtype)
