@@ -174,7 +174,9 @@ moe_status_t moe_workspace_layout(const moe_config_t* cfg, moe_ws_layout_t* L) {
   L->act = take(mp * c->I * es);
   L->xs = take(gather_bytes(c, B));
   L->y = take(n * c->H * es);
-  L->splitk = take(std::max(split_bytes(1, c, B), split_bytes(2, c, B)));
+  // split-K scratch of the grouped GEMMs, or the sync words of the one-launch decode kernel
+  L->splitk = take(std::max({split_bytes(1, c, B), split_bytes(2, c, B),
+                             decode_applies(*cfg) ? decode_sync_bytes(*cfg) : (size_t)0}));
   L->total = off;
   L->block_m = B;
   L->max_padded = (int)mp;
@@ -193,12 +195,21 @@ moe_status_t moe_workspace_size(const moe_config_t* c, size_t* bytes) {
 // spread over many SMs. Otherwise bf16 runs on the tensor cores (E <= 256 fits one MMA N),
 // fp32 on FFMA tiles.
 static moe_status_t router_logits(const moe_config_t* c, const void* x, const void* Wg,
-                                  float* logits, cudaStream_t stream) {
+                                  float* logits, cudaStream_t stream, int* zero = nullptr,
+                                  int n_zero = 0) {
   if (c->dtype == MOE_BF16 && (!aligned16(x) || !aligned16(Wg))) return MOE_ERR_INVALID_ARG;
   if (c->T <= kFewTokens && aligned16(x) && aligned16(Wg))
-    return launch_router_few_tokens(*c, x, Wg, logits, stream);
+    return launch_router_few_tokens(*c, x, Wg, logits, stream, zero, n_zero);
   if (c->dtype == MOE_BF16 && c->E <= 256) return launch_router_tc(*c, x, Wg, logits, stream);
   return launch_router_simt(*c, x, Wg, logits, stream);
+}
+
+moe_status_t moe_route_logits(const moe_config_t* c, const void* x, const void* Wg,
+                              float* logits, cudaStream_t stream) {
+  moe_status_t st = check_cfg(c);
+  if (st != MOE_OK) return st;
+  if (!x || !Wg || !logits) return MOE_ERR_INVALID_ARG;
+  return router_logits(c, x, Wg, logits, stream);
 }
 
 moe_status_t moe_route(const moe_config_t* c, const void* x, const void* Wg, float* logits,
@@ -513,6 +524,18 @@ moe_status_t moe_forward(const moe_config_t* c, const void* x, const void* Wg, c
   int32_t* npp = (int32_t*)(b + L.num_post_padded);
   int32_t* counts = (int32_t*)(b + L.counts);
   const moe_config_t e = effective(c);  // shared experts as ordinary slots / experts
+  if (decode_applies(*c)) {
+    // decode batch: the router GEMM (which also zeroes the decode kernel's sync words), then
+    // top-k, table, both expert GEMMs and the combine in one launch
+    if (!aligned16(x) || !aligned16(W13) || !aligned16(W2) || !aligned16(out))
+      return MOE_ERR_INVALID_ARG;
+    int* sync = (int*)(b + L.splitk);
+    if ((st = router_logits(c, x, Wg, logits, stream, sync,
+                            (int)(decode_sync_bytes(*c) / sizeof(int)))) != MOE_OK)
+      return st;
+    const DecodeWs dw{ids, w, sid, eid, npp, counts, b + L.act, b + L.y, sync};
+    return launch_decode(*c, logits, x, W13, W2, out, dw, stream);
+  }
   if (topk_align_fits(*c)) {
     // decode-sized batch: router GEMM, then top-k and the align table in one CTA (the same
     // device code as moe_route's top-k and moe_align's one-CTA table)
@@ -555,8 +578,38 @@ moe_status_t moe_forward(const moe_config_t* c, const void* x, const void* Wg, c
   return moe_combine(b + L.y, e.T, e.k, e.H, e.dtype, out, stream);
 }
 
+int moe_decode_one_launch(const moe_config_t* cfg) {
+  if (check_cfg(cfg) != MOE_OK) return 0;
+  return decode_applies(*cfg) ? 1 : 0;
+}
+
+moe_status_t moe_expert_decode(const moe_config_t* c, const float* logits, const void* x,
+                               const void* W13, const void* W2, void* out, void* ws,
+                               size_t ws_bytes, cudaStream_t stream) {
+  moe_ws_layout_t L;
+  moe_status_t st = moe_workspace_layout(c, &L);
+  if (st != MOE_OK) return st;
+  if (!decode_applies(*c)) return MOE_ERR_UNSUPPORTED;
+  if (!logits || !x || !W13 || !W2 || !out) return MOE_ERR_INVALID_ARG;
+  if (!aligned16(x) || !aligned16(W13) || !aligned16(W2) || !aligned16(out))
+    return MOE_ERR_INVALID_ARG;
+  if (!ws || ws_bytes < L.total || ((uintptr_t)ws & 255u)) return MOE_ERR_WORKSPACE;
+  uint8_t* b = (uint8_t*)ws;
+  if (cudaMemsetAsync(b + L.splitk, 0, decode_sync_bytes(*c), stream) != cudaSuccess)
+    return MOE_ERR_CUDA;
+  const DecodeWs dw{(int32_t*)(b + L.topk_ids), (float*)(b + L.topk_w),
+                    (int32_t*)(b + L.sorted_ids), (int32_t*)(b + L.expert_ids),
+                    (int32_t*)(b + L.num_post_padded), (int32_t*)(b + L.counts), b + L.act,
+                    b + L.y, b + L.splitk};
+  return launch_decode(*c, logits, x, W13, W2, out, dw, stream);
+}
+
 moe_status_t moe_selftest_wait_timeout(cudaStream_t stream) {
   return launch_selftest_wait(stream);
+}
+
+moe_status_t moe_selftest_barrier_timeout(cudaStream_t stream) {
+  return launch_selftest_barrier(stream);
 }
 
 int moe_device_status(int reset) {
@@ -564,7 +617,8 @@ int moe_device_status(int reset) {
   const int r = router_status_read(reset);
   const int g = grouped_status_read(reset);
   const int c = combine_status_read(reset);
-  return g ? g : (r ? r : (a ? a : c));
+  const int d = decode_status_read(reset);
+  return g ? g : (d ? d : (r ? r : (a ? a : c)));
 }
 
 }  // extern "C"

@@ -64,8 +64,11 @@ inline moe_status_t launch_k(void (*kern)(KArgs...), dim3 grid, dim3 block, size
 
 moe_status_t launch_router_simt(const moe_config_t& c, const void* x, const void* Wg,
                                 float* logits, cudaStream_t s);
+// Few tokens (decode): CUDA cores. zero/n_zero: int words the kernel also clears (the sync
+// words of the one-launch decode kernel that follows it), or null.
 moe_status_t launch_router_few_tokens(const moe_config_t& c, const void* x, const void* Wg,
-                                      float* logits, cudaStream_t s);
+                                      float* logits, cudaStream_t s, int* zero = nullptr,
+                                      int n_zero = 0);
 moe_status_t launch_router_tc(const moe_config_t& c, const void* x, const void* Wg,
                               float* logits, cudaStream_t s);
 moe_status_t launch_topk(const moe_config_t& c, const float* logits, int32_t* ids, float* w,
@@ -122,6 +125,28 @@ moe_status_t launch_combine_local(const void* y, const int32_t* ids, const int32
                                   int T, int k, int H, moe_dtype_t dt, void* out, cudaStream_t s);
 moe_status_t launch_combine(const void* y, int T, int k, int H, moe_dtype_t dt, void* out,
                             cudaStream_t s);
+
+// The rest of a decode-sized layer after its router GEMM in one cooperative launch
+// (decode.cu): whether it applies (cfg as given, shared experts not folded in), the bytes of
+// its sync words (zero at launch), and the launch with the moe_forward workspace slices.
+bool decode_applies(const moe_config_t& c);
+size_t decode_sync_bytes(const moe_config_t& c);
+struct DecodeWs {
+  int32_t* ids;
+  float* w;
+  int32_t* sid;
+  int32_t* eid;
+  int32_t* npp;
+  int32_t* counts;
+  void* act;
+  void* y;
+  void* sync;
+};
+moe_status_t launch_decode(const moe_config_t& c, const float* logits, const void* x,
+                           const void* W13, const void* W2, void* out, const DecodeWs& w,
+                           cudaStream_t s);
+moe_status_t launch_selftest_barrier(cudaStream_t s);
+int decode_status_read(int reset);
 
 moe_status_t launch_selftest_wait(cudaStream_t s);
 
