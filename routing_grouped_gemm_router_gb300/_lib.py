@@ -82,7 +82,7 @@ def _load():
         "moe_forward": (ST, [CFG, P, P, P, P, P, P, SZ, P]),
         "moe_device_status": (I32, [I32]),
         "moe_selftest_wait_timeout": (ST, [P]),
-        "moe_selftest_barrier_timeout": (ST, [P]),
+        "moe_selftest_decode_wait_timeout": (ST, [P]),
         "moe_route_logits": (ST, [CFG, P, P, P, P]),
         "moe_decode_one_launch": (I32, [CFG]),
         "moe_expert_decode": (ST, [CFG, P, P, P, P, P, P, SZ, P]),
@@ -104,7 +104,7 @@ EXPORTED = ("moe_abi_version", "moe_status_string", "moe_block_m", "moe_small_ba
             "moe_grouped_swiglu", "moe_combine", "moe_apply_expert_map", "moe_combine_local",
             "moe_masked_table", "moe_masked_workspace_size", "moe_masked_forward",
             "moe_forward", "moe_device_status", "moe_selftest_wait_timeout",
-            "moe_selftest_barrier_timeout", "moe_route_logits", "moe_decode_one_launch",
+            "moe_selftest_decode_wait_timeout", "moe_route_logits", "moe_decode_one_launch",
             "moe_expert_decode")
 
 
@@ -160,10 +160,10 @@ def moe_selftest_wait_timeout(stream=None):
     _check("moe_selftest_wait_timeout", _lib.moe_selftest_wait_timeout(_stream(stream)))
 
 
-def moe_selftest_barrier_timeout(stream=None):
-    """Diagnostic: a grid barrier that nothing completes times out (see include/moe.h);
-    afterwards moe_device_status() reads 2."""
-    _check("moe_selftest_barrier_timeout", _lib.moe_selftest_barrier_timeout(_stream(stream)))
+def moe_selftest_decode_wait_timeout(stream=None):
+    """Diagnostic: the decode kernel's dependency wait on a counter that nothing raises times
+    out (see include/moe.h); afterwards moe_device_status() reads 2."""
+    _check("moe_selftest_decode_wait_timeout", _lib.moe_selftest_decode_wait_timeout(_stream(stream)))
 
 
 def moe_abi_version() -> int:

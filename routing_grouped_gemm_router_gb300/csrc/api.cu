@@ -608,8 +608,8 @@ moe_status_t moe_selftest_wait_timeout(cudaStream_t stream) {
   return launch_selftest_wait(stream);
 }
 
-moe_status_t moe_selftest_barrier_timeout(cudaStream_t stream) {
-  return launch_selftest_barrier(stream);
+moe_status_t moe_selftest_decode_wait_timeout(cudaStream_t stream) {
+  return launch_selftest_decode_wait(stream);
 }
 
 int moe_device_status(int reset) {

@@ -113,15 +113,20 @@ constexpr int kMinCtas = (!FP8 && RMAX <= 2) ? 3 : 2;
 template <int MODE, bool FP8, int RMAX>
 constexpr int kPieces = RMAX == 1 ? (FP8 ? 8 : 6) : 4;
 
-// Activation rows: read-only inputs through the non-coherent path (__ldg), or, when another
-// CTA of the same launch wrote them (ACT_L2), coherently from L2 (__ldcg).
-template <bool ACT_L2>
+// Activation rows: read-only inputs through the non-coherent path (__ldg), or, when other
+// CTAs of the same launch wrote them before a grid barrier (ACT_WRITTEN), with plain
+// coherent loads (L1-cached): the barrier's acquire orders the writes before them, which the
+// non-coherent path does not promise for data written during the launch.
+template <bool ACT_WRITTEN>
 __device__ __forceinline__ uint4 ld_act(const uint8_t* p) {
-  if constexpr (ACT_L2) return __ldcg(reinterpret_cast<const uint4*>(p));
-  else return __ldg(reinterpret_cast<const uint4*>(p));
+  if constexpr (ACT_WRITTEN) {
+    return __ldca(reinterpret_cast<const uint4*>(p));
+  } else {
+    return __ldg(reinterpret_cast<const uint4*>(p));
+  }
 }
 
-template <int MODE, bool FP8, int R, int S, bool ACT_L2 = false>
+template <int MODE, bool FP8, int R, int S, bool ACT_WRITTEN = false>
 __device__ __forceinline__ void item_pass(const Params& P, const uint8_t* w0, const uint8_t* w1,
                                           const float* s0, const float* s1, const int2* rl,
                                           int rv, int n) {
@@ -161,8 +166,8 @@ __device__ __forceinline__ void item_pass(const Params& P, const uint8_t* w0, co
 #pragma unroll
         for (int r = 0; r < R; ++r) {
           float xf[16];
-          bf16x8_to_f32(ld_act<ACT_L2>(ar[r] + (size_t)kk * 2), xf);
-          bf16x8_to_f32(ld_act<ACT_L2>(ar[r] + (size_t)kk * 2 + 16), xf + 8);
+          bf16x8_to_f32(ld_act<ACT_WRITTEN>(ar[r] + (size_t)kk * 2), xf);
+          bf16x8_to_f32(ld_act<ACT_WRITTEN>(ar[r] + (size_t)kk * 2 + 16), xf + 8);
           float p0 = 0.f, p1 = 0.f;
 #pragma unroll
           for (int i = 0; i < 16; ++i) {
@@ -179,7 +184,7 @@ __device__ __forceinline__ void item_pass(const Params& P, const uint8_t* w0, co
 #pragma unroll
         for (int r = 0; r < R; ++r) {
           float xf[8];
-          bf16x8_to_f32(ld_act<ACT_L2>(ar[r] + (size_t)kk * 2), xf);
+          bf16x8_to_f32(ld_act<ACT_WRITTEN>(ar[r] + (size_t)kk * 2), xf);
 #pragma unroll
           for (int i = 0; i < 8; ++i) {
             a0[r] = fmaf(f0[i], xf[i], a0[r]);
