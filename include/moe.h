@@ -328,11 +328,11 @@ int moe_decode_one_launch(const moe_config_t* cfg);
  * moe_expert_gemm2) and the combine (as moe_combine / moe_combine_local) into out[T, H]. ws is
  * a moe_forward workspace (moe_workspace_size(cfg) bytes, 256-byte aligned): topk_ids,
  * topk_w, the table, act and y are left at their moe_workspace_layout offsets, bit for bit
- * as the separate entry points write them. Inside the kernel a GEMM2 item waits for the
- * GEMM1 columns of its own tile (a bounded wait: one that cannot complete records device
- * status 2 and the warp returns); the kernel's work queue and counters live in the
- * workspace's split-K slice and are cleared here with a memset. Returns MOE_ERR_UNSUPPORTED
- * unless moe_decode_one_launch(cfg). */
+ * as the separate entry points write them. The kernel is a cooperative launch whose CTAs
+ * meet once at a grid barrier between the two GEMMs (bounded: a barrier that cannot complete
+ * records device status 2 and the kernel returns); its sync words live in the workspace's
+ * split-K slice and are cleared here with a memset. Returns MOE_ERR_UNSUPPORTED unless
+ * moe_decode_one_launch(cfg). */
 moe_status_t moe_expert_decode(const moe_config_t* cfg, const float* logits, const void* x,
                                const void* W13, const void* W2, void* out, void* ws,
                                size_t ws_bytes, cudaStream_t stream);
@@ -344,9 +344,9 @@ moe_status_t moe_expert_decode(const moe_config_t* cfg, const float* logits, con
  * the context stays usable. Takes about 2 s of device time. */
 moe_status_t moe_selftest_wait_timeout(cudaStream_t stream);
 
-/* Diagnostic self-test of the decode kernel's dependency wait: one warp waits, through the
- * same bounded wait, for a counter that nothing raises. After the 2 s limit the wait gives
- * up, the device status word reads 2 and the kernel returns: a dependency that cannot
+/* Diagnostic self-test of the decode kernel's grid barrier: one CTA enters, through the same
+ * bounded wait, a barrier of two CTAs that nothing completes. After the 2 s limit the wait
+ * gives up, the device status word reads 2 and the kernel returns: a barrier that cannot
  * complete ends with a status, not a hang, and the context stays usable. Takes about 2 s of
  * device time. */
 moe_status_t moe_selftest_decode_wait_timeout(cudaStream_t stream);

@@ -161,8 +161,8 @@ def moe_selftest_wait_timeout(stream=None):
 
 
 def moe_selftest_decode_wait_timeout(stream=None):
-    """Diagnostic: the decode kernel's dependency wait on a counter that nothing raises times
-    out (see include/moe.h); afterwards moe_device_status() reads 2."""
+    """Diagnostic: the decode kernel's grid barrier, entered by one CTA of two, times out (see
+    include/moe.h); afterwards moe_device_status() reads 2."""
     _check("moe_selftest_decode_wait_timeout", _lib.moe_selftest_decode_wait_timeout(_stream(stream)))
 
 

@@ -126,9 +126,9 @@ moe_status_t launch_combine_local(const void* y, const int32_t* ids, const int32
 moe_status_t launch_combine(const void* y, int T, int k, int H, moe_dtype_t dt, void* out,
                             cudaStream_t s);
 
-// The rest of a decode-sized layer after its router GEMM in one launch (decode.cu): whether
-// it applies (cfg as given, shared experts not folded in), the bytes of its sync words (zero
-// at launch), and the launch with the moe_forward workspace slices.
+// The rest of a decode-sized layer after its router GEMM in one cooperative launch
+// (decode.cu): whether it applies (cfg as given, shared experts not folded in), the bytes of
+// its sync words (zero at launch), and the launch with the moe_forward workspace slices.
 bool decode_applies(const moe_config_t& c);
 size_t decode_sync_bytes(const moe_config_t& c);
 struct DecodeWs {

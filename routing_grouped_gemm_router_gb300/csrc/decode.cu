@@ -10,30 +10,27 @@
 // With a few tokens (bf16 weights: one or two; FP8 E4M3 weights: up to eight, at most 32
 // routed slots) the layer streams the few active experts' weights (gpt-oss-shaped, one token:
 // 4 experts, 199 MB) and every separate launch costs a ramp and a tail of several
-// microseconds. Here one launch of every CTA that fits on the GPU does the rest of the layer
-// after the router GEMM:
+// microseconds. Here one persistent cooperative launch (every CTA resident) does the rest
+// of the layer after the router GEMM:
 //   1. every CTA routes the batch itself (warp t: top-k of token t, the same device code as
 //      the top-k kernel) and builds the tile list in shared memory (a lane per flat row:
 //      warp match, ballots); CTA 0 also writes topk_ids / topk_w and the align table
 //      (sorted_ids, expert_ids with the expert map applied, num_post_padded, counts) to
 //      the workspace, exactly as the separate route, align and expert-map kernels would;
-//   2. GEMM1 items (local tile, column) and then GEMM2 items (local tile, column pair) are
-//      handed out from one work queue (an atomic head) in chunks, so warps that stream
-//      faster take more and the tails even out; GEMM1 items use the weight-streaming device
-//      code of the small-batch GEMV kernels and write act in padded order;
-//   3. a GEMM2 item waits only for its own tile: each finished GEMM1 chunk adds its columns
-//      to the tile's counter, and the item starts once that counter reaches I (a bounded
-//      wait: after the pipeline time limit it records kStatusTimeout and the warp leaves).
-//      All GEMM1 chunks are handed out before any GEMM2 chunk and never wait, so every wait
-//      is on work that a running warp already holds: no deadlock, with or without all CTAs
-//      resident, and no grid-wide barrier: GEMM2 starts on the first tiles while the last
-//      GEMM1 chunks still stream;
-//   4. the warp whose GEMM2 item completes a column pair last (an arrival counter per pair)
-//      adds the k slots of every token in slot order and writes those two columns of out:
-//      no separate combine launch.
+//   2. GEMM1 items (tile, column) spread over the warps in contiguous ranges (the weight
+//      streaming device code of the small-batch GEMV kernels, loads marked to leave L2
+//      first), act in padded order; the warps left without GEMM1 items prefetch the local
+//      experts' W2 into L2 meanwhile (bulk prefetches, up to half the L2), so the DRAM keeps
+//      streaming through GEMM1's tail and the barrier and GEMM2 reads mostly from L2;
+//   3. one grid barrier (bounded: after the pipeline time limit it records kStatusTimeout
+//      and the CTA returns);
+//   4. GEMM2 items (tile, column pair); the warp whose item completes a column pair last
+//      (an arrival counter per pair) adds the k slots of every token in slot order and
+//      writes those two columns of out: no second barrier, no separate combine launch.
 // Results are bit-identical to the separate entry points (same products, same summation
-// orders). The queue head and the counters must be zero at launch: the router GEMM of
-// moe_forward zeroes them and moe_expert_decode clears them with a memset.
+// orders). The barrier word and the per-pair counters must be zero at launch: the router
+// GEMM of moe_forward zeroes them, moe_expert_decode clears them with a memset, and each
+// launch leaves them zero again.
 #include "gemv_dev.cuh"
 #include "route_dev.cuh"
 #include "tc_ptx.cuh"
@@ -46,6 +43,8 @@ __device__ int g_decode_status;
 constexpr int kMaxRows = 32;  // flat rows T*kk of one launch: a lane each
 constexpr int kMaxTokens = 8;  // tokens: a warp each for the top-k
 constexpr int kWarps = gv::kWarps;
+constexpr uint32_t kPrefetchPiece = 32768;         // bytes of one bulk L2 prefetch
+constexpr size_t kPrefetchBudget = 64ull << 20;    // W2 bytes prefetched at most
 constexpr int kThreads = gv::kThreads;
 
 struct Params {
@@ -77,10 +76,8 @@ struct Params {
   uint8_t* act;
   uint8_t* y;
   uint8_t* out;
-  int* qc;         // work queue head (0 at launch)
-  int* tdone;      // [kMaxRows] GEMM1 columns finished per local tile (0 at launch)
-  int* cnt;        // [H / 2] GEMM2 arrivals per output column pair (0 at launch)
-  int chunk1, chunk2;  // queue chunk sizes (items) of the two GEMMs
+  unsigned* bar;  // [0] arrivals, [1] generation (arrivals 0 at launch)
+  int* cnt;       // [H / 2] arrivals per output column pair (0 at launch)
 };
 
 struct Smem {
@@ -94,7 +91,7 @@ struct Smem {
   int gt_cnt[kMaxRows];         // tile of the table (all experts) -> real rows
   int gt_label[kMaxRows];       // tile of the table -> expert_ids label
   int local_row[kMaxRows];      // flat row r is computed on this device
-  int n_local, n_tiles;
+  int n_local, n_tiles, ok;
 };
 
 __device__ __forceinline__ unsigned ld_acquire(const unsigned* p) {
@@ -102,23 +99,44 @@ __device__ __forceinline__ unsigned ld_acquire(const unsigned* p) {
   asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
   return v;
 }
-
-// Bounded wait (one lane) until *p >= target. After the pipeline time limit it records
-// kStatusTimeout and returns false: a dependency that never completes ends with a status, not
-// a hang.
-__device__ __noinline__ bool wait_count(const int* p, int target) {
-  const uint64_t t0 = ptx::gtimer();
-  while ((int)ld_acquire(reinterpret_cast<const unsigned*>(p)) < target) {
-    if (ptx::gtimer() - t0 > ptx::kTimeoutNs) {
-      atomicExch(&g_decode_status, kStatusTimeout);
-      return false;
-    }
-    __nanosleep(64);
-  }
-  return true;
+__device__ __forceinline__ void st_release(unsigned* p, unsigned v) {
+  asm volatile("st.release.gpu.global.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
 }
 
-// Step 1 (routing and the table) of the kernel; returns with the table in shared memory.
+// Sense-reversing grid barrier over n_ctas CTAs (arrival count bar[0], generation bar[1]).
+// The last arrival resets the count and advances the generation; the others poll the
+// generation. A wait that outlasts the pipeline time limit records kStatusTimeout and
+// returns false (the CTA then leaves the kernel): a barrier that cannot complete ends with a
+// status, not a hang.
+__device__ bool grid_barrier(unsigned* bar, unsigned n_ctas, int* ok_sh) {
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    const unsigned g = ld_acquire(bar + 1);
+    __threadfence();
+    int ok = 1;
+    if (atomicAdd(bar, 1u) == n_ctas - 1) {
+      atomicExch(bar, 0u);
+      __threadfence();
+      st_release(bar + 1, g + 1);
+    } else {
+      const uint64_t t0 = ptx::gtimer();
+      while (ld_acquire(bar + 1) == g) {
+        if (ptx::gtimer() - t0 > ptx::kTimeoutNs) {
+          atomicExch(&g_decode_status, kStatusTimeout);
+          ok = 0;
+          break;
+        }
+        __nanosleep(64);
+      }
+    }
+    __threadfence();
+    *ok_sh = ok;
+  }
+  __syncthreads();
+  return *ok_sh != 0;
+}
+
+// Steps 1 (routing and the table) of the kernel; returns with the table in shared memory.
 template <int MPL>
 __device__ __forceinline__ void route_and_table(const Params& P, Smem& S) {
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
@@ -197,118 +215,9 @@ __device__ __forceinline__ void route_and_table(const Params& P, Smem& S) {
   }
 }
 
-// GEMM1 + SwiGLU on items [u0, u1) (tile-major: item u is column u % I of local tile u / I):
-// act[p][c] for the tile's rows, then the chunk's arrival on the tile counter(s).
-template <int RMAX, bool FP8>
-__device__ __forceinline__ void gemm1_chunk(const Params& P, const Smem& S, int u0, int u1) {
-  const int lane = threadIdx.x % 32;
-  const int I = P.I;
-  const int rb = (I + 127) / 128, kb = (P.H + 127) / 128;  // FP8 scale grid of W13
-  const size_t row = (size_t)P.H * (FP8 ? 1 : 2);
-  gv::Params G{};
-  G.a = P.x;
-  G.a_gathered = 0;
-  G.k = P.kk;
-  G.K = P.H;
-  G.N = I;
-  G.out = P.act;
-  for (int u = u0; u < u1; ++u) {
-    const int t = u / I, c = u - t * I;
-    const int slot = S.tile_slot[t];
-    const uint8_t* wg = P.W13 + ((size_t)slot * 2 * I + c) * row;
-    const uint8_t* wu = wg + (size_t)I * row;
-    const float* sg = nullptr;
-    const float* su = nullptr;
-    if (FP8) {
-      sg = P.s13 + (((size_t)slot * 2 + 0) * rb + c / 128) * kb;
-      su = P.s13 + (((size_t)slot * 2 + 1) * rb + c / 128) * kb;
-    }
-    const int2* rl = S.rows + S.tile_c0[t];
-    const int nv = S.tile_n[t];
-    for (int rc = 0; rc < nv; rc += RMAX)
-      gv::item_pass<0, FP8, RMAX, gv::kPieces<0, FP8, RMAX>>(G, wg, wu, sg, su, rl + rc,
-                                                             min(RMAX, nv - rc), c);
-  }
-  __threadfence();  // the chunk's act columns before its arrival on the tile counter(s)
-  __syncwarp();
-  if (lane == 0) {
-    const int ta = u0 / I, tb = (u1 - 1) / I;
-    if (ta == tb) {
-      atomicAdd(&P.tdone[ta], u1 - u0);
-    } else {
-      atomicAdd(&P.tdone[ta], (ta + 1) * I - u0);
-      atomicAdd(&P.tdone[tb], u1 - tb * I);
-    }
-  }
-}
-
-// GEMM2 * topk_w on items [u0, u1) (item u is column pair u % (H/2) of local tile
-// u / (H/2)): y[r][2c, 2c+1], each item after its tile's act rows are complete; the last
-// arrival on a column pair adds the slots of every token into out. Returns false when a
-// dependency wait ran out of time.
-template <int RMAX, bool FP8>
-__device__ __forceinline__ bool gemm2_chunk(const Params& P, const Smem& S, int u0, int u1,
-                                         int A, unsigned& ready) {
-  const int lane = threadIdx.x % 32;
-  const int I = P.I, pairs = P.H / 2;
-  const int rb = (P.H + 127) / 128, kb = (I + 127) / 128;  // FP8 scale grid of W2
-  const size_t row = (size_t)I * (FP8 ? 1 : 2);
-  gv::Params G{};
-  G.a = P.act;
-  G.a_gathered = 1;
-  G.k = 1;
-  G.K = I;
-  G.N = P.H;
-  G.topk_w = S.w;
-  G.out = P.y;
-  for (int u = u0; u < u1; ++u) {
-    const int t = u / pairs, c = u - t * pairs, n0 = 2 * c;
-    if (!((ready >> t) & 1u)) {  // the tile's act rows: every GEMM1 column finished
-      int ok = 1;
-      if (lane == 0) ok = wait_count(&P.tdone[t], I);
-      if (!__shfl_sync(0xffffffffu, ok, 0)) return false;
-      ready |= 1u << t;
-    }
-    const int slot = S.tile_slot[t];
-    const uint8_t* wa = P.W2 + ((size_t)slot * P.H + n0) * row;
-    // columns n0 and n0 + 1 lie in one 128-row block (n0 is even)
-    const float* sa = FP8 ? P.s2 + ((size_t)slot * rb + n0 / 128) * kb : nullptr;
-    const int2* rl = S.rows + S.tile_c0[t];
-    const int nv = S.tile_n[t];
-    for (int rc = 0; rc < nv; rc += RMAX)
-      gv::item_pass<1, FP8, RMAX, gv::kPieces<1, FP8, RMAX>, true>(
-          G, wa, wa + row, sa, sa, rl + rc, min(RMAX, nv - rc), n0);
-  }
-  __threadfence();  // the chunk's y columns before their arrivals
-  __syncwarp();
-  for (int u = u0; u < u1; ++u) {
-    const int c = u % pairs, n0 = 2 * c;
-    int prev = 0;
-    if (lane == 0) prev = atomicAdd(&P.cnt[c], 1);
-    prev = __shfl_sync(0xffffffffu, prev, 0);
-    if (prev != A - 1) continue;
-    // last arrival on this column pair: out[tok][n0, n0+1] = sum over the token's slots
-    __threadfence();
-    for (int tok = lane; tok < P.T; tok += 32) {
-      float a0 = 0.f, a1 = 0.f;
-      for (int j = 0; j < P.kk; ++j) {
-        const int r = tok * P.kk + j;
-        if (!S.local_row[r]) continue;
-        const uint32_t v =
-            __ldcg(reinterpret_cast<const unsigned*>(P.y + ((size_t)r * P.H + n0) * 2));
-        a0 += gv::bf_lo(v);
-        a1 += gv::bf_hi(v);
-      }
-      *reinterpret_cast<uint32_t*>(P.out + ((size_t)tok * P.H + n0) * 2) =
-          gv::pack_bf16x2(a0, a1);
-    }
-  }
-  return true;
-}
-
 template <int RMAX, int MPL, bool FP8>
 __global__ void __launch_bounds__(kThreads, (gv::kMinCtas<0, FP8, RMAX>))
-    decode_kernel(const __grid_constant__ Params P) {
+    decode_kernel(const Params P) {
   __shared__ Smem S;
   pdl_trigger();
   pdl_wait();
@@ -316,59 +225,142 @@ __global__ void __launch_bounds__(kThreads, (gv::kMinCtas<0, FP8, RMAX>))
   route_and_table<MPL>(P, S);
 
   const int A = S.n_local;
+  const int gw = blockIdx.x * kWarps + warp, nwarps = gridDim.x * kWarps;
   if (A == 0) {  // no expert of the batch on this device: out is zero
     uint32_t* o = reinterpret_cast<uint32_t*>(P.out);
     for (int i = blockIdx.x * kThreads + threadIdx.x; i < P.T * P.H / 2; i += gridDim.x * kThreads)
       o[i] = 0u;
     return;
   }
-  const int n1 = A * P.I, n2 = A * (P.H / 2);  // GEMM1 / GEMM2 items, tile-major
-  const int q1 = (n1 + P.chunk1 - 1) / P.chunk1, q2 = (n2 + P.chunk2 - 1) / P.chunk2;
-  // A warp's first chunk is its own index; later ones come from the queue head, each claimed
-  // before the one in hand is worked on. GEMM1 chunks come first: once a claim lands past
-  // them, the warp only gets GEMM2 chunks.
-  const int nwarps = gridDim.x * kWarps;
-  int q = blockIdx.x * kWarps + warp;
-  while (q < q1) {
-    int qn = 0;
-    if (lane == 0) qn = nwarps + atomicAdd(P.qc, 1);
-    gemm1_chunk<RMAX, FP8>(P, S, q * P.chunk1, min(n1, (q + 1) * P.chunk1));
-    q = __shfl_sync(0xffffffffu, qn, 0);
+
+  // ---- GEMM1 + SwiGLU: item (local tile t, column c) -> act[p][c] for the tile's rows
+  {
+    gv::Params G{};
+    G.a = P.x;
+    G.a_gathered = 0;
+    G.k = P.kk;
+    G.K = P.H;
+    G.N = P.I;
+    G.out = P.act;
+    const size_t row_bytes = (size_t)P.H * (FP8 ? 1 : 2);
+    const int rb = (P.I + 127) / 128, kb = (P.H + 127) / 128;
+    const int total = A * P.I;
+    const int per = (total + nwarps - 1) / nwarps;
+    const int w0i = min(total, gw * per), w1i = min(total, w0i + per);
+    const int busy = (total + per - 1) / per;
+    if (gw >= busy) {
+      // no GEMM1 item here: prefetch W2 of the local tiles, tile by tile, into L2
+      const size_t tile_bytes = (size_t)P.H * P.I * (FP8 ? 1 : 2);
+      const int per_tile = (int)((tile_bytes + kPrefetchPiece - 1) / kPrefetchPiece);
+      const int n_pieces = (int)min((size_t)A * per_tile, kPrefetchBudget / kPrefetchPiece);
+      for (int i = (gw - busy) * 32 + lane; i < n_pieces; i += (nwarps - busy) * 32) {
+        const int t = i / per_tile;
+        const size_t off = (size_t)(i - t * per_tile) * kPrefetchPiece;
+        const uint32_t len = (uint32_t)min((size_t)kPrefetchPiece, tile_bytes - off);
+        const uint8_t* a = P.W2 + (size_t)S.tile_slot[t] * tile_bytes + off;
+        asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(a), "r"(len) : "memory");
+      }
+    }
+    const uint64_t pol = gv::l2_evict_first_policy();
+    for (int w = w0i; w < w1i; ++w) {
+      const int t = w / P.I, c = w - t * P.I;
+      const int slot = S.tile_slot[t];
+      const uint8_t* wg = P.W13 + ((size_t)slot * 2 * P.I + c) * row_bytes;
+      const uint8_t* wu = wg + (size_t)P.I * row_bytes;
+      const float* sg = nullptr;
+      const float* su = nullptr;
+      if (FP8) {
+        sg = P.s13 + (((size_t)slot * 2 + 0) * rb + c / 128) * kb;
+        su = P.s13 + (((size_t)slot * 2 + 1) * rb + c / 128) * kb;
+      }
+      const int2* rl = S.rows + S.tile_c0[t];
+      const int nv = S.tile_n[t];
+      for (int rc = 0; rc < nv; rc += RMAX)
+        gv::item_pass<0, FP8, RMAX, gv::kPieces<0, FP8, RMAX>, false, true>(
+            G, wg, wu, sg, su, rl + rc, min(RMAX, nv - rc), c, pol);
+    }
   }
-  unsigned ready = 0;  // local tiles whose act rows this warp has seen complete
-  while (q < q1 + q2) {
-    int qn = 0;
-    if (lane == 0) qn = nwarps + atomicAdd(P.qc, 1);
-    const int c = q - q1;
-    if (!gemm2_chunk<RMAX, FP8>(P, S, c * P.chunk2, min(n2, (c + 1) * P.chunk2), A, ready))
-      return;
-    q = __shfl_sync(0xffffffffu, qn, 0);
+
+  if (!grid_barrier(P.bar, gridDim.x, &S.ok)) return;
+
+  // ---- GEMM2 * topk_w: item (local tile t, column pair c) -> y[r][2c, 2c+1]; the last
+  // item of a column pair adds the slots of every token into out
+  {
+    gv::Params G{};
+    G.a = P.act;
+    G.a_gathered = 1;
+    G.k = 1;
+    G.K = P.I;
+    G.N = P.H;
+    G.topk_w = S.w;
+    G.out = P.y;
+    const size_t row_bytes = (size_t)P.I * (FP8 ? 1 : 2);
+    const int rb = (P.H + 127) / 128, kb = (P.I + 127) / 128;
+    const int pairs = P.H / 2;
+    const int total = A * pairs;
+    const int per = (total + nwarps - 1) / nwarps;
+    const int w0i = min(total, gw * per), w1i = min(total, w0i + per);
+    for (int w = w0i; w < w1i; ++w) {
+      const int t = w / pairs, c = w - t * pairs, n0 = 2 * c;
+      const int slot = S.tile_slot[t];
+      const uint8_t* wa = P.W2 + ((size_t)slot * P.H + n0) * row_bytes;
+      // columns n0 and n0 + 1 lie in one 128-row block (n0 is even)
+      const float* sa = FP8 ? P.s2 + ((size_t)slot * rb + n0 / 128) * kb : nullptr;
+      const int2* rl = S.rows + S.tile_c0[t];
+      const int nv = S.tile_n[t];
+      for (int rc = 0; rc < nv; rc += RMAX)
+        gv::item_pass<1, FP8, RMAX, gv::kPieces<1, FP8, RMAX>, true>(
+            G, wa, wa + row_bytes, sa, sa, rl + rc, min(RMAX, nv - rc), n0);
+      __threadfence();  // this item's y columns before its arrival
+      __syncwarp();
+      int prev = 0;
+      if (lane == 0) prev = atomicAdd(&P.cnt[c], 1);
+      prev = __shfl_sync(0xffffffffu, prev, 0);
+      if (prev == A - 1) {
+        __threadfence();
+        for (int tok = lane; tok < P.T; tok += 32) {
+          float a0 = 0.f, a1 = 0.f;
+          for (int j = 0; j < P.kk; ++j) {
+            const int r = tok * P.kk + j;
+            if (!S.local_row[r]) continue;
+            const uint32_t v = __ldcg(reinterpret_cast<const unsigned*>(
+                P.y + ((size_t)r * P.H + n0) * 2));
+            a0 += gv::bf_lo(v);
+            a1 += gv::bf_hi(v);
+          }
+          *reinterpret_cast<uint32_t*>(P.out + ((size_t)tok * P.H + n0) * 2) =
+              gv::pack_bf16x2(a0, a1);
+        }
+        __syncwarp();
+        if (lane == 0) P.cnt[c] = 0;  // zero again for the next launch
+      }
+    }
   }
 }
 
-// Failure-path self-test of the decode kernel's dependency wait: one warp waits for a
-// counter that nothing raises; after the time limit the wait gives up and records
-// kStatusTimeout.
-__device__ int g_selftest_count;
+// Failure-path self-test of the grid barrier: one CTA enters a barrier of two, which
+// nothing completes; after the time limit the wait gives up and records kStatusTimeout.
+__device__ unsigned g_selftest_bar[2];
 
-__global__ void __launch_bounds__(32) selftest_wait_count_kernel() {
+__global__ void __launch_bounds__(64) selftest_barrier_kernel() {
+  __shared__ int ok;
   pdl_wait();
   pdl_trigger();
   if (threadIdx.x == 0) {
-    g_selftest_count = 0;
+    g_selftest_bar[0] = 0u;
+    g_selftest_bar[1] = 0u;
     __threadfence();
-    wait_count(&g_selftest_count, 1);
   }
+  grid_barrier(g_selftest_bar, 2u, &ok);
 }
 
-// Launch: every CTA that fits on the GPU at once (a warp never waits for a CTA that has not
-// started, so residency is for speed, not for progress); queue chunks of about a third of a
-// warp's share (at least two items, at most one tile: a GEMM1 chunk then spans at most two
-// tiles), so that each warp claims a few.
+// Launch: cooperative (the grid barrier needs every CTA resident) with programmatic stream
+// serialisation when the runtime accepts both; the grid is every CTA that fits at once.
 template <int RMAX, int MPL, bool FP8>
-static moe_status_t launch_rm(Params P, cudaStream_t s) {
+static moe_status_t launch_rm(const Params& P, cudaStream_t s) {
   auto kern = decode_kernel<RMAX, MPL, FP8>;
   static int per_sm[64];
+  static int pdl_state[64];  // 0: untried, 1: cooperative + PDL accepted, 2: cooperative only
   int dev = 0;
   cudaGetDevice(&dev);
   dev &= 63;
@@ -379,14 +371,34 @@ static moe_status_t launch_rm(Params P, cudaStream_t s) {
       return MOE_ERR_CUDA;
     per_sm[dev] = v;
   }
-  const int ctas = num_sms() * per_sm[dev];
-  const int64_t warps = (int64_t)ctas * kWarps;
-  // items are counted for the largest possible number of local tiles (all routed slots)
-  const int64_t tiles = std::min(P.T * P.kk, P.E_eff);
-  P.chunk1 = (int)std::min<int64_t>(P.I, std::max<int64_t>(2, tiles * P.I / (3 * warps)));
-  P.chunk2 = (int)std::min<int64_t>(P.H / 2,
-                                    std::max<int64_t>(2, tiles * (P.H / 2) / (3 * warps)));
-  return launch_k(kern, dim3(ctas), dim3(kThreads), 0, s, P);
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(num_sms() * per_sm[dev]);
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = 0;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[2];
+  attr[0].id = cudaLaunchAttributeCooperative;
+  attr[0].val.cooperative = 1;
+  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[1].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  if (pdl_state[dev] != 2) {
+    cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+    cudaStreamIsCapturing(s, &cs);
+    // the first try of both attributes happens outside stream capture
+    if (pdl_state[dev] == 1 || cs == cudaStreamCaptureStatusNone) {
+      cfg.numAttrs = 2;
+      if (cudaLaunchKernelEx(&cfg, kern, P) == cudaSuccess) {
+        pdl_state[dev] = 1;
+        return MOE_OK;
+      }
+      if (pdl_state[dev] == 1) return MOE_ERR_CUDA;
+      cudaGetLastError();
+      pdl_state[dev] = 2;
+    }
+  }
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kern, P) == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
 }
 
 template <int RMAX, bool FP8>
@@ -422,7 +434,7 @@ bool decode_applies(const moe_config_t& c) {
 }
 
 size_t decode_sync_bytes(const moe_config_t& c) {
-  return align_up((size_t)(1 + dec::kMaxRows + c.H / 2) * sizeof(int), 256);
+  return align_up((size_t)(2 + c.H / 2) * sizeof(int), 256);
 }
 
 moe_status_t launch_decode(const moe_config_t& c, const float* logits, const void* x,
@@ -464,14 +476,13 @@ moe_status_t launch_decode(const moe_config_t& c, const float* logits, const voi
   P.act = (uint8_t*)w.act;
   P.y = (uint8_t*)w.y;
   P.out = (uint8_t*)out;
-  P.qc = (int*)w.sync;
-  P.tdone = (int*)w.sync + 1;
-  P.cnt = (int*)w.sync + 1 + dec::kMaxRows;
+  P.bar = (unsigned*)w.sync;
+  P.cnt = (int*)w.sync + 2;
   return fp8 ? dec::launch_fmt<true>(P, s) : dec::launch_fmt<false>(P, s);
 }
 
 moe_status_t launch_selftest_decode_wait(cudaStream_t s) {
-  return launch_k(dec::selftest_wait_count_kernel, dim3(1), dim3(32), 0, s);
+  return launch_k(dec::selftest_barrier_kernel, dim3(1), dim3(64), 0, s);
 }
 
 int decode_status_read(int reset) {

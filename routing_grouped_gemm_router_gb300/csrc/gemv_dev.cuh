@@ -37,13 +37,27 @@ struct Params {
   void* out;            // GEMM1: act [padded, N]; GEMM2: y [T*k, N] (bf16)
 };
 
-// Weights are read once: no L1 allocation.
-__device__ __forceinline__ uint4 ld_stream(const uint8_t* p) {
+// Weights are read once: no L1 allocation. EVICT_FIRST: the lines also leave L2 first (an
+// L2 cache policy from createpolicy), so a stream read once does not push out data that
+// another phase still needs there.
+template <bool EVICT_FIRST = false>
+__device__ __forceinline__ uint4 ld_stream(const uint8_t* p, uint64_t policy = 0) {
   uint4 v;
-  asm("ld.global.nc.L1::no_allocate.v4.u32 {%0, %1, %2, %3}, [%4];"
-      : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
-      : "l"(p));
+  if constexpr (EVICT_FIRST)
+    asm("ld.global.nc.L1::no_allocate.L2::cache_hint.v4.u32 {%0, %1, %2, %3}, [%4], %5;"
+        : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+        : "l"(p), "l"(policy));
+  else
+    asm("ld.global.nc.L1::no_allocate.v4.u32 {%0, %1, %2, %3}, [%4];"
+        : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+        : "l"(p));
   return v;
+}
+
+__device__ __forceinline__ uint64_t l2_evict_first_policy() {
+  uint64_t p;
+  asm("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(p));
+  return p;
 }
 
 __device__ __forceinline__ float bf_lo(uint32_t u) { return __uint_as_float(u << 16); }
@@ -126,10 +140,10 @@ __device__ __forceinline__ uint4 ld_act(const uint8_t* p) {
   }
 }
 
-template <int MODE, bool FP8, int R, int S, bool ACT_WRITTEN = false>
+template <int MODE, bool FP8, int R, int S, bool ACT_WRITTEN = false, bool W_EVICT_FIRST = false>
 __device__ __forceinline__ void item_pass(const Params& P, const uint8_t* w0, const uint8_t* w1,
                                           const float* s0, const float* s1, const int2* rl,
-                                          int rv, int n) {
+                                          int rv, int n, uint64_t policy = 0) {
   constexpr int EPL = FP8 ? 16 : 8;  // elements of a 16-byte weight piece
   constexpr int ES = FP8 ? 1 : 2;    // weight element bytes
   constexpr int kStride = 32 * EPL;  // elements per warp step
@@ -150,8 +164,8 @@ __device__ __forceinline__ void item_pass(const Params& P, const uint8_t* w0, co
     for (int j = 0; j < S; ++j) {
       const int kk = k0 + j * kStride;
       if (kk < K) {
-        q0[j] = ld_stream(w0 + (size_t)kk * ES);
-        q1[j] = ld_stream(w1 + (size_t)kk * ES);
+        q0[j] = ld_stream<W_EVICT_FIRST>(w0 + (size_t)kk * ES, policy);
+        q1[j] = ld_stream<W_EVICT_FIRST>(w1 + (size_t)kk * ES, policy);
       }
     }
 #pragma unroll

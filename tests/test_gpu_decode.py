@@ -2,8 +2,8 @@
 kernel for top-k, the align table, both expert GEMMs and the combine.
 
 Its results must be the separate entry points' bits (same device arithmetic, same summation
-orders), its intermediates the same tables, it must replay from a CUDA graph, and its
-dependency wait must end with a status, not a hang, when it cannot complete.
+orders), its intermediates the same tables, it must replay from a CUDA graph, and its grid
+barrier must end with a status, not a hang, when it cannot complete.
 """
 import time
 
@@ -217,10 +217,10 @@ def test_decode_graph_capture_and_replay(L, T):
         assert torch.equal(out_static, eager)
 
 
-def test_stalled_dependency_wait_times_out_with_a_status(L):
-    """The decode kernel's dependency wait on a counter that nothing raises gives up after its
-    limit (about 2 s): the kernel returns, the status word reads 2, and the context still runs
-    a decode layer correctly."""
+def test_stalled_grid_barrier_times_out_with_a_status(L):
+    """The decode kernel's grid barrier, entered by one CTA of two, gives up after its limit
+    (about 2 s): the kernel returns, the status word reads 2, and the context still runs a
+    decode layer correctly."""
     L.moe_device_status(True)
     t0 = time.time()
     L.moe_selftest_decode_wait_timeout()
