@@ -17,11 +17,10 @@
 //      warp match, ballots); CTA 0 also writes topk_ids / topk_w and the align table
 //      (sorted_ids, expert_ids with the expert map applied, num_post_padded, counts) to
 //      the workspace, exactly as the separate route, align and expert-map kernels would;
-//   2. GEMM1 items (tile, column) spread over the warps in contiguous ranges (the weight
-//      streaming device code of the small-batch GEMV kernels, loads marked to leave L2
-//      first), act in padded order; the warps left without GEMM1 items prefetch the local
-//      experts' W2 into L2 meanwhile (bulk prefetches, up to half the L2), so the DRAM keeps
-//      streaming through GEMM1's tail and the barrier and GEMM2 reads mostly from L2;
+//   2. GEMM1 items (tile, column) spread evenly over all warps in contiguous ranges (the
+//      weight-streaming device code of the small-batch GEMV kernels, loads marked to leave
+//      L2 first), act in padded order; each warp first starts a bulk L2 prefetch of its first
+//      GEMM2 item's W2 rows, so GEMM2 opens on L2 hits;
 //   3. one grid barrier (bounded: after the pipeline time limit it records kStatusTimeout
 //      and the CTA returns);
 //   4. GEMM2 items (tile, column pair); the warp whose item completes a column pair last
@@ -43,8 +42,6 @@ __device__ int g_decode_status;
 constexpr int kMaxRows = 32;  // flat rows T*kk of one launch: a lane each
 constexpr int kMaxTokens = 8;  // tokens: a warp each for the top-k
 constexpr int kWarps = gv::kWarps;
-constexpr uint32_t kPrefetchPiece = 32768;         // bytes of one bulk L2 prefetch
-constexpr size_t kPrefetchBudget = 64ull << 20;    // W2 bytes prefetched at most
 constexpr int kThreads = gv::kThreads;
 
 struct Params {
@@ -244,21 +241,22 @@ __global__ void __launch_bounds__(kThreads, (gv::kMinCtas<0, FP8, RMAX>))
     G.out = P.act;
     const size_t row_bytes = (size_t)P.H * (FP8 ? 1 : 2);
     const int rb = (P.I + 127) / 128, kb = (P.H + 127) / 128;
+    // every warp takes total / nwarps items, rounded down or up, so every SM carries the
+    // same share of the stream
     const int total = A * P.I;
-    const int per = (total + nwarps - 1) / nwarps;
-    const int w0i = min(total, gw * per), w1i = min(total, w0i + per);
-    const int busy = (total + per - 1) / per;
-    if (gw >= busy) {
-      // no GEMM1 item here: prefetch W2 of the local tiles, tile by tile, into L2
-      const size_t tile_bytes = (size_t)P.H * P.I * (FP8 ? 1 : 2);
-      const int per_tile = (int)((tile_bytes + kPrefetchPiece - 1) / kPrefetchPiece);
-      const int n_pieces = (int)min((size_t)A * per_tile, kPrefetchBudget / kPrefetchPiece);
-      for (int i = (gw - busy) * 32 + lane; i < n_pieces; i += (nwarps - busy) * 32) {
-        const int t = i / per_tile;
-        const size_t off = (size_t)(i - t * per_tile) * kPrefetchPiece;
-        const uint32_t len = (uint32_t)min((size_t)kPrefetchPiece, tile_bytes - off);
-        const uint8_t* a = P.W2 + (size_t)S.tile_slot[t] * tile_bytes + off;
-        asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(a), "r"(len) : "memory");
+    const int w0i = (int)((int64_t)gw * total / nwarps);
+    const int w1i = (int)((int64_t)(gw + 1) * total / nwarps);
+    {
+      // this warp's first GEMM2 item: its two W2 rows start moving into L2 now, so GEMM2
+      // opens on L2 hits while the DRAM streams GEMM1
+      const int n2 = A * (P.H / 2);
+      const int u = (int)((int64_t)gw * n2 / nwarps);
+      if (u < n2 && lane < 2) {
+        const int t = u / (P.H / 2), n0 = 2 * (u - t * (P.H / 2)) + lane;
+        const size_t row2 = (size_t)P.I * (FP8 ? 1 : 2);
+        const uint8_t* a = P.W2 + ((size_t)S.tile_slot[t] * P.H + n0) * row2;
+        asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(a), "r"((uint32_t)row2)
+                     : "memory");
       }
     }
     const uint64_t pol = gv::l2_evict_first_policy();
@@ -298,8 +296,8 @@ __global__ void __launch_bounds__(kThreads, (gv::kMinCtas<0, FP8, RMAX>))
     const int rb = (P.H + 127) / 128, kb = (P.I + 127) / 128;
     const int pairs = P.H / 2;
     const int total = A * pairs;
-    const int per = (total + nwarps - 1) / nwarps;
-    const int w0i = min(total, gw * per), w1i = min(total, w0i + per);
+    const int w0i = (int)((int64_t)gw * total / nwarps);
+    const int w1i = (int)((int64_t)(gw + 1) * total / nwarps);
     for (int w = w0i; w < w1i; ++w) {
       const int t = w / pairs, c = w - t * pairs, n0 = 2 * c;
       const int slot = S.tile_slot[t];
