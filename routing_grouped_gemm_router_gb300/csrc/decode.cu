@@ -19,10 +19,10 @@
 //      the workspace, exactly as the separate route, align and expert-map kernels would;
 //   2. GEMM1 items (tile, column) spread evenly over all warps in contiguous ranges (the
 //      weight-streaming device code of the small-batch GEMV kernels, loads marked to leave
-//      L2 first), act in padded order; each warp first starts a bulk L2 prefetch of its first
-//      GEMM2 item's W2 rows, so GEMM2 opens on L2 hits;
+//      L2 first), act in padded order;
 //   3. one grid barrier (bounded: after the pipeline time limit it records kStatusTimeout
-//      and the CTA returns);
+//      and the CTA returns); before entering it each warp starts an L2 prefetch of the first
+//      round of its first GEMM2 item's weights, so GEMM2 opens on L2 hits;
 //   4. GEMM2 items (tile, column pair); the warp whose item completes a column pair last
 //      (an arrival counter per pair) adds the k slots of every token in slot order and
 //      writes those two columns of out: no second barrier, no separate combine launch.
@@ -246,19 +246,6 @@ __global__ void __launch_bounds__(kThreads, (gv::kMinCtas<0, FP8, RMAX>))
     const int total = A * P.I;
     const int w0i = (int)((int64_t)gw * total / nwarps);
     const int w1i = (int)((int64_t)(gw + 1) * total / nwarps);
-    {
-      // this warp's first GEMM2 item: its two W2 rows start moving into L2 now, so GEMM2
-      // opens on L2 hits while the DRAM streams GEMM1
-      const int n2 = A * (P.H / 2);
-      const int u = (int)((int64_t)gw * n2 / nwarps);
-      if (u < n2 && lane < 2) {
-        const int t = u / (P.H / 2), n0 = 2 * (u - t * (P.H / 2)) + lane;
-        const size_t row2 = (size_t)P.I * (FP8 ? 1 : 2);
-        const uint8_t* a = P.W2 + ((size_t)S.tile_slot[t] * P.H + n0) * row2;
-        asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(a), "r"((uint32_t)row2)
-                     : "memory");
-      }
-    }
     const uint64_t pol = gv::l2_evict_first_policy();
     for (int w = w0i; w < w1i; ++w) {
       const int t = w / P.I, c = w - t * P.I;
@@ -279,6 +266,19 @@ __global__ void __launch_bounds__(kThreads, (gv::kMinCtas<0, FP8, RMAX>))
     }
   }
 
+  {
+    // the head of this warp's first GEMM2 item (its first round of weight pieces) starts
+    // moving into L2 while the barrier completes
+    const int n2 = A * (P.H / 2);
+    const int u = (int)((int64_t)gw * n2 / nwarps);
+    if (u < n2 && lane < 2) {
+      const int t = u / (P.H / 2), n0 = 2 * (u - t * (P.H / 2)) + lane;
+      const size_t row2 = (size_t)P.I * (FP8 ? 1 : 2);
+      const uint32_t head = (uint32_t)min(row2, (size_t)gv::kPieces<1, FP8, RMAX> * 512);
+      const uint8_t* a = P.W2 + ((size_t)S.tile_slot[t] * P.H + n0) * row2;
+      asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(a), "r"(head) : "memory");
+    }
+  }
   if (!grid_barrier(P.bar, gridDim.x, &S.ok)) return;
 
   // ---- GEMM2 * topk_w: item (local tile t, column pair c) -> y[r][2c, 2c+1]; the last

@@ -123,6 +123,75 @@ __device__ __forceinline__ float warp_sum(float v) {
   return v;
 }
 
+// The K best (key, expert, value) entries of a warp, sorted (larger key first, equal keys to
+// the lower expert id), in every lane. Lane l holds the candidates of experts l + 32*i
+// (i < MPL); each lane first keeps its own K best by insertion, then five butterfly steps
+// merge each lane's list with its xor partner's: the element-wise better of one list and
+// the other list reversed is a bitonic sequence holding the K best of both, which a bitonic
+// merge network puts back in order. Both lanes of a pair end with the same list, and after
+// the fifth step every lane holds the warp's K best. The order is a total order, so the
+// result is the one k rounds of warp argmax give, in a few dependent shuffle steps instead of
+// k times five.
+template <int MPL, int K>
+__device__ __forceinline__ void warp_topk_sorted(const float (&key)[MPL], const float (&val)[MPL],
+                                                 int E, float (&lk)[K], int (&li)[K],
+                                                 float (&lv)[K]) {
+  const int lane = threadIdx.x % 32;
+#pragma unroll
+  for (int s = 0; s < K; ++s) {
+    lk[s] = -INFINITY;
+    li[s] = 0x7fffffff;  // an empty slot sorts after every expert
+    lv[s] = 0.f;
+  }
+#pragma unroll
+  for (int i = 0; i < MPL; ++i) {
+    const int e = lane + 32 * i;
+    if (e >= E) continue;
+    float ck = key[i], cv = val[i];
+    int ci = e;
+#pragma unroll
+    for (int s = 0; s < K; ++s) {
+      if (better(ck, ci, lk[s], li[s])) {
+        const float tk = lk[s], tv = lv[s];
+        const int ti = li[s];
+        lk[s] = ck; li[s] = ci; lv[s] = cv;
+        ck = tk; ci = ti; cv = tv;
+      }
+    }
+  }
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) {
+    float pk[K], pv[K];
+    int pi[K];
+#pragma unroll
+    for (int s = 0; s < K; ++s) {
+      pk[s] = __shfl_xor_sync(0xffffffffu, lk[s], off);
+      pi[s] = __shfl_xor_sync(0xffffffffu, li[s], off);
+      pv[s] = __shfl_xor_sync(0xffffffffu, lv[s], off);
+    }
+#pragma unroll
+    for (int s = 0; s < K; ++s) {
+      if (!better(lk[s], li[s], pk[K - 1 - s], pi[K - 1 - s])) {
+        lk[s] = pk[K - 1 - s];
+        li[s] = pi[K - 1 - s];
+        lv[s] = pv[K - 1 - s];
+      }
+    }
+#pragma unroll
+    for (int d = K / 2; d >= 1; d >>= 1) {
+#pragma unroll
+      for (int s = 0; s < K; ++s) {
+        if ((s & d) == 0 && !better(lk[s], li[s], lk[s + d], li[s + d])) {
+          const float tk = lk[s], tv = lv[s];
+          const int ti = li[s];
+          lk[s] = lk[s + d]; li[s] = li[s + d]; lv[s] = lv[s + d];
+          lk[s + d] = tk; li[s + d] = ti; lv[s + d] = tv;
+        }
+      }
+    }
+  }
+}
+
 constexpr int kTopkWarps = 8;
 constexpr int kMaxPerLane = 16;  // E <= 512
 
@@ -198,13 +267,35 @@ __device__ __forceinline__ void topk_token(const float* __restrict__ logits, int
     }
   }
 
-  // k rounds of warp argmax. Taken entries drop to a key below every real one.
   float my_sel_val = 0.f;   // lane j keeps the value of slot j
   int my_sel_id = 0;
+  if (k <= 8) {
+    // the k best from the warp's sorted 4 or 8 best (butterfly merge)
+    auto take = [&](auto& lk, auto& li, auto& lv) {
+#pragma unroll
+      for (int s = 0; s < (int)(sizeof(lk) / sizeof(lk[0])); ++s)
+        if (lane == s) {
+          my_sel_val = lv[s];
+          my_sel_id = li[s];
+        }
+    };
+    if (k <= 4) {
+      float lk[4], lv[4];
+      int li[4];
+      warp_topk_sorted<MPL, 4>(key, val, E, lk, li, lv);
+      take(lk, li, lv);
+    } else {
+      float lk[8], lv[8];
+      int li[8];
+      warp_topk_sorted<MPL, 8>(key, val, E, lk, li, lv);
+      take(lk, li, lv);
+    }
+  }
+  // larger k: k rounds of warp argmax. Taken entries drop to a key below every real one.
   bool taken[MPL];
 #pragma unroll
   for (int i = 0; i < MPL; ++i) taken[i] = false;
-  for (int j = 0; j < k; ++j) {
+  for (int j = 0; k > 8 && j < k; ++j) {
     float bv = NEG;
     int be = 1 << 30;
 #pragma unroll
