@@ -18,14 +18,13 @@
 //      (sorted_ids, expert_ids with the expert map applied, num_post_padded, counts) to
 //      the workspace, exactly as the separate route, align and expert-map kernels would;
 //   2. GEMM1 items (tile, column) spread evenly over all warps in contiguous ranges (the
-//      weight-streaming device code of the small-batch GEMV kernels, loads marked to leave
-//      L2 first), act in padded order;
+//      weight-streaming device code of the small-batch GEMV kernels), act in padded order;
 //   3. one grid barrier (bounded: after the pipeline time limit it records kStatusTimeout
-//      and the CTA returns); before entering it each warp starts an L2 prefetch of the first
-//      round of its first GEMM2 item's weights, so GEMM2 opens on L2 hits;
-//   4. GEMM2 items (tile, column pair); the warp whose item completes a column pair last
-//      (an arrival counter per pair) adds the k slots of every token in slot order and
-//      writes those two columns of out: no second barrier, no separate combine launch.
+//      and the CTA returns);
+//   4. GEMM2 items (tile, column pair); after its items a warp makes its y columns visible
+//      once and arrives on each item's column pair; the arrival that completes a pair (an
+//      arrival counter per pair) adds the k slots of every token in slot order and writes
+//      those two columns of out: no second barrier, no separate combine launch.
 // Results are bit-identical to the separate entry points (same products, same summation
 // orders). The barrier word and the per-pair counters must be zero at launch: the router
 // GEMM of moe_forward zeroes them, moe_expert_decode clears them with a memset, and each
@@ -246,7 +245,6 @@ __global__ void __launch_bounds__(kThreads, (gv::kMinCtas<0, FP8, RMAX>))
     const int total = A * P.I;
     const int w0i = (int)((int64_t)gw * total / nwarps);
     const int w1i = (int)((int64_t)(gw + 1) * total / nwarps);
-    const uint64_t pol = gv::l2_evict_first_policy();
     for (int w = w0i; w < w1i; ++w) {
       const int t = w / P.I, c = w - t * P.I;
       const int slot = S.tile_slot[t];
@@ -261,24 +259,11 @@ __global__ void __launch_bounds__(kThreads, (gv::kMinCtas<0, FP8, RMAX>))
       const int2* rl = S.rows + S.tile_c0[t];
       const int nv = S.tile_n[t];
       for (int rc = 0; rc < nv; rc += RMAX)
-        gv::item_pass<0, FP8, RMAX, gv::kPieces<0, FP8, RMAX>, false, true>(
-            G, wg, wu, sg, su, rl + rc, min(RMAX, nv - rc), c, pol);
+        gv::item_pass<0, FP8, RMAX, gv::kPieces<0, FP8, RMAX>>(G, wg, wu, sg, su, rl + rc,
+                                                               min(RMAX, nv - rc), c);
     }
   }
 
-  {
-    // the head of this warp's first GEMM2 item (its first round of weight pieces) starts
-    // moving into L2 while the barrier completes
-    const int n2 = A * (P.H / 2);
-    const int u = (int)((int64_t)gw * n2 / nwarps);
-    if (u < n2 && lane < 2) {
-      const int t = u / (P.H / 2), n0 = 2 * (u - t * (P.H / 2)) + lane;
-      const size_t row2 = (size_t)P.I * (FP8 ? 1 : 2);
-      const uint32_t head = (uint32_t)min(row2, (size_t)gv::kPieces<1, FP8, RMAX> * 512);
-      const uint8_t* a = P.W2 + ((size_t)S.tile_slot[t] * P.H + n0) * row2;
-      asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(a), "r"(head) : "memory");
-    }
-  }
   if (!grid_barrier(P.bar, gridDim.x, &S.ok)) return;
 
   // ---- GEMM2 * topk_w: item (local tile t, column pair c) -> y[r][2c, 2c+1]; the last
@@ -309,8 +294,15 @@ __global__ void __launch_bounds__(kThreads, (gv::kMinCtas<0, FP8, RMAX>))
       for (int rc = 0; rc < nv; rc += RMAX)
         gv::item_pass<1, FP8, RMAX, gv::kPieces<1, FP8, RMAX>, true>(
             G, wa, wa + row_bytes, sa, sa, rl + rc, min(RMAX, nv - rc), n0);
-      __threadfence();  // this item's y columns before its arrival
+    }
+    // one fence for all of this warp's y columns, then one arrival per item on its column
+    // pair; the arrival that completes a pair adds the slots of every token into out
+    if (w0i < w1i) {
+      __threadfence();
       __syncwarp();
+    }
+    for (int w = w0i; w < w1i; ++w) {
+      const int c = w % pairs, n0 = 2 * c;
       int prev = 0;
       if (lane == 0) prev = atomicAdd(&P.cnt[c], 1);
       prev = __shfl_sync(0xffffffffu, prev, 0);
