@@ -415,17 +415,6 @@ def measure_layer(args, wl, ctx, seed, steps, warmup, shared=0, fp8=False, ep_ha
     # 8 tokens) run the CUDA-core grouped GEMMs, which read the token rows in place
     small = L.moe_small_batch(cfg)
     gathered = wl.dtype == "bf16" and not small
-    # decode batches of one or two tokens: moe_forward is the router GEMM plus one kernel for
-    # top-k, align, both expert GEMMs and the combine
-    one_launch = bool(L.moe_decode_one_launch(cfg))
-
-    def step_one_launch(ev, sh=sh, c=0):
-        ev[0].record(stream)
-        L.moe_route_logits(cfg, inp.x, inp.Wg, p["logits"], sh)
-        ev[1].record(stream)
-        L.moe_expert_decode(cfg, p["logits"], inp.x, W13s[c], W2s[c], out, ws, lay.total, sh)
-        ev[2].record(stream)
-
     def step(ev=None, sh=sh, c=0):
         # The same kernels moe_forward enqueues, called stage by stage so that CUDA events
         # between them give each stage's device time.
@@ -472,15 +461,15 @@ def measure_layer(args, wl, ctx, seed, steps, warmup, shared=0, fp8=False, ep_ha
         L.moe_forward(cfg, inp.x, inp.Wg, W13s[c], W2s[c], out, ws, lay.total, sh)
 
     # kernels moe_forward enqueues: router GEMM + top-k, align (one kernel up to 4096 rows,
-    # else three; up to 8 tokens top-k and align are one kernel), expert map, row gather
-    # (bf16 tensor-core path), GEMM1, GEMM2 (each + a counter-zeroing kernel when split
-    # along K) and the combine
+    # else three; up to 8 tokens top-k and align are one kernel), expert map (applied by the
+    # routing kernel of batches of at most 32 slots), row gather (bf16 tensor-core path),
+    # GEMM1, GEMM2 (each + a counter-zeroing kernel when split along K) and the combine (inside
+    # the small-batch GEMM2 for batches of at most 32 slots)
+    tiny = T <= 8 and T * k <= 32
     routing_launches = 2 if (T <= 8 and T * k <= 4096) else 2 + (1 if T * k <= 4096 else 3)
-    launches_per_step = routing_launches + (1 if emap is not None else 0) + \
-        (1 if gathered else 0) + 3 + \
+    launches_per_step = routing_launches + (1 if (emap is not None and not tiny) else 0) + \
+        (1 if gathered else 0) + 3 - (1 if (tiny and small) else 0) + \
         (0 if small else sum(1 for g in (1, 2) if split_ws_bytes(L, cfg, B, g) > 0))
-    if one_launch:
-        launches_per_step = 2
 
     for _ in range(max(3, warmup)):
         step()
@@ -524,13 +513,11 @@ def measure_layer(args, wl, ctx, seed, steps, warmup, shared=0, fp8=False, ep_ha
     # per-stage device times: the same steps launched eagerly with CUDA events between stages
     evs = [[torch.cuda.Event(enable_timing=True) for _ in range(7)] for _ in range(steps)]
     for i in range(steps):
-        (step_one_launch if one_launch else step)(evs[i], c=i % n_copies)
+        step(evs[i], c=i % n_copies)
     torch.cuda.synchronize()
     clocks = sampler.stop()
-    names = ("route", "experts") if one_launch else \
-        ("route", "align", "gather", "gemm1", "gemm2", "combine")
     stage = {n: statistics.mean(e[i].elapsed_time(e[i + 1]) for e in evs)
-             for i, n in enumerate(names)}
+             for i, n in enumerate(("route", "align", "gather", "gemm1", "gemm2", "combine"))}
     res = {"ms": ms, "stage": stage, "clocks": clocks, "npp": npp, "active": active,
            "local_rows": local_rows, "small": bool(small), "n_copies": n_copies,
            "wbytes": wbytes, "launches_per_step": launches_per_step, "graph": bool(graphs),
@@ -583,19 +570,6 @@ def summarize(wl, m, world, fp8=False):
     hbm_bound = is_decode(wl) or intensity < bf16_burst * 1e12 / (hbm * 1e9)
     # The dominant kernel is timed alone (eager, CUDA events around it): the burst peaks are
     # its denominators.
-    if "experts" in m["stage"]:
-        # one-launch decode: the kernel streams every active expert's W13 and W2 once
-        w_bytes = active * 3 * H * I * wbytes
-        roof = {"bound": "hbm", "achieved": w_bytes / (m["stage"]["experts"] * 1e-3) / 1e9,
-                "peak": hbm, "unit": "GB/s",
-                "kernel": "decode kernel (top-k, align, GEMM1, GEMM2, combine in one launch)",
-                "algorithmic_bytes_per_launch": w_bytes,
-                "peak_kind": f"{peak_src} HBM copy bandwidth"}
-        roof["frac"] = roof["achieved"] / roof["peak"]
-        src = os.path.join(ROOT, "routing_grouped_gemm_router_gb300", "csrc", "decode.cu")
-        roof["traffic"] = profile_traffic("decode" + ("_fp8" if fp8 else ""), wl.name, active,
-                                          src)
-        return _line_fields(wl, m, world, value, intensity, True, roof, hbm, bf16_burst)
     g1_ms = m["stage"]["gemm1"]
     if hbm_bound:
         w_bytes = active * 2 * H * I * wbytes   # gate/up weights of every active expert

@@ -309,33 +309,13 @@ moe_status_t moe_masked_forward(const moe_config_t* cfg, const void* x_masked,
 
 /* The whole layer: route -> align (-> expert map) -> GEMM1+SwiGLU -> GEMM2 -> combine, all
  * enqueued on `stream` with no host round-trip. ws must hold moe_workspace_size(cfg) bytes, 256-byte
- * aligned; its intermediates sit at moe_workspace_layout(cfg) offsets. */
+ * aligned; its intermediates sit at moe_workspace_layout(cfg) offsets. Decode batches (at most
+ * 8 tokens and 32 routed slots) take top-k and the table from one small CTA; when their
+ * grouped GEMMs are the small-batch kernels, the combine runs inside GEMM2 (counters in the
+ * workspace's split-K slice). The results are those of the separate entry points. */
 moe_status_t moe_forward(const moe_config_t* cfg, const void* x, const void* Wg,
                          const void* W13, const void* W2, void* out, void* ws,
                          size_t ws_bytes, cudaStream_t stream);
-
-/* 1 when moe_forward runs a decode batch of this configuration as two launches, the router
- * GEMM and moe_expert_decode's kernel: bf16 tokens, at most 32 routed slots T*(k+n_shared),
- * and at most 2 tokens with bf16 expert weights or 8 with FP8 ones (the small-batch GEMMs'
- * range); 0 otherwise or on bad args. */
-int moe_decode_one_launch(const moe_config_t* cfg);
-
-/* Everything of a decode-sized layer after the router GEMM, in one launch (page §7: decode
- * needs its own small-batch kernels; §10: at decode the router, align and combine cost as
- * much as the GEMMs): from logits[T, E] (fp32, device; e.g. moe_route_logits' output) the
- * top-k (as moe_route), the align table (as moe_align, then moe_apply_expert_map when
- * cfg->expert_map is set), GEMM1 + SwiGLU and GEMM2 (as the small-batch moe_expert_gemm1 /
- * moe_expert_gemm2) and the combine (as moe_combine / moe_combine_local) into out[T, H]. ws is
- * a moe_forward workspace (moe_workspace_size(cfg) bytes, 256-byte aligned): topk_ids,
- * topk_w, the table, act and y are left at their moe_workspace_layout offsets, bit for bit
- * as the separate entry points write them. The kernel is a cooperative launch whose CTAs
- * meet once at a grid barrier between the two GEMMs (bounded: a barrier that cannot complete
- * records device status 2 and the kernel returns); its sync words live in the workspace's
- * split-K slice and are cleared here with a memset. Returns MOE_ERR_UNSUPPORTED unless
- * moe_decode_one_launch(cfg). */
-moe_status_t moe_expert_decode(const moe_config_t* cfg, const float* logits, const void* x,
-                               const void* W13, const void* W2, void* out, void* ws,
-                               size_t ws_bytes, cudaStream_t stream);
 
 /* Diagnostic self-test of the failure path: enqueues one CTA whose pipeline waits nothing
  * will satisfy (it also holds tensor memory). After the 2 s pipeline-wait limit the waits
@@ -343,13 +323,6 @@ moe_status_t moe_expert_decode(const moe_config_t* cfg, const float* logits, con
  * (a pipeline wait ran out of time): a stalled pipeline ends with a status, not a hang, and
  * the context stays usable. Takes about 2 s of device time. */
 moe_status_t moe_selftest_wait_timeout(cudaStream_t stream);
-
-/* Diagnostic self-test of the decode kernel's grid barrier: one CTA enters, through the same
- * bounded wait, a barrier of two CTAs that nothing completes. After the 2 s limit the wait
- * gives up, the device status word reads 2 and the kernel returns: a barrier that cannot
- * complete ends with a status, not a hang, and the context stays usable. Takes about 2 s of
- * device time. */
-moe_status_t moe_selftest_decode_wait_timeout(cudaStream_t stream);
 
 /* Diagnostic (synchronises the current device): returns the device status word (0 = no
  * fault seen; 1 = an expert id outside [0, E); 2 = a wait ran out of time; 3 = the

@@ -14,6 +14,5 @@ from ._lib import (EXPORTED, MOE_BF16, MOE_F32, MOE_ROUTE_SIGMOID_GROUPED,  # no
                    moe_expert_gemm2_workspace_size, moe_forward, moe_gather_rows,
                    moe_grouped_swiglu, moe_grouped_swiglu_workspace_size, moe_masked_forward,
                    moe_masked_table, moe_masked_workspace_size, moe_max_padded_rows, moe_route,
-                   moe_small_batch, moe_route_logits, moe_decode_one_launch, moe_expert_decode,
-                   moe_selftest_wait_timeout, moe_selftest_decode_wait_timeout,
+                   moe_small_batch, moe_route_logits, moe_selftest_wait_timeout,
                    moe_workspace_layout, moe_workspace_size, status_string)

@@ -82,10 +82,7 @@ def _load():
         "moe_forward": (ST, [CFG, P, P, P, P, P, P, SZ, P]),
         "moe_device_status": (I32, [I32]),
         "moe_selftest_wait_timeout": (ST, [P]),
-        "moe_selftest_decode_wait_timeout": (ST, [P]),
         "moe_route_logits": (ST, [CFG, P, P, P, P]),
-        "moe_decode_one_launch": (I32, [CFG]),
-        "moe_expert_decode": (ST, [CFG, P, P, P, P, P, P, SZ, P]),
     }
     for name, (res, args) in sig.items():
         f = getattr(lib, name)
@@ -104,8 +101,7 @@ EXPORTED = ("moe_abi_version", "moe_status_string", "moe_block_m", "moe_small_ba
             "moe_grouped_swiglu", "moe_combine", "moe_apply_expert_map", "moe_combine_local",
             "moe_masked_table", "moe_masked_workspace_size", "moe_masked_forward",
             "moe_forward", "moe_device_status", "moe_selftest_wait_timeout",
-            "moe_selftest_decode_wait_timeout", "moe_route_logits", "moe_decode_one_launch",
-            "moe_expert_decode")
+            "moe_route_logits")
 
 
 def lib():
@@ -160,12 +156,6 @@ def moe_selftest_wait_timeout(stream=None):
     _check("moe_selftest_wait_timeout", _lib.moe_selftest_wait_timeout(_stream(stream)))
 
 
-def moe_selftest_decode_wait_timeout(stream=None):
-    """Diagnostic: the decode kernel's grid barrier, entered by one CTA of two, times out (see
-    include/moe.h); afterwards moe_device_status() reads 2."""
-    _check("moe_selftest_decode_wait_timeout", _lib.moe_selftest_decode_wait_timeout(_stream(stream)))
-
-
 def moe_abi_version() -> int:
     return _lib.moe_abi_version()
 
@@ -204,16 +194,6 @@ def moe_workspace_size(cfg) -> int:
 def moe_route_logits(cfg, x, Wg, logits, stream=None):
     _check("moe_route_logits", _lib.moe_route_logits(ctypes.byref(cfg), _ptr(x), _ptr(Wg),
                                                      _ptr(logits), _stream(stream)))
-
-
-def moe_decode_one_launch(cfg) -> int:
-    return _lib.moe_decode_one_launch(ctypes.byref(cfg))
-
-
-def moe_expert_decode(cfg, logits, x, W13, W2, out, ws, ws_bytes, stream=None):
-    _check("moe_expert_decode", _lib.moe_expert_decode(
-        ctypes.byref(cfg), _ptr(logits), _ptr(x), _ptr(W13), _ptr(W2), _ptr(out), _ptr(ws),
-        ws_bytes, _stream(stream)))
 
 
 def moe_route(cfg, x, Wg, logits, topk_ids, topk_w, stream=None):

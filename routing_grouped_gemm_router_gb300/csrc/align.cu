@@ -443,3 +443,120 @@ moe_status_t launch_topk_align_small(const moe_config_t& c, const float* logits,
 }
 
 }  // namespace moe
+
+namespace moe {
+
+// ---- decode batches: top-k and the table in one small CTA ---------------------------------
+// For at most kTinyRows routed slots the table needs no histogram pass: warp t routes token t
+// (the top-k device code of the top-k kernel) into shared memory, then warp 0 gives each flat
+// row r a lane: a warp match finds the rows of its expert (its rank among them keeps them in
+// ascending r), and counting, over the other lanes, the first rows of lower experts gives its
+// tile of the table (experts ascending, one tile each). The result is the table moe_align
+// writes (and, with an expert map, moe_apply_expert_map after it): rows first in each tile,
+// then sentinels, tail tiles -1.
+constexpr int kTinyRows = 32;
+constexpr int kTinyThreads = 256;
+
+__device__ int g_tiny_status;
+
+int tiny_status_read(int reset) {
+  int v = 0;
+  cudaMemcpyFromSymbol(&v, g_tiny_status, sizeof(int));
+  if (reset) {
+    int z = 0;
+    cudaMemcpyToSymbol(g_tiny_status, &z, sizeof(int));
+  }
+  return v;
+}
+
+template <int MPL>
+__global__ void __launch_bounds__(kTinyThreads) topk_table_tiny_kernel(
+    const TopkArgs a, int32_t* __restrict__ ids, float* __restrict__ w, int n, int E_eff, int B,
+    int max_padded, int32_t* __restrict__ sorted_ids, int32_t* __restrict__ expert_ids,
+    int32_t* npp, int32_t* counts, const int32_t* __restrict__ map, int* __restrict__ zero,
+    int n_zero) {
+  __shared__ float skey[kTopkWarps][512];
+  __shared__ int32_t ids_s[kTinyRows];
+  __shared__ float w_s[kTinyRows];
+  __shared__ int gt_cnt[kTinyRows], gt_label[kTinyRows];
+  __shared__ int n_tiles_s;
+  pdl_wait();
+  pdl_trigger();
+  const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+  for (int i = threadIdx.x; i < n_zero; i += blockDim.x) zero[i] = 0;
+  if (warp < a.Tn)
+    topk_token<MPL>(a.logits, warp, a.E, a.k, a.mode, a.renorm, a.scale, a.n_group, a.topk_group,
+                    a.logit_bias, a.select_bias, a.n_shared, ids_s, w_s, skey[warp]);
+  __syncthreads();
+  if (warp == 0) {
+    const int e = lane < n ? ids_s[lane] : 0x7fffffff;
+    const unsigned peers = __match_any_sync(0xffffffffu, e);
+    const int rank = __popc(peers & ((1u << lane) - 1u));
+    const bool first = lane < n && rank == 0;
+    int g = 0;
+#pragma unroll 8
+    for (int j = 0; j < kTinyRows; ++j) {
+      const int ej = __shfl_sync(0xffffffffu, e, j);
+      const int fj = __shfl_sync(0xffffffffu, (int)first, j);
+      g += (fj && ej < e);
+    }
+    if (first) {
+      int label = e;
+      if (map) {
+        label = map[e];
+        if (label < -1 || label >= E_eff) {  // as moe_apply_expert_map: flagged, skipped
+          atomicExch(&g_tiny_status, kStatusBadExpert);
+          label = -1;
+        }
+      }
+      gt_cnt[g] = __popc(peers);
+      gt_label[g] = label;
+    }
+    if (lane < n) {
+      ids[lane] = e;
+      w[lane] = w_s[lane];
+      sorted_ids[g * B + rank] = lane;
+    }
+    const int nt = __popc(__ballot_sync(0xffffffffu, first));
+    if (lane == 0) n_tiles_s = nt;
+  }
+  __syncthreads();
+  const int nt = n_tiles_s;
+  for (int q = threadIdx.x; q < max_padded; q += blockDim.x) {
+    const int t = q / B, i = q - t * B;
+    if (!(t < nt && i < gt_cnt[t])) sorted_ids[q] = n;
+  }
+  for (int t = threadIdx.x; t < max_padded / B; t += blockDim.x)
+    expert_ids[t] = t < nt ? gt_label[t] : -1;
+  for (int e = threadIdx.x; e < E_eff; e += blockDim.x) {
+    int c = 0;
+    for (int r = 0; r < n; ++r) c += ids_s[r] == e;
+    counts[e] = c;
+  }
+  if (threadIdx.x == 0) *npp = nt * B;
+}
+
+bool topk_table_tiny_fits(const moe_config_t& c) {
+  return c.T <= kTopkWarps && c.T * (c.k + c.n_shared) <= kTinyRows;
+}
+
+moe_status_t launch_topk_table_tiny(const moe_config_t& c, const float* logits, int32_t* ids,
+                                    float* w, int B, int max_padded, int32_t* sorted_ids,
+                                    int32_t* expert_ids, int32_t* npp, int32_t* counts,
+                                    int* zero, int n_zero, cudaStream_t s) {
+  if (!topk_table_tiny_fits(c) || !counts) return MOE_ERR_UNSUPPORTED;
+  const int kk = c.k + c.n_shared, E_eff = c.E + c.n_shared;
+  const TopkArgs a{logits, c.T, c.E, c.k, (int)c.mode, c.renormalize, c.scale, c.n_group,
+                   c.topk_group, c.logit_bias, c.select_bias, c.n_shared};
+  auto run = [&](auto kern) {
+    return launch_k(kern, dim3(1), dim3(kTinyThreads), 0, s, a, ids, w, c.T * kk, E_eff, B,
+                    max_padded, sorted_ids, expert_ids, npp, counts, c.expert_map, zero, n_zero);
+  };
+  switch (topk_per_lane(c.E)) {
+    case 4: return run(topk_table_tiny_kernel<4>);
+    case 8: return run(topk_table_tiny_kernel<8>);
+    default: return run(topk_table_tiny_kernel<kMaxPerLane>);
+  }
+}
+
+}  // namespace moe

@@ -100,6 +100,18 @@ moe_status_t align_check_args(const int32_t* topk_ids, int T, int k, int E, int 
   return MOE_OK;
 }
 
+// Decode batches whose routing fits one small CTA and whose grouped GEMMs run on CUDA cores:
+// moe_forward then runs the combine inside the small-batch GEMM2 (its counters live in the
+// workspace's split-K slice, which that path does not use otherwise).
+static bool decode_combine_fused(const moe_config_t& c) {
+  const moe_config_t e = effective(&c);
+  return c.dtype == MOE_BF16 && topk_table_tiny_fits(c) &&
+         gemv_applies(e, (int)moe_max_padded_rows(e.T, e.k, e.E, block_m_for(e.dtype)));
+}
+static size_t combine_counter_bytes(const moe_config_t& c) {
+  return align_up((size_t)(c.H / 2) * sizeof(int), 256);
+}
+
 }  // namespace moe
 
 using namespace moe;
@@ -174,9 +186,9 @@ moe_status_t moe_workspace_layout(const moe_config_t* cfg, moe_ws_layout_t* L) {
   L->act = take(mp * c->I * es);
   L->xs = take(gather_bytes(c, B));
   L->y = take(n * c->H * es);
-  // split-K scratch of the grouped GEMMs, or the sync words of the one-launch decode kernel
+  // split-K scratch of the grouped GEMMs, or the combine counters of the decode path
   L->splitk = take(std::max({split_bytes(1, c, B), split_bytes(2, c, B),
-                             decode_applies(*cfg) ? decode_sync_bytes(*cfg) : (size_t)0}));
+                             decode_combine_fused(*cfg) ? combine_counter_bytes(*cfg) : 0}));
   L->total = off;
   L->block_m = B;
   L->max_padded = (int)mp;
@@ -195,11 +207,10 @@ moe_status_t moe_workspace_size(const moe_config_t* c, size_t* bytes) {
 // spread over many SMs. Otherwise bf16 runs on the tensor cores (E <= 256 fits one MMA N),
 // fp32 on FFMA tiles.
 static moe_status_t router_logits(const moe_config_t* c, const void* x, const void* Wg,
-                                  float* logits, cudaStream_t stream, int* zero = nullptr,
-                                  int n_zero = 0) {
+                                  float* logits, cudaStream_t stream) {
   if (c->dtype == MOE_BF16 && (!aligned16(x) || !aligned16(Wg))) return MOE_ERR_INVALID_ARG;
   if (c->T <= kFewTokens && aligned16(x) && aligned16(Wg))
-    return launch_router_few_tokens(*c, x, Wg, logits, stream, zero, n_zero);
+    return launch_router_few_tokens(*c, x, Wg, logits, stream);
   if (c->dtype == MOE_BF16 && c->E <= 256) return launch_router_tc(*c, x, Wg, logits, stream);
   return launch_router_simt(*c, x, Wg, logits, stream);
 }
@@ -524,19 +535,18 @@ moe_status_t moe_forward(const moe_config_t* c, const void* x, const void* Wg, c
   int32_t* npp = (int32_t*)(b + L.num_post_padded);
   int32_t* counts = (int32_t*)(b + L.counts);
   const moe_config_t e = effective(c);  // shared experts as ordinary slots / experts
-  if (decode_applies(*c)) {
-    // decode batch: the router GEMM (which also zeroes the decode kernel's sync words), then
-    // top-k, table, both expert GEMMs and the combine in one launch
-    if (!aligned16(x) || !aligned16(W13) || !aligned16(W2) || !aligned16(out))
-      return MOE_ERR_INVALID_ARG;
-    int* sync = (int*)(b + L.splitk);
-    if ((st = router_logits(c, x, Wg, logits, stream, sync,
-                            (int)(decode_sync_bytes(*c) / sizeof(int)))) != MOE_OK)
+  const bool tiny = topk_table_tiny_fits(*c);
+  // decode batches on the small-batch GEMMs: the combine runs inside GEMM2, on counters the
+  // routing kernel zeroes
+  int* cnt = decode_combine_fused(*c) ? (int*)(b + L.splitk) : nullptr;
+  if (tiny) {
+    // at most 32 routed slots: router GEMM, then top-k and the table (expert map applied) in
+    // one small CTA
+    if ((st = router_logits(c, x, Wg, logits, stream)) != MOE_OK) return st;
+    if ((st = launch_topk_table_tiny(*c, logits, ids, w, L.block_m, L.max_padded, sid, eid, npp,
+                                     counts, cnt, cnt ? c->H / 2 : 0, stream)) != MOE_OK)
       return st;
-    const DecodeWs dw{ids, w, sid, eid, npp, counts, b + L.act, b + L.y, sync};
-    return launch_decode(*c, logits, x, W13, W2, out, dw, stream);
-  }
-  if (topk_align_fits(*c)) {
+  } else if (topk_align_fits(*c)) {
     // decode-sized batch: router GEMM, then top-k and the align table in one CTA (the same
     // device code as moe_route's top-k and moe_align's one-CTA table)
     if ((st = router_logits(c, x, Wg, logits, stream)) != MOE_OK) return st;
@@ -549,7 +559,7 @@ moe_status_t moe_forward(const moe_config_t* c, const void* x, const void* Wg, c
                         b + L.align_scratch, L.act - L.align_scratch, stream)) != MOE_OK)
       return st;
   }
-  if (c->expert_map &&
+  if (c->expert_map && !tiny &&
       (st = moe_apply_expert_map(eid, L.max_padded / L.block_m, c->expert_map, e.E, stream)) !=
           MOE_OK)
     return st;
@@ -569,6 +579,11 @@ moe_status_t moe_forward(const moe_config_t* c, const void* x, const void* Wg, c
                                     stream)) != MOE_OK) {
     return st;
   }
+  if (cnt) {
+    if (!aligned16(out)) return MOE_ERR_INVALID_ARG;
+    return launch_gemv2_combine(e, b + L.act, W2, sid, eid, npp, L.block_m, w, b + L.y, ids, cnt,
+                                out, stream);
+  }
   if ((st = moe_expert_gemm2(c, b + L.act, W2, sid, eid, npp, L.block_m, w, b + L.y,
                              b + L.splitk, L.total - L.splitk, stream)) != MOE_OK)
     return st;
@@ -578,38 +593,8 @@ moe_status_t moe_forward(const moe_config_t* c, const void* x, const void* Wg, c
   return moe_combine(b + L.y, e.T, e.k, e.H, e.dtype, out, stream);
 }
 
-int moe_decode_one_launch(const moe_config_t* cfg) {
-  if (check_cfg(cfg) != MOE_OK) return 0;
-  return decode_applies(*cfg) ? 1 : 0;
-}
-
-moe_status_t moe_expert_decode(const moe_config_t* c, const float* logits, const void* x,
-                               const void* W13, const void* W2, void* out, void* ws,
-                               size_t ws_bytes, cudaStream_t stream) {
-  moe_ws_layout_t L;
-  moe_status_t st = moe_workspace_layout(c, &L);
-  if (st != MOE_OK) return st;
-  if (!decode_applies(*c)) return MOE_ERR_UNSUPPORTED;
-  if (!logits || !x || !W13 || !W2 || !out) return MOE_ERR_INVALID_ARG;
-  if (!aligned16(x) || !aligned16(W13) || !aligned16(W2) || !aligned16(out))
-    return MOE_ERR_INVALID_ARG;
-  if (!ws || ws_bytes < L.total || ((uintptr_t)ws & 255u)) return MOE_ERR_WORKSPACE;
-  uint8_t* b = (uint8_t*)ws;
-  if (cudaMemsetAsync(b + L.splitk, 0, decode_sync_bytes(*c), stream) != cudaSuccess)
-    return MOE_ERR_CUDA;
-  const DecodeWs dw{(int32_t*)(b + L.topk_ids), (float*)(b + L.topk_w),
-                    (int32_t*)(b + L.sorted_ids), (int32_t*)(b + L.expert_ids),
-                    (int32_t*)(b + L.num_post_padded), (int32_t*)(b + L.counts), b + L.act,
-                    b + L.y, b + L.splitk};
-  return launch_decode(*c, logits, x, W13, W2, out, dw, stream);
-}
-
 moe_status_t moe_selftest_wait_timeout(cudaStream_t stream) {
   return launch_selftest_wait(stream);
-}
-
-moe_status_t moe_selftest_decode_wait_timeout(cudaStream_t stream) {
-  return launch_selftest_decode_wait(stream);
 }
 
 int moe_device_status(int reset) {
@@ -617,8 +602,8 @@ int moe_device_status(int reset) {
   const int r = router_status_read(reset);
   const int g = grouped_status_read(reset);
   const int c = combine_status_read(reset);
-  const int d = decode_status_read(reset);
-  return g ? g : (d ? d : (r ? r : (a ? a : c)));
+  const int t = tiny_status_read(reset);
+  return g ? g : (r ? r : (a ? a : (t ? t : c)));
 }
 
 }  // extern "C"

@@ -64,11 +64,8 @@ inline moe_status_t launch_k(void (*kern)(KArgs...), dim3 grid, dim3 block, size
 
 moe_status_t launch_router_simt(const moe_config_t& c, const void* x, const void* Wg,
                                 float* logits, cudaStream_t s);
-// Few tokens (decode): CUDA cores. zero/n_zero: int words the kernel also clears (the sync
-// words of the one-launch decode kernel that follows it), or null.
 moe_status_t launch_router_few_tokens(const moe_config_t& c, const void* x, const void* Wg,
-                                      float* logits, cudaStream_t s, int* zero = nullptr,
-                                      int n_zero = 0);
+                                      float* logits, cudaStream_t s);
 moe_status_t launch_router_tc(const moe_config_t& c, const void* x, const void* Wg,
                               float* logits, cudaStream_t s);
 moe_status_t launch_topk(const moe_config_t& c, const float* logits, int32_t* ids, float* w,
@@ -88,6 +85,15 @@ moe_status_t launch_topk_align_small(const moe_config_t& c, const float* logits,
                                      float* w, int B, int max_padded, int32_t* sorted_ids,
                                      int32_t* expert_ids, int32_t* npp, int32_t* counts,
                                      cudaStream_t s);
+// Decode batches of at most 32 routed slots: top-k and the table from one warp per token and
+// one lane per slot, with cfg.expert_map applied to the tile labels, in one small CTA
+// (align.cu); it also zeroes n_zero ints at zero (the combine counters of the small-batch
+// GEMM2 that follows it in moe_forward).
+bool topk_table_tiny_fits(const moe_config_t& c);
+moe_status_t launch_topk_table_tiny(const moe_config_t& c, const float* logits, int32_t* ids,
+                                    float* w, int B, int max_padded, int32_t* sorted_ids,
+                                    int32_t* expert_ids, int32_t* npp, int32_t* counts,
+                                    int* zero, int n_zero, cudaStream_t s);
 moe_status_t launch_gemm1_simt(const moe_config_t& c, const float* x, const float* W13,
                                const int32_t* sid, const int32_t* eid, const int32_t* npp,
                                int block_m, int max_padded, float* act, cudaStream_t s);
@@ -115,6 +121,14 @@ moe_status_t launch_gemv1(const moe_config_t& c, const void* a, bool gathered, c
 moe_status_t launch_gemv2(const moe_config_t& c, const void* act, const void* W2,
                           const int32_t* sid, const int32_t* eid, const int32_t* npp,
                           int block_m, const float* topk_w, void* y, cudaStream_t s);
+// The small-batch GEMM2 followed by the top-k combine in the same launch: every item
+// (tile, column pair) arrives on its pair's counter (cnt[H/2], zero at launch, left zero)
+// once the warp's y columns are visible; the last arrival adds the slots of every token
+// (skipping slots whose expert map entry is negative) into out[T, H].
+moe_status_t launch_gemv2_combine(const moe_config_t& c, const void* act, const void* W2,
+                                  const int32_t* sid, const int32_t* eid, const int32_t* npp,
+                                  int block_m, const float* topk_w, void* y,
+                                  const int32_t* topk_ids, int* cnt, void* out, cudaStream_t s);
 moe_status_t launch_gather_rows(const void* x, const int32_t* sid, const int32_t* npp,
                                 int n_rows, int k, int row_bytes, void* xs, cudaStream_t s);
 moe_status_t launch_masked_table(const int32_t* counts, int E, int C, int B, int32_t* sid,
@@ -126,33 +140,12 @@ moe_status_t launch_combine_local(const void* y, const int32_t* ids, const int32
 moe_status_t launch_combine(const void* y, int T, int k, int H, moe_dtype_t dt, void* out,
                             cudaStream_t s);
 
-// The rest of a decode-sized layer after its router GEMM in one cooperative launch
-// (decode.cu): whether it applies (cfg as given, shared experts not folded in), the bytes of
-// its sync words (zero at launch), and the launch with the moe_forward workspace slices.
-bool decode_applies(const moe_config_t& c);
-size_t decode_sync_bytes(const moe_config_t& c);
-struct DecodeWs {
-  int32_t* ids;
-  float* w;
-  int32_t* sid;
-  int32_t* eid;
-  int32_t* npp;
-  int32_t* counts;
-  void* act;
-  void* y;
-  void* sync;
-};
-moe_status_t launch_decode(const moe_config_t& c, const float* logits, const void* x,
-                           const void* W13, const void* W2, void* out, const DecodeWs& w,
-                           cudaStream_t s);
-moe_status_t launch_selftest_decode_wait(cudaStream_t s);
-int decode_status_read(int reset);
-
 moe_status_t launch_selftest_wait(cudaStream_t s);
 
 int align_status_read(int reset);
 int router_status_read(int reset);
 int grouped_status_read(int reset);
 int combine_status_read(int reset);
+int tiny_status_read(int reset);
 
 }  // namespace moe

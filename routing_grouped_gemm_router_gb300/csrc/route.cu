@@ -76,15 +76,9 @@ template <typename T, int TB>
 __global__ void __launch_bounds__(256) router_few_tokens_kernel(const T* __restrict__ x,
                                                                 const T* __restrict__ Wg,
                                                                 float* __restrict__ logits,
-                                                                int Tn, int H, int E,
-                                                                int* __restrict__ zero,
-                                                                int n_zero) {
+                                                                int Tn, int H, int E) {
   pdl_wait();
   pdl_trigger();
-  if (zero) {  // sync words of the decode kernel that follows (see decode.cu)
-    const int nb = gridDim.x * gridDim.y, b = blockIdx.y * gridDim.x + blockIdx.x;
-    for (int i = b * 256 + threadIdx.x; i < n_zero; i += nb * 256) zero[i] = 0;
-  }
   const int warp = threadIdx.x / 32;
   const int e = blockIdx.x * 8 + warp;
   const int t0 = blockIdx.y * TB;
@@ -94,21 +88,20 @@ __global__ void __launch_bounds__(256) router_few_tokens_kernel(const T* __restr
 
 template <int TB>
 static moe_status_t launch_few(const moe_config_t& c, const void* x, const void* Wg,
-                               float* logits, cudaStream_t s, int* zero, int n_zero) {
+                               float* logits, cudaStream_t s) {
   dim3 grid(ceil_div(c.E, 8), ceil_div(c.T, TB));
   if (c.dtype == MOE_F32)
     return launch_k(router_few_tokens_kernel<float, TB>, grid, dim3(256), 0, s, (const float*)x,
-                    (const float*)Wg, logits, c.T, c.H, c.E, zero, n_zero);
+                    (const float*)Wg, logits, c.T, c.H, c.E);
   return launch_k(router_few_tokens_kernel<__nv_bfloat16, TB>, grid, dim3(256), 0, s,
-                  (const __nv_bfloat16*)x, (const __nv_bfloat16*)Wg, logits, c.T, c.H, c.E, zero,
-                  n_zero);
+                  (const __nv_bfloat16*)x, (const __nv_bfloat16*)Wg, logits, c.T, c.H, c.E);
 }
 
 moe_status_t launch_router_few_tokens(const moe_config_t& c, const void* x, const void* Wg,
-                                      float* logits, cudaStream_t s, int* zero, int n_zero) {
-  if (c.T <= 1) return launch_few<1>(c, x, Wg, logits, s, zero, n_zero);
-  if (c.T <= 8) return launch_few<8>(c, x, Wg, logits, s, zero, n_zero);
-  return launch_few<16>(c, x, Wg, logits, s, zero, n_zero);
+                                      float* logits, cudaStream_t s) {
+  if (c.T <= 1) return launch_few<1>(c, x, Wg, logits, s);
+  if (c.T <= 8) return launch_few<8>(c, x, Wg, logits, s);
+  return launch_few<16>(c, x, Wg, logits, s);
 }
 
 moe_status_t launch_router_simt(const moe_config_t& c, const void* x, const void* Wg,

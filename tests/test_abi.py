@@ -155,23 +155,3 @@ def test_fp8_weight_config_checks(L):
         with pytest.raises(L.MoeError) as ei:
             L.moe_workspace_size(cfg)
         assert ei.value.status == want
-
-
-def test_one_launch_decode_applies(L):
-    """Which configurations moe_forward runs as the router GEMM plus one decode kernel: at most
-    32 routed slots, and at most 2 tokens with bf16 expert weights or 8 with FP8 ones (host
-    arithmetic only)."""
-    mk = lambda T, k=4, E=128, n_shared=0, dt=None: L.make_config(  # noqa: E731
-        T, 2880, 2880, E, k, L.MOE_BF16 if dt is None else dt, n_shared=n_shared)
-    assert L.moe_decode_one_launch(mk(1)) == 1 and L.moe_decode_one_launch(mk(2)) == 1
-    assert L.moe_decode_one_launch(mk(3)) == 0           # tensor cores from 3 tokens
-    assert L.moe_decode_one_launch(mk(2, k=16)) == 1     # 32 slots
-    assert L.moe_decode_one_launch(mk(2, k=16, n_shared=1)) == 0   # 34 slots
-    assert L.moe_decode_one_launch(mk(1, dt=L.MOE_F32)) == 0
-    fp8 = lambda T: L.make_config(T, 2880, 2880, 128, 4, L.MOE_BF16,  # noqa: E731
-                                  w13_scale=16, w2_scale=16)
-    assert L.moe_decode_one_launch(fp8(1)) == 1 and L.moe_decode_one_launch(fp8(8)) == 1
-    assert L.moe_decode_one_launch(fp8(9)) == 0       # 36 slots
-    # the workspace holds the decode kernel's sync words (2 + H/2 ints) in its split-K slice
-    lay = L.moe_workspace_layout(mk(1))
-    assert lay.total - lay.splitk >= 4 * (2 + 2880 // 2)
