@@ -21,42 +21,46 @@ namespace moe {
 namespace gv {
 
 // GEMM2 with the combine: every item (tile, column pair) arrives once on its pair's counter,
-// after one fence for all of the warp's y columns; the arrival that completes a pair (one
-// per tile of the table) adds, for every token, its slots j = 0..k-1 in order (slots whose
-// expert is mapped to another device skipped) into those two columns of out, and zeroes
-// the counter again. Same sums, in the same order, as the separate combine kernels.
+// after one fence for all of the warp's y columns (the lanes of the warp arrive for up to 32
+// items at once, so the round trips overlap); the arrival that completes a pair (one per
+// tile of the table) adds, for every token, its slots j = 0..k-1 in order (slots whose expert
+// is mapped to another device skipped) into those two columns of out, and zeroes the counter
+// again. Same sums, in the same order, as the separate combine kernels.
 __device__ __noinline__ void combine_arrivals(const Params& P, int num_m, int cols, int w_begin,
                                               int w_end) {
   const int lane = threadIdx.x % 32;
   if (w_begin >= w_end) return;
   __threadfence();
   __syncwarp();
-  for (int w = w_begin; w < w_end; ++w) {
-    const int c = w % cols, n0 = 2 * c;
-    int prev = 0;
-    if (lane == 0) prev = atomicAdd(&P.cnt[c], 1);
-    prev = __shfl_sync(0xffffffffu, prev, 0);
-    if (prev != num_m - 1) continue;
-    __threadfence();
-    for (int tok = lane; tok < P.T; tok += 32) {
-      float a0 = 0.f, a1 = 0.f;
-      for (int j = 0; j < P.k; ++j) {
-        const int r = tok * P.k + j;
-        if (P.map) {
-          const int e = P.topk_ids[r];
-          if (e < 0 || e >= P.E_map || P.map[e] < 0) continue;
+  // up to 32 items a round, one arrival per lane, all in flight together
+  for (int w0 = w_begin; w0 < w_end; w0 += 32) {
+    const int w = w0 + lane;
+    bool last = false;
+    if (w < w_end) last = atomicAdd(&P.cnt[w % cols], 1) == num_m - 1;
+    unsigned todo = __ballot_sync(0xffffffffu, last);
+    if (todo) __threadfence();
+    while (todo) {
+      const int src = __ffs(todo) - 1;
+      todo &= todo - 1;
+      const int c = (w0 + src) % cols, n0 = 2 * c;
+      for (int tok = lane; tok < P.T; tok += 32) {
+        float a0 = 0.f, a1 = 0.f;
+        for (int j = 0; j < P.k; ++j) {
+          const int r = tok * P.k + j;
+          if (P.map) {
+            const int e = P.topk_ids[r];
+            if (e < 0 || e >= P.E_map || P.map[e] < 0) continue;
+          }
+          const uint32_t v = __ldcg(reinterpret_cast<const unsigned*>(
+              reinterpret_cast<const uint8_t*>(P.out) + ((size_t)r * P.N + n0) * 2));
+          a0 += bf_lo(v);
+          a1 += bf_hi(v);
         }
-        const uint32_t v =
-            __ldcg(reinterpret_cast<const unsigned*>(reinterpret_cast<const uint8_t*>(P.out) +
-                                                     ((size_t)r * P.N + n0) * 2));
-        a0 += bf_lo(v);
-        a1 += bf_hi(v);
+        *reinterpret_cast<uint32_t*>(reinterpret_cast<uint8_t*>(P.comb_out) +
+                                     ((size_t)tok * P.N + n0) * 2) = pack_bf16x2(a0, a1);
       }
-      *reinterpret_cast<uint32_t*>(reinterpret_cast<uint8_t*>(P.comb_out) +
-                                   ((size_t)tok * P.N + n0) * 2) = pack_bf16x2(a0, a1);
+      if (lane == 0) P.cnt[c] = 0;  // zero again for the next launch
     }
-    __syncwarp();
-    if (lane == 0) P.cnt[c] = 0;  // zero again for the next launch
   }
 }
 
