@@ -463,12 +463,11 @@ def measure_layer(args, wl, ctx, seed, steps, warmup, shared=0, fp8=False, ep_ha
     # kernels moe_forward enqueues: router GEMM + top-k, align (one kernel up to 4096 rows,
     # else three; up to 8 tokens top-k and align are one kernel), expert map (applied by the
     # routing kernel of batches of at most 32 slots), row gather (bf16 tensor-core path),
-    # GEMM1, GEMM2 (each + a counter-zeroing kernel when split along K) and the combine (inside
-    # the small-batch GEMM2 for batches of at most 32 slots)
+    # GEMM1, GEMM2 (each + a counter-zeroing kernel when split along K) and the combine
     tiny = T <= 8 and T * k <= 32
     routing_launches = 2 if (T <= 8 and T * k <= 4096) else 2 + (1 if T * k <= 4096 else 3)
     launches_per_step = routing_launches + (1 if (emap is not None and not tiny) else 0) + \
-        (1 if gathered else 0) + 3 - (1 if (tiny and small) else 0) + \
+        (1 if gathered else 0) + 3 + \
         (0 if small else sum(1 for g in (1, 2) if split_ws_bytes(L, cfg, B, g) > 0))
 
     for _ in range(max(3, warmup)):

@@ -310,9 +310,8 @@ moe_status_t moe_masked_forward(const moe_config_t* cfg, const void* x_masked,
 /* The whole layer: route -> align (-> expert map) -> GEMM1+SwiGLU -> GEMM2 -> combine, all
  * enqueued on `stream` with no host round-trip. ws must hold moe_workspace_size(cfg) bytes, 256-byte
  * aligned; its intermediates sit at moe_workspace_layout(cfg) offsets. Decode batches (at most
- * 8 tokens and 32 routed slots) take top-k and the table from one small CTA; when their
- * grouped GEMMs are the small-batch kernels, the combine runs inside GEMM2 (counters in the
- * workspace's split-K slice). The results are those of the separate entry points. */
+ * 8 tokens and 32 routed slots) take top-k and the table (expert map applied) from one small
+ * CTA. The results are those of the separate entry points. */
 moe_status_t moe_forward(const moe_config_t* cfg, const void* x, const void* Wg,
                          const void* W13, const void* W2, void* out, void* ws,
                          size_t ws_bytes, cudaStream_t stream);

@@ -473,8 +473,7 @@ template <int MPL>
 __global__ void __launch_bounds__(kTinyThreads) topk_table_tiny_kernel(
     const TopkArgs a, int32_t* __restrict__ ids, float* __restrict__ w, int n, int E_eff, int B,
     int max_padded, int32_t* __restrict__ sorted_ids, int32_t* __restrict__ expert_ids,
-    int32_t* npp, int32_t* counts, const int32_t* __restrict__ map, int* __restrict__ zero,
-    int n_zero) {
+    int32_t* npp, int32_t* counts, const int32_t* __restrict__ map) {
   __shared__ float skey[kTopkWarps][512];
   __shared__ int32_t ids_s[kTinyRows];
   __shared__ float w_s[kTinyRows];
@@ -483,7 +482,6 @@ __global__ void __launch_bounds__(kTinyThreads) topk_table_tiny_kernel(
   pdl_wait();
   pdl_trigger();
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
-  for (int i = threadIdx.x; i < n_zero; i += blockDim.x) zero[i] = 0;
   if (warp < a.Tn)
     topk_token<MPL>(a.logits, warp, a.E, a.k, a.mode, a.renorm, a.scale, a.n_group, a.topk_group,
                     a.logit_bias, a.select_bias, a.n_shared, ids_s, w_s, skey[warp]);
@@ -543,14 +541,14 @@ bool topk_table_tiny_fits(const moe_config_t& c) {
 moe_status_t launch_topk_table_tiny(const moe_config_t& c, const float* logits, int32_t* ids,
                                     float* w, int B, int max_padded, int32_t* sorted_ids,
                                     int32_t* expert_ids, int32_t* npp, int32_t* counts,
-                                    int* zero, int n_zero, cudaStream_t s) {
+                                    cudaStream_t s) {
   if (!topk_table_tiny_fits(c) || !counts) return MOE_ERR_UNSUPPORTED;
   const int kk = c.k + c.n_shared, E_eff = c.E + c.n_shared;
   const TopkArgs a{logits, c.T, c.E, c.k, (int)c.mode, c.renormalize, c.scale, c.n_group,
                    c.topk_group, c.logit_bias, c.select_bias, c.n_shared};
   auto run = [&](auto kern) {
     return launch_k(kern, dim3(1), dim3(kTinyThreads), 0, s, a, ids, w, c.T * kk, E_eff, B,
-                    max_padded, sorted_ids, expert_ids, npp, counts, c.expert_map, zero, n_zero);
+                    max_padded, sorted_ids, expert_ids, npp, counts, c.expert_map);
   };
   switch (topk_per_lane(c.E)) {
     case 4: return run(topk_table_tiny_kernel<4>);

@@ -100,18 +100,6 @@ moe_status_t align_check_args(const int32_t* topk_ids, int T, int k, int E, int 
   return MOE_OK;
 }
 
-// Decode batches whose routing fits one small CTA and whose grouped GEMMs run on CUDA cores:
-// moe_forward then runs the combine inside the small-batch GEMM2 (its counters live in the
-// workspace's split-K slice, which that path does not use otherwise).
-static bool decode_combine_fused(const moe_config_t& c) {
-  const moe_config_t e = effective(&c);
-  return c.dtype == MOE_BF16 && topk_table_tiny_fits(c) &&
-         gemv_applies(e, (int)moe_max_padded_rows(e.T, e.k, e.E, block_m_for(e.dtype)));
-}
-static size_t combine_counter_bytes(const moe_config_t& c) {
-  return align_up((size_t)(c.H / 2) * sizeof(int), 256);
-}
-
 }  // namespace moe
 
 using namespace moe;
@@ -186,9 +174,7 @@ moe_status_t moe_workspace_layout(const moe_config_t* cfg, moe_ws_layout_t* L) {
   L->act = take(mp * c->I * es);
   L->xs = take(gather_bytes(c, B));
   L->y = take(n * c->H * es);
-  // split-K scratch of the grouped GEMMs, or the combine counters of the decode path
-  L->splitk = take(std::max({split_bytes(1, c, B), split_bytes(2, c, B),
-                             decode_combine_fused(*cfg) ? combine_counter_bytes(*cfg) : 0}));
+  L->splitk = take(std::max(split_bytes(1, c, B), split_bytes(2, c, B)));
   L->total = off;
   L->block_m = B;
   L->max_padded = (int)mp;
@@ -536,15 +522,12 @@ moe_status_t moe_forward(const moe_config_t* c, const void* x, const void* Wg, c
   int32_t* counts = (int32_t*)(b + L.counts);
   const moe_config_t e = effective(c);  // shared experts as ordinary slots / experts
   const bool tiny = topk_table_tiny_fits(*c);
-  // decode batches on the small-batch GEMMs: the combine runs inside GEMM2, on counters the
-  // routing kernel zeroes
-  int* cnt = decode_combine_fused(*c) ? (int*)(b + L.splitk) : nullptr;
   if (tiny) {
     // at most 32 routed slots: router GEMM, then top-k and the table (expert map applied) in
     // one small CTA
     if ((st = router_logits(c, x, Wg, logits, stream)) != MOE_OK) return st;
     if ((st = launch_topk_table_tiny(*c, logits, ids, w, L.block_m, L.max_padded, sid, eid, npp,
-                                     counts, cnt, cnt ? c->H / 2 : 0, stream)) != MOE_OK)
+                                     counts, stream)) != MOE_OK)
       return st;
   } else if (topk_align_fits(*c)) {
     // decode-sized batch: router GEMM, then top-k and the align table in one CTA (the same
@@ -578,11 +561,6 @@ moe_status_t moe_forward(const moe_config_t* c, const void* x, const void* Wg, c
   } else if ((st = moe_expert_gemm1(c, x, W13, sid, eid, npp, L.block_m, b + L.act, nullptr, 0,
                                     stream)) != MOE_OK) {
     return st;
-  }
-  if (cnt) {
-    if (!aligned16(out)) return MOE_ERR_INVALID_ARG;
-    return launch_gemv2_combine(e, b + L.act, W2, sid, eid, npp, L.block_m, w, b + L.y, ids, cnt,
-                                out, stream);
   }
   if ((st = moe_expert_gemm2(c, b + L.act, W2, sid, eid, npp, L.block_m, w, b + L.y,
                              b + L.splitk, L.total - L.splitk, stream)) != MOE_OK)

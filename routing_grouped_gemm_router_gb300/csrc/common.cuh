@@ -87,13 +87,12 @@ moe_status_t launch_topk_align_small(const moe_config_t& c, const float* logits,
                                      cudaStream_t s);
 // Decode batches of at most 32 routed slots: top-k and the table from one warp per token and
 // one lane per slot, with cfg.expert_map applied to the tile labels, in one small CTA
-// (align.cu); it also zeroes n_zero ints at zero (the combine counters of the small-batch
-// GEMM2 that follows it in moe_forward).
+// (align.cu).
 bool topk_table_tiny_fits(const moe_config_t& c);
 moe_status_t launch_topk_table_tiny(const moe_config_t& c, const float* logits, int32_t* ids,
                                     float* w, int B, int max_padded, int32_t* sorted_ids,
                                     int32_t* expert_ids, int32_t* npp, int32_t* counts,
-                                    int* zero, int n_zero, cudaStream_t s);
+                                    cudaStream_t s);
 moe_status_t launch_gemm1_simt(const moe_config_t& c, const float* x, const float* W13,
                                const int32_t* sid, const int32_t* eid, const int32_t* npp,
                                int block_m, int max_padded, float* act, cudaStream_t s);
@@ -121,14 +120,6 @@ moe_status_t launch_gemv1(const moe_config_t& c, const void* a, bool gathered, c
 moe_status_t launch_gemv2(const moe_config_t& c, const void* act, const void* W2,
                           const int32_t* sid, const int32_t* eid, const int32_t* npp,
                           int block_m, const float* topk_w, void* y, cudaStream_t s);
-// The small-batch GEMM2 followed by the top-k combine in the same launch: every item
-// (tile, column pair) arrives on its pair's counter (cnt[H/2], zero at launch, left zero)
-// once the warp's y columns are visible; the last arrival adds the slots of every token
-// (skipping slots whose expert map entry is negative) into out[T, H].
-moe_status_t launch_gemv2_combine(const moe_config_t& c, const void* act, const void* W2,
-                                  const int32_t* sid, const int32_t* eid, const int32_t* npp,
-                                  int block_m, const float* topk_w, void* y,
-                                  const int32_t* topk_ids, int* cnt, void* out, cudaStream_t s);
 moe_status_t launch_gather_rows(const void* x, const int32_t* sid, const int32_t* npp,
                                 int n_rows, int k, int row_bytes, void* xs, cudaStream_t s);
 moe_status_t launch_masked_table(const int32_t* counts, int E, int C, int B, int32_t* sid,

@@ -20,50 +20,6 @@
 namespace moe {
 namespace gv {
 
-// GEMM2 with the combine: every item (tile, column pair) arrives once on its pair's counter,
-// after one fence for all of the warp's y columns (the lanes of the warp arrive for up to 32
-// items at once, so the round trips overlap); the arrival that completes a pair (one per
-// tile of the table) adds, for every token, its slots j = 0..k-1 in order (slots whose expert
-// is mapped to another device skipped) into those two columns of out, and zeroes the counter
-// again. Same sums, in the same order, as the separate combine kernels.
-__device__ __noinline__ void combine_arrivals(const Params& P, int num_m, int cols, int w_begin,
-                                              int w_end) {
-  const int lane = threadIdx.x % 32;
-  if (w_begin >= w_end) return;
-  __threadfence();
-  __syncwarp();
-  // up to 32 items a round, one arrival per lane, all in flight together
-  for (int w0 = w_begin; w0 < w_end; w0 += 32) {
-    const int w = w0 + lane;
-    bool last = false;
-    if (w < w_end) last = atomicAdd(&P.cnt[w % cols], 1) == num_m - 1;
-    unsigned todo = __ballot_sync(0xffffffffu, last);
-    if (todo) __threadfence();
-    while (todo) {
-      const int src = __ffs(todo) - 1;
-      todo &= todo - 1;
-      const int c = (w0 + src) % cols, n0 = 2 * c;
-      for (int tok = lane; tok < P.T; tok += 32) {
-        float a0 = 0.f, a1 = 0.f;
-        for (int j = 0; j < P.k; ++j) {
-          const int r = tok * P.k + j;
-          if (P.map) {
-            const int e = P.topk_ids[r];
-            if (e < 0 || e >= P.E_map || P.map[e] < 0) continue;
-          }
-          const uint32_t v = __ldcg(reinterpret_cast<const unsigned*>(
-              reinterpret_cast<const uint8_t*>(P.out) + ((size_t)r * P.N + n0) * 2));
-          a0 += bf_lo(v);
-          a1 += bf_hi(v);
-        }
-        *reinterpret_cast<uint32_t*>(reinterpret_cast<uint8_t*>(P.comb_out) +
-                                     ((size_t)tok * P.N + n0) * 2) = pack_bf16x2(a0, a1);
-      }
-      if (lane == 0) P.cnt[c] = 0;  // zero again for the next launch
-    }
-  }
-}
-
 // MODE 0: GEMM1 (item = output column n of act: gate row n, up row N + n).
 // MODE 1: GEMM2 (item = output columns n, n + 1 of y: W2 rows n, n + 1).
 // RMAX: real rows a pass takes (a tile holds at most T of them); one pass shape per kernel.
@@ -117,7 +73,6 @@ __global__ void __launch_bounds__(kThreads, (kMinCtas<MODE, FP8, RMAX>)) gemv_ke
       item_pass<MODE, FP8, RMAX, kPieces<MODE, FP8, RMAX>>(P, w0, w1, s0, s1, rl + rc, rv, n);
     }
   }
-  if (MODE == 1 && P.cnt) combine_arrivals(P, num_m, cols, w_begin, w_end);
 }
 
 template <int MODE, bool FP8, int RMAX>
@@ -191,31 +146,6 @@ moe_status_t launch_gemv1(const moe_config_t& c, const void* a, bool gathered, c
   P.N = c.I;
   P.out = act;
   return fp8 ? gv::launch_fmt<0, true>(P, c.T, s) : gv::launch_fmt<0, false>(P, c.T, s);
-}
-
-moe_status_t launch_gemv2_combine(const moe_config_t& c, const void* act, const void* W2,
-                                  const int32_t* sid, const int32_t* eid, const int32_t* npp,
-                                  int block_m, const float* topk_w, void* y,
-                                  const int32_t* topk_ids, int* cnt, void* out, cudaStream_t s) {
-  gv::Params P = gv::base_params(c, sid, eid, npp, block_m);
-  const bool fp8 = c.weight_format == MOE_WEIGHTS_FP8_E4M3_B128;
-  P.a = (const uint8_t*)act;
-  P.a_gathered = 1;
-  P.w = (const uint8_t*)W2;
-  P.scale = fp8 ? c.w2_scale : nullptr;
-  P.sc_rb = ceil_div(c.H, 128);
-  P.sc_kb = ceil_div(c.I, 128);
-  P.K = c.I;
-  P.N = c.H;
-  P.topk_w = topk_w;
-  P.out = y;
-  P.cnt = cnt;
-  P.topk_ids = topk_ids;
-  P.map = c.expert_map;
-  P.E_map = c.E;
-  P.T = c.T;
-  P.comb_out = out;
-  return fp8 ? gv::launch_fmt<1, true>(P, c.T, s) : gv::launch_fmt<1, false>(P, c.T, s);
 }
 
 moe_status_t launch_gemv2(const moe_config_t& c, const void* act, const void* W2,

@@ -35,14 +35,6 @@ struct Params {
   int block_m, n_rows, k, K, N, n_slots;
   const float* topk_w;  // GEMM2
   void* out;            // GEMM1: act [padded, N]; GEMM2: y [T*k, N] (bf16)
-  // GEMM2 with the combine in the same launch (cnt != null): per column pair arrival
-  // counters cnt[N/2] (zero at launch), the routing ids [T, k] for the expert map's skip
-  // (map [E_map] or null) and the layer output comb_out [T, N]
-  int* cnt;
-  const int32_t* topk_ids;
-  const int32_t* map;
-  int E_map, T;
-  void* comb_out;
 };
 
 // Weights are read once: no L1 allocation. EVICT_FIRST: the lines also leave L2 first (an

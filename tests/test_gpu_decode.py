@@ -1,7 +1,5 @@
 """The decode path of moe_forward: batches of at most 8 tokens and 32 routed slots take top-k
-and the align table from one small CTA (expert map applied there), and when their grouped
-GEMMs run on CUDA cores the combine runs inside GEMM2 (the last arrival on each column pair
-adds the slots).
+and the align table from one small CTA (expert map applied there).
 
 Its results must be the separate entry points' bits (same device arithmetic, same summation
 orders), its intermediates the same tables, and it must replay from a CUDA graph.
