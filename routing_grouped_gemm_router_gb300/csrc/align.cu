@@ -202,9 +202,9 @@ __global__ void __launch_bounds__(kAlignThreads) topk_align_small_kernel(
   extern __shared__ int sm[];
   const int warp = threadIdx.x / 32;
   if (warp < a.Tn)
-    topk_token<MPL>(a.logits, warp, a.E, a.k, a.mode, a.renorm, a.scale, a.n_group, a.topk_group,
-               a.logit_bias, a.select_bias, a.n_shared, ids, w,
-               reinterpret_cast<float*>(sm) + warp * 512);
+    topk_token<MPL, 4>(a.logits, warp, a.E, a.k, a.mode, a.renorm, a.scale, a.n_group,
+                       a.topk_group, a.logit_bias, a.select_bias, a.n_shared, ids, w,
+                       reinterpret_cast<float*>(sm) + warp * 512);
   __syncthreads();
   align_small_body(ids, n, E_eff, B, max_padded, sorted_ids, expert_ids, npp, counts, sm);
 }

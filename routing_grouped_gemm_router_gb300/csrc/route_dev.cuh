@@ -198,14 +198,15 @@ constexpr int kMaxPerLane = 16;  // E <= 512
 // Experts a lane holds for E router experts (4, 8 or 16): top-k loops run over that many.
 inline int topk_per_lane(int E) { return E <= 128 ? 4 : (E <= 256 ? 8 : kMaxPerLane); }
 
-// Top-k of one token, one warp (lane l holds experts l + 32*i, i < MPL, 32*MPL >= E): k
-// rounds of a warp-wide
-// argmax (larger key wins, equal keys go to the lower id) over the experts not taken yet, so
-// slot j holds the j-th largest key; then the weights of the mode (softmax over E or over
-// the k kept logits; sigmoid scores renormalised and scaled), written to row t of ids / w,
-// after which the shared experts' slots follow. skey_w: this warp's 512 floats of shared memory (used
-// by the group scores of mode 1). Logits are read from L2 (ld.global.cg).
-template <int MPL>
+// Top-k of one token, one warp (lane l holds experts l + 32*i, i < MPL, 32*MPL >= E): the k
+// largest keys (equal keys to the lower id), slot j holding the j-th, from the butterfly
+// merge when k <= KMAX (KMAX 4 or 8: the registers of the sorted lists; kernels of 1024
+// threads keep 4) and otherwise from k rounds of a warp-wide argmax over the experts not
+// taken yet; then the weights of the mode (softmax over E or over the k kept logits; sigmoid
+// scores renormalised and scaled), written to row t of ids / w, after which the shared
+// experts' slots follow. skey_w: this warp's 512 floats of shared memory (used by the group
+// scores of mode 1). Logits are read from L2 (ld.global.cg).
+template <int MPL, int KMAX = 8>
 __device__ __forceinline__ void topk_token(const float* __restrict__ logits, int t, int E, int k,
                                            int mode, int renorm, float scale, int n_group,
                                            int topk_group, const float* __restrict__ logit_bias,
@@ -269,7 +270,7 @@ __device__ __forceinline__ void topk_token(const float* __restrict__ logits, int
 
   float my_sel_val = 0.f;   // lane j keeps the value of slot j
   int my_sel_id = 0;
-  if (k <= 8) {
+  if (k <= KMAX) {
     // the k best from the warp's sorted 4 or 8 best (butterfly merge)
     auto take = [&](auto& lk, auto& li, auto& lv) {
 #pragma unroll
@@ -284,7 +285,7 @@ __device__ __forceinline__ void topk_token(const float* __restrict__ logits, int
       int li[4];
       warp_topk_sorted<MPL, 4>(key, val, E, lk, li, lv);
       take(lk, li, lv);
-    } else {
+    } else if (KMAX >= 8) {
       float lk[8], lv[8];
       int li[8];
       warp_topk_sorted<MPL, 8>(key, val, E, lk, li, lv);
@@ -295,7 +296,7 @@ __device__ __forceinline__ void topk_token(const float* __restrict__ logits, int
   bool taken[MPL];
 #pragma unroll
   for (int i = 0; i < MPL; ++i) taken[i] = false;
-  for (int j = 0; k > 8 && j < k; ++j) {
+  for (int j = 0; k > KMAX && j < k; ++j) {
     float bv = NEG;
     int be = 1 << 30;
 #pragma unroll
