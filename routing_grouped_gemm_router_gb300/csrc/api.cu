@@ -287,6 +287,8 @@ moe_status_t moe_expert_gemm1_gathered(const moe_config_t* cfg, const void* xs,
   const int mp = (int)moe_max_padded_rows(c->T, c->k, c->E, block_m);
   if (gemv_applies(*c, mp))
     return launch_gemv1(*c, xs, true, W13, sorted_ids, expert_ids, npp, block_m, act, stream);
+  if (dec_gemm_applies(*c, mp))
+    return launch_gemm1_dec(*c, xs, W13, sorted_ids, expert_ids, npp, block_m, mp, act, stream);
   return launch_gemm1_tc(*c, xs, W13, sorted_ids, expert_ids, npp, block_m, mp, act, ws,
                          ws_bytes, stream);
 }
@@ -345,6 +347,9 @@ moe_status_t moe_expert_gemm2(const moe_config_t* cfg, const void* act, const vo
     if (need && (!ws || ws_bytes < need || ((uintptr_t)ws & 255u))) return MOE_ERR_WORKSPACE;
     if (gemv_applies(*c, mp))
       return launch_gemv2(*c, act, W2, sorted_ids, expert_ids, npp, block_m, topk_w, y, stream);
+    if (dec_gemm_applies(*c, mp))
+      return launch_gemm2_dec(*c, act, W2, sorted_ids, expert_ids, npp, block_m, mp, topk_w, y,
+                              stream);
     return launch_gemm2_tc(*c, act, W2, sorted_ids, expert_ids, npp, block_m, mp, topk_w, y,
                            ws, ws_bytes, stream);
   }
@@ -581,7 +586,8 @@ int moe_device_status(int reset) {
   const int g = grouped_status_read(reset);
   const int c = combine_status_read(reset);
   const int t = tiny_status_read(reset);
-  return g ? g : (r ? r : (a ? a : (t ? t : c)));
+  const int d = dec_status_read(reset);
+  return g ? g : (d ? d : (r ? r : (a ? a : (t ? t : c))));
 }
 
 }  // extern "C"

@@ -120,6 +120,18 @@ moe_status_t launch_gemv1(const moe_config_t& c, const void* a, bool gathered, c
 moe_status_t launch_gemv2(const moe_config_t& c, const void* act, const void* W2,
                           const int32_t* sid, const int32_t* eid, const int32_t* npp,
                           int block_m, const float* topk_w, void* y, cudaStream_t s);
+// Grouped GEMMs of decode-sized batches on the tensor cores with the weights as the 128-row
+// MMA operand (gemm_dec.cu): whether they apply, and the two GEMMs with the pair kernels'
+// inputs and outputs (GEMM1 reads the routed rows gathered in padded order).
+bool dec_gemm_applies(const moe_config_t& c, int max_padded);
+moe_status_t launch_gemm1_dec(const moe_config_t& c, const void* xs, const void* W13,
+                              const int32_t* sid, const int32_t* eid, const int32_t* npp,
+                              int block_m, int max_padded, void* act, cudaStream_t s);
+moe_status_t launch_gemm2_dec(const moe_config_t& c, const void* act, const void* W2,
+                              const int32_t* sid, const int32_t* eid, const int32_t* npp,
+                              int block_m, int max_padded, const float* topk_w, void* y,
+                              cudaStream_t s);
+int dec_status_read(int reset);
 moe_status_t launch_gather_rows(const void* x, const int32_t* sid, const int32_t* npp,
                                 int n_rows, int k, int row_bytes, void* xs, cudaStream_t s);
 moe_status_t launch_masked_table(const int32_t* counts, int E, int C, int B, int32_t* sid,

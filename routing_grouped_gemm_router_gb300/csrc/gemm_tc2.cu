@@ -160,29 +160,6 @@ __device__ __forceinline__ void item_of(int w, int n_tiles, const Table& tb, int
   e = tb.run_e[lo];
 }
 
-// E4M3 -> bf16 with integer operations only. An E4M3 byte s.eeee.mmm moved into the bf16
-// bit pattern s.0000eeee.mmm0000 is, read as bf16, the code's value times 2^-120, for
-// subnormal codes too (E4M3 exponent 0 lands in the bf16 subnormal range with the same
-// mantissa). The bf16 subnormals take part in the bf16 multiply below without flushing.
-// (The NaN code 0x7F is not propagated; weights hold finite codes.)
-__device__ __forceinline__ void e4m3x4_to_bf16x4_lowexp(uint32_t x, uint32_t& p01, uint32_t& p23) {
-  const uint32_t a = __byte_perm(x, 0u, 0x1404u);  // [b1 0 b0 0]
-  const uint32_t b = __byte_perm(x, 0u, 0x3424u);  // [b3 0 b2 0]
-  p01 = (a & 0x80008000u) | ((a & 0x7F007F00u) >> 4);
-  p23 = (b & 0x80008000u) | ((b & 0x7F007F00u) >> 4);
-}
-__device__ __forceinline__ uint32_t bf16x2_mul(uint32_t a, uint32_t b) {
-  uint32_t d;
-  asm("mul.rn.bf16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
-  return d;
-}
-// General scale: exact fp32 products, one rounding to bf16.
-__device__ __forceinline__ uint32_t bf16x2_lowexp_scale_f32(uint32_t p, float sc) {
-  const float lo = __uint_as_float(p << 16) * 0x1p120f;
-  const float hi = __uint_as_float(p & 0xFFFF0000u) * 0x1p120f;
-  return pack_bf16(lo * sc, hi * sc);
-}
-
 // Work item w of a launch split ksplit ways along K -> base item and its k-block range.
 __device__ __forceinline__ void split_of(int w, int ksplit, int num_kb, int& wi, int& kb0,
                                          int& kb1, int& sp) {

@@ -249,6 +249,15 @@ __device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&r)[32]) {
         "=r"(r[31])
       : "r"(taddr));
 }
+__device__ __forceinline__ void tmem_ld16(uint32_t taddr, uint32_t (&r)[16]) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, "
+      "%11, %12, %13, %14, %15}, [%16];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+        "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]),
+        "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
+      : "r"(taddr));
+}
 __device__ __forceinline__ void tmem_ld_wait() {
   asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
 }
@@ -274,6 +283,51 @@ __host__ __device__ constexpr uint32_t idesc_bf16(int M, int N) {
 __device__ __forceinline__ uint32_t pack_bf16(float a, float b) {
   __nv_bfloat162 h = __floats2bfloat162_rn(a, b);
   return *reinterpret_cast<uint32_t*>(&h);
+}
+
+// ------------------------------------------------------------------- FP8 E4M3 weights
+// E4M3 -> bf16 with integer operations only. An E4M3 byte s.eeee.mmm moved into the bf16
+// bit pattern s.0000eeee.mmm0000 is, read as bf16, the code's value times 2^-120, for
+// subnormal codes too (E4M3 exponent 0 lands in the bf16 subnormal range with the same
+// mantissa). The bf16 subnormals take part in the bf16 multiply below without flushing.
+// (The NaN code 0x7F is not propagated; weights hold finite codes.)
+__device__ __forceinline__ void e4m3x4_to_bf16x4_lowexp(uint32_t x, uint32_t& p01, uint32_t& p23) {
+  const uint32_t a = __byte_perm(x, 0u, 0x1404u);  // [b1 0 b0 0]
+  const uint32_t b = __byte_perm(x, 0u, 0x3424u);  // [b3 0 b2 0]
+  p01 = (a & 0x80008000u) | ((a & 0x7F007F00u) >> 4);
+  p23 = (b & 0x80008000u) | ((b & 0x7F007F00u) >> 4);
+}
+__device__ __forceinline__ uint32_t bf16x2_mul(uint32_t a, uint32_t b) {
+  uint32_t d;
+  asm("mul.rn.bf16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+  return d;
+}
+// General scale: exact fp32 products, one rounding to bf16.
+__device__ __forceinline__ uint32_t bf16x2_lowexp_scale_f32(uint32_t p, float sc) {
+  const float lo = __uint_as_float(p << 16) * 0x1p120f;
+  const float hi = __uint_as_float(p & 0xFFFF0000u) * 0x1p120f;
+  return pack_bf16(lo * sc, hi * sc);
+}
+
+// Sixteen E4M3 codes (raw bytes) times their block scale sc, as eight packed bf16 pairs: the
+// operand a bf16 MMA reads in place of the weights. A power-of-two scale below 2^8 (or 0)
+// times 2^120 is an exact bf16, so one packed bf16 multiply per two weights is exact; any
+// other scale takes exact fp32 products and one rounding.
+__device__ __forceinline__ void e4m3x16_scaled_bf16(const uint4& q, float sc, uint32_t (&v)[8]) {
+  const float scb = sc * 0x1p120f;
+  const bool fast = (__float_as_uint(sc) & 0x807FFFFFu) == 0 && sc < 0x1p8f;
+  const uint32_t sc2 = (__float_as_uint(scb) >> 16) * 0x10001u;
+  e4m3x4_to_bf16x4_lowexp(q.x, v[0], v[1]);
+  e4m3x4_to_bf16x4_lowexp(q.y, v[2], v[3]);
+  e4m3x4_to_bf16x4_lowexp(q.z, v[4], v[5]);
+  e4m3x4_to_bf16x4_lowexp(q.w, v[6], v[7]);
+  if (fast) {
+#pragma unroll
+    for (int i = 0; i < 8; ++i) v[i] = bf16x2_mul(v[i], sc2);
+  } else {
+#pragma unroll
+    for (int i = 0; i < 8; ++i) v[i] = bf16x2_lowexp_scale_f32(v[i], sc);
+  }
 }
 
 // ------------------------------------------------------------------- host: tensor maps
