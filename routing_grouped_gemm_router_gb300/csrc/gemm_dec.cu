@@ -65,12 +65,11 @@ struct Cfg {
   static constexpr int NA = MODE == kGemm1 ? 2 : 1;  // weight blocks per k-block (gate, up)
   static constexpr int OP_BYTES = NA * A_BYTES + X_BYTES;
   static constexpr int RAWS_BYTES = NA * RAW_BYTES;
-  static constexpr int kOpStages = FP8 ? (MODE == kGemm1 ? 2 : 3) : (MODE == kGemm1 ? 4 : 6);
-  static constexpr int kRawStages = FP8 ? (MODE == kGemm1 ? 6 : 10) : 0;
+  static constexpr int kOpStages = FP8 ? (MODE == kGemm1 ? 3 : 4) : (MODE == kGemm1 ? 4 : 6);
+  static constexpr int kRawStages = FP8 ? (MODE == kGemm1 ? 4 : 10) : 0;
   static constexpr int kCvtWarps = 4;
   static constexpr int kThreads = (6 + (FP8 ? kCvtWarps : 0)) * 32;
   static constexpr uint32_t kTmemCols = 2u * NA * 128u;  // two accumulators of NA x 128 columns
-  static constexpr uint32_t IDESC = idesc_bf16(128, 128);
   // shared memory (offsets from a 1024-aligned base)
   static constexpr size_t op = 0;
   static constexpr size_t raw = op + (size_t)kOpStages * OP_BYTES;
@@ -201,12 +200,26 @@ __global__ void __launch_bounds__(Cfg<MODE, FP8>::kThreads, 1)
     __syncwarp();
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer (one lane)
-    if (lane == 0) {
-      int g = 0, acc = 0;
-      uint32_t acc_phase = 0;
-      bool ok = true, issued = false;
-      for (int w = blockIdx.x; w < total && ok; w += gridDim.x) {
-        if (!wait_bounded(&tempty[acc], acc_phase ^ 1u, abort_flag, status)) break;
+    // The MMA's N covers the tile's rows up to its last real one (rounded up to 16): at decode
+    // a tile holds a few real rows, and the columns past them would only cost tensor time.
+    int g = 0, acc = 0;
+    uint32_t acc_phase = 0;
+    bool ok = true, issued = false;
+    for (int w = blockIdx.x; w < total && ok; w += gridDim.x) {
+      const int t = tl[w / P.m_blocks];
+      int last = -1;  // the tile's last real row (sorted_ids needs only 4-byte alignment)
+#pragma unroll
+      for (int i = 0; i < 4; ++i)
+        if (P.sid[t * 128 + i * 32 + lane] < P.n_rows) last = i * 32 + lane;
+#pragma unroll
+      for (int off = 16; off > 0; off >>= 1) last = max(last, __shfl_xor_sync(0xffffffffu, last, off));
+      const int n_cols = last < 16 ? 16 : (last + 16) / 16 * 16;
+      const uint32_t idesc = idesc_bf16(128, n_cols);
+      if (lane == 0) {
+        if (!wait_bounded(&tempty[acc], acc_phase ^ 1u, abort_flag, status)) ok = false;
+      }
+      if (!__shfl_sync(0xffffffffu, (int)ok, 0)) break;
+      if (lane == 0) {
         tc_fence_after();
         const uint32_t d = tmem_base + (uint32_t)(acc * NA * 128);
         for (int kb = 0; kb < num_kb; ++kb, ++g) {
@@ -223,18 +236,18 @@ __global__ void __launch_bounds__(Cfg<MODE, FP8>::kThreads, 1)
 #pragma unroll
             for (int a = 0; a < NA; ++a)
               umma_bf16<1>(d + a * 128, sw128_desc(base + a * A_BYTES + kk * 32),
-                           sw128_desc(xb + kk * 32), C::IDESC, (kb | kk) != 0 ? 1u : 0u);
+                           sw128_desc(xb + kk * 32), idesc, (kb | kk) != 0 ? 1u : 0u);
           umma_commit<1>(&opempty[s]);
           issued = true;
         }
-        if (!ok) break;
-        umma_commit<1>(&tfull[acc]);
-        if (++acc == 2) { acc = 0; acc_phase ^= 1u; }
+        if (ok) umma_commit<1>(&tfull[acc]);
       }
-      if (issued) {  // every MMA of this thread finished before TMEM is freed
-        umma_commit<1>(drain);
-        wait_bounded(drain, 0, abort_flag, status);
-      }
+      if (!__shfl_sync(0xffffffffu, (int)ok, 0)) break;
+      if (++acc == 2) { acc = 0; acc_phase ^= 1u; }
+    }
+    if (lane == 0 && issued) {  // every MMA of this thread finished before TMEM is freed
+      umma_commit<1>(drain);
+      wait_bounded(drain, 0, abort_flag, status);
     }
     __syncwarp();
   } else if (warp < 6) {
