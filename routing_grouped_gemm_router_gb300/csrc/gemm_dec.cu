@@ -315,14 +315,26 @@ __global__ void __launch_bounds__(Cfg<MODE, FP8>::kThreads, 1)
       const int t = tl[w / P.m_blocks], j = w % P.m_blocks;
       const int e = P.eid[(t * 128) / P.block_m];
       const bool sc_ok = e >= 0 && e < P.n_slots && j < P.sc_rb;
+      // block scales of this item in windows of 32 k-block pairs: lane i holds the scale of
+      // 128-wide k-block win + i of each weight block, so a k-block's scale is a shuffle, not
+      // a global load on the critical path (the raw codes are usually waiting already)
+      float scw[NA];
+      int win = -32;
       for (int kb = 0; kb < num_kb; ++kb, ++g) {
         const int r = g % R, s = g % S;
+        const int sb = kb >> 1;
+        if (sb - win >= 32) {
+          win = sb & ~31;
+#pragma unroll
+          for (int a = 0; a < NA; ++a)
+            scw[a] = sc_ok && win + lane < P.sc_kb
+                         ? __ldg(P.scale + (((int64_t)e * NA + a) * P.sc_rb + j) * P.sc_kb +
+                                 win + lane)
+                         : 0.f;
+        }
         float sc[NA];
 #pragma unroll
-        for (int a = 0; a < NA; ++a)  // in flight during the waits
-          sc[a] = sc_ok ? __ldg(P.scale + (((int64_t)e * NA + a) * P.sc_rb + j) * P.sc_kb +
-                                (kb >> 1))
-                        : 0.f;
+        for (int a = 0; a < NA; ++a) sc[a] = __shfl_sync(0xffffffffu, scw[a], sb - win);
         int okw = 1;
         if (lane == 0) {
           okw = wait_bounded(&opempty[s], ((uint32_t)(g / S) & 1u) ^ 1u, abort_flag, status) &&
