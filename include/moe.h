@@ -143,7 +143,7 @@ const char* moe_status_string(moe_status_t s);
 int moe_block_m(const moe_config_t* cfg);
 
 /* 1 when the grouped GEMMs of this configuration run as the small-batch kernels (bf16
- * layers of at most 2 tokens, or at most 32 with FP8 expert weights; see
+ * layers of at most 2 tokens, or at most 12 with FP8 expert weights; see
  * moe_expert_gemm1), 0 otherwise or on bad args. Host arithmetic only. */
 int moe_small_batch(const moe_config_t* cfg);
 
@@ -212,13 +212,20 @@ moe_status_t moe_apply_expert_map(int32_t* expert_ids, int num_tiles, const int3
  * gathered into padded order in ws (moe_expert_gemm1_workspace_size bytes, 256-byte
  * aligned), then multiplied on the tensor cores; fp32 gathers inside the GEMM.
  *
- * Split-K (all bf16 grouped GEMMs): when T*k is so small that the (m-tile pair, n-tile)
- * work items cannot fill the GPU twice over (decode), each item is split along K; the
- * splits write fp32 partial sums to the GEMM's workspace and the last split of a tile adds
- * them in split order and applies the epilogue (deterministic). The workspace sizes below
- * include that scratch; it depends only on cfg and block_m.
+ * Split-K (bf16 grouped GEMMs of more than 128 tokens): when T*k is so small that the
+ * (m-tile pair, n-tile) work items cannot fill the GPU twice over, each item is split along
+ * K; the splits write fp32 partial sums to the GEMM's workspace and the last split of a
+ * tile adds them in split order and applies the epilogue (deterministic). The workspace
+ * sizes below include that scratch; it depends only on cfg and block_m.
  *
- * Small batches (moe_small_batch(cfg) = 1: bf16 layers of at most 2 tokens, 32 with FP8
+ * Decode batches (bf16 activations, at most 128 tokens, not small): both grouped GEMMs run
+ * on the tensor cores with the expert weights as the 128-row MMA operand and each tile's
+ * token rows, up to its last real one, as the other; one work item is (tile, 128 output
+ * columns), one CTA per SM streams the weights. FP8 weights are turned into bf16 (code times
+ * block scale) in shared memory on the way. Results agree with the larger-batch kernels to
+ * within rounding (the same products, summed in another order), bit for bit from run to run.
+ *
+ * Small batches (moe_small_batch(cfg) = 1: bf16 layers of at most 2 tokens, 12 with FP8
  * weights): a tile then holds a few
  * real rows, and both grouped GEMMs run on CUDA cores as one pass over the active experts'
  * weights, fp32 products of the same operands summed in another order than the tensor-core

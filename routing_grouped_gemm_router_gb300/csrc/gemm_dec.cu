@@ -19,14 +19,26 @@
 // accumulators, so the thread of TMEM lane m holds gate and up of column m for every tile row.
 // The epilogue reads the tile's sorted_ids and stores only the real rows.
 //
-// FP8 E4M3 weights (128 x 128 block scales): the producer streams raw codes into a ring of
-// their own, several k-blocks deep; four converter warps turn each k-block into the bf16
-// operand (code * scale, exact for power-of-two scales) in a shallower operand ring, all
-// with CTA-local barriers.
+// The tile rows are loaded only up to the tile's last real row (16-row boxes): at decode a
+// tile holds a few tokens, and the MMA's N is cut to the same width.
 //
-// Warp roles: 0 TMA producer, 1 MMA issuer (one lane), 2-5 epilogue, 6-9 converters (FP8).
+// FP8 E4M3 weights (128 x 128 block scales): the producer streams raw codes into a ring of
+// their own, several k-blocks deep; eight converter warps turn each k-block into the bf16
+// operand (code * scale, exact for power-of-two scales) in a shallower operand ring, and a
+// warp of its own streams the tile rows into a third ring, all with CTA-local barriers.
+// Measured per k-block (timestamps in the kernel): the raw codes wait long before they are
+// needed, so conversion and the tile rows set the pace. Each lane therefore loads all of its
+// codes of a k-block before it stores any converted operand (the stores could otherwise
+// alias the next loads, which serialises them), and the tile rows are requested several
+// k-blocks ahead instead of when an operand slot frees (behind the weight copies in flight,
+// that cost about a microsecond per k-block).
+//
+// Warp roles: 0 TMA producer (weights; bf16 also the tile rows), 1 MMA issuer (one lane),
+// 2-5 epilogue; FP8 adds 8 converters on warps 6-15 and the tile-row producer on warp 16.
 // Every mbarrier wait is bounded (time-out: status kStatusTimeout, abort, copies in flight
-// drained, TMEM freed).
+// drained, TMEM freed). All roles but the MMA issuer wait with a suspend hint: measured (ncu),
+// the polling of the waiting warps took about half of all issue slots of the FP8 variant,
+// away from the converters.
 #include "tc_ptx.cuh"
 
 namespace moe {
@@ -41,6 +53,7 @@ constexpr int kMaxTokens = 128;       // batches this kernel takes (see dec_gemm
 constexpr int kMaxTiles = 1024;       // 128-row tiles of the table a launch may hold
 constexpr int A_BYTES = 128 * 128;    // 128 weight rows x 64 bf16 (one swizzled k-block)
 constexpr int X_BYTES = 128 * 128;    // 128 tile rows x 64 bf16
+constexpr int X_BOX = 16;             // tile rows per TMA box (2 KB, 1024-byte aligned)
 constexpr int RAW_BYTES = 128 * BK;   // 128 weight rows x 64 E4M3 codes
 
 struct Params {
@@ -63,31 +76,72 @@ struct Params {
 template <int MODE, bool FP8>
 struct Cfg {
   static constexpr int NA = MODE == kGemm1 ? 2 : 1;  // weight blocks per k-block (gate, up)
-  static constexpr int OP_BYTES = NA * A_BYTES + X_BYTES;
+  static constexpr int OP_BYTES = NA * A_BYTES + (FP8 ? 0 : X_BYTES);
   static constexpr int RAWS_BYTES = NA * RAW_BYTES;
   static constexpr int kOpStages = FP8 ? (MODE == kGemm1 ? 3 : 4) : (MODE == kGemm1 ? 4 : 6);
-  static constexpr int kRawStages = FP8 ? (MODE == kGemm1 ? 4 : 10) : 0;
-  static constexpr int kCvtWarps = 4;
-  static constexpr int kThreads = (6 + (FP8 ? kCvtWarps : 0)) * 32;
+  static constexpr int kRawStages = FP8 ? (MODE == kGemm1 ? 6 : 12) : 0;
+  // FP8 tile-row ring: XR_BYTES split into slots of one k-block of the item's n_cols rows
+  // (n_cols * 128 bytes), at most kMaxXSlots of them (GEMM1: 8 k-blocks ahead at decode, one
+  // for a full tile; GEMM2: 24 and 3)
+  static constexpr int XR_BYTES = FP8 ? (MODE == kGemm1 ? 16 : 48) * 1024 : 0;
+  static constexpr int kMaxXSlots = FP8 ? 32 : 0;
+  // FP8 converters: 8 warps of 16 rows each, on warps 6-8, 10-12, 14-15, so that none shares
+  // the MMA issuer's scheduler (warp 1; a warp runs on scheduler warp % 4); warps 9 and 13
+  // have no role. Warp 16 streams the tile rows.
+  static constexpr int kCvtWarps = 8;
+  static constexpr int kXWarp = 16;
+  static constexpr int kThreads = (FP8 ? 17 : 6) * 32;
   static constexpr uint32_t kTmemCols = 2u * NA * 128u;  // two accumulators of NA x 128 columns
   // shared memory (offsets from a 1024-aligned base)
   static constexpr size_t op = 0;
   static constexpr size_t raw = op + (size_t)kOpStages * OP_BYTES;
-  static constexpr size_t bars = raw + (size_t)kRawStages * RAWS_BYTES;
-  static constexpr size_t n_bars = 2 * kOpStages + 2 * kRawStages + 5;
+  static constexpr size_t xr = raw + (size_t)kRawStages * RAWS_BYTES;
+  static constexpr size_t bars = xr + (size_t)XR_BYTES;
+  static constexpr size_t n_bars = 2 * kOpStages + 2 * kRawStages + 2 * kMaxXSlots + 5;
   static constexpr size_t misc = bars + n_bars * 8;  // tmem slot, abort flag, tile count
   static constexpr size_t tiles = misc + 16;
   static constexpr size_t end = tiles + kMaxTiles * 4;
   static constexpr size_t bytes = 1024 + end;
   // the op-stage barrier completes on: bf16, the producer's expect_tx arrival (weights and
-  // tile rows); FP8, converter warp 0's expect_tx arrival (tile rows) plus one arrival of
-  // each converter warp once its rows of the weights are written
-  static constexpr int kOpArrivals = FP8 ? 1 + kCvtWarps : 1;
+  // tile rows); FP8, one arrival of each converter warp once its rows are written
+  static constexpr int kOpArrivals = FP8 ? kCvtWarps : 1;
 };
 static_assert(Cfg<kGemm1, false>::bytes <= 232448, "shared memory");
 static_assert(Cfg<kGemm1, true>::bytes <= 232448, "shared memory");
 static_assert(Cfg<kGemm2, false>::bytes <= 232448, "shared memory");
 static_assert(Cfg<kGemm2, true>::bytes <= 232448, "shared memory");
+
+// Tile rows the MMA covers for tile t: up to its last real row (sorted_ids < T*k), rounded up
+// to 16. Warp-collective; sorted_ids needs only 4-byte alignment, so four scalar loads a lane.
+__device__ __forceinline__ int tile_cols(const Params& P, int t, int lane) {
+  int last = -1;
+#pragma unroll
+  for (int i = 0; i < 4; ++i)
+    if (P.sid[t * 128 + i * 32 + lane] < P.n_rows) last = i * 32 + lane;
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) last = max(last, __shfl_xor_sync(0xffffffffu, last, off));
+  return last < 16 ? 16 : (last + 16) / 16 * 16;
+}
+
+// Bytes of one slot of the FP8 tile-row ring for an item of n_cols tile rows (n_cols rounded
+// up to a power of two, so that the slot size changes rarely between items), and the slots.
+__device__ __forceinline__ int x_slot_bytes(int n_cols) {
+  int r = 16;
+  while (r < n_cols) r *= 2;
+  return r * 128;
+}
+template <class C>
+__device__ __forceinline__ int x_slots(int slot_bytes) {
+  return min(C::kMaxXSlots, C::XR_BYTES / slot_bytes);
+}
+
+// The tile rows [t*128, t*128 + n_cols) of k-block kb as n_cols / 16 boxes of 16 rows, laid
+// out as the first n_cols rows of a 128-row swizzled block.
+__device__ __forceinline__ void load_tile_rows(uint8_t* dst, const CUtensorMap* tm, uint64_t* bar,
+                                               int kb, int t, int n_cols) {
+  for (int c = 0; c < n_cols / X_BOX; ++c)
+    tma_2d(dst + c * X_BOX * 128, tm, bar, kb * BK, t * 128 + c * X_BOX);
+}
 
 template <int MODE, bool FP8>
 __global__ void __launch_bounds__(Cfg<MODE, FP8>::kThreads, 1)
@@ -97,6 +151,7 @@ __global__ void __launch_bounds__(Cfg<MODE, FP8>::kThreads, 1)
   constexpr int NA = C::NA;
   constexpr int S = C::kOpStages;
   constexpr int R = C::kRawStages;
+  constexpr int SX = C::kMaxXSlots;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = (uint8_t*)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
   uint64_t* bars = (uint64_t*)(smem + C::bars);
@@ -104,7 +159,9 @@ __global__ void __launch_bounds__(Cfg<MODE, FP8>::kThreads, 1)
   uint64_t* opempty = bars + S;
   uint64_t* rawfull = bars + 2 * S;
   uint64_t* rawempty = rawfull + R;
-  uint64_t* tfull = rawempty + R;
+  uint64_t* xfull = rawempty + R;
+  uint64_t* xempty = xfull + SX;
+  uint64_t* tfull = xempty + SX;
   uint64_t* tempty = tfull + 2;
   uint64_t* drain = tempty + 2;
   uint32_t* tmem_slot = (uint32_t*)(smem + C::misc);
@@ -123,6 +180,10 @@ __global__ void __launch_bounds__(Cfg<MODE, FP8>::kThreads, 1)
     for (int r = 0; r < R; ++r) {
       mbar_init(&rawfull[r], 1);
       mbar_init(&rawempty[r], C::kCvtWarps);
+    }
+    for (int x = 0; x < SX; ++x) {  // slots of the tile-row ring
+      mbar_init(&xfull[x], 1);
+      mbar_init(&xempty[x], 1);
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(&tfull[b], 1);
@@ -165,16 +226,17 @@ __global__ void __launch_bounds__(Cfg<MODE, FP8>::kThreads, 1)
 
   if (warp == 0) {
     // ------------------------------------------------------------ TMA producer
-    if (lane == 0) {
-      int g = 0;
-      bool ok = true;
-      for (int w = blockIdx.x; w < total && ok; w += gridDim.x) {
-        const int t = tl[w / P.m_blocks], j = w % P.m_blocks;
+    int g = 0;
+    bool ok = true;
+    for (int w = blockIdx.x; w < total && ok; w += gridDim.x) {
+      const int t = tl[w / P.m_blocks], j = w % P.m_blocks;
+      const int n_cols = FP8 ? 0 : tile_cols(P, t, lane);
+      if (lane == 0) {
         const int e = P.eid[(t * 128) / P.block_m];
         for (int kb = 0; kb < num_kb; ++kb, ++g) {
           if constexpr (FP8) {  // raw codes of the weight blocks into the raw ring
             const int r = g % R;
-            if (!wait_bounded(&rawempty[r], ((uint32_t)(g / R) & 1u) ^ 1u, abort_flag, status)) {
+            if (!wait_bounded_sleep(&rawempty[r], ((uint32_t)(g / R) & 1u) ^ 1u, abort_flag, status)) {
               ok = false;
               break;
             }
@@ -184,36 +246,38 @@ __global__ void __launch_bounds__(Cfg<MODE, FP8>::kThreads, 1)
             if (MODE == kGemm1) tma_3d(dst + RAW_BYTES, &tmW1, &rawfull[r], kb * BK, j * 128, e);
           } else {  // bf16 weight blocks and the tile rows into the operand ring
             const int s = g % S;
-            if (!wait_bounded(&opempty[s], ((uint32_t)(g / S) & 1u) ^ 1u, abort_flag, status)) {
+            if (!wait_bounded_sleep(&opempty[s], ((uint32_t)(g / S) & 1u) ^ 1u, abort_flag, status)) {
               ok = false;
               break;
             }
             uint8_t* dst = smem + C::op + (size_t)s * C::OP_BYTES;
-            mbar_expect_tx(&opfull[s], C::OP_BYTES);
+            mbar_expect_tx(&opfull[s], NA * A_BYTES + n_cols * 128);
             tma_3d(dst, &tmW0, &opfull[s], kb * BK, j * 128, e);
             if (MODE == kGemm1) tma_3d(dst + A_BYTES, &tmW1, &opfull[s], kb * BK, j * 128, e);
-            tma_2d(dst + NA * A_BYTES, &tmX, &opfull[s], kb * BK, t * 128);
+            load_tile_rows(dst + NA * A_BYTES, &tmX, &opfull[s], kb, t, n_cols);
           }
         }
       }
+      ok = __shfl_sync(0xffffffffu, (int)ok, 0);
     }
     __syncwarp();
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer (one lane)
     // The MMA's N covers the tile's rows up to its last real one (rounded up to 16): at decode
     // a tile holds a few real rows, and the columns past them would only cost tensor time.
-    int g = 0, acc = 0;
-    uint32_t acc_phase = 0;
+    // One thread issues every MMA of the CTA, so its instructions per k-block set the pace at
+    // decode (measured: about 10 cycles an instruction with all barriers already complete):
+    // descriptors are low words plus constants, ring positions are counters, not divisions.
+    int acc = 0, s = 0, x = 0, prev_xsb = 0;
+    uint32_t acc_phase = 0, sph = 0, xph = 0;  // xph: phase bit of each tile-row slot
     bool ok = true, issued = false;
+    const uint32_t op_lo = sw128_desc_lo(su32(smem + C::op));
+    const uint32_t xr_lo = sw128_desc_lo(su32(smem + C::xr));
     for (int w = blockIdx.x; w < total && ok; w += gridDim.x) {
-      const int t = tl[w / P.m_blocks];
-      int last = -1;  // the tile's last real row (sorted_ids needs only 4-byte alignment)
-#pragma unroll
-      for (int i = 0; i < 4; ++i)
-        if (P.sid[t * 128 + i * 32 + lane] < P.n_rows) last = i * 32 + lane;
-#pragma unroll
-      for (int off = 16; off > 0; off >>= 1) last = max(last, __shfl_xor_sync(0xffffffffu, last, off));
-      const int n_cols = last < 16 ? 16 : (last + 16) / 16 * 16;
+      const int n_cols = tile_cols(P, tl[w / P.m_blocks], lane);
+      const int xsb = x_slot_bytes(n_cols), nxs = FP8 ? x_slots<C>(xsb) : 1;
+      if (xsb != prev_xsb) x = 0;  // the tile-row producer restarts the same way
+      prev_xsb = xsb;
       const uint32_t idesc = idesc_bf16(128, n_cols);
       if (lane == 0) {
         if (!wait_bounded(&tempty[acc], acc_phase ^ 1u, abort_flag, status)) ok = false;
@@ -222,22 +286,32 @@ __global__ void __launch_bounds__(Cfg<MODE, FP8>::kThreads, 1)
       if (lane == 0) {
         tc_fence_after();
         const uint32_t d = tmem_base + (uint32_t)(acc * NA * 128);
-        for (int kb = 0; kb < num_kb; ++kb, ++g) {
-          const int s = g % S;
-          if (!wait_bounded(&opfull[s], (uint32_t)(g / S) & 1u, abort_flag, status)) {
+        for (int kb = 0; kb < num_kb; ++kb) {
+          if (!wait_bounded(&opfull[s], sph, abort_flag, status) ||
+              (FP8 && !wait_bounded(&xfull[x], (xph >> x) & 1u, abort_flag, status))) {
             ok = false;
             break;
           }
           tc_fence_after();
-          const uint32_t base = su32(smem + C::op + (size_t)s * C::OP_BYTES);
-          const uint32_t xb = base + NA * A_BYTES;
+          const uint32_t alo = op_lo + (uint32_t)s * (C::OP_BYTES >> 4);
+          const uint32_t blo = FP8 ? xr_lo + (uint32_t)x * ((uint32_t)xsb >> 4)
+                                   : alo + ((NA * A_BYTES) >> 4);
 #pragma unroll
           for (int kk = 0; kk < BK / UMMA_K; ++kk)
 #pragma unroll
             for (int a = 0; a < NA; ++a)
-              umma_bf16<1>(d + a * 128, sw128_desc(base + a * A_BYTES + kk * 32),
-                           sw128_desc(xb + kk * 32), idesc, (kb | kk) != 0 ? 1u : 0u);
+              umma_bf16_lo(d + a * 128, alo + ((a * A_BYTES + kk * 32) >> 4), blo + kk * 2, idesc,
+                           (kb | kk) != 0 ? 1u : 0u);
           umma_commit<1>(&opempty[s]);
+          if (++s == S) {
+            s = 0;
+            sph ^= 1u;
+          }
+          if (FP8) {
+            umma_commit<1>(&xempty[x]);
+            xph ^= 1u << x;
+            if (++x == nxs) x = 0;
+          }
           issued = true;
         }
         if (ok) umma_commit<1>(&tfull[acc]);
@@ -263,7 +337,7 @@ __global__ void __launch_bounds__(Cfg<MODE, FP8>::kThreads, 1)
 #pragma unroll
       for (int c = 0; c < 4; ++c) sid4[c] = P.sid[t * 128 + c * 32 + lane];
       int ok = 1;
-      if (lane == 0) ok = wait_bounded(&tfull[acc], acc_phase, abort_flag, status);
+      if (lane == 0) ok = wait_bounded_sleep(&tfull[acc], acc_phase, abort_flag, status);
       ok = __shfl_sync(0xffffffffu, ok, 0);
       if (!ok) break;
       tc_fence_after();
@@ -273,16 +347,22 @@ __global__ void __launch_bounds__(Cfg<MODE, FP8>::kThreads, 1)
         const unsigned real = __ballot_sync(0xffffffffu, sid4[c] < P.n_rows);
         if (!real) continue;  // 32 padding rows: nothing to store
         if (MODE == kGemm1) {
-          uint32_t gv[32], uv[32];
-          tmem_ld32(tb + c * 32, gv);
-          tmem_ld32(tb + 128 + c * 32, uv);
-          tmem_ld_wait();
-          __nv_bfloat16* dst = (__nv_bfloat16*)P.out + (int64_t)(t * 128 + c * 32) * P.N + col;
+#pragma unroll 1
+          for (int hf = 0; hf < 2; ++hf) {  // 16 tile rows at a time (gate and up in registers)
+            if (!((real >> (hf * 16)) & 0xFFFFu)) continue;
+            uint32_t gv[16], uv[16];
+            tmem_ld16(tb + c * 32 + hf * 16, gv);
+            tmem_ld16(tb + 128 + c * 32 + hf * 16, uv);
+            tmem_ld_wait();
+            __nv_bfloat16* dst =
+                (__nv_bfloat16*)P.out + (int64_t)(t * 128 + c * 32 + hf * 16) * P.N + col;
 #pragma unroll
-          for (int i = 0; i < 32; ++i) {
-            if (!((real >> i) & 1u) || col >= P.N) continue;
-            const float g0 = __uint_as_float(gv[i]);
-            dst[(int64_t)i * P.N] = __float2bfloat16(g0 / (1.f + __expf(-g0)) * __uint_as_float(uv[i]));
+            for (int i = 0; i < 16; ++i) {
+              if (!((real >> (hf * 16 + i)) & 1u) || col >= P.N) continue;
+              const float g0 = __uint_as_float(gv[i]);
+              dst[(int64_t)i * P.N] =
+                  __float2bfloat16(g0 / (1.f + __expf(-g0)) * __uint_as_float(uv[i]));
+            }
           }
         } else {
           uint32_t dv[32];
@@ -303,77 +383,121 @@ __global__ void __launch_bounds__(Cfg<MODE, FP8>::kThreads, 1)
       if (++acc == 2) { acc = 0; acc_phase ^= 1u; }
     }
   } else if constexpr (FP8) {
-    // ------------------------------------------------------------ FP8 converters (4 warps)
-    // Warp cw turns rows cw*32 .. cw*32+31 of each raw 128 x 64 code block into the
-    // 128-byte-swizzled bf16 K-major layout the MMA descriptor expects (16-byte chunk c of
-    // row r at r*128 + ((c ^ (r & 7)) << 4)), scaled by the block's scale. Converter warp 0
-    // also loads the tile rows into the operand slot once it is free.
-    const int cw = warp - 6;
-    int g = 0;
-    bool ok = true;
-    for (int w = blockIdx.x; w < total && ok; w += gridDim.x) {
-      const int t = tl[w / P.m_blocks], j = w % P.m_blocks;
-      const int e = P.eid[(t * 128) / P.block_m];
-      const bool sc_ok = e >= 0 && e < P.n_slots && j < P.sc_rb;
-      // block scales of this item in windows of 32 k-block pairs: lane i holds the scale of
-      // 128-wide k-block win + i of each weight block, so a k-block's scale is a shuffle, not
-      // a global load on the critical path (the raw codes are usually waiting already)
-      float scw[NA];
-      int win = -32;
-      for (int kb = 0; kb < num_kb; ++kb, ++g) {
-        const int r = g % R, s = g % S;
-        const int sb = kb >> 1;
-        if (sb - win >= 32) {
-          win = sb & ~31;
-#pragma unroll
+    if (warp == C::kXWarp) {
+      // ---------------------------------------------------------- tile-row producer (FP8)
+      // The tile rows of each k-block into the tile-row ring, as many k-blocks ahead of the
+      // MMA as the item's slots allow; the MMA frees a slot with its commit. Both sides walk
+      // the slots in the same order (the slot index wraps at the item's slot count and
+      // restarts at 0 when the slot size changes) and keep one phase bit per slot. When the
+      // slot size changes, every slot of the old layout is first released (the new slots
+      // overlap the old ones).
+      int x = 0, prev_nxs = 0, prev_xsb = 0;
+      uint32_t xph = 0;
+      bool ok = true;
+      for (int w = blockIdx.x; w < total && ok; w += gridDim.x) {
+        const int t = tl[w / P.m_blocks];
+        const int n_cols = tile_cols(P, t, lane);
+        const int xsb = x_slot_bytes(n_cols), nxs = x_slots<C>(xsb);
+        if (lane == 0) {
+          if (xsb != prev_xsb) {
+            for (int y = 0; y < prev_nxs && ok; ++y)
+              ok = wait_bounded_sleep(&xempty[y], ((xph >> y) & 1u) ^ 1u, abort_flag, status);
+            x = 0;
+          }
+          prev_xsb = xsb;
+          prev_nxs = nxs;
+          for (int kb = 0; kb < num_kb && ok; ++kb) {
+            if (!wait_bounded_sleep(&xempty[x], ((xph >> x) & 1u) ^ 1u, abort_flag, status)) {
+              ok = false;
+              break;
+            }
+            xph ^= 1u << x;
+            mbar_expect_tx(&xfull[x], n_cols * 128);
+            load_tile_rows(smem + C::xr + (size_t)x * xsb, &tmX, &xfull[x], kb, t, n_cols);
+            if (++x == nxs) x = 0;
+          }
+        }
+        ok = __shfl_sync(0xffffffffu, (int)ok, 0);
+      }
+      __syncwarp();
+    } else if ((warp - 6) % 4 != 3) {
+      // ---------------------------------------------------------- FP8 converters
+      // Converter cw turns rows cw*16 .. cw*16+15 of each raw 128 x 64 code block into the
+      // 128-byte-swizzled bf16 K-major layout the MMA descriptor expects (16-byte chunk c of
+      // row r at r*128 + ((c ^ (r & 7)) << 4)), scaled by the block's scale.
+      const int cw = (warp - 6) - (warp - 6) / 4;
+      constexpr int kRows = 128 / C::kCvtWarps;  // rows of each block this warp converts
+      constexpr int kUnits = kRows * 4 / 32;     // 16-code units per lane and block
+      static_assert(kRows * 4 % 32 == 0, "each lane converts whole units");
+      int g = 0;
+      bool ok = true;
+      for (int w = blockIdx.x; w < total && ok; w += gridDim.x) {
+        const int t = tl[w / P.m_blocks], j = w % P.m_blocks;
+        const int e = P.eid[(t * 128) / P.block_m];
+        const bool sc_ok = e >= 0 && e < P.n_slots && j < P.sc_rb;
+        // block scales of this item in windows of 32 k-block pairs: lane i holds the scale of
+        // 128-wide k-block win + i of each weight block, so a k-block's scale is a shuffle, not
+        // a global load on the critical path (the raw codes are usually waiting already)
+        float scw[NA];
+        int win = -32;
+        for (int kb = 0; kb < num_kb; ++kb, ++g) {
+          const int r = g % R, s = g % S;
+          const int sb = kb >> 1;
+          if (sb - win >= 32) {
+            win = sb & ~31;
+  #pragma unroll
+            for (int a = 0; a < NA; ++a)
+              scw[a] = sc_ok && win + lane < P.sc_kb
+                           ? __ldg(P.scale + (((int64_t)e * NA + a) * P.sc_rb + j) * P.sc_kb +
+                                   win + lane)
+                           : 0.f;
+          }
+          float sc[NA];
+  #pragma unroll
+          for (int a = 0; a < NA; ++a) sc[a] = __shfl_sync(0xffffffffu, scw[a], sb - win);
+          int okw = 1;
+          if (lane == 0) {
+            okw = wait_bounded_sleep(&opempty[s], ((uint32_t)(g / S) & 1u) ^ 1u, abort_flag, status) &&
+                  wait_bounded_sleep(&rawfull[r], (uint32_t)(g / R) & 1u, abort_flag, status);
+          }
+          okw = __shfl_sync(0xffffffffu, okw, 0);
+          if (!okw) {
+            ok = false;
+            break;
+          }
+          const uint8_t* src = smem + C::raw + (size_t)r * C::RAWS_BYTES;
+          uint8_t* dst = smem + C::op + (size_t)s * C::OP_BYTES;
+          // all of this lane's 16-code units first (row u / 4, codes (u % 4) * 16 .. +15 of the
+          // warp's rows), then the conversions and stores
+          uint4 qv[NA][kUnits];
+  #pragma unroll
           for (int a = 0; a < NA; ++a)
-            scw[a] = sc_ok && win + lane < P.sc_kb
-                         ? __ldg(P.scale + (((int64_t)e * NA + a) * P.sc_rb + j) * P.sc_kb +
-                                 win + lane)
-                         : 0.f;
-        }
-        float sc[NA];
-#pragma unroll
-        for (int a = 0; a < NA; ++a) sc[a] = __shfl_sync(0xffffffffu, scw[a], sb - win);
-        int okw = 1;
-        if (lane == 0) {
-          okw = wait_bounded(&opempty[s], ((uint32_t)(g / S) & 1u) ^ 1u, abort_flag, status) &&
-                wait_bounded(&rawfull[r], (uint32_t)(g / R) & 1u, abort_flag, status);
-          if (okw && cw == 0) {
-            uint8_t* xdst = smem + C::op + (size_t)s * C::OP_BYTES + NA * A_BYTES;
-            mbar_expect_tx(&opfull[s], X_BYTES);
-            tma_2d(xdst, &tmX, &opfull[s], kb * BK, t * 128);
+  #pragma unroll
+            for (int i = 0; i < kUnits; ++i) {
+              const int u = i * 32 + lane;
+              const int row = cw * kRows + (u >> 2), h = u & 3;
+              qv[a][i] = *reinterpret_cast<const uint4*>(src + a * RAW_BYTES + row * BK + h * 16);
+            }
+  #pragma unroll
+          for (int a = 0; a < NA; ++a)
+  #pragma unroll
+            for (int i = 0; i < kUnits; ++i) {
+              const int u = i * 32 + lane;
+              const int row = cw * kRows + (u >> 2), h = u & 3;
+              uint32_t v[8];
+              e4m3x16_scaled_bf16(qv[a][i], sc[a], v);
+              uint8_t* drow = dst + a * A_BYTES + row * 128;
+              *reinterpret_cast<uint4*>(drow + (((2 * h) ^ (row & 7)) << 4)) =
+                  make_uint4(v[0], v[1], v[2], v[3]);
+              *reinterpret_cast<uint4*>(drow + (((2 * h + 1) ^ (row & 7)) << 4)) =
+                  make_uint4(v[4], v[5], v[6], v[7]);
+            }
+          fence_proxy_async_smem();
+          __syncwarp();
+          if (lane == 0) {
+            mbar_arrive(&rawempty[r]);
+            mbar_arrive(&opfull[s]);
           }
-        }
-        okw = __shfl_sync(0xffffffffu, okw, 0);
-        if (!okw) {
-          ok = false;
-          break;
-        }
-        const uint8_t* src = smem + C::raw + (size_t)r * C::RAWS_BYTES;
-        uint8_t* dst = smem + C::op + (size_t)s * C::OP_BYTES;
-#pragma unroll
-        for (int a = 0; a < NA; ++a) {
-#pragma unroll
-          for (int i = 0; i < 4; ++i) {
-            // 16-code unit u of this warp's 32 rows: row u / 4, codes (u % 4) * 16 .. +15
-            const int u = i * 32 + lane;
-            const int row = cw * 32 + (u >> 2), h = u & 3;
-            const uint4 qv = *reinterpret_cast<const uint4*>(src + a * RAW_BYTES + row * BK + h * 16);
-            uint32_t v[8];
-            e4m3x16_scaled_bf16(qv, sc[a], v);
-            uint8_t* drow = dst + a * A_BYTES + row * 128;
-            *reinterpret_cast<uint4*>(drow + (((2 * h) ^ (row & 7)) << 4)) =
-                make_uint4(v[0], v[1], v[2], v[3]);
-            *reinterpret_cast<uint4*>(drow + (((2 * h + 1) ^ (row & 7)) << 4)) =
-                make_uint4(v[4], v[5], v[6], v[7]);
-          }
-        }
-        fence_proxy_async_smem();
-        __syncwarp();
-        if (lane == 0) {
-          mbar_arrive(&rawempty[r]);
-          mbar_arrive(&opfull[s]);
         }
       }
     }
@@ -442,7 +566,7 @@ moe_status_t launch_gemm1_dec(const moe_config_t& c, const void* xs, const void*
   }
   {
     uint64_t d[2] = {H, (uint64_t)max_padded}, st[1] = {H};
-    uint32_t box[2] = {BK, 128};
+    uint32_t box[2] = {BK, X_BOX};
     if (!make_map(&mX, xs, 2, d, st, box, false)) return MOE_ERR_CUDA;
   }
   Params P{};
@@ -481,7 +605,7 @@ moe_status_t launch_gemm2_dec(const moe_config_t& c, const void* act, const void
   }
   {
     uint64_t d[2] = {I, (uint64_t)max_padded}, st[1] = {I};
-    uint32_t box[2] = {BK, 128};
+    uint32_t box[2] = {BK, X_BOX};
     if (!make_map(&mX, act, 2, d, st, box, false)) return MOE_ERR_CUDA;
   }
   Params P{};

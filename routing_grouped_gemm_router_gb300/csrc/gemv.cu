@@ -117,12 +117,12 @@ static Params base_params(const moe_config_t& c, const int32_t* sid, const int32
 }  // namespace gv
 
 // Up to this many tokens the grouped GEMMs of a layer run here. Measured on GB300 against
-// the tensor-core kernels (gpt-oss-shaped decode layer, one step): bf16 weights 58 vs 80 us
-// at 1 token, 96 vs 123 at 2, behind from 3 tokens (151 vs 144); FP8 weights, whose
-// tensor-core path converts codes in shared memory, 46 vs 134 us at 1 token, 0.54 vs 1.08 ms
-// at 16, 1.16 vs 1.55 at 32, behind at 128 (3.06 vs 2.58).
+// the decode tensor-core kernel (gemm_dec.cu; gpt-oss-shaped decode layer, one step in a CUDA
+// graph): bf16 weights 49.5 vs 62.6 us at 1 token, 88 vs 117 at 2, behind from 3 tokens;
+// FP8 weights 41 vs 87 us at 1 token, 316 vs 340 at 8, 457 vs 464 at 12, behind from 16
+// (542 vs 533) and far behind at 32 (1160 vs 767).
 constexpr int kGemvMaxTokens = 2;
-constexpr int kGemvMaxTokensFp8 = 32;
+constexpr int kGemvMaxTokensFp8 = 12;
 
 bool gemv_applies(const moe_config_t& c, int max_padded) {
   const bool fp8 = c.weight_format == MOE_WEIGHTS_FP8_E4M3_B128;

@@ -59,14 +59,27 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* b, uint32_t parity) {
       : "memory");
   return ok != 0;
 }
+// try_wait with a suspend-time hint: a thread whose phase is not complete sleeps in hardware
+// until the phase completes or about `ns` nanoseconds pass, issuing nothing meanwhile.
+__device__ __forceinline__ bool mbar_try_wait_sleep(uint64_t* b, uint32_t parity, uint32_t ns) {
+  uint32_t ok;
+  asm volatile(
+      "{\n .reg .pred p;\n mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2, %3;\n"
+      " selp.u32 %0, 1, 0, p;\n}\n"
+      : "=r"(ok)
+      : "r"(su32(b)), "r"(parity), "r"(ns)
+      : "memory");
+  return ok != 0;
+}
 // Bounded wait for the phase of parity `parity`. Returns false (after raising the CTA's
 // abort flag and writing kStatusTimeout to *status) when it runs out of time, or when
-// another role of the CTA has aborted.
+// another role of the CTA has aborted. sleep_ns > 0 suspends the thread between polls (for
+// roles whose spinning would take issue slots from warps doing arithmetic).
 static __device__ __noinline__ bool wait_slow(uint64_t* b, uint32_t parity, volatile int* abort_flag,
-                                       int* status) {
+                                       int* status, uint32_t sleep_ns = 0) {
   const uint64_t t0 = gtimer();
   for (uint32_t it = 1;; ++it) {
-    if (mbar_try_wait(b, parity)) return true;
+    if (sleep_ns ? mbar_try_wait_sleep(b, parity, sleep_ns) : mbar_try_wait(b, parity)) return true;
     if ((it & 63u) == 0) {
       if (*abort_flag) return false;
       if (gtimer() - t0 > kTimeoutNs) {
@@ -81,6 +94,12 @@ __device__ __forceinline__ bool wait_bounded(uint64_t* b, uint32_t parity,
                                              volatile int* abort_flag, int* status) {
   if (mbar_try_wait(b, parity)) return true;
   return wait_slow(b, parity, abort_flag, status);
+}
+constexpr uint32_t kSleepNs = 1000;  // suspend hint of the sleeping waits
+__device__ __forceinline__ bool wait_bounded_sleep(uint64_t* b, uint32_t parity,
+                                                   volatile int* abort_flag, int* status) {
+  if (mbar_try_wait(b, parity)) return true;
+  return wait_slow(b, parity, abort_flag, status, kSleepNs);
 }
 
 // ------------------------------------------------------------------- cluster
@@ -265,7 +284,7 @@ __device__ __forceinline__ void tmem_ld_wait() {
 // Shared-memory matrix descriptor: K-major operand, 128-byte swizzle, rows of 128 bytes,
 // 8-row swizzle atoms 1024 bytes apart (stride byte offset). Tile bases are 1024-aligned;
 // stepping K by 16 elements inside the atom advances the start address by 32 bytes.
-__device__ __forceinline__ uint64_t sw128_desc(uint32_t saddr) {
+__host__ __device__ constexpr uint64_t sw128_desc(uint32_t saddr) {
   uint64_t d = 0;
   d |= (uint64_t)((saddr & 0x3FFFFu) >> 4);  // bits 0-13: start address / 16
   d |= (uint64_t)1 << 16;                    // bits 16-29: leading byte offset (unused)
@@ -273,6 +292,26 @@ __device__ __forceinline__ uint64_t sw128_desc(uint32_t saddr) {
   d |= (uint64_t)1 << 46;                    // bits 46-47: descriptor version 1
   d |= (uint64_t)2 << 61;                    // bits 61-63: 128-byte swizzle
   return d;
+}
+// The same descriptor as its two 32-bit words: the high word is one constant for every
+// operand, the low word (start address / 16, plus the leading-offset field) differs. A
+// descriptor `off` bytes (a multiple of 16) past another is its low word plus off / 16.
+constexpr uint32_t kSw128DescHi = (1024u >> 4) | (1u << 14) | (2u << 29);
+__host__ __device__ constexpr uint32_t sw128_desc_lo(uint32_t saddr) {
+  return ((saddr & 0x3FFFFu) >> 4) | (1u << 16);
+}
+static_assert((uint32_t)(sw128_desc(0x2C40u) >> 32) == kSw128DescHi &&
+                  (uint32_t)sw128_desc(0x2C40u) == sw128_desc_lo(0x2C40u),
+              "split descriptor words");
+// tcgen05.mma (cta_group::1, kind::f16) with both operand descriptors given by their low words.
+__device__ __forceinline__ void umma_bf16_lo(uint32_t d_tmem, uint32_t alo, uint32_t blo,
+                                             uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n .reg .pred p;\n .reg .b64 ad, bd;\n mov.b64 ad, {%1, %5};\n mov.b64 bd, {%2, %5};\n"
+      " setp.ne.b32 p, %4, 0;\n"
+      " tcgen05.mma.cta_group::1.kind::f16 [%0], ad, bd, %3, p;\n}\n" ::"r"(d_tmem),
+      "r"(alo), "r"(blo), "r"(idesc), "r"(accumulate), "r"(kSw128DescHi)
+      : "memory");
 }
 // Instruction descriptor for kind::f16: fp32 accumulator, bf16 A and B, both K-major.
 __host__ __device__ constexpr uint32_t idesc_bf16(int M, int N) {
@@ -291,11 +330,16 @@ __device__ __forceinline__ uint32_t pack_bf16(float a, float b) {
 // subnormal codes too (E4M3 exponent 0 lands in the bf16 subnormal range with the same
 // mantissa). The bf16 subnormals take part in the bf16 multiply below without flushing.
 // (The NaN code 0x7F is not propagated; weights hold finite codes.)
+// Per 16-bit half holding a code b in its low byte, (b & 0x7F) << 4 | (b & 0x80) << 8 equals
+// 16 b + 240 (b & 0x80): times 16 puts the magnitude in place and the sign at bit 11, and
+// 15 * 0x800 more carries that bit to bit 15 (no half overflows into the next). Written as
+// multiply-adds, half of the work runs on the FMA pipe instead of the integer ALU, which
+// the conversion otherwise saturates.
 __device__ __forceinline__ void e4m3x4_to_bf16x4_lowexp(uint32_t x, uint32_t& p01, uint32_t& p23) {
-  const uint32_t a = __byte_perm(x, 0u, 0x1404u);  // [b1 0 b0 0]
-  const uint32_t b = __byte_perm(x, 0u, 0x3424u);  // [b3 0 b2 0]
-  p01 = (a & 0x80008000u) | ((a & 0x7F007F00u) >> 4);
-  p23 = (b & 0x80008000u) | ((b & 0x7F007F00u) >> 4);
+  const uint32_t a = __byte_perm(x, 0u, 0x4140u);  // [0 b1 0 b0]
+  const uint32_t b = __byte_perm(x, 0u, 0x4342u);  // [0 b3 0 b2]
+  p01 = a * 16u + (a & 0x00800080u) * 240u;
+  p23 = b * 16u + (b & 0x00800080u) * 240u;
 }
 __device__ __forceinline__ uint32_t bf16x2_mul(uint32_t a, uint32_t b) {
   uint32_t d;

@@ -66,7 +66,7 @@ def test_block_m_and_workspace(L):
 
 
 def test_small_batch_predicate(L):
-    """bf16 layers of at most 2 tokens (32 with FP8 weights) take the small-batch grouped
+    """bf16 layers of at most 2 tokens (12 with FP8 weights) take the small-batch grouped
     GEMMs; fp32 layers, larger batches and bad configurations do not (host arithmetic)."""
     assert L.moe_small_batch(L.make_config(1, 2880, 2880, 128, 4, L.MOE_BF16))
     assert L.moe_small_batch(L.make_config(2, 7168, 2048, 256, 8, L.MOE_BF16))
@@ -76,17 +76,18 @@ def test_small_batch_predicate(L):
     s13, s2 = torch.ones(128, 2, 23, 23), torch.ones(128, 23, 23)  # scale grids (host only)
     fp8 = lambda T: L.make_config(T, 2880, 2880, 128, 4, L.MOE_BF16, w13_scale=s13,  # noqa: E731
                                   w2_scale=s2)
-    assert L.moe_small_batch(fp8(32)) and not L.moe_small_batch(fp8(33))
+    assert L.moe_small_batch(fp8(12)) and not L.moe_small_batch(fp8(13))
 
 
 def test_decode_parity_cases_take_their_paths(L):
     """The decode layers of the GPU parity tests exercise the paths they are named for: the
-    9-token layer runs the tensor-core GEMMs split along K (both GEMMs have split scratch),
+    9-token layer and the FP8 layers of 13 tokens and more run the decode tensor-core GEMMs,
     the 1- and 2-token layers the small-batch kernels."""
     cfg = L.make_config(9, 320, 448, 8, 4, L.MOE_BF16)
     assert not L.moe_small_batch(cfg)
-    assert L.moe_expert_gemm1_gathered_workspace_size(cfg, 128) > 0
-    assert L.moe_expert_gemm2_workspace_size(cfg, 128) > 0
+    s13, s2 = torch.ones(8, 2, 3, 3), torch.ones(8, 3, 3)  # scale grids (host only)
+    assert not L.moe_small_batch(L.make_config(20, 320, 272, 8, 2, L.MOE_BF16, w13_scale=s13,
+                                               w2_scale=s2))
     for T, H, I, E, k in ((1, 2880, 2880, 128, 4), (2, 2880, 2880, 32, 4), (2, 1000, 776, 4, 2)):
         assert L.moe_small_batch(L.make_config(T, H, I, E, k, L.MOE_BF16))
 

@@ -272,9 +272,11 @@ LAYER_CASES = [
     mi.Workload("bf16-skewed", T=600, H=256, I=256, E=32, k=4, dtype="bf16",
                 logit_bias_std=1.5, seed=15),
     mi.Workload("bf16-top1", T=37, H=128, I=192, E=8, k=1, dtype="bf16", seed=16),
-    # decode above the small-batch limit: tensor cores with split-K over ragged k-block
-    # ranges (GEMM1 5 k-blocks in 2 splits, GEMM2 7 in 4)
-    mi.Workload("bf16-decode-splitk", T=9, H=320, I=448, E=8, k=4, dtype="bf16", seed=18),
+    # decode above the small-batch limit: the decode tensor-core kernel (weights as the
+    # 128-row operand) over ragged K and N; then tiles nearly full (three experts, 256 rows),
+    # where the MMA's N covers up to 128 tile rows
+    mi.Workload("bf16-decode-T9", T=9, H=320, I=448, E=8, k=4, dtype="bf16", seed=18),
+    mi.Workload("bf16-decode-full-tiles", T=128, H=256, I=320, E=3, k=2, dtype="bf16", seed=21),
     # small batches (CUDA-core grouped GEMMs): passes of two rows, the second case with K and
     # N off the 256-element step
     mi.Workload("bf16-decode-T2", T=2, H=2880, I=2880, E=32, k=4, dtype="bf16", seed=19),
@@ -715,6 +717,13 @@ FP8_CASES = [
     (mi.Workload("fp8-decode-ragged", T=6, H=1040, I=784, E=4, k=2, dtype="bf16", seed=66), 0,
      True),
     (mi.Workload("fp8-decode-shared", T=3, H=2880, I=1024, E=16, k=4, dtype="bf16", seed=67), 1,
+     False),
+    # decode tensor-core kernel (13 to 128 tokens): ragged K and N with any scales; 64 tokens
+    # plus a shared expert (a 64-row tile); tiles nearly full (one tile-row slot in GEMM1)
+    (mi.Workload("fp8-dec-ragged", T=20, H=320, I=272, E=8, k=2, dtype="bf16", seed=68), 0, True),
+    (mi.Workload("fp8-dec-shared", T=64, H=512, I=384, E=32, k=4, dtype="bf16", seed=69), 1,
+     False),
+    (mi.Workload("fp8-dec-full-tiles", T=128, H=256, I=256, E=3, k=2, dtype="bf16", seed=70), 0,
      False),
 ]
 
