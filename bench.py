@@ -211,13 +211,6 @@ def host_copies(inp):
     return f64(inp.x), f64(inp.Wg), bits(inp.W13), bits(inp.W2), lb, sb
 
 
-def split_ws_bytes(L, cfg, B, gemm):
-    """Split-K scratch a grouped GEMM of this configuration uses (0: no split)."""
-    if gemm == 1:
-        return L.moe_expert_gemm1_gathered_workspace_size(cfg, B) if cfg.dtype == L.MOE_BF16 else 0
-    return L.moe_expert_gemm2_workspace_size(cfg, B)
-
-
 def default_sample(wl):
     """Tokens per oracle pass: about 10-20 s of float64 work on a 16-core host."""
     return {"mixtral-prefill": 1536, "qwen3-skewed": 768,
@@ -404,8 +397,8 @@ def measure_layer(args, wl, ctx, seed, steps, warmup, shared=0, fp8=False, ep_ha
     base = ws.data_ptr()
     p = {n: base + getattr(lay, n) for n in ("logits", "topk_ids", "topk_w", "sorted_ids",
                                                "expert_ids", "num_post_padded", "counts",
-                                               "align_scratch", "act", "xs", "y", "splitk")}
-    ws_split = lay.total - lay.splitk
+                                               "align_scratch", "act", "xs", "y", "gemm_scratch")}
+    ws_gemm = lay.total - lay.gemm_scratch
     ws_align = lay.act - lay.align_scratch
     ws_xs = lay.y - lay.xs
     out = torch.empty(T, H, dtype=inp.x.dtype, device=dev)
@@ -435,8 +428,8 @@ def measure_layer(args, wl, ctx, seed, steps, warmup, shared=0, fp8=False, ep_ha
             if ev is not None:
                 ev[3].record(stream)
             L.moe_expert_gemm1_gathered(cfg, p["xs"], W13s[c], p["sorted_ids"], p["expert_ids"],
-                                        p["num_post_padded"], B, p["act"], p["splitk"],
-                                        ws_split, sh)
+                                        p["num_post_padded"], B, p["act"], p["gemm_scratch"],
+                                        ws_gemm, sh)
         else:
             if ev is not None:
                 ev[3].record(stream)
@@ -445,8 +438,8 @@ def measure_layer(args, wl, ctx, seed, steps, warmup, shared=0, fp8=False, ep_ha
         if ev is not None:
             ev[4].record(stream)
         L.moe_expert_gemm2(cfg, p["act"], W2s[c], p["sorted_ids"], p["expert_ids"],
-                           p["num_post_padded"], B, p["topk_w"], p["y"], p["splitk"], ws_split,
-                           sh)
+                           p["num_post_padded"], B, p["topk_w"], p["y"], p["gemm_scratch"],
+                           ws_gemm, sh)
         if ev is not None:
             ev[5].record(stream)
         if emap is not None:
@@ -463,12 +456,11 @@ def measure_layer(args, wl, ctx, seed, steps, warmup, shared=0, fp8=False, ep_ha
     # kernels moe_forward enqueues: router GEMM + top-k, align (one kernel up to 4096 rows,
     # else three; up to 8 tokens top-k and align are one kernel), expert map (applied by the
     # routing kernel of batches of at most 32 slots), row gather (bf16 tensor-core path),
-    # GEMM1, GEMM2 (each + a counter-zeroing kernel when split along K) and the combine
+    # GEMM1, GEMM2 and the combine
     tiny = T <= 8 and T * k <= 32
     routing_launches = 2 if (T <= 8 and T * k <= 4096) else 2 + (1 if T * k <= 4096 else 3)
     launches_per_step = routing_launches + (1 if (emap is not None and not tiny) else 0) + \
-        (1 if gathered else 0) + 3 + \
-        (0 if small else sum(1 for g in (1, 2) if split_ws_bytes(L, cfg, B, g) > 0))
+        (1 if gathered else 0) + 3
 
     for _ in range(max(3, warmup)):
         step()

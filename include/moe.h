@@ -126,7 +126,7 @@ typedef struct moe_ws_layout {
   size_t act;              /* dtype [max_padded, I] */
   size_t xs;               /* bf16 [max_padded, H]: routed token rows in padded order */
   size_t y;                /* dtype [T*k, H] */
-  size_t splitk;           /* split-K scratch of the grouped GEMMs (may be empty) */
+  size_t gemm_scratch;     /* scratch of the grouped GEMMs: empty with the current kernels */
   size_t total;            /* bytes required */
   int block_m;
   int max_padded;
@@ -212,12 +212,6 @@ moe_status_t moe_apply_expert_map(int32_t* expert_ids, int num_tiles, const int3
  * gathered into padded order in ws (moe_expert_gemm1_workspace_size bytes, 256-byte
  * aligned), then multiplied on the tensor cores; fp32 gathers inside the GEMM.
  *
- * Split-K (bf16 grouped GEMMs of more than 128 tokens): when T*k is so small that the
- * (m-tile pair, n-tile) work items cannot fill the GPU twice over, each item is split along
- * K; the splits write fp32 partial sums to the GEMM's workspace and the last split of a
- * tile adds them in split order and applies the epilogue (deterministic). The workspace
- * sizes below include that scratch; it depends only on cfg and block_m.
- *
  * Decode batches (bf16 activations, at most 128 tokens, not small): both grouped GEMMs run
  * on the tensor cores with the expert weights as the 128-row MMA operand and each tile's
  * token rows, up to its last real one, as the other; one work item is (tile, 128 output
@@ -243,8 +237,9 @@ moe_status_t moe_expert_gemm1(const moe_config_t* cfg, const void* x, const void
  * moe_gather_rows writes xs[p, :] = x[sorted_ids[p] / k, :] for every p < num_post_padded
  * with sorted_ids[p] < T*k (padding rows untouched; xs is [max_padded, H] of dtype, 16-byte
  * aligned); moe_expert_gemm1_gathered runs GEMM1 + SwiGLU on those rows (bf16 only, else
- * MOE_ERR_UNSUPPORTED) with ws of moe_expert_gemm1_gathered_workspace_size bytes (the
- * split-K scratch; 0 bytes and ws may be NULL when there is no split). Page §2 lists both
+ * MOE_ERR_UNSUPPORTED) with ws of moe_expert_gemm1_gathered_workspace_size bytes (0 with the
+ * current kernels, ws may then be NULL; callers that size ws through this query stay correct
+ * if a kernel needs scratch). Page §2 lists both
  * feeds, a permuted copy and an in-GEMM gather; this pair is the permuted-copy feed with the
  * permutation taken from sorted_ids. */
 moe_status_t moe_gather_rows(const void* x, const int32_t* sorted_ids,
@@ -261,7 +256,7 @@ moe_status_t moe_expert_gemm1_gathered(const moe_config_t* cfg, const void* xs,
 /* GEMM2 with the router weight (page §6): for every padded position p with r < T*k,
  *   y[r, :] = topk_w[r] * (act[p] @ W2[e]^T).  Each row r < T*k is written exactly once;
  * padding rows are never written. ws: moe_expert_gemm2_workspace_size bytes, 256-byte
- * aligned (the split-K scratch; 0 bytes and ws may be NULL when there is no split). */
+ * aligned (0 with the current kernels, ws may then be NULL). */
 moe_status_t moe_expert_gemm2_workspace_size(const moe_config_t* cfg, int block_m,
                                              size_t* bytes);
 moe_status_t moe_expert_gemm2(const moe_config_t* cfg, const void* act, const void* W2,
@@ -270,8 +265,8 @@ moe_status_t moe_expert_gemm2(const moe_config_t* cfg, const void* act, const vo
                               const float* topk_w, void* y, void* ws, size_t ws_bytes,
                               cudaStream_t stream);
 
-/* Both expert GEMMs: GEMM1 into ws (act, then GEMM1's scratch, which GEMM2 reuses for its
- * own), then GEMM2 into y[T*k, H]. ws: moe_grouped_swiglu_workspace_size bytes, 256-byte
+/* Both expert GEMMs: GEMM1 into ws (act, then GEMM1's scratch: the gathered rows of bf16),
+ * then GEMM2 into y[T*k, H]. ws: moe_grouped_swiglu_workspace_size bytes, 256-byte
  * aligned. */
 moe_status_t moe_grouped_swiglu_workspace_size(const moe_config_t* cfg, int block_m,
                                                size_t* bytes);

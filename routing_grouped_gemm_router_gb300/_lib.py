@@ -40,7 +40,7 @@ class moe_config_t(ctypes.Structure):
 class moe_ws_layout_t(ctypes.Structure):
     _fields_ = [(n, ctypes.c_size_t) for n in ("logits", "topk_ids", "topk_w", "sorted_ids",
                                               "expert_ids", "num_post_padded", "counts",
-                                              "align_scratch", "act", "xs", "y", "splitk",
+                                              "align_scratch", "act", "xs", "y", "gemm_scratch",
                                               "total")] + \
                [("block_m", ctypes.c_int), ("max_padded", ctypes.c_int)]
 

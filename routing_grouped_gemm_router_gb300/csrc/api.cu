@@ -76,14 +76,9 @@ static size_t gather_bytes(const moe_config_t* c, int block_m) {
   if (c->dtype != MOE_BF16) return 0;
   return align_up(moe_max_padded_rows(c->T, c->k, c->E, block_m) * (size_t)c->H * 2, 256);
 }
-// Split-K scratch of grouped GEMM 1 or 2 (bf16 tensor-core path only).
-static size_t split_bytes(int gemm, const moe_config_t* c, int block_m) {
-  if (c->dtype != MOE_BF16) return 0;
-  return gemm_split_bytes(gemm, *c, (int)moe_max_padded_rows(c->T, c->k, c->E, block_m));
-}
-// Bytes of GEMM1's scratch: the gathered rows, then GEMM1's split-K scratch.
+// Bytes of GEMM1's scratch: the gathered rows (bf16).
 static size_t gemm1_scratch_bytes(const moe_config_t* c, int block_m) {
-  return gather_bytes(c, block_m) + split_bytes(1, c, block_m);
+  return gather_bytes(c, block_m);
 }
 
 // Argument checks of the align entry points (moe_align, moe_align_noalloc) and the padded
@@ -174,7 +169,7 @@ moe_status_t moe_workspace_layout(const moe_config_t* cfg, moe_ws_layout_t* L) {
   L->act = take(mp * c->I * es);
   L->xs = take(gather_bytes(c, B));
   L->y = take(n * c->H * es);
-  L->splitk = take(std::max(split_bytes(1, c, B), split_bytes(2, c, B)));
+  L->gemm_scratch = take(0);  // no grouped GEMM needs scratch of its own
   L->total = off;
   L->block_m = B;
   L->max_padded = (int)mp;
@@ -265,8 +260,7 @@ moe_status_t moe_expert_gemm1_gathered_workspace_size(const moe_config_t* cfg, i
   moe_status_t st = check_gemm_args(cfg, block_m);
   if (st != MOE_OK) return st;
   if (!bytes) return MOE_ERR_INVALID_ARG;
-  const moe_config_t eff = effective(cfg);
-  *bytes = split_bytes(1, &eff, block_m);
+  *bytes = 0;  // the kernels need no scratch
   return MOE_OK;
 }
 
@@ -282,15 +276,14 @@ moe_status_t moe_expert_gemm1_gathered(const moe_config_t* cfg, const void* xs,
   if (c->dtype != MOE_BF16) return MOE_ERR_UNSUPPORTED;
   if (!xs || !W13 || !sorted_ids || !expert_ids || !npp || !act) return MOE_ERR_INVALID_ARG;
   if (!aligned16(xs) || !aligned16(W13) || !aligned16(act)) return MOE_ERR_INVALID_ARG;
-  const size_t need = split_bytes(1, c, block_m);
-  if (need && (!ws || ws_bytes < need || ((uintptr_t)ws & 255u))) return MOE_ERR_WORKSPACE;
+  (void)ws;
+  (void)ws_bytes;
   const int mp = (int)moe_max_padded_rows(c->T, c->k, c->E, block_m);
   if (gemv_applies(*c, mp))
     return launch_gemv1(*c, xs, true, W13, sorted_ids, expert_ids, npp, block_m, act, stream);
   if (dec_gemm_applies(*c, mp))
     return launch_gemm1_dec(*c, xs, W13, sorted_ids, expert_ids, npp, block_m, mp, act, stream);
-  return launch_gemm1_tc(*c, xs, W13, sorted_ids, expert_ids, npp, block_m, mp, act, ws,
-                         ws_bytes, stream);
+  return launch_gemm1_tc(*c, xs, W13, sorted_ids, expert_ids, npp, block_m, mp, act, stream);
 }
 
 moe_status_t moe_expert_gemm1(const moe_config_t* cfg, const void* x, const void* W13,
@@ -325,8 +318,7 @@ moe_status_t moe_expert_gemm2_workspace_size(const moe_config_t* cfg, int block_
   moe_status_t st = check_gemm_args(cfg, block_m);
   if (st != MOE_OK) return st;
   if (!bytes) return MOE_ERR_INVALID_ARG;
-  const moe_config_t eff = effective(cfg);
-  *bytes = split_bytes(2, &eff, block_m);
+  *bytes = 0;  // the kernels need no scratch
   return MOE_OK;
 }
 
@@ -343,15 +335,15 @@ moe_status_t moe_expert_gemm2(const moe_config_t* cfg, const void* act, const vo
   const int mp = (int)moe_max_padded_rows(c->T, c->k, c->E, block_m);
   if (c->dtype == MOE_BF16) {
     if (!aligned16(act) || !aligned16(W2) || !aligned16(y)) return MOE_ERR_INVALID_ARG;
-    const size_t need = split_bytes(2, c, block_m);
-    if (need && (!ws || ws_bytes < need || ((uintptr_t)ws & 255u))) return MOE_ERR_WORKSPACE;
+    (void)ws;
+    (void)ws_bytes;
     if (gemv_applies(*c, mp))
       return launch_gemv2(*c, act, W2, sorted_ids, expert_ids, npp, block_m, topk_w, y, stream);
     if (dec_gemm_applies(*c, mp))
       return launch_gemm2_dec(*c, act, W2, sorted_ids, expert_ids, npp, block_m, mp, topk_w, y,
                               stream);
     return launch_gemm2_tc(*c, act, W2, sorted_ids, expert_ids, npp, block_m, mp, topk_w, y,
-                           ws, ws_bytes, stream);
+                           stream);
   }
   return launch_gemm2_simt(*c, (const float*)act, (const float*)W2, sorted_ids, expert_ids, npp,
                            block_m, mp, topk_w, (float*)y, stream);
@@ -365,8 +357,7 @@ moe_status_t moe_grouped_swiglu_workspace_size(const moe_config_t* cfg, int bloc
   if (st != MOE_OK) return st;
   if (!bytes) return MOE_ERR_INVALID_ARG;
   const size_t mp = moe_max_padded_rows(c->T, c->k, c->E, block_m);
-  *bytes = align_up(mp * c->I * dtype_size(c->dtype), 256) +
-           std::max(gemm1_scratch_bytes(c, block_m), split_bytes(2, c, block_m));
+  *bytes = align_up(mp * c->I * dtype_size(c->dtype), 256) + gemm1_scratch_bytes(c, block_m);
   return MOE_OK;
 }
 
@@ -454,8 +445,7 @@ moe_status_t moe_masked_workspace_size(const moe_config_t* cfg, int capacity, si
   if (!bytes) return MOE_ERR_INVALID_ARG;
   const size_t n = (size_t)m.T, B = block_m_for(m.dtype);
   *bytes = align_up(n * 4, 256) + align_up(n / B * 4, 256) + 256 + align_up(n * 4, 256) +
-           align_up(n * m.I * dtype_size(m.dtype), 256) +
-           std::max(split_bytes(1, &m, (int)B), split_bytes(2, &m, (int)B));
+           align_up(n * m.I * dtype_size(m.dtype), 256);
   return MOE_OK;
 }
 
@@ -482,9 +472,6 @@ moe_status_t moe_masked_forward(const moe_config_t* cfg, const void* x_masked,
   float* ones = (float*)b;
   b += align_up(n * 4, 256);
   void* act = b;
-  b += align_up(n * m.I * dtype_size(m.dtype), 256);
-  void* split_ws = b;  // split-K scratch, shared by the two GEMMs (they run one after another)
-  const size_t split_ws_bytes = std::max(split_bytes(1, &m, B), split_bytes(2, &m, B));
   st = launch_masked_table(counts, m.E, capacity, B, sid, eid, npp, row_w ? nullptr : ones,
                            stream);
   if (st != MOE_OK) return st;
@@ -496,11 +483,9 @@ moe_status_t moe_masked_forward(const moe_config_t* cfg, const void* x_masked,
   if (m.dtype == MOE_BF16) {
     if (!aligned16(x_masked) || !aligned16(W13) || !aligned16(W2) || !aligned16(y_masked))
       return MOE_ERR_INVALID_ARG;
-    st = launch_gemm1_tc(m, x_masked, W13, sid, eid, npp, B, rows, act, split_ws,
-                         split_ws_bytes, stream);
+    st = launch_gemm1_tc(m, x_masked, W13, sid, eid, npp, B, rows, act, stream);
     if (st != MOE_OK) return st;
-    return launch_gemm2_tc(m, act, W2, sid, eid, npp, B, rows, w, y_masked, split_ws,
-                           split_ws_bytes, stream);
+    return launch_gemm2_tc(m, act, W2, sid, eid, npp, B, rows, w, y_masked, stream);
   }
   st = launch_gemm1_simt(m, (const float*)x_masked, (const float*)W13, sid, eid, npp, B, rows,
                          (float*)act, stream);
@@ -557,18 +542,18 @@ moe_status_t moe_forward(const moe_config_t* c, const void* x, const void* Wg, c
     if ((st = launch_gemv1(e, x, false, W13, sid, eid, npp, L.block_m, b + L.act, stream)) !=
         MOE_OK)
       return st;
-  } else if (e.dtype == MOE_BF16) {  // gather pass, then the tensor-core GEMM1 (split-K scratch)
+  } else if (e.dtype == MOE_BF16) {  // gather pass, then the tensor-core GEMM1
     if ((st = moe_gather_rows(x, sid, npp, e.T, e.k, e.H, e.dtype, b + L.xs, stream)) != MOE_OK)
       return st;
     if ((st = moe_expert_gemm1_gathered(c, b + L.xs, W13, sid, eid, npp, L.block_m, b + L.act,
-                                        b + L.splitk, L.total - L.splitk, stream)) != MOE_OK)
+                                        nullptr, 0, stream)) != MOE_OK)
       return st;
   } else if ((st = moe_expert_gemm1(c, x, W13, sid, eid, npp, L.block_m, b + L.act, nullptr, 0,
                                     stream)) != MOE_OK) {
     return st;
   }
-  if ((st = moe_expert_gemm2(c, b + L.act, W2, sid, eid, npp, L.block_m, w, b + L.y,
-                             b + L.splitk, L.total - L.splitk, stream)) != MOE_OK)
+  if ((st = moe_expert_gemm2(c, b + L.act, W2, sid, eid, npp, L.block_m, w, b + L.y, nullptr,
+                             0, stream)) != MOE_OK)
     return st;
   if (c->expert_map)
     return moe_combine_local(b + L.y, ids, c->expert_map, e.E, e.T, e.k, e.H, e.dtype, out,

@@ -100,16 +100,13 @@ moe_status_t launch_gemm2_simt(const moe_config_t& c, const float* act, const fl
                                const int32_t* sid, const int32_t* eid, const int32_t* npp,
                                int block_m, int max_padded, const float* topk_w, float* y,
                                cudaStream_t s);
-// Split-K scratch (fp32 partials + tile counters) of grouped GEMM 1 or 2; 0 = no split.
-size_t gemm_split_bytes(int gemm, const moe_config_t& c, int max_padded);
 moe_status_t launch_gemm1_tc(const moe_config_t& c, const void* xs, const void* W13,
                              const int32_t* sid, const int32_t* eid, const int32_t* npp,
-                             int block_m, int max_padded, void* act, void* ws, size_t ws_bytes,
-                             cudaStream_t s);
+                             int block_m, int max_padded, void* act, cudaStream_t s);
 moe_status_t launch_gemm2_tc(const moe_config_t& c, const void* act, const void* W2,
                              const int32_t* sid, const int32_t* eid, const int32_t* npp,
                              int block_m, int max_padded, const float* topk_w, void* y,
-                             void* ws, size_t ws_bytes, cudaStream_t s);
+                             cudaStream_t s);
 // Grouped GEMMs of small bf16 batches on CUDA cores (gemv.cu): whether they apply to a
 // layer, and the two GEMMs with the tensor-core kernels' inputs and outputs (GEMM1 reads
 // the routed rows gathered in padded order, or the token rows through sorted_ids).

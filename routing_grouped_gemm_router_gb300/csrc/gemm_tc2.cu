@@ -39,9 +39,9 @@
 // kernel. Every mbarrier wait is bounded (time-out: status kStatusTimeout, abort, copies in
 // flight drained, TMEM freed).
 //
-// Variants of the same kernel: split-K for decode-sized problems (items split along K, fp32
-// partial sums, the last split of a tile finishes it), and FP8 E4M3 weights with 128 x 128
-// block scales, turned into the bf16 operand by converter warps (see Roles below).
+// A variant of the same kernel takes FP8 E4M3 weights with 128 x 128 block scales, turned
+// into the bf16 operand by converter warps (see Roles below). Batches of at most 128 tokens
+// run the decode kernel (gemm_dec.cu) instead.
 #include "tc_ptx.cuh"
 
 namespace moe {
@@ -78,14 +78,6 @@ struct Params {
   const float* scale;
   int sc_rb, sc_kb;  // row blocks and k blocks of one grid
   int n_slots;       // expert slots the weights hold
-  // Split-K (few work items, e.g. decode): each item is split ksplit ways along K; every
-  // split writes fp32 partial sums of its valid rows to part[split][row r][ldp], and the
-  // split that arrives last on the counter of its (m-tile, n-tile, warp quarter) adds them
-  // up and applies the epilogue.
-  int ksplit;
-  int ldp;
-  float* part;
-  int* cnt;
 };
 
 // FP8 weights add kCvtGroups groups of kCvtWarps converter warps (6..) and a ring of raw
@@ -158,100 +150,6 @@ __device__ __forceinline__ void item_of(int w, int n_tiles, const Table& tb, int
   m0 = tb.run_first[lo] + 2 * i;
   live1 = 2 * i + 1 < tb.run_len[lo];
   e = tb.run_e[lo];
-}
-
-// Work item w of a launch split ksplit ways along K -> base item and its k-block range.
-__device__ __forceinline__ void split_of(int w, int ksplit, int num_kb, int& wi, int& kb0,
-                                         int& kb1, int& sp) {
-  wi = w / ksplit;
-  sp = w - wi * ksplit;
-  kb0 = sp * num_kb / ksplit;
-  kb1 = (sp + 1) * num_kb / ksplit;
-}
-
-// Split-K completion for one warp's 32 rows of a tile (counter index ctr): the split that
-// arrives last adds the fp32 partials of every split in split order and applies the
-// epilogue (GEMM1: silu(gate) * up into act row p; GEMM2: topk_w[r] times the sum into y
-// row r), then resets the counter for the next launch. The warp reduces its valid rows one
-// after another with all 32 lanes across the columns, every split's loads in flight at
-// in flight two splits at a time; partials of other SMs are read from L2 (ld.global.cg)
-// after the threadfence / counter handshake.
-constexpr int kMaxSplit = 8;
-constexpr int kSplitBatch = 2;
-template <int MODE>
-__device__ void splitk_finish(const Params& P, int ctr, int p, int r, bool valid, int n) {
-  const int lane = threadIdx.x & 31;
-  __threadfence();
-  __syncwarp();
-  int prev = 0;
-  if (lane == 0) prev = atomicAdd(&P.cnt[ctr], 1);
-  prev = __shfl_sync(0xffffffffu, prev, 0);
-  if (prev != P.ksplit - 1) return;
-  __threadfence();
-  unsigned todo = __ballot_sync(0xffffffffu, valid);
-  while (todo) {
-    const int src = __ffs(todo) - 1;
-    todo &= todo - 1;
-    const int rr = __shfl_sync(0xffffffffu, r, src);
-    const int pp = __shfl_sync(0xffffffffu, p, src);
-    if (MODE == kGemm1) {
-      const int col = n * 128 + lane * 4;  // 4 gate and the matching 4 up columns per lane
-      float gs[4] = {0.f, 0.f, 0.f, 0.f}, us[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll 1
-      for (int s0 = 0; s0 < P.ksplit; s0 += kSplitBatch) {
-        float4 g[kSplitBatch], u[kSplitBatch];
-#pragma unroll
-        for (int b = 0; b < kSplitBatch; ++b)
-          if (s0 + b < P.ksplit) {
-            const float* row = P.part + ((int64_t)(s0 + b) * P.n_rows + rr) * P.ldp + col;
-            g[b] = __ldcg(reinterpret_cast<const float4*>(row));
-            u[b] = __ldcg(reinterpret_cast<const float4*>(row + P.ldp / 2));
-          }
-#pragma unroll
-        for (int b = 0; b < kSplitBatch; ++b)
-          if (s0 + b < P.ksplit) {
-            gs[0] += g[b].x; gs[1] += g[b].y; gs[2] += g[b].z; gs[3] += g[b].w;
-            us[0] += u[b].x; us[1] += u[b].y; us[2] += u[b].z; us[3] += u[b].w;
-          }
-      }
-      if (col < P.N) {
-        float a[4];
-#pragma unroll
-        for (int j = 0; j < 4; ++j) a[j] = gs[j] / (1.f + __expf(-gs[j])) * us[j];
-        __nv_bfloat16* dst = (__nv_bfloat16*)P.out + (int64_t)pp * P.ld_out + col;
-        *reinterpret_cast<uint2*>(dst) = make_uint2(pack_bf16(a[0], a[1]), pack_bf16(a[2], a[3]));
-      }
-    } else {
-      const int col = n * 256 + lane * 8;  // 8 output columns per lane
-      float a[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
-#pragma unroll 1
-      for (int s0 = 0; s0 < P.ksplit; s0 += kSplitBatch) {
-        float4 a0[kSplitBatch], a1[kSplitBatch];
-#pragma unroll
-        for (int b = 0; b < kSplitBatch; ++b)
-          if (s0 + b < P.ksplit) {
-            const float* row = P.part + ((int64_t)(s0 + b) * P.n_rows + rr) * P.ldp + col;
-            a0[b] = __ldcg(reinterpret_cast<const float4*>(row));
-            a1[b] = __ldcg(reinterpret_cast<const float4*>(row + 4));
-          }
-#pragma unroll
-        for (int b = 0; b < kSplitBatch; ++b)
-          if (s0 + b < P.ksplit) {
-            a[0] += a0[b].x; a[1] += a0[b].y; a[2] += a0[b].z; a[3] += a0[b].w;
-            a[4] += a1[b].x; a[5] += a1[b].y; a[6] += a1[b].z; a[7] += a1[b].w;
-          }
-      }
-      if (col < P.N) {
-        const float wr = P.topk_w[rr];
-        __nv_bfloat16* dst = (__nv_bfloat16*)P.out + (int64_t)rr * P.ld_out + col;
-        *reinterpret_cast<uint4*>(dst) =
-            make_uint4(pack_bf16(wr * a[0], wr * a[1]), pack_bf16(wr * a[2], wr * a[3]),
-                       pack_bf16(wr * a[4], wr * a[5]), pack_bf16(wr * a[6], wr * a[7]));
-      }
-    }
-  }
-  __syncwarp();
-  if (lane == 0) P.cnt[ctr] = 0;
 }
 
 template <int MODE, bool FP8>
@@ -390,7 +288,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Roles<FP8>::kThreads
   }
   __syncthreads();
   const Table tb{run_first, run_len, run_e, run_pref, *nruns_sh};
-  const int total = tb.nruns > 0 ? tb.run_pref[tb.nruns] * P.n_tiles * P.ksplit : 0;
+  const int total = tb.nruns > 0 ? tb.run_pref[tb.nruns] * P.n_tiles : 0;
   const int pair = blockIdx.x >> 1, num_pairs = gridDim.x >> 1;
   const int num_kb = (P.K + BK - 1) / BK;
 
@@ -399,12 +297,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Roles<FP8>::kThreads
     if (lane == 0) {
       int g = 0;
       for (int w = pair; w < total; w += num_pairs) {
-        int wi, kb0, kb1, sp, m0, n, e;
+        int m0, n, e;
         bool live1;
-        split_of(w, P.ksplit, num_kb, wi, kb0, kb1, sp);
-        item_of(wi, P.n_tiles, tb, m0, n, e, live1);
+        item_of(w, P.n_tiles, tb, m0, n, e, live1);
         bool ok = true;
-        for (int kb = kb0; kb < kb1; ++kb, ++g) {
+        for (int kb = 0; kb < num_kb; ++kb, ++g) {
           const int s = g % kStages;
           if (!wait_bounded(&empty[s], ((uint32_t)(g / kStages) & 1u) ^ 1u, abort_flag, status)) {
             ok = false;
@@ -439,9 +336,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Roles<FP8>::kThreads
         tc_fence_after();
         if (*abort_flag) break;
         const uint32_t d = tmem_base + (uint32_t)(acc * 256);
-        int wi, kb0, kb1, sp;
-        split_of(w, P.ksplit, num_kb, wi, kb0, kb1, sp);
-        for (int kb = kb0; kb < kb1; ++kb, ++g) {
+        for (int kb = 0; kb < num_kb; ++kb, ++g) {
           const int s = g % kStages;
           if (!wait_bounded(&full[s], (uint32_t)(g / kStages) & 1u, abort_flag, status)) {
             ok = false;
@@ -453,7 +348,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Roles<FP8>::kThreads
 #pragma unroll
           for (int kk = 0; kk < BK / UMMA_K; ++kk)
             umma_bf16<2>(d, sw128_desc(a + kk * 32), sw128_desc(b + kk * 32), IDESC,
-                         (kb != kb0 || kk != 0) ? 1u : 0u);
+                         (kb | kk) != 0 ? 1u : 0u);
           umma_commit_pair(&empty[s], 0x3);
           issued = true;
         }
@@ -474,12 +369,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Roles<FP8>::kThreads
     int acc = 0;
     uint32_t acc_phase = 0;
     for (int w = pair; w < total; w += num_pairs) {
-      int wi, kb0, kb1, sp, m0, n, e;
+      int m0, n, e;
       bool live1;
-      split_of(w, P.ksplit, num_kb, wi, kb0, kb1, sp);
-      item_of(wi, P.n_tiles, tb, m0, n, e, live1);
+      item_of(w, P.n_tiles, tb, m0, n, e, live1);
       const bool live = leader || live1;
-      const bool split = P.ksplit > 1;
       int ok = 1;
       if (lane == 0) ok = wait_bounded(&tfull[acc], acc_phase, abort_flag, status);
       ok = __shfl_sync(0xffffffffu, ok, 0);
@@ -489,26 +382,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Roles<FP8>::kThreads
       const int p = (m0 + (int)rank) * BM + row;
       const int r = live ? P.sid[p] : P.n_rows;
       const bool valid = r < P.n_rows;
-      if (split) {  // fp32 partial sums of the valid rows; the last split finishes below
-        float* prow = P.part + ((int64_t)sp * P.n_rows + (valid ? r : 0)) * P.ldp;
-        // 32-column chunks of the accumulator; GEMM1: gate chunks 0..3, then up chunks 4..7
-        // (TMEM columns 128..255, partial columns ldp/2 + ...)
-#pragma unroll 1
-        for (int c = 0; c < 8; ++c) {
-          uint32_t v0[32];
-          tmem_ld32(tbase + c * 32, v0);
-          tmem_ld_wait();
-          if (valid) {
-            float* d0 = prow + (MODE == kGemm1 ? (c < 4 ? 0 : P.ldp / 2) + n * 128 + (c & 3) * 32
-                                               : n * 256 + c * 32);
-#pragma unroll
-            for (int v = 0; v < 8; ++v)
-              reinterpret_cast<float4*>(d0)[v] =
-                  make_float4(__uint_as_float(v0[4 * v]), __uint_as_float(v0[4 * v + 1]),
-                              __uint_as_float(v0[4 * v + 2]), __uint_as_float(v0[4 * v + 3]));
-          }
-        }
-      } else if (MODE == kGemm1) {
+      if (MODE == kGemm1) {
         __nv_bfloat16* dst = (__nv_bfloat16*)P.out + (int64_t)p * P.ld_out + n * 128;
         const int col0 = n * 128;
 #pragma unroll 1
@@ -569,10 +443,6 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Roles<FP8>::kThreads
         else mbar_arrive_cta(&tempty[acc], 0);
       }
       if (++acc == kAccs) { acc = 0; acc_phase ^= 1u; }
-      // Split-K: rows of this warp that are real (the same set in every split) meet on the
-      // counter of (m-tile, n-tile, quarter); the accumulator was released above.
-      if (split && __any_sync(0xffffffffu, valid))
-        splitk_finish<MODE>(P, (((m0 + (int)rank) * P.n_tiles) + n) * 4 + q, p, r, valid, n);
     }
   } else if (FP8 && warp >= R::kCvtWarp0) {
     // ------------------------------------------------------------ FP8 converters (4 warps)
@@ -585,16 +455,15 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Roles<FP8>::kThreads
     const int grid = MODE == kGemm1 ? (int)rank : 0;
     int g = 0;
     for (int w = pair; w < total; w += num_pairs) {
-      int wi, kb0, kb1, sp, m0, n, e;
+      int m0, n, e;
       bool live1;
-      split_of(w, P.ksplit, num_kb, wi, kb0, kb1, sp);
-      item_of(wi, P.n_tiles, tb, m0, n, e, live1);
+      item_of(w, P.n_tiles, tb, m0, n, e, live1);
       const int rb = MODE == kGemm1 ? n : 2 * n + (int)rank;
       const bool sc_ok = e >= 0 && e < P.n_slots && rb < P.sc_rb;
       const float* srow =
           P.scale + (((int64_t)e * (MODE == kGemm1 ? 2 : 1) + grid) * P.sc_rb + rb) * P.sc_kb;
       bool ok = true;
-      for (int kb = kb0; kb < kb1; ++kb, ++g) {
+      for (int kb = 0; kb < num_kb; ++kb, ++g) {
         if ((g % kStages) % R::kCvtGroups != grp) continue;  // the group's own slots
         const int s = g % kStages;
         const float sc = sc_ok ? __ldg(srow + (kb >> 1)) : 0.f;  // in flight during the wait
@@ -696,70 +565,6 @@ static int max_items_for(int max_padded, int n_rows, int E, int n_tiles) {
   return ((tiles + std::min(E, n_rows)) / 2 + 1) * n_tiles;
 }
 
-// Split-K plan of one grouped GEMM, from host-known sizes only (so workspace sizes can be
-// computed before any launch). The split count minimises a makespan model: every pair runs
-// ceil(items * ksplit / pairs) items of num_kb / ksplit k-blocks plus a fixed per-item cost
-// of about four k-blocks (accumulator hand-off, epilogue, partial sums); at most 8 splits,
-// at least one k-block each. Splitting is kept to T*k <= 128 (the partial sums stay a few
-// hundred KB) and to plans the model rates at least 10 % faster; there every expert holds at
-// most one m-tile, so the item count is at most min(E, T*k) per n-tile.
-struct SplitPlan {
-  int ksplit, ldp, n_tiles;
-  size_t part_bytes, cnt_bytes;
-};
-static SplitPlan split_plan(int mode, const moe_config_t& c, int max_padded) {
-  SplitPlan sp{};
-  const int K = mode == kGemm1 ? c.H : c.I;
-  sp.n_tiles = mode == kGemm1 ? ceil_div(c.I, 128) : ceil_div(c.H, 256);
-  sp.ldp = mode == kGemm1 ? 2 * sp.n_tiles * 128 : sp.n_tiles * 256;
-  const int n_rows = c.T * c.k;
-  int items = max_items_for(max_padded, n_rows, c.E, sp.n_tiles);
-  if (n_rows <= BM) items = std::min(items, std::min(c.E, n_rows) * sp.n_tiles);
-  items = std::max(items, 1);
-  const int pairs = std::max(1, num_sms() / 2);
-  const int num_kb = ceil_div(K, BK);
-  sp.ksplit = 1;
-  if (c.dtype == MOE_BF16 && n_rows <= BM) {
-    const double t1 = (double)ceil_div(items, pairs) * (num_kb + 4.0);
-    double best = 0.9 * t1;
-    for (int ks = 2; ks <= std::min(kMaxSplit, num_kb); ++ks) {
-      const double t = (double)ceil_div(items * ks, pairs) * ((double)num_kb / ks + 4.0);
-      if (t < best) {
-        best = t;
-        sp.ksplit = ks;
-      }
-    }
-  }
-  if (sp.ksplit > 1) {
-    sp.part_bytes = align_up((size_t)sp.ksplit * n_rows * sp.ldp * sizeof(float), 256);
-    sp.cnt_bytes = align_up((size_t)(max_padded / BM) * sp.n_tiles * 4 * sizeof(int), 256);
-  }
-  return sp;
-}
-
-__global__ void __launch_bounds__(256) zero_counters_kernel(int* __restrict__ p, int n) {
-  pdl_wait();
-  pdl_trigger();
-  for (int i = blockIdx.x * blockDim.x + threadIdx.x; i < n; i += gridDim.x * blockDim.x) p[i] = 0;
-}
-
-// Points P at the split-K scratch in ws and zeroes the counters (an enqueued kernel).
-static moe_status_t setup_split(const SplitPlan& sp, void* ws, size_t ws_bytes, Params& P,
-                                cudaStream_t s) {
-  P.ksplit = sp.ksplit;
-  P.ldp = sp.ldp;
-  P.part = nullptr;
-  P.cnt = nullptr;
-  if (sp.ksplit == 1) return MOE_OK;
-  if (!ws || ws_bytes < sp.part_bytes + sp.cnt_bytes || ((uintptr_t)ws & 255u))
-    return MOE_ERR_WORKSPACE;
-  P.part = (float*)ws;
-  P.cnt = (int*)((uint8_t*)ws + sp.part_bytes);
-  const int n = (int)(sp.cnt_bytes / sizeof(int));
-  return launch_k(zero_counters_kernel, dim3(std::min(ceil_div(n, 256), 64)), dim3(256), 0, s,
-                  P.cnt, n);
-}
-
 // Failure-path self-test: one CTA allocates tensor memory, then two warps wait, through the
 // same bounded wait as the GEMM pipelines, on mbarriers that nothing ever arrives on. The
 // first wait gives up after the pipeline time limit, raises the CTA's abort flag and records
@@ -810,15 +615,9 @@ int grouped_status_read(int reset) {
   return v;
 }
 
-size_t gemm_split_bytes(int gemm, const moe_config_t& c, int max_padded) {
-  const tc2::SplitPlan sp = tc2::split_plan(gemm == 1 ? tc2::kGemm1 : tc2::kGemm2, c, max_padded);
-  return sp.part_bytes + sp.cnt_bytes;
-}
-
 moe_status_t launch_gemm1_tc(const moe_config_t& c, const void* xs, const void* W13,
                              const int32_t* sid, const int32_t* eid, const int32_t* npp,
-                             int block_m, int max_padded, void* act, void* ws, size_t ws_bytes,
-                             cudaStream_t s) {
+                             int block_m, int max_padded, void* act, cudaStream_t s) {
   using namespace tc2;
   if (max_padded / BM > kMaxTiles) return MOE_ERR_UNSUPPORTED;
   const bool fp8 = c.weight_format == MOE_WEIGHTS_FP8_E4M3_B128;
@@ -852,10 +651,7 @@ moe_status_t launch_gemm1_tc(const moe_config_t& c, const void* xs, const void* 
   P.sc_rb = ceil_div(c.I, 128);
   P.sc_kb = ceil_div(c.H, 128);
   P.n_slots = c.E;
-  const SplitPlan sp = split_plan(kGemm1, c, max_padded);
-  moe_status_t st = setup_split(sp, ws, ws_bytes, P, s);
-  if (st != MOE_OK) return st;
-  const int items = max_items_for(max_padded, P.n_rows, c.E, P.n_tiles) * sp.ksplit;
+  const int items = max_items_for(max_padded, P.n_rows, c.E, P.n_tiles);
   return fp8 ? launch<kGemm1, true>(mA, mG, mU, P, items, s)
              : launch<kGemm1, false>(mA, mG, mU, P, items, s);
 }
@@ -863,7 +659,7 @@ moe_status_t launch_gemm1_tc(const moe_config_t& c, const void* xs, const void* 
 moe_status_t launch_gemm2_tc(const moe_config_t& c, const void* act, const void* W2,
                              const int32_t* sid, const int32_t* eid, const int32_t* npp,
                              int block_m, int max_padded, const float* topk_w, void* y,
-                             void* ws, size_t ws_bytes, cudaStream_t s) {
+                             cudaStream_t s) {
   using namespace tc2;
   if (max_padded / BM > kMaxTiles) return MOE_ERR_UNSUPPORTED;
   const bool fp8 = c.weight_format == MOE_WEIGHTS_FP8_E4M3_B128;
@@ -896,10 +692,7 @@ moe_status_t launch_gemm2_tc(const moe_config_t& c, const void* act, const void*
   P.sc_rb = ceil_div(c.H, 128);
   P.sc_kb = ceil_div(c.I, 128);
   P.n_slots = c.E;
-  const SplitPlan sp = split_plan(kGemm2, c, max_padded);
-  moe_status_t st = setup_split(sp, ws, ws_bytes, P, s);
-  if (st != MOE_OK) return st;
-  const int items = max_items_for(max_padded, P.n_rows, c.E, P.n_tiles) * sp.ksplit;
+  const int items = max_items_for(max_padded, P.n_rows, c.E, P.n_tiles);
   return fp8 ? launch<kGemm2, true>(mA, mB, mB, P, items, s)
              : launch<kGemm2, false>(mA, mB, mB, P, items, s);
 }
