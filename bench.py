@@ -30,6 +30,7 @@ import moe_inputs as mi  # noqa: E402
 
 METRIC = "MoE layer TFLOPS (6*T*k*H*I/s) & % BF16 peak; decode weight GB/s vs HBM"
 DEFAULT_WORKLOAD = "mixtral-prefill"
+DEC_MAX_TOKENS = 128  # bf16-activation batches up to this size run the decode GEMM kernel
 
 
 def parse(argv=None):
@@ -59,6 +60,9 @@ def parse(argv=None):
                    help="override T of the workload (smaller cases for profiling)")
     p.add_argument("--experts", type=int, default=0,
                    help="override E of the workload (smaller cases for profiling)")
+    p.add_argument("--inter", type=int, default=0,
+                   help="override I of the workload (captures of the routing kernels, which "
+                        "depend on T, H, E and k only, with small expert weights)")
     p.add_argument("--no-sweep", action="store_true",
                    help="only the headline workload (the default run also measures the other "
                         "prefill shapes, the decode sweep and FP8 decode)")
@@ -86,6 +90,27 @@ def peaks():
         return 6800.0, 1900.0, 1700.0, "fallback"
 
 
+def source_hash(src_path: str) -> str:
+    """sha256 of a kernel's source: the file, then every header it includes from its own
+    directory (recursively, each once, in include order), so that an edit to a kernel body
+    kept in a header voids the summaries taken on the old code."""
+    d, seen = os.path.dirname(src_path), []
+
+    def visit(path):
+        if path in seen:
+            return
+        seen.append(path)
+        for m in re.finditer(r'#include "([^"]+)"', open(path).read()):
+            q = os.path.join(d, m.group(1))
+            if os.path.exists(q):
+                visit(q)
+    visit(src_path)
+    h = hashlib.sha256()
+    for path in seen:
+        h.update(open(path, "rb").read())
+    return h.hexdigest()
+
+
 def profile_traffic(kernel: str, wl_name: str, active: int, src_path: str):
     """DRAM bytes per launch recorded in a committed ncu summary, if the kernel source it
     was taken on is unchanged (the summary stores the source's sha256); else None.
@@ -100,7 +125,7 @@ def profile_traffic(kernel: str, wl_name: str, active: int, src_path: str):
         return None
     txt = open(path).read()
     h = re.search(r"source_sha256:\s*([0-9a-f]{64})", txt)
-    if not h or hashlib.sha256(open(src_path, "rb").read()).hexdigest() != h.group(1):
+    if not h or source_hash(src_path) != h.group(1):
         return None
     m = re.search(r"traffic_bytes_per_launch:\s*([0-9.eE+]+)", txt)
     if m:
@@ -404,9 +429,11 @@ def measure_layer(args, wl, ctx, seed, steps, warmup, shared=0, fp8=False, ep_ha
     out = torch.empty(T, H, dtype=inp.x.dtype, device=dev)
     stream = torch.cuda.current_stream(dev)
     sh = stream.cuda_stream
-    # bf16 GEMM1 = row gather + tensor-core GEMM, timed apart; small batches (decode up to
-    # 8 tokens) run the CUDA-core grouped GEMMs, which read the token rows in place
+    # bf16 GEMM1 = row gather + tensor-core GEMM, timed apart; small batches (up to 2 tokens,
+    # 12 with FP8 weights) run the CUDA-core grouped GEMMs, which read the token rows in
+    # place; other batches of up to 128 tokens run the decode tensor-core kernel
     small = L.moe_small_batch(cfg)
+    dec = wl.dtype == "bf16" and not small and T <= DEC_MAX_TOKENS
     gathered = wl.dtype == "bf16" and not small
     def step(ev=None, sh=sh, c=0):
         # The same kernels moe_forward enqueues, called stage by stage so that CUDA events
@@ -510,7 +537,8 @@ def measure_layer(args, wl, ctx, seed, steps, warmup, shared=0, fp8=False, ep_ha
     stage = {n: statistics.mean(e[i].elapsed_time(e[i + 1]) for e in evs)
              for i, n in enumerate(("route", "align", "gather", "gemm1", "gemm2", "combine"))}
     res = {"ms": ms, "stage": stage, "clocks": clocks, "npp": npp, "active": active,
-           "local_rows": local_rows, "small": bool(small), "n_copies": n_copies,
+           "local_rows": local_rows, "small": bool(small), "dec": bool(dec),
+           "n_copies": n_copies,
            "wbytes": wbytes, "launches_per_step": launches_per_step, "graph": bool(graphs),
            "T": T, "k": k, "E": E, "H": H, "I": I, "block_m": B}
     del graphs
@@ -567,7 +595,8 @@ def summarize(wl, m, world, fp8=False):
         roof = {"bound": "hbm", "achieved": w_bytes / (g1_ms * 1e-3) / 1e9, "peak": hbm,
                 "unit": "GB/s",
                 "kernel": "gemm1 (gate/up grouped GEMV, small batch)" if m["small"] else
-                          "gemm1 (gate/up grouped GEMM)",
+                          "gemm1 (gate/up decode grouped GEMM, weights as the 128-row operand)"
+                          if m["dec"] else "gemm1 (gate/up grouped GEMM)",
                 "algorithmic_bytes_per_launch": w_bytes,
                 "peak_kind": f"{peak_src} HBM copy bandwidth"}
     else:
@@ -578,9 +607,9 @@ def summarize(wl, m, world, fp8=False):
                 "algorithmic_flops_per_launch": g1_flops,
                 "peak_kind": f"{peak_src} bf16 burst (GEMM1 timed alone, CUDA events)"}
     roof["frac"] = roof["achieved"] / roof["peak"]
-    kern = "gemv1" if m["small"] else "gemm1"
-    src = os.path.join(ROOT, "routing_grouped_gemm_router_gb300", "csrc",
-                       "gemv.cu" if m["small"] else "gemm_tc2.cu")
+    kern, src = (("gemv1", "gemv.cu") if m["small"] else ("gemmdec1", "gemm_dec.cu")
+                 if m["dec"] else ("gemm1", "gemm_tc2.cu"))
+    src = os.path.join(ROOT, "routing_grouped_gemm_router_gb300", "csrc", src)
     roof["traffic"] = profile_traffic(kern + ("_fp8" if fp8 else ""), wl.name, active, src)
     return _line_fields(wl, m, world, value, intensity, hbm_bound, roof, hbm, bf16_burst)
 
@@ -665,7 +694,8 @@ def run_ours(args, wl, measure=None):
     if "cpu_baseline" in m:
         line["cpu_baseline"] = m["cpu_baseline"]
     if world == 1 and not args.no_sweep and args.workload == DEFAULT_WORKLOAD and \
-            not (args.tokens or args.experts or args.fp8 or args.shared or args.ep_half):
+            not (args.tokens or args.experts or args.inter or args.fp8 or args.shared or
+                 args.ep_half):
         line["sweep"] = run_sweep(args, ctx)
     if rank == 0:
         print(json.dumps(line), flush=True)
@@ -751,6 +781,9 @@ def main():
     if args.experts:
         import dataclasses
         wl = dataclasses.replace(wl, E=args.experts, name=f"{wl.name}@E={args.experts}")
+    if args.inter:
+        import dataclasses
+        wl = dataclasses.replace(wl, I=args.inter, name=f"{wl.name}@I={args.inter}")
     if args.impl == "reference":
         run_reference(args, wl)
     elif args.masked:

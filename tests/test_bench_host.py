@@ -49,6 +49,24 @@ def test_changed_kernel_source_voids_the_traffic(tmp_path, monkeypatch):
     assert bench.profile_traffic("gemm1", "gpt-oss-decode@T=1", 4, src) is None
 
 
+def test_included_header_edit_voids_the_traffic(tmp_path, monkeypatch):
+    """The pinned hash covers the headers a kernel file includes from its directory: an edit
+    to a kernel body kept in a header voids the figure; one to another file does not."""
+    src = _setup(tmp_path, monkeypatch, "traffic_bytes_per_launch: 1.5e9\nsource_sha256: SHA\n",
+                 b'#include "k_dev.cuh"\n#include <cstdint>\n')
+    (tmp_path / "k_dev.cuh").write_bytes(b"device code")
+    (tmp_path / "other.cuh").write_bytes(b"unrelated")
+    txt = (tmp_path / "profiles" / "gemv1_gpt-oss-decode.md").read_text()
+    (tmp_path / "profiles" / "gemv1_gpt-oss-decode.md").write_text(
+        txt.replace(hashlib.sha256(b'#include "k_dev.cuh"\n#include <cstdint>\n').hexdigest(),
+                    bench.source_hash(src)))
+    assert bench.profile_traffic("gemv1", "gpt-oss-decode", 128, src) == 1.5e9
+    (tmp_path / "other.cuh").write_bytes(b"edited")
+    assert bench.profile_traffic("gemv1", "gpt-oss-decode", 128, src) == 1.5e9
+    (tmp_path / "k_dev.cuh").write_bytes(b"device code, edited")
+    assert bench.profile_traffic("gemv1", "gpt-oss-decode", 128, src) is None
+
+
 def test_committed_summaries_parse():
     """Every committed summary that bench.py may read names a source hash and a traffic
     figure in one of the two forms."""
