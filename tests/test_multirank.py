@@ -86,7 +86,7 @@ def _repo_arm_worker(rank, world, port, q):
                 "stage": {n: ms / 6 for n in ("route", "align", "gather", "gemm1", "gemm2",
                                               "combine")},
                 "clocks": {"sm_mhz": None}, "npp": T * k, "active": wl.E,
-                "local_rows": T * k, "small": False, "n_copies": 1, "wbytes": 4,
+                "local_rows": T * k, "small": False, "dec": False, "n_copies": 1, "wbytes": 4,
                 "launches_per_step": 7, "graph": True, "T": T, "k": k, "E": wl.E, "H": H,
                 "I": I, "block_m": 16}
 
