@@ -298,6 +298,8 @@ moe_status_t moe_combine_local(const void* y, const int32_t* topk_ids, const int
  *   y_masked[e, i, :] = row_w[e, i] * W2[e] (silu(W1[e] x) * (W3[e] x)),   x = x_masked[e, i]
  * (row_w: device fp32 [E, C], or NULL for weight 1). Rows past a count are never written.
  * C must be a multiple of moe_block_m(cfg); cfg->T, k and the router fields are ignored.
+ * bf16 with C = 128 (one tile per expert, the decode case) runs the decode tensor-core
+ * GEMMs, which stream each active expert's weights once; larger C the CTA-pair GEMMs.
  * moe_masked_table builds the equivalent sorted_ids / expert_ids / num_post_padded (the
  * identity on valid rows, tiles past a count labelled -1) for callers of the GEMM entries. */
 moe_status_t moe_masked_table(const int32_t* counts, int E, int capacity, int block_m,

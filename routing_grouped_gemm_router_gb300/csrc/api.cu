@@ -483,6 +483,13 @@ moe_status_t moe_masked_forward(const moe_config_t* cfg, const void* x_masked,
   if (m.dtype == MOE_BF16) {
     if (!aligned16(x_masked) || !aligned16(W13) || !aligned16(W2) || !aligned16(y_masked))
       return MOE_ERR_INVALID_ARG;
+    if (dec_masked_applies(m, capacity)) {
+      // capacity 128: at most one tile per expert, holding its few tokens (decode); the
+      // decode kernels stream each active expert's weights once
+      st = launch_gemm1_dec(m, x_masked, W13, sid, eid, npp, B, rows, act, stream);
+      if (st != MOE_OK) return st;
+      return launch_gemm2_dec(m, act, W2, sid, eid, npp, B, rows, w, y_masked, stream);
+    }
     st = launch_gemm1_tc(m, x_masked, W13, sid, eid, npp, B, rows, act, stream);
     if (st != MOE_OK) return st;
     return launch_gemm2_tc(m, act, W2, sid, eid, npp, B, rows, w, y_masked, stream);

@@ -121,6 +121,7 @@ moe_status_t launch_gemv2(const moe_config_t& c, const void* act, const void* W2
 // MMA operand (gemm_dec.cu): whether they apply, and the two GEMMs with the pair kernels'
 // inputs and outputs (GEMM1 reads the routed rows gathered in padded order).
 bool dec_gemm_applies(const moe_config_t& c, int max_padded);
+bool dec_masked_applies(const moe_config_t& m, int capacity);
 moe_status_t launch_gemm1_dec(const moe_config_t& c, const void* xs, const void* W13,
                               const int32_t* sid, const int32_t* eid, const int32_t* npp,
                               int block_m, int max_padded, void* act, cudaStream_t s);

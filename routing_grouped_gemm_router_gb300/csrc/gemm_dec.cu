@@ -549,6 +549,12 @@ bool dec_gemm_applies(const moe_config_t& c, int max_padded) {
   return c.dtype == MOE_BF16 && c.T <= dec::kMaxTokens && max_padded / 128 <= dec::kMaxTiles;
 }
 
+// The fixed-capacity layout with at most one 128-row tile per expert (capacity 128, the
+// decode case: each tile holds an expert's few tokens, empty tiles are labelled -1).
+bool dec_masked_applies(const moe_config_t& m, int capacity) {
+  return m.dtype == MOE_BF16 && capacity == 128 && m.T / 128 <= dec::kMaxTiles;
+}
+
 moe_status_t launch_gemm1_dec(const moe_config_t& c, const void* xs, const void* W13,
                               const int32_t* sid, const int32_t* eid, const int32_t* npp,
                               int block_m, int max_padded, void* act, cudaStream_t s) {

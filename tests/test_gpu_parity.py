@@ -700,6 +700,41 @@ def test_masked_layout(L, dtype, with_w):
     assert np.array_equal(eid.cpu().numpy(), exp_eid)
 
 
+@pytest.mark.parametrize("fp8", [False, True], ids=["bf16", "fp8"])
+def test_masked_layout_capacity_128(L, fp8):
+    """Capacity 128 (one tile per expert, the decode case) takes the decode tensor-core
+    kernels: empty experts, experts of 1-9 rows and one full tile (128 rows) all match the
+    oracle's masked forward, and rows past each count are never written."""
+    H, I, E, B = 320, 272, 12, 128
+    wl = mi.Workload("masked-128", T=1, H=H, I=I, E=E, k=1, dtype="bf16", seed=53)
+    inp = mi.make_layer(wl, "cpu")
+    counts = np.array([0, 1, 3, 9, 0, 2, 128, 5, 1, 0, 7, 4], dtype=np.int32)
+    g = torch.Generator().manual_seed(54)
+    xm = torch.randn(E, B, H, generator=g).bfloat16()
+    wm = (torch.rand(E, B, generator=g) + 0.5).numpy()
+    W13, W2, sc = inp.W13, inp.W2, {}
+    if fp8:
+        (W13, s13), (W2, s2) = mi.quantize_fp8_w13(W13), mi.quantize_fp8_blocks(W2)
+        sc = dict(w13_scale=s13.to(DEV), w2_scale=s2.to(DEV))
+        W13o = O.dequant_w13(W13.numpy(), s13.double().numpy())
+        W2o = O.dequant_blockwise(W2.numpy(), s2.double().numpy())
+    else:
+        W13o, W2o = weights_for_oracle(W13), weights_for_oracle(W2)
+    cfg = L.make_config(1, H, I, E, 1, L.MOE_BF16, **sc)
+    y = torch.full((E, B, H), float("nan"), dtype=torch.bfloat16, device=DEV)
+    wsb = L.moe_masked_workspace_size(cfg, B)
+    ws = torch.empty(wsb, dtype=torch.uint8, device=DEV)
+    L.moe_masked_forward(cfg, xm.to(DEV), torch.tensor(counts, device=DEV), B,
+                         torch.tensor(wm, device=DEV), W13.to(DEV), W2.to(DEV), y, ws, wsb)
+    torch.cuda.synchronize()
+    assert L.moe_device_status(True) == 0
+    ref = O.masked_forward(to_np(xm), counts, W13o, W2o, wm)
+    got = to_np(y)
+    valid = np.arange(B)[None, :] < counts[:, None]
+    assert np.all(np.isnan(got[~valid])), "a row past an expert's count was written"
+    assert_close(got[valid], ref[valid], "bf16")
+
+
 # --------------------------------------------------------------------- FP8 expert weights
 
 FP8_CASES = [
