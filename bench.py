@@ -90,10 +90,16 @@ def peaks():
         return 6800.0, 1900.0, 1700.0, "fallback"
 
 
+# Headers left out of a kernel's source hash: common.cuh is the library's internal launch
+# table (host declarations of every launcher) plus one-line helpers, included everywhere; an
+# entry point added there does not change any kernel.
+HASH_SKIP = ("common.cuh",)
+
+
 def source_hash(src_path: str) -> str:
     """sha256 of a kernel's source: the file, then every header it includes from its own
-    directory (recursively, each once, in include order), so that an edit to a kernel body
-    kept in a header voids the summaries taken on the old code."""
+    directory (recursively, each once, in include order; HASH_SKIP excepted), so that an edit
+    to a kernel body kept in a header voids the summaries taken on the old code."""
     d, seen = os.path.dirname(src_path), []
 
     def visit(path):
@@ -102,7 +108,7 @@ def source_hash(src_path: str) -> str:
         seen.append(path)
         for m in re.finditer(r'#include "([^"]+)"', open(path).read()):
             q = os.path.join(d, m.group(1))
-            if os.path.exists(q):
+            if os.path.exists(q) and m.group(1) not in HASH_SKIP:
                 visit(q)
     visit(src_path)
     h = hashlib.sha256()
