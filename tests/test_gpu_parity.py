@@ -528,8 +528,9 @@ def test_all_tokens_to_one_expert(L):
     assert_close(to_np(out), ref, "bf16")
 
 
-def test_cuda_graph_capture_and_replay(L):
-    wl = mi.Workload("graph", T=256, H=256, I=256, E=16, k=4, dtype="bf16", seed=21)
+@pytest.mark.parametrize("T", [256, 48])  # the CTA-pair GEMMs; the decode tensor-core GEMMs
+def test_cuda_graph_capture_and_replay(L, T):
+    wl = mi.Workload("graph", T=T, H=256, I=256, E=16, k=4, dtype="bf16", seed=21)
     inp = _to_dev(mi.make_layer(wl, "cpu"))
     layer = _layer(L, inp)
     x_static = inp.x.clone()
@@ -557,7 +558,8 @@ def test_cuda_graph_capture_and_replay(L):
 
 @pytest.mark.parametrize("dtype,variant,T", [("bf16", "half", 300), ("bf16", "perm", 300),
                                              ("f32", "half", 300), ("fp8", "perm", 300),
-                                             ("bf16", "half", 2), ("fp8", "perm", 6)])
+                                             ("bf16", "half", 2), ("fp8", "perm", 6),
+                                             ("bf16", "half", 40), ("fp8", "perm", 40)])
 def test_expert_map(L, dtype, variant, T):
     """Odd experts held elsewhere (map -1), or local experts stored in permuted weight slots:
     the layer equals the oracle with the same expert_map; tiles carry the mapped labels.
@@ -623,7 +625,7 @@ def test_combine_local_skips_and_flags_bad_expert_id(L):
 
 # --------------------------------------------------------------------- shared experts
 
-@pytest.mark.parametrize("dtype,T", [("bf16", 200), ("f32", 200), ("bf16", 2)])
+@pytest.mark.parametrize("dtype,T", [("bf16", 200), ("f32", 200), ("bf16", 2), ("bf16", 40)])
 def test_shared_expert(L, dtype, T):
     """DeepSeek-style layer with one shared expert (weight 1 on every token), grouped
     sigmoid routing with scale 2.5: equals the oracle with the shared slot appended."""
