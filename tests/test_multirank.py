@@ -82,7 +82,7 @@ def _repo_arm_worker(rank, world, port, q):
         ms = bench.timed(ctx, steps, lambda i: time.sleep(0.02 * (ctx.rank + 1)),
                          lambda: None, bench.WallTimer())
         T, k, H, I = wl.T, wl.k, wl.H, wl.I
-        return {"ms": ms, "e2e_ms": 2 * ms, "io_bytes": T * H * 4,
+        return {"ms": ms, "e2e_ms": 2 * ms, "e2e_serial_ms": 3 * ms, "io_bytes": T * H * 4,
                 "stage": {n: ms / 6 for n in ("route", "align", "gather", "gemm1", "gemm2",
                                               "combine")},
                 "clocks": {"sm_mhz": None}, "npp": T * k, "active": wl.E,
@@ -128,6 +128,7 @@ def test_repo_arm_rank_plumbing_gloo():
     assert abs(d["value"] - 2 * flops / (d["ms_per_step"] * 1e-3) / 1e12) <= 1e-9 * d["value"]
     assert d["config"]["global_batch"] == 2 * wl.T and d["config"]["parallelism"] == "replicas x2"
     assert abs(d["e2e"]["value"] - d["value"] / 2) <= 1e-9 * d["value"]
+    assert abs(d["e2e"]["serial"]["value"] - d["value"] / 3) <= 1e-9 * d["value"]
     assert d["gpu_launches"] == 7 * 3
 
 
