@@ -25,20 +25,19 @@
 // FP8 E4M3 weights (128 x 128 block scales): the producer streams raw codes into a ring of
 // their own, several k-blocks deep; eight converter warps turn each k-block into the bf16
 // operand (code * scale, exact for power-of-two scales) in a shallower operand ring, and a
-// warp of its own streams the tile rows into a third ring, all with CTA-local barriers.
-// Measured per k-block (timestamps in the kernel): the raw codes wait long before they are
-// needed, so conversion and the tile rows set the pace. Each lane therefore loads all of its
-// codes of a k-block before it stores any converted operand (the stores could otherwise
-// alias the next loads, which serialises them), and the tile rows are requested several
-// k-blocks ahead instead of when an operand slot frees (behind the weight copies in flight,
-// that cost about a microsecond per k-block).
+// warp of its own streams the tile rows into a third ring (slots sized to the item's rows),
+// all with CTA-local barriers, so that no copy waits for an operand slot. Each converter lane
+// loads all of its codes of a k-block before it stores any converted operand (the stores
+// could otherwise alias the next loads, which serialises them). Measured per k-block
+// (timestamps in the kernel): the codes wait in their ring long before they are needed; the
+// converters' integer work (~0.5 us a k-block) and the MMA thread (~0.26 us fixed per
+// k-block plus ~32 ns per N = 16 MMA) set the pace.
 //
 // Warp roles: 0 TMA producer (weights; bf16 also the tile rows), 1 MMA issuer (one lane),
 // 2-5 epilogue; FP8 adds 8 converters on warps 6-15 and the tile-row producer on warp 16.
 // Every mbarrier wait is bounded (time-out: status kStatusTimeout, abort, copies in flight
-// drained, TMEM freed). All roles but the MMA issuer wait with a suspend hint: measured (ncu),
-// the polling of the waiting warps took about half of all issue slots of the FP8 variant,
-// away from the converters.
+// drained, TMEM freed). All roles but the MMA issuer wait with a suspend hint, so that
+// waiting warps do not take issue slots from the converters.
 #include "tc_ptx.cuh"
 
 namespace moe {
