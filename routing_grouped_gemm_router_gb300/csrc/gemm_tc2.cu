@@ -308,8 +308,14 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Roles<FP8>::kThreads
             break;
           }
           const uint32_t fl = cluster_addr(&full[s], 0);
-          if (leader) mbar_expect_tx(&full[s], R::kPairTmaBytes);
-          tma_2d_pair(sA + s * A_BYTES, &tmA, fl, kb * BK, (m0 + (int)rank) * BM);
+          // An expert's odd last m-tile runs in a pair whose peer half is masked (its rows are
+          // never stored): the peer copies no A tile then, and its MMA rows read whatever the
+          // slot held. That is one 16 KB tile a stage less through L2 on every such item
+          // (all of them when experts hold one tile, as in DeepSeek-V3-shaped layers).
+          if (leader)
+            mbar_expect_tx(&full[s], live1 ? R::kPairTmaBytes : R::kPairTmaBytes - A_BYTES);
+          if (leader || live1)
+            tma_2d_pair(sA + s * A_BYTES, &tmA, fl, kb * BK, (m0 + (int)rank) * BM);
           // leader: gate rows of panel n (GEMM1) / rows n*256 .. +127 of W2[e] (GEMM2);
           // peer: the up rows / the next 128 rows
           const CUtensorMap* tb_map = (MODE == kGemm1 && rank) ? &tmB1 : &tmB0;
