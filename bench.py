@@ -30,7 +30,6 @@ import moe_inputs as mi  # noqa: E402
 
 METRIC = "MoE layer TFLOPS (6*T*k*H*I/s) & % BF16 peak; decode weight GB/s vs HBM"
 DEFAULT_WORKLOAD = "mixtral-prefill"
-DEC_MAX_TOKENS = 128  # bf16-activation batches up to this size run the decode GEMM kernel
 
 
 def parse(argv=None):
@@ -435,11 +434,12 @@ def measure_layer(args, wl, ctx, seed, steps, warmup, shared=0, fp8=False, ep_ha
     out = torch.empty(T, H, dtype=inp.x.dtype, device=dev)
     stream = torch.cuda.current_stream(dev)
     sh = stream.cuda_stream
-    # bf16 GEMM1 = row gather + tensor-core GEMM, timed apart; small batches (up to 2 tokens,
-    # 12 with FP8 weights) run the CUDA-core grouped GEMMs, which read the token rows in
-    # place; other batches of up to 128 tokens run the decode tensor-core kernel
-    small = L.moe_small_batch(cfg)
-    dec = wl.dtype == "bf16" and not small and T <= DEC_MAX_TOKENS
+    # bf16 GEMM1 = row gather + tensor-core GEMM, timed apart; the library says which grouped
+    # GEMM kernels the batch runs: small batches the CUDA-core kernels (which read the token
+    # rows in place), other decode batches the decode tensor-core kernel
+    kind = L.moe_gemm_kernel(cfg)
+    small = kind == L.MOE_GEMM_SMALL_BATCH
+    dec = kind == L.MOE_GEMM_DECODE_TC
     gathered = wl.dtype == "bf16" and not small
     def step(ev=None, sh=sh, c=0):
         # The same kernels moe_forward enqueues, called stage by stage so that CUDA events

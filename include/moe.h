@@ -44,7 +44,7 @@
 extern "C" {
 #endif
 
-#define MOE_ABI_VERSION 7
+#define MOE_ABI_VERSION 8
 
 typedef enum {
   MOE_OK = 0,
@@ -146,6 +146,17 @@ int moe_block_m(const moe_config_t* cfg);
  * layers of at most 2 tokens, or at most 12 with FP8 expert weights; see
  * moe_expert_gemm1), 0 otherwise or on bad args. Host arithmetic only. */
 int moe_small_batch(const moe_config_t* cfg);
+
+/* Which kernels run the grouped GEMMs of a configuration (with block_m = moe_block_m(cfg)):
+ * the same predicates the GEMM entry points dispatch on. Host arithmetic only. */
+typedef enum {
+  MOE_GEMM_INVALID = 0,      /* bad configuration */
+  MOE_GEMM_SIMT = 1,         /* fp32 layers: CUDA-core tiles */
+  MOE_GEMM_SMALL_BATCH = 2,  /* bf16 <= 2 tokens (FP8 weights <= 12): CUDA-core GEMVs */
+  MOE_GEMM_DECODE_TC = 3,    /* other bf16 batches of <= 128 tokens: decode tensor-core GEMMs */
+  MOE_GEMM_PAIR_TC = 4       /* larger bf16 batches: CTA-pair tensor-core GEMMs */
+} moe_gemm_kernel_t;
+moe_gemm_kernel_t moe_gemm_kernel(const moe_config_t* cfg);
 
 /* Worst-case padded length T*k + min(E, T*k)*(block_m-1) (page §5: every expert that can
  * hold a row pads at most block_m-1 slots). Host arithmetic only; 0 on bad args. */

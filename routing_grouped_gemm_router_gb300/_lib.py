@@ -57,6 +57,7 @@ def _load():
         "moe_status_string": (ctypes.c_char_p, [ST]),
         "moe_block_m": (I32, [CFG]),
         "moe_small_batch": (I32, [CFG]),
+        "moe_gemm_kernel": (I32, [CFG]),
         "moe_max_padded_rows": (SZ, [I32, I32, I32, I32]),
         "moe_align_workspace_size": (ST, [I32, I32, I32, I32, ctypes.POINTER(SZ)]),
         "moe_workspace_layout": (ST, [CFG, ctypes.POINTER(moe_ws_layout_t)]),
@@ -92,6 +93,7 @@ def _load():
 
 _lib = _load()
 EXPORTED = ("moe_abi_version", "moe_status_string", "moe_block_m", "moe_small_batch",
+            "moe_gemm_kernel",
             "moe_max_padded_rows",
             "moe_align_workspace_size", "moe_workspace_layout", "moe_workspace_size",
             "moe_route", "moe_align", "moe_align_noalloc", "moe_expert_gemm1_workspace_size",
@@ -167,6 +169,14 @@ def moe_block_m(cfg) -> int:
 def moe_small_batch(cfg) -> bool:
     """Whether the grouped GEMMs of cfg run as the small-batch (decode) kernels."""
     return bool(_lib.moe_small_batch(ctypes.byref(cfg)))
+
+
+MOE_GEMM_INVALID, MOE_GEMM_SIMT, MOE_GEMM_SMALL_BATCH, MOE_GEMM_DECODE_TC, MOE_GEMM_PAIR_TC = range(5)
+
+
+def moe_gemm_kernel(cfg) -> int:
+    """Which kernels run the grouped GEMMs of cfg (one of the MOE_GEMM_* values)."""
+    return _lib.moe_gemm_kernel(ctypes.byref(cfg))
 
 
 def moe_max_padded_rows(T, k, E, block_m) -> int:

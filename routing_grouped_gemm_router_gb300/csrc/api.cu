@@ -126,6 +126,16 @@ int moe_small_batch(const moe_config_t* cfg) {
   return gemv_applies(e, (int)moe_max_padded_rows(e.T, e.k, e.E, B)) ? 1 : 0;
 }
 
+moe_gemm_kernel_t moe_gemm_kernel(const moe_config_t* cfg) {
+  if (check_cfg(cfg) != MOE_OK) return MOE_GEMM_INVALID;
+  const moe_config_t e = effective(cfg);
+  if (e.dtype != MOE_BF16) return MOE_GEMM_SIMT;
+  const int mp = (int)moe_max_padded_rows(e.T, e.k, e.E, block_m_for(e.dtype));
+  if (gemv_applies(e, mp)) return MOE_GEMM_SMALL_BATCH;
+  if (dec_gemm_applies(e, mp)) return MOE_GEMM_DECODE_TC;
+  return MOE_GEMM_PAIR_TC;
+}
+
 size_t moe_max_padded_rows(int T, int k, int E, int block_m) {
   if (T < 1 || k < 1 || E < 1 || block_m < 1) return 0;
   // total = sum_e ceil(n_e / B) * B <= T*k + min(E, T*k) * (B - 1), and total is a

@@ -37,7 +37,7 @@ def test_library_exports_every_declared_symbol(L):
     missing = [n for n in decl if not hasattr(cdll, n)]
     assert not missing, f"declared but not exported: {missing}"
     assert set(decl) <= set(L.EXPORTED) | set(decl)
-    assert L.moe_abi_version() == 7
+    assert L.moe_abi_version() == 8
 
 
 def test_status_strings(L):
@@ -79,15 +79,36 @@ def test_small_batch_predicate(L):
     assert L.moe_small_batch(fp8(12)) and not L.moe_small_batch(fp8(13))
 
 
+def test_gemm_kernel_query(L):
+    """moe_gemm_kernel names the grouped-GEMM kernels each configuration runs: fp32 layers the
+    CUDA-core tiles, bf16 layers by batch size (2 tokens, 12 with FP8 weights, 128), shared
+    experts counted into the effective top-k, and 0 for a bad configuration (host only)."""
+    mk = lambda T, **kw: L.make_config(T, 2880, 2880, 128, 4, L.MOE_BF16, **kw)  # noqa: E731
+    assert L.moe_gemm_kernel(L.make_config(4, 64, 96, 8, 2, L.MOE_F32)) == L.MOE_GEMM_SIMT
+    assert L.moe_gemm_kernel(mk(1)) == L.MOE_GEMM_SMALL_BATCH
+    assert L.moe_gemm_kernel(mk(2)) == L.MOE_GEMM_SMALL_BATCH
+    assert L.moe_gemm_kernel(mk(3)) == L.MOE_GEMM_DECODE_TC
+    assert L.moe_gemm_kernel(mk(128)) == L.MOE_GEMM_DECODE_TC
+    assert L.moe_gemm_kernel(mk(129)) == L.MOE_GEMM_PAIR_TC
+    assert L.moe_gemm_kernel(mk(16384)) == L.MOE_GEMM_PAIR_TC
+    s13, s2 = torch.ones(128, 2, 23, 23), torch.ones(128, 23, 23)  # scale grids (host only)
+    assert L.moe_gemm_kernel(mk(12, w13_scale=s13, w2_scale=s2)) == L.MOE_GEMM_SMALL_BATCH
+    assert L.moe_gemm_kernel(mk(13, w13_scale=s13, w2_scale=s2)) == L.MOE_GEMM_DECODE_TC
+    assert L.moe_gemm_kernel(mk(0)) == L.MOE_GEMM_INVALID
+    for T in (1, 2, 3, 12, 13, 128, 129, 4096):
+        assert L.moe_small_batch(mk(T)) == (L.moe_gemm_kernel(mk(T)) == L.MOE_GEMM_SMALL_BATCH)
+
+
 def test_decode_parity_cases_take_their_paths(L):
     """The decode layers of the GPU parity tests exercise the paths they are named for: the
     9-token layer and the FP8 layers of 13 tokens and more run the decode tensor-core GEMMs,
     the 1- and 2-token layers the small-batch kernels."""
-    cfg = L.make_config(9, 320, 448, 8, 4, L.MOE_BF16)
-    assert not L.moe_small_batch(cfg)
+    dec = L.MOE_GEMM_DECODE_TC
+    assert L.moe_gemm_kernel(L.make_config(9, 320, 448, 8, 4, L.MOE_BF16)) == dec
     s13, s2 = torch.ones(8, 2, 3, 3), torch.ones(8, 3, 3)  # scale grids (host only)
-    assert not L.moe_small_batch(L.make_config(20, 320, 272, 8, 2, L.MOE_BF16, w13_scale=s13,
-                                               w2_scale=s2))
+    for T in (20, 64):
+        assert L.moe_gemm_kernel(L.make_config(T, 320, 272, 8, 2, L.MOE_BF16, w13_scale=s13,
+                                               w2_scale=s2)) == dec
     for T, H, I, E, k in ((1, 2880, 2880, 128, 4), (2, 2880, 2880, 32, 4), (2, 1000, 776, 4, 2)):
         assert L.moe_small_batch(L.make_config(T, H, I, E, k, L.MOE_BF16))
 

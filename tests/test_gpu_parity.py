@@ -791,6 +791,9 @@ def test_fp8_layer_parity(L, wl, n_shared, any_scale):
     layer = MoELayer(d(inp.Wg), d(c13), d(c2), wl.k, wl.mode, wl.renormalize, wl.scale,
                      wl.n_group, wl.topk_group, d(inp.logit_bias), d(inp.select_bias),
                      n_shared=n_shared, w13_scale=d(s13), w2_scale=d(s2))
+    kind = (L.MOE_GEMM_SMALL_BATCH if wl.name.startswith("fp8-decode") else
+            L.MOE_GEMM_DECODE_TC if wl.name.startswith("fp8-dec-") else L.MOE_GEMM_PAIR_TC)
+    assert L.moe_gemm_kernel(layer.config(wl.T)) == kind
     out = layer(d(inp.x))
     torch.cuda.synchronize()
     mids = layer.intermediates(wl.T)
