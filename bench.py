@@ -683,7 +683,8 @@ def _line_fields(wl, m, world, value, intensity, hbm_bound, roof, hbm, bf16_burs
 SWEEP = [("qwen3-skewed", False), ("deepseek-v3", False),
          ("gpt-oss-decode@T=1", False), ("gpt-oss-decode@T=8", False),
          ("gpt-oss-decode@T=32", False), ("gpt-oss-decode@T=128", False),
-         ("gpt-oss-decode@T=1", True), ("gpt-oss-decode@T=128", True)]
+         ("gpt-oss-decode@T=1", True), ("gpt-oss-decode@T=8", True),
+         ("gpt-oss-decode@T=32", True), ("gpt-oss-decode@T=128", True)]
 
 
 def run_sweep(args, ctx):

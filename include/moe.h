@@ -143,7 +143,7 @@ const char* moe_status_string(moe_status_t s);
 int moe_block_m(const moe_config_t* cfg);
 
 /* 1 when the grouped GEMMs of this configuration run as the small-batch kernels (bf16
- * layers of at most 2 tokens, or at most 12 with FP8 expert weights; see
+ * layers of at most 2 tokens, or at most 24 with FP8 expert weights; see
  * moe_expert_gemm1), 0 otherwise or on bad args. Host arithmetic only. */
 int moe_small_batch(const moe_config_t* cfg);
 
@@ -152,7 +152,7 @@ int moe_small_batch(const moe_config_t* cfg);
 typedef enum {
   MOE_GEMM_INVALID = 0,      /* bad configuration */
   MOE_GEMM_SIMT = 1,         /* fp32 layers: CUDA-core tiles */
-  MOE_GEMM_SMALL_BATCH = 2,  /* bf16 <= 2 tokens (FP8 weights <= 12): CUDA-core GEMVs */
+  MOE_GEMM_SMALL_BATCH = 2,  /* bf16 <= 2 tokens (FP8 weights <= 24): CUDA-core GEMVs */
   MOE_GEMM_DECODE_TC = 3,    /* other bf16 batches of <= 128 tokens: decode tensor-core GEMMs */
   MOE_GEMM_PAIR_TC = 4       /* larger bf16 batches: CTA-pair tensor-core GEMMs */
 } moe_gemm_kernel_t;
@@ -230,7 +230,7 @@ moe_status_t moe_apply_expert_map(int32_t* expert_ids, int num_tiles, const int3
  * block scale) in shared memory on the way. Results agree with the larger-batch kernels to
  * within rounding (the same products, summed in another order), bit for bit from run to run.
  *
- * Small batches (moe_small_batch(cfg) = 1: bf16 layers of at most 2 tokens, 12 with FP8
+ * Small batches (moe_small_batch(cfg) = 1: bf16 layers of at most 2 tokens, 24 with FP8
  * weights): a tile then holds a few
  * real rows, and both grouped GEMMs run on CUDA cores as one pass over the active experts'
  * weights, fp32 products of the same operands summed in another order than the tensor-core

@@ -118,11 +118,11 @@ static Params base_params(const moe_config_t& c, const int32_t* sid, const int32
 
 // Up to this many tokens the grouped GEMMs of a layer run here. Measured on GB300 against
 // the decode tensor-core kernel (gemm_dec.cu; gpt-oss-shaped decode layer, one step in a CUDA
-// graph): bf16 weights 49.5 vs 62.6 us at 1 token, 88 vs 117 at 2, behind from 3 tokens;
-// FP8 weights 41 vs 87 us at 1 token, 316 vs 340 at 8, 457 vs 464 at 12, behind from 16
-// (542 vs 533) and far behind at 32 (1160 vs 767).
+// graph): bf16 weights 49.5 vs 62.6 us at 1 token, 88 vs 117 at 2, behind at 3 (134 vs 124)
+// and from 6 tokens (236 vs 220); FP8 weights 41 vs 87 us at 1 token, 242 vs 340 at 8, 411 vs
+// 532 at 16, 559 vs 658 at 24, behind at 32 (993 vs 770).
 constexpr int kGemvMaxTokens = 2;
-constexpr int kGemvMaxTokensFp8 = 12;
+constexpr int kGemvMaxTokensFp8 = 24;
 
 bool gemv_applies(const moe_config_t& c, int max_padded) {
   const bool fp8 = c.weight_format == MOE_WEIGHTS_FP8_E4M3_B128;

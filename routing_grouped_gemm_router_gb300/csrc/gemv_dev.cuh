@@ -1,6 +1,5 @@
 // gemv_dev.cuh — device code of the small-batch grouped GEMMs on CUDA cores (internal
-// header), shared by the separate GEMV kernels (gemv.cu) and the one-launch decode kernel
-// (decode.cu), so both produce the same bits.
+// header of gemv.cu).
 //
 // One warp owns two weight rows of one expert at a time (an item; GEMM1: the gate and up
 // rows of output column n; GEMM2: the rows of columns n and n+1): the 32 lanes stream them
@@ -37,27 +36,13 @@ struct Params {
   void* out;            // GEMM1: act [padded, N]; GEMM2: y [T*k, N] (bf16)
 };
 
-// Weights are read once: no L1 allocation. EVICT_FIRST: the lines also leave L2 first (an
-// L2 cache policy from createpolicy), so a stream read once does not push out data that
-// another phase still needs there.
-template <bool EVICT_FIRST = false>
-__device__ __forceinline__ uint4 ld_stream(const uint8_t* p, uint64_t policy = 0) {
+// Weights are read once: no L1 allocation.
+__device__ __forceinline__ uint4 ld_stream(const uint8_t* p) {
   uint4 v;
-  if constexpr (EVICT_FIRST)
-    asm("ld.global.nc.L1::no_allocate.L2::cache_hint.v4.u32 {%0, %1, %2, %3}, [%4], %5;"
-        : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
-        : "l"(p), "l"(policy));
-  else
-    asm("ld.global.nc.L1::no_allocate.v4.u32 {%0, %1, %2, %3}, [%4];"
-        : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
-        : "l"(p));
+  asm("ld.global.nc.L1::no_allocate.v4.u32 {%0, %1, %2, %3}, [%4];"
+      : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+      : "l"(p));
   return v;
-}
-
-__device__ __forceinline__ uint64_t l2_evict_first_policy() {
-  uint64_t p;
-  asm("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(p));
-  return p;
 }
 
 __device__ __forceinline__ float bf_lo(uint32_t u) { return __uint_as_float(u << 16); }
@@ -117,8 +102,8 @@ __device__ __forceinline__ int tile_rows(const Params& P, int t, int2* rl) {
 }
 
 // One pass of an item: weight rows w0, w1 (K elements each) against the real rows rl[0..rv)
-// (R >= rv; rows past rv repeat the last one and are discarded), then the epilogue of the
-// item's output column(s) n for those rows. S: 16-byte pieces of each weight row in flight.
+// (R >= rv), then the epilogue of the item's output column(s) n for those rows. S: 16-byte
+// pieces of each weight row in flight.
 // Pieces in flight per row and CTAs per SM, measured at one and two tokens on GB300: bf16
 // passes of 1-2 rows run 3 CTAs an SM (80 registers; 6 or 4 pieces in flight), 5-6 % faster
 // than 2 CTAs with 8 pieces; FP8 codes (half the bytes a piece) keep 2 CTAs and 8 pieces.
@@ -127,26 +112,25 @@ constexpr int kMinCtas = (!FP8 && RMAX <= 2) ? 3 : 2;
 template <int MODE, bool FP8, int RMAX>
 constexpr int kPieces = RMAX == 1 ? (FP8 ? 8 : 6) : 4;
 
-// Activation rows: read-only inputs through the non-coherent path (__ldg), or, when other
-// CTAs of the same launch wrote them before a grid barrier (ACT_WRITTEN), with plain
-// coherent loads (L1-cached): the barrier's acquire orders the writes before them, which the
-// non-coherent path does not promise for data written during the launch.
-template <bool ACT_WRITTEN>
+// Activation rows: read-only inputs of the launch, through the non-coherent path (L1-cached;
+// every warp of a tile reads them).
 __device__ __forceinline__ uint4 ld_act(const uint8_t* p) {
-  if constexpr (ACT_WRITTEN) {
-    return __ldca(reinterpret_cast<const uint4*>(p));
-  } else {
-    return __ldg(reinterpret_cast<const uint4*>(p));
-  }
+  return __ldg(reinterpret_cast<const uint4*>(p));
 }
 
-template <int MODE, bool FP8, int R, int S, bool ACT_WRITTEN = false, bool W_EVICT_FIRST = false>
+template <int MODE, bool FP8, int R, int S>
 __device__ __forceinline__ void item_pass(const Params& P, const uint8_t* w0, const uint8_t* w1,
                                           const float* s0, const float* s1, const int2* rl,
-                                          int rv, int n, uint64_t policy = 0) {
+                                          int rv, int n) {
   constexpr int EPL = FP8 ? 16 : 8;  // elements of a 16-byte weight piece
   constexpr int ES = FP8 ? 1 : 2;    // weight element bytes
   constexpr int kStride = 32 * EPL;  // elements per warp step
+  // Rows past rv are skipped (warp-uniform branches) where their multiply-adds would cost
+  // issue slots: FP8 codes and passes of four rows (a decode tile mostly holds one real row).
+  // Measured on GB300 (gpt-oss-shaped layer, FP8 weights): 23-25 % less time a layer at 4 to
+  // 16 tokens. bf16 passes of two rows stream well below the issue rate, and the branches
+  // would cost them registers.
+  constexpr bool kSkip = R > 1 && (FP8 || R > 2);
   const int lane = threadIdx.x % 32;
   const int K = P.K;
   const uint8_t* ar[R];
@@ -164,8 +148,8 @@ __device__ __forceinline__ void item_pass(const Params& P, const uint8_t* w0, co
     for (int j = 0; j < S; ++j) {
       const int kk = k0 + j * kStride;
       if (kk < K) {
-        q0[j] = ld_stream<W_EVICT_FIRST>(w0 + (size_t)kk * ES, policy);
-        q1[j] = ld_stream<W_EVICT_FIRST>(w1 + (size_t)kk * ES, policy);
+        q0[j] = ld_stream(w0 + (size_t)kk * ES);
+        q1[j] = ld_stream(w1 + (size_t)kk * ES);
       }
     }
 #pragma unroll
@@ -179,9 +163,10 @@ __device__ __forceinline__ void item_pass(const Params& P, const uint8_t* w0, co
         const float sc0 = __ldg(s0 + kk / 128), sc1 = __ldg(s1 + kk / 128);
 #pragma unroll
         for (int r = 0; r < R; ++r) {
+          if (kSkip && r >= rv) break;
           float xf[16];
-          bf16x8_to_f32(ld_act<ACT_WRITTEN>(ar[r] + (size_t)kk * 2), xf);
-          bf16x8_to_f32(ld_act<ACT_WRITTEN>(ar[r] + (size_t)kk * 2 + 16), xf + 8);
+          bf16x8_to_f32(ld_act(ar[r] + (size_t)kk * 2), xf);
+          bf16x8_to_f32(ld_act(ar[r] + (size_t)kk * 2 + 16), xf + 8);
           float p0 = 0.f, p1 = 0.f;
 #pragma unroll
           for (int i = 0; i < 16; ++i) {
@@ -197,8 +182,9 @@ __device__ __forceinline__ void item_pass(const Params& P, const uint8_t* w0, co
         bf16x8_to_f32(q1[j], f1);
 #pragma unroll
         for (int r = 0; r < R; ++r) {
+          if (kSkip && r >= rv) break;
           float xf[8];
-          bf16x8_to_f32(ld_act<ACT_WRITTEN>(ar[r] + (size_t)kk * 2), xf);
+          bf16x8_to_f32(ld_act(ar[r] + (size_t)kk * 2), xf);
 #pragma unroll
           for (int i = 0; i < 8; ++i) {
             a0[r] = fmaf(f0[i], xf[i], a0[r]);
@@ -210,6 +196,7 @@ __device__ __forceinline__ void item_pass(const Params& P, const uint8_t* w0, co
   }
 #pragma unroll
   for (int r = 0; r < R; ++r) {
+    if (kSkip && r >= rv) break;
     const float d0 = warp_sum(a0[r]), d1 = warp_sum(a1[r]);
     if (r < rv && lane == r) {
       const int2 q = rl[r];

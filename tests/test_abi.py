@@ -66,7 +66,7 @@ def test_block_m_and_workspace(L):
 
 
 def test_small_batch_predicate(L):
-    """bf16 layers of at most 2 tokens (12 with FP8 weights) take the small-batch grouped
+    """bf16 layers of at most 2 tokens (24 with FP8 weights) take the small-batch grouped
     GEMMs; fp32 layers, larger batches and bad configurations do not (host arithmetic)."""
     assert L.moe_small_batch(L.make_config(1, 2880, 2880, 128, 4, L.MOE_BF16))
     assert L.moe_small_batch(L.make_config(2, 7168, 2048, 256, 8, L.MOE_BF16))
@@ -76,12 +76,12 @@ def test_small_batch_predicate(L):
     s13, s2 = torch.ones(128, 2, 23, 23), torch.ones(128, 23, 23)  # scale grids (host only)
     fp8 = lambda T: L.make_config(T, 2880, 2880, 128, 4, L.MOE_BF16, w13_scale=s13,  # noqa: E731
                                   w2_scale=s2)
-    assert L.moe_small_batch(fp8(12)) and not L.moe_small_batch(fp8(13))
+    assert L.moe_small_batch(fp8(24)) and not L.moe_small_batch(fp8(25))
 
 
 def test_gemm_kernel_query(L):
     """moe_gemm_kernel names the grouped-GEMM kernels each configuration runs: fp32 layers the
-    CUDA-core tiles, bf16 layers by batch size (2 tokens, 12 with FP8 weights, 128), shared
+    CUDA-core tiles, bf16 layers by batch size (2 tokens, 24 with FP8 weights, 128), shared
     experts counted into the effective top-k, and 0 for a bad configuration (host only)."""
     mk = lambda T, **kw: L.make_config(T, 2880, 2880, 128, 4, L.MOE_BF16, **kw)  # noqa: E731
     assert L.moe_gemm_kernel(L.make_config(4, 64, 96, 8, 2, L.MOE_F32)) == L.MOE_GEMM_SIMT
@@ -92,8 +92,8 @@ def test_gemm_kernel_query(L):
     assert L.moe_gemm_kernel(mk(129)) == L.MOE_GEMM_PAIR_TC
     assert L.moe_gemm_kernel(mk(16384)) == L.MOE_GEMM_PAIR_TC
     s13, s2 = torch.ones(128, 2, 23, 23), torch.ones(128, 23, 23)  # scale grids (host only)
-    assert L.moe_gemm_kernel(mk(12, w13_scale=s13, w2_scale=s2)) == L.MOE_GEMM_SMALL_BATCH
-    assert L.moe_gemm_kernel(mk(13, w13_scale=s13, w2_scale=s2)) == L.MOE_GEMM_DECODE_TC
+    assert L.moe_gemm_kernel(mk(24, w13_scale=s13, w2_scale=s2)) == L.MOE_GEMM_SMALL_BATCH
+    assert L.moe_gemm_kernel(mk(25, w13_scale=s13, w2_scale=s2)) == L.MOE_GEMM_DECODE_TC
     assert L.moe_gemm_kernel(mk(0)) == L.MOE_GEMM_INVALID
     for T in (1, 2, 3, 12, 13, 128, 129, 4096):
         assert L.moe_small_batch(mk(T)) == (L.moe_gemm_kernel(mk(T)) == L.MOE_GEMM_SMALL_BATCH)
@@ -101,14 +101,16 @@ def test_gemm_kernel_query(L):
 
 def test_decode_parity_cases_take_their_paths(L):
     """The decode layers of the GPU parity tests exercise the paths they are named for: the
-    9-token layer and the FP8 layers of 13 tokens and more run the decode tensor-core GEMMs,
-    the 1- and 2-token layers the small-batch kernels."""
+    9-token layer and the FP8 layers of 25 tokens and more run the decode tensor-core GEMMs,
+    the 1- and 2-token layers and the 24-token FP8 layer the small-batch kernels."""
     dec = L.MOE_GEMM_DECODE_TC
     assert L.moe_gemm_kernel(L.make_config(9, 320, 448, 8, 4, L.MOE_BF16)) == dec
     s13, s2 = torch.ones(8, 2, 3, 3), torch.ones(8, 3, 3)  # scale grids (host only)
-    for T in (20, 64):
-        assert L.moe_gemm_kernel(L.make_config(T, 320, 272, 8, 2, L.MOE_BF16, w13_scale=s13,
-                                               w2_scale=s2)) == dec
+    fp8 = lambda T: L.make_config(T, 320, 272, 8, 2, L.MOE_BF16, w13_scale=s13,  # noqa: E731
+                                  w2_scale=s2)
+    assert L.moe_gemm_kernel(fp8(24)) == L.MOE_GEMM_SMALL_BATCH
+    for T in (28, 64):
+        assert L.moe_gemm_kernel(fp8(T)) == dec
     for T, H, I, E, k in ((1, 2880, 2880, 128, 4), (2, 2880, 2880, 32, 4), (2, 1000, 776, 4, 2)):
         assert L.moe_small_batch(L.make_config(T, H, I, E, k, L.MOE_BF16))
 

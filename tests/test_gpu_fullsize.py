@@ -77,7 +77,8 @@ def test_full_size_parity(L, wl, n_sample):
     assert torch.isfinite(out.float()).all()
 
 
-FP8_CASES = [(mi.DSV3, 16), (mi.GPTOSS.with_T(1), 1), (mi.GPTOSS.with_T(128), 32)]
+FP8_CASES = [(mi.DSV3, 16), (mi.GPTOSS.with_T(1), 1), (mi.GPTOSS.with_T(16), 16),
+             (mi.GPTOSS.with_T(128), 32)]
 
 
 @pytest.mark.parametrize("wl,n_sample", FP8_CASES, ids=[c[0].name + "-fp8" for c in FP8_CASES])

@@ -749,15 +749,17 @@ FP8_CASES = [
     # scales that are not powers of two: the kernel rounds code * scale to bf16 once
     (mi.Workload("fp8-any-scale", T=200, H=256, I=256, E=16, k=4, dtype="bf16", seed=63), 0, True),
     # decode (small-batch kernels): one token; six tokens on four experts (rows of an expert
-    # in two passes) with K off the 512-code step and any scales; three tokens + a shared one
+    # in two passes) with K off the 512-code step and any scales; three tokens + a shared one;
+    # 24 tokens on eight experts (tiles of 2-10 rows: passes of four rows and shorter ones)
     (mi.Workload("fp8-decode", T=1, H=512, I=512, E=64, k=4, dtype="bf16", seed=64), 0, False),
     (mi.Workload("fp8-decode-ragged", T=6, H=1040, I=784, E=4, k=2, dtype="bf16", seed=66), 0,
      True),
     (mi.Workload("fp8-decode-shared", T=3, H=2880, I=1024, E=16, k=4, dtype="bf16", seed=67), 1,
      False),
-    # decode tensor-core kernel (13 to 128 tokens): ragged K and N with any scales; 64 tokens
+    (mi.Workload("fp8-decode-T24", T=24, H=320, I=272, E=8, k=2, dtype="bf16", seed=71), 0, True),
+    # decode tensor-core kernel (25 to 128 tokens): ragged K and N with any scales; 64 tokens
     # plus a shared expert (a 64-row tile); tiles nearly full (one tile-row slot in GEMM1)
-    (mi.Workload("fp8-dec-ragged", T=20, H=320, I=272, E=8, k=2, dtype="bf16", seed=68), 0, True),
+    (mi.Workload("fp8-dec-ragged", T=28, H=320, I=272, E=8, k=2, dtype="bf16", seed=68), 0, True),
     (mi.Workload("fp8-dec-shared", T=64, H=512, I=384, E=32, k=4, dtype="bf16", seed=69), 1,
      False),
     (mi.Workload("fp8-dec-full-tiles", T=128, H=256, I=256, E=3, k=2, dtype="bf16", seed=70), 0,
