@@ -553,11 +553,16 @@ moe_status_t moe_forward(const moe_config_t* c, const void* x, const void* Wg, c
       (st = moe_apply_expert_map(eid, L.max_padded / L.block_m, c->expert_map, e.E, stream)) !=
           MOE_OK)
     return st;
-  if (e.dtype == MOE_BF16 && gemv_applies(e, (int)L.max_padded)) {
-    // a small batch: GEMM1 reads the token rows in place, no gather pass
+  const bool small = e.dtype == MOE_BF16 && gemv_applies(e, (int)L.max_padded);
+  if (small) {
+    // a small batch: GEMM1 reads the token rows in place, no gather pass; GEMM2 directly
+    // follows it, so its first weight loads may start before its dependency wait
     if (!aligned16(x) || !aligned16(W13) || !aligned16(W2)) return MOE_ERR_INVALID_ARG;
     if ((st = launch_gemv1(e, x, false, W13, sid, eid, npp, L.block_m, b + L.act, stream)) !=
         MOE_OK)
+      return st;
+    if ((st = launch_gemv2(e, b + L.act, W2, sid, eid, npp, L.block_m, w, b + L.y, stream,
+                           true)) != MOE_OK)
       return st;
   } else if (e.dtype == MOE_BF16) {  // gather pass, then the tensor-core GEMM1
     if ((st = moe_gather_rows(x, sid, npp, e.T, e.k, e.H, e.dtype, b + L.xs, stream)) != MOE_OK)
@@ -569,8 +574,8 @@ moe_status_t moe_forward(const moe_config_t* c, const void* x, const void* Wg, c
                                     stream)) != MOE_OK) {
     return st;
   }
-  if ((st = moe_expert_gemm2(c, b + L.act, W2, sid, eid, npp, L.block_m, w, b + L.y, nullptr,
-                             0, stream)) != MOE_OK)
+  if (!small && (st = moe_expert_gemm2(c, b + L.act, W2, sid, eid, npp, L.block_m, w, b + L.y,
+                                       nullptr, 0, stream)) != MOE_OK)
     return st;
   if (c->expert_map)
     return moe_combine_local(b + L.y, ids, c->expert_map, e.E, e.T, e.k, e.H, e.dtype, out,

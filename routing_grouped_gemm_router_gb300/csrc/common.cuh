@@ -114,9 +114,12 @@ bool gemv_applies(const moe_config_t& c, int max_padded);
 moe_status_t launch_gemv1(const moe_config_t& c, const void* a, bool gathered, const void* W13,
                           const int32_t* sid, const int32_t* eid, const int32_t* npp,
                           int block_m, void* act, cudaStream_t s);
+// early: the launch directly follows launch_gemv1 on the same table (the fused layer), so the
+// kernel may read the table and the weights before its dependency wait.
 moe_status_t launch_gemv2(const moe_config_t& c, const void* act, const void* W2,
                           const int32_t* sid, const int32_t* eid, const int32_t* npp,
-                          int block_m, const float* topk_w, void* y, cudaStream_t s);
+                          int block_m, const float* topk_w, void* y, cudaStream_t s,
+                          bool early = false);
 // Grouped GEMMs of decode-sized batches on the tensor cores with the weights as the 128-row
 // MMA operand (gemm_dec.cu): whether they apply, and the two GEMMs with the pair kernels'
 // inputs and outputs (GEMM1 reads the routed rows gathered in padded order).

@@ -24,55 +24,113 @@ namespace gv {
 // MODE 1: GEMM2 (item = output columns n, n + 1 of y: W2 rows n, n + 1).
 // RMAX: real rows a pass takes (a tile holds at most T of them); one pass shape per kernel.
 
+// The weight rows of item (expert e, output column n) and, with FP8 codes, their block scales.
+template <int MODE, bool FP8>
+__device__ __forceinline__ void item_rows(const Params& P, int e, int n, const uint8_t*& w0,
+                                          const uint8_t*& w1, const float*& s0,
+                                          const float*& s1) {
+  const size_t row_bytes = (size_t)P.K * (FP8 ? 1 : 2);
+  s0 = s1 = nullptr;
+  if (MODE == 0) {
+    w0 = P.w + ((size_t)e * 2 * P.N + n) * row_bytes;
+    w1 = P.w + ((size_t)e * 2 * P.N + P.N + n) * row_bytes;
+    if (FP8) {
+      s0 = P.scale + (((size_t)e * 2 + 0) * P.sc_rb + n / 128) * P.sc_kb;
+      s1 = P.scale + (((size_t)e * 2 + 1) * P.sc_rb + n / 128) * P.sc_kb;
+    }
+  } else {
+    w0 = P.w + ((size_t)e * P.N + n) * row_bytes;
+    w1 = w0 + row_bytes;
+    if (FP8) s0 = s1 = P.scale + ((size_t)e * P.sc_rb + n / 128) * P.sc_kb;  // n, n+1: one block
+  }
+}
+
+// Item w (tile w / cols, column c = w % cols) of one warp: the tile's real rows (kept in rl
+// while the warp stays on the tile), then one pass over the item's weight rows per RMAX real
+// rows.
+template <int MODE, bool FP8, int RMAX>
+__device__ __forceinline__ void run_item(const Params& P, int w, int cols, int& cur_t,
+                                         int& nvalid, int& e, int2* rl) {
+  const int t = w / cols, c = w - t * cols;
+  if (t != cur_t) {
+    __syncwarp();
+    cur_t = t;
+    e = P.eid[(t * kTile) / P.block_m];
+    nvalid = tile_rows(P, t, rl);
+    __syncwarp();
+  }
+  if (e < 0 || e >= P.n_slots || nvalid == 0) return;
+  const int n = MODE == 0 ? c : 2 * c;
+  const uint8_t *w0, *w1;
+  const float *s0, *s1;
+  item_rows<MODE, FP8>(P, e, n, w0, w1, s0, s1);
+  for (int rc = 0; rc < nvalid; rc += RMAX)
+    item_pass<MODE, FP8, RMAX, kPieces<MODE, FP8, RMAX>>(P, w0, w1, s0, s1, rl + rc,
+                                                         min(RMAX, nvalid - rc), n);
+}
+
 template <int MODE, bool FP8, int RMAX>
 __global__ void __launch_bounds__(kThreads, (kMinCtas<MODE, FP8, RMAX>)) gemv_kernel(const Params P) {
-  pdl_wait();
-  pdl_trigger();
-  __shared__ int2 rows_sh[kWarps][kTile];
-  const int warp = threadIdx.x / 32;
-  int2* rl = rows_sh[warp];
+  constexpr int S = kPieces<MODE, FP8, RMAX>;
   constexpr int ES = FP8 ? 1 : 2;
-  const int num_m = *P.npp / kTile;
+  constexpr int EPL = FP8 ? 16 : 8;  // elements of a 16-byte weight piece
+  __shared__ int2 rows_sh[kWarps][kTile];
+  const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+  int2* rl = rows_sh[warp];
   const int cols = MODE == 0 ? P.N : P.N / 2;
-  const int total = num_m * cols;  // bounded on the host
   const int nwarps = gridDim.x * kWarps;
-  const int per = (total + nwarps - 1) / nwarps;
   const int gw = blockIdx.x * kWarps + warp;
-  const int w_begin = min(total, gw * per), w_end = min(total, w_begin + per);
   int cur_t = -1, nvalid = 0, e = -1;
-  for (int w = w_begin; w < w_end; ++w) {
-    const int t = w / cols, c = w - t * cols;
-    if (t != cur_t) {
-      __syncwarp();
+  // GEMM2 inside the fused layer (P.early): the kernel before this one is GEMM1, which writes
+  // only act. The weights are the layer's inputs and the table was written by the routing
+  // kernel, which completed before GEMM1 started (and so before this grid was launched), so
+  // this warp's first item is set up (table read past L1) and the first pieces of its weight
+  // rows are loaded before the dependency wait, during GEMM1's tail; act and y wait.
+  uint4 pre0[S], pre1[S];
+  bool pre = false;
+  int pre_n = 0;
+  const uint8_t *pw0 = nullptr, *pw1 = nullptr;
+  const float *ps0 = nullptr, *ps1 = nullptr;
+  if (MODE == 1 && P.early) {
+    const int total0 = __ldcg(P.npp) / kTile * cols;
+    const int per0 = (total0 + nwarps - 1) / nwarps;
+    const int wb = min(total0, gw * per0);
+    if (wb < min(total0, wb + per0)) {
+      const int t = wb / cols, c = wb - t * cols;
       cur_t = t;
-      e = P.eid[(t * kTile) / P.block_m];
-      nvalid = tile_rows(P, t, rl);
+      e = __ldcg(P.eid + (t * kTile) / P.block_m);
+      nvalid = tile_rows<true>(P, t, rl);
       __syncwarp();
-    }
-    if (e < 0 || e >= P.n_slots || nvalid == 0) continue;
-    const int n = MODE == 0 ? c : 2 * c;
-    const size_t row_bytes = (size_t)P.K * ES;
-    const uint8_t* w0;
-    const uint8_t* w1;
-    const float* s0 = nullptr;
-    const float* s1 = nullptr;
-    if (MODE == 0) {
-      w0 = P.w + ((size_t)e * 2 * P.N + n) * row_bytes;
-      w1 = P.w + ((size_t)e * 2 * P.N + P.N + n) * row_bytes;
-      if (FP8) {
-        s0 = P.scale + (((size_t)e * 2 + 0) * P.sc_rb + n / 128) * P.sc_kb;
-        s1 = P.scale + (((size_t)e * 2 + 1) * P.sc_rb + n / 128) * P.sc_kb;
+      if (e >= 0 && e < P.n_slots && nvalid > 0) {
+        pre_n = 2 * c;
+        item_rows<MODE, FP8>(P, e, pre_n, pw0, pw1, ps0, ps1);
+#pragma unroll
+        for (int j = 0; j < S; ++j) {
+          const int kk = lane * EPL + j * 32 * EPL;
+          if (kk < P.K) {
+            pre0[j] = ld_stream(pw0 + (size_t)kk * ES);
+            pre1[j] = ld_stream(pw1 + (size_t)kk * ES);
+          }
+        }
+        pre = true;
       }
-    } else {
-      w0 = P.w + ((size_t)e * P.N + n) * row_bytes;
-      w1 = w0 + row_bytes;
-      if (FP8) s0 = s1 = P.scale + ((size_t)e * P.sc_rb + n / 128) * P.sc_kb;  // n, n+1: one block
-    }
-    for (int rc = 0; rc < nvalid; rc += RMAX) {
-      const int rv = min(RMAX, nvalid - rc);
-      item_pass<MODE, FP8, RMAX, kPieces<MODE, FP8, RMAX>>(P, w0, w1, s0, s1, rl + rc, rv, n);
     }
   }
+  pdl_wait();
+  pdl_trigger();
+  const int num_m = *P.npp / kTile;
+  const int total = num_m * cols;  // bounded on the host
+  const int per = (total + nwarps - 1) / nwarps;
+  const int w_begin = min(total, gw * per), w_end = min(total, w_begin + per);
+  int w = w_begin;
+  if (MODE == 1 && pre) {  // the first item: its first pass from the loaded pieces
+    item_pass<MODE, FP8, RMAX, S, true>(P, pw0, pw1, ps0, ps1, rl, min(RMAX, nvalid), pre_n, pre0,
+                                        pre1);
+    for (int rc = RMAX; rc < nvalid; rc += RMAX)
+      item_pass<MODE, FP8, RMAX, S>(P, pw0, pw1, ps0, ps1, rl + rc, min(RMAX, nvalid - rc), pre_n);
+    ++w;
+  }
+  for (; w < w_end; ++w) run_item<MODE, FP8, RMAX>(P, w, cols, cur_t, nvalid, e, rl);
 }
 
 template <int MODE, bool FP8, int RMAX>
@@ -150,8 +208,9 @@ moe_status_t launch_gemv1(const moe_config_t& c, const void* a, bool gathered, c
 
 moe_status_t launch_gemv2(const moe_config_t& c, const void* act, const void* W2,
                           const int32_t* sid, const int32_t* eid, const int32_t* npp,
-                          int block_m, const float* topk_w, void* y, cudaStream_t s) {
+                          int block_m, const float* topk_w, void* y, cudaStream_t s, bool early) {
   gv::Params P = gv::base_params(c, sid, eid, npp, block_m);
+  P.early = early ? 1 : 0;
   const bool fp8 = c.weight_format == MOE_WEIGHTS_FP8_E4M3_B128;
   P.a = (const uint8_t*)act;
   P.a_gathered = 1;

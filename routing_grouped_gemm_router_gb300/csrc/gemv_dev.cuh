@@ -34,6 +34,9 @@ struct Params {
   int block_m, n_rows, k, K, N, n_slots;
   const float* topk_w;  // GEMM2
   void* out;            // GEMM1: act [padded, N]; GEMM2: y [T*k, N] (bf16)
+  // GEMM2 inside the fused layer: each warp loads the first pieces of its first item's
+  // weight rows before the dependency wait (see gemv_kernel)
+  int early;
 };
 
 // Weights are read once: no L1 allocation.
@@ -85,14 +88,16 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
   return *reinterpret_cast<const uint32_t*>(&h);
 }
 
-// Real rows of tile t: their count, and their (p, r) in padded order into rl.
+// Real rows of tile t: their count, and their (p, r) in padded order into rl. CG: the table
+// is read past L1 (before the dependency wait).
+template <bool CG = false>
 __device__ __forceinline__ int tile_rows(const Params& P, int t, int2* rl) {
   const int lane = threadIdx.x % 32;
   int n = 0;
 #pragma unroll
   for (int i = 0; i < kTile / 32; ++i) {
     const int p = t * kTile + i * 32 + lane;
-    const int r = P.sid[p];
+    const int r = CG ? __ldcg(P.sid + p) : P.sid[p];
     const bool v = r >= 0 && r < P.n_rows;
     const unsigned m = __ballot_sync(0xffffffffu, v);
     if (v) rl[n + __popc(m & ((1u << lane) - 1u))] = make_int2(p, r);
@@ -118,10 +123,12 @@ __device__ __forceinline__ uint4 ld_act(const uint8_t* p) {
   return __ldg(reinterpret_cast<const uint4*>(p));
 }
 
-template <int MODE, bool FP8, int R, int S>
+// PRE: the first S pieces of both rows are already in pre0 / pre1 (loaded by the caller).
+template <int MODE, bool FP8, int R, int S, bool PRE = false>
 __device__ __forceinline__ void item_pass(const Params& P, const uint8_t* w0, const uint8_t* w1,
                                           const float* s0, const float* s1, const int2* rl,
-                                          int rv, int n) {
+                                          int rv, int n, const uint4 (&pre0)[S] = {},
+                                          const uint4 (&pre1)[S] = {}) {
   constexpr int EPL = FP8 ? 16 : 8;  // elements of a 16-byte weight piece
   constexpr int ES = FP8 ? 1 : 2;    // weight element bytes
   constexpr int kStride = 32 * EPL;  // elements per warp step
@@ -142,16 +149,8 @@ __device__ __forceinline__ void item_pass(const Params& P, const uint8_t* w0, co
   float a0[R], a1[R];
 #pragma unroll
   for (int r = 0; r < R; ++r) a0[r] = a1[r] = 0.f;
-  for (int k0 = lane * EPL; k0 < K; k0 += kStride * S) {
-    uint4 q0[S], q1[S];
-#pragma unroll
-    for (int j = 0; j < S; ++j) {
-      const int kk = k0 + j * kStride;
-      if (kk < K) {
-        q0[j] = ld_stream(w0 + (size_t)kk * ES);
-        q1[j] = ld_stream(w1 + (size_t)kk * ES);
-      }
-    }
+  // one step of S pieces of both rows at k0 into the row sums
+  auto step = [&](const uint4 (&q0)[S], const uint4 (&q1)[S], int k0) {
 #pragma unroll
     for (int j = 0; j < S; ++j) {
       const int kk = k0 + j * kStride;
@@ -193,6 +192,23 @@ __device__ __forceinline__ void item_pass(const Params& P, const uint8_t* w0, co
         }
       }
     }
+  };
+  int k0 = lane * EPL;
+  if constexpr (PRE) {  // the first step from the pieces already loaded
+    step(pre0, pre1, k0);
+    k0 += kStride * S;
+  }
+  for (; k0 < K; k0 += kStride * S) {
+    uint4 q0[S], q1[S];
+#pragma unroll
+    for (int j = 0; j < S; ++j) {
+      const int kk = k0 + j * kStride;
+      if (kk < K) {
+        q0[j] = ld_stream(w0 + (size_t)kk * ES);
+        q1[j] = ld_stream(w1 + (size_t)kk * ES);
+      }
+    }
+    step(q0, q1, k0);
   }
 #pragma unroll
   for (int r = 0; r < R; ++r) {

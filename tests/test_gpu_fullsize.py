@@ -3,7 +3,8 @@
 Each layer is drawn on the GPU (seeded), routed, aligned and run through moe_forward.
 Routing and the indirection table are checked bit-exactly for every token; the layer
 output is checked on a sample of tokens (tokens of the hottest and of the least-loaded
-non-empty expert among them), each recomputed by the float64 oracle.
+non-empty expert among them), and the grouped GEMMs' output y on the first and last routed
+row of every active expert, each recomputed by the float64 oracle.
 """
 import numpy as np
 import pytest
@@ -75,6 +76,23 @@ def test_full_size_parity(L, wl, n_sample):
     got = to_np(out[torch.as_tensor(toks, device=DEV)])
     assert_close(got, ref, wl.dtype)
     assert torch.isfinite(out.float()).all()
+
+    # y: for every active expert its first and last routed rows (its first and last m-tile),
+    # each a full row of H outputs against the oracle's single-slot layer (w_r times the
+    # expert's FFN of the token), so an error confined to one weight panel of any expert,
+    # in either grouped GEMM, shows
+    k = wl.k
+    flat = ids_o.ravel()
+    rows = []
+    for e in np.unique(flat):
+        r_e = np.nonzero(flat == e)[0]
+        rows += sorted({int(r_e[0]), int(r_e[-1])})
+    rows = np.array(rows)
+    t_sel = rows // k
+    y_ref = O.moe_loop(to_np(inp.x[torch.as_tensor(t_sel, device=DEV)]), flat[rows][:, None],
+                       w_o.ravel()[rows][:, None], LazyExperts(inp.W13), LazyExperts(inp.W2))
+    y_got = to_np(mids["y"][torch.as_tensor(rows, device=DEV)])
+    assert_close(y_got, y_ref, wl.dtype)
 
 
 FP8_CASES = [(mi.DSV3, 16), (mi.GPTOSS.with_T(1), 1), (mi.GPTOSS.with_T(16), 16),
