@@ -5,7 +5,8 @@
 // every SM gets one.
 //
 // One persistent CTA per SM (up to ceil(T/128) CTAs) with three warp roles: warp 0 issues
-// TMA copies of x and Wg k-blocks into a 4-stage shared-memory ring, warp 1 (one lane)
+// TMA copies of x and Wg k-blocks into a shared-memory ring (4 to 10 stages, see stages_for),
+// warp 1 (one lane)
 // issues tcgen05.mma, warps 2-5 read the fp32 accumulator back (tcgen05.ld) and store the
 // logits; two TMEM accumulators let the epilogue of one tile overlap the next tile's MMAs.
 // Every mbarrier wait is bounded: on time-out the kernel records kStatusTimeout, stops
@@ -20,7 +21,13 @@ using namespace ptx;
 __device__ int g_router_status;
 
 constexpr int kThreads = 192;
-constexpr int kStages = 4;
+// Ring depth: as many k-blocks of x and Wg in flight as about 200 KB of shared memory holds
+// (4 stages at BN = 256, 10 at BN = 32). With few 128-token tiles a CTA streams a long K loop
+// alone on its SM, so its bytes in flight set its share of the HBM bandwidth.
+__host__ __device__ constexpr int stages_for(int bn) {
+  const int s = (200 * 1024) / (BM * 128 + bn * 128);
+  return s < 4 ? 4 : (s > 12 ? 12 : s);
+}
 
 struct RouterParams {
   int T, E, H;
@@ -32,7 +39,7 @@ __host__ __device__ constexpr int tmem_cols_for(int bn) {
   return 2 * bn <= 32 ? 32 : 2 * bn <= 64 ? 64 : 2 * bn <= 128 ? 128 : 2 * bn <= 256 ? 256 : 512;
 }
 __host__ __device__ constexpr size_t router_smem_bytes(int bn) {
-  return 1024 + (size_t)kStages * (BM * 128 + (size_t)bn * 128) + 256;
+  return 1024 + (size_t)stages_for(bn) * (BM * 128 + (size_t)bn * 128) + 256;
 }
 
 template <int BN>
@@ -41,6 +48,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                      const __grid_constant__ CUtensorMap tmW, const RouterParams P) {
   constexpr int A_BYTES = BM * 128;
   constexpr int B_BYTES = BN * 128;
+  constexpr int kStages = stages_for(BN);
   constexpr uint32_t TMEM_COLS = tmem_cols_for(BN);
   constexpr uint32_t IDESC = idesc_bf16(BM, BN);
 
