@@ -6,9 +6,9 @@
 //
 // One persistent CTA per SM (up to ceil(T/128) CTAs) with three warp roles: warp 0 issues
 // TMA copies of x and Wg k-blocks into a shared-memory ring (4 to 10 stages, see stages_for),
-// warp 1 (one lane)
-// issues tcgen05.mma, warps 2-5 read the fp32 accumulator back (tcgen05.ld) and store the
-// logits; two TMEM accumulators let the epilogue of one tile overlap the next tile's MMAs.
+// warp 1 (one lane) issues tcgen05.mma, warps 2-5 read the fp32 accumulator back
+// (tcgen05.ld) and store the logits; two TMEM accumulators let the epilogue of one tile
+// overlap the next tile's MMAs.
 // Every mbarrier wait is bounded: on time-out the kernel records kStatusTimeout, stops
 // issuing work, lets copies in flight land and frees its TMEM before returning.
 #include "tc_ptx.cuh"
