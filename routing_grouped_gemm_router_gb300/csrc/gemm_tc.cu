@@ -21,12 +21,14 @@ using namespace ptx;
 __device__ int g_router_status;
 
 constexpr int kThreads = 192;
-// Ring depth: as many k-blocks of x and Wg in flight as about 200 KB of shared memory holds
-// (4 stages at BN = 256, 10 at BN = 32). With few 128-token tiles a CTA streams a long K loop
-// alone on its SM, so its bytes in flight set its share of the HBM bandwidth.
+// A ring stage holds kKbStage k-blocks of x and Wg (one full-barrier wait and one commit of
+// the MMA thread per stage: with a narrow N the MMA thread's round trip per stage, not the
+// bytes in flight, sets a tile's time), and the ring is as deep as about 200 KB of shared
+// memory holds (2 stages at BN = 256, 5 at BN = 32).
+constexpr int kKbStage = 2;
 __host__ __device__ constexpr int stages_for(int bn) {
-  const int s = (200 * 1024) / (BM * 128 + bn * 128);
-  return s < 4 ? 4 : (s > 12 ? 12 : s);
+  const int s = (200 * 1024) / (kKbStage * (BM * 128 + bn * 128));
+  return s < 2 ? 2 : (s > 8 ? 8 : s);
 }
 
 struct RouterParams {
@@ -39,15 +41,15 @@ __host__ __device__ constexpr int tmem_cols_for(int bn) {
   return 2 * bn <= 32 ? 32 : 2 * bn <= 64 ? 64 : 2 * bn <= 128 ? 128 : 2 * bn <= 256 ? 256 : 512;
 }
 __host__ __device__ constexpr size_t router_smem_bytes(int bn) {
-  return 1024 + (size_t)stages_for(bn) * (BM * 128 + (size_t)bn * 128) + 256;
+  return 1024 + (size_t)stages_for(bn) * kKbStage * (BM * 128 + (size_t)bn * 128) + 256;
 }
 
 template <int BN>
 __global__ void __launch_bounds__(kThreads, 1)
     router_tc_kernel(const __grid_constant__ CUtensorMap tmX,
                      const __grid_constant__ CUtensorMap tmW, const RouterParams P) {
-  constexpr int A_BYTES = BM * 128;
-  constexpr int B_BYTES = BN * 128;
+  constexpr int A_BYTES = kKbStage * BM * 128;  // x: kKbStage k-blocks of 128 rows
+  constexpr int B_BYTES = kKbStage * BN * 128;  // Wg: kKbStage k-blocks of BN rows
   constexpr int kStages = stages_for(BN);
   constexpr uint32_t TMEM_COLS = tmem_cols_for(BN);
   constexpr uint32_t IDESC = idesc_bf16(BM, BN);
@@ -91,7 +93,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
-  const int num_kb = (P.H + BK - 1) / BK;
+  const int num_kb = (P.H + kKbStage * BK - 1) / (kKbStage * BK);  // ring stages per tile
   pdl_wait();  // x, Wg and logits are touched only past this point
 
   if (warp == 0) {
@@ -105,10 +107,14 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (lane == 0) ok = wait_bounded(&empty[stage], phase ^ 1u, abort_flag, status);
         ok = __shfl_sync(0xffffffffu, ok, 0);
         if (!ok) goto producer_done;
-        if (lane == 0) {
+        if (lane == 0) {  // a k-block past H reads zeros (TMA fill) and adds nothing
           mbar_expect_tx(&full[stage], A_BYTES + B_BYTES);
-          tma_2d(sA + stage * A_BYTES, &tmX, &full[stage], kb * BK, m * BM);
-          tma_2d(sB + stage * B_BYTES, &tmW, &full[stage], kb * BK, n * BN);
+#pragma unroll
+          for (int h = 0; h < kKbStage; ++h) {
+            const int kx = (kb * kKbStage + h) * BK;
+            tma_2d(sA + stage * A_BYTES + h * (BM * 128), &tmX, &full[stage], kx, m * BM);
+            tma_2d(sB + stage * B_BYTES + h * (BN * 128), &tmW, &full[stage], kx, n * BN);
+          }
         }
         __syncwarp();
         if (++stage == kStages) { stage = 0; phase ^= 1u; }
@@ -131,9 +137,12 @@ __global__ void __launch_bounds__(kThreads, 1)
           const uint32_t a = su32(sA + stage * A_BYTES);
           const uint32_t b = su32(sB + stage * B_BYTES);
 #pragma unroll
-          for (int kk = 0; kk < BK / UMMA_K; ++kk)
-            umma_bf16<1>(d, sw128_desc(a + kk * 32), sw128_desc(b + kk * 32), IDESC,
-                         (kb | kk) != 0 ? 1u : 0u);
+          for (int h = 0; h < kKbStage; ++h)
+#pragma unroll
+            for (int kk = 0; kk < BK / UMMA_K; ++kk)
+              umma_bf16<1>(d, sw128_desc(a + h * (BM * 128) + kk * 32),
+                           sw128_desc(b + h * (BN * 128) + kk * 32), IDESC,
+                           (kb | h | kk) != 0 ? 1u : 0u);
           umma_commit<1>(&empty[stage]);
           issued = true;
           if (++stage == kStages) { stage = 0; phase ^= 1u; }
