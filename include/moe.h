@@ -126,7 +126,9 @@ typedef struct moe_ws_layout {
   size_t act;              /* dtype [max_padded, I] */
   size_t xs;               /* bf16 [max_padded, H]: routed token rows in padded order */
   size_t y;                /* dtype [T*k, H] */
-  size_t gemm_scratch;     /* scratch of the grouped GEMMs: empty with the current kernels */
+  size_t gemm_scratch;     /* FP8 weights, batches of > 128 tokens with >= 256 routed rows per
+                              expert (shared experts counted): bf16 copies of one grouped GEMM's
+                              weights, E x 2I x H x 2 bytes (see moe_forward); else empty */
   size_t total;            /* bytes required */
   int block_m;
   int max_padded;
@@ -326,7 +328,11 @@ moe_status_t moe_masked_forward(const moe_config_t* cfg, const void* x_masked,
  * enqueued on `stream` with no host round-trip. ws must hold moe_workspace_size(cfg) bytes, 256-byte
  * aligned; its intermediates sit at moe_workspace_layout(cfg) offsets. Decode batches (at most
  * 8 tokens and 32 routed slots) take top-k and the table (expert map applied) from one small
- * CTA. The results are those of the separate entry points. */
+ * CTA. With FP8 weights and a large batch (the layout's gemm_scratch is not empty), each
+ * grouped GEMM's weights are first written as bf16 (code times block scale, rounded as the
+ * GEMMs' in-kernel conversion rounds it) into gemm_scratch, skipping experts no row reached
+ * unless an expert map is set, and the bf16 GEMM runs on them. The results are those of the
+ * separate entry points, bit for bit. */
 moe_status_t moe_forward(const moe_config_t* cfg, const void* x, const void* Wg,
                          const void* W13, const void* W2, void* out, void* ws,
                          size_t ws_bytes, cudaStream_t stream);

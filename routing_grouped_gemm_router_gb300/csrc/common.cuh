@@ -114,6 +114,12 @@ bool gemv_applies(const moe_config_t& c, int max_padded);
 moe_status_t launch_gemv1(const moe_config_t& c, const void* a, bool gathered, const void* W13,
                           const int32_t* sid, const int32_t* eid, const int32_t* npp,
                           int block_m, void* act, cudaStream_t s);
+// FP8 E4M3 weights [E, R, K] with block scales [E, R / Rg grids, ceil(Rg / 128), K / 128]
+// into bf16 weights (code times block scale, as the converter warps round it); experts whose
+// counts entry is 0 are skipped when counts is given (dequant.cu).
+moe_status_t launch_dequant_fp8(const void* codes, const float* scale, int E, int R, int Rg,
+                                int K, int sc_rb, int sc_kb, const int32_t* counts, void* out,
+                                cudaStream_t s);
 // early: the launch directly follows launch_gemv1 on the same table (the fused layer), so the
 // kernel may read the table and the weights before its dependency wait.
 moe_status_t launch_gemv2(const moe_config_t& c, const void* act, const void* W2,

@@ -99,6 +99,24 @@ def test_gemm_kernel_query(L):
         assert L.moe_small_batch(mk(T)) == (L.moe_gemm_kernel(mk(T)) == L.MOE_GEMM_SMALL_BATCH)
 
 
+def test_fp8_prefill_workspace_holds_bf16_weights(L):
+    """With FP8 weights, the batches the CTA-pair kernels take with at least 256 routed rows
+    per expert convert each grouped GEMM's weights to bf16 in the workspace first: its GEMM
+    scratch region holds E slots (shared experts included) of 2I x H bf16 weights; other
+    batches and bf16 weights need none."""
+    E, H, I, ns = 8, 512, 384, 1
+    s13, s2 = torch.ones(E + ns, 2, 3, 4), torch.ones(E + ns, 4, 3)  # scale grids (host only)
+    fp8 = lambda T: L.make_config(T, H, I, E, 2, L.MOE_BF16, n_shared=ns,  # noqa: E731
+                                  w13_scale=s13, w2_scale=s2)
+    lay = L.moe_workspace_layout(fp8(1024))
+    assert lay.total - lay.gemm_scratch >= (E + ns) * 2 * I * H * 2
+    few = L.make_config(512, H, I, 64, 2, L.MOE_BF16, w13_scale=torch.ones(64, 2, 3, 4),
+                        w2_scale=torch.ones(64, 4, 3))  # 16 rows an expert: converted in-GEMM
+    for cfg in (fp8(64), few, L.make_config(1024, H, I, E, 2, L.MOE_BF16, n_shared=ns)):
+        lay = L.moe_workspace_layout(cfg)
+        assert lay.total == lay.gemm_scratch
+
+
 def test_decode_parity_cases_take_their_paths(L):
     """The decode layers of the GPU parity tests exercise the paths they are named for: the
     9-token layer and the FP8 layers of 25 tokens and more run the decode tensor-core GEMMs,

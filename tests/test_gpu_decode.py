@@ -1,5 +1,6 @@
 """The decode path of moe_forward: batches of at most 8 tokens and 32 routed slots take top-k
-and the align table from one small CTA (expert map applied there).
+and the align table from one small CTA (expert map applied there); and the FP8 prefill path,
+which converts each grouped GEMM's weights to bf16 before the GEMM.
 
 Its results must be the separate entry points' bits (same device arithmetic, same summation
 orders), its intermediates the same tables, and it must replay from a CUDA graph.
@@ -53,6 +54,18 @@ CASES = [
      0, "fp8"),
     ("T8-fp8", mi.Workload("dec-f8b", T=8, H=512, I=640, E=8, k=4, dtype="bf16", seed=51),
      0, "fp8"),
+    # FP8 weights at prefill: moe_forward turns each GEMM's weights into bf16 in its workspace
+    # and runs the bf16 kernels, the separate entry points convert inside the GEMM; the same
+    # operands (code times scale, rounded once), so the same bits. Scales that are not powers
+    # of two, a shared expert, half of the experts remote (every slot converted then).
+    ("T1024-fp8", mi.Workload("pre-f8", T=1024, H=512, I=384, E=8, k=2, dtype="bf16", seed=52),
+     0, "fp8"),
+    ("T1024-fp8-any", mi.Workload("pre-f8a", T=1024, H=384, I=272, E=8, k=2, dtype="bf16",
+                                  seed=53), 0, "fp8-any"),
+    ("T1024-fp8-shared", mi.Workload("pre-f8s", T=1024, H=512, I=256, E=8, k=2, dtype="bf16",
+                                     seed=54), 1, "fp8"),
+    ("T1024-fp8-map", mi.Workload("pre-f8m", T=1024, H=512, I=384, E=8, k=2, dtype="bf16",
+                                  seed=55), 0, "fp8-half"),
 ]
 
 
@@ -69,10 +82,14 @@ def _setup(L, wl, n_shared, variant):
     Ee = wl.E + n_shared
     emap = None
     scales = {}
-    if variant == "fp8":
+    if variant and variant.startswith("fp8"):
         (W13, s13), (W2, s2) = mi.quantize_fp8_w13(W13), mi.quantize_fp8_blocks(W2)
+        if variant == "fp8-any":
+            g = torch.Generator().manual_seed(wl.seed + 7)
+            s13 = s13 * (1.0 + torch.rand(s13.shape, generator=g))
+            s2 = s2 * (1.0 + torch.rand(s2.shape, generator=g))
         scales = dict(w13_scale=_dev(s13), w2_scale=_dev(s2))
-    if variant == "half":
+    if variant in ("half", "fp8-half"):
         emap = torch.tensor([e if e % 2 == 0 else -1 for e in range(Ee)], dtype=torch.int32)
     elif variant == "none":
         emap = torch.full((Ee,), -1, dtype=torch.int32)
@@ -153,7 +170,7 @@ def test_decode_forward_is_the_separate_entry_points_bit_for_bit(L, name, wl, n_
         sb = to_np(inp.select_bias) if inp.select_bias is not None else None
         oids, ow = oracle_route_from_logits(oracle_logits(inp), wl, sb)
         assert np.array_equal(to_np(ref["ids"]), oids)
-        if variant == "fp8":
+        if variant and variant.startswith("fp8"):
             W13o = O.dequant_w13(W13.cpu().numpy(), keep["w13_scale"].double().cpu().numpy())
             W2o = O.dequant_blockwise(W2.cpu().numpy(), keep["w2_scale"].double().cpu().numpy())
         else:
