@@ -441,6 +441,14 @@ def measure_layer(args, wl, ctx, seed, steps, warmup, shared=0, fp8=False, ep_ha
     small = kind == L.MOE_GEMM_SMALL_BATCH
     dec = kind == L.MOE_GEMM_DECODE_TC
     gathered = wl.dtype == "bf16" and not small
+    # FP8 weights at prefill: moe_forward writes each GEMM's weights as bf16 into the
+    # workspace's GEMM scratch and runs the bf16 kernels on them (the region is empty otherwise)
+    dq = fp8 and lay.total > lay.gemm_scratch
+    cfg_dq = layer.config(T)
+    if dq:
+        cfg_dq.weight_format, cfg_dq.w13_scale, cfg_dq.w2_scale = L.MOE_WEIGHTS_NATIVE, None, None
+    dq_counts = None if emap is not None else p["counts"]
+
     def step(ev=None, sh=sh, c=0):
         # The same kernels moe_forward enqueues, called stage by stage so that CUDA events
         # between them give each stage's device time.
@@ -458,29 +466,45 @@ def measure_layer(args, wl, ctx, seed, steps, warmup, shared=0, fp8=False, ep_ha
         if gathered:
             L.moe_gather_rows(inp.x, p["sorted_ids"], p["num_post_padded"], T, k, H, cfg.dtype,
                               p["xs"], sh)
-            if ev is not None:
-                ev[3].record(stream)
+        if ev is not None:
+            ev[3].record(stream)
+        if dq:
+            L.moe_dequant_fp8_weights(cfg, 1, W13s[c], dq_counts, p["gemm_scratch"], sh)
+        if ev is not None:
+            ev[4].record(stream)
+        if dq:
+            L.moe_expert_gemm1_gathered(cfg_dq, p["xs"], p["gemm_scratch"], p["sorted_ids"],
+                                        p["expert_ids"], p["num_post_padded"], B, p["act"],
+                                        None, 0, sh)
+        elif gathered:
             L.moe_expert_gemm1_gathered(cfg, p["xs"], W13s[c], p["sorted_ids"], p["expert_ids"],
                                         p["num_post_padded"], B, p["act"], p["gemm_scratch"],
                                         ws_gemm, sh)
         else:
-            if ev is not None:
-                ev[3].record(stream)
             L.moe_expert_gemm1(cfg, inp.x, W13s[c], p["sorted_ids"], p["expert_ids"],
                                p["num_post_padded"], B, p["act"], p["xs"], ws_xs, sh)
         if ev is not None:
-            ev[4].record(stream)
-        L.moe_expert_gemm2(cfg, p["act"], W2s[c], p["sorted_ids"], p["expert_ids"],
-                           p["num_post_padded"], B, p["topk_w"], p["y"], p["gemm_scratch"],
-                           ws_gemm, sh)
-        if ev is not None:
             ev[5].record(stream)
+        if dq:
+            L.moe_dequant_fp8_weights(cfg, 2, W2s[c], dq_counts, p["gemm_scratch"], sh)
+        if ev is not None:
+            ev[6].record(stream)
+        if dq:
+            L.moe_expert_gemm2(cfg_dq, p["act"], p["gemm_scratch"], p["sorted_ids"],
+                               p["expert_ids"], p["num_post_padded"], B, p["topk_w"], p["y"],
+                               None, 0, sh)
+        else:
+            L.moe_expert_gemm2(cfg, p["act"], W2s[c], p["sorted_ids"], p["expert_ids"],
+                               p["num_post_padded"], B, p["topk_w"], p["y"], p["gemm_scratch"],
+                               ws_gemm, sh)
+        if ev is not None:
+            ev[7].record(stream)
         if emap is not None:
             L.moe_combine_local(p["y"], p["topk_ids"], emap, E, T, k, H, cfg.dtype, out, sh)
         else:
             L.moe_combine(p["y"], T, k, H, cfg.dtype, out, sh)
         if ev is not None:
-            ev[6].record(stream)
+            ev[8].record(stream)
 
     def forward(sh=sh, c=0):
         # the timed step: the public entry point, moe_forward, with the workspace above
@@ -493,7 +517,7 @@ def measure_layer(args, wl, ctx, seed, steps, warmup, shared=0, fp8=False, ep_ha
     tiny = T <= 8 and T * k <= 32
     routing_launches = 2 if (T <= 8 and T * k <= 4096) else 2 + (1 if T * k <= 4096 else 3)
     launches_per_step = routing_launches + (1 if (emap is not None and not tiny) else 0) + \
-        (1 if gathered else 0) + 3
+        (1 if gathered else 0) + 3 + (2 if dq else 0)
 
     for _ in range(max(3, warmup)):
         step()
@@ -535,15 +559,18 @@ def measure_layer(args, wl, ctx, seed, steps, warmup, shared=0, fp8=False, ep_ha
     time.sleep(0.3)
     ms = timed(ctx, steps, run_step, torch.cuda.synchronize, CudaTimer(stream), dev)
     # per-stage device times: the same steps launched eagerly with CUDA events between stages
-    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(7)] for _ in range(steps)]
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(9)] for _ in range(steps)]
     for i in range(steps):
         step(evs[i], c=i % n_copies)
     torch.cuda.synchronize()
     clocks = sampler.stop()
     stage = {n: statistics.mean(e[i].elapsed_time(e[i + 1]) for e in evs)
-             for i, n in enumerate(("route", "align", "gather", "gemm1", "gemm2", "combine"))}
+             for i, n in enumerate(("route", "align", "gather", "dequant1", "gemm1", "dequant2",
+                                    "gemm2", "combine"))}
+    if not dq:
+        del stage["dequant1"], stage["dequant2"]
     res = {"ms": ms, "stage": stage, "clocks": clocks, "npp": npp, "active": active,
-           "local_rows": local_rows, "small": bool(small), "dec": bool(dec),
+           "local_rows": local_rows, "small": bool(small), "dec": bool(dec), "dq": bool(dq),
            "n_copies": n_copies,
            "wbytes": wbytes, "launches_per_step": launches_per_step, "graph": bool(graphs),
            "T": T, "k": k, "E": E, "H": H, "I": I, "block_m": B}
@@ -659,7 +686,10 @@ def summarize(wl, m, world, fp8=False):
     kern, src = (("gemv1", "gemv.cu") if m["small"] else ("gemmdec1", "gemm_dec.cu")
                  if m["dec"] else ("gemm1", "gemm_tc2.cu"))
     src = os.path.join(ROOT, "routing_grouped_gemm_router_gb300", "csrc", src)
-    roof["traffic"] = profile_traffic(kern + ("_fp8" if fp8 else ""), wl.name, active, src)
+    if m.get("dq"):  # FP8 weights at prefill: GEMM1 is the bf16 kernel on bf16 copies
+        roof["kernel"] += ", bf16 weights written from the FP8 codes just before"
+    roof["traffic"] = profile_traffic(kern + ("_fp8" if fp8 and not m.get("dq") else ""),
+                                      wl.name, active, src)
     return _line_fields(wl, m, world, value, intensity, hbm_bound, roof, hbm, bf16_burst)
 
 
@@ -679,12 +709,13 @@ def _line_fields(wl, m, world, value, intensity, hbm_bound, roof, hbm, bf16_burs
 
 
 # The rest of the metric, measured in the default run next to the headline (one GPU): the
-# other prefill shapes, the decode sweep and FP8 expert weights at decode.
+# other prefill shapes, the decode sweep, FP8 expert weights at decode and at prefill.
 SWEEP = [("qwen3-skewed", False), ("deepseek-v3", False),
          ("gpt-oss-decode@T=1", False), ("gpt-oss-decode@T=8", False),
          ("gpt-oss-decode@T=32", False), ("gpt-oss-decode@T=128", False),
          ("gpt-oss-decode@T=1", True), ("gpt-oss-decode@T=8", True),
-         ("gpt-oss-decode@T=32", True), ("gpt-oss-decode@T=128", True)]
+         ("gpt-oss-decode@T=32", True), ("gpt-oss-decode@T=128", True),
+         ("mixtral-prefill", True)]
 
 
 def run_sweep(args, ctx):

@@ -44,7 +44,7 @@
 extern "C" {
 #endif
 
-#define MOE_ABI_VERSION 8
+#define MOE_ABI_VERSION 9
 
 typedef enum {
   MOE_OK = 0,
@@ -265,6 +265,21 @@ moe_status_t moe_expert_gemm1_gathered(const moe_config_t* cfg, const void* xs,
                                        const int32_t* expert_ids,
                                        const int32_t* num_post_padded, int block_m, void* act,
                                        void* ws, size_t ws_bytes, cudaStream_t stream);
+
+/* FP8 E4M3 expert weights (cfg->weight_format MOE_WEIGHTS_FP8_E4M3_B128) as bf16 weights:
+ * out[e, r, c] = code[e, r, c] * its 128 x 128 block scale, rounded to bf16 as the grouped
+ * GEMMs' in-kernel conversion rounds it (exact for power-of-two scales), for every expert slot
+ * e < E + n_shared. matrix 1: codes are W13 [E+n_shared, 2I, H] with cfg->w13_scale; matrix
+ * 2: W2 [E+n_shared, H, I] with cfg->w2_scale. counts (optional, E+n_shared entries, e.g.
+ * moe_align's): experts whose count is 0 are skipped (out left untouched). codes and out
+ * 16-byte aligned; out holds (E+n_shared) x 2I x H (matrix 1) or x H x I (matrix 2) bf16.
+ * moe_forward does this at prefill, with out in its workspace's gemm_scratch, and runs the
+ * bf16 grouped GEMMs on it; a caller of the separate entry points can do the same (a
+ * configuration without the scales then describes the bf16 weights). The pages give FP8
+ * weights as a storage format (§8 intensity with 1-byte weights); the conversion is this
+ * library's. */
+moe_status_t moe_dequant_fp8_weights(const moe_config_t* cfg, int matrix, const void* codes,
+                                     const int32_t* counts, void* out, cudaStream_t stream);
 
 /* GEMM2 with the router weight (page §6): for every padded position p with r < T*k,
  *   y[r, :] = topk_w[r] * (act[p] @ W2[e]^T).  Each row r < T*k is written exactly once;

@@ -9,6 +9,7 @@ from ._lib import (EXPORTED, MOE_BF16, MOE_F32, MOE_GEMM_DECODE_TC,  # noqa: F40
                    MOE_ROUTE_SIGMOID_GROUPED,
                    MOE_ROUTE_SOFTMAX, MOE_WEIGHTS_FP8_E4M3_B128, MOE_WEIGHTS_NATIVE, MoeError,
                    make_config, moe_abi_version, moe_align, moe_align_noalloc,
+                   moe_dequant_fp8_weights,
                    moe_align_workspace_size, moe_apply_expert_map, moe_block_m, moe_combine,
                    moe_combine_local, moe_config_t, moe_device_status, moe_expert_gemm1,
                    moe_expert_gemm1_gathered, moe_expert_gemm1_gathered_workspace_size,

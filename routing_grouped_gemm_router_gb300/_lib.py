@@ -84,6 +84,7 @@ def _load():
         "moe_device_status": (I32, [I32]),
         "moe_selftest_wait_timeout": (ST, [P]),
         "moe_route_logits": (ST, [CFG, P, P, P, P]),
+        "moe_dequant_fp8_weights": (ST, [CFG, I32, P, P, P, P]),
     }
     for name, (res, args) in sig.items():
         f = getattr(lib, name)
@@ -103,7 +104,7 @@ EXPORTED = ("moe_abi_version", "moe_status_string", "moe_block_m", "moe_small_ba
             "moe_grouped_swiglu", "moe_combine", "moe_apply_expert_map", "moe_combine_local",
             "moe_masked_table", "moe_masked_workspace_size", "moe_masked_forward",
             "moe_forward", "moe_device_status", "moe_selftest_wait_timeout",
-            "moe_route_logits")
+            "moe_route_logits", "moe_dequant_fp8_weights")
 
 
 def lib():
@@ -260,6 +261,12 @@ def moe_expert_gemm1(cfg, x, W13, sorted_ids, expert_ids, num_post_padded, block
     _check("moe_expert_gemm1", _lib.moe_expert_gemm1(
         ctypes.byref(cfg), _ptr(x), _ptr(W13), _ptr(sorted_ids), _ptr(expert_ids),
         _ptr(num_post_padded), block_m, _ptr(act), _ptr(ws), ws_bytes, _stream(stream)))
+
+
+def moe_dequant_fp8_weights(cfg, matrix, codes, counts, out, stream=None):
+    """FP8 codes of W13 (matrix 1) or W2 (matrix 2) times their block scales as bf16 weights."""
+    _check("moe_dequant_fp8_weights", _lib.moe_dequant_fp8_weights(
+        ctypes.byref(cfg), matrix, _ptr(codes), _ptr(counts), _ptr(out), _stream(stream)))
 
 
 def moe_gather_rows(x, sorted_ids, num_post_padded, T, k, H, dtype, xs, stream=None):

@@ -144,6 +144,22 @@ int moe_small_batch(const moe_config_t* cfg) {
   return gemv_applies(e, (int)moe_max_padded_rows(e.T, e.k, e.E, B)) ? 1 : 0;
 }
 
+moe_status_t moe_dequant_fp8_weights(const moe_config_t* cfg, int matrix, const void* codes,
+                                     const int32_t* counts, void* out, cudaStream_t stream) {
+  moe_status_t st = check_cfg(cfg);
+  if (st != MOE_OK) return st;
+  if (cfg->weight_format != MOE_WEIGHTS_FP8_E4M3_B128 || (matrix != 1 && matrix != 2))
+    return MOE_ERR_INVALID_ARG;
+  if (!codes || !out || !aligned16(codes) || !aligned16(out)) return MOE_ERR_INVALID_ARG;
+  const moe_config_t e = effective(cfg);
+  if (matrix == 1)
+    return launch_dequant_fp8(codes, cfg->w13_scale, e.E, 2 * e.I, e.I, e.H,
+                              (int)ceil_div(e.I, 128), (int)ceil_div(e.H, 128), counts, out,
+                              stream);
+  return launch_dequant_fp8(codes, cfg->w2_scale, e.E, e.H, e.H, e.I, (int)ceil_div(e.H, 128),
+                            (int)ceil_div(e.I, 128), counts, out, stream);
+}
+
 moe_gemm_kernel_t moe_gemm_kernel(const moe_config_t* cfg) {
   if (check_cfg(cfg) != MOE_OK) return MOE_GEMM_INVALID;
   const moe_config_t e = effective(cfg);
@@ -595,9 +611,8 @@ moe_status_t moe_forward(const moe_config_t* c, const void* x, const void* Wg, c
       return st;
     const void* w13 = W13;
     if (dq) {  // FP8 weights of a large batch: bf16 gate/up weights first
-      if ((st = launch_dequant_fp8(W13, c->w13_scale, e.E, 2 * e.I, e.I, e.H,
-                                   (int)ceil_div(e.I, 128), (int)ceil_div(e.H, 128), dq_counts,
-                                   b + L.gemm_scratch, stream)) != MOE_OK)
+      if ((st = moe_dequant_fp8_weights(c, 1, W13, dq_counts, b + L.gemm_scratch, stream)) !=
+          MOE_OK)
         return st;
       w13 = b + L.gemm_scratch;
     }
@@ -608,12 +623,9 @@ moe_status_t moe_forward(const moe_config_t* c, const void* x, const void* Wg, c
                                     stream)) != MOE_OK) {
     return st;
   }
-  if (dq) {  // and bf16 down-projection weights, over the gate/up copy GEMM1 is done with
-    if ((st = launch_dequant_fp8(W2, c->w2_scale, e.E, e.H, e.H, e.I, (int)ceil_div(e.H, 128),
-                                 (int)ceil_div(e.I, 128), dq_counts, b + L.gemm_scratch,
-                                 stream)) != MOE_OK)
-      return st;
-  }
+  if (dq &&  // and bf16 down-projection weights, over the gate/up copy GEMM1 is done with
+      (st = moe_dequant_fp8_weights(c, 2, W2, dq_counts, b + L.gemm_scratch, stream)) != MOE_OK)
+    return st;
   if (!small && (st = moe_expert_gemm2(dq ? &cb : c, b + L.act, dq ? b + L.gemm_scratch : W2, sid,
                                        eid, npp, L.block_m, w, b + L.y, nullptr, 0, stream)) !=
                     MOE_OK)

@@ -37,7 +37,7 @@ def test_library_exports_every_declared_symbol(L):
     missing = [n for n in decl if not hasattr(cdll, n)]
     assert not missing, f"declared but not exported: {missing}"
     assert set(decl) <= set(L.EXPORTED) | set(decl)
-    assert L.moe_abi_version() == 8
+    assert L.moe_abi_version() == 9
 
 
 def test_status_strings(L):

@@ -851,3 +851,34 @@ def test_fp8_masked_layout(L):
     valid = ~np.isnan(ref[:, :, 0])
     assert np.all(np.isnan(got[~valid])), "a row past an expert's count was written"
     assert_close(got[valid], ref[valid], "bf16")
+
+
+@pytest.mark.parametrize("any_scale", [False, True], ids=["pow2-scales", "any-scales"])
+def test_dequant_fp8_weights(L, any_scale):
+    """moe_dequant_fp8_weights: every weight of W13 and W2 is code * block scale as bf16 —
+    equal to the oracle's float64 dequantisation for power-of-two scales (the products are
+    exact), within one bf16 rounding of it otherwise; experts whose count is 0 are not
+    written."""
+    wl = mi.Workload("dq", T=64, H=384, I=272, E=4, k=2, dtype="bf16", seed=81)
+    inp = mi.make_layer(wl, "cpu")
+    c13, s13, c2, s2 = _fp8_weights(inp, 1, any_scale, wl.seed)
+    E, H, I = wl.E + 1, wl.H, wl.I
+    s13d, s2d = s13.to(DEV), s2.to(DEV)  # the config holds their addresses
+    cfg = L.make_config(wl.T, H, I, wl.E, wl.k, L.MOE_BF16, n_shared=1, w13_scale=s13d,
+                        w2_scale=s2d)
+    counts = torch.tensor([3, 0, 5, 1, 2], dtype=torch.int32, device=DEV)
+    for matrix, codes, ref in ((1, c13, O.dequant_w13(c13.numpy(), s13.double().numpy())),
+                               (2, c2, O.dequant_blockwise(c2.numpy(), s2.double().numpy()))):
+        out = torch.full(tuple(codes.shape), float("nan"), dtype=torch.bfloat16, device=DEV)
+        L.moe_dequant_fp8_weights(cfg, matrix, codes.to(DEV), None, out)
+        got = to_np(out)
+        if any_scale:
+            assert np.all(np.abs(got - ref) <= 2.0 ** -8 * np.abs(ref))
+        else:
+            assert np.array_equal(got, ref)
+        skip = torch.full_like(out, float("nan"))
+        L.moe_dequant_fp8_weights(cfg, matrix, codes.to(DEV), counts, skip)
+        torch.cuda.synchronize()
+        live = (counts > 0).cpu()
+        assert torch.equal(skip[live.to(DEV)], out[live.to(DEV)])
+        assert torch.isnan(skip[~live.to(DEV)].float()).all()
