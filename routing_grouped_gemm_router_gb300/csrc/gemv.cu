@@ -14,7 +14,9 @@
 // gemv_dev.cuh. The activations (a few rows, read by every warp of the tile) come through L1;
 // the weights bypass it. Each warp takes a contiguous range of items, adjacent columns of
 // one tile, so its tile's row list (kept in the warp's shared memory) and expert change
-// rarely; a pass takes one, two or four rows, from the batch size.
+// rarely; a pass takes up to one, two or four rows (from the batch size) and skips the rows
+// a tile does not have. Inside the fused layer GEMM2's first weight loads are issued before
+// its dependency wait (see gemv_kernel).
 #include "gemv_dev.cuh"
 
 namespace moe {
