@@ -14,6 +14,8 @@
 // (topk_align_small_kernel): the routing tail of a decode step is then a single launch.
 #include <mutex>
 
+#include <cooperative_groups.h>
+
 #include "route_dev.cuh"
 
 namespace moe {
@@ -469,22 +471,50 @@ int tiny_status_read(int reset) {
   return v;
 }
 
-template <int MPL>
-__global__ void __launch_bounds__(kTinyThreads) topk_table_tiny_kernel(
-    const TopkArgs a, int32_t* __restrict__ ids, float* __restrict__ w, int n, int E_eff, int B,
-    int max_padded, int32_t* __restrict__ sorted_ids, int32_t* __restrict__ expert_ids,
-    int32_t* npp, int32_t* counts, const int32_t* __restrict__ map) {
+// The router GEMM of a one-token batch fused in front (bf16): a cluster of up to 8 CTAs of 16
+// warps, a warp per expert (the few-token router's device code), writes the logits into the
+// shared memory of the cluster's first CTA; after a cluster barrier (release / acquire) that CTA
+// stores them to the workspace and runs the top-k and the table on them, as the kernel above
+// does on the logits in global memory. One launch, and one dependency wait, fewer on the
+// decode step's critical path.
+constexpr int kRouteTinyWarps = 16;
+constexpr int kRouteTinyMaxCtas = 8;
+constexpr int kRouteTinyLogits = 512;  // the token's E logits, held by the first CTA
+
+template <int MPL, int TB, bool FUSED>
+__global__ void __launch_bounds__(FUSED ? kRouteTinyWarps * 32 : kTinyThreads)
+    topk_table_tiny_kernel(const TopkArgs a, int32_t* __restrict__ ids, float* __restrict__ w,
+                           int n, int E_eff, int B, int max_padded,
+                           int32_t* __restrict__ sorted_ids, int32_t* __restrict__ expert_ids,
+                           int32_t* npp, int32_t* counts, const int32_t* __restrict__ map,
+                           const __nv_bfloat16* __restrict__ x,
+                           const __nv_bfloat16* __restrict__ Wg, int H, float* logits_out) {
   __shared__ float skey[kTopkWarps][512];
   __shared__ int32_t ids_s[kTinyRows];
   __shared__ float w_s[kTinyRows];
   __shared__ int gt_cnt[kTinyRows], gt_label[kTinyRows];
   __shared__ int n_tiles_s;
+  __shared__ float lg_sh[FUSED ? kRouteTinyLogits : 1];
   pdl_wait();
   pdl_trigger();
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+  const float* logits = a.logits;
+  if constexpr (FUSED) {
+    namespace cg = cooperative_groups;
+    cg::cluster_group cl = cg::this_cluster();
+    float* lg0 = cl.map_shared_rank(&lg_sh[0], 0);  // the first CTA's logits, from any CTA
+    const int rank = (int)cl.block_rank(), nw = (int)cl.num_blocks() * kRouteTinyWarps;
+    for (int e = rank * kRouteTinyWarps + warp; e < a.E; e += nw)
+      router_warp_logits<__nv_bfloat16, TB>(x, Wg, lg0, 0, a.Tn, H, a.E, e);
+    cl.sync();  // every CTA's logits are in the first CTA's shared memory
+    if (rank != 0) return;
+    for (int i = threadIdx.x; i < a.Tn * a.E; i += blockDim.x) logits_out[i] = lg_sh[i];
+    logits = lg_sh;
+  }
   if (warp < a.Tn)
-    topk_token<MPL>(a.logits, warp, a.E, a.k, a.mode, a.renorm, a.scale, a.n_group, a.topk_group,
-                    a.logit_bias, a.select_bias, a.n_shared, ids_s, w_s, skey[warp]);
+    topk_token<MPL, 8, FUSED>(logits, warp, a.E, a.k, a.mode, a.renorm, a.scale, a.n_group,
+                              a.topk_group, a.logit_bias, a.select_bias, a.n_shared, ids_s, w_s,
+                              skey[warp]);
   __syncthreads();
   if (warp == 0) {
     const int e = lane < n ? ids_s[lane] : 0x7fffffff;
@@ -548,12 +578,59 @@ moe_status_t launch_topk_table_tiny(const moe_config_t& c, const float* logits, 
                    c.topk_group, c.logit_bias, c.select_bias, c.n_shared};
   auto run = [&](auto kern) {
     return launch_k(kern, dim3(1), dim3(kTinyThreads), 0, s, a, ids, w, c.T * kk, E_eff, B,
-                    max_padded, sorted_ids, expert_ids, npp, counts, c.expert_map);
+                    max_padded, sorted_ids, expert_ids, npp, counts, c.expert_map,
+                    (const __nv_bfloat16*)nullptr, (const __nv_bfloat16*)nullptr, 0,
+                    (float*)nullptr);
   };
   switch (topk_per_lane(c.E)) {
-    case 4: return run(topk_table_tiny_kernel<4>);
-    case 8: return run(topk_table_tiny_kernel<8>);
-    default: return run(topk_table_tiny_kernel<kMaxPerLane>);
+    case 4: return run(topk_table_tiny_kernel<4, 1, false>);
+    case 8: return run(topk_table_tiny_kernel<8, 1, false>);
+    default: return run(topk_table_tiny_kernel<kMaxPerLane, 1, false>);
+  }
+}
+
+// One token only. Measured on GB300 (gpt-oss-shaped layer, CUDA graph): 1 token 49.4 -> 48.7
+// us (FP8 weights 41.0 -> 40.0); at 2-8 tokens the router's 8-token path, on the cluster's 8
+// SMs instead of 16, is slower than the launch it saves (2 tokens 87.0 -> 88.5 us).
+bool route_table_tiny_fits(const moe_config_t& c) {
+  return topk_table_tiny_fits(c) && c.dtype == MOE_BF16 && c.T == 1 &&
+         c.E <= kRouteTinyLogits;
+}
+
+moe_status_t launch_route_table_tiny(const moe_config_t& c, const void* x, const void* Wg,
+                                     float* logits, int32_t* ids, float* w, int B,
+                                     int max_padded, int32_t* sorted_ids, int32_t* expert_ids,
+                                     int32_t* npp, int32_t* counts, cudaStream_t s) {
+  if (!route_table_tiny_fits(c) || !counts) return MOE_ERR_UNSUPPORTED;
+  const int kk = c.k + c.n_shared, E_eff = c.E + c.n_shared;
+  const TopkArgs a{logits, c.T, c.E, c.k, (int)c.mode, c.renormalize, c.scale, c.n_group,
+                   c.topk_group, c.logit_bias, c.select_bias, c.n_shared};
+  const int ctas = std::max(1, std::min(kRouteTinyMaxCtas, ceil_div(c.E, kRouteTinyWarps)));
+  auto run = [&](auto kern) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(ctas);
+    cfg.blockDim = dim3(kRouteTinyWarps * 32);
+    cfg.stream = s;
+    cudaLaunchAttribute attr[2];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    attr[1].id = cudaLaunchAttributeClusterDimension;
+    attr[1].val.clusterDim.x = ctas;
+    attr[1].val.clusterDim.y = 1;
+    attr[1].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 2;
+    return cudaLaunchKernelEx(&cfg, kern, a, ids, w, c.T * kk, E_eff, B, max_padded,
+                              sorted_ids, expert_ids, npp, counts, c.expert_map,
+                              (const __nv_bfloat16*)x, (const __nv_bfloat16*)Wg, c.H,
+                              logits) == cudaSuccess
+               ? MOE_OK
+               : MOE_ERR_CUDA;
+  };
+  switch (topk_per_lane(c.E)) {
+    case 4: return run(topk_table_tiny_kernel<4, 1, true>);
+    case 8: return run(topk_table_tiny_kernel<8, 1, true>);
+    default: return run(topk_table_tiny_kernel<kMaxPerLane, 1, true>);
   }
 }
 

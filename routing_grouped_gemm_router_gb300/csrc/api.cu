@@ -563,7 +563,13 @@ moe_status_t moe_forward(const moe_config_t* c, const void* x, const void* Wg, c
   int32_t* counts = (int32_t*)(b + L.counts);
   const moe_config_t e = effective(c);  // shared experts as ordinary slots / experts
   const bool tiny = topk_table_tiny_fits(*c);
-  if (tiny) {
+  if (tiny && route_table_tiny_fits(*c) && aligned16(x) && aligned16(Wg)) {
+    // at most 32 routed slots, bf16: the router GEMM, then top-k and the table (expert map
+    // applied), in one launch
+    if ((st = launch_route_table_tiny(*c, x, Wg, logits, ids, w, L.block_m, L.max_padded, sid,
+                                      eid, npp, counts, stream)) != MOE_OK)
+      return st;
+  } else if (tiny) {
     // at most 32 routed slots: router GEMM, then top-k and the table (expert map applied) in
     // one small CTA
     if ((st = router_logits(c, x, Wg, logits, stream)) != MOE_OK) return st;

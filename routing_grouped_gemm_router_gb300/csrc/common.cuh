@@ -93,6 +93,13 @@ moe_status_t launch_topk_table_tiny(const moe_config_t& c, const float* logits, 
                                     float* w, int B, int max_padded, int32_t* sorted_ids,
                                     int32_t* expert_ids, int32_t* npp, int32_t* counts,
                                     cudaStream_t s);
+// The same for one token with the router GEMM fused in front (bf16 x and Wg, 16-byte
+// aligned): one cluster launch writes the logits too (align.cu).
+bool route_table_tiny_fits(const moe_config_t& c);
+moe_status_t launch_route_table_tiny(const moe_config_t& c, const void* x, const void* Wg,
+                                     float* logits, int32_t* ids, float* w, int B,
+                                     int max_padded, int32_t* sorted_ids, int32_t* expert_ids,
+                                     int32_t* npp, int32_t* counts, cudaStream_t s);
 moe_status_t launch_gemm1_simt(const moe_config_t& c, const float* x, const float* W13,
                                const int32_t* sid, const int32_t* eid, const int32_t* npp,
                                int block_m, int max_padded, float* act, cudaStream_t s);

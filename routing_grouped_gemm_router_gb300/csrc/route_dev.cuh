@@ -205,8 +205,10 @@ inline int topk_per_lane(int E) { return E <= 128 ? 4 : (E <= 256 ? 8 : kMaxPerL
 // taken yet; then the weights of the mode (softmax over E or over the k kept logits; sigmoid
 // scores renormalised and scaled), written to row t of ids / w, after which the shared
 // experts' slots follow. skey_w: this warp's 512 floats of shared memory (used by the group
-// scores of mode 1). Logits are read from L2 (ld.global.cg).
-template <int MPL, int KMAX = 8>
+// scores of mode 1). Logits in global memory (written by an earlier kernel) are read from L2
+// (ld.global.cg); with LSH they are in shared memory and read with plain loads (a global-only
+// load of a shared address faults).
+template <int MPL, int KMAX = 8, bool LSH = false>
 __device__ __forceinline__ void topk_token(const float* __restrict__ logits, int t, int E, int k,
                                            int mode, int renorm, float scale, int n_group,
                                            int topk_group, const float* __restrict__ logit_bias,
@@ -224,7 +226,7 @@ __device__ __forceinline__ void topk_token(const float* __restrict__ logits, int
     key[i] = NEG;
     val[i] = 0.f;
     if (e < E) {
-      float l = __ldcg(lrow + e);
+      float l = LSH ? lrow[e] : __ldcg(lrow + e);
       if (mode == MOE_ROUTE_SOFTMAX) {
         if (logit_bias) l += logit_bias[e];
         key[i] = l;
