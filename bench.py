@@ -516,6 +516,8 @@ def measure_layer(args, wl, ctx, seed, steps, warmup, shared=0, fp8=False, ep_ha
     # GEMM1, GEMM2 and the combine
     tiny = T <= 8 and T * k <= 32
     routing_launches = 2 if (T <= 8 and T * k <= 4096) else 2 + (1 if T * k <= 4096 else 3)
+    if tiny and T == 1 and wl.dtype == "bf16":
+        routing_launches = 1  # one token: router, top-k and table in one cluster launch
     launches_per_step = routing_launches + (1 if (emap is not None and not tiny) else 0) + \
         (1 if gathered else 0) + 3 + (2 if dq else 0)
 
