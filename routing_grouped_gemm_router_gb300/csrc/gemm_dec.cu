@@ -221,13 +221,20 @@ __global__ void __launch_bounds__(Cfg<MODE, FP8>::kThreads, 1)
   }
   __syncthreads();
   const int total = *ntiles_sh * P.m_blocks;
+  // Items go to the first `active` CTAs, each taking the same count (the last possibly fewer):
+  // the weight stream bounds these GEMMs, so the bandwidth of CTAs left without an item goes
+  // to the others instead of a last round in which most SMs idle (GEMM1 at 8 tokens: 644
+  // items on 152 CTAs took 5 rounds, the last with 36 CTAs; now 129 CTAs take 5 each).
+  const int per_cta = (total + gridDim.x - 1) / gridDim.x;
+  const int active = per_cta > 0 ? (total + per_cta - 1) / per_cta : 0;
+  const int first = (int)blockIdx.x < active ? (int)blockIdx.x : total;
   const int num_kb = (P.K + BK - 1) / BK;
 
   if (warp == 0) {
     // ------------------------------------------------------------ TMA producer
     int g = 0;
     bool ok = true;
-    for (int w = blockIdx.x; w < total && ok; w += gridDim.x) {
+    for (int w = first; w < total && ok; w += active) {
       const int t = tl[w / P.m_blocks], j = w % P.m_blocks;
       const int n_cols = FP8 ? 0 : tile_cols(P, t, lane);
       if (lane == 0) {
@@ -272,7 +279,7 @@ __global__ void __launch_bounds__(Cfg<MODE, FP8>::kThreads, 1)
     bool ok = true, issued = false;
     const uint32_t op_lo = sw128_desc_lo(su32(smem + C::op));
     const uint32_t xr_lo = sw128_desc_lo(su32(smem + C::xr));
-    for (int w = blockIdx.x; w < total && ok; w += gridDim.x) {
+    for (int w = first; w < total && ok; w += active) {
       const int n_cols = tile_cols(P, tl[w / P.m_blocks], lane);
       const int xsb = x_slot_bytes(n_cols), nxs = FP8 ? x_slots<C>(xsb) : 1;
       if (xsb != prev_xsb) x = 0;  // the tile-row producer restarts the same way
@@ -329,7 +336,7 @@ __global__ void __launch_bounds__(Cfg<MODE, FP8>::kThreads, 1)
     const int m = q * 32 + lane;
     int acc = 0;
     uint32_t acc_phase = 0;
-    for (int w = blockIdx.x; w < total; w += gridDim.x) {
+    for (int w = first; w < total; w += active) {
       const int t = tl[w / P.m_blocks], j = w % P.m_blocks;
       const int col = j * 128 + m;  // output column of this thread
       int sid4[4];                  // flat rows of tile rows c*32 + lane
@@ -393,7 +400,7 @@ __global__ void __launch_bounds__(Cfg<MODE, FP8>::kThreads, 1)
       int x = 0, prev_nxs = 0, prev_xsb = 0;
       uint32_t xph = 0;
       bool ok = true;
-      for (int w = blockIdx.x; w < total && ok; w += gridDim.x) {
+      for (int w = first; w < total && ok; w += active) {
         const int t = tl[w / P.m_blocks];
         const int n_cols = tile_cols(P, t, lane);
         const int xsb = x_slot_bytes(n_cols), nxs = x_slots<C>(xsb);
@@ -430,7 +437,7 @@ __global__ void __launch_bounds__(Cfg<MODE, FP8>::kThreads, 1)
       static_assert(kRows * 4 % 32 == 0, "each lane converts whole units");
       int g = 0;
       bool ok = true;
-      for (int w = blockIdx.x; w < total && ok; w += gridDim.x) {
+      for (int w = first; w < total && ok; w += active) {
         const int t = tl[w / P.m_blocks], j = w % P.m_blocks;
         const int e = P.eid[(t * 128) / P.block_m];
         const bool sc_ok = e >= 0 && e < P.n_slots && j < P.sc_rb;
